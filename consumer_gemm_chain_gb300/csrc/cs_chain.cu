@@ -1,0 +1,631 @@
+// Host side of the C ABI declared in include/cs_chain.h: plan construction,
+// dependency-ordered schedule, TMA descriptor encoding, launches and status.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "../../include/cs_chain.h"
+#include "cs_kernel.cuh"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+cs_status fail(cs_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+#define CS_CUDA(call)                                                                              \
+  do {                                                                                             \
+    cudaError_t e_ = (call);                                                                       \
+    if (e_ != cudaSuccess) return fail(CS_ERR_CUDA, "%s: %s", #call, cudaGetErrorString(e_));     \
+  } while (0)
+
+constexpr int kMaxMaps = 8;
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
+
+// Kernel configurations: ring depth x stage bytes.  A stage holds the A slice
+// (128 x 64) and the B slice (128 x 64, or 256 x 64 for gate|up).
+constexpr int NS_A = 5, SB_A = cs::TILE_A_BYTES + 128 * cs::BK * 2;      // 32 KB stages
+constexpr int NS_B = 4, SB_B = cs::TILE_A_BYTES + 2 * 128 * cs::BK * 2;  // 48 KB stages
+
+template <int NS, int SB>
+constexpr int smem_bytes_for() {
+  return NS * SB + cs::STAGING_BYTES + static_cast<int>(sizeof(cs::SmemCtl<NS>)) + 1024;
+}
+
+struct MapSlot {
+  const void* ptr = nullptr;  // caller pointer the map was encoded for (nullptr: plan-owned or unset)
+  bool valid = false;
+};
+
+}  // namespace
+
+struct cs_chain_s {
+  cs_chain_desc d{};
+  int device = 0;
+  int num_sms = 0;
+  int m_tiles = 0;
+  int stages = 0;
+  int n_tiles[3] = {0, 0, 0};
+  int k_iters[3] = {0, 0, 0};
+  int units[3] = {0, 0, 0};
+  int lag = 0;
+  int stride = 1;
+  int cfg_b = 0;  // 1: 48 KB-stage kernel (gate|up)
+  int smem = 0;
+  // device memory owned by the plan
+  void* inter[2] = {nullptr, nullptr};
+  uint32_t* sems[2] = {nullptr, nullptr};
+  size_t sem_words[2] = {0, 0};
+  size_t inter_bytes[2] = {0, 0};
+  uint32_t* ctrl = nullptr;
+  uint32_t* sched_fused = nullptr;
+  int n_fused = 0;
+  uint32_t* sched_stage[3] = {nullptr, nullptr, nullptr};
+  uint32_t* delays[3] = {nullptr, nullptr, nullptr};
+  int skip[3] = {-1, -1, -1};
+  // TMA descriptors
+  CUtensorMap maps[kMaxMaps];
+  MapSlot slots[kMaxMaps];
+  bool error_latched = false;
+};
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D row-major tensor [outer, inner] of 16-bit elements, box [box_outer, box_inner],
+// 128-byte swizzle, zero fill out of bounds.
+cs_status encode_2d(CUtensorMap* map, const void* ptr, int bf16, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                    uint32_t box_outer) {
+  auto enc = get_encode();
+  if (!enc) return fail(CS_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable (driver too old?)");
+  if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return fail(CS_ERR_INVALID_ARG, "pointer %p is not 16-byte aligned", ptr);
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                   const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(CS_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for [%llu x %llu] box [%u x %u]", (int)r,
+                (unsigned long long)outer, (unsigned long long)inner, box_outer, box_inner);
+  return CS_OK;
+}
+
+inline int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+inline uint32_t enc_unit(int s, int m, int n) {
+  return (static_cast<uint32_t>(s) << 28) | (static_cast<uint32_t>(m) << 14) | static_cast<uint32_t>(n);
+}
+
+// Geometry shared by the host-only schedule builder and the plan.
+struct Geometry {
+  int stages = 0, m_tiles = 0;
+  int n_tiles[3] = {0, 0, 0};
+  int k_iters[3] = {0, 0, 0};
+  int lag = 0, stride = 1;
+};
+
+cs_status validate(const cs_chain_desc* d) {
+  if (!d) return fail(CS_ERR_INVALID_ARG, "desc is NULL");
+  if (d->kind < CS_CHAIN_MLP_GELU || d->kind > CS_CHAIN_ATTN) return fail(CS_ERR_INVALID_ARG, "bad kind %d", d->kind);
+  if (d->dtype != CS_F16 && d->dtype != CS_BF16) return fail(CS_ERR_INVALID_ARG, "bad dtype %d", d->dtype);
+  if (d->policy < CS_SYNC_TILE || d->policy > CS_SYNC_STREAM) return fail(CS_ERR_INVALID_ARG, "bad policy %d", d->policy);
+  if (d->weight_layout != CS_WEIGHTS_KN && d->weight_layout != CS_WEIGHTS_NK)
+    return fail(CS_ERR_INVALID_ARG, "bad weight_layout %d", d->weight_layout);
+  if (d->M < 1 || d->M > 128 * 16383) return fail(CS_ERR_INVALID_ARG, "M=%d out of range [1, %d]", d->M, 128 * 16383);
+  if (d->H < 8 || d->H % 8 != 0 || d->H > (1 << 20)) return fail(CS_ERR_INVALID_ARG, "H=%d must be a positive multiple of 8", d->H);
+  if (d->F < 8 || d->F % 8 != 0 || d->F > (1 << 20)) return fail(CS_ERR_INVALID_ARG, "F=%d must be a positive multiple of 8", d->F);
+  if (d->stride < 0) return fail(CS_ERR_INVALID_ARG, "stride=%d", d->stride);
+  if (d->num_sms < 0) return fail(CS_ERR_INVALID_ARG, "num_sms=%d", d->num_sms);
+  if (d->lag < -1) return fail(CS_ERR_INVALID_ARG, "lag=%d", d->lag);
+  if (d->kind == CS_CHAIN_ATTN) {
+    if (d->head_dim != 128) return fail(CS_ERR_UNSUPPORTED, "head_dim=%d (only 128 is built)", d->head_dim);
+    if (d->heads < 1 || d->heads * d->head_dim != d->F)
+      return fail(CS_ERR_INVALID_ARG, "ATTN needs F == heads*head_dim (F=%d heads=%d)", d->F, d->heads);
+    return fail(CS_ERR_UNSUPPORTED, "the attention chain is not built yet");
+  }
+  return CS_OK;
+}
+
+Geometry geometry(const cs_chain_desc* d, int num_sms) {
+  Geometry g;
+  g.m_tiles = cdiv(d->M, cs::BM);
+  if (d->kind == CS_CHAIN_ATTN) {
+    g.stages = 3;
+    g.n_tiles[0] = cdiv(3 * d->F, 128);
+    g.k_iters[0] = cdiv(d->H, cs::BK);
+    g.n_tiles[1] = d->heads;
+    g.k_iters[1] = 0;
+    g.n_tiles[2] = cdiv(d->H, 128);
+    g.k_iters[2] = cdiv(d->F, cs::BK);
+  } else {
+    g.stages = 2;
+    g.n_tiles[0] = cdiv(d->F, 128);
+    g.k_iters[0] = cdiv(d->H, cs::BK);
+    g.n_tiles[1] = cdiv(d->H, 128);
+    g.k_iters[1] = cdiv(d->F, cs::BK);
+  }
+  if (d->lag >= 0) {
+    g.lag = d->lag;
+  } else {
+    // enough producer row blocks ahead to fill one wave of the grid
+    g.lag = cdiv(num_sms, g.n_tiles[0] > 0 ? g.n_tiles[0] : 1);
+  }
+  if (g.lag > g.m_tiles) g.lag = g.m_tiles;
+  g.stride = d->stride > 0 ? d->stride : (d->kind == CS_CHAIN_ATTN ? d->heads : 4);
+  return g;
+}
+
+// Dependency-respecting dispatch order: at step t, stage s emits row block
+// t - s*lag.  Every unit a consumer waits on (same row block, or for the
+// attention stage every earlier row block) is emitted at an earlier step or
+// earlier in the same step, so a dynamic in-order dispatcher cannot deadlock.
+std::vector<uint32_t> build_fused(const Geometry& g) {
+  std::vector<uint32_t> v;
+  const int steps = g.m_tiles + (g.stages - 1) * g.lag;
+  for (int t = 0; t < steps; ++t)
+    for (int s = 0; s < g.stages; ++s) {
+      const int m = t - s * g.lag;
+      if (m < 0 || m >= g.m_tiles) continue;
+      for (int n = 0; n < g.n_tiles[s]; ++n) v.push_back(enc_unit(s, m, n));
+    }
+  return v;
+}
+
+std::vector<uint32_t> build_stage(const Geometry& g, int s) {
+  std::vector<uint32_t> v;
+  for (int m = 0; m < g.m_tiles; ++m)
+    for (int n = 0; n < g.n_tiles[s]; ++n) v.push_back(enc_unit(s, m, n));
+  return v;
+}
+
+int device_sms(int* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  int v = 0;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  *out = v;
+  return dev;
+}
+
+template <int NS, int SB>
+cs_status set_smem_attr() {
+  static cudaError_t once = cudaFuncSetAttribute(cs::cs_chain_kernel<NS, SB>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes_for<NS, SB>());
+  if (once != cudaSuccess) return fail(CS_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(once));
+  return CS_OK;
+}
+
+void free_plan(cs_chain_s* p) {
+  if (!p) return;
+  for (auto& b : p->inter) if (b) cudaFree(b);
+  for (auto& b : p->sems) if (b) cudaFree(b);
+  if (p->ctrl) cudaFree(p->ctrl);
+  if (p->sched_fused) cudaFree(p->sched_fused);
+  for (auto& b : p->sched_stage) if (b) cudaFree(b);
+  for (auto& b : p->delays) if (b) cudaFree(b);
+  delete p;
+}
+
+template <typename T>
+cs_status upload(T** dst, const std::vector<T>& v) {
+  if (v.empty()) {
+    *dst = nullptr;
+    return CS_OK;
+  }
+  if (cudaMalloc(reinterpret_cast<void**>(dst), v.size() * sizeof(T)) != cudaSuccess)
+    return fail(CS_ERR_OOM, "cudaMalloc(%zu) failed", v.size() * sizeof(T));
+  CS_CUDA(cudaMemcpy(*dst, v.data(), v.size() * sizeof(T), cudaMemcpyHostToDevice));
+  return CS_OK;
+}
+
+// Map indices (MLP): 0 X, 1 W1/Wg, 2 Wu, 3 H store, 4 H load, 5 W2, 6 Y store.
+enum { MAP_X = 0, MAP_W1 = 1, MAP_WU = 2, MAP_HST = 3, MAP_HLD = 4, MAP_W2 = 5, MAP_Y = 6 };
+
+// Encode a weight map: math shape [K, N].  KN storage: row-major [K, N], boxes of
+// 64 N x 64 K.  NK storage: row-major [N, K], boxes of 64 K x 128 N.
+cs_status encode_weight(cs_chain_s* p, int slot, const void* ptr, int K, int N) {
+  if (p->slots[slot].valid && p->slots[slot].ptr == ptr) return CS_OK;
+  const int bf16 = p->d.dtype == CS_BF16;
+  cs_status s = p->d.weight_layout == CS_WEIGHTS_KN ? encode_2d(&p->maps[slot], ptr, bf16, N, K, 64, 64)
+                                                     : encode_2d(&p->maps[slot], ptr, bf16, K, N, 64, 128);
+  if (s != CS_OK) return s;
+  p->slots[slot].ptr = ptr;
+  p->slots[slot].valid = true;
+  return CS_OK;
+}
+
+// Activation-side map: row-major [rows, cols]; box 64 cols x (128 rows for loads / 32 for stores).
+cs_status encode_act(cs_chain_s* p, int slot, const void* ptr, int rows, int cols, bool store) {
+  if (p->slots[slot].valid && p->slots[slot].ptr == ptr) return CS_OK;
+  cs_status s = encode_2d(&p->maps[slot], ptr, p->d.dtype == CS_BF16, cols, rows, 64, store ? 32 : 128);
+  if (s != CS_OK) return s;
+  p->slots[slot].ptr = ptr;
+  p->slots[slot].valid = true;
+  return CS_OK;
+}
+
+void fill_common(const cs_chain_s* p, cs::KParams& kp) {
+  std::memcpy(kp.maps, p->maps, sizeof(kp.maps));
+  kp.ctrl = p->ctrl;
+  kp.timeout_ns = p->d.spin_timeout_ns ? p->d.spin_timeout_ns : kDefaultTimeoutNs;
+  kp.watchdog_ns = kp.timeout_ns * 4 > 4000000000ull ? kp.timeout_ns * 4 : 4000000000ull;
+  kp.bf16 = p->d.dtype == CS_BF16;
+}
+
+void fill_mlp_stages(const cs_chain_s* p, const cs_mlp_args* a, cs::KParams& kp) {
+  const bool swiglu = p->d.kind == CS_CHAIN_MLP_SWIGLU;
+  const int b_major = p->d.weight_layout == CS_WEIGHTS_KN ? 1 : 0;
+  const int wait = p->d.policy == CS_SYNC_TILE ? cs::WAIT_TILE
+                   : p->d.policy == CS_SYNC_ROW ? cs::WAIT_ROW
+                   : p->d.policy == CS_SYNC_STRIDED ? cs::WAIT_STRIDED
+                                                    : cs::WAIT_NONE;
+  cs::StageP& s0 = kp.st[0];
+  std::memset(&s0, 0, sizeof(s0));
+  s0.kind = cs::STAGE_GEMM;
+  s0.epi = swiglu ? cs::EPI_SWIGLU : cs::EPI_BIAS_GELU;
+  s0.m_tiles = p->m_tiles;
+  s0.n_tiles = p->n_tiles[0];
+  s0.k_iters = p->k_iters[0];
+  s0.n_extent = p->d.F;
+  s0.m_extent = p->d.M;
+  s0.mma_n = swiglu ? 256 : 128;
+  s0.b_major = b_major;
+  s0.map_a = MAP_X;
+  s0.map_b = MAP_W1;
+  s0.map_b2 = swiglu ? MAP_WU : -1;
+  s0.map_out = MAP_HST;
+  s0.b_bytes = swiglu ? 2 * 128 * cs::BK * 2 : 128 * cs::BK * 2;
+  s0.bias_f16 = reinterpret_cast<const __half*>(a ? a->b1 : nullptr);
+  s0.bias_bf16 = reinterpret_cast<const __nv_bfloat16*>(a ? a->b1 : nullptr);
+  s0.wait = cs::WAIT_NONE;
+  s0.rel_tile = p->sems[0];
+  s0.rel_row = p->sems[0] + static_cast<size_t>(p->m_tiles) * p->n_tiles[0];
+  s0.delay_ns = p->delays[0];
+  s0.skip_unit = p->skip[0];
+
+  cs::StageP& s1 = kp.st[1];
+  std::memset(&s1, 0, sizeof(s1));
+  s1.kind = cs::STAGE_GEMM;
+  s1.epi = cs::EPI_NONE;
+  s1.m_tiles = p->m_tiles;
+  s1.n_tiles = p->n_tiles[1];
+  s1.k_iters = p->k_iters[1];
+  s1.n_extent = p->d.H;
+  s1.m_extent = p->d.M;
+  s1.mma_n = 128;
+  s1.b_major = b_major;
+  s1.map_a = MAP_HLD;
+  s1.map_b = MAP_W2;
+  s1.map_b2 = -1;
+  s1.map_out = MAP_Y;
+  s1.b_bytes = 128 * cs::BK * 2;
+  s1.wait = wait;
+  s1.dep_tile = p->sems[0];
+  s1.dep_row = p->sems[0] + static_cast<size_t>(p->m_tiles) * p->n_tiles[0];
+  s1.dep_ntiles = p->n_tiles[0];
+  s1.dep_bn = 128;
+  s1.stride = p->stride;
+  s1.rel_tile = nullptr;
+  s1.rel_row = nullptr;
+  s1.skip_unit = -1;
+  kp.acc_stride = swiglu ? 256 : 128;
+}
+
+cs_status launch(cs_chain_s* p, cs::KParams& kp, const uint32_t* sched, int n_units, cudaStream_t stream) {
+  kp.sched = sched;
+  kp.n_units = n_units;
+  int grid = p->num_sms < n_units ? p->num_sms : n_units;
+  if (grid < 1) grid = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(cs::NUM_THREADS);
+  cfg.dynamicSmemBytes = p->smem;
+  cfg.stream = stream;
+  cudaError_t e;
+  if (p->cfg_b) {
+    cs_status s = set_smem_attr<NS_B, SB_B>();
+    if (s != CS_OK) return s;
+    e = cudaLaunchKernelEx(&cfg, cs::cs_chain_kernel<NS_B, SB_B>, kp);
+  } else {
+    cs_status s = set_smem_attr<NS_A, SB_A>();
+    if (s != CS_OK) return s;
+    e = cudaLaunchKernelEx(&cfg, cs::cs_chain_kernel<NS_A, SB_A>, kp);
+  }
+  if (e != cudaSuccess) return fail(CS_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
+  return CS_OK;
+}
+
+cs_status bind_mlp(cs_chain_s* p, const cs_mlp_args* a) {
+  if (!a) return fail(CS_ERR_INVALID_ARG, "args is NULL");
+  const bool swiglu = p->d.kind == CS_CHAIN_MLP_SWIGLU;
+  if (!a->X || !a->W2 || !a->Y) return fail(CS_ERR_INVALID_ARG, "X, W2 and Y are required");
+  if (swiglu ? (!a->Wg || !a->Wu) : (!a->W1 || !a->b1))
+    return fail(CS_ERR_INVALID_ARG, swiglu ? "Wg and Wu are required" : "W1 and b1 are required");
+  if (!swiglu && reinterpret_cast<uintptr_t>(a->b1) % 16 != 0) return fail(CS_ERR_INVALID_ARG, "b1 is not 16-byte aligned");
+  const int M = p->d.M, H = p->d.H, F = p->d.F;
+  cs_status s;
+  if ((s = encode_act(p, MAP_X, a->X, M, H, false)) != CS_OK) return s;
+  if ((s = encode_weight(p, MAP_W1, swiglu ? a->Wg : a->W1, H, F)) != CS_OK) return s;
+  if (swiglu && (s = encode_weight(p, MAP_WU, a->Wu, H, F)) != CS_OK) return s;
+  if ((s = encode_weight(p, MAP_W2, a->W2, F, H)) != CS_OK) return s;
+  if ((s = encode_act(p, MAP_Y, a->Y, M, H, true)) != CS_OK) return s;
+  return CS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int cs_abi_version(void) { return CS_ABI_VERSION; }
+
+const char* cs_last_error_string(void) { return g_err; }
+
+cs_status cs_chain_desc_init(cs_chain_desc* d) {
+  if (!d) return fail(CS_ERR_INVALID_ARG, "desc is NULL");
+  std::memset(d, 0, sizeof(*d));
+  d->kind = CS_CHAIN_MLP_GELU;
+  d->dtype = CS_F16;
+  d->policy = CS_SYNC_TILE;
+  d->weight_layout = CS_WEIGHTS_KN;
+  d->heads = 12;
+  d->head_dim = 128;
+  d->lag = -1;
+  return CS_OK;
+}
+
+cs_status cs_schedule_build(const cs_chain_desc* desc, int num_sms, uint32_t* units, size_t cap, size_t* n_out) {
+  cs_status s = validate(desc);
+  if (s != CS_OK) return s;
+  if (num_sms < 1) return fail(CS_ERR_INVALID_ARG, "num_sms=%d", num_sms);
+  if (!n_out) return fail(CS_ERR_INVALID_ARG, "n_out is NULL");
+  if (cap > 0 && !units) return fail(CS_ERR_INVALID_ARG, "units is NULL");
+  Geometry g = geometry(desc, num_sms);
+  std::vector<uint32_t> v = build_fused(g);
+  *n_out = v.size();
+  for (size_t i = 0; i < v.size() && i < cap; ++i) units[i] = v[i];
+  return CS_OK;
+}
+
+cs_status cs_chain_plan(const cs_chain_desc* desc, cs_chain_t* out) {
+  if (!out) return fail(CS_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  cs_status s = validate(desc);
+  if (s != CS_OK) return s;
+  int sms = 0;
+  const int dev = device_sms(&sms);
+  if (dev < 0) return fail(CS_ERR_CUDA, "no CUDA device available");
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major * 10 + minor != 103)
+    return fail(CS_ERR_UNSUPPORTED, "device is sm_%d%d; this library is built for sm_103a only", major, minor);
+
+  cs_chain_s* p = new (std::nothrow) cs_chain_s();
+  if (!p) return fail(CS_ERR_OOM, "host allocation failed");
+  p->d = *desc;
+  p->device = dev;
+  p->num_sms = desc->num_sms > 0 && desc->num_sms < sms ? desc->num_sms : sms;
+  Geometry g = geometry(desc, p->num_sms);
+  p->m_tiles = g.m_tiles;
+  p->stages = g.stages;
+  for (int i = 0; i < 3; ++i) {
+    p->n_tiles[i] = g.n_tiles[i];
+    p->k_iters[i] = g.k_iters[i];
+    p->units[i] = g.m_tiles * g.n_tiles[i];
+  }
+  p->lag = g.lag;
+  p->stride = g.stride;
+  p->cfg_b = desc->kind == CS_CHAIN_MLP_SWIGLU;
+  p->smem = p->cfg_b ? smem_bytes_for<NS_B, SB_B>() : smem_bytes_for<NS_A, SB_A>();
+
+  auto bail = [&](cs_status st) {
+    free_plan(p);
+    return st;
+  };
+  const size_t esz = 2;
+  // intermediate H [M, F]
+  p->inter_bytes[0] = static_cast<size_t>(desc->M) * desc->F * esz;
+  if (cudaMalloc(&p->inter[0], p->inter_bytes[0]) != cudaSuccess)
+    return bail(fail(CS_ERR_OOM, "cudaMalloc of the intermediate failed"));
+  for (int b = 0; b < g.stages - 1; ++b) {
+    p->sem_words[b] = static_cast<size_t>(g.m_tiles) * g.n_tiles[b];
+    const size_t words = p->sem_words[b] + g.m_tiles;
+    if (cudaMalloc(reinterpret_cast<void**>(&p->sems[b]), words * 4) != cudaSuccess)
+      return bail(fail(CS_ERR_OOM, "cudaMalloc of semaphores failed"));
+    if (cudaMemset(p->sems[b], 0, words * 4) != cudaSuccess) return bail(fail(CS_ERR_CUDA, "cudaMemset failed"));
+  }
+  if (cudaMalloc(reinterpret_cast<void**>(&p->ctrl), cs::CTRL_WORDS * 4) != cudaSuccess)
+    return bail(fail(CS_ERR_OOM, "cudaMalloc of the control block failed"));
+  if (cudaMemset(p->ctrl, 0, cs::CTRL_WORDS * 4) != cudaSuccess) return bail(fail(CS_ERR_CUDA, "cudaMemset failed"));
+  std::vector<uint32_t> fused = build_fused(g);
+  p->n_fused = static_cast<int>(fused.size());
+  if ((s = upload(&p->sched_fused, fused)) != CS_OK) return bail(s);
+  for (int st = 0; st < g.stages; ++st)
+    if ((s = upload(&p->sched_stage[st], build_stage(g, st))) != CS_OK) return bail(s);
+  // plan-owned intermediate maps
+  if ((s = encode_act(p, MAP_HST, p->inter[0], desc->M, desc->F, true)) != CS_OK) return bail(s);
+  p->slots[MAP_HST].ptr = nullptr;  // plan-owned: never re-encoded
+  if ((s = encode_act(p, MAP_HLD, p->inter[0], desc->M, desc->F, false)) != CS_OK) return bail(s);
+  p->slots[MAP_HLD].ptr = nullptr;
+  // unused map slots must still hold a well-formed descriptor for the prefetch
+  for (int i = 0; i < kMaxMaps; ++i)
+    if (!p->slots[i].valid) std::memcpy(&p->maps[i], &p->maps[MAP_HLD], sizeof(CUtensorMap));
+  for (int i = 0; i < kMaxMaps; ++i)
+    if (i != MAP_HST && i != MAP_HLD) p->slots[i].valid = false;
+  *out = p;
+  return CS_OK;
+}
+
+cs_status cs_chain_destroy(cs_chain_t p) {
+  if (!p) return CS_OK;
+  cudaSetDevice(p->device);
+  cudaDeviceSynchronize();
+  free_plan(p);
+  return CS_OK;
+}
+
+cs_status cs_mlp_forward(cs_chain_t p, const cs_mlp_args* a, void* stream) {
+  if (!p) return fail(CS_ERR_INVALID_ARG, "plan is NULL");
+  if (p->d.kind == CS_CHAIN_ATTN) return fail(CS_ERR_INVALID_ARG, "plan is an attention chain");
+  if (p->error_latched) return fail(CS_ERR_NEEDS_RESET, "plan holds a device error; call cs_chain_reset");
+  cs_status s = bind_mlp(p, a);
+  if (s != CS_OK) return s;
+  cs::KParams kp;
+  std::memset(&kp, 0, sizeof(kp));
+  fill_common(p, kp);
+  fill_mlp_stages(p, a, kp);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (p->d.policy == CS_SYNC_STREAM) {
+    kp.waits = 0;
+    kp.release = 1;
+    kp.bump_epoch = 0;
+    if ((s = launch(p, kp, p->sched_stage[0], p->units[0], st)) != CS_OK) return s;
+    kp.bump_epoch = 1;
+    return launch(p, kp, p->sched_stage[1], p->units[1], st);
+  }
+  kp.waits = 1;
+  kp.release = 1;
+  kp.bump_epoch = 1;
+  return launch(p, kp, p->sched_fused, p->n_fused, st);
+}
+
+cs_status cs_attn_chain_forward(cs_chain_t p, const cs_attn_args* a, void* stream) {
+  (void)a;
+  (void)stream;
+  if (!p) return fail(CS_ERR_INVALID_ARG, "plan is NULL");
+  return fail(CS_ERR_UNSUPPORTED, "the attention chain is not built yet");
+}
+
+cs_status cs_chain_forward_stage(cs_chain_t p, const void* args, int stage, void* stream) {
+  if (!p) return fail(CS_ERR_INVALID_ARG, "plan is NULL");
+  if (p->error_latched) return fail(CS_ERR_NEEDS_RESET, "plan holds a device error; call cs_chain_reset");
+  if (stage < 0 || stage >= p->stages) return fail(CS_ERR_INVALID_ARG, "stage %d out of range", stage);
+  if (p->d.kind == CS_CHAIN_ATTN) return fail(CS_ERR_UNSUPPORTED, "the attention chain is not built yet");
+  const cs_mlp_args* a = static_cast<const cs_mlp_args*>(args);
+  cs_status s = bind_mlp(p, a);
+  if (s != CS_OK) return s;
+  cs::KParams kp;
+  std::memset(&kp, 0, sizeof(kp));
+  fill_common(p, kp);
+  fill_mlp_stages(p, a, kp);
+  kp.waits = 0;
+  kp.release = 0;
+  kp.bump_epoch = 0;
+  return launch(p, kp, p->sched_stage[stage], p->units[stage], static_cast<cudaStream_t>(stream));
+}
+
+cs_status cs_chain_status(cs_chain_t p) {
+  if (!p) return fail(CS_ERR_INVALID_ARG, "plan is NULL");
+  uint32_t w[cs::CTRL_WORDS];
+  CS_CUDA(cudaMemcpy(w, p->ctrl, sizeof(w), cudaMemcpyDeviceToHost));
+  if (w[cs::CTRL_ERROR] == 0) return CS_OK;
+  p->error_latched = true;
+  const cs_status code = static_cast<cs_status>(w[cs::CTRL_ERROR]);
+  return fail(code, "device error %u: unit 0x%08x where 0x%x cta %u", w[cs::CTRL_ERROR], w[cs::CTRL_ERR_UNIT],
+              w[cs::CTRL_ERR_WHERE], w[cs::CTRL_ERR_CTA]);
+}
+
+cs_status cs_chain_reset(cs_chain_t p) {
+  if (!p) return fail(CS_ERR_INVALID_ARG, "plan is NULL");
+  CS_CUDA(cudaDeviceSynchronize());
+  for (int b = 0; b < p->stages - 1; ++b)
+    CS_CUDA(cudaMemset(p->sems[b], 0, (p->sem_words[b] + p->m_tiles) * 4));
+  CS_CUDA(cudaMemset(p->ctrl, 0, cs::CTRL_WORDS * 4));
+  CS_CUDA(cudaDeviceSynchronize());
+  p->error_latched = false;
+  return CS_OK;
+}
+
+cs_status cs_chain_query(cs_chain_t p, cs_chain_info* info) {
+  if (!p || !info) return fail(CS_ERR_INVALID_ARG, "NULL argument");
+  std::memset(info, 0, sizeof(*info));
+  info->stages = p->stages;
+  info->m_tiles = p->m_tiles;
+  for (int i = 0; i < 3; ++i) {
+    info->n_tiles[i] = p->n_tiles[i];
+    info->units[i] = p->units[i];
+  }
+  info->n_units = p->n_fused;
+  info->num_sms = p->num_sms;
+  info->smem_bytes = p->smem;
+  info->lag = p->lag;
+  info->stride = p->stride;
+  info->intermediate[0] = p->inter[0];
+  info->intermediate[1] = p->inter[1];
+  info->sem_words[0] = p->sem_words[0];
+  info->sem_words[1] = p->sem_words[1];
+  return CS_OK;
+}
+
+cs_status cs_chain_debug_read_sems(cs_chain_t p, int boundary, uint32_t* host, size_t n, uint32_t* epoch) {
+  if (!p || !host) return fail(CS_ERR_INVALID_ARG, "NULL argument");
+  if (boundary < 0 || boundary >= p->stages - 1) return fail(CS_ERR_INVALID_ARG, "boundary %d", boundary);
+  const size_t words = p->sem_words[boundary] + p->m_tiles;
+  if (n < words) return fail(CS_ERR_INVALID_ARG, "need %zu words, got %zu", words, n);
+  CS_CUDA(cudaMemcpy(host, p->sems[boundary], words * 4, cudaMemcpyDeviceToHost));
+  if (epoch) CS_CUDA(cudaMemcpy(epoch, p->ctrl + cs::CTRL_EPOCH, 4, cudaMemcpyDeviceToHost));
+  return CS_OK;
+}
+
+cs_status cs_chain_debug_set_delays(cs_chain_t p, int stage, const uint32_t* ns, size_t n) {
+  if (!p) return fail(CS_ERR_INVALID_ARG, "plan is NULL");
+  if (stage < 0 || stage >= p->stages - 1) return fail(CS_ERR_INVALID_ARG, "stage %d has no consumers", stage);
+  if (!ns || n == 0) {
+    if (p->delays[stage]) cudaFree(p->delays[stage]);
+    p->delays[stage] = nullptr;
+    return CS_OK;
+  }
+  if (n != static_cast<size_t>(p->units[stage])) return fail(CS_ERR_INVALID_ARG, "need %d delays", p->units[stage]);
+  if (!p->delays[stage] && cudaMalloc(reinterpret_cast<void**>(&p->delays[stage]), n * 4) != cudaSuccess)
+    return fail(CS_ERR_OOM, "cudaMalloc failed");
+  CS_CUDA(cudaMemcpy(p->delays[stage], ns, n * 4, cudaMemcpyHostToDevice));
+  return CS_OK;
+}
+
+cs_status cs_chain_debug_skip_release(cs_chain_t p, int stage, int unit) {
+  if (!p) return fail(CS_ERR_INVALID_ARG, "plan is NULL");
+  if (stage < 0 || stage >= p->stages - 1) return fail(CS_ERR_INVALID_ARG, "stage %d has no consumers", stage);
+  if (unit < -1 || unit >= p->units[stage]) return fail(CS_ERR_INVALID_ARG, "unit %d out of range", unit);
+  p->skip[stage] = unit;
+  return CS_OK;
+}
+
+cs_status cs_chain_debug_copy_intermediate(cs_chain_t p, int which, void* dst, size_t bytes) {
+  if (!p || !dst) return fail(CS_ERR_INVALID_ARG, "NULL argument");
+  if (which < 0 || which > 1 || !p->inter[which]) return fail(CS_ERR_INVALID_ARG, "no intermediate %d", which);
+  if (bytes > p->inter_bytes[which]) return fail(CS_ERR_INVALID_ARG, "%zu bytes > buffer (%zu)", bytes, p->inter_bytes[which]);
+  CS_CUDA(cudaDeviceSynchronize());
+  CS_CUDA(cudaMemcpy(dst, p->inter[which], bytes, cudaMemcpyDeviceToDevice));
+  return CS_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,225 @@
+/*
+ * cs_chain.h -- C ABI of a tile-synchronised GEMM-chain library for GB300 (sm_103a).
+ *
+ * What it computes.  A chain of dependent GEMMs on one GPU, for example a
+ * transformer MLP  Y = GeLU(X W1 + b1) W2  (CuSync README, MLP paragraph:
+ * "8 way model parallelism GPT3 175B (H=12288 FP16) and LLAMA 65.2B
+ * (H=8192)", with GeLU fused into the first GEMM).  The consumer GEMM's
+ * thread-block tiles start as soon as the producer tiles they read are
+ * finished, instead of at the kernel boundary (CuSync README, first
+ * paragraph: a programmer writes policies that synchronise dependent tiles
+ * of a producer/consumer kernel chain, which raises utilisation in the last
+ * thread-block wave).  The result is the plain composed chain; only the
+ * timing changes.
+ *
+ * How.  One persistent kernel per forward call: a dependency-ordered tile
+ * scheduler hands producer and consumer tile units to the SMs; tcgen05 MMAs
+ * accumulate in tensor memory, fed by TMA into a multi-stage shared-memory
+ * ring; the producer epilogue (bias + activation, downcast, TMA store) then
+ * release-increments a per-tile semaphore in global memory; the consumer's
+ * TMA warp acquire-waits on those semaphores per K-slice before loading the
+ * intermediate.  The wait policy is selectable (cs_policy).
+ *
+ * Conventions for every entry point.
+ *  - Every entry point returns a cs_status and never aborts the process.
+ *    On failure, cs_last_error_string() (thread-local) says why.
+ *  - Matrices are row-major, contiguous, with 16-byte aligned base pointers.
+ *    Device pointers are CUDA device (or managed) memory on the device that
+ *    was current when the plan was made; the caller owns them.
+ *  - "stream" is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Forward calls only enqueue work; device-side failures surface
+ *    through cs_chain_status() after the caller synchronises the stream.
+ *  - A plan is not thread-safe and must be used by one stream at a time: its
+ *    semaphores and intermediate buffers are per plan.
+ */
+#ifndef CS_CHAIN_H
+#define CS_CHAIN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CS_ABI_VERSION 1
+
+typedef struct cs_chain_s* cs_chain_t;
+
+typedef enum cs_status {
+  CS_OK = 0,
+  CS_ERR_INVALID_ARG = 1,  /* NULL/misaligned pointer, bad shape or enum value */
+  CS_ERR_UNSUPPORTED = 2,  /* well-formed request this build does not implement */
+  CS_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed (see cs_last_error_string) */
+  CS_ERR_TIMEOUT = 4,      /* a consumer tile gave up waiting for a producer tile */
+  CS_ERR_OOM = 5,          /* device allocation failed */
+  CS_ERR_WATCHDOG = 6,     /* an in-CTA pipeline wait exceeded its limit (internal error) */
+  CS_ERR_NEEDS_RESET = 7   /* the plan holds a device error; call cs_chain_reset() */
+} cs_status;
+
+typedef enum cs_dtype { CS_F16 = 0, CS_BF16 = 1 } cs_dtype;
+
+/* Which chain the plan runs.
+ *  MLP_GELU : H = GeLU_tanh(X W1 + b1),  Y = H W2            (GPT-3 MLP shard)
+ *  MLP_SWIGLU: H = SiLU(X Wg) * (X Wu),  Y = H Wd            (LLaMA MLP shard)
+ *  ATTN     : QKV = X Wqkv; O = per-head causal softmax(Q K^T/sqrt(d)) V;
+ *             Y = O Wo                                         (attention shard)
+ * GeLU_tanh(x) = x/2 (1 + tanh(sqrt(2/pi)(x + 0.044715 x^3))), SiLU(x) = x/(1+e^-x). */
+typedef enum cs_chain_kind { CS_CHAIN_MLP_GELU = 0, CS_CHAIN_MLP_SWIGLU = 1, CS_CHAIN_ATTN = 2 } cs_chain_kind;
+
+/* When a consumer tile may read the intermediate (CuSync README, first paragraph:
+ * policies over dependent tiles).  A producer tile covers 128 rows x 128 columns
+ * of the intermediate; a consumer K-slice of 64 columns lies inside one of them.
+ *  TILE    : wait for the one producer tile that wrote the K-slice.
+ *  ROW     : wait for every producer tile of the consumer's 128-row block.
+ *  STRIDED : wait for every producer tile of the row block whose column-tile index
+ *            is congruent (mod stride) to the one that wrote the K-slice.  With
+ *            stride = heads this is "the Q, K and V tiles of one head".
+ *  STREAM  : two-kernel control: all producer tiles in one launch, all consumer
+ *            tiles in a second launch on the same stream, no tile waits.        */
+typedef enum cs_policy { CS_SYNC_TILE = 0, CS_SYNC_ROW = 1, CS_SYNC_STRIDED = 2, CS_SYNC_STREAM = 3 } cs_policy;
+
+/* Storage layout of every weight matrix of the chain.
+ *  KN : W stored as in the maths, [K, N] row-major (W1 is [H, F]).
+ *  NK : W stored transposed, [N, K] row-major (W1 is [F, H]; torch.nn.Linear). */
+typedef enum cs_weight_layout { CS_WEIGHTS_KN = 0, CS_WEIGHTS_NK = 1 } cs_weight_layout;
+
+typedef struct cs_chain_desc {
+  int kind;            /* cs_chain_kind */
+  int M;               /* rows (tokens; for ATTN also the causal sequence length), >= 1 */
+  int H;               /* model width: GEMM1 K and GEMM2 N; multiple of 8 */
+  int F;               /* MLP: FFN shard width (GEMM1 N, GEMM2 K), multiple of 8.
+                          ATTN: heads * head_dim.                                   */
+  int dtype;           /* cs_dtype of X, weights, bias, intermediate and Y; fp32 accumulate */
+  int policy;          /* cs_policy */
+  int weight_layout;   /* cs_weight_layout */
+  int stride;          /* CS_SYNC_STRIDED stride in producer column tiles; 0 = auto
+                          (heads for ATTN, 4 for MLPs)                               */
+  int heads;           /* ATTN only: number of heads */
+  int head_dim;        /* ATTN only: must be 128 */
+  int num_sms;         /* persistent grid size; 0 = every SM of the device */
+  int lag;             /* schedule: producer 128-row blocks issued before the first
+                          consumer block; -1 = auto                                  */
+  unsigned long long spin_timeout_ns; /* per-wait limit of a consumer tile; 0 = 2 s */
+} cs_chain_desc;
+
+/* Fill *desc with defaults (kind MLP_GELU, F16, TILE, KN, auto everything else). */
+cs_status cs_chain_desc_init(cs_chain_desc* desc);
+
+/* Make a plan: validates the shapes, builds the tile schedule, allocates the
+ * per-tile semaphores, the intermediate buffer(s) and the device control block
+ * with cudaMalloc on the current device, and encodes the TMA descriptors of the
+ * intermediates.  *out receives the handle (NULL on failure).  The plan fixes M. */
+cs_status cs_chain_plan(const cs_chain_desc* desc, cs_chain_t* out);
+
+/* Free everything the plan owns.  NULL-safe.  Synchronises the device first. */
+cs_status cs_chain_destroy(cs_chain_t plan);
+
+/* Device pointers of one MLP forward, caller-owned.
+ *  X [M,H]; Y [M,H] (written).  MLP_GELU: W1, b1 [F], W2.  MLP_SWIGLU: Wg, Wu, W2 (= Wd).
+ *  Weight shapes follow desc.weight_layout: KN -> W1/Wg/Wu [H,F], W2 [F,H];
+ *  NK -> W1/Wg/Wu [F,H], W2 [H,F].  Unused pointers may be NULL. */
+typedef struct cs_mlp_args {
+  const void* X;
+  const void* W1;
+  const void* b1;
+  const void* Wg;
+  const void* Wu;
+  const void* W2;
+  void* Y;
+} cs_mlp_args;
+
+/* Enqueue one chain forward on `stream` (one persistent-kernel launch; two for
+ * CS_SYNC_STREAM).  TMA descriptors of caller pointers are re-encoded when a
+ * pointer changes.  Returns CS_ERR_NEEDS_RESET if an earlier call of this plan
+ * reported a device error that has not been cleared. */
+cs_status cs_mlp_forward(cs_chain_t plan, const cs_mlp_args* args, void* stream);
+
+/* Device pointers of one attention-chain forward, caller-owned.
+ *  X [M,H]; Wqkv: KN [H, 3F] / NK [3F, H], columns (KN) [Q | K | V], head-major;
+ *  Wo: KN [F, H] / NK [H, F]; Y [M,H] (written). */
+typedef struct cs_attn_args {
+  const void* X;
+  const void* Wqkv;
+  const void* Wo;
+  void* Y;
+} cs_attn_args;
+
+/* Enqueue one attention-chain forward (QKV GEMM -> causal attention -> Wo GEMM). */
+cs_status cs_attn_chain_forward(cs_chain_t plan, const cs_attn_args* args, void* stream);
+
+/* Run ONE stage of the chain alone, as its own persistent launch with no tile
+ * waits and no semaphore releases (the "best standalone GEMM" timing of the
+ * effective-overhead measurement; Flux summary, idea I2: total time minus the
+ * time of the best unsplit GEMM).  args is a cs_mlp_args* or cs_attn_args* as
+ * the plan's kind requires; stage is 0..(stages-1) (2 for MLPs, 3 for ATTN).
+ * The stage reads its input from the plan's intermediate buffer when it is a
+ * consumer stage. */
+cs_status cs_chain_forward_stage(cs_chain_t plan, const void* args, int stage, void* stream);
+
+/* After the caller has synchronised the stream: CS_OK, or the device error the
+ * last forward calls recorded (CS_ERR_TIMEOUT / CS_ERR_WATCHDOG).  Blocking. */
+cs_status cs_chain_status(cs_chain_t plan);
+
+/* Zero the semaphores, counters, epoch and error word (blocking).  Required
+ * after a device error before the plan runs again. */
+cs_status cs_chain_reset(cs_chain_t plan);
+
+/* Thread-local, human-readable reason for the last non-CS_OK status. */
+const char* cs_last_error_string(void);
+
+/* Sizes and device pointers of a plan, for tests and tools. */
+typedef struct cs_chain_info {
+  int stages;              /* 2 (MLP) or 3 (ATTN) */
+  int m_tiles;             /* ceil(M/128) */
+  int n_tiles[3];          /* column tiles of each stage's output */
+  int units[3];            /* work units of each stage */
+  int n_units;             /* total units of a fused forward */
+  int num_sms;             /* persistent grid size */
+  int smem_bytes;          /* dynamic shared memory per CTA */
+  int lag;                 /* schedule lag actually used */
+  int stride;              /* strided-policy stride actually used */
+  void* intermediate[2];   /* H (MLP) or QKV, O (ATTN): device pointers owned by the plan */
+  size_t sem_words[2];     /* length of each boundary's tile-semaphore array */
+} cs_chain_info;
+
+cs_status cs_chain_query(cs_chain_t plan, cs_chain_info* info);
+
+/* Host-only: the dispatch order a plan with this desc and grid size would use.
+ * Each entry encodes one unit as (stage << 28) | (m_tile << 14) | n_tile; for an
+ * ATTN stage n_tile is the head.  *n_out receives the count; entries beyond cap
+ * are not written (cap may be 0 to query the count).  Needs no GPU. */
+cs_status cs_schedule_build(const cs_chain_desc* desc, int num_sms, uint32_t* units, size_t cap,
+                            size_t* n_out);
+
+/* Testing aids. ------------------------------------------------------------ */
+
+/* Copy boundary b's tile semaphores (b = 0: stage0->stage1, b = 1: stage1->stage2)
+ * to host[0..n), then the boundary's row counters after them (m_tiles words).
+ * *epoch receives the number of completed forwards.  Blocking. */
+cs_status cs_chain_debug_read_sems(cs_chain_t plan, int boundary, uint32_t* host, size_t n,
+                                   uint32_t* epoch);
+
+/* Stall producer units before they release: ns[u] nanoseconds for producer unit
+ * u = m_tile * n_tiles + n_tile of `stage` (at most 10 ms each).  ns = NULL or
+ * n = 0 clears.  Blocking copy. */
+cs_status cs_chain_debug_set_delays(cs_chain_t plan, int stage, const uint32_t* ns, size_t n);
+
+/* Make producer unit `unit` of `stage` skip its semaphore release (-1 clears), so
+ * that a consumer waiting on it times out: the bounded-wait path, without any
+ * GPU fault.  The next forward then returns its error via cs_chain_status(). */
+cs_status cs_chain_debug_skip_release(cs_chain_t plan, int stage, int unit);
+
+/* Blocking device-to-device copy of plan-owned intermediate `which` (0: H or QKV,
+ * 1: O) into caller device memory dst; bytes must not exceed the buffer's size
+ * (M * F * 2 for H and O, M * 3F * 2 for QKV).  For stage-by-stage parity tests. */
+cs_status cs_chain_debug_copy_intermediate(cs_chain_t plan, int which, void* dst, size_t bytes);
+
+/* ABI version of the loaded library (CS_ABI_VERSION). */
+int cs_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CS_CHAIN_H */

@@ -1,0 +1,94 @@
+"""Host-side checks of the C-ABI library that need no GPU: it loads, exports every
+symbol include/cs_chain.h declares, validates descriptors and builds a
+dependency-respecting schedule."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def cs():
+    import __graft_entry__
+    __graft_entry__._build_module().build()
+    import consumer_gemm_chain_gb300 as cs
+    return cs
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "cs_chain.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(cs_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(cs):
+    lib = ctypes.CDLL(cs.chain.LIB_PATH)
+    names = header_functions()
+    assert "cs_chain_plan" in names and "cs_mlp_forward" in names and "cs_chain_destroy" in names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in cs_chain.h but not exported"
+    assert set(cs.chain.EXPORTED) == set(names)
+    assert cs.cs_abi_version() == 1
+
+
+def test_desc_defaults(cs):
+    d = cs.cs_chain_desc_init()
+    assert (d.kind, d.dtype, d.policy, d.weight_layout, d.lag) == (0, 0, 0, 0, -1)
+    assert d.head_dim == 128
+
+
+@pytest.mark.parametrize("field,value", [("M", 0), ("H", 12), ("F", 0), ("dtype", 7), ("policy", 9),
+                                         ("kind", 5), ("weight_layout", 3), ("lag", -2), ("num_sms", -1)])
+def test_invalid_descs_are_rejected_without_a_gpu(cs, field, value):
+    d = cs.cs_chain_desc_init(M=64, H=256, F=1024)
+    setattr(d, field, value)
+    with pytest.raises(cs.CSError) as e:
+        cs.cs_chain_plan(d)
+    assert e.value.status == cs.CS_ERR_INVALID_ARG
+    with pytest.raises(cs.CSError):
+        cs.cs_schedule_build(d, 148)
+
+
+def test_null_arguments(cs):
+    lib = cs.chain._lib
+    assert lib.cs_chain_plan(None, None) == cs.CS_ERR_INVALID_ARG
+    assert lib.cs_chain_destroy(None) == cs.CS_OK
+    assert lib.cs_mlp_forward(None, None, None) == cs.CS_ERR_INVALID_ARG
+    assert lib.cs_chain_status(None) == cs.CS_ERR_INVALID_ARG
+    assert lib.cs_chain_desc_init(None) == cs.CS_ERR_INVALID_ARG
+    assert "NULL" in cs.cs_last_error_string()
+
+
+def _deps(stage_kind, s, m, n, d, q):
+    """Producer units (stage, m, n) a unit waits on, under the plan's policy (TILE: the
+    tiles its K-slices read; every policy waits on a superset of those)."""
+    if s == 0:
+        return []
+    if stage_kind == "attn" and s == 1:
+        heads = d.heads
+        return [(0, j, t) for j in range(m + 1) for t in (n, n + heads, n + 2 * heads)]
+    ntp = q[s - 1]
+    return [(s - 1, m, t) for t in range(ntp)]
+
+
+@pytest.mark.parametrize("M,H,F,sms,lag", [(64, 256, 1024, 148, -1), (2048, 12288, 6144, 148, -1),
+                                           (2048, 12288, 6144, 152, 0), (1, 12288, 6144, 148, -1),
+                                           (1000, 8192, 2752, 148, 2), (1536, 8192, 8192, 148, 5)])
+def test_schedule_is_dependency_ordered(cs, M, H, F, sms, lag):
+    d = cs.cs_chain_desc_init(M=M, H=H, F=F, lag=lag)
+    units = cs.cs_schedule_build(d, sms)
+    m_tiles = -(-M // 128)
+    n0, n1 = -(-F // 128), -(-H // 128)
+    dec = [cs.decode_unit(u) for u in units]
+    # every unit exactly once
+    expect = {(0, m, n) for m in range(m_tiles) for n in range(n0)} | {(1, m, n) for m in range(m_tiles) for n in range(n1)}
+    assert len(dec) == len(expect) and set(dec) == expect
+    pos = {u: i for i, u in enumerate(dec)}
+    for (s, m, n), i in pos.items():
+        for dep in _deps("mlp", s, m, n, d, [n0, n1]):
+            assert pos[dep] < i, f"unit {(s, m, n)} at {i} precedes its producer {dep}"

@@ -1,0 +1,203 @@
+"""GPU parity of the fused MLP chain against the fp64 oracle, through the C ABI.
+
+Bar: max|gpu - oracle| / max|oracle| <= 5e-3 (fp16/bf16 inputs, fp32
+accumulate, intermediate rounded to the input dtype).  Outputs of every sync
+policy are compared with one another bit for bit: tile synchronisation only
+changes when a consumer tile runs, never what it computes.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import cs_inputs
+import oracle
+from tests.gpu_util import TOL, device_tensors, forward, intermediate, plan_for
+
+pytestmark = pytest.mark.gpu
+
+cs = pytest.importorskip("consumer_gemm_chain_gb300")
+
+
+def _oracle(inp, rows=None):
+    X = inp.X if rows is None else inp.X[rows]
+    if inp.kind == "gelu":
+        return oracle.mlp_gelu(X, inp.W1, inp.b1, inp.W2, return_hidden=True)
+    return oracle.mlp_swiglu(X, inp.Wg, inp.Wu, inp.W2, return_hidden=True)
+
+
+def test_tiny_chain_tile_sync():
+    inp = cs_inputs.make_inputs("tiny", seed=0)
+    dev = device_tensors(inp)
+    with plan_for(inp, "tile") as plan:
+        Y = forward(plan, dev)
+        H = intermediate(plan, 0, inp.M, inp.F, inp.dtype)
+    Yref, Href = _oracle(inp)
+    assert oracle.rel_err(H.cpu(), Href) <= TOL
+    assert oracle.rel_err(Y.cpu(), Yref) <= TOL
+
+
+def test_tiny_chain_golden_values():
+    from tests.test_golden import load_tiny_golden
+    inp = cs_inputs.make_inputs("tiny", seed=0)
+    dev = device_tensors(inp)
+    with plan_for(inp, "tile") as plan:
+        Y = forward(plan, dev).double().cpu().numpy()
+    g = load_tiny_golden()
+    ref = np.array([v for _, _, v in g])
+    got = np.array([Y[r, c] for r, c, _ in g])
+    full_ref = _oracle(inp)[0]
+    assert np.max(np.abs(got - ref)) <= TOL * np.max(np.abs(full_ref))
+
+
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("M,H,F", [(1, 256, 1024), (100, 320, 392), (200, 200, 136), (384, 512, 640),
+                                   (129, 1024, 2752)])
+def test_ragged_shapes(M, H, F, dtype, layout):
+    inp = cs_inputs.make_custom("gelu", M, H, F, dtype=dtype, seed=3)
+    dev = device_tensors(inp, layout)
+    with plan_for(inp, "tile", layout) as plan:
+        Y = forward(plan, dev)
+    Yref, _ = _oracle(inp)
+    assert oracle.rel_err(Y.cpu(), Yref) <= TOL
+
+
+def test_policies_bit_identical_and_layouts_agree():
+    inp = cs_inputs.make_custom("gelu", 300, 768, 1536, seed=5)
+    outs = {}
+    for layout in ("kn", "nk"):
+        dev = device_tensors(inp, layout)
+        for pol in ("tile", "row", "strided", "stream"):
+            with plan_for(inp, pol, layout) as plan:
+                outs[(layout, pol)] = forward(plan, dev).cpu()
+    Yref, _ = _oracle(inp)
+    base = outs[("kn", "tile")]
+    assert oracle.rel_err(base, Yref) <= TOL
+    for k, v in outs.items():
+        assert torch.equal(v, base), f"{k} differs from kn/tile"
+
+
+def test_flags_end_at_expected_counts():
+    inp = cs_inputs.make_custom("gelu", 520, 512, 1280, seed=6)
+    dev = device_tensors(inp)
+    with plan_for(inp, "tile") as plan:
+        q = cs.cs_chain_query(plan)
+        Y = torch.empty_like(dev["X"])
+        for e in range(1, 6):
+            forward(plan, dev, Y)
+            tiles, rows, epoch = cs.cs_chain_debug_read_sems(plan, 0)
+            assert epoch == e
+            assert all(v == e for r in tiles for v in r), tiles
+            assert rows == [e * q["n_tiles"][0]] * q["m_tiles"]
+
+
+def test_policies_and_control_keep_flags_consistent():
+    inp = cs_inputs.make_custom("gelu", 256, 512, 512, seed=7)
+    dev = device_tensors(inp)
+    for pol in ("row", "strided", "stream"):
+        with plan_for(inp, pol) as plan:
+            for _ in range(3):
+                forward(plan, dev)
+            tiles, rows, epoch = cs.cs_chain_debug_read_sems(plan, 0)
+            assert epoch == 3 and all(v == 3 for r in tiles for v in r) and rows == [3 * 4] * 2
+
+
+def test_delay_injection_never_changes_a_bit():
+    inp = cs_inputs.make_custom("gelu", 640, 1024, 2048, seed=8)
+    dev = device_tensors(inp)
+    ref = None
+    for pol in ("tile", "row", "strided"):
+        with plan_for(inp, pol) as plan:
+            q = cs.cs_chain_query(plan)
+            for seed in range(3):
+                g = torch.Generator().manual_seed(100 + seed)
+                delays = (torch.rand(q["units"][0], generator=g) * 200_000).to(torch.int64).tolist()
+                cs.cs_chain_debug_set_delays(plan, 0, delays)
+                Y = forward(plan, dev).cpu()
+                if ref is None:
+                    ref = Y
+                    Yref, _ = _oracle(inp)
+                    assert oracle.rel_err(Y, Yref) <= TOL
+                assert torch.equal(Y, ref), (pol, seed)
+            cs.cs_chain_debug_set_delays(plan, 0, None)
+            tiles, rows, epoch = cs.cs_chain_debug_read_sems(plan, 0)
+            assert epoch == 3 and all(v == 3 for r in tiles for v in r)
+
+
+def test_missing_release_times_out_and_reset_recovers():
+    inp = cs_inputs.make_custom("gelu", 256, 512, 512, seed=9)
+    dev = device_tensors(inp)
+    with plan_for(inp, "tile", spin_timeout_ns=20_000_000) as plan:
+        good = forward(plan, dev).cpu()
+        cs.cs_chain_debug_skip_release(plan, 0, 5)
+        Y = torch.empty_like(dev["X"])
+        cs.cs_mlp_forward(plan, Y=Y, **dev)
+        torch.cuda.synchronize()
+        assert cs.cs_chain_status(plan) == cs.CS_ERR_TIMEOUT
+        with pytest.raises(cs.CSError) as e:
+            cs.cs_mlp_forward(plan, Y=Y, **dev)
+        assert e.value.status == cs.CS_ERR_NEEDS_RESET
+        cs.cs_chain_debug_skip_release(plan, 0, -1)
+        cs.cs_chain_reset(plan)
+        again = forward(plan, dev).cpu()
+        assert torch.equal(again, good)
+        tiles, rows, epoch = cs.cs_chain_debug_read_sems(plan, 0)
+        assert epoch == 1 and all(v == 1 for r in tiles for v in r)
+
+
+def test_forward_stage_matches_chain():
+    inp = cs_inputs.make_custom("gelu", 300, 512, 1024, seed=10)
+    dev = device_tensors(inp)
+    with plan_for(inp, "tile") as plan:
+        Y = forward(plan, dev).clone()
+        H = intermediate(plan, 0, inp.M, inp.F, inp.dtype).clone()
+        Y2 = torch.zeros_like(Y)
+        cs.cs_chain_forward_stage(plan, 0, Y=Y2, **dev)
+        cs.cs_chain_forward_stage(plan, 1, Y=Y2, **dev)
+        torch.cuda.synchronize()
+        assert cs.cs_chain_status(plan) == cs.CS_OK
+        assert torch.equal(intermediate(plan, 0, inp.M, inp.F, inp.dtype), H)
+        assert torch.equal(Y2, Y)
+        _, _, epoch = cs.cs_chain_debug_read_sems(plan, 0)
+        assert epoch == 1
+
+
+def test_shape_and_dtype_checks_in_binding():
+    inp = cs_inputs.make_custom("gelu", 64, 256, 512, seed=11)
+    dev = device_tensors(inp)
+    with plan_for(inp, "tile") as plan:
+        with pytest.raises(ValueError):
+            cs.cs_mlp_forward(plan, Y=torch.empty(64, 256, dtype=torch.bfloat16, device="cuda"), **dev)
+        bad = dict(dev)
+        bad["W1"] = dev["W1"].t()
+        with pytest.raises(ValueError):
+            cs.cs_mlp_forward(plan, Y=torch.empty_like(dev["X"]), **bad)
+
+
+@pytest.mark.parametrize("M", cs_inputs.GPT3_M_SWEEP)
+def test_gpt3_shard_sampled_rows(M):
+    inp = cs_inputs.make_inputs("gpt3", M=M, seed=0)
+    dev = device_tensors(inp)
+    with plan_for(inp, "tile") as plan:
+        Y = forward(plan, dev).cpu()
+    rows = cs_inputs.sample_rows(M, 64)
+    Yref, _ = _oracle(inp, rows)
+    assert oracle.rel_err(Y[rows], Yref) <= TOL
+
+
+@pytest.mark.parametrize("M", [128 * 3, 128 * 7, 128 * 12])
+def test_stress_shape_all_policies(M):
+    inp = cs_inputs.make_inputs("stress", M=M, seed=0)
+    rows = cs_inputs.sample_rows(M, 32)
+    Yref, _ = _oracle(inp, rows)
+    dev = device_tensors(inp)
+    base = None
+    for pol in ("tile", "row", "strided", "stream"):
+        with plan_for(inp, pol) as plan:
+            Y = forward(plan, dev).cpu()
+        if base is None:
+            base = Y
+            assert oracle.rel_err(Y[rows], Yref) <= TOL
+        assert torch.equal(Y, base), pol
