@@ -1,0 +1,492 @@
+"""Benchmark of the fused, tile-synchronised MLP chain on GB300.
+
+Headline: TFLOP/s of one fused chain forward of the GPT-3 175B 8-way MLP shard
+(X[2048,12288] -> W1[12288,6144] + b1, GeLU -> W2[6144,12288], fp16 in, fp32
+accumulate), TileSync policy, inputs resident in HBM.  One "step" is one chain
+forward (every step of the hot path: dispatch, producer GEMM + bias/GeLU
+epilogue + release, consumer wait + GEMM + store).
+
+Also reported on the same line: the roofline of the kernel, the two-kernel
+stream-ordered control (plain and captured in a CUDA graph), the best
+standalone GEMM times (this library's and cuBLAS through torch), the effective
+sync overhead (chain time minus the best standalone GEMMs, after the Flux
+summary's ECT idea), a sweep over M, an end-to-end number through the C ABI
+with host buffers, and the fp64 CPU oracle timed on the host cores.
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload gpt3|stress|llama]
+                        [--M M] [--policy tile|row|strided|stream] [--quick] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="gpt3", choices=["gpt3", "stress", "llama", "tiny"])
+    ap.add_argument("--M", type=int, default=None)
+    ap.add_argument("--policy", default="tile", choices=["tile", "row", "strided", "stream"])
+    ap.add_argument("--layout", default="kn", choices=["kn", "nk"])
+    ap.add_argument("--lag", type=int, default=-1)
+    ap.add_argument("--tile-n", type=int, default=0)
+    ap.add_argument("--group-m", type=int, default=0)
+    ap.add_argument("--quick", action="store_true", help="headline kernel only (profiling runs)")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU-oracle sample time")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ workload arithmetic
+def chain_flops(kind, M, H, F):
+    if kind == "gelu":
+        return 4.0 * M * H * F
+    if kind == "swiglu":
+        return 6.0 * M * H * F
+    raise ValueError(kind)
+
+
+def chain_bytes(kind, M, H, F, esz=2):
+    """Algorithmic HBM bytes of one chain forward: weights once, X, Y, bias, and
+    the intermediate written once and read once."""
+    if kind == "gelu":
+        w = 2 * H * F
+        b = F
+    else:
+        w = 3 * H * F
+        b = 0
+    return esz * (w + b + 2 * M * H + 2 * M * F)
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append((time.monotonic(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inside = [s for t, s in self.samples if t0 <= t <= t1]
+        used = inside if inside else [s for _, s in self.samples]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(s[0]) for s in used if num(s[0]) is not None]
+        mx = [num(s[1]) for s in used if num(s[1]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for s in used:
+            for name, v in zip(names, s[4:8]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(used), "samples_in_timed_region": len(inside)}
+
+
+# ------------------------------------------------------------------ timing helpers
+def time_loop(fn, steps, warmup, stream):
+    """Mean ms per call of fn over `steps` calls (after `warmup`), CUDA events on `stream`,
+    plus the mean of per-call event pairs (the kernel's average launch duration)."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    n_pairs = min(steps, 200)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_pairs)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(steps):
+        if i < n_pairs:
+            ev[i][0].record(stream)
+        fn()
+        if i < n_pairs:
+            ev[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    total = start.elapsed_time(end) / steps
+    per = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    return total, per
+
+
+def simple_time(fn, iters=50, warmup=5):
+    import torch
+    s = torch.cuda.current_stream()
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s)
+    for _ in range(iters):
+        fn()
+    b.record(s)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / iters
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+def time_cpu_oracle(inp, target_s):
+    """Time the fp64 oracle on a bounded row sample of the workload; returns
+    (flop/s, rows, seconds, rows used, oracle output for those rows)."""
+    import oracle
+    rows = 8
+    while True:
+        t0 = time.perf_counter()
+        Y = _oracle_rows(oracle, inp, list(range(rows)))
+        dt = time.perf_counter() - t0
+        if dt >= target_s or rows >= inp.M:
+            break
+        rows = min(inp.M, max(rows * 2, int(rows * target_s / max(dt, 1e-3) * 1.1)))
+    fl = chain_flops(inp.kind, rows, inp.H, inp.F)
+    return fl / dt, rows, dt, Y
+
+
+def _oracle_rows(oracle, inp, rows):
+    if inp.kind == "gelu":
+        return oracle.mlp_gelu(inp.X[rows], inp.W1, inp.b1, inp.W2)
+    return oracle.mlp_swiglu(inp.X[rows], inp.Wg, inp.Wu, inp.W2)
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+# ------------------------------------------------------------------ distributed
+def dist_setup(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        dist.init_process_group(backend=backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, ws, device=None):
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args):
+    """The fp64 CPU oracle as the reference arm: same metric, workload and unit."""
+    ws, rank, _ = dist_setup(args)
+    if rank != 0:
+        return
+    import cs_inputs
+    import oracle
+    M = args.M or cs_inputs.WORKLOADS[args.workload][4]
+    inp = cs_inputs.make_inputs(args.workload, M=M, seed=0)
+    per_step = max(0.5, min(10.0, 60.0 / max(1, args.steps + args.warmup)))
+    # size the row sample so one step is about `per_step` seconds
+    fl, rows, dt, _ = time_cpu_oracle(inp, per_step)
+    rows_list = list(range(rows))
+    for _ in range(args.warmup):
+        _oracle_rows(oracle, inp, rows_list)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_rows(oracle, inp, rows_list)
+    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    value = chain_flops(inp.kind, rows, inp.H, inp.F) / dt / 1e12
+    sample = f"first {rows} of {M} rows per step (rows are independent), numpy float64 BLAS"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(args.workload, M, inp, args.policy),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+METRIC = "MLP-chain TFLOP/s & % roofline vs M on 1 GB300; sync overhead vs best solo GEMMs"
+
+
+def workload_config(name, M, inp, policy):
+    desc = {"gpt3": "GPT-3 175B 8-way TP MLP shard", "stress": "last-wave stress two-GEMM GeLU chain",
+            "llama": "LLaMA 65.2B 8-way TP SwiGLU shard", "tiny": "tiny MLP chain"}[name]
+    return {"workload": f"{desc}: X[{M},{inp.H}] -> F={inp.F} -> H={inp.H}, {str(inp.dtype).split('.')[-1]}, "
+                        f"policy={policy}",
+            "M": M, "H": inp.H, "F": inp.F, "policy": policy, "accumulate": "fp32",
+            "l2": "inputs larger than L2 (weights alone exceed the 126 MB L2), no flush"}
+
+
+# ------------------------------------------------------------------ our arm
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+
+    import consumer_gemm_chain_gb300 as cs
+    import cs_inputs
+
+    ws, rank, local = dist_setup(args)
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    peaks, peak_src = load_peaks()
+    M = args.M or cs_inputs.WORKLOADS[args.workload][4]
+    inp = cs_inputs.make_inputs(args.workload, M=M, seed=0)
+    kind = inp.kind
+    lay = args.layout
+
+    def w(t):
+        t = t if lay == "kn" else t.t().contiguous()
+        return t.to(device)
+
+    X = inp.X.to(device)
+    dev = {"X": X}
+    if kind == "gelu":
+        dev.update(W1=w(inp.W1), b1=inp.b1.to(device), W2=w(inp.W2))
+    else:
+        dev.update(Wg=w(inp.Wg), Wu=w(inp.Wu), W2=w(inp.W2))
+    Y = torch.empty_like(X)
+
+    def make_plan(policy, MM=M):
+        d = cs.cs_chain_desc_init(kind=kind, M=MM, H=inp.H, F=inp.F, dtype=inp.dtype, policy=policy,
+                                  weight_layout=lay, lag=args.lag, tile_n=args.tile_n, group_m=args.group_m)
+        return cs.cs_chain_plan(d)
+
+    plan = make_plan(args.policy)
+    plan_info = cs.cs_chain_query(plan)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        cs.cs_mlp_forward(plan, Y=Y, **dev)
+
+    flops = chain_flops(kind, M, inp.H, inp.F)
+    nbytes = chain_bytes(kind, M, inp.H, inp.F)
+    launches_per_step = 2 if args.policy == "stream" else 1
+
+    # ---- headline timed region
+    sampler = ClockSampler(local) if rank == 0 else None
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(ws)
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    torch.cuda.synchronize()
+    barrier(ws)
+    t_wall0 = time.monotonic()
+    ms_total, ms_launch = time_loop(step, args.steps, 0, stream)
+    t_wall1 = time.monotonic()
+    barrier(ws)
+    if sampler:
+        time.sleep(0.15)
+        sampler.stop()
+    st = cs.cs_chain_status(plan)
+    if st != cs.CS_OK:
+        raise RuntimeError(f"device status {cs.STATUS_NAMES.get(st)}: {cs.cs_last_error_string()}")
+    ms_step = max_over_ranks(ms_total, ws, device)
+    value = ws * flops / (ms_step * 1e-3) / 1e12
+
+    timed_s = ms_total * args.steps / 1e3
+    sustained = timed_s >= 1.0
+    tc_peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]  # fp16 dense rate = bf16 rate
+    hbm_peak = peaks["hbm_gbs"]
+    achieved = flops / (ms_launch * 1e-3) / 1e12
+    t_roof_ms = max(flops / (tc_peak * 1e12), nbytes / (hbm_peak * 1e9)) * 1e3
+    bound = "tensor" if flops / (tc_peak * 1e12) >= nbytes / (hbm_peak * 1e9) else "hbm"
+    if bound == "tensor":
+        roof = {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
+                "frac": achieved / tc_peak}
+    else:
+        gbs = nbytes / (ms_launch * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak}
+    roof.update({"traffic": None, "peak_source": f"{peak_src} ({'sustained' if sustained else 'burst'})",
+                 "kernel": "cs_chain_kernel<4,49152>" if (kind == "swiglu" or 256 in plan_info["tile_n"])
+                 else "cs_chain_kernel<6,32768>",
+                 "algorithmic_flops_per_launch": flops if launches_per_step == 1 else None,
+                 "algorithmic_bytes_per_launch": nbytes if launches_per_step == 1 else None,
+                 "launch_ms": ms_launch, "roofline_time_ms": t_roof_ms})
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16" if inp.dtype == torch.float16 else "bf16", "data": "synthetic",
+        "config": dict(workload_config(args.workload, M, inp, args.policy), parallelism=f"replicas{ws}",
+                       tile_n=plan_info["tile_n"][:2], group_m=plan_info["group_m"], lag=plan_info["lag"],
+                       grid=plan_info["num_sms"]),
+        "roofline": roof, "gpu_launches": args.steps * launches_per_step,
+    }
+    if sampler:
+        line["clocks"] = sampler.summary(t_wall0, t_wall1)
+
+    # ---- end to end through the C ABI with host buffers
+    Xh = inp.X.pin_memory()
+    Yh = torch.empty(Y.shape, dtype=Y.dtype).pin_memory()
+
+    def e2e_step():
+        X.copy_(Xh, non_blocking=True)
+        cs.cs_mlp_forward(plan, Y=Y, **dev)
+        Yh.copy_(Y, non_blocking=True)
+
+    e2e_ms, _ = time_loop(e2e_step, max(3, min(args.steps, 200)), 3, stream)
+    e2e_ms = max_over_ranks(e2e_ms, ws, device)
+    line["e2e"] = {"value": ws * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                   "h2d_bytes_per_step": Xh.numel() * Xh.element_size(),
+                   "d2h_bytes_per_step": Yh.numel() * Yh.element_size(), "ms_per_step": e2e_ms}
+
+    if rank == 0 and not args.quick:
+        line["extras"] = extras(cs, torch, inp, dev, Y, make_plan, plan, M, kind, peaks, stream)
+        fl, rows, dt, Yref = time_cpu_oracle(inp, args.cpu_seconds)
+        import oracle
+        Yg = Yh[:rows] if rows <= Yh.shape[0] else Yh
+        line["parity_rel_err_rows"] = oracle.rel_err(Yg[:rows], Yref)
+        line["cpu_baseline"] = {"value": fl / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                                "sample": f"first {rows} of {M} rows, {dt:.1f} s, numpy float64 BLAS"}
+    cs.cs_chain_destroy(plan)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def extras(cs, torch, inp, dev, Y, make_plan, plan, M, kind, peaks, stream):
+    """Control, graph control, solo stages, cuBLAS solo GEMMs, sync overhead, M sweep."""
+    import torch.nn.functional as Fn
+    out = {}
+    fwd = lambda p: cs.cs_mlp_forward(p, Y=Y, **dev)  # noqa: E731
+    chain_ms = simple_time(lambda: fwd(plan), 50)
+    out["chain_ms"] = chain_ms
+    for pol in ("row", "strided", "stream"):
+        with make_plan(pol) as p:
+            out[f"{pol}_ms"] = simple_time(lambda: fwd(p), 50)
+    # control captured in a CUDA graph (launch cost amortised)
+    with make_plan("stream") as pc:
+        fwd(pc)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fwd(pc)
+        out["stream_graph_ms"] = simple_time(g.replay, 50)
+        ok = cs.cs_chain_status(pc)
+        out["stream_graph_status"] = cs.STATUS_NAMES.get(ok)
+        del g
+    # best standalone GEMMs: this library's stage kernels and cuBLAS via torch
+    solo = [simple_time(lambda s=s: cs.cs_chain_forward_stage(plan, s, Y=Y, **dev), 50) for s in (0, 1)]
+    out["solo_stage_ms"] = solo
+    X = dev["X"]
+    if kind == "gelu":
+        W1 = dev["W1"] if plan.desc.weight_layout == 0 else dev["W1"].t()
+        W2 = dev["W2"] if plan.desc.weight_layout == 0 else dev["W2"].t()
+        Hbuf = torch.empty(M, inp.F, dtype=inp.dtype, device=X.device)
+        c1 = simple_time(lambda: Fn.gelu(torch.addmm(dev["b1"], X, W1), approximate="tanh"), 50)
+        c2 = simple_time(lambda: torch.mm(Hbuf, W2, out=Y), 50)
+    else:
+        Wg = dev["Wg"] if plan.desc.weight_layout == 0 else dev["Wg"].t()
+        Wu = dev["Wu"] if plan.desc.weight_layout == 0 else dev["Wu"].t()
+        W2 = dev["W2"] if plan.desc.weight_layout == 0 else dev["W2"].t()
+        Hbuf = torch.empty(M, inp.F, dtype=inp.dtype, device=X.device)
+        c1 = simple_time(lambda: Fn.silu(X @ Wg) * (X @ Wu), 50)
+        c2 = simple_time(lambda: torch.mm(Hbuf, W2, out=Y), 50)
+    out["cublas_ms"] = [c1, c2]
+    best = [min(solo[0], c1), min(solo[1], c2)]
+    out["best_solo_ms"] = best
+    out["sync_overhead_ms"] = chain_ms - sum(best)
+    out["sync_overhead_frac"] = (chain_ms - sum(best)) / chain_ms
+    out["beats_control"] = chain_ms < out["stream_ms"]
+    # sweep over M (first M rows of the same draw)
+    sweep = []
+    tc, hbm = peaks["bf16_tflops"], peaks["hbm_gbs"]
+    Ms = (1, 16, 64, 256, 512, 1024, 2048) if inp.H == 12288 else tuple(128 * b for b in range(1, 13))
+    for m in Ms:
+        if m > M:
+            continue
+        sub = {k: (v[:m].contiguous() if k == "X" else v) for k, v in dev.items()}
+        Ym = torch.empty(m, inp.H, dtype=inp.dtype, device=X.device)
+        rec = {"M": m}
+        for pol in ("tile", "stream"):
+            with make_plan(pol, m) as p:
+                ms = simple_time(lambda: cs.cs_mlp_forward(p, Y=Ym, **sub), 30)
+            rec[f"{pol}_us"] = ms * 1e3
+        fl = chain_flops(kind, m, inp.H, inp.F)
+        by = chain_bytes(kind, m, inp.H, inp.F)
+        roof_ms = max(fl / (tc * 1e12), by / (hbm * 1e9)) * 1e3
+        rec["tflops"] = fl / (rec["tile_us"] * 1e-6) / 1e12
+        rec["roofline_frac"] = roof_ms / (rec["tile_us"] * 1e-3)
+        rec["bound"] = "tensor" if fl / (tc * 1e12) >= by / (hbm * 1e9) else "hbm"
+        rec["beats_control"] = rec["tile_us"] < rec["stream_us"]
+        sweep.append(rec)
+    out["sweep"] = sweep
+    return out
+
+
+if __name__ == "__main__":
+    main()

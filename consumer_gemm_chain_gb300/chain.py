@@ -44,7 +44,8 @@ class cs_chain_desc(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int), ("M", ctypes.c_int), ("H", ctypes.c_int), ("F", ctypes.c_int),
                 ("dtype", ctypes.c_int), ("policy", ctypes.c_int), ("weight_layout", ctypes.c_int),
                 ("stride", ctypes.c_int), ("heads", ctypes.c_int), ("head_dim", ctypes.c_int),
-                ("num_sms", ctypes.c_int), ("lag", ctypes.c_int), ("spin_timeout_ns", ctypes.c_ulonglong)]
+                ("num_sms", ctypes.c_int), ("lag", ctypes.c_int), ("group_m", ctypes.c_int),
+                ("tile_n", ctypes.c_int), ("spin_timeout_ns", ctypes.c_ulonglong)]
 
 
 class cs_mlp_args(ctypes.Structure):
@@ -59,7 +60,8 @@ class cs_attn_args(ctypes.Structure):
 class cs_chain_info(ctypes.Structure):
     _fields_ = [("stages", ctypes.c_int), ("m_tiles", ctypes.c_int), ("n_tiles", ctypes.c_int * 3),
                 ("units", ctypes.c_int * 3), ("n_units", ctypes.c_int), ("num_sms", ctypes.c_int),
-                ("smem_bytes", ctypes.c_int), ("lag", ctypes.c_int), ("stride", ctypes.c_int),
+                ("smem_bytes", ctypes.c_int), ("lag", ctypes.c_int), ("group_m", ctypes.c_int),
+                ("tile_n", ctypes.c_int * 3), ("stride", ctypes.c_int),
                 ("intermediate", ctypes.c_void_p * 2), ("sem_words", ctypes.c_size_t * 2)]
 
 
@@ -275,6 +277,7 @@ def cs_chain_query(plan: Plan) -> dict:
     _check(_lib.cs_chain_query(plan.handle, ctypes.byref(i)), "cs_chain_query")
     return {"stages": i.stages, "m_tiles": i.m_tiles, "n_tiles": list(i.n_tiles), "units": list(i.units),
             "n_units": i.n_units, "num_sms": i.num_sms, "smem_bytes": i.smem_bytes, "lag": i.lag,
+            "group_m": i.group_m, "tile_n": list(i.tile_n),
             "stride": i.stride, "intermediate": [i.intermediate[0], i.intermediate[1]],
             "sem_words": [i.sem_words[0], i.sem_words[1]]}
 

@@ -8,6 +8,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <algorithm>
 #include <mutex>
 #include <new>
 #include <vector>
@@ -37,8 +38,9 @@ constexpr int kMaxMaps = 8;
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
 
 // Kernel configurations: ring depth x stage bytes.  A stage holds the A slice
-// (128 x 64) and the B slice (128 x 64, or 256 x 64 for gate|up).
-constexpr int NS_A = 5, SB_A = cs::TILE_A_BYTES + 128 * cs::BK * 2;      // 32 KB stages
+// (128 x 64) and the B slice (128 x 64; or 256 x 64 for 256-wide tiles and for
+// gate|up).  Both rings keep 192 KB of operands in flight per SM.
+constexpr int NS_A = 6, SB_A = cs::TILE_A_BYTES + 128 * cs::BK * 2;      // 32 KB stages
 constexpr int NS_B = 4, SB_B = cs::TILE_A_BYTES + 2 * 128 * cs::BK * 2;  // 48 KB stages
 
 template <int NS, int SB>
@@ -63,8 +65,10 @@ struct cs_chain_s {
   int k_iters[3] = {0, 0, 0};
   int units[3] = {0, 0, 0};
   int lag = 0;
+  int group_m = 1;
   int stride = 1;
-  int cfg_b = 0;  // 1: 48 KB-stage kernel (gate|up)
+  int bn[3] = {128, 128, 128};
+  int cfg_b = 0;  // 1: 48 KB-stage kernel (256-wide tiles or gate|up)
   int smem = 0;
   // device memory owned by the plan
   void* inter[2] = {nullptr, nullptr};
@@ -130,7 +134,8 @@ struct Geometry {
   int stages = 0, m_tiles = 0;
   int n_tiles[3] = {0, 0, 0};
   int k_iters[3] = {0, 0, 0};
-  int lag = 0, stride = 1;
+  int bn[3] = {128, 128, 128};
+  int lag = 1, group_m = 1, stride = 1;
 };
 
 cs_status validate(const cs_chain_desc* d) {
@@ -146,6 +151,9 @@ cs_status validate(const cs_chain_desc* d) {
   if (d->stride < 0) return fail(CS_ERR_INVALID_ARG, "stride=%d", d->stride);
   if (d->num_sms < 0) return fail(CS_ERR_INVALID_ARG, "num_sms=%d", d->num_sms);
   if (d->lag < -1) return fail(CS_ERR_INVALID_ARG, "lag=%d", d->lag);
+  if (d->group_m < 0) return fail(CS_ERR_INVALID_ARG, "group_m=%d", d->group_m);
+  if (d->tile_n != 0 && d->tile_n != 128 && d->tile_n != 256)
+    return fail(CS_ERR_INVALID_ARG, "tile_n=%d (0, 128 or 256)", d->tile_n);
   if (d->kind == CS_CHAIN_ATTN) {
     if (d->head_dim != 128) return fail(CS_ERR_UNSUPPORTED, "head_dim=%d (only 128 is built)", d->head_dim);
     if (d->heads < 1 || d->heads * d->head_dim != d->F)
@@ -158,52 +166,66 @@ cs_status validate(const cs_chain_desc* d) {
 Geometry geometry(const cs_chain_desc* d, int num_sms) {
   Geometry g;
   g.m_tiles = cdiv(d->M, cs::BM);
+  // 256-wide tiles halve the operand bytes per FLOP of the 128-wide ones; they
+  // pay off once there are enough tiles to fill the grid several times.
+  int tn = d->tile_n;
+  if (tn == 0) tn = (g.m_tiles * cdiv(d->F, 256) >= 2 * num_sms) ? 256 : 128;
   if (d->kind == CS_CHAIN_ATTN) {
     g.stages = 3;
+    g.bn[0] = 128;
     g.n_tiles[0] = cdiv(3 * d->F, 128);
     g.k_iters[0] = cdiv(d->H, cs::BK);
     g.n_tiles[1] = d->heads;
     g.k_iters[1] = 0;
-    g.n_tiles[2] = cdiv(d->H, 128);
+    g.bn[2] = tn;
+    g.n_tiles[2] = cdiv(d->H, tn);
     g.k_iters[2] = cdiv(d->F, cs::BK);
   } else {
     g.stages = 2;
-    g.n_tiles[0] = cdiv(d->F, 128);
+    g.bn[0] = d->kind == CS_CHAIN_MLP_SWIGLU ? 128 : tn;
+    g.n_tiles[0] = cdiv(d->F, g.bn[0]);
     g.k_iters[0] = cdiv(d->H, cs::BK);
-    g.n_tiles[1] = cdiv(d->H, 128);
+    g.bn[1] = tn;
+    g.n_tiles[1] = cdiv(d->H, tn);
     g.k_iters[1] = cdiv(d->F, cs::BK);
   }
-  if (d->lag >= 0) {
-    g.lag = d->lag;
-  } else {
-    // enough producer row blocks ahead to fill one wave of the grid
-    g.lag = cdiv(num_sms, g.n_tiles[0] > 0 ? g.n_tiles[0] : 1);
-  }
-  if (g.lag > g.m_tiles) g.lag = g.m_tiles;
+  g.group_m = d->group_m > 0 ? d->group_m : 8;
+  if (g.group_m > g.m_tiles) g.group_m = g.m_tiles;
+  const int groups = cdiv(g.m_tiles, g.group_m);
+  g.lag = d->lag >= 0 ? d->lag : 1;
+  if (g.lag > groups) g.lag = groups;
   g.stride = d->stride > 0 ? d->stride : (d->kind == CS_CHAIN_ATTN ? d->heads : 4);
+  (void)num_sms;
   return g;
 }
 
-// Dependency-respecting dispatch order: at step t, stage s emits row block
-// t - s*lag.  Every unit a consumer waits on (same row block, or for the
-// attention stage every earlier row block) is emitted at an earlier step or
-// earlier in the same step, so a dynamic in-order dispatcher cannot deadlock.
+// Dependency-respecting dispatch order.  Row blocks form groups of group_m; at
+// step t, stage s lists every unit of group t - s*lag, column-tile-major so that
+// the tiles running at the same time share their weight tiles in L2.  Every
+// unit a consumer waits on (same row block, or for the attention stage every
+// earlier row block) is listed at an earlier step or earlier in the same step,
+// so a dynamic in-order dispatcher cannot deadlock.
 std::vector<uint32_t> build_fused(const Geometry& g) {
   std::vector<uint32_t> v;
-  const int steps = g.m_tiles + (g.stages - 1) * g.lag;
+  const int groups = cdiv(g.m_tiles, g.group_m);
+  const int steps = groups + (g.stages - 1) * g.lag;
   for (int t = 0; t < steps; ++t)
     for (int s = 0; s < g.stages; ++s) {
-      const int m = t - s * g.lag;
-      if (m < 0 || m >= g.m_tiles) continue;
-      for (int n = 0; n < g.n_tiles[s]; ++n) v.push_back(enc_unit(s, m, n));
+      const int gg = t - s * g.lag;
+      if (gg < 0 || gg >= groups) continue;
+      const int m0 = gg * g.group_m, m1 = std::min(g.m_tiles, m0 + g.group_m);
+      for (int n = 0; n < g.n_tiles[s]; ++n)
+        for (int m = m0; m < m1; ++m) v.push_back(enc_unit(s, m, n));
     }
   return v;
 }
 
+// One stage alone (two-kernel control, standalone timings): same grouping.
 std::vector<uint32_t> build_stage(const Geometry& g, int s) {
   std::vector<uint32_t> v;
-  for (int m = 0; m < g.m_tiles; ++m)
-    for (int n = 0; n < g.n_tiles[s]; ++n) v.push_back(enc_unit(s, m, n));
+  for (int m0 = 0; m0 < g.m_tiles; m0 += g.group_m)
+    for (int n = 0; n < g.n_tiles[s]; ++n)
+      for (int m = m0; m < std::min(g.m_tiles, m0 + g.group_m); ++m) v.push_back(enc_unit(s, m, n));
   return v;
 }
 
@@ -297,13 +319,14 @@ void fill_mlp_stages(const cs_chain_s* p, const cs_mlp_args* a, cs::KParams& kp)
   s0.k_iters = p->k_iters[0];
   s0.n_extent = p->d.F;
   s0.m_extent = p->d.M;
-  s0.mma_n = swiglu ? 256 : 128;
+  s0.bn = p->bn[0];
+  s0.mma_n = swiglu ? 256 : p->bn[0];
   s0.b_major = b_major;
   s0.map_a = MAP_X;
   s0.map_b = MAP_W1;
   s0.map_b2 = swiglu ? MAP_WU : -1;
   s0.map_out = MAP_HST;
-  s0.b_bytes = swiglu ? 2 * 128 * cs::BK * 2 : 128 * cs::BK * 2;
+  s0.b_bytes = (swiglu ? 2 : 1) * p->bn[0] * cs::BK * 2;
   s0.bias_f16 = reinterpret_cast<const __half*>(a ? a->b1 : nullptr);
   s0.bias_bf16 = reinterpret_cast<const __nv_bfloat16*>(a ? a->b1 : nullptr);
   s0.wait = cs::WAIT_NONE;
@@ -321,23 +344,24 @@ void fill_mlp_stages(const cs_chain_s* p, const cs_mlp_args* a, cs::KParams& kp)
   s1.k_iters = p->k_iters[1];
   s1.n_extent = p->d.H;
   s1.m_extent = p->d.M;
-  s1.mma_n = 128;
+  s1.bn = p->bn[1];
+  s1.mma_n = p->bn[1];
   s1.b_major = b_major;
   s1.map_a = MAP_HLD;
   s1.map_b = MAP_W2;
   s1.map_b2 = -1;
   s1.map_out = MAP_Y;
-  s1.b_bytes = 128 * cs::BK * 2;
+  s1.b_bytes = p->bn[1] * cs::BK * 2;
   s1.wait = wait;
   s1.dep_tile = p->sems[0];
   s1.dep_row = p->sems[0] + static_cast<size_t>(p->m_tiles) * p->n_tiles[0];
   s1.dep_ntiles = p->n_tiles[0];
-  s1.dep_bn = 128;
+  s1.dep_bn = p->bn[0];
   s1.stride = p->stride;
   s1.rel_tile = nullptr;
   s1.rel_row = nullptr;
   s1.skip_unit = -1;
-  kp.acc_stride = swiglu ? 256 : 128;
+  kp.acc_stride = (s0.mma_n > 128 || s1.mma_n > 128) ? 256 : 128;
 }
 
 cs_status launch(cs_chain_s* p, cs::KParams& kp, const uint32_t* sched, int n_units, cudaStream_t stream) {
@@ -399,6 +423,8 @@ cs_status cs_chain_desc_init(cs_chain_desc* d) {
   d->heads = 12;
   d->head_dim = 128;
   d->lag = -1;
+  d->group_m = 0;
+  d->tile_n = 0;
   return CS_OK;
 }
 
@@ -443,8 +469,10 @@ cs_status cs_chain_plan(const cs_chain_desc* desc, cs_chain_t* out) {
     p->units[i] = g.m_tiles * g.n_tiles[i];
   }
   p->lag = g.lag;
+  p->group_m = g.group_m;
   p->stride = g.stride;
-  p->cfg_b = desc->kind == CS_CHAIN_MLP_SWIGLU;
+  for (int i = 0; i < 3; ++i) p->bn[i] = g.bn[i];
+  p->cfg_b = desc->kind == CS_CHAIN_MLP_SWIGLU || g.bn[0] == 256 || g.bn[1] == 256 || g.bn[2] == 256;
   p->smem = p->cfg_b ? smem_bytes_for<NS_B, SB_B>() : smem_bytes_for<NS_A, SB_A>();
 
   auto bail = [&](cs_status st) {
@@ -578,6 +606,8 @@ cs_status cs_chain_query(cs_chain_t p, cs_chain_info* info) {
   info->num_sms = p->num_sms;
   info->smem_bytes = p->smem;
   info->lag = p->lag;
+  info->group_m = p->group_m;
+  for (int i = 0; i < 3; ++i) info->tile_n[i] = p->bn[i];
   info->stride = p->stride;
   info->intermediate[0] = p->inter[0];
   info->intermediate[1] = p->inter[1];

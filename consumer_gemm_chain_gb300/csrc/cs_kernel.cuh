@@ -59,7 +59,8 @@ struct StageP {
   int k_iters;     // BK-slices of the reduction
   int n_extent;    // valid output columns (bias guard, store guard)
   int m_extent;    // valid output rows (store guard)
-  int mma_n;       // UMMA N (128, or 256 for gate|up)
+  int bn;          // output columns per tile (128 or 256)
+  int mma_n;       // UMMA N (bn, or 256 for gate|up with bn = 128)
   int b_major;     // 0: weights K-major ([N,K]); 1: MN-major ([K,N])
   int map_a, map_b, map_b2, map_out;
   int b_bytes;     // bytes of the B operand per pipeline stage
@@ -219,17 +220,18 @@ __device__ bool tma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
     uint64_t* bar = &sc->full[rp.slot];
     mbar_arrive_expect_tx(bar, bytes);
     tma_load_2d(sa, &p.maps[S.map_a], kb * BK, m * BM, bar);
-    if (S.b_major == 0) {
-      // weights [N, K]: one box of 64 K x 128 N rows per operand
-      tma_load_2d(sb, &p.maps[S.map_b], kb * BK, n * 128, bar);
-      if (S.map_b2 >= 0) tma_load_2d(sb + 128 * BK * 2, &p.maps[S.map_b2], kb * BK, n * 128, bar);
-    } else {
-      // weights [K, N]: boxes of 64 N (contiguous) x 64 K rows, 8 KB each
-      tma_load_2d(sb, &p.maps[S.map_b], n * 128, kb * BK, bar);
-      tma_load_2d(sb + 8192, &p.maps[S.map_b], n * 128 + 64, kb * BK, bar);
-      if (S.map_b2 >= 0) {
-        tma_load_2d(sb + 16384, &p.maps[S.map_b2], n * 128, kb * BK, bar);
-        tma_load_2d(sb + 24576, &p.maps[S.map_b2], n * 128 + 64, kb * BK, bar);
+    // B operand(s): bn rows of N per operand; a second operand (the up
+    // projection of gate|up) follows the first, so one N = 2*bn MMA covers both.
+    const int nops = S.map_b2 >= 0 ? 2 : 1;
+    for (int op = 0; op < nops; ++op) {
+      const CUtensorMap* bm = &p.maps[op == 0 ? S.map_b : S.map_b2];
+      uint8_t* dst = sb + op * S.bn * (BK * 2);
+      if (S.b_major == 0) {
+        // weights [N, K]: boxes of 64 K x 128 N rows (16 KB), stacked along N
+        for (int h = 0; h < S.bn / 128; ++h) tma_load_2d(dst + h * 16384, bm, kb * BK, n * S.bn + h * 128, bar);
+      } else {
+        // weights [K, N]: boxes of 64 N (contiguous) x 64 K rows (8 KB), one per 64 columns
+        for (int h = 0; h < S.bn / 64; ++h) tma_load_2d(dst + h * 8192, bm, n * S.bn + h * 64, kb * BK, bar);
       }
     }
     sc->issued_parity[rp.slot] = static_cast<int>(rp.phase);
@@ -337,7 +339,7 @@ __device__ void release_tile(const KParams& p, const StageP& S, SmemCtl<NS>* sc,
 
 template <int NS>
 __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* staging, uint32_t unit, uint32_t& acc,
-                              uint32_t& acc_phase) {
+                              uint32_t& acc_phase, int& last_buf) {
   const StageP& S = p.st[unit_stage(unit)];
   const int m = unit_m(unit), n = unit_n(unit);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -346,24 +348,25 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
   if (!wait_bar(&sc->tfull[acc], acc_phase, sc, p, 4)) return false;
   tc_fence_after();
   const uint32_t tbase = sc->tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * static_cast<uint32_t>(p.acc_stride);
+  const int nchunks = S.bn / 64;
 #pragma unroll 1
-  for (int c = 0; c < 2; ++c) {
+  for (int c = 0; c < nchunks; ++c) {
     uint32_t v[2][32];
     uint32_t u[2][32];
     tmem_ld32(tbase + c * 64, v[0]);
     tmem_ld32(tbase + c * 64 + 32, v[1]);
     if (S.epi == EPI_SWIGLU) {
-      tmem_ld32(tbase + 128 + c * 64, u[0]);
-      tmem_ld32(tbase + 128 + c * 64 + 32, u[1]);
+      tmem_ld32(tbase + S.bn + c * 64, u[0]);
+      tmem_ld32(tbase + S.bn + c * 64 + 32, u[1]);
     }
     tc_wait_ld();
-    if (c == 1) {
+    if (c == nchunks - 1) {
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sc->tempty[acc]);
     }
     uint32_t w[32];
-    const int col0 = n * 128 + c * 64;
+    const int col0 = n * S.bn + c * 64;
 #pragma unroll
     for (int j = 0; j < 64; j += 2) {
       float a = __uint_as_float(v[j >> 5][j & 31]);
@@ -377,21 +380,35 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
       }
       w[j >> 1] = pack2(a, b, p.bf16);
     }
-    // the previous store out of this chunk buffer must have finished reading it
-    if (lane == 0) tma_store_wait_read<1>();
+    // Two chunk buffers alternate.  Every earlier store that read this buffer
+    // must be done: if the newest committed store read the other buffer, all
+    // but that one group suffice; if it read this buffer, wait for all.
+    const int buf = c & 1;
+    if (lane == 0) {
+      if (last_buf == buf)
+        tma_store_wait_read<0>();
+      else
+        tma_store_wait_read<1>();
+    }
     __syncwarp();
-    stage_row(staging, c, row, w);
+    stage_row(staging, buf, row, w);
     fence_proxy_async_shared();
     __syncwarp();
     // boxes that start past the tensor's end are skipped, not clipped
-    if (lane == 0 && col0 < S.n_extent && m * BM + q * 32 < S.m_extent) {
-      tma_store_2d(&p.maps[S.map_out], staging + c * (BM * 128) + q * 32 * 128, col0, m * BM + q * 32);
-      tma_store_commit();
+    if (col0 < S.n_extent && m * BM + q * 32 < S.m_extent) {
+      if (lane == 0) {
+        tma_store_2d(&p.maps[S.map_out], staging + buf * (BM * 128) + q * 32 * 128, col0, m * BM + q * 32);
+        tma_store_commit();
+      }
+      last_buf = buf;
     }
   }
   acc ^= 1u;
   if (acc == 0u) acc_phase ^= 1u;
-  if (S.rel_tile != nullptr) release_tile(p, S, sc, m, n, lane);
+  if (S.rel_tile != nullptr) {
+    release_tile(p, S, sc, m, n, lane);
+    last_buf = -1;
+  }
   return true;
 }
 
@@ -496,6 +513,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
     }
   } else {
     uint32_t q = 0, qphase = 0, acc = 0, acc_phase = 0;
+    int last_buf = -1;  // staging buffer read by this warp's newest committed store
     bool ok = true;
     while (ok) {
       if (!wait_bar(&sc->uq_full[q], qphase, sc, p, 7)) break;
@@ -507,7 +525,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
         qphase ^= 1u;
       }
       if (unit == UNIT_END) break;
-      if (p.st[unit_stage(unit)].kind == STAGE_GEMM) ok = epi_gemm_unit<NS>(p, sc, staging, unit, acc, acc_phase);
+      if (p.st[unit_stage(unit)].kind == STAGE_GEMM)
+        ok = epi_gemm_unit<NS>(p, sc, staging, unit, acc, acc_phase, last_buf);
     }
     if (lane == 0) tma_store_wait_all<0>();
     __syncwarp();

@@ -68,7 +68,7 @@ typedef enum cs_dtype { CS_F16 = 0, CS_BF16 = 1 } cs_dtype;
 typedef enum cs_chain_kind { CS_CHAIN_MLP_GELU = 0, CS_CHAIN_MLP_SWIGLU = 1, CS_CHAIN_ATTN = 2 } cs_chain_kind;
 
 /* When a consumer tile may read the intermediate (CuSync README, first paragraph:
- * policies over dependent tiles).  A producer tile covers 128 rows x 128 columns
+ * policies over dependent tiles).  A producer tile covers 128 rows x tile_n columns
  * of the intermediate; a consumer K-slice of 64 columns lies inside one of them.
  *  TILE    : wait for the one producer tile that wrote the K-slice.
  *  ROW     : wait for every producer tile of the consumer's 128-row block.
@@ -98,8 +98,13 @@ typedef struct cs_chain_desc {
   int heads;           /* ATTN only: number of heads */
   int head_dim;        /* ATTN only: must be 128 */
   int num_sms;         /* persistent grid size; 0 = every SM of the device */
-  int lag;             /* schedule: producer 128-row blocks issued before the first
-                          consumer block; -1 = auto                                  */
+  int lag;             /* schedule: producer row-block groups issued before the
+                          first consumer group; -1 = auto (1)                       */
+  int group_m;         /* schedule: 128-row blocks per rasterisation group (units of
+                          a group run column-tile-major so concurrent tiles share
+                          weights in L2); 0 = auto                                  */
+  int tile_n;          /* output columns per GEMM tile: 128 or 256; 0 = auto.
+                          SwiGLU producer tiles are always 128 (gate|up = 256).     */
   unsigned long long spin_timeout_ns; /* per-wait limit of a consumer tile; 0 = 2 s */
 } cs_chain_desc;
 
@@ -177,7 +182,9 @@ typedef struct cs_chain_info {
   int n_units;             /* total units of a fused forward */
   int num_sms;             /* persistent grid size */
   int smem_bytes;          /* dynamic shared memory per CTA */
-  int lag;                 /* schedule lag actually used */
+  int lag;                 /* schedule lag actually used (groups) */
+  int group_m;             /* rasterisation group actually used (row blocks) */
+  int tile_n[3];           /* output columns per tile of each stage */
   int stride;              /* strided-policy stride actually used */
   void* intermediate[2];   /* H (MLP) or QKV, O (ATTN): device pointers owned by the plan */
   size_t sem_words[2];     /* length of each boundary's tile-semaphore array */
@@ -187,7 +194,9 @@ cs_status cs_chain_query(cs_chain_t plan, cs_chain_info* info);
 
 /* Host-only: the dispatch order a plan with this desc and grid size would use.
  * Each entry encodes one unit as (stage << 28) | (m_tile << 14) | n_tile; for an
- * ATTN stage n_tile is the head.  *n_out receives the count; entries beyond cap
+ * ATTN stage n_tile is the head.  Row blocks are taken in groups of group_m; a
+ * stage's units of one group are listed column-tile-major; at step t, stage s
+ * lists group t - s*lag, so every producer a unit waits on is listed before it.  *n_out receives the count; entries beyond cap
  * are not written (cap may be 0 to query the count).  Needs no GPU. */
 cs_status cs_schedule_build(const cs_chain_desc* desc, int num_sms, uint32_t* units, size_t cap,
                             size_t* n_out);

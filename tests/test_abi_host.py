@@ -76,14 +76,15 @@ def _deps(stage_kind, s, m, n, d, q):
     return [(s - 1, m, t) for t in range(ntp)]
 
 
-@pytest.mark.parametrize("M,H,F,sms,lag", [(64, 256, 1024, 148, -1), (2048, 12288, 6144, 148, -1),
-                                           (2048, 12288, 6144, 152, 0), (1, 12288, 6144, 148, -1),
-                                           (1000, 8192, 2752, 148, 2), (1536, 8192, 8192, 148, 5)])
-def test_schedule_is_dependency_ordered(cs, M, H, F, sms, lag):
-    d = cs.cs_chain_desc_init(M=M, H=H, F=F, lag=lag)
+@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("M,H,F,sms,lag,group", [(64, 256, 1024, 148, -1, 0), (2048, 12288, 6144, 148, -1, 0),
+                                                 (2048, 12288, 6144, 152, 0, 3), (1, 12288, 6144, 148, -1, 0),
+                                                 (1000, 8192, 2752, 148, 2, 1), (1536, 8192, 8192, 148, 5, 5)])
+def test_schedule_is_dependency_ordered(cs, M, H, F, sms, lag, group, tile_n):
+    d = cs.cs_chain_desc_init(M=M, H=H, F=F, lag=lag, group_m=group, tile_n=tile_n)
     units = cs.cs_schedule_build(d, sms)
     m_tiles = -(-M // 128)
-    n0, n1 = -(-F // 128), -(-H // 128)
+    n0, n1 = -(-F // tile_n), -(-H // tile_n)
     dec = [cs.decode_unit(u) for u in units]
     # every unit exactly once
     expect = {(0, m, n) for m in range(m_tiles) for n in range(n0)} | {(1, m, n) for m in range(m_tiles) for n in range(n1)}
@@ -92,3 +93,19 @@ def test_schedule_is_dependency_ordered(cs, M, H, F, sms, lag):
     for (s, m, n), i in pos.items():
         for dep in _deps("mlp", s, m, n, d, [n0, n1]):
             assert pos[dep] < i, f"unit {(s, m, n)} at {i} precedes its producer {dep}"
+
+
+def test_schedule_rasterises_column_major_within_a_group(cs):
+    d = cs.cs_chain_desc_init(M=2048, H=12288, F=6144, group_m=4, lag=1, tile_n=128)
+    dec = [cs.decode_unit(u) for u in cs.cs_schedule_build(d, 148)]
+    # first group of producers: (n, m) with m fastest
+    assert dec[:8] == [(0, 0, 0), (0, 1, 0), (0, 2, 0), (0, 3, 0), (0, 0, 1), (0, 1, 1), (0, 2, 1), (0, 3, 1)]
+    # then the second producer group, then the first consumer group
+    assert dec[192] == (0, 4, 0) and dec[384] == (1, 0, 0)
+
+
+def test_auto_tile_width(cs):
+    big = cs.cs_schedule_build(cs.cs_chain_desc_init(M=2048, H=12288, F=6144), 148)
+    small = cs.cs_schedule_build(cs.cs_chain_desc_init(M=256, H=12288, F=6144), 148)
+    assert len(big) == 16 * 24 + 16 * 48        # 256-wide tiles once the grid is filled twice
+    assert len(small) == 2 * 48 + 2 * 96        # 128-wide tiles otherwise

@@ -51,26 +51,28 @@ def test_tiny_chain_golden_values():
     assert np.max(np.abs(got - ref)) <= TOL * np.max(np.abs(full_ref))
 
 
+@pytest.mark.parametrize("tile_n", [128, 256])
 @pytest.mark.parametrize("layout", ["kn", "nk"])
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
 @pytest.mark.parametrize("M,H,F", [(1, 256, 1024), (100, 320, 392), (200, 200, 136), (384, 512, 640),
                                    (129, 1024, 2752)])
-def test_ragged_shapes(M, H, F, dtype, layout):
+def test_ragged_shapes(M, H, F, dtype, layout, tile_n):
     inp = cs_inputs.make_custom("gelu", M, H, F, dtype=dtype, seed=3)
     dev = device_tensors(inp, layout)
-    with plan_for(inp, "tile", layout) as plan:
+    with plan_for(inp, "tile", layout, tile_n=tile_n) as plan:
         Y = forward(plan, dev)
     Yref, _ = _oracle(inp)
     assert oracle.rel_err(Y.cpu(), Yref) <= TOL
 
 
-def test_policies_bit_identical_and_layouts_agree():
+@pytest.mark.parametrize("tile_n", [128, 256])
+def test_policies_bit_identical_and_layouts_agree(tile_n):
     inp = cs_inputs.make_custom("gelu", 300, 768, 1536, seed=5)
     outs = {}
     for layout in ("kn", "nk"):
         dev = device_tensors(inp, layout)
         for pol in ("tile", "row", "strided", "stream"):
-            with plan_for(inp, pol, layout) as plan:
+            with plan_for(inp, pol, layout, tile_n=tile_n, group_m=2) as plan:
                 outs[(layout, pol)] = forward(plan, dev).cpu()
     Yref, _ = _oracle(inp)
     base = outs[("kn", "tile")]
@@ -79,10 +81,11 @@ def test_policies_bit_identical_and_layouts_agree():
         assert torch.equal(v, base), f"{k} differs from kn/tile"
 
 
-def test_flags_end_at_expected_counts():
+@pytest.mark.parametrize("tile_n", [128, 256])
+def test_flags_end_at_expected_counts(tile_n):
     inp = cs_inputs.make_custom("gelu", 520, 512, 1280, seed=6)
     dev = device_tensors(inp)
-    with plan_for(inp, "tile") as plan:
+    with plan_for(inp, "tile", tile_n=tile_n) as plan:
         q = cs.cs_chain_query(plan)
         Y = torch.empty_like(dev["X"])
         for e in range(1, 6):
@@ -97,19 +100,20 @@ def test_policies_and_control_keep_flags_consistent():
     inp = cs_inputs.make_custom("gelu", 256, 512, 512, seed=7)
     dev = device_tensors(inp)
     for pol in ("row", "strided", "stream"):
-        with plan_for(inp, pol) as plan:
+        with plan_for(inp, pol, tile_n=128) as plan:
             for _ in range(3):
                 forward(plan, dev)
             tiles, rows, epoch = cs.cs_chain_debug_read_sems(plan, 0)
             assert epoch == 3 and all(v == 3 for r in tiles for v in r) and rows == [3 * 4] * 2
 
 
-def test_delay_injection_never_changes_a_bit():
+@pytest.mark.parametrize("tile_n", [128, 256])
+def test_delay_injection_never_changes_a_bit(tile_n):
     inp = cs_inputs.make_custom("gelu", 640, 1024, 2048, seed=8)
     dev = device_tensors(inp)
     ref = None
     for pol in ("tile", "row", "strided"):
-        with plan_for(inp, pol) as plan:
+        with plan_for(inp, pol, tile_n=tile_n, group_m=2) as plan:
             q = cs.cs_chain_query(plan)
             for seed in range(3):
                 g = torch.Generator().manual_seed(100 + seed)
@@ -180,7 +184,7 @@ def test_shape_and_dtype_checks_in_binding():
 def test_gpt3_shard_sampled_rows(M):
     inp = cs_inputs.make_inputs("gpt3", M=M, seed=0)
     dev = device_tensors(inp)
-    with plan_for(inp, "tile") as plan:
+    with plan_for(inp, "tile") as plan:  # the bench configuration (auto tile width, grouping)
         Y = forward(plan, dev).cpu()
     rows = cs_inputs.sample_rows(M, 64)
     Yref, _ = _oracle(inp, rows)
