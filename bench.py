@@ -50,10 +50,12 @@ def parse():
     ap.add_argument("--workload", default="gpt3", choices=["gpt3", "stress", "llama", "tiny"])
     ap.add_argument("--M", type=int, default=None)
     ap.add_argument("--policy", default="tile", choices=["tile", "row", "strided", "stream"])
-    ap.add_argument("--layout", default="kn", choices=["kn", "nk"])
+    ap.add_argument("--layout", default="nk", choices=["kn", "nk"],
+                    help="weight storage: nk = [N, K] (torch.nn.Linear), kn = [K, N]")
     ap.add_argument("--lag", type=int, default=-1)
     ap.add_argument("--tile-n", type=int, default=0)
     ap.add_argument("--group-m", type=int, default=0)
+    ap.add_argument("--tile-m", type=int, default=0)
     ap.add_argument("--quick", action="store_true", help="headline kernel only (profiling runs)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU-oracle sample time")
@@ -274,12 +276,13 @@ def run_reference(args):
 METRIC = "MLP-chain TFLOP/s & % roofline vs M on 1 GB300; sync overhead vs best solo GEMMs"
 
 
-def workload_config(name, M, inp, policy):
+def workload_config(name, M, inp, policy, layout="nk"):
     desc = {"gpt3": "GPT-3 175B 8-way TP MLP shard", "stress": "last-wave stress two-GEMM GeLU chain",
             "llama": "LLaMA 65.2B 8-way TP SwiGLU shard", "tiny": "tiny MLP chain"}[name]
     return {"workload": f"{desc}: X[{M},{inp.H}] -> F={inp.F} -> H={inp.H}, {str(inp.dtype).split('.')[-1]}, "
                         f"policy={policy}",
             "M": M, "H": inp.H, "F": inp.F, "policy": policy, "accumulate": "fp32",
+            "weights": "[N, K] row-major (torch.nn.Linear)" if layout == "nk" else "[K, N] row-major",
             "l2": "inputs larger than L2 (weights alone exceed the 126 MB L2), no flush"}
 
 
@@ -317,7 +320,8 @@ def main():
 
     def make_plan(policy, MM=M):
         d = cs.cs_chain_desc_init(kind=kind, M=MM, H=inp.H, F=inp.F, dtype=inp.dtype, policy=policy,
-                                  weight_layout=lay, lag=args.lag, tile_n=args.tile_n, group_m=args.group_m)
+                                  weight_layout=lay, lag=args.lag, tile_n=args.tile_n, group_m=args.group_m,
+                                  tile_m=args.tile_m)
         return cs.cs_chain_plan(d)
 
     plan = make_plan(args.policy)
@@ -369,8 +373,9 @@ def main():
         gbs = nbytes / (ms_launch * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak}
     roof.update({"traffic": None, "peak_source": f"{peak_src} ({'sustained' if sustained else 'burst'})",
-                 "kernel": "cs_chain_kernel<4,49152>" if (kind == "swiglu" or 256 in plan_info["tile_n"])
-                 else "cs_chain_kernel<6,32768>",
+                 "kernel": ("cs_chain_kernel<6,32768,2>" if plan_info["tile_m"] == 256 else
+                            "cs_chain_kernel<4,49152,1>" if (kind == "swiglu" or 256 in plan_info["tile_n"])
+                            else "cs_chain_kernel<6,32768,1>"),
                  "algorithmic_flops_per_launch": flops if launches_per_step == 1 else None,
                  "algorithmic_bytes_per_launch": nbytes if launches_per_step == 1 else None,
                  "launch_ms": ms_launch, "roofline_time_ms": t_roof_ms})
@@ -379,8 +384,9 @@ def main():
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16" if inp.dtype == torch.float16 else "bf16", "data": "synthetic",
-        "config": dict(workload_config(args.workload, M, inp, args.policy), parallelism=f"replicas{ws}",
-                       tile_n=plan_info["tile_n"][:2], group_m=plan_info["group_m"], lag=plan_info["lag"],
+        "config": dict(workload_config(args.workload, M, inp, args.policy, lay), parallelism=f"replicas{ws}",
+                       tile_n=plan_info["tile_n"][:2], tile_m=plan_info["tile_m"], group_m=plan_info["group_m"],
+                       lag=plan_info["lag"],
                        grid=plan_info["num_sms"]),
         "roofline": roof, "gpu_launches": args.steps * launches_per_step,
     }

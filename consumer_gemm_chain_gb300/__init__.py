@@ -14,8 +14,10 @@ from .chain import (  # noqa: F401
     cs_attn_chain_forward,
     cs_chain_debug_copy_intermediate,
     cs_chain_debug_read_sems,
+    cs_chain_debug_read_trace,
     cs_chain_debug_set_delays,
     cs_chain_debug_skip_release,
+    cs_chain_debug_trace,
     cs_chain_desc_init,
     cs_chain_destroy,
     cs_chain_forward_stage,

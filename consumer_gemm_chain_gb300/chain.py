@@ -36,7 +36,7 @@ EXPORTED = (
     "cs_chain_desc_init", "cs_chain_plan", "cs_chain_destroy", "cs_mlp_forward", "cs_attn_chain_forward",
     "cs_chain_forward_stage", "cs_chain_status", "cs_chain_reset", "cs_last_error_string", "cs_chain_query",
     "cs_schedule_build", "cs_chain_debug_read_sems", "cs_chain_debug_set_delays", "cs_chain_debug_skip_release",
-    "cs_chain_debug_copy_intermediate", "cs_abi_version",
+    "cs_chain_debug_copy_intermediate", "cs_chain_debug_trace", "cs_chain_debug_read_trace", "cs_abi_version",
 )
 
 
@@ -45,7 +45,7 @@ class cs_chain_desc(ctypes.Structure):
                 ("dtype", ctypes.c_int), ("policy", ctypes.c_int), ("weight_layout", ctypes.c_int),
                 ("stride", ctypes.c_int), ("heads", ctypes.c_int), ("head_dim", ctypes.c_int),
                 ("num_sms", ctypes.c_int), ("lag", ctypes.c_int), ("group_m", ctypes.c_int),
-                ("tile_n", ctypes.c_int), ("spin_timeout_ns", ctypes.c_ulonglong)]
+                ("tile_n", ctypes.c_int), ("tile_m", ctypes.c_int), ("spin_timeout_ns", ctypes.c_ulonglong)]
 
 
 class cs_mlp_args(ctypes.Structure):
@@ -61,7 +61,8 @@ class cs_chain_info(ctypes.Structure):
     _fields_ = [("stages", ctypes.c_int), ("m_tiles", ctypes.c_int), ("n_tiles", ctypes.c_int * 3),
                 ("units", ctypes.c_int * 3), ("n_units", ctypes.c_int), ("num_sms", ctypes.c_int),
                 ("smem_bytes", ctypes.c_int), ("lag", ctypes.c_int), ("group_m", ctypes.c_int),
-                ("tile_n", ctypes.c_int * 3), ("stride", ctypes.c_int),
+                ("tile_n", ctypes.c_int * 3), ("tile_m", ctypes.c_int), ("sched_units", ctypes.c_int * 3),
+                ("stride", ctypes.c_int),
                 ("intermediate", ctypes.c_void_p * 2), ("sem_words", ctypes.c_size_t * 2)]
 
 
@@ -87,6 +88,8 @@ def _load() -> ctypes.CDLL:
         "cs_chain_debug_set_delays": (I, [V, I, ctypes.POINTER(ctypes.c_uint32), S]),
         "cs_chain_debug_skip_release": (I, [V, I, I]),
         "cs_chain_debug_copy_intermediate": (I, [V, I, V, S]),
+        "cs_chain_debug_trace": (I, [V, I]),
+        "cs_chain_debug_read_trace": (I, [V, ctypes.POINTER(ctypes.c_uint64), S, ctypes.POINTER(S)]),
         "cs_abi_version": (I, []),
     }
     for name, (res, args) in sig.items():
@@ -277,7 +280,8 @@ def cs_chain_query(plan: Plan) -> dict:
     _check(_lib.cs_chain_query(plan.handle, ctypes.byref(i)), "cs_chain_query")
     return {"stages": i.stages, "m_tiles": i.m_tiles, "n_tiles": list(i.n_tiles), "units": list(i.units),
             "n_units": i.n_units, "num_sms": i.num_sms, "smem_bytes": i.smem_bytes, "lag": i.lag,
-            "group_m": i.group_m, "tile_n": list(i.tile_n),
+            "group_m": i.group_m, "tile_n": list(i.tile_n), "tile_m": i.tile_m,
+            "sched_units": list(i.sched_units),
             "stride": i.stride, "intermediate": [i.intermediate[0], i.intermediate[1]],
             "sem_words": [i.sem_words[0], i.sem_words[1]]}
 
@@ -327,3 +331,18 @@ def cs_chain_debug_copy_intermediate(plan: Plan, which: int, out) -> None:
     nbytes = out.numel() * out.element_size()
     _check(_lib.cs_chain_debug_copy_intermediate(plan.handle, which, out.data_ptr(), nbytes),
            "cs_chain_debug_copy_intermediate")
+
+
+def cs_chain_debug_trace(plan: Plan, enable: bool = True) -> None:
+    """Record a per-unit timeline in every later forward (see cs_chain.h)."""
+    _check(_lib.cs_chain_debug_trace(plan.handle, 1 if enable else 0), "cs_chain_debug_trace")
+
+
+def cs_chain_debug_read_trace(plan: Plan) -> list[list[int]]:
+    """Trace records (8 integers each) of the latest forward."""
+    n = ctypes.c_size_t()
+    _check(_lib.cs_chain_debug_read_trace(plan.handle, None, 0, ctypes.byref(n)), "cs_chain_debug_read_trace")
+    buf = (ctypes.c_uint64 * (8 * max(1, n.value)))()
+    _check(_lib.cs_chain_debug_read_trace(plan.handle, buf, n.value, ctypes.byref(n)), "cs_chain_debug_read_trace")
+    vals = list(buf)
+    return [vals[i * 8:(i + 1) * 8] for i in range(n.value)]

@@ -68,7 +68,11 @@ struct cs_chain_s {
   int group_m = 1;
   int stride = 1;
   int bn[3] = {128, 128, 128};
-  int cfg_b = 0;  // 1: 48 KB-stage kernel (256-wide tiles or gate|up)
+  int cfg_b = 0;  // 1: 48 KB-stage kernel (256-wide one-SM tiles or gate|up)
+  int cg = 1;     // CTAs per tile (2: 256-row tiles on a 2-SM cluster)
+  int m_units = 0;   // tile rows of the schedule
+  int m_blocks = 0;  // 128-row blocks (semaphore rows)
+  int sched_units[3] = {0, 0, 0};
   int smem = 0;
   // device memory owned by the plan
   void* inter[2] = {nullptr, nullptr};
@@ -80,6 +84,8 @@ struct cs_chain_s {
   int n_fused = 0;
   uint32_t* sched_stage[3] = {nullptr, nullptr, nullptr};
   uint32_t* delays[3] = {nullptr, nullptr, nullptr};
+  unsigned long long* trace = nullptr;
+  int trace_records = 0;
   int skip[3] = {-1, -1, -1};
   // TMA descriptors
   CUtensorMap maps[kMaxMaps];
@@ -131,7 +137,9 @@ inline uint32_t enc_unit(int s, int m, int n) {
 
 // Geometry shared by the host-only schedule builder and the plan.
 struct Geometry {
-  int stages = 0, m_tiles = 0;
+  int stages = 0, m_tiles = 0;  // m_tiles: tile rows (tile_m each)
+  int cg = 1;                   // CTAs per tile
+  int m_blocks = 0;             // 128-row blocks
   int n_tiles[3] = {0, 0, 0};
   int k_iters[3] = {0, 0, 0};
   int bn[3] = {128, 128, 128};
@@ -154,6 +162,10 @@ cs_status validate(const cs_chain_desc* d) {
   if (d->group_m < 0) return fail(CS_ERR_INVALID_ARG, "group_m=%d", d->group_m);
   if (d->tile_n != 0 && d->tile_n != 128 && d->tile_n != 256)
     return fail(CS_ERR_INVALID_ARG, "tile_n=%d (0, 128 or 256)", d->tile_n);
+  if (d->tile_m != 0 && d->tile_m != 128 && d->tile_m != 256)
+    return fail(CS_ERR_INVALID_ARG, "tile_m=%d (0, 128 or 256)", d->tile_m);
+  if (d->tile_m == 256 && (d->tile_n == 128 || d->kind != CS_CHAIN_MLP_GELU))
+    return fail(CS_ERR_UNSUPPORTED, "tile_m=256 is built for 256-wide GeLU-MLP tiles only");
   if (d->kind == CS_CHAIN_ATTN) {
     if (d->head_dim != 128) return fail(CS_ERR_UNSUPPORTED, "head_dim=%d (only 128 is built)", d->head_dim);
     if (d->heads < 1 || d->heads * d->head_dim != d->F)
@@ -165,11 +177,18 @@ cs_status validate(const cs_chain_desc* d) {
 
 Geometry geometry(const cs_chain_desc* d, int num_sms) {
   Geometry g;
-  g.m_tiles = cdiv(d->M, cs::BM);
-  // 256-wide tiles halve the operand bytes per FLOP of the 128-wide ones; they
-  // pay off once there are enough tiles to fill the grid several times.
+  const int blocks = cdiv(d->M, cs::BM);
+  // 256-wide tiles need 2/3 of the operand bytes per FLOP of 128-wide ones;
+  // they pay off once the producer stage alone fills half of the grid.
   int tn = d->tile_n;
-  if (tn == 0) tn = (g.m_tiles * cdiv(d->F, 256) >= 2 * num_sms) ? 256 : 128;
+  if (tn == 0) tn = (2 * blocks * cdiv(d->F, 256) >= num_sms) ? 256 : 128;
+  // A 2-SM pair per 256 x 256 tile halves them again (each SM loads half of B).
+  int tm = d->tile_m;
+  if (tm == 0) tm = (tn == 256 && d->kind == CS_CHAIN_MLP_GELU && blocks >= 8) ? 256 : 128;
+  if (tm == 256 && (tn != 256 || d->kind != CS_CHAIN_MLP_GELU)) tm = 128;
+  g.cg = tm / cs::BM;
+  g.m_tiles = cdiv(d->M, tm);
+  g.m_blocks = g.m_tiles * g.cg;
   if (d->kind == CS_CHAIN_ATTN) {
     g.stages = 3;
     g.bn[0] = 128;
@@ -189,13 +208,12 @@ Geometry geometry(const cs_chain_desc* d, int num_sms) {
     g.n_tiles[1] = cdiv(d->H, tn);
     g.k_iters[1] = cdiv(d->F, cs::BK);
   }
-  g.group_m = d->group_m > 0 ? d->group_m : 8;
+  g.group_m = d->group_m > 0 ? d->group_m : 8 / g.cg;
   if (g.group_m > g.m_tiles) g.group_m = g.m_tiles;
   const int groups = cdiv(g.m_tiles, g.group_m);
   g.lag = d->lag >= 0 ? d->lag : 1;
   if (g.lag > groups) g.lag = groups;
   g.stride = d->stride > 0 ? d->stride : (d->kind == CS_CHAIN_ATTN ? d->heads : 4);
-  (void)num_sms;
   return g;
 }
 
@@ -238,9 +256,9 @@ int device_sms(int* out) {
   return dev;
 }
 
-template <int NS, int SB>
+template <int NS, int SB, int CG>
 cs_status set_smem_attr() {
-  static cudaError_t once = cudaFuncSetAttribute(cs::cs_chain_kernel<NS, SB>,
+  static cudaError_t once = cudaFuncSetAttribute(cs::cs_chain_kernel<NS, SB, CG>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes_for<NS, SB>());
   if (once != cudaSuccess) return fail(CS_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(once));
   return CS_OK;
@@ -254,6 +272,7 @@ void free_plan(cs_chain_s* p) {
   if (p->sched_fused) cudaFree(p->sched_fused);
   for (auto& b : p->sched_stage) if (b) cudaFree(b);
   for (auto& b : p->delays) if (b) cudaFree(b);
+  if (p->trace) cudaFree(p->trace);
   delete p;
 }
 
@@ -273,12 +292,13 @@ cs_status upload(T** dst, const std::vector<T>& v) {
 enum { MAP_X = 0, MAP_W1 = 1, MAP_WU = 2, MAP_HST = 3, MAP_HLD = 4, MAP_W2 = 5, MAP_Y = 6 };
 
 // Encode a weight map: math shape [K, N].  KN storage: row-major [K, N], boxes of
-// 64 N x 64 K.  NK storage: row-major [N, K], boxes of 64 K x 128 N.
-cs_status encode_weight(cs_chain_s* p, int slot, const void* ptr, int K, int N) {
+// 64 N x 64 K.  NK storage: row-major [N, K], boxes of 64 K x box_n N rows (the
+// columns of a tile one CTA loads).
+cs_status encode_weight(cs_chain_s* p, int slot, const void* ptr, int K, int N, int box_n) {
   if (p->slots[slot].valid && p->slots[slot].ptr == ptr) return CS_OK;
   const int bf16 = p->d.dtype == CS_BF16;
   cs_status s = p->d.weight_layout == CS_WEIGHTS_KN ? encode_2d(&p->maps[slot], ptr, bf16, N, K, 64, 64)
-                                                     : encode_2d(&p->maps[slot], ptr, bf16, K, N, 64, 128);
+                                                     : encode_2d(&p->maps[slot], ptr, bf16, K, N, 64, box_n);
   if (s != CS_OK) return s;
   p->slots[slot].ptr = ptr;
   p->slots[slot].valid = true;
@@ -301,6 +321,8 @@ void fill_common(const cs_chain_s* p, cs::KParams& kp) {
   kp.timeout_ns = p->d.spin_timeout_ns ? p->d.spin_timeout_ns : kDefaultTimeoutNs;
   kp.watchdog_ns = kp.timeout_ns * 4 > 4000000000ull ? kp.timeout_ns * 4 : 4000000000ull;
   kp.bf16 = p->d.dtype == CS_BF16;
+  kp.trace = p->trace;
+  kp.trace_records = p->trace_records;
 }
 
 void fill_mlp_stages(const cs_chain_s* p, const cs_mlp_args* a, cs::KParams& kp) {
@@ -326,12 +348,12 @@ void fill_mlp_stages(const cs_chain_s* p, const cs_mlp_args* a, cs::KParams& kp)
   s0.map_b = MAP_W1;
   s0.map_b2 = swiglu ? MAP_WU : -1;
   s0.map_out = MAP_HST;
-  s0.b_bytes = (swiglu ? 2 : 1) * p->bn[0] * cs::BK * 2;
+  s0.b_bytes = (swiglu ? 2 : 1) * (p->bn[0] / p->cg) * cs::BK * 2;
   s0.bias_f16 = reinterpret_cast<const __half*>(a ? a->b1 : nullptr);
   s0.bias_bf16 = reinterpret_cast<const __nv_bfloat16*>(a ? a->b1 : nullptr);
   s0.wait = cs::WAIT_NONE;
   s0.rel_tile = p->sems[0];
-  s0.rel_row = p->sems[0] + static_cast<size_t>(p->m_tiles) * p->n_tiles[0];
+  s0.rel_row = p->sems[0] + static_cast<size_t>(p->m_blocks) * p->n_tiles[0];
   s0.delay_ns = p->delays[0];
   s0.skip_unit = p->skip[0];
 
@@ -351,10 +373,10 @@ void fill_mlp_stages(const cs_chain_s* p, const cs_mlp_args* a, cs::KParams& kp)
   s1.map_b = MAP_W2;
   s1.map_b2 = -1;
   s1.map_out = MAP_Y;
-  s1.b_bytes = p->bn[1] * cs::BK * 2;
+  s1.b_bytes = (p->bn[1] / p->cg) * cs::BK * 2;
   s1.wait = wait;
   s1.dep_tile = p->sems[0];
-  s1.dep_row = p->sems[0] + static_cast<size_t>(p->m_tiles) * p->n_tiles[0];
+  s1.dep_row = p->sems[0] + static_cast<size_t>(p->m_blocks) * p->n_tiles[0];
   s1.dep_ntiles = p->n_tiles[0];
   s1.dep_bn = p->bn[0];
   s1.stride = p->stride;
@@ -367,22 +389,36 @@ void fill_mlp_stages(const cs_chain_s* p, const cs_mlp_args* a, cs::KParams& kp)
 cs_status launch(cs_chain_s* p, cs::KParams& kp, const uint32_t* sched, int n_units, cudaStream_t stream) {
   kp.sched = sched;
   kp.n_units = n_units;
-  int grid = p->num_sms < n_units ? p->num_sms : n_units;
+  // one CTA (or CTA pair) per SM; no more than there are units
+  int grid = p->num_sms / p->cg;
+  if (grid > n_units) grid = n_units;
   if (grid < 1) grid = 1;
+  grid *= p->cg;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(cs::NUM_THREADS);
   cfg.dynamicSmemBytes = p->smem;
   cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (p->cg == 2) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
   cudaError_t e;
-  if (p->cfg_b) {
-    cs_status s = set_smem_attr<NS_B, SB_B>();
-    if (s != CS_OK) return s;
-    e = cudaLaunchKernelEx(&cfg, cs::cs_chain_kernel<NS_B, SB_B>, kp);
+  cs_status s;
+  if (p->cg == 2) {
+    if ((s = set_smem_attr<NS_A, SB_A, 2>()) != CS_OK) return s;
+    e = cudaLaunchKernelEx(&cfg, cs::cs_chain_kernel<NS_A, SB_A, 2>, kp);
+  } else if (p->cfg_b) {
+    if ((s = set_smem_attr<NS_B, SB_B, 1>()) != CS_OK) return s;
+    e = cudaLaunchKernelEx(&cfg, cs::cs_chain_kernel<NS_B, SB_B, 1>, kp);
   } else {
-    cs_status s = set_smem_attr<NS_A, SB_A>();
-    if (s != CS_OK) return s;
-    e = cudaLaunchKernelEx(&cfg, cs::cs_chain_kernel<NS_A, SB_A>, kp);
+    if ((s = set_smem_attr<NS_A, SB_A, 1>()) != CS_OK) return s;
+    e = cudaLaunchKernelEx(&cfg, cs::cs_chain_kernel<NS_A, SB_A, 1>, kp);
   }
   if (e != cudaSuccess) return fail(CS_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
   return CS_OK;
@@ -398,9 +434,9 @@ cs_status bind_mlp(cs_chain_s* p, const cs_mlp_args* a) {
   const int M = p->d.M, H = p->d.H, F = p->d.F;
   cs_status s;
   if ((s = encode_act(p, MAP_X, a->X, M, H, false)) != CS_OK) return s;
-  if ((s = encode_weight(p, MAP_W1, swiglu ? a->Wg : a->W1, H, F)) != CS_OK) return s;
-  if (swiglu && (s = encode_weight(p, MAP_WU, a->Wu, H, F)) != CS_OK) return s;
-  if ((s = encode_weight(p, MAP_W2, a->W2, F, H)) != CS_OK) return s;
+  if ((s = encode_weight(p, MAP_W1, swiglu ? a->Wg : a->W1, H, F, p->bn[0] / p->cg)) != CS_OK) return s;
+  if (swiglu && (s = encode_weight(p, MAP_WU, a->Wu, H, F, p->bn[0] / p->cg)) != CS_OK) return s;
+  if ((s = encode_weight(p, MAP_W2, a->W2, F, H, p->bn[1] / p->cg)) != CS_OK) return s;
   if ((s = encode_act(p, MAP_Y, a->Y, M, H, true)) != CS_OK) return s;
   return CS_OK;
 }
@@ -425,6 +461,7 @@ cs_status cs_chain_desc_init(cs_chain_desc* d) {
   d->lag = -1;
   d->group_m = 0;
   d->tile_n = 0;
+  d->tile_m = 0;
   return CS_OK;
 }
 
@@ -461,18 +498,22 @@ cs_status cs_chain_plan(const cs_chain_desc* desc, cs_chain_t* out) {
   p->device = dev;
   p->num_sms = desc->num_sms > 0 && desc->num_sms < sms ? desc->num_sms : sms;
   Geometry g = geometry(desc, p->num_sms);
-  p->m_tiles = g.m_tiles;
+  p->m_tiles = g.m_blocks;
+  p->m_units = g.m_tiles;
+  p->m_blocks = g.m_blocks;
+  p->cg = g.cg;
   p->stages = g.stages;
   for (int i = 0; i < 3; ++i) {
     p->n_tiles[i] = g.n_tiles[i];
     p->k_iters[i] = g.k_iters[i];
-    p->units[i] = g.m_tiles * g.n_tiles[i];
+    p->units[i] = g.m_blocks * g.n_tiles[i];
+    p->sched_units[i] = g.m_tiles * g.n_tiles[i];
   }
   p->lag = g.lag;
   p->group_m = g.group_m;
   p->stride = g.stride;
   for (int i = 0; i < 3; ++i) p->bn[i] = g.bn[i];
-  p->cfg_b = desc->kind == CS_CHAIN_MLP_SWIGLU || g.bn[0] == 256 || g.bn[1] == 256 || g.bn[2] == 256;
+  p->cfg_b = g.cg == 1 && (desc->kind == CS_CHAIN_MLP_SWIGLU || g.bn[0] == 256 || g.bn[1] == 256 || g.bn[2] == 256);
   p->smem = p->cfg_b ? smem_bytes_for<NS_B, SB_B>() : smem_bytes_for<NS_A, SB_A>();
 
   auto bail = [&](cs_status st) {
@@ -485,8 +526,8 @@ cs_status cs_chain_plan(const cs_chain_desc* desc, cs_chain_t* out) {
   if (cudaMalloc(&p->inter[0], p->inter_bytes[0]) != cudaSuccess)
     return bail(fail(CS_ERR_OOM, "cudaMalloc of the intermediate failed"));
   for (int b = 0; b < g.stages - 1; ++b) {
-    p->sem_words[b] = static_cast<size_t>(g.m_tiles) * g.n_tiles[b];
-    const size_t words = p->sem_words[b] + g.m_tiles;
+    p->sem_words[b] = static_cast<size_t>(g.m_blocks) * g.n_tiles[b];
+    const size_t words = p->sem_words[b] + g.m_blocks;
     if (cudaMalloc(reinterpret_cast<void**>(&p->sems[b]), words * 4) != cudaSuccess)
       return bail(fail(CS_ERR_OOM, "cudaMalloc of semaphores failed"));
     if (cudaMemset(p->sems[b], 0, words * 4) != cudaSuccess) return bail(fail(CS_ERR_CUDA, "cudaMemset failed"));
@@ -499,6 +540,7 @@ cs_status cs_chain_plan(const cs_chain_desc* desc, cs_chain_t* out) {
   if ((s = upload(&p->sched_fused, fused)) != CS_OK) return bail(s);
   for (int st = 0; st < g.stages; ++st)
     if ((s = upload(&p->sched_stage[st], build_stage(g, st))) != CS_OK) return bail(s);
+  p->num_sms = p->num_sms / g.cg * g.cg;
   // plan-owned intermediate maps
   if ((s = encode_act(p, MAP_HST, p->inter[0], desc->M, desc->F, true)) != CS_OK) return bail(s);
   p->slots[MAP_HST].ptr = nullptr;  // plan-owned: never re-encoded
@@ -536,9 +578,9 @@ cs_status cs_mlp_forward(cs_chain_t p, const cs_mlp_args* a, void* stream) {
     kp.waits = 0;
     kp.release = 1;
     kp.bump_epoch = 0;
-    if ((s = launch(p, kp, p->sched_stage[0], p->units[0], st)) != CS_OK) return s;
+    if ((s = launch(p, kp, p->sched_stage[0], p->sched_units[0], st)) != CS_OK) return s;
     kp.bump_epoch = 1;
-    return launch(p, kp, p->sched_stage[1], p->units[1], st);
+    return launch(p, kp, p->sched_stage[1], p->sched_units[1], st);
   }
   kp.waits = 1;
   kp.release = 1;
@@ -568,7 +610,7 @@ cs_status cs_chain_forward_stage(cs_chain_t p, const void* args, int stage, void
   kp.waits = 0;
   kp.release = 0;
   kp.bump_epoch = 0;
-  return launch(p, kp, p->sched_stage[stage], p->units[stage], static_cast<cudaStream_t>(stream));
+  return launch(p, kp, p->sched_stage[stage], p->sched_units[stage], static_cast<cudaStream_t>(stream));
 }
 
 cs_status cs_chain_status(cs_chain_t p) {
@@ -607,7 +649,11 @@ cs_status cs_chain_query(cs_chain_t p, cs_chain_info* info) {
   info->smem_bytes = p->smem;
   info->lag = p->lag;
   info->group_m = p->group_m;
-  for (int i = 0; i < 3; ++i) info->tile_n[i] = p->bn[i];
+  for (int i = 0; i < 3; ++i) {
+    info->tile_n[i] = p->bn[i];
+    info->sched_units[i] = p->sched_units[i];
+  }
+  info->tile_m = cs::BM * p->cg;
   info->stride = p->stride;
   info->intermediate[0] = p->inter[0];
   info->intermediate[1] = p->inter[1];
@@ -655,6 +701,32 @@ cs_status cs_chain_debug_copy_intermediate(cs_chain_t p, int which, void* dst, s
   if (bytes > p->inter_bytes[which]) return fail(CS_ERR_INVALID_ARG, "%zu bytes > buffer (%zu)", bytes, p->inter_bytes[which]);
   CS_CUDA(cudaDeviceSynchronize());
   CS_CUDA(cudaMemcpy(dst, p->inter[which], bytes, cudaMemcpyDeviceToDevice));
+  return CS_OK;
+}
+
+cs_status cs_chain_debug_trace(cs_chain_t p, int enable) {
+  if (!p) return fail(CS_ERR_INVALID_ARG, "plan is NULL");
+  if (p->trace) {
+    cudaFree(p->trace);
+    p->trace = nullptr;
+    p->trace_records = 0;
+  }
+  if (!enable) return CS_OK;
+  const int recs = p->n_fused * p->cg;
+  const size_t bytes = static_cast<size_t>(recs) * cs::TRACE_WORDS * 8;
+  if (cudaMalloc(reinterpret_cast<void**>(&p->trace), bytes) != cudaSuccess) return fail(CS_ERR_OOM, "cudaMalloc failed");
+  CS_CUDA(cudaMemset(p->trace, 0, bytes));
+  p->trace_records = recs;
+  return CS_OK;
+}
+
+cs_status cs_chain_debug_read_trace(cs_chain_t p, uint64_t* host, size_t n, size_t* n_out) {
+  if (!p || !n_out) return fail(CS_ERR_INVALID_ARG, "NULL argument");
+  *n_out = static_cast<size_t>(p->trace_records);
+  if (!p->trace || n == 0) return CS_OK;
+  if (!host) return fail(CS_ERR_INVALID_ARG, "host is NULL");
+  const size_t m = n < *n_out ? n : *n_out;
+  CS_CUDA(cudaMemcpy(host, p->trace, m * cs::TRACE_WORDS * 8, cudaMemcpyDeviceToHost));
   return CS_OK;
 }
 

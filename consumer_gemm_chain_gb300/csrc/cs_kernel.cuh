@@ -1,18 +1,30 @@
 // Persistent tile-synchronised GEMM-chain kernel for sm_103a.
 //
-// One CTA per SM pulls work units from a dependency-ordered schedule through a
-// global atomic counter (a megakernel-style task queue: a dependent task starts
-// once the slice it reads is done, not when the whole producer op is done).
-// Roles inside a CTA (192 threads):
-//   warp 0      : dispatcher + TMA producer (lane 0).  For consumer units it
-//                 acquire-spins on the producer tile semaphores of each K-slice
-//                 before issuing the TMA loads of the intermediate.
+// CTAs (or CTA pairs) pull work units from a dependency-ordered schedule
+// through a global atomic counter (a megakernel-style task queue: a dependent
+// task starts once the slice it reads is done, not when the whole producer op
+// is done).  Roles inside a CTA (224 threads):
+//   warp 6      : scheduler.  Claims the next unit just in time (when the TMA
+//                 warp is a few K-slices from the end of its current unit),
+//                 and for consumer units polls the producer tile semaphores with
+//                 all 32 lanes at once, publishing how many leading producer
+//                 tiles are complete in shared memory (acquire at gpu scope,
+//                 release at CTA scope).
+//   warp 0      : TMA producer (lane 0).  Before loading a K-slice of the
+//                 intermediate it checks the published readiness (shared
+//                 memory only) and fences the async proxy.
 //   warp 1      : TMEM allocator (whole warp) and tcgen05.mma issuer (lane 0).
 //   warps 2..5  : epilogue: tcgen05.ld of the fp32 accumulator, bias + GeLU /
 //                 SiLU*up / none, downcast, swizzled smem staging, TMA store,
 //                 then (producer stages) release-increment of the tile
 //                 semaphore and of the row counter.
-// Every wait is bounded: semaphore spins by the plan's timeout (error word +
+// CG = 2 (pair mode): a 2-CTA cluster shares one 256 x 256 tile.  Each CTA
+// loads its 128 rows of A and its half of B's columns; the leader (rank 0)
+// issues tcgen05.mma.cta_group::2, whose accumulator rows 0-127 land in the
+// leader's TMEM and rows 128-255 in the peer's; commits are multicast to both.
+// Semaphores stay per 128-row block, so each CTA of a consumer pair waits only
+// for the producer rows it reads.
+// Every wait is bounded: semaphore polls by the plan's timeout (error word +
 // global abort flag), mbarrier waits by a watchdog (error word + CTA abort).
 #pragma once
 #include <cuda_bf16.h>
@@ -22,15 +34,18 @@
 
 namespace cs {
 
-constexpr int BM = 128;           // tile rows (UMMA M)
+constexpr int BM = 128;           // tile rows per CTA (UMMA M per SM)
 constexpr int BK = 64;            // K-slice per pipeline stage (128 bytes of fp16/bf16)
 constexpr int UMMA_K = 16;        // K per tcgen05.mma (kind::f16)
 constexpr int TILE_A_BYTES = BM * BK * 2;  // 16 KB
-constexpr int STAGING_BYTES = 2 * BM * 128;  // two 64-column chunks of a 128x128 tile
-constexpr int UQ = 4;             // unit-queue depth (dispatcher -> MMA/epilogue)
-constexpr int NUM_THREADS = 192;
+constexpr int STAGING_BYTES = 2 * BM * 128;  // two 64-column chunk buffers of 128 rows
+constexpr int UQ = 4;             // unit-queue depth (scheduler -> TMA/MMA/epilogue)
+constexpr int NUM_THREADS = 224;
 constexpr int EPI_WARP0 = 2;
 constexpr int EPI_THREADS = 128;
+constexpr int SCHED_WARP = 6;
+constexpr int CLAIM_AHEAD = 12;   // K-slices before a unit's end at which the next unit is claimed
+constexpr uint32_t READY_ALL = 0x7FFFFFFFu;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t UNIT_END = 0xFFFFFFFFu;
 
@@ -55,7 +70,7 @@ enum : int { WAIT_NONE = 0, WAIT_TILE = 1, WAIT_ROW = 2, WAIT_STRIDED = 3 };
 struct StageP {
   int kind;        // STAGE_GEMM / STAGE_ATTN
   int epi;         // EPI_*
-  int m_tiles, n_tiles;
+  int m_tiles, n_tiles;  // n_tiles: column tiles; semaphores are [128-row blocks][n_tiles]
   int k_iters;     // BK-slices of the reduction
   int n_extent;    // valid output columns (bias guard, store guard)
   int m_extent;    // valid output rows (store guard)
@@ -63,21 +78,21 @@ struct StageP {
   int mma_n;       // UMMA N (bn, or 256 for gate|up with bn = 128)
   int b_major;     // 0: weights K-major ([N,K]); 1: MN-major ([K,N])
   int map_a, map_b, map_b2, map_out;
-  int b_bytes;     // bytes of the B operand per pipeline stage
+  int b_bytes;     // bytes of the B operand per pipeline stage and CTA
   const __nv_bfloat16* bias_bf16;  // exactly one of these two is used (per dtype)
   const __half* bias_f16;
   // consumer side
   int wait;        // WAIT_*
-  const uint32_t* dep_tile;  // producer tile semaphores [m_tiles][dep_ntiles]
-  const uint32_t* dep_row;   // producer row counters [m_tiles]
+  const uint32_t* dep_tile;  // producer tile semaphores [128-row blocks][dep_ntiles]
+  const uint32_t* dep_row;   // producer row counters [128-row blocks]
   int dep_ntiles;
   int dep_bn;      // intermediate columns per producer tile
   int stride;      // WAIT_STRIDED stride (producer column tiles)
   // producer side
   uint32_t* rel_tile;  // this stage's tile semaphores (null: no release)
   uint32_t* rel_row;
-  const uint32_t* delay_ns;  // per unit m*n_tiles+n, or null
-  int skip_unit;   // unit that skips its release (-1: none)
+  const uint32_t* delay_ns;  // per 128-row block x column tile, or null
+  int skip_unit;   // 128-row block x column tile that skips its release (-1: none)
   // attention (STAGE_ATTN)
   int heads;
   float softmax_scale_log2;  // log2(e) / sqrt(head_dim)
@@ -96,7 +111,26 @@ struct KParams {
   int release;     // producers release semaphores
   int bump_epoch;  // this launch completes a forward
   int acc_stride;  // TMEM columns between the two accumulator buffers
+  unsigned long long* trace;  // optional per-unit timestamps (TRACE_WORDS per record), or null
+  int trace_records;
 };
+
+// Trace record of one unit on one CTA (index = dispatch index * CTAs per tile + rank):
+//   [0] unit | dispatch index << 32   [1] smid | blockIdx << 16 | rank << 31
+//   [2] claimed   [3] dependencies published   [4] first TMA load   [5] last TMA load
+//   [6] accumulator complete (epilogue)   [7] epilogue done (stores + release)
+constexpr int TRACE_WORDS = 8;
+__device__ __forceinline__ uint32_t smid() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void trace_put(const KParams& p, uint32_t idx, uint32_t rank, int cg, int word,
+                                          unsigned long long v) {
+  if (p.trace == nullptr) return;
+  const uint32_t rec = idx * static_cast<uint32_t>(cg) + rank;
+  if (rec < static_cast<uint32_t>(p.trace_records)) p.trace[static_cast<size_t>(rec) * TRACE_WORDS + word] = v;
+}
 
 template <int NS>
 struct SmemCtl {
@@ -105,7 +139,12 @@ struct SmemCtl {
   uint64_t uq_full[UQ], uq_empty[UQ];
   uint64_t s_full, s_empty, p_full, o_full, o_empty;
   uint64_t drain;
+  uint64_t claim_req;       // TMA warp -> scheduler: claim the next unit now
+  uint64_t mb_full, mb_empty;  // pair mode: leader -> peer unit mailbox
   uint32_t uq[UQ];
+  uint32_t uq_idx[UQ];      // dispatch index of each queued unit (trace records)
+  uint32_t uq_ready[UQ];    // per queued unit: leading producer items known complete
+  uint32_t mb_unit;         // pair mode: dispatch index handed to the peer
   uint32_t tmem_base;
   volatile int abort;
   int issued_parity[NS];  // TMA thread: parity of the last load issued into each slot (-1: none)
@@ -122,38 +161,20 @@ __device__ __forceinline__ void record_error(const KParams& p, uint32_t code, ui
 }
 
 // Bounded mbarrier wait.  False when the CTA is aborting or the watchdog fired.
-template <int NS>
+// CLUSTER: acquire at cluster scope (the arrivals come from the peer CTA).
+template <int NS, bool CLUSTER = false>
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, SmemCtl<NS>* sc, const KParams& p,
                                          uint32_t where) {
-  if (mbar_try_wait(bar, parity)) return true;
+  auto try_once = [&]() { return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+  if (try_once()) return true;
   const uint64_t t0 = globaltimer();
   uint32_t it = 0;
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (try_once()) return true;
     if (sc->abort) return false;
     if ((++it & 63u) == 0u && globaltimer() - t0 > p.watchdog_ns) {
       record_error(p, ERR_WATCHDOG, 0xFFFFFFFFu, where);
       sc->abort = 1;
-      return false;
-    }
-  }
-}
-
-// Bounded acquire-spin until *ptr >= target (wrap-safe).  False on timeout or
-// global abort; the caller then proceeds without the data (the call's result is
-// void and cs_chain_status reports the error).
-__device__ __forceinline__ bool spin_geq(const uint32_t* ptr, uint32_t target, const KParams& p, uint32_t unit,
-                                         uint32_t where) {
-  if (static_cast<int32_t>(ld_acquire_gpu(ptr) - target) >= 0) return true;
-  const uint64_t t0 = globaltimer();
-  uint32_t ns = 32;
-  while (true) {
-    __nanosleep(ns);
-    if (ns < 256) ns <<= 1;
-    if (static_cast<int32_t>(ld_acquire_gpu(ptr) - target) >= 0) return true;
-    if (ld_relaxed_gpu(&p.ctrl[CTRL_ABORT]) != 0u) return false;
-    if (globaltimer() - t0 > p.timeout_ns) {
-      record_error(p, ERR_TIMEOUT, unit, where);
       return false;
     }
   }
@@ -174,64 +195,154 @@ struct RingPos {
   }
 };
 
-// Wait until producer tile column `t` of row block `m` may be read, under the
-// stage's policy.  `epoch1` = number of this forward (completed forwards + 1).
-__device__ __forceinline__ void wait_gemm_dep(const KParams& p, const StageP& S, int m, int t, uint32_t epoch1,
-                                              uint32_t unit, bool first) {
-  bool waited = false;
-  if (S.wait == WAIT_TILE) {
-    spin_geq(S.dep_tile + static_cast<size_t>(m) * S.dep_ntiles + t, epoch1, p, unit, static_cast<uint32_t>(t));
-    waited = true;
-  } else if (S.wait == WAIT_ROW) {
-    if (first) {
-      spin_geq(S.dep_row + m, epoch1 * static_cast<uint32_t>(S.dep_ntiles), p, unit, 0x10000u);
-      waited = true;
+// Scheduler warp: poll the producer flags a consumer unit depends on and
+// publish, in sc->uq_ready[q], how many leading dependency items are complete.
+// Items are producer column tiles 0..dep_ntiles-1 of 128-row block m, in the
+// order the consumer's K-loop reads them: TILE publishes the first incomplete
+// tile; ROW publishes 0 until the row counter is complete, then dep_ntiles;
+// STRIDED publishes the smallest residue class (mod stride) with an incomplete
+// tile.  Flags are read with relaxed loads (32 lanes in parallel) and each
+// observing lane fences (acquire pattern) before the CTA-scope release.
+template <int NS>
+__device__ void sched_poll_gemm(const KParams& p, const StageP& S, SmemCtl<NS>* sc, uint32_t q, int m,
+                                uint32_t epoch1, uint32_t unit, int lane) {
+  const uint32_t* tiles = S.dep_tile + static_cast<size_t>(m) * S.dep_ntiles;
+  const int nt = S.dep_ntiles;
+  int published = 0;
+  const uint64_t t0 = globaltimer();
+  uint32_t ns = 64;
+  while (true) {
+    int ready;
+    if (S.wait == WAIT_ROW) {
+      uint32_t v = lane == 0 ? ld_relaxed_gpu(S.dep_row + m) : 0u;
+      v = __shfl_sync(0xFFFFFFFFu, v, 0);
+      ready = static_cast<int32_t>(v - epoch1 * static_cast<uint32_t>(nt)) >= 0 ? nt : 0;
+    } else {
+      ready = nt;
+      for (int base = 0; base < nt; base += 32) {
+        const int t = base + lane;
+        const bool done = t >= nt || static_cast<int32_t>(ld_relaxed_gpu(tiles + t) - epoch1) >= 0;
+        const uint32_t bad = __ballot_sync(0xFFFFFFFFu, !done);
+        if (S.wait == WAIT_TILE) {
+          if (bad) {
+            ready = base + __ffs(bad) - 1;
+            break;
+          }
+        } else {  // STRIDED: residue class of each incomplete tile
+          int mn = done ? 0x7FFFFFFF : (t % S.stride);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) mn = min(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, o));
+          if (mn < ready) ready = mn;
+        }
+      }
     }
-  } else if (S.wait == WAIT_STRIDED) {
-    for (int tt = t % S.stride; tt < S.dep_ntiles; tt += S.stride)
-      spin_geq(S.dep_tile + static_cast<size_t>(m) * S.dep_ntiles + tt, epoch1, p, unit, static_cast<uint32_t>(tt));
-    waited = true;
+    if (ready > published) {
+      fence_acq_rel_gpu();
+      __syncwarp();
+      if (lane == 0) st_release_cta_shared(&sc->uq_ready[q], static_cast<uint32_t>(ready));
+      published = ready;
+    }
+    if (published >= nt) return;
+    bool give_up = false;
+    if (lane == 0) {
+      if (ld_relaxed_gpu(&p.ctrl[CTRL_ABORT]) != 0u) {
+        give_up = true;
+      } else if (globaltimer() - t0 > p.timeout_ns) {
+        record_error(p, ERR_TIMEOUT, unit, static_cast<uint32_t>(published));
+        give_up = true;
+      }
+    }
+    give_up = __shfl_sync(0xFFFFFFFFu, give_up ? 1 : 0, 0) != 0;
+    if (give_up) {
+      // the forward is void; let the pipeline drain without the data
+      if (lane == 0) st_release_cta_shared(&sc->uq_ready[q], READY_ALL);
+      return;
+    }
+    __nanosleep(ns);
+    if (ns < 512) ns <<= 1;
   }
-  // The intermediate was written through the async proxy (TMA store) on other
-  // SMs and will be read through the async proxy (TMA load) here.
-  if (waited) fence_proxy_async_global();
+}
+
+// TMA thread: wait until the scheduler has published at least `need` items
+// for queue slot q (shared memory only), then fence the async proxy so the
+// TMA loads that follow see the intermediate the producers stored.
+template <int NS>
+__device__ __forceinline__ bool tma_wait_ready(SmemCtl<NS>* sc, uint32_t q, int need, int& cached,
+                                               const KParams& p) {
+  if (cached >= need) return true;
+  const uint64_t t0 = globaltimer();
+  uint32_t it = 0;
+  while (true) {
+    const int v = static_cast<int>(ld_acquire_cta_shared(&sc->uq_ready[q]));
+    if (v >= need) {
+      cached = v;
+      fence_proxy_async_global();
+      return true;
+    }
+    if (sc->abort) return false;
+    if ((++it & 63u) == 0u && globaltimer() - t0 > p.watchdog_ns) {
+      record_error(p, ERR_WATCHDOG, 0xFFFFFFFFu, 8);
+      sc->abort = 1;
+      return false;
+    }
+    __nanosleep(32);
+  }
 }
 
 // ---------------------------------------------------------------- TMA role
-template <int NS, int STAGE_BYTES>
+template <int NS, int STAGE_BYTES, int CG>
 __device__ bool tma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, RingPos& rp, uint32_t unit,
-                              uint32_t epoch1) {
+                              uint32_t q, uint32_t rank) {
+  const uint32_t tidx = sc->uq_idx[q];
   const StageP& S = p.st[unit_stage(unit)];
   const int m = unit_m(unit), n = unit_n(unit);
   const uint32_t bytes = TILE_A_BYTES + S.b_bytes;
   const bool do_wait = p.waits && S.wait != WAIT_NONE;
-  int last_t = -1;
+  const int claim_at = S.k_iters > CLAIM_AHEAD ? S.k_iters - CLAIM_AHEAD : 0;
+  const int row0 = (m * CG + static_cast<int>(rank)) * BM;  // this CTA's A rows
+  const int bcols = S.bn / CG;                               // this CTA's share of B's columns
+  const int col0 = n * S.bn + static_cast<int>(rank) * bcols;
+  int ready = 0;
   for (int kb = 0; kb < S.k_iters; ++kb) {
-    if (do_wait) {
-      const int t = (kb * BK) / S.dep_bn;
-      if (t != last_t) {
-        wait_gemm_dep(p, S, m, t, epoch1, unit, last_t < 0);
-        last_t = t;
-      }
-    }
+    if (rank == 0 && kb == claim_at) mbar_arrive(&sc->claim_req);
+    if (do_wait && !tma_wait_ready(sc, q, (kb * BK) / S.dep_bn + 1, ready, p)) return false;
     if (!wait_bar(&sc->empty[rp.slot], rp.phase ^ 1u, sc, p, 1)) return false;
     uint8_t* sa = ring + rp.slot * STAGE_BYTES;
     uint8_t* sb = sa + TILE_A_BYTES;
-    uint64_t* bar = &sc->full[rp.slot];
-    mbar_arrive_expect_tx(bar, bytes);
-    tma_load_2d(sa, &p.maps[S.map_a], kb * BK, m * BM, bar);
-    // B operand(s): bn rows of N per operand; a second operand (the up
-    // projection of gate|up) follows the first, so one N = 2*bn MMA covers both.
+    // Completion goes to the leader's full barrier (each CTA of a pair adds its bytes).
+    uint32_t bar_addr;
+    if constexpr (CG == 1) {
+      bar_addr = smem_u32(&sc->full[rp.slot]);
+      mbar_arrive_expect_tx(&sc->full[rp.slot], bytes);
+    } else {
+      bar_addr = mapa_shared(&sc->full[rp.slot], 0);
+      if (rank == 0)
+        mbar_arrive_expect_tx(&sc->full[rp.slot], bytes);
+      else
+        mbar_expect_tx_remote(bar_addr, bytes);
+    }
+    auto load = [&](void* dst, const CUtensorMap* map, int x, int y) {
+      if constexpr (CG == 1)
+        tma_load_2d(dst, map, x, y, &sc->full[rp.slot]);
+      else
+        tma_load_2d_pair(dst, map, x, y, bar_addr);
+    };
+    if (kb == 0) trace_put(p, tidx, rank, CG, 4, globaltimer());
+    if (kb == S.k_iters - 1) trace_put(p, tidx, rank, CG, 5, globaltimer());
+    load(sa, &p.maps[S.map_a], kb * BK, row0);
+    // B operand(s): this CTA's bcols rows of N per operand; a second operand
+    // (the up projection of gate|up) follows the first, so one N = 2*bn MMA
+    // covers both.
     const int nops = S.map_b2 >= 0 ? 2 : 1;
     for (int op = 0; op < nops; ++op) {
       const CUtensorMap* bm = &p.maps[op == 0 ? S.map_b : S.map_b2];
-      uint8_t* dst = sb + op * S.bn * (BK * 2);
+      uint8_t* dst = sb + op * bcols * (BK * 2);
       if (S.b_major == 0) {
-        // weights [N, K]: boxes of 64 K x 128 N rows (16 KB), stacked along N
-        for (int h = 0; h < S.bn / 128; ++h) tma_load_2d(dst + h * 16384, bm, kb * BK, n * S.bn + h * 128, bar);
+        // weights [N, K]: one box of 64 K x bcols N rows
+        load(dst, bm, kb * BK, col0);
       } else {
         // weights [K, N]: boxes of 64 N (contiguous) x 64 K rows (8 KB), one per 64 columns
-        for (int h = 0; h < S.bn / 64; ++h) tma_load_2d(dst + h * 8192, bm, n * S.bn + h * 64, kb * BK, bar);
+        for (int h = 0; h < bcols / 64; ++h) load(dst + h * 8192, bm, col0 + h * 64, kb * BK);
       }
     }
     sc->issued_parity[rp.slot] = static_cast<int>(rp.phase);
@@ -241,11 +352,11 @@ __device__ bool tma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
 }
 
 // ---------------------------------------------------------------- MMA role
-template <int NS, int STAGE_BYTES>
+template <int NS, int STAGE_BYTES, int CG>
 __device__ bool mma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, RingPos& rp, uint32_t unit,
                               uint32_t& acc, uint32_t& acc_phase) {
   const StageP& S = p.st[unit_stage(unit)];
-  const uint32_t idesc = make_idesc_f16(p.bf16, S.b_major, BM, S.mma_n);
+  const uint32_t idesc = make_idesc_f16(p.bf16, S.b_major, BM * CG, S.mma_n);
   if (!wait_bar(&sc->tempty[acc], acc_phase ^ 1u, sc, p, 2)) return false;
   tc_fence_after();
   const uint32_t d = sc->tmem_base + acc * static_cast<uint32_t>(p.acc_stride);
@@ -262,24 +373,56 @@ __device__ bool mma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
     for (int kk = 0; kk < BK / UMMA_K; ++kk) {
       const uint64_t a = adesc + static_cast<uint64_t>(kk * 2);  // +32 bytes along K
       const uint64_t b = bdesc + static_cast<uint64_t>(S.b_major == 0 ? kk * 2 : kk * 128);  // +32 B / +16 rows
-      tc_mma_f16(d, a, b, idesc, (kb | kk) != 0 ? 1u : 0u);
+      tc_mma_f16<CG>(d, a, b, idesc, (kb | kk) != 0 ? 1u : 0u);
     }
-    tc_commit(&sc->empty[rp.slot]);
+    tc_commit<CG>(&sc->empty[rp.slot]);
     rp.next<NS>();
   }
-  tc_commit(&sc->tfull[acc]);
+  tc_commit<CG>(&sc->tfull[acc]);
   acc ^= 1u;
   if (acc == 0u) acc_phase ^= 1u;
   return true;
 }
 
 // ---------------------------------------------------------------- epilogue role
+// tanh-form GeLU: x/2 (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))), with the
+// hardware tanh approximation (its error is below the fp16/bf16 rounding of
+// the stored intermediate).
 __device__ __forceinline__ float gelu_tanh_f(float x) {
   const float k0 = 0.7978845608028654f;  // sqrt(2/pi)
   const float k1 = 0.044715f;
-  return 0.5f * x * (1.0f + tanhf(k0 * (x + k1 * x * x * x)));
+  const float u = k0 * x * fmaf(k1 * x, x, 1.0f);
+  const float hx = 0.5f * x;
+  return fmaf(hx, tanh_approx(u), hx);
 }
-__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
+// SiLU(x) = x * sigmoid(x) = x/2 (1 + tanh(x/2)).
+__device__ __forceinline__ float silu_f(float x) {
+  const float hx = 0.5f * x;
+  return fmaf(hx, tanh_approx(hx), hx);
+}
+
+// 64 bias values of columns [col0, col0 + 64) as floats (0 past the end);
+// the extent is a multiple of 8, so each 16-byte group is wholly in or out.
+__device__ __forceinline__ void load_bias64(const StageP& S, int col0, int bf16, float (&b)[64]) {
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    const int col = col0 + g * 8;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (col < S.n_extent)
+      v = ldg_nc_v4(bf16 ? static_cast<const void*>(S.bias_bf16 + col) : static_cast<const void*>(S.bias_f16 + col));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 f;
+      if (bf16)
+        f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+      else
+        f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+      b[g * 8 + 2 * i] = f.x;
+      b[g * 8 + 2 * i + 1] = f.y;
+    }
+  }
+}
 
 __device__ __forceinline__ uint32_t pack2(float a, float b, int bf16) {
   if (bf16) {
@@ -288,11 +431,6 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, int bf16) {
   }
   __half2 h = __floats2half2_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
-}
-
-__device__ __forceinline__ float load_bias(const StageP& S, int col, int bf16) {
-  if (col >= S.n_extent) return 0.0f;
-  return bf16 ? __bfloat162float(S.bias_bf16[col]) : __half2float(S.bias_f16[col]);
 }
 
 // Write one thread's 64 packed values (32 words) into the 128-byte-swizzled
@@ -311,17 +449,15 @@ __device__ __forceinline__ void stage_row(uint8_t* staging, int chunk, int row, 
 }
 
 // Producer release: all epilogue threads have their stores complete; one thread
-// publishes the tile (and its row) with gpu-scope release semantics.
-template <int NS>
-__device__ void release_tile(const KParams& p, const StageP& S, SmemCtl<NS>* sc, int m, int n, int lane) {
-  (void)sc;
+// publishes the 128-row block's tile (and its row) with gpu-scope release.
+__device__ void release_tile(const KParams& p, const StageP& S, int mb, int n, int lane) {
   if (lane == 0) {
     tma_store_wait_all<0>();
     fence_proxy_async_global();
   }
   named_bar_sync(1, EPI_THREADS);
   if (threadIdx.x == EPI_WARP0 * 32) {
-    const int u = m * S.n_tiles + n;
+    const int u = mb * S.n_tiles + n;
     if (S.delay_ns != nullptr) {
       const uint64_t d = S.delay_ns[u] > 10000000u ? 10000000u : S.delay_ns[u];
       if (d) {
@@ -332,22 +468,25 @@ __device__ void release_tile(const KParams& p, const StageP& S, SmemCtl<NS>* sc,
     if (p.release && S.rel_tile != nullptr && u != S.skip_unit) {
       __threadfence();
       red_release_gpu_add(S.rel_tile + u, 1u);
-      red_release_gpu_add(S.rel_row + m, 1u);
+      red_release_gpu_add(S.rel_row + mb, 1u);
     }
   }
 }
 
-template <int NS>
+template <int NS, int CG>
 __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* staging, uint32_t unit, uint32_t& acc,
-                              uint32_t& acc_phase, int& last_buf) {
+                              uint32_t& acc_phase, int& last_buf, uint32_t rank, uint32_t tidx) {
   const StageP& S = p.st[unit_stage(unit)];
-  const int m = unit_m(unit), n = unit_n(unit);
+  const int mb = unit_m(unit) * CG + static_cast<int>(rank);  // this CTA's 128-row block
+  const int n = unit_n(unit);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;  // TMEM lane quadrant this warp may access
   const int row = q * 32 + lane;
   if (!wait_bar(&sc->tfull[acc], acc_phase, sc, p, 4)) return false;
   tc_fence_after();
-  const uint32_t tbase = sc->tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * static_cast<uint32_t>(p.acc_stride);
+  if (threadIdx.x == EPI_WARP0 * 32) trace_put(p, tidx, rank, CG, 6, globaltimer());
+  const uint32_t tbase =
+      sc->tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * static_cast<uint32_t>(p.acc_stride);
   const int nchunks = S.bn / 64;
 #pragma unroll 1
   for (int c = 0; c < nchunks; ++c) {
@@ -361,24 +500,39 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
     }
     tc_wait_ld();
     if (c == nchunks - 1) {
+      // this warp is done with the accumulator buffer: hand it back to the MMA
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sc->tempty[acc]);
+      if (lane == 0) {
+        if constexpr (CG == 1)
+          mbar_arrive(&sc->tempty[acc]);
+        else
+          mbar_arrive_cluster(mapa_shared(&sc->tempty[acc], 0));
+      }
     }
     uint32_t w[32];
     const int col0 = n * S.bn + c * 64;
+    if (S.epi == EPI_BIAS_GELU) {
+      float bias[64];
+      load_bias64(S, col0, p.bf16, bias);
 #pragma unroll
-    for (int j = 0; j < 64; j += 2) {
-      float a = __uint_as_float(v[j >> 5][j & 31]);
-      float b = __uint_as_float(v[(j + 1) >> 5][(j + 1) & 31]);
-      if (S.epi == EPI_BIAS_GELU) {
-        a = gelu_tanh_f(a + load_bias(S, col0 + j, p.bf16));
-        b = gelu_tanh_f(b + load_bias(S, col0 + j + 1, p.bf16));
-      } else if (S.epi == EPI_SWIGLU) {
-        a = silu_f(a) * __uint_as_float(u[j >> 5][j & 31]);
-        b = silu_f(b) * __uint_as_float(u[(j + 1) >> 5][(j + 1) & 31]);
+      for (int j = 0; j < 64; j += 2) {
+        const float a = gelu_tanh_f(__uint_as_float(v[j >> 5][j & 31]) + bias[j]);
+        const float b = gelu_tanh_f(__uint_as_float(v[(j + 1) >> 5][(j + 1) & 31]) + bias[j + 1]);
+        w[j >> 1] = pack2(a, b, p.bf16);
       }
-      w[j >> 1] = pack2(a, b, p.bf16);
+    } else if (S.epi == EPI_SWIGLU) {
+#pragma unroll
+      for (int j = 0; j < 64; j += 2) {
+        const float a = silu_f(__uint_as_float(v[j >> 5][j & 31])) * __uint_as_float(u[j >> 5][j & 31]);
+        const float b =
+            silu_f(__uint_as_float(v[(j + 1) >> 5][(j + 1) & 31])) * __uint_as_float(u[(j + 1) >> 5][(j + 1) & 31]);
+        w[j >> 1] = pack2(a, b, p.bf16);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 64; j += 2)
+        w[j >> 1] = pack2(__uint_as_float(v[j >> 5][j & 31]), __uint_as_float(v[(j + 1) >> 5][(j + 1) & 31]), p.bf16);
     }
     // Two chunk buffers alternate.  Every earlier store that read this buffer
     // must be done: if the newest committed store read the other buffer, all
@@ -395,9 +549,10 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
     fence_proxy_async_shared();
     __syncwarp();
     // boxes that start past the tensor's end are skipped, not clipped
-    if (col0 < S.n_extent && m * BM + q * 32 < S.m_extent) {
+    const int grow = mb * BM + q * 32;
+    if (col0 < S.n_extent && grow < S.m_extent) {
       if (lane == 0) {
-        tma_store_2d(&p.maps[S.map_out], staging + buf * (BM * 128) + q * 32 * 128, col0, m * BM + q * 32);
+        tma_store_2d(&p.maps[S.map_out], staging + buf * (BM * 128) + q * 32 * 128, col0, grow);
         tma_store_commit();
       }
       last_buf = buf;
@@ -406,14 +561,28 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
   acc ^= 1u;
   if (acc == 0u) acc_phase ^= 1u;
   if (S.rel_tile != nullptr) {
-    release_tile(p, S, sc, m, n, lane);
+    release_tile(p, S, mb, n, lane);
     last_buf = -1;
   }
+  if (threadIdx.x == EPI_WARP0 * 32) trace_put(p, tidx, rank, CG, 7, globaltimer());
   return true;
 }
 
+// ---------------------------------------------------------------- scheduler role
+template <int NS>
+__device__ __forceinline__ void push_unit(SmemCtl<NS>* sc, uint32_t q, uint32_t unit, uint32_t idx, int lane,
+                                          bool consumer) {
+  if (lane == 0) {
+    sc->uq[q] = unit;
+    sc->uq_idx[q] = idx;
+    sc->uq_ready[q] = consumer ? 0u : READY_ALL;
+    mbar_arrive(&sc->uq_full[q]);
+  }
+  __syncwarp();
+}
+
 // ---------------------------------------------------------------- the kernel
-template <int NS, int STAGE_BYTES>
+template <int NS, int STAGE_BYTES, int CG>
 __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_constant__ KParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -422,21 +591,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
   SmemCtl<NS>* sc = reinterpret_cast<SmemCtl<NS>*>(staging + STAGING_BYTES);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = CG == 1 ? 0u : cluster_ctarank();
+  const bool leader = rank == 0;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
-      mbar_init(&sc->full[i], 1);
+      mbar_init(&sc->full[i], CG);  // one expect_tx arrival per CTA of the tile
       mbar_init(&sc->empty[i], 1);
       sc->issued_parity[i] = -1;
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sc->tfull[i], 1);
-      mbar_init(&sc->tempty[i], 4);
+      mbar_init(&sc->tempty[i], 4 * CG);  // every epilogue warp of the tile
     }
     for (int i = 0; i < UQ; ++i) {
       mbar_init(&sc->uq_full[i], 1);
-      mbar_init(&sc->uq_empty[i], 5);
+      mbar_init(&sc->uq_empty[i], 6);  // TMA + MMA + 4 epilogue warps
     }
+    mbar_init(&sc->claim_req, 1);
+    mbar_init(&sc->mb_full, 1);
+    mbar_init(&sc->mb_empty, 1);
     mbar_init(&sc->s_full, 1);
     mbar_init(&sc->s_empty, 4);
     mbar_init(&sc->p_full, 4);
@@ -448,51 +622,105 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
     for (int i = 0; i < 8; ++i) prefetch_tmap(&p.maps[i]);
   }
   if (warp == 1) {
-    tmem_alloc(&sc->tmem_base, TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc<CG>(&sc->tmem_base, TMEM_COLS);
+    tmem_relinquish<CG>();
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (CG == 2) cluster_sync();  // the peer's barriers exist before anyone arrives on them
   tc_fence_after();
 
   const uint32_t epoch1 = p.ctrl[CTRL_EPOCH] + 1u;
 
-  if (warp == 0) {
+  if (warp == SCHED_WARP) {
+    uint32_t q = 0, qphase = 0, req_phase = 0, mb_phase = 0;
+    bool first = true;
+    while (true) {
+      uint32_t idx = 0xFFFFFFFFu;  // dispatch index (>= n_units: no more work)
+      if (leader) {
+        // claim units in schedule order, one at a time, just in time
+        if (!first) {
+          if (!wait_bar(&sc->claim_req, req_phase, sc, p, 9)) break;
+          req_phase ^= 1u;
+        }
+        first = false;
+        if (lane == 0 && ld_relaxed_gpu(&p.ctrl[CTRL_ABORT]) == 0u) idx = atomicAdd(&p.ctrl[CTRL_DISPATCH], 1u);
+        idx = __shfl_sync(0xFFFFFFFFu, idx, 0);
+        if constexpr (CG == 2) {
+          // hand the dispatch index to the peer CTA of the pair
+          if (!wait_bar<NS, true>(&sc->mb_empty, mb_phase ^ 1u, sc, p, 10)) break;
+          if (lane == 0) {
+            st_cluster_u32(mapa_shared(&sc->mb_unit, 1), idx);
+            mbar_arrive_cluster(mapa_shared(&sc->mb_full, 1));
+          }
+          __syncwarp();
+          mb_phase ^= 1u;
+        }
+      } else {
+        if (!wait_bar<NS, true>(&sc->mb_full, mb_phase, sc, p, 11)) break;
+        idx = *reinterpret_cast<volatile uint32_t*>(&sc->mb_unit);
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(&sc->mb_empty, 0));
+        mb_phase ^= 1u;
+      }
+      const uint32_t unit = idx < static_cast<uint32_t>(p.n_units) ? p.sched[idx] : UNIT_END;
+      if (unit != UNIT_END && lane == 0) {
+        trace_put(p, idx, rank, CG, 0, unit | (static_cast<unsigned long long>(idx) << 32));
+        trace_put(p, idx, rank, CG, 1, smid() | (blockIdx.x << 16) | (rank << 31));
+        trace_put(p, idx, rank, CG, 2, globaltimer());
+      }
+      if (!wait_bar(&sc->uq_empty[q], qphase ^ 1u, sc, p, 5)) break;
+      const StageP& S = p.st[unit == UNIT_END ? 0 : unit_stage(unit)];
+      const bool consumer = unit != UNIT_END && p.waits && S.wait != WAIT_NONE;
+      push_unit(sc, q, unit, idx, lane, consumer);
+      if (unit == UNIT_END) break;
+      if (consumer && S.kind == STAGE_GEMM)
+        sched_poll_gemm<NS>(p, S, sc, q, unit_m(unit) * CG + static_cast<int>(rank), epoch1, unit, lane);
+      if (lane == 0) trace_put(p, idx, rank, CG, 3, globaltimer());
+      if (++q == UQ) {
+        q = 0;
+        qphase ^= 1u;
+      }
+    }
+  } else if (warp == 0) {
     if (lane == 0) {
       RingPos rp;
       uint32_t q = 0, qphase = 0;
       bool ok = true;
       while (ok) {
-        uint32_t unit = UNIT_END;
-        if (ld_relaxed_gpu(&p.ctrl[CTRL_ABORT]) == 0u) {
-          const uint32_t idx = atomicAdd(&p.ctrl[CTRL_DISPATCH], 1u);
-          if (idx < static_cast<uint32_t>(p.n_units)) unit = p.sched[idx];
-        }
-        if (!wait_bar(&sc->uq_empty[q], qphase ^ 1u, sc, p, 5)) break;
-        sc->uq[q] = unit;
-        mbar_arrive(&sc->uq_full[q]);
+        if (!wait_bar(&sc->uq_full[q], qphase, sc, p, 6)) break;
+        const uint32_t unit = sc->uq[q];
+        if (unit != UNIT_END && p.st[unit_stage(unit)].kind == STAGE_GEMM)
+          ok = tma_gemm_unit<NS, STAGE_BYTES, CG>(p, sc, ring, rp, unit, q, rank);
+        mbar_arrive(&sc->uq_empty[q]);
         if (++q == UQ) {
           q = 0;
           qphase ^= 1u;
         }
         if (unit == UNIT_END) break;
-        if (p.st[unit_stage(unit)].kind == STAGE_GEMM)
-          ok = tma_gemm_unit<NS, STAGE_BYTES>(p, sc, ring, rp, unit, epoch1);
       }
-      // let every load this thread issued land before the CTA can exit
-      for (int i = 0; i < NS; ++i)
-        if (sc->issued_parity[i] >= 0) {
-          const uint64_t t0 = globaltimer();
-          while (!mbar_try_wait(&sc->full[i], static_cast<uint32_t>(sc->issued_parity[i])) &&
-                 globaltimer() - t0 < p.watchdog_ns) {
+      // Let every load this thread issued land before the CTA can exit.  In
+      // pair mode the loads complete on the leader's barrier, which its MMA
+      // waits for; after an abort, give in-flight copies a bounded grace time.
+      if constexpr (CG == 1) {
+        for (int i = 0; i < NS; ++i)
+          if (sc->issued_parity[i] >= 0) {
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(&sc->full[i], static_cast<uint32_t>(sc->issued_parity[i])) &&
+                   globaltimer() - t0 < p.watchdog_ns) {
+            }
           }
-        }
+      } else if (!ok) {
+        const uint64_t t0 = globaltimer();
+        while (globaltimer() - t0 < 200000u) __nanosleep(1000);
+      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       RingPos rp;
       uint32_t q = 0, qphase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
+      bool issued = false;
       while (ok) {
         if (!wait_bar(&sc->uq_full[q], qphase, sc, p, 6)) break;
         const uint32_t unit = sc->uq[q];
@@ -502,13 +730,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
           qphase ^= 1u;
         }
         if (unit == UNIT_END) break;
-        if (p.st[unit_stage(unit)].kind == STAGE_GEMM)
-          ok = mma_gemm_unit<NS, STAGE_BYTES>(p, sc, ring, rp, unit, acc, acc_phase);
+        if (leader && p.st[unit_stage(unit)].kind == STAGE_GEMM) {
+          ok = mma_gemm_unit<NS, STAGE_BYTES, CG>(p, sc, ring, rp, unit, acc, acc_phase);
+          issued = true;
+        }
       }
       // every MMA this thread issued completes before TMEM is freed
-      tc_commit(&sc->drain);
-      const uint64_t t0 = globaltimer();
-      while (!mbar_try_wait(&sc->drain, 0) && globaltimer() - t0 < p.watchdog_ns) {
+      if (issued) {
+        if constexpr (CG == 1)
+          tc_commit<1>(&sc->drain);
+        else
+          tc_commit_local_pair(&sc->drain);
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(&sc->drain, 0) && globaltimer() - t0 < p.watchdog_ns) {
+        }
       }
     }
   } else {
@@ -518,6 +753,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
     while (ok) {
       if (!wait_bar(&sc->uq_full[q], qphase, sc, p, 7)) break;
       const uint32_t unit = sc->uq[q];
+      const uint32_t tidx = sc->uq_idx[q];
       __syncwarp();
       if (lane == 0) mbar_arrive(&sc->uq_empty[q]);
       if (++q == UQ) {
@@ -526,7 +762,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
       }
       if (unit == UNIT_END) break;
       if (p.st[unit_stage(unit)].kind == STAGE_GEMM)
-        ok = epi_gemm_unit<NS>(p, sc, staging, unit, acc, acc_phase, last_buf);
+        ok = epi_gemm_unit<NS, CG>(p, sc, staging, unit, acc, acc_phase, last_buf, rank, tidx);
     }
     if (lane == 0) tma_store_wait_all<0>();
     __syncwarp();
@@ -534,8 +770,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
 
   tc_fence_before();
   __syncthreads();
+  // no CTA of a pair leaves while its peer may still signal its barriers or
+  // read its shared memory through the pair MMA
+  if constexpr (CG == 2) cluster_sync();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(sc->tmem_base, TMEM_COLS);
+  if (warp == 1) tmem_dealloc<CG>(sc->tmem_base, TMEM_COLS);
 
   // Last CTA out re-arms the dispatch counter for the next launch on this
   // stream and, when this launch completes a forward, advances the epoch.

@@ -105,6 +105,9 @@ typedef struct cs_chain_desc {
                           weights in L2); 0 = auto                                  */
   int tile_n;          /* output columns per GEMM tile: 128 or 256; 0 = auto.
                           SwiGLU producer tiles are always 128 (gate|up = 256).     */
+  int tile_m;          /* rows per GEMM tile: 128 (one SM) or 256 (a 2-SM cluster
+                          sharing one tcgen05 MMA; needs tile_n = 256); 0 = auto.
+                          Semaphores stay per 128-row block either way.             */
   unsigned long long spin_timeout_ns; /* per-wait limit of a consumer tile; 0 = 2 s */
 } cs_chain_desc;
 
@@ -178,13 +181,15 @@ typedef struct cs_chain_info {
   int stages;              /* 2 (MLP) or 3 (ATTN) */
   int m_tiles;             /* ceil(M/128) */
   int n_tiles[3];          /* column tiles of each stage's output */
-  int units[3];            /* work units of each stage */
-  int n_units;             /* total units of a fused forward */
+  int units[3];            /* 128-row-block x column-tile units of each stage (semaphores) */
+  int n_units;             /* schedule entries of a fused forward */
   int num_sms;             /* persistent grid size */
   int smem_bytes;          /* dynamic shared memory per CTA */
   int lag;                 /* schedule lag actually used (groups) */
-  int group_m;             /* rasterisation group actually used (row blocks) */
+  int group_m;             /* rasterisation group actually used (tile rows) */
   int tile_n[3];           /* output columns per tile of each stage */
+  int tile_m;              /* rows per GEMM tile actually used (128 or 256) */
+  int sched_units[3];      /* schedule entries of each stage (tiles) */
   int stride;              /* strided-policy stride actually used */
   void* intermediate[2];   /* H (MLP) or QKV, O (ATTN): device pointers owned by the plan */
   size_t sem_words[2];     /* length of each boundary's tile-semaphore array */
@@ -193,8 +198,8 @@ typedef struct cs_chain_info {
 cs_status cs_chain_query(cs_chain_t plan, cs_chain_info* info);
 
 /* Host-only: the dispatch order a plan with this desc and grid size would use.
- * Each entry encodes one unit as (stage << 28) | (m_tile << 14) | n_tile; for an
- * ATTN stage n_tile is the head.  Row blocks are taken in groups of group_m; a
+ * Each entry encodes one unit as (stage << 28) | (m_tile << 14) | n_tile, m_tile
+ * counting tile_m-row tiles; for an ATTN stage n_tile is the head.  Row blocks are taken in groups of group_m; a
  * stage's units of one group are listed column-tile-major; at step t, stage s
  * lists group t - s*lag, so every producer a unit waits on is listed before it.  *n_out receives the count; entries beyond cap
  * are not written (cap may be 0 to query the count).  Needs no GPU. */
@@ -223,6 +228,17 @@ cs_status cs_chain_debug_skip_release(cs_chain_t plan, int stage, int unit);
  * 1: O) into caller device memory dst; bytes must not exceed the buffer's size
  * (M * F * 2 for H and O, M * 3F * 2 for QKV).  For stage-by-stage parity tests. */
 cs_status cs_chain_debug_copy_intermediate(cs_chain_t plan, int which, void* dst, size_t bytes);
+
+/* Per-unit timeline: enable = 1 allocates (cudaMalloc) and zeroes a trace buffer
+ * that every later forward of this plan overwrites; 0 frees it.  Each record is
+ * 8 uint64: [0] unit | dispatch index << 32, [1] SM id | CTA << 16 | pair rank << 31,
+ * then globaltimer ns at [2] claim, [3] dependencies published, [4] first and
+ * [5] last TMA load, [6] accumulator complete, [7] epilogue done (0 = not reached).
+ * Record r belongs to dispatch index r / (tile_m / 128). */
+cs_status cs_chain_debug_trace(cs_chain_t plan, int enable);
+
+/* Copy up to n records of the trace to host (8 uint64 each); *n_out = records. */
+cs_status cs_chain_debug_read_trace(cs_chain_t plan, uint64_t* host, size_t n, size_t* n_out);
 
 /* ABI version of the loaded library (CS_ABI_VERSION). */
 int cs_abi_version(void);

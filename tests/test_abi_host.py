@@ -76,14 +76,14 @@ def _deps(stage_kind, s, m, n, d, q):
     return [(s - 1, m, t) for t in range(ntp)]
 
 
-@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("tile_m,tile_n", [(128, 128), (128, 256), (256, 256)])
 @pytest.mark.parametrize("M,H,F,sms,lag,group", [(64, 256, 1024, 148, -1, 0), (2048, 12288, 6144, 148, -1, 0),
                                                  (2048, 12288, 6144, 152, 0, 3), (1, 12288, 6144, 148, -1, 0),
                                                  (1000, 8192, 2752, 148, 2, 1), (1536, 8192, 8192, 148, 5, 5)])
-def test_schedule_is_dependency_ordered(cs, M, H, F, sms, lag, group, tile_n):
-    d = cs.cs_chain_desc_init(M=M, H=H, F=F, lag=lag, group_m=group, tile_n=tile_n)
+def test_schedule_is_dependency_ordered(cs, M, H, F, sms, lag, group, tile_n, tile_m):
+    d = cs.cs_chain_desc_init(M=M, H=H, F=F, lag=lag, group_m=group, tile_n=tile_n, tile_m=tile_m)
     units = cs.cs_schedule_build(d, sms)
-    m_tiles = -(-M // 128)
+    m_tiles = -(-M // tile_m)
     n0, n1 = -(-F // tile_n), -(-H // tile_n)
     dec = [cs.decode_unit(u) for u in units]
     # every unit exactly once
@@ -104,8 +104,17 @@ def test_schedule_rasterises_column_major_within_a_group(cs):
     assert dec[192] == (0, 4, 0) and dec[384] == (1, 0, 0)
 
 
-def test_auto_tile_width(cs):
+def test_auto_tile_shape(cs):
     big = cs.cs_schedule_build(cs.cs_chain_desc_init(M=2048, H=12288, F=6144), 148)
+    mid = cs.cs_schedule_build(cs.cs_chain_desc_init(M=640, H=12288, F=6144), 148)
     small = cs.cs_schedule_build(cs.cs_chain_desc_init(M=256, H=12288, F=6144), 148)
-    assert len(big) == 16 * 24 + 16 * 48        # 256-wide tiles once the grid is filled twice
-    assert len(small) == 2 * 48 + 2 * 96        # 128-wide tiles otherwise
+    assert len(big) == 8 * 24 + 8 * 48      # 256 x 256 tiles on CTA pairs for large M
+    assert len(mid) == 5 * 24 + 5 * 48      # 128 x 256 tiles on single SMs in between
+    assert len(small) == 2 * 48 + 2 * 96    # 128 x 128 tiles for small M
+
+
+def test_pair_tiles_need_wide_gelu_tiles(cs):
+    d = cs.cs_chain_desc_init(M=512, H=512, F=512, tile_m=256, tile_n=128)
+    with pytest.raises(cs.CSError) as e:
+        cs.cs_schedule_build(d, 148)
+    assert e.value.status == cs.CS_ERR_UNSUPPORTED

@@ -51,28 +51,31 @@ def test_tiny_chain_golden_values():
     assert np.max(np.abs(got - ref)) <= TOL * np.max(np.abs(full_ref))
 
 
-@pytest.mark.parametrize("tile_n", [128, 256])
+TILES = [(128, 128), (128, 256), (256, 256)]  # (tile_m, tile_n); 256 rows = a 2-SM pair
+
+
+@pytest.mark.parametrize("tile_m,tile_n", TILES)
 @pytest.mark.parametrize("layout", ["kn", "nk"])
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
 @pytest.mark.parametrize("M,H,F", [(1, 256, 1024), (100, 320, 392), (200, 200, 136), (384, 512, 640),
-                                   (129, 1024, 2752)])
-def test_ragged_shapes(M, H, F, dtype, layout, tile_n):
+                                   (129, 1024, 2752), (700, 264, 520)])
+def test_ragged_shapes(M, H, F, dtype, layout, tile_m, tile_n):
     inp = cs_inputs.make_custom("gelu", M, H, F, dtype=dtype, seed=3)
     dev = device_tensors(inp, layout)
-    with plan_for(inp, "tile", layout, tile_n=tile_n) as plan:
+    with plan_for(inp, "tile", layout, tile_n=tile_n, tile_m=tile_m) as plan:
         Y = forward(plan, dev)
     Yref, _ = _oracle(inp)
     assert oracle.rel_err(Y.cpu(), Yref) <= TOL
 
 
-@pytest.mark.parametrize("tile_n", [128, 256])
-def test_policies_bit_identical_and_layouts_agree(tile_n):
+@pytest.mark.parametrize("tile_m,tile_n", TILES)
+def test_policies_bit_identical_and_layouts_agree(tile_m, tile_n):
     inp = cs_inputs.make_custom("gelu", 300, 768, 1536, seed=5)
     outs = {}
     for layout in ("kn", "nk"):
         dev = device_tensors(inp, layout)
         for pol in ("tile", "row", "strided", "stream"):
-            with plan_for(inp, pol, layout, tile_n=tile_n, group_m=2) as plan:
+            with plan_for(inp, pol, layout, tile_n=tile_n, tile_m=tile_m, group_m=1) as plan:
                 outs[(layout, pol)] = forward(plan, dev).cpu()
     Yref, _ = _oracle(inp)
     base = outs[("kn", "tile")]
@@ -81,11 +84,11 @@ def test_policies_bit_identical_and_layouts_agree(tile_n):
         assert torch.equal(v, base), f"{k} differs from kn/tile"
 
 
-@pytest.mark.parametrize("tile_n", [128, 256])
-def test_flags_end_at_expected_counts(tile_n):
+@pytest.mark.parametrize("tile_m,tile_n", TILES)
+def test_flags_end_at_expected_counts(tile_m, tile_n):
     inp = cs_inputs.make_custom("gelu", 520, 512, 1280, seed=6)
     dev = device_tensors(inp)
-    with plan_for(inp, "tile", tile_n=tile_n) as plan:
+    with plan_for(inp, "tile", tile_n=tile_n, tile_m=tile_m) as plan:
         q = cs.cs_chain_query(plan)
         Y = torch.empty_like(dev["X"])
         for e in range(1, 6):
@@ -107,13 +110,13 @@ def test_policies_and_control_keep_flags_consistent():
             assert epoch == 3 and all(v == 3 for r in tiles for v in r) and rows == [3 * 4] * 2
 
 
-@pytest.mark.parametrize("tile_n", [128, 256])
-def test_delay_injection_never_changes_a_bit(tile_n):
+@pytest.mark.parametrize("tile_m,tile_n", TILES)
+def test_delay_injection_never_changes_a_bit(tile_m, tile_n):
     inp = cs_inputs.make_custom("gelu", 640, 1024, 2048, seed=8)
     dev = device_tensors(inp)
     ref = None
     for pol in ("tile", "row", "strided"):
-        with plan_for(inp, pol, tile_n=tile_n, group_m=2) as plan:
+        with plan_for(inp, pol, tile_n=tile_n, tile_m=tile_m, group_m=1) as plan:
             q = cs.cs_chain_query(plan)
             for seed in range(3):
                 g = torch.Generator().manual_seed(100 + seed)
@@ -130,12 +133,13 @@ def test_delay_injection_never_changes_a_bit(tile_n):
             assert epoch == 3 and all(v == 3 for r in tiles for v in r)
 
 
-def test_missing_release_times_out_and_reset_recovers():
+@pytest.mark.parametrize("tile_m,tile_n", TILES)
+def test_missing_release_times_out_and_reset_recovers(tile_m, tile_n):
     inp = cs_inputs.make_custom("gelu", 256, 512, 512, seed=9)
     dev = device_tensors(inp)
-    with plan_for(inp, "tile", spin_timeout_ns=20_000_000) as plan:
+    with plan_for(inp, "tile", spin_timeout_ns=20_000_000, tile_m=tile_m, tile_n=tile_n) as plan:
         good = forward(plan, dev).cpu()
-        cs.cs_chain_debug_skip_release(plan, 0, 5)
+        cs.cs_chain_debug_skip_release(plan, 0, 1)
         Y = torch.empty_like(dev["X"])
         cs.cs_mlp_forward(plan, Y=Y, **dev)
         torch.cuda.synchronize()
@@ -151,10 +155,11 @@ def test_missing_release_times_out_and_reset_recovers():
         assert epoch == 1 and all(v == 1 for r in tiles for v in r)
 
 
-def test_forward_stage_matches_chain():
+@pytest.mark.parametrize("tile_m,tile_n", TILES)
+def test_forward_stage_matches_chain(tile_m, tile_n):
     inp = cs_inputs.make_custom("gelu", 300, 512, 1024, seed=10)
     dev = device_tensors(inp)
-    with plan_for(inp, "tile") as plan:
+    with plan_for(inp, "tile", tile_m=tile_m, tile_n=tile_n) as plan:
         Y = forward(plan, dev).clone()
         H = intermediate(plan, 0, inp.M, inp.F, inp.dtype).clone()
         Y2 = torch.zeros_like(Y)
