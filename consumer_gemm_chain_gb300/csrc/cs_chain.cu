@@ -7,6 +7,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
+#include <cmath>
 #include <cstring>
 #include <algorithm>
 #include <mutex>
@@ -170,7 +171,8 @@ cs_status validate(const cs_chain_desc* d) {
     if (d->head_dim != 128) return fail(CS_ERR_UNSUPPORTED, "head_dim=%d (only 128 is built)", d->head_dim);
     if (d->heads < 1 || d->heads * d->head_dim != d->F)
       return fail(CS_ERR_INVALID_ARG, "ATTN needs F == heads*head_dim (F=%d heads=%d)", d->F, d->heads);
-    return fail(CS_ERR_UNSUPPORTED, "the attention chain is not built yet");
+    if (d->tile_n == 256 || d->tile_m == 256)
+      return fail(CS_ERR_UNSUPPORTED, "the attention chain runs 128 x 128 tiles only");
   }
   return CS_OK;
 }
@@ -182,6 +184,8 @@ Geometry geometry(const cs_chain_desc* d, int num_sms) {
   // they pay off once the producer stage alone fills half of the grid.
   int tn = d->tile_n;
   if (tn == 0) tn = (2 * blocks * cdiv(d->F, 256) >= num_sms) ? 256 : 128;
+  // attention units keep S and O in TMEM next to the two 128-column accumulators
+  if (d->kind == CS_CHAIN_ATTN) tn = 128;
   // A 2-SM pair per 256 x 256 tile halves them again (each SM loads half of B).
   int tm = d->tile_m;
   if (tm == 0) tm = (tn == 256 && d->kind == CS_CHAIN_MLP_GELU && blocks >= 8) ? 256 : 128;
@@ -256,9 +260,9 @@ int device_sms(int* out) {
   return dev;
 }
 
-template <int NS, int SB, int CG>
+template <int NS, int SB, int CG, bool ATTN>
 cs_status set_smem_attr() {
-  static cudaError_t once = cudaFuncSetAttribute(cs::cs_chain_kernel<NS, SB, CG>,
+  static cudaError_t once = cudaFuncSetAttribute(cs::cs_chain_kernel<NS, SB, CG, ATTN>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes_for<NS, SB>());
   if (once != cudaSuccess) return fail(CS_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(once));
   return CS_OK;
@@ -315,6 +319,13 @@ cs_status encode_act(cs_chain_s* p, int slot, const void* ptr, int rows, int col
   return CS_OK;
 }
 
+int wait_kind(const cs_chain_s* p) {
+  return p->d.policy == CS_SYNC_TILE ? cs::WAIT_TILE
+         : p->d.policy == CS_SYNC_ROW ? cs::WAIT_ROW
+         : p->d.policy == CS_SYNC_STRIDED ? cs::WAIT_STRIDED
+                                          : cs::WAIT_NONE;
+}
+
 void fill_common(const cs_chain_s* p, cs::KParams& kp) {
   std::memcpy(kp.maps, p->maps, sizeof(kp.maps));
   kp.ctrl = p->ctrl;
@@ -328,10 +339,7 @@ void fill_common(const cs_chain_s* p, cs::KParams& kp) {
 void fill_mlp_stages(const cs_chain_s* p, const cs_mlp_args* a, cs::KParams& kp) {
   const bool swiglu = p->d.kind == CS_CHAIN_MLP_SWIGLU;
   const int b_major = p->d.weight_layout == CS_WEIGHTS_KN ? 1 : 0;
-  const int wait = p->d.policy == CS_SYNC_TILE ? cs::WAIT_TILE
-                   : p->d.policy == CS_SYNC_ROW ? cs::WAIT_ROW
-                   : p->d.policy == CS_SYNC_STRIDED ? cs::WAIT_STRIDED
-                                                    : cs::WAIT_NONE;
+  const int wait = wait_kind(p);
   cs::StageP& s0 = kp.st[0];
   std::memset(&s0, 0, sizeof(s0));
   s0.kind = cs::STAGE_GEMM;
@@ -410,17 +418,116 @@ cs_status launch(cs_chain_s* p, cs::KParams& kp, const uint32_t* sched, int n_un
   }
   cudaError_t e;
   cs_status s;
-  if (p->cg == 2) {
-    if ((s = set_smem_attr<NS_A, SB_A, 2>()) != CS_OK) return s;
-    e = cudaLaunchKernelEx(&cfg, cs::cs_chain_kernel<NS_A, SB_A, 2>, kp);
+  if (p->d.kind == CS_CHAIN_ATTN) {
+    if ((s = set_smem_attr<NS_A, SB_A, 1, true>()) != CS_OK) return s;
+    e = cudaLaunchKernelEx(&cfg, cs::cs_chain_kernel<NS_A, SB_A, 1, true>, kp);
+  } else if (p->cg == 2) {
+    if ((s = set_smem_attr<NS_A, SB_A, 2, false>()) != CS_OK) return s;
+    e = cudaLaunchKernelEx(&cfg, cs::cs_chain_kernel<NS_A, SB_A, 2, false>, kp);
   } else if (p->cfg_b) {
-    if ((s = set_smem_attr<NS_B, SB_B, 1>()) != CS_OK) return s;
-    e = cudaLaunchKernelEx(&cfg, cs::cs_chain_kernel<NS_B, SB_B, 1>, kp);
+    if ((s = set_smem_attr<NS_B, SB_B, 1, false>()) != CS_OK) return s;
+    e = cudaLaunchKernelEx(&cfg, cs::cs_chain_kernel<NS_B, SB_B, 1, false>, kp);
   } else {
-    if ((s = set_smem_attr<NS_A, SB_A, 1>()) != CS_OK) return s;
-    e = cudaLaunchKernelEx(&cfg, cs::cs_chain_kernel<NS_A, SB_A, 1>, kp);
+    if ((s = set_smem_attr<NS_A, SB_A, 1, false>()) != CS_OK) return s;
+    e = cudaLaunchKernelEx(&cfg, cs::cs_chain_kernel<NS_A, SB_A, 1, false>, kp);
   }
   if (e != cudaSuccess) return fail(CS_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
+  return CS_OK;
+}
+
+// Map indices (ATTN): 0 X, 1 Wqkv, 2 QKV store, 3 QKV load, 4 O store, 5 O load, 6 Wo, 7 Y store.
+enum { AMAP_X = 0, AMAP_WQKV = 1, AMAP_QKVST = 2, AMAP_QKVLD = 3, AMAP_OST = 4, AMAP_OLD = 5, AMAP_WO = 6, AMAP_Y = 7 };
+
+void fill_attn_stages(const cs_chain_s* p, cs::KParams& kp) {
+  const int b_major = p->d.weight_layout == CS_WEIGHTS_KN ? 1 : 0;
+  const int F = p->d.F, H = p->d.H, M = p->d.M;
+  uint32_t* rows0 = p->sems[0] + static_cast<size_t>(p->m_blocks) * p->n_tiles[0];
+  uint32_t* rows1 = p->sems[1] + static_cast<size_t>(p->m_blocks) * p->n_tiles[1];
+  // stage 0: QKV = X Wqkv
+  cs::StageP& s0 = kp.st[0];
+  std::memset(&s0, 0, sizeof(s0));
+  s0.kind = cs::STAGE_GEMM;
+  s0.epi = cs::EPI_NONE;
+  s0.m_tiles = p->m_units;
+  s0.n_tiles = p->n_tiles[0];
+  s0.k_iters = p->k_iters[0];
+  s0.n_extent = 3 * F;
+  s0.m_extent = M;
+  s0.bn = 128;
+  s0.mma_n = 128;
+  s0.b_major = b_major;
+  s0.map_a = AMAP_X;
+  s0.map_b = AMAP_WQKV;
+  s0.map_b2 = -1;
+  s0.map_out = AMAP_QKVST;
+  s0.b_bytes = 128 * cs::BK * 2;
+  s0.wait = cs::WAIT_NONE;
+  s0.rel_tile = p->sems[0];
+  s0.rel_row = rows0;
+  s0.delay_ns = p->delays[0];
+  s0.skip_unit = p->skip[0];
+  // stage 1: causal attention, one unit per (128-query block, head)
+  cs::StageP& s1 = kp.st[1];
+  std::memset(&s1, 0, sizeof(s1));
+  s1.kind = cs::STAGE_ATTN;
+  s1.m_tiles = p->m_units;
+  s1.n_tiles = p->n_tiles[1];
+  s1.n_extent = F;
+  s1.m_extent = M;
+  s1.bn = 128;
+  s1.map_a = AMAP_QKVLD;
+  s1.map_b = -1;
+  s1.map_b2 = -1;
+  s1.map_out = AMAP_OST;
+  s1.wait = wait_kind(p);
+  s1.dep_tile = p->sems[0];
+  s1.dep_row = rows0;
+  s1.dep_ntiles = p->n_tiles[0];
+  s1.dep_bn = 128;
+  s1.stride = p->stride;
+  s1.rel_tile = p->sems[1];
+  s1.rel_row = rows1;
+  s1.delay_ns = p->delays[1];
+  s1.skip_unit = p->skip[1];
+  s1.heads = p->d.heads;
+  s1.softmax_scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(p->d.head_dim)));
+  // stage 2: Y = O Wo
+  cs::StageP& s2 = kp.st[2];
+  std::memset(&s2, 0, sizeof(s2));
+  s2.kind = cs::STAGE_GEMM;
+  s2.epi = cs::EPI_NONE;
+  s2.m_tiles = p->m_units;
+  s2.n_tiles = p->n_tiles[2];
+  s2.k_iters = p->k_iters[2];
+  s2.n_extent = H;
+  s2.m_extent = M;
+  s2.bn = 128;
+  s2.mma_n = 128;
+  s2.b_major = b_major;
+  s2.map_a = AMAP_OLD;
+  s2.map_b = AMAP_WO;
+  s2.map_b2 = -1;
+  s2.map_out = AMAP_Y;
+  s2.b_bytes = 128 * cs::BK * 2;
+  s2.wait = wait_kind(p);
+  s2.dep_tile = p->sems[1];
+  s2.dep_row = rows1;
+  s2.dep_ntiles = p->n_tiles[1];
+  s2.dep_bn = 128;
+  s2.stride = p->stride;
+  s2.skip_unit = -1;
+  kp.acc_stride = 128;
+}
+
+cs_status bind_attn(cs_chain_s* p, const cs_attn_args* a) {
+  if (!a) return fail(CS_ERR_INVALID_ARG, "args is NULL");
+  if (!a->X || !a->Wqkv || !a->Wo || !a->Y) return fail(CS_ERR_INVALID_ARG, "X, Wqkv, Wo and Y are required");
+  const int M = p->d.M, H = p->d.H, F = p->d.F;
+  cs_status s;
+  if ((s = encode_act(p, AMAP_X, a->X, M, H, false)) != CS_OK) return s;
+  if ((s = encode_weight(p, AMAP_WQKV, a->Wqkv, H, 3 * F, 128)) != CS_OK) return s;
+  if ((s = encode_weight(p, AMAP_WO, a->Wo, F, H, 128)) != CS_OK) return s;
+  if ((s = encode_act(p, AMAP_Y, a->Y, M, H, true)) != CS_OK) return s;
   return CS_OK;
 }
 
@@ -522,9 +629,13 @@ cs_status cs_chain_plan(const cs_chain_desc* desc, cs_chain_t* out) {
   };
   const size_t esz = 2;
   // intermediate H [M, F]
-  p->inter_bytes[0] = static_cast<size_t>(desc->M) * desc->F * esz;
-  if (cudaMalloc(&p->inter[0], p->inter_bytes[0]) != cudaSuccess)
-    return bail(fail(CS_ERR_OOM, "cudaMalloc of the intermediate failed"));
+  const bool attn = desc->kind == CS_CHAIN_ATTN;
+  // intermediates: H [M, F] (MLP); QKV [M, 3F] and O [M, F] (attention)
+  p->inter_bytes[0] = static_cast<size_t>(desc->M) * (attn ? 3 : 1) * desc->F * esz;
+  p->inter_bytes[1] = attn ? static_cast<size_t>(desc->M) * desc->F * esz : 0;
+  for (int b = 0; b < 2; ++b)
+    if (p->inter_bytes[b] && cudaMalloc(&p->inter[b], p->inter_bytes[b]) != cudaSuccess)
+      return bail(fail(CS_ERR_OOM, "cudaMalloc of the intermediate failed"));
   for (int b = 0; b < g.stages - 1; ++b) {
     p->sem_words[b] = static_cast<size_t>(g.m_blocks) * g.n_tiles[b];
     const size_t words = p->sem_words[b] + g.m_blocks;
@@ -541,16 +652,33 @@ cs_status cs_chain_plan(const cs_chain_desc* desc, cs_chain_t* out) {
   for (int st = 0; st < g.stages; ++st)
     if ((s = upload(&p->sched_stage[st], build_stage(g, st))) != CS_OK) return bail(s);
   p->num_sms = p->num_sms / g.cg * g.cg;
-  // plan-owned intermediate maps
-  if ((s = encode_act(p, MAP_HST, p->inter[0], desc->M, desc->F, true)) != CS_OK) return bail(s);
-  p->slots[MAP_HST].ptr = nullptr;  // plan-owned: never re-encoded
-  if ((s = encode_act(p, MAP_HLD, p->inter[0], desc->M, desc->F, false)) != CS_OK) return bail(s);
-  p->slots[MAP_HLD].ptr = nullptr;
+  // plan-owned intermediate maps (never re-encoded)
+  int owned[4];
+  int n_owned = 0;
+  if (attn) {
+    if ((s = encode_act(p, AMAP_QKVST, p->inter[0], desc->M, 3 * desc->F, true)) != CS_OK) return bail(s);
+    if ((s = encode_act(p, AMAP_QKVLD, p->inter[0], desc->M, 3 * desc->F, false)) != CS_OK) return bail(s);
+    if ((s = encode_act(p, AMAP_OST, p->inter[1], desc->M, desc->F, true)) != CS_OK) return bail(s);
+    if ((s = encode_act(p, AMAP_OLD, p->inter[1], desc->M, desc->F, false)) != CS_OK) return bail(s);
+    owned[0] = AMAP_QKVST, owned[1] = AMAP_QKVLD, owned[2] = AMAP_OST, owned[3] = AMAP_OLD;
+    n_owned = 4;
+  } else {
+    if ((s = encode_act(p, MAP_HST, p->inter[0], desc->M, desc->F, true)) != CS_OK) return bail(s);
+    if ((s = encode_act(p, MAP_HLD, p->inter[0], desc->M, desc->F, false)) != CS_OK) return bail(s);
+    owned[0] = MAP_HST, owned[1] = MAP_HLD;
+    n_owned = 2;
+  }
+  bool is_owned[kMaxMaps] = {};
+  for (int i = 0; i < n_owned; ++i) {
+    is_owned[owned[i]] = true;
+    p->slots[owned[i]].ptr = nullptr;
+  }
   // unused map slots must still hold a well-formed descriptor for the prefetch
   for (int i = 0; i < kMaxMaps; ++i)
-    if (!p->slots[i].valid) std::memcpy(&p->maps[i], &p->maps[MAP_HLD], sizeof(CUtensorMap));
-  for (int i = 0; i < kMaxMaps; ++i)
-    if (i != MAP_HST && i != MAP_HLD) p->slots[i].valid = false;
+    if (!is_owned[i]) {
+      std::memcpy(&p->maps[i], &p->maps[owned[0]], sizeof(CUtensorMap));
+      p->slots[i].valid = false;
+    }
   *out = p;
   return CS_OK;
 }
@@ -589,24 +717,49 @@ cs_status cs_mlp_forward(cs_chain_t p, const cs_mlp_args* a, void* stream) {
 }
 
 cs_status cs_attn_chain_forward(cs_chain_t p, const cs_attn_args* a, void* stream) {
-  (void)a;
-  (void)stream;
   if (!p) return fail(CS_ERR_INVALID_ARG, "plan is NULL");
-  return fail(CS_ERR_UNSUPPORTED, "the attention chain is not built yet");
+  if (p->d.kind != CS_CHAIN_ATTN) return fail(CS_ERR_INVALID_ARG, "plan is not an attention chain");
+  if (p->error_latched) return fail(CS_ERR_NEEDS_RESET, "plan holds a device error; call cs_chain_reset");
+  cs_status s = bind_attn(p, a);
+  if (s != CS_OK) return s;
+  cs::KParams kp;
+  std::memset(&kp, 0, sizeof(kp));
+  fill_common(p, kp);
+  fill_attn_stages(p, kp);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (p->d.policy == CS_SYNC_STREAM) {
+    kp.waits = 0;
+    kp.release = 1;
+    for (int stg = 0; stg < 3; ++stg) {
+      kp.bump_epoch = stg == 2;
+      if ((s = launch(p, kp, p->sched_stage[stg], p->sched_units[stg], st)) != CS_OK) return s;
+    }
+    return CS_OK;
+  }
+  kp.waits = 1;
+  kp.release = 1;
+  kp.bump_epoch = 1;
+  return launch(p, kp, p->sched_fused, p->n_fused, st);
 }
 
 cs_status cs_chain_forward_stage(cs_chain_t p, const void* args, int stage, void* stream) {
   if (!p) return fail(CS_ERR_INVALID_ARG, "plan is NULL");
   if (p->error_latched) return fail(CS_ERR_NEEDS_RESET, "plan holds a device error; call cs_chain_reset");
   if (stage < 0 || stage >= p->stages) return fail(CS_ERR_INVALID_ARG, "stage %d out of range", stage);
-  if (p->d.kind == CS_CHAIN_ATTN) return fail(CS_ERR_UNSUPPORTED, "the attention chain is not built yet");
-  const cs_mlp_args* a = static_cast<const cs_mlp_args*>(args);
-  cs_status s = bind_mlp(p, a);
-  if (s != CS_OK) return s;
   cs::KParams kp;
   std::memset(&kp, 0, sizeof(kp));
-  fill_common(p, kp);
-  fill_mlp_stages(p, a, kp);
+  cs_status s;
+  if (p->d.kind == CS_CHAIN_ATTN) {
+    const cs_attn_args* a = static_cast<const cs_attn_args*>(args);
+    if ((s = bind_attn(p, a)) != CS_OK) return s;
+    fill_common(p, kp);
+    fill_attn_stages(p, kp);
+  } else {
+    const cs_mlp_args* a = static_cast<const cs_mlp_args*>(args);
+    if ((s = bind_mlp(p, a)) != CS_OK) return s;
+    fill_common(p, kp);
+    fill_mlp_stages(p, a, kp);
+  }
   kp.waits = 0;
   kp.release = 0;
   kp.bump_epoch = 0;

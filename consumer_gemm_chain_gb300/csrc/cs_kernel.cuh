@@ -568,6 +568,286 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
   return true;
 }
 
+// ---------------------------------------------------------------- attention unit
+// One unit = one 128-query block i of one head h (head_dim 128) of causal
+// attention over the QKV intermediate [M, 3F] (columns [Q | K | V], head-major).
+// For every key block j <= i (FlashAttention-style online softmax):
+//   S = Q_i K_j^T            tcgen05, fp32 in TMEM columns [ATT_S_COL, +128)
+//   P = exp2(S*c - m)         epilogue warps (one query row per thread), fp16/bf16
+//                             into the staging buffers as a K-major SW128 operand
+//   O_j = P V_j               tcgen05 (V is an MN-major B operand), TMEM [ATT_O_COL, +128)
+//   acc = acc*alpha + O_j     in registers, alpha = exp2(m_old - m_new)
+// then O = acc / l is stored like a GEMM tile and the (i, h) semaphore released.
+constexpr uint32_t ATT_S_COL = 256;
+constexpr uint32_t ATT_O_COL = 384;
+
+// TMA: three 32 KB slots per key block: [Q dims 0-63 | K_j dims 0-63],
+// [Q dims 64-127 | K_j dims 64-127], [V_j dims 0-63 | V_j dims 64-127] (128 rows each).
+template <int NS, int STAGE_BYTES>
+__device__ bool tma_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, RingPos& rp, uint32_t unit,
+                              uint32_t q) {
+  const StageP& S = p.st[unit_stage(unit)];
+  const uint32_t tidx = sc->uq_idx[q];
+  const int i = unit_m(unit), h = unit_n(unit);
+  const int F = S.heads * 128;
+  const int nslots = 3 * (i + 1);
+  const int claim_at = nslots > CLAIM_AHEAD ? nslots - CLAIM_AHEAD : 0;
+  int ready = 0;
+  // every key block 0..i (and the query block i) must be complete first
+  if (p.waits && S.wait != WAIT_NONE && !tma_wait_ready(sc, q, i + 1, ready, p)) return false;
+  const CUtensorMap* m = &p.maps[S.map_a];
+  int sidx = 0;
+  for (int j = 0; j <= i; ++j) {
+    for (int part = 0; part < 3; ++part, ++sidx) {
+      if (sidx == claim_at) mbar_arrive(&sc->claim_req);
+      if (!wait_bar(&sc->empty[rp.slot], rp.phase ^ 1u, sc, p, 1)) return false;
+      if (sidx == 0) trace_put(p, tidx, 0, 1, 4, globaltimer());
+      if (sidx == nslots - 1) trace_put(p, tidx, 0, 1, 5, globaltimer());
+      uint8_t* s0 = ring + rp.slot * STAGE_BYTES;
+      uint64_t* bar = &sc->full[rp.slot];
+      mbar_arrive_expect_tx(bar, 2 * TILE_A_BYTES);
+      if (part < 2) {
+        tma_load_2d(s0, m, h * 128 + part * 64, i * BM, bar);                   // Q_i dims chunk
+        tma_load_2d(s0 + TILE_A_BYTES, m, F + h * 128 + part * 64, j * BM, bar);  // K_j dims chunk
+      } else {
+        tma_load_2d(s0, m, 2 * F + h * 128, j * BM, bar);                       // V_j dims 0-63
+        tma_load_2d(s0 + TILE_A_BYTES, m, 2 * F + h * 128 + 64, j * BM, bar);    // V_j dims 64-127
+      }
+      sc->issued_parity[rp.slot] = static_cast<int>(rp.phase);
+      rp.next<NS>();
+    }
+  }
+  return true;
+}
+
+template <int NS, int STAGE_BYTES>
+__device__ bool mma_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, uint8_t* pbuf, RingPos& rp,
+                              uint32_t unit, uint32_t& p_phase) {
+  const int i = unit_m(unit);
+  const uint32_t idesc_s = make_idesc_f16(p.bf16, 0, BM, 128);  // Q K^T: both operands K-major
+  const uint32_t idesc_o = make_idesc_f16(p.bf16, 1, BM, 128);  // P V: V is MN-major
+  const uint32_t s_tm = sc->tmem_base + ATT_S_COL, o_tm = sc->tmem_base + ATT_O_COL;
+  const uint32_t pb = smem_u32(pbuf);
+  for (int j = 0; j <= i; ++j) {
+    for (int part = 0; part < 2; ++part) {
+      if (!wait_bar(&sc->full[rp.slot], rp.phase, sc, p, 3)) return false;
+      tc_fence_after();
+      const uint32_t sa = smem_u32(ring + rp.slot * STAGE_BYTES);
+      const uint64_t ad = smem_desc_sw128(sa, 16, 1024), bd = smem_desc_sw128(sa + TILE_A_BYTES, 16, 1024);
+#pragma unroll
+      for (int kk = 0; kk < BK / UMMA_K; ++kk)
+        tc_mma_f16<1>(s_tm, ad + static_cast<uint64_t>(kk * 2), bd + static_cast<uint64_t>(kk * 2), idesc_s,
+                      (part | kk) != 0 ? 1u : 0u);
+      tc_commit<1>(&sc->empty[rp.slot]);
+      rp.next<NS>();
+    }
+    tc_commit<1>(&sc->s_full);
+    // P_j is in shared memory and the previous O_j has been read back
+    if (!wait_bar(&sc->p_full, p_phase, sc, p, 12)) return false;
+    p_phase ^= 1u;
+    tc_fence_after();
+    if (!wait_bar(&sc->full[rp.slot], rp.phase, sc, p, 3)) return false;
+    tc_fence_after();
+    const uint32_t sv = smem_u32(ring + rp.slot * STAGE_BYTES);
+    const uint64_t vd = smem_desc_sw128(sv, TILE_A_BYTES, 1024);  // V: 64-dim atoms 16 KB apart, 8-key groups 1 KB apart
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      // P: chunk of 64 keys per 16 KB, +32 bytes per 16 keys; V: +16 key rows (2 KB)
+      const uint64_t a = smem_desc_sw128(pb + (kk >> 2) * (BM * 128), 16, 1024) + static_cast<uint64_t>((kk & 3) * 2);
+      tc_mma_f16<1>(o_tm, a, vd + static_cast<uint64_t>(kk * 128), idesc_o, kk != 0 ? 1u : 0u);
+    }
+    tc_commit<1>(&sc->empty[rp.slot]);
+    rp.next<NS>();
+    tc_commit<1>(&sc->o_full);
+  }
+  return true;
+}
+
+// Epilogue warps: online softmax for one query row per thread.
+template <int NS>
+__device__ bool epi_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* staging, uint32_t unit, uint32_t& s_phase,
+                              uint32_t& o_phase, int& last_buf, uint32_t tidx) {
+  const StageP& S = p.st[unit_stage(unit)];
+  const int i = unit_m(unit), h = unit_n(unit);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q = warp & 3;
+  const int r = q * 32 + lane;  // query row within the block
+  const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+  const uint32_t s_tm = sc->tmem_base + lane_base + ATT_S_COL;
+  const uint32_t o_tm = sc->tmem_base + lane_base + ATT_O_COL;
+  const float sl2 = S.softmax_scale_log2;
+  float acc[128];
+#pragma unroll
+  for (int t = 0; t < 128; ++t) acc[t] = 0.0f;
+  float m_run = -INFINITY, l_run = 0.0f, alpha_prev = 0.0f;
+  // the staging buffers double as the P operand: earlier stores must be done reading them
+  if (lane == 0) tma_store_wait_read<0>();
+  __syncwarp();
+  last_buf = -1;
+  for (int j = 0; j <= i; ++j) {
+    if (!wait_bar(&sc->s_full, s_phase, sc, p, 13)) return false;
+    s_phase ^= 1u;
+    tc_fence_after();
+    if (j == 0 && threadIdx.x == EPI_WARP0 * 32) trace_put(p, tidx, 0, 1, 6, globaltimer());
+    const bool diag = j == i;
+    // pass 1: row maximum of the scaled, masked logits
+    float mx = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t v[32];
+      tmem_ld32(s_tm + c * 32, v);
+      tc_wait_ld();
+#pragma unroll
+      for (int t = 0; t < 32; ++t) {
+        const float s = (diag && c * 32 + t > r) ? -INFINITY : __uint_as_float(v[t]) * sl2;
+        mx = fmaxf(mx, s);
+      }
+    }
+    const float m_new = fmaxf(m_run, mx);
+    const float alpha = exp2f(m_run - m_new);
+    if (j > 0) {
+      // fold O_{j-1} (computed against m_{j-1}) into the accumulator
+      if (!wait_bar(&sc->o_full, o_phase, sc, p, 14)) return false;
+      o_phase ^= 1u;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(o_tm + c * 32, v);
+        tc_wait_ld();
+#pragma unroll
+        for (int t = 0; t < 32; ++t) acc[c * 32 + t] = fmaf(acc[c * 32 + t], alpha_prev, __uint_as_float(v[t]));
+      }
+    }
+    // pass 2: P = exp2(s - m_new), row sum, write P_j as the A operand of P V
+    float lsum = 0.0f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t v[32];
+      tmem_ld32(s_tm + c * 32, v);
+      tc_wait_ld();
+      uint32_t w[16];
+#pragma unroll
+      for (int t = 0; t < 32; t += 2) {
+        const float p0 = (diag && c * 32 + t > r) ? 0.0f : exp2f(fmaf(__uint_as_float(v[t]), sl2, -m_new));
+        const float p1 = (diag && c * 32 + t + 1 > r) ? 0.0f : exp2f(fmaf(__uint_as_float(v[t + 1]), sl2, -m_new));
+        lsum += p0 + p1;
+        w[t >> 1] = pack2(p0, p1, p.bf16);
+      }
+      // keys c*32 .. c*32+31 live in 64-key chunk c/2, 16-byte pieces (c%2)*4 .. +3 of row r
+      uint8_t* rowp = staging + (c >> 1) * (BM * 128) + r * 128;
+#pragma unroll
+      for (int pc = 0; pc < 4; ++pc) {
+        const int piece = (c & 1) * 4 + pc;
+        const uint32_t addr = smem_u32(rowp + ((piece ^ (r & 7)) << 4));
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[pc * 4 + 0]),
+                     "r"(w[pc * 4 + 1]), "r"(w[pc * 4 + 2]), "r"(w[pc * 4 + 3])
+                     : "memory");
+      }
+    }
+    l_run = fmaf(l_run, alpha, lsum);
+    m_run = m_new;
+    alpha_prev = alpha;
+    fence_proxy_async_shared();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sc->p_full);
+  }
+  if (!wait_bar(&sc->o_full, o_phase, sc, p, 14)) return false;
+  o_phase ^= 1u;
+  tc_fence_after();
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t v[32];
+    tmem_ld32(o_tm + c * 32, v);
+    tc_wait_ld();
+#pragma unroll
+    for (int t = 0; t < 32; ++t) acc[c * 32 + t] = fmaf(acc[c * 32 + t], alpha_prev, __uint_as_float(v[t]));
+  }
+  tc_fence_before();
+  const float inv = 1.0f / l_run;
+  // O tile rows of this warp -> staging (the last P V has completed) -> TMA store
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    uint32_t w[32];
+#pragma unroll
+    for (int t = 0; t < 64; t += 2) w[t >> 1] = pack2(acc[c * 64 + t] * inv, acc[c * 64 + t + 1] * inv, p.bf16);
+    stage_row(staging, c, r, w);
+    fence_proxy_async_shared();
+    __syncwarp();
+    const int grow = i * BM + q * 32;
+    if (grow < S.m_extent) {
+      if (lane == 0) {
+        tma_store_2d(&p.maps[S.map_out], staging + c * (BM * 128) + q * 32 * 128, h * 128 + c * 64, grow);
+        tma_store_commit();
+      }
+      last_buf = c;
+    }
+  }
+  if (S.rel_tile != nullptr) {
+    release_tile(p, S, i, h, lane);
+    last_buf = -1;
+  }
+  if (threadIdx.x == EPI_WARP0 * 32) trace_put(p, tidx, 0, 1, 7, globaltimer());
+  return true;
+}
+
+// Scheduler poll for an attention unit: items are row blocks 0..i whose Q, K
+// and V tiles of head h (TILE / STRIDED) or whose whole row (ROW) are complete.
+template <int NS>
+__device__ void sched_poll_attn(const KParams& p, const StageP& S, SmemCtl<NS>* sc, uint32_t q, int i, int h,
+                                uint32_t epoch1, uint32_t unit, int lane) {
+  const int nt = S.dep_ntiles;
+  int published = 0;
+  const uint64_t t0 = globaltimer();
+  uint32_t ns = 64;
+  while (true) {
+    int ready = i + 1;
+    for (int base = 0; base <= i; base += 32) {
+      const int j = base + lane;
+      bool done = true;
+      if (j <= i) {
+        if (S.wait == WAIT_ROW) {
+          done = static_cast<int32_t>(ld_relaxed_gpu(S.dep_row + j) - epoch1 * static_cast<uint32_t>(nt)) >= 0;
+        } else {
+#pragma unroll
+          for (int part = 0; part < 3; ++part)
+            done = done && static_cast<int32_t>(ld_relaxed_gpu(S.dep_tile + static_cast<size_t>(j) * nt + h +
+                                                               part * S.heads) - epoch1) >= 0;
+        }
+      }
+      const uint32_t bad = __ballot_sync(0xFFFFFFFFu, !done);
+      if (bad) {
+        ready = base + __ffs(bad) - 1;
+        break;
+      }
+    }
+    if (ready > published) {
+      fence_acq_rel_gpu();
+      __syncwarp();
+      if (lane == 0) st_release_cta_shared(&sc->uq_ready[q], static_cast<uint32_t>(ready));
+      published = ready;
+    }
+    if (published >= i + 1) return;
+    bool give_up = false;
+    if (lane == 0) {
+      if (ld_relaxed_gpu(&p.ctrl[CTRL_ABORT]) != 0u) {
+        give_up = true;
+      } else if (globaltimer() - t0 > p.timeout_ns) {
+        record_error(p, ERR_TIMEOUT, unit, static_cast<uint32_t>(published));
+        give_up = true;
+      }
+    }
+    give_up = __shfl_sync(0xFFFFFFFFu, give_up ? 1 : 0, 0) != 0;
+    if (give_up) {
+      if (lane == 0) st_release_cta_shared(&sc->uq_ready[q], READY_ALL);
+      return;
+    }
+    __nanosleep(ns);
+    if (ns < 512) ns <<= 1;
+  }
+}
+
 // ---------------------------------------------------------------- scheduler role
 template <int NS>
 __device__ __forceinline__ void push_unit(SmemCtl<NS>* sc, uint32_t q, uint32_t unit, uint32_t idx, int lane,
@@ -582,7 +862,9 @@ __device__ __forceinline__ void push_unit(SmemCtl<NS>* sc, uint32_t q, uint32_t 
 }
 
 // ---------------------------------------------------------------- the kernel
-template <int NS, int STAGE_BYTES, int CG>
+// ATTN: the instantiation also runs attention units (the attention chain);
+// the MLP instantiations leave that code out and keep their registers.
+template <int NS, int STAGE_BYTES, int CG, bool ATTN>
 __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_constant__ KParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -676,6 +958,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
       if (unit == UNIT_END) break;
       if (consumer && S.kind == STAGE_GEMM)
         sched_poll_gemm<NS>(p, S, sc, q, unit_m(unit) * CG + static_cast<int>(rank), epoch1, unit, lane);
+      else if constexpr (ATTN)
+        if (consumer && S.kind == STAGE_ATTN)
+          sched_poll_attn<NS>(p, S, sc, q, unit_m(unit), unit_n(unit), epoch1, unit, lane);
       if (lane == 0) trace_put(p, idx, rank, CG, 3, globaltimer());
       if (++q == UQ) {
         q = 0;
@@ -692,6 +977,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
         const uint32_t unit = sc->uq[q];
         if (unit != UNIT_END && p.st[unit_stage(unit)].kind == STAGE_GEMM)
           ok = tma_gemm_unit<NS, STAGE_BYTES, CG>(p, sc, ring, rp, unit, q, rank);
+        else if constexpr (CG == 1 && ATTN)
+          if (unit != UNIT_END) ok = tma_attn_unit<NS, STAGE_BYTES>(p, sc, ring, rp, unit, q);
         mbar_arrive(&sc->uq_empty[q]);
         if (++q == UQ) {
           q = 0;
@@ -718,7 +1005,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
   } else if (warp == 1) {
     if (lane == 0) {
       RingPos rp;
-      uint32_t q = 0, qphase = 0, acc = 0, acc_phase = 0;
+      uint32_t q = 0, qphase = 0, acc = 0, acc_phase = 0, p_phase = 0;
       bool ok = true;
       bool issued = false;
       while (ok) {
@@ -732,6 +1019,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
         if (unit == UNIT_END) break;
         if (leader && p.st[unit_stage(unit)].kind == STAGE_GEMM) {
           ok = mma_gemm_unit<NS, STAGE_BYTES, CG>(p, sc, ring, rp, unit, acc, acc_phase);
+          issued = true;
+        } else if constexpr (CG == 1 && ATTN) {
+          ok = mma_attn_unit<NS, STAGE_BYTES>(p, sc, ring, staging, rp, unit, p_phase);
           issued = true;
         }
       }
@@ -747,7 +1037,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
       }
     }
   } else {
-    uint32_t q = 0, qphase = 0, acc = 0, acc_phase = 0;
+    uint32_t q = 0, qphase = 0, acc = 0, acc_phase = 0, s_phase = 0, o_phase = 0;
     int last_buf = -1;  // staging buffer read by this warp's newest committed store
     bool ok = true;
     while (ok) {
@@ -763,6 +1053,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
       if (unit == UNIT_END) break;
       if (p.st[unit_stage(unit)].kind == STAGE_GEMM)
         ok = epi_gemm_unit<NS, CG>(p, sc, staging, unit, acc, acc_phase, last_buf, rank, tidx);
+      else if constexpr (CG == 1 && ATTN)
+        ok = epi_attn_unit<NS>(p, sc, staging, unit, s_phase, o_phase, last_buf, tidx);
     }
     if (lane == 0) tma_store_wait_all<0>();
     __syncwarp();

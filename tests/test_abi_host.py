@@ -95,6 +95,36 @@ def test_schedule_is_dependency_ordered(cs, M, H, F, sms, lag, group, tile_n, ti
             assert pos[dep] < i, f"unit {(s, m, n)} at {i} precedes its producer {dep}"
 
 
+@pytest.mark.parametrize("M,lag,group", [(1, -1, 0), (300, -1, 0), (2048, -1, 0), (2048, 2, 3), (1000, 0, 1)])
+def test_attention_schedule_is_dependency_ordered(cs, M, lag, group):
+    d = cs.cs_chain_desc_init(kind="attn", M=M, H=12288, F=1536, heads=12, head_dim=128, lag=lag, group_m=group)
+    dec = [cs.decode_unit(u) for u in cs.cs_schedule_build(d, 148)]
+    m_tiles = -(-M // 128)
+    nt = [36, 12, 96]
+    expect = {(s, m, n) for s in range(3) for m in range(m_tiles) for n in range(nt[s])}
+    assert len(dec) == len(expect) and set(dec) == expect
+    pos = {u: i for i, u in enumerate(dec)}
+    for (s, m, n), i in pos.items():
+        deps = []
+        if s == 1:   # causal: key blocks 0..m of head n (Q, K and V tiles)
+            deps = [(0, j, t) for j in range(m + 1) for t in (n, n + 12, n + 24)]
+        elif s == 2:  # every head of the same row block
+            deps = [(1, m, h) for h in range(12)]
+        for dep in deps:
+            assert pos[dep] < i, (s, m, n, dep)
+
+
+def test_attention_desc_validation(cs):
+    d = cs.cs_chain_desc_init(kind="attn", M=64, H=256, F=256, heads=2, head_dim=64)
+    with pytest.raises(cs.CSError) as e:
+        cs.cs_schedule_build(d, 148)
+    assert e.value.status == cs.CS_ERR_UNSUPPORTED
+    d = cs.cs_chain_desc_init(kind="attn", M=64, H=256, F=384, heads=2, head_dim=128)
+    with pytest.raises(cs.CSError) as e:
+        cs.cs_schedule_build(d, 148)
+    assert e.value.status == cs.CS_ERR_INVALID_ARG
+
+
 def test_schedule_rasterises_column_major_within_a_group(cs):
     d = cs.cs_chain_desc_init(M=2048, H=12288, F=6144, group_m=4, lag=1, tile_n=128)
     dec = [cs.decode_unit(u) for u in cs.cs_schedule_build(d, 148)]

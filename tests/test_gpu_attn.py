@@ -1,0 +1,100 @@
+"""GPU parity of the attention chain (QKV GEMM -> causal attention -> Wo GEMM)
+against the fp64 oracle, through the C ABI.
+
+Stage by stage: the QKV intermediate, the attention output O and Y are each
+compared with the oracle; outputs of every sync policy agree bit for bit, and
+the semaphores of both boundaries end at their expected counts."""
+from __future__ import annotations
+
+import pytest
+import torch
+
+import cs_inputs
+import oracle
+from tests.gpu_util import TOL, device_tensors, forward, intermediate, plan_for
+
+pytestmark = pytest.mark.gpu
+
+cs = pytest.importorskip("consumer_gemm_chain_gb300")
+
+
+def _oracle(inp):
+    return oracle.attention_chain(inp.X, inp.Wqkv, inp.Wo, heads=inp.F // 128, head_dim=128, return_parts=True)
+
+
+@pytest.mark.parametrize("layout", ["nk", "kn"])
+@pytest.mark.parametrize("M,H,heads", [(1, 256, 1), (100, 256, 2), (128, 512, 1), (300, 384, 3), (513, 256, 2)])
+def test_attention_chain_parity(M, H, heads, layout):
+    inp = cs_inputs.make_custom("attn", M, H, heads * 128, seed=31)
+    dev = device_tensors(inp, layout)
+    with plan_for(inp, "row", layout) as plan:
+        Y = forward(plan, dev)
+        QKV = intermediate(plan, 0, M, 3 * inp.F, inp.dtype)
+        O = intermediate(plan, 1, M, inp.F, inp.dtype)
+    Yref, QKVref, Oref = _oracle(inp)
+    assert oracle.rel_err(QKV.cpu(), QKVref) <= TOL
+    assert oracle.rel_err(O.cpu(), Oref) <= TOL
+    assert oracle.rel_err(Y.cpu(), Yref) <= TOL
+
+
+def test_attention_policies_bit_identical_and_flags():
+    inp = cs_inputs.make_custom("attn", 520, 512, 256, seed=32)
+    dev = device_tensors(inp, "nk")
+    outs = {}
+    for pol in ("tile", "row", "strided", "stream"):
+        with plan_for(inp, pol, "nk", group_m=1) as plan:
+            for _ in range(2):
+                outs[pol] = forward(plan, dev).cpu()
+            q = cs.cs_chain_query(plan)
+            for b in (0, 1):
+                tiles, rows, epoch = cs.cs_chain_debug_read_sems(plan, b)
+                assert epoch == 2
+                assert all(v == 2 for r in tiles for v in r)
+                assert rows == [2 * q["n_tiles"][b]] * q["m_tiles"]
+    Yref, _, _ = _oracle(inp)
+    assert oracle.rel_err(outs["row"], Yref) <= TOL
+    for k, v in outs.items():
+        assert torch.equal(v, outs["row"]), k
+
+
+def test_attention_delay_injection_never_changes_a_bit():
+    inp = cs_inputs.make_custom("attn", 400, 512, 384, seed=33)
+    dev = device_tensors(inp, "nk")
+    ref = None
+    for pol in ("row", "tile"):
+        with plan_for(inp, pol, "nk", group_m=1) as plan:
+            q = cs.cs_chain_query(plan)
+            for seed in range(2):
+                g = torch.Generator().manual_seed(200 + seed)
+                for stage in (0, 1):
+                    d = (torch.rand(q["units"][stage], generator=g) * 200_000).to(torch.int64).tolist()
+                    cs.cs_chain_debug_set_delays(plan, stage, d)
+                Y = forward(plan, dev).cpu()
+                if ref is None:
+                    ref = Y
+                assert torch.equal(Y, ref), (pol, seed)
+
+
+def test_attention_missing_release_times_out():
+    inp = cs_inputs.make_custom("attn", 256, 256, 256, seed=34)
+    dev = device_tensors(inp, "nk")
+    with plan_for(inp, "tile", "nk", spin_timeout_ns=20_000_000) as plan:
+        good = forward(plan, dev).cpu()
+        cs.cs_chain_debug_skip_release(plan, 1, 0)  # attention unit (block 0, head 0)
+        Y = torch.empty_like(dev["X"])
+        cs.cs_attn_chain_forward(plan, dev["X"], dev["Wqkv"], dev["Wo"], Y)
+        torch.cuda.synchronize()
+        assert cs.cs_chain_status(plan) == cs.CS_ERR_TIMEOUT
+        cs.cs_chain_debug_skip_release(plan, 1, -1)
+        cs.cs_chain_reset(plan)
+        assert torch.equal(forward(plan, dev).cpu(), good)
+
+
+@pytest.mark.parametrize("M", (1, 64, 512, 2048))
+def test_gpt3_attention_shard(M):
+    inp = cs_inputs.make_inputs("attn", M=M, seed=0)
+    dev = device_tensors(inp, "nk")
+    with plan_for(inp, "row", "nk") as plan:
+        Y = forward(plan, dev).cpu()
+    Yref, _, _ = _oracle(inp)
+    assert oracle.rel_err(Y, Yref) <= TOL
