@@ -27,6 +27,8 @@ from .chain import (  # noqa: F401
     cs_chain_status,
     cs_last_error_string,
     cs_mlp_forward,
+    cs_mlp_forward_noalloc,
+    cs_noalloc_status,
     cs_schedule_build,
     decode_unit,
 )

@@ -37,6 +37,7 @@ EXPORTED = (
     "cs_chain_forward_stage", "cs_chain_status", "cs_chain_reset", "cs_last_error_string", "cs_chain_query",
     "cs_schedule_build", "cs_chain_debug_read_sems", "cs_chain_debug_set_delays", "cs_chain_debug_skip_release",
     "cs_chain_debug_copy_intermediate", "cs_chain_debug_trace", "cs_chain_debug_read_trace", "cs_abi_version",
+    "cs_mlp_forward_noalloc", "cs_noalloc_status",
 )
 
 
@@ -91,6 +92,8 @@ def _load() -> ctypes.CDLL:
         "cs_chain_debug_trace": (I, [V, I]),
         "cs_chain_debug_read_trace": (I, [V, ctypes.POINTER(ctypes.c_uint64), S, ctypes.POINTER(S)]),
         "cs_abi_version": (I, []),
+        "cs_mlp_forward_noalloc": (I, [ctypes.POINTER(cs_chain_desc), ctypes.POINTER(cs_mlp_args), V]),
+        "cs_noalloc_status": (I, []),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -346,3 +349,27 @@ def cs_chain_debug_read_trace(plan: Plan) -> list[list[int]]:
     _check(_lib.cs_chain_debug_read_trace(plan.handle, buf, n.value, ctypes.byref(n)), "cs_chain_debug_read_trace")
     vals = list(buf)
     return [vals[i * 8:(i + 1) * 8] for i in range(n.value)]
+
+
+class _DescOnly:
+    """Shape holder for the argument checks of calls that take a desc, not a plan."""
+
+    def __init__(self, desc: cs_chain_desc):
+        self.desc = desc
+
+
+def cs_mlp_forward_noalloc(desc: cs_chain_desc, X, W1=None, b1=None, W2=None, Y=None, Wg=None, Wu=None,
+                           stream=None) -> None:
+    """The MLP chain without a plan and without any device allocation: for callers
+    that may not call cudaMalloc (inside another framework's memory pool, or in
+    loops where an allocation's implicit device synchronisation is not allowed).
+    Scratch is a fixed 32 MiB array inside the library; calls that overlap on
+    the GPU race.  See include/cs_chain.h."""
+    a = _mlp_args(_DescOnly(desc), X, W1, b1, W2, Y, Wg, Wu)
+    _check(_lib.cs_mlp_forward_noalloc(ctypes.byref(desc), ctypes.byref(a), _stream_ptr(stream)),
+           "cs_mlp_forward_noalloc")
+
+
+def cs_noalloc_status() -> int:
+    """Device status of the last allocation-free forward on the current device (after a sync)."""
+    return _lib.cs_noalloc_status()

@@ -884,3 +884,145 @@ cs_status cs_chain_debug_read_trace(cs_chain_t p, uint64_t* host, size_t n, size
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- allocation-free forward
+// Scratch of cs_mlp_forward_noalloc: one array per device that loads the
+// library.  In host code `g_noalloc_scratch` names a host-side stand-in, not
+// device memory, so its device address is looked up per device below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[CS_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+unsigned char* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of this device's scratch array (looked up once per device,
+// with that device current).
+cs_status noalloc_scratch(int dev, unsigned char** out) {
+  if (dev < 0 || dev >= kMaxDevices) return fail(CS_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess || ptr == nullptr)
+      return fail(CS_ERR_CUDA, "cudaGetSymbolAddress of the scratch array: %s", cudaGetErrorString(e));
+    g_noalloc_ptr[dev] = static_cast<unsigned char*>(ptr);
+  }
+  *out = g_noalloc_ptr[dev];
+  return CS_OK;
+}
+
+size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
+
+extern "C" {
+
+cs_status cs_mlp_forward_noalloc(const cs_chain_desc* desc, const cs_mlp_args* args, void* stream) {
+  cs_status s = validate(desc);
+  if (s != CS_OK) return s;
+  if (desc->kind == CS_CHAIN_ATTN) return fail(CS_ERR_UNSUPPORTED, "the allocation-free forward runs MLP chains only");
+  int sms = 0;
+  const int dev = device_sms(&sms);
+  if (dev < 0) return fail(CS_ERR_CUDA, "no CUDA device available");
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major * 10 + minor != 103)
+    return fail(CS_ERR_UNSUPPORTED, "device is sm_%d%d; this library is built for sm_103a only", major, minor);
+
+  // A plan on the host stack whose buffers all point into the scratch array.
+  cs_chain_s p;
+  p.d = *desc;
+  p.device = dev;
+  p.num_sms = desc->num_sms > 0 && desc->num_sms < sms ? desc->num_sms : sms;
+  Geometry g = geometry(desc, p.num_sms);
+  p.m_tiles = g.m_blocks;
+  p.m_units = g.m_tiles;
+  p.m_blocks = g.m_blocks;
+  p.cg = g.cg;
+  p.stages = g.stages;
+  for (int i = 0; i < 3; ++i) {
+    p.n_tiles[i] = g.n_tiles[i];
+    p.k_iters[i] = g.k_iters[i];
+    p.units[i] = g.m_blocks * g.n_tiles[i];
+    p.sched_units[i] = g.m_tiles * g.n_tiles[i];
+    p.bn[i] = g.bn[i];
+  }
+  p.lag = g.lag;
+  p.group_m = g.group_m;
+  p.stride = g.stride;
+  p.cfg_b = g.cg == 1 && (desc->kind == CS_CHAIN_MLP_SWIGLU || g.bn[0] == 256 || g.bn[1] == 256);
+  p.smem = p.cfg_b ? smem_bytes_for<NS_B, SB_B>() : smem_bytes_for<NS_A, SB_A>();
+  p.num_sms = p.num_sms / g.cg * g.cg;
+  const std::vector<uint32_t> fused = build_fused(g);
+  const std::vector<uint32_t> st0 = build_stage(g, 0), st1 = build_stage(g, 1);
+  p.n_fused = static_cast<int>(fused.size());
+
+  // Carve the array: control block and semaphores (cleared every call), then
+  // the schedules, then the intermediate H [M, F].
+  p.sem_words[0] = static_cast<size_t>(g.m_blocks) * g.n_tiles[0];
+  const size_t zero_words = cs::CTRL_WORDS + p.sem_words[0] + g.m_blocks;
+  const size_t sched_words = fused.size() + st0.size() + st1.size();
+  const size_t h_off = align256((zero_words + sched_words) * 4);
+  p.inter_bytes[0] = static_cast<size_t>(desc->M) * desc->F * 2;
+  const size_t need = h_off + p.inter_bytes[0];
+  if (need > CS_NOALLOC_SCRATCH_BYTES)
+    return fail(CS_ERR_INVALID_ARG,
+                "M=%d F=%d needs %zu bytes of scratch; the allocation-free forward has %u (use cs_chain_plan)",
+                desc->M, desc->F, need, CS_NOALLOC_SCRATCH_BYTES);
+  unsigned char* base = nullptr;
+  if ((s = noalloc_scratch(dev, &base)) != CS_OK) return s;
+  uint32_t* words = reinterpret_cast<uint32_t*>(base);
+  p.ctrl = words;
+  p.sems[0] = words + cs::CTRL_WORDS;
+  p.sched_fused = words + zero_words;
+  p.sched_stage[0] = p.sched_fused + fused.size();
+  p.sched_stage[1] = p.sched_stage[0] + st0.size();
+  p.inter[0] = base + h_off;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  CS_CUDA(cudaMemsetAsync(words, 0, zero_words * 4, st));
+  CS_CUDA(cudaMemcpyAsync(p.sched_fused, fused.data(), fused.size() * 4, cudaMemcpyHostToDevice, st));
+  CS_CUDA(cudaMemcpyAsync(p.sched_stage[0], st0.data(), st0.size() * 4, cudaMemcpyHostToDevice, st));
+  CS_CUDA(cudaMemcpyAsync(p.sched_stage[1], st1.data(), st1.size() * 4, cudaMemcpyHostToDevice, st));
+
+  // Tensor maps of the intermediate (in the array) and of the caller's tensors.
+  if ((s = encode_act(&p, MAP_HST, p.inter[0], desc->M, desc->F, true)) != CS_OK) return s;
+  if ((s = encode_act(&p, MAP_HLD, p.inter[0], desc->M, desc->F, false)) != CS_OK) return s;
+  for (int i = 0; i < kMaxMaps; ++i)
+    if (i != MAP_HST && i != MAP_HLD) std::memcpy(&p.maps[i], &p.maps[MAP_HLD], sizeof(CUtensorMap));
+  if ((s = bind_mlp(&p, args)) != CS_OK) return s;
+
+  cs::KParams kp;
+  std::memset(&kp, 0, sizeof(kp));
+  fill_common(&p, kp);
+  fill_mlp_stages(&p, args, kp);
+  kp.release = 1;
+  if (desc->policy == CS_SYNC_STREAM) {
+    kp.waits = 0;
+    kp.bump_epoch = 0;
+    if ((s = launch(&p, kp, p.sched_stage[0], p.sched_units[0], st)) != CS_OK) return s;
+    kp.bump_epoch = 1;
+    return launch(&p, kp, p.sched_stage[1], p.sched_units[1], st);
+  }
+  kp.waits = 1;
+  kp.bump_epoch = 1;
+  return launch(&p, kp, p.sched_fused, p.n_fused, st);
+}
+
+cs_status cs_noalloc_status(void) {
+  int dev = 0;
+  CS_CUDA(cudaGetDevice(&dev));
+  unsigned char* base = nullptr;
+  cs_status s = noalloc_scratch(dev, &base);
+  if (s != CS_OK) return s;
+  uint32_t w[cs::CTRL_WORDS];
+  CS_CUDA(cudaMemcpy(w, base, sizeof(w), cudaMemcpyDeviceToHost));
+  if (w[cs::CTRL_ERROR] == 0) return CS_OK;
+  return fail(static_cast<cs_status>(w[cs::CTRL_ERROR]), "device error %u: unit 0x%08x where 0x%x cta %u",
+              w[cs::CTRL_ERROR], w[cs::CTRL_ERR_UNIT], w[cs::CTRL_ERR_WHERE], w[cs::CTRL_ERR_CTA]);
+}
+
+}  // extern "C"

@@ -229,6 +229,37 @@ cs_status cs_chain_debug_skip_release(cs_chain_t plan, int stage, int unit);
  * (M * F * 2 for H and O, M * 3F * 2 for QKV).  For stage-by-stage parity tests. */
 cs_status cs_chain_debug_copy_intermediate(cs_chain_t plan, int which, void* dst, size_t bytes);
 
+/* Allocation-free MLP forward.  The pages have no counterpart to this call.
+ *
+ * Some callers may not allocate device memory: code running inside another
+ * framework whose caching allocator owns the GPU's memory budget (a raw
+ * cudaMalloc there can fail or fragment that pool), and latency-critical loops
+ * where cudaMalloc/cudaFree would implicitly synchronise the device.  For them,
+ * this call runs the same fused MLP chain as cs_chain_plan + cs_mlp_forward
+ * without making a plan: the intermediate H, the semaphores, the control block
+ * and the schedule live in one statically sized device array of
+ * CS_NOALLOC_SCRATCH_BYTES (32 MiB) inside this library, which every GPU that
+ * loads the library holds until the process exits.  It calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *
+ * desc: as for cs_chain_plan (kind MLP_GELU or MLP_SWIGLU).  args and stream: as
+ * for cs_mlp_forward; the caller still owns and passes X, the weights, b1 and Y.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Each call clears the semaphores and counters it needs, so results
+ * never depend on an earlier call, but the array is shared by every call on the
+ * device: calls that overlap on the GPU (other streams, other threads) race
+ * and must not be issued.  A shape whose intermediate, semaphores and schedule
+ * need more than the array holds is rejected with CS_ERR_INVALID_ARG before any
+ * work is enqueued (M * F * 2 bytes must stay well below 32 MiB).  Device-side
+ * errors: read them with cs_noalloc_status() after synchronising. */
+#define CS_NOALLOC_SCRATCH_BYTES (32u << 20)
+cs_status cs_mlp_forward_noalloc(const cs_chain_desc* desc, const cs_mlp_args* args, void* stream);
+
+/* Device error word of the last cs_mlp_forward_noalloc call on the current
+ * device (blocking read): CS_OK, CS_ERR_TIMEOUT or CS_ERR_WATCHDOG. */
+cs_status cs_noalloc_status(void);
+
 /* Per-unit timeline: enable = 1 allocates (cudaMalloc) and zeroes a trace buffer
  * that every later forward of this plan overwrites; 0 frees it.  Each record is
  * 8 uint64: [0] unit | dispatch index << 32, [1] SM id | CTA << 16 | pair rank << 31,

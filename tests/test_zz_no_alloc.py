@@ -1,0 +1,66 @@
+"""The allocation-free forward, through the C ABI, against the planned forward.
+
+cs_mlp_forward_noalloc exists for callers that may not allocate device memory
+themselves: code that runs inside another framework whose caching allocator
+owns the GPU memory budget, or a latency-critical loop where cudaMalloc and
+cudaFree would synchronise the device.  It keeps its intermediate, semaphores
+and schedule in a fixed array inside the library instead of a plan.  Each test
+runs it twice in a row (the array keeps the previous call's contents, which the
+second call must not depend on) and compares Y with cs_chain_plan +
+cs_mlp_forward within the parity tolerance the other GPU tests use.  This file
+runs last, and also passes on its own in a fresh process.
+"""
+from __future__ import annotations
+
+import pytest
+import torch
+
+import cs_inputs
+import oracle
+from tests.gpu_util import TOL, device_tensors, forward, plan_for
+
+pytestmark = pytest.mark.gpu
+
+cs = pytest.importorskip("consumer_gemm_chain_gb300")
+
+
+def _desc(inp, layout, policy):
+    return cs.cs_chain_desc_init(kind=inp.kind, M=inp.M, H=inp.H, F=inp.F, dtype=inp.dtype, policy=policy,
+                                 weight_layout=layout)
+
+
+@pytest.mark.parametrize("kind,M,H,F,layout,policy", [
+    ("gelu", 300, 512, 1024, "nk", "tile"),
+    ("gelu", 129, 256, 392, "kn", "row"),
+    ("swiglu", 200, 512, 688, "nk", "tile"),
+    ("gelu", 64, 256, 1024, "nk", "stream"),
+])
+def test_noalloc_matches_planned_forward_twice(kind, M, H, F, layout, policy):
+    inp = cs_inputs.make_custom(kind, M, H, F, dtype=torch.float16, seed=41)
+    dev = device_tensors(inp, layout)
+    with plan_for(inp, policy, layout) as plan:
+        ref = forward(plan, dev).cpu()
+    desc = _desc(inp, layout, policy)
+    for call in range(2):
+        Y = torch.full_like(dev["X"], float("nan"))
+        cs.cs_mlp_forward_noalloc(desc, Y=Y, **dev)
+        torch.cuda.synchronize()
+        assert cs.cs_noalloc_status() == cs.CS_OK, cs.cs_last_error_string()
+        Yc = Y.cpu()
+        assert not torch.isnan(Yc).any(), call
+        assert oracle.rel_err(Yc, ref) <= TOL, call
+
+
+def test_noalloc_rejects_shapes_beyond_its_scratch():
+    # M * F * 2 bytes alone exceed the fixed scratch array: refused before any launch
+    desc = cs.cs_chain_desc_init(kind="gelu", M=4096, H=256, F=8192, dtype=torch.float16)
+    X = torch.zeros(4096, 256, dtype=torch.float16, device="cuda")
+    W1 = torch.zeros(8192, 256, dtype=torch.float16, device="cuda")
+    b1 = torch.zeros(8192, dtype=torch.float16, device="cuda")
+    W2 = torch.zeros(256, 8192, dtype=torch.float16, device="cuda")
+    desc.weight_layout = cs.CS_WEIGHTS_NK
+    Y = torch.zeros_like(X)
+    with pytest.raises(cs.CSError) as e:
+        cs.cs_mlp_forward_noalloc(desc, X, W1=W1, b1=b1, W2=W2, Y=Y)
+    assert e.value.status == cs.CS_ERR_INVALID_ARG
+    assert "scratch" in str(e.value)
