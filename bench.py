@@ -42,6 +42,29 @@ def load_peaks():
     return dict(PEAKS_FALLBACK), "fallback"
 
 
+def kernel_sha():
+    """sha256[:16] of the kernel sources; DRAM-traffic counters are reported only
+    while the sources still match the ones they were taken with."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("cs_kernel.cuh", "cs_ptx.cuh", "cs_chain.cu"):
+        with open(os.path.join(ROOT, "consumer_gemm_chain_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(key):
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_sha") != kernel_sha():
+        return None
+    return d.get(key)
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -372,7 +395,8 @@ def main():
     else:
         gbs = nbytes / (ms_launch * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak}
-    roof.update({"traffic": None, "peak_source": f"{peak_src} ({'sustained' if sustained else 'burst'})",
+    traffic_key = f"{args.workload}_M{M}_{args.policy}_{lay}"
+    roof.update({"traffic": measured_traffic(traffic_key), "peak_source": f"{peak_src} ({'sustained' if sustained else 'burst'})",
                  "kernel": ("cs_chain_kernel<6,32768,2>" if plan_info["tile_m"] == 256 else
                             "cs_chain_kernel<4,49152,1>" if (kind == "swiglu" or 256 in plan_info["tile_n"])
                             else "cs_chain_kernel<6,32768,1>"),
