@@ -46,7 +46,8 @@ class cs_chain_desc(ctypes.Structure):
                 ("dtype", ctypes.c_int), ("policy", ctypes.c_int), ("weight_layout", ctypes.c_int),
                 ("stride", ctypes.c_int), ("heads", ctypes.c_int), ("head_dim", ctypes.c_int),
                 ("num_sms", ctypes.c_int), ("lag", ctypes.c_int), ("group_m", ctypes.c_int),
-                ("tile_n", ctypes.c_int), ("tile_m", ctypes.c_int), ("spin_timeout_ns", ctypes.c_ulonglong)]
+                ("tile_n", ctypes.c_int), ("tile_m", ctypes.c_int), ("split_k", ctypes.c_int),
+                ("spin_timeout_ns", ctypes.c_ulonglong)]
 
 
 class cs_mlp_args(ctypes.Structure):
@@ -63,6 +64,7 @@ class cs_chain_info(ctypes.Structure):
                 ("units", ctypes.c_int * 3), ("n_units", ctypes.c_int), ("num_sms", ctypes.c_int),
                 ("smem_bytes", ctypes.c_int), ("lag", ctypes.c_int), ("group_m", ctypes.c_int),
                 ("tile_n", ctypes.c_int * 3), ("tile_m", ctypes.c_int), ("sched_units", ctypes.c_int * 3),
+                ("split_k", ctypes.c_int * 3),
                 ("stride", ctypes.c_int),
                 ("intermediate", ctypes.c_void_p * 2), ("sem_words", ctypes.c_size_t * 2)]
 
@@ -284,7 +286,7 @@ def cs_chain_query(plan: Plan) -> dict:
     return {"stages": i.stages, "m_tiles": i.m_tiles, "n_tiles": list(i.n_tiles), "units": list(i.units),
             "n_units": i.n_units, "num_sms": i.num_sms, "smem_bytes": i.smem_bytes, "lag": i.lag,
             "group_m": i.group_m, "tile_n": list(i.tile_n), "tile_m": i.tile_m,
-            "sched_units": list(i.sched_units),
+            "sched_units": list(i.sched_units), "split_k": list(i.split_k),
             "stride": i.stride, "intermediate": [i.intermediate[0], i.intermediate[1]],
             "sem_words": [i.sem_words[0], i.sem_words[1]]}
 
@@ -297,9 +299,9 @@ def cs_schedule_build(desc: cs_chain_desc, num_sms: int) -> list[int]:
     return list(buf[: n.value])
 
 
-def decode_unit(u: int) -> tuple[int, int, int]:
-    """(stage, m_tile, n_tile) of a schedule entry."""
-    return u >> 28, (u >> 14) & 0x3FFF, u & 0x3FFF
+def decode_unit(u: int) -> tuple[int, int, int, int]:
+    """(stage, m_tile, n_tile, k_split) of a schedule entry."""
+    return u >> 30, (u >> 14) & 0xFFF, u & 0x3FFF, (u >> 26) & 0xF
 
 
 def cs_chain_debug_read_sems(plan: Plan, boundary: int):

@@ -74,6 +74,10 @@ struct cs_chain_s {
   int m_units = 0;   // tile rows of the schedule
   int m_blocks = 0;  // 128-row blocks (semaphore rows)
   int sched_units[3] = {0, 0, 0};
+  int splits[3] = {1, 1, 1};
+  int kps[3] = {0, 0, 0};
+  float* partial[3] = {nullptr, nullptr, nullptr};   // split-K fp32 partial tiles
+  uint32_t* split_ctr[3] = {nullptr, nullptr, nullptr};  // split-K arrivals per tile
   int smem = 0;
   // device memory owned by the plan
   void* inter[2] = {nullptr, nullptr};
@@ -132,8 +136,9 @@ cs_status encode_2d(CUtensorMap* map, const void* ptr, int bf16, uint64_t inner,
 
 inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 
-inline uint32_t enc_unit(int s, int m, int n) {
-  return (static_cast<uint32_t>(s) << 28) | (static_cast<uint32_t>(m) << 14) | static_cast<uint32_t>(n);
+inline uint32_t enc_unit(int s, int m, int n, int ks) {
+  return (static_cast<uint32_t>(s) << 30) | (static_cast<uint32_t>(ks) << 26) | (static_cast<uint32_t>(m) << 14) |
+         static_cast<uint32_t>(n);
 }
 
 // Geometry shared by the host-only schedule builder and the plan.
@@ -144,6 +149,8 @@ struct Geometry {
   int n_tiles[3] = {0, 0, 0};
   int k_iters[3] = {0, 0, 0};
   int bn[3] = {128, 128, 128};
+  int splits[3] = {1, 1, 1};
+  int kps[3] = {0, 0, 0};  // K-slices per split
   int lag = 1, group_m = 1, stride = 1;
 };
 
@@ -154,7 +161,8 @@ cs_status validate(const cs_chain_desc* d) {
   if (d->policy < CS_SYNC_TILE || d->policy > CS_SYNC_STREAM) return fail(CS_ERR_INVALID_ARG, "bad policy %d", d->policy);
   if (d->weight_layout != CS_WEIGHTS_KN && d->weight_layout != CS_WEIGHTS_NK)
     return fail(CS_ERR_INVALID_ARG, "bad weight_layout %d", d->weight_layout);
-  if (d->M < 1 || d->M > 128 * 16383) return fail(CS_ERR_INVALID_ARG, "M=%d out of range [1, %d]", d->M, 128 * 16383);
+  if (d->M < 1 || d->M > 128 * 4095) return fail(CS_ERR_INVALID_ARG, "M=%d out of range [1, %d]", d->M, 128 * 4095);
+  if (d->split_k < 0 || d->split_k > 15) return fail(CS_ERR_INVALID_ARG, "split_k=%d (0..15)", d->split_k);
   if (d->H < 8 || d->H % 8 != 0 || d->H > (1 << 20)) return fail(CS_ERR_INVALID_ARG, "H=%d must be a positive multiple of 8", d->H);
   if (d->F < 8 || d->F % 8 != 0 || d->F > (1 << 20)) return fail(CS_ERR_INVALID_ARG, "F=%d must be a positive multiple of 8", d->F);
   if (d->stride < 0) return fail(CS_ERR_INVALID_ARG, "stride=%d", d->stride);
@@ -212,6 +220,20 @@ Geometry geometry(const cs_chain_desc* d, int num_sms) {
     g.n_tiles[1] = cdiv(d->H, tn);
     g.k_iters[1] = cdiv(d->F, cs::BK);
   }
+  // K-splits: a stage with fewer tiles than CTAs (small M) splits K so that
+  // enough SMs stream its weights; at least 8 K-slices per split.
+  const int capacity = num_sms / g.cg;
+  for (int s = 0; s < g.stages; ++s) {
+    g.splits[s] = 1;
+    if (d->kind == CS_CHAIN_ATTN && s == 1) continue;  // attention units do not split
+    const int tiles = g.m_tiles * g.n_tiles[s];
+    int sp = d->split_k;
+    if (sp == 0) sp = tiles < capacity ? capacity / tiles : 1;
+    sp = std::min(sp, std::max(1, g.k_iters[s] / 8));
+    sp = std::max(1, std::min(sp, 15));
+    g.kps[s] = cdiv(g.k_iters[s], sp);
+    g.splits[s] = cdiv(g.k_iters[s], g.kps[s]);  // no empty split
+  }
   g.group_m = d->group_m > 0 ? d->group_m : 8 / g.cg;
   if (g.group_m > g.m_tiles) g.group_m = g.m_tiles;
   const int groups = cdiv(g.m_tiles, g.group_m);
@@ -237,7 +259,8 @@ std::vector<uint32_t> build_fused(const Geometry& g) {
       if (gg < 0 || gg >= groups) continue;
       const int m0 = gg * g.group_m, m1 = std::min(g.m_tiles, m0 + g.group_m);
       for (int n = 0; n < g.n_tiles[s]; ++n)
-        for (int m = m0; m < m1; ++m) v.push_back(enc_unit(s, m, n));
+        for (int m = m0; m < m1; ++m)
+          for (int ks = 0; ks < g.splits[s]; ++ks) v.push_back(enc_unit(s, m, n, ks));
     }
   return v;
 }
@@ -247,7 +270,8 @@ std::vector<uint32_t> build_stage(const Geometry& g, int s) {
   std::vector<uint32_t> v;
   for (int m0 = 0; m0 < g.m_tiles; m0 += g.group_m)
     for (int n = 0; n < g.n_tiles[s]; ++n)
-      for (int m = m0; m < std::min(g.m_tiles, m0 + g.group_m); ++m) v.push_back(enc_unit(s, m, n));
+      for (int m = m0; m < std::min(g.m_tiles, m0 + g.group_m); ++m)
+        for (int ks = 0; ks < g.splits[s]; ++ks) v.push_back(enc_unit(s, m, n, ks));
   return v;
 }
 
@@ -277,6 +301,8 @@ void free_plan(cs_chain_s* p) {
   for (auto& b : p->sched_stage) if (b) cudaFree(b);
   for (auto& b : p->delays) if (b) cudaFree(b);
   if (p->trace) cudaFree(p->trace);
+  for (auto& b : p->partial) if (b) cudaFree(b);
+  for (auto& b : p->split_ctr) if (b) cudaFree(b);
   delete p;
 }
 
@@ -324,6 +350,14 @@ int wait_kind(const cs_chain_s* p) {
          : p->d.policy == CS_SYNC_ROW ? cs::WAIT_ROW
          : p->d.policy == CS_SYNC_STRIDED ? cs::WAIT_STRIDED
                                           : cs::WAIT_NONE;
+}
+
+void fill_split(const cs_chain_s* p, int st, cs::StageP& s) {
+  s.splits = p->splits[st];
+  s.kps = p->kps[st] > 0 ? p->kps[st] : p->k_iters[st];
+  s.m_blocks = p->m_blocks;
+  s.partial = p->partial[st];
+  s.split_ctr = p->split_ctr[st];
 }
 
 void fill_common(const cs_chain_s* p, cs::KParams& kp) {
@@ -391,6 +425,8 @@ void fill_mlp_stages(const cs_chain_s* p, const cs_mlp_args* a, cs::KParams& kp)
   s1.rel_tile = nullptr;
   s1.rel_row = nullptr;
   s1.skip_unit = -1;
+  fill_split(p, 0, s0);
+  fill_split(p, 1, s1);
   kp.acc_stride = (s0.mma_n > 128 || s1.mma_n > 128) ? 256 : 128;
 }
 
@@ -516,6 +552,9 @@ void fill_attn_stages(const cs_chain_s* p, cs::KParams& kp) {
   s2.dep_bn = 128;
   s2.stride = p->stride;
   s2.skip_unit = -1;
+  fill_split(p, 0, s0);
+  fill_split(p, 1, s1);
+  fill_split(p, 2, s2);
   kp.acc_stride = 128;
 }
 
@@ -569,6 +608,7 @@ cs_status cs_chain_desc_init(cs_chain_desc* d) {
   d->group_m = 0;
   d->tile_n = 0;
   d->tile_m = 0;
+  d->split_k = 0;
   return CS_OK;
 }
 
@@ -614,7 +654,9 @@ cs_status cs_chain_plan(const cs_chain_desc* desc, cs_chain_t* out) {
     p->n_tiles[i] = g.n_tiles[i];
     p->k_iters[i] = g.k_iters[i];
     p->units[i] = g.m_blocks * g.n_tiles[i];
-    p->sched_units[i] = g.m_tiles * g.n_tiles[i];
+    p->sched_units[i] = g.m_tiles * g.n_tiles[i] * g.splits[i];
+    p->splits[i] = g.splits[i];
+    p->kps[i] = g.kps[i];
   }
   p->lag = g.lag;
   p->group_m = g.group_m;
@@ -645,6 +687,16 @@ cs_status cs_chain_plan(const cs_chain_desc* desc, cs_chain_t* out) {
   }
   if (cudaMalloc(reinterpret_cast<void**>(&p->ctrl), cs::CTRL_WORDS * 4) != cudaSuccess)
     return bail(fail(CS_ERR_OOM, "cudaMalloc of the control block failed"));
+  for (int st = 0; st < g.stages; ++st) {
+    if (g.splits[st] <= 1) continue;
+    const int acc_n = (desc->kind == CS_CHAIN_MLP_SWIGLU && st == 0) ? 256 : g.bn[st];
+    const size_t pf = static_cast<size_t>(g.splits[st]) * g.m_blocks * g.n_tiles[st] * cs::BM * acc_n;
+    const size_t words = static_cast<size_t>(g.m_blocks) * g.n_tiles[st];
+    if (cudaMalloc(reinterpret_cast<void**>(&p->partial[st]), pf * 4) != cudaSuccess ||
+        cudaMalloc(reinterpret_cast<void**>(&p->split_ctr[st]), words * 4) != cudaSuccess)
+      return bail(fail(CS_ERR_OOM, "cudaMalloc of the split-K workspace failed"));
+    if (cudaMemset(p->split_ctr[st], 0, words * 4) != cudaSuccess) return bail(fail(CS_ERR_CUDA, "cudaMemset failed"));
+  }
   if (cudaMemset(p->ctrl, 0, cs::CTRL_WORDS * 4) != cudaSuccess) return bail(fail(CS_ERR_CUDA, "cudaMemset failed"));
   std::vector<uint32_t> fused = build_fused(g);
   p->n_fused = static_cast<int>(fused.size());
@@ -783,6 +835,9 @@ cs_status cs_chain_reset(cs_chain_t p) {
   for (int b = 0; b < p->stages - 1; ++b)
     CS_CUDA(cudaMemset(p->sems[b], 0, (p->sem_words[b] + p->m_tiles) * 4));
   CS_CUDA(cudaMemset(p->ctrl, 0, cs::CTRL_WORDS * 4));
+  for (int st = 0; st < p->stages; ++st)
+    if (p->split_ctr[st])
+      CS_CUDA(cudaMemset(p->split_ctr[st], 0, static_cast<size_t>(p->m_blocks) * p->n_tiles[st] * 4));
   CS_CUDA(cudaDeviceSynchronize());
   p->error_latched = false;
   return CS_OK;
@@ -805,6 +860,7 @@ cs_status cs_chain_query(cs_chain_t p, cs_chain_info* info) {
   for (int i = 0; i < 3; ++i) {
     info->tile_n[i] = p->bn[i];
     info->sched_units[i] = p->sched_units[i];
+    info->split_k[i] = p->splits[i];
   }
   info->tile_m = cs::BM * p->cg;
   info->stride = p->stride;
@@ -935,9 +991,10 @@ cs_status cs_mlp_forward_noalloc(const cs_chain_desc* desc, const cs_mlp_args* a
   // A plan on the host stack whose buffers all point into the scratch array.
   cs_chain_s p;
   p.d = *desc;
+  p.d.split_k = 1;  // no split-K workspace in the fixed array
   p.device = dev;
   p.num_sms = desc->num_sms > 0 && desc->num_sms < sms ? desc->num_sms : sms;
-  Geometry g = geometry(desc, p.num_sms);
+  Geometry g = geometry(&p.d, p.num_sms);
   p.m_tiles = g.m_blocks;
   p.m_units = g.m_tiles;
   p.m_blocks = g.m_blocks;
@@ -947,7 +1004,9 @@ cs_status cs_mlp_forward_noalloc(const cs_chain_desc* desc, const cs_mlp_args* a
     p.n_tiles[i] = g.n_tiles[i];
     p.k_iters[i] = g.k_iters[i];
     p.units[i] = g.m_blocks * g.n_tiles[i];
-    p.sched_units[i] = g.m_tiles * g.n_tiles[i];
+    p.sched_units[i] = g.m_tiles * g.n_tiles[i] * g.splits[i];
+    p.splits[i] = g.splits[i];
+    p.kps[i] = g.kps[i];
     p.bn[i] = g.bn[i];
   }
   p.lag = g.lag;

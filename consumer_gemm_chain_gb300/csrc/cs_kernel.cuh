@@ -93,6 +93,12 @@ struct StageP {
   uint32_t* rel_row;
   const uint32_t* delay_ns;  // per 128-row block x column tile, or null
   int skip_unit;   // 128-row block x column tile that skips its release (-1: none)
+  // split-K: `splits` units per tile, each over `kps` K-slices, writing fp32
+  // partial tiles [splits][m_blocks][n_tiles][128][mma_n]; the last to arrive
+  // (per-tile counter, `splits` arrivals per forward) reduces them in split order
+  int splits, kps, m_blocks;
+  float* partial;
+  uint32_t* split_ctr;
   // attention (STAGE_ATTN)
   int heads;
   float softmax_scale_log2;  // log2(e) / sqrt(head_dim)
@@ -147,6 +153,7 @@ struct SmemCtl {
   uint32_t mb_unit;         // pair mode: dispatch index handed to the peer
   uint32_t tmem_base;
   volatile int abort;
+  volatile int split_last;  // epilogue: this unit was the last split of its tile
   int issued_parity[NS];  // TMA thread: parity of the last load issued into each slot (-1: none)
 };
 
@@ -180,8 +187,10 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, SmemCtl
   }
 }
 
-__device__ __forceinline__ uint32_t unit_stage(uint32_t u) { return u >> 28; }
-__device__ __forceinline__ int unit_m(uint32_t u) { return static_cast<int>((u >> 14) & 0x3FFFu); }
+// Unit encoding: stage [31:30] | K-split [29:26] | tile row [25:14] | tile column [13:0].
+__device__ __forceinline__ uint32_t unit_stage(uint32_t u) { return u >> 30; }
+__device__ __forceinline__ int unit_ks(uint32_t u) { return static_cast<int>((u >> 26) & 0xFu); }
+__device__ __forceinline__ int unit_m(uint32_t u) { return static_cast<int>((u >> 14) & 0xFFFu); }
 __device__ __forceinline__ int unit_n(uint32_t u) { return static_cast<int>(u & 0x3FFFu); }
 
 struct RingPos {
@@ -298,12 +307,14 @@ __device__ bool tma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
   const int m = unit_m(unit), n = unit_n(unit);
   const uint32_t bytes = TILE_A_BYTES + S.b_bytes;
   const bool do_wait = p.waits && S.wait != WAIT_NONE;
-  const int claim_at = S.k_iters > CLAIM_AHEAD ? S.k_iters - CLAIM_AHEAD : 0;
+  const int kb0 = unit_ks(unit) * S.kps;
+  const int kb1 = min(S.k_iters, kb0 + S.kps);
+  const int claim_at = kb1 - kb0 > CLAIM_AHEAD ? kb1 - CLAIM_AHEAD : kb0;
   const int row0 = (m * CG + static_cast<int>(rank)) * BM;  // this CTA's A rows
   const int bcols = S.bn / CG;                               // this CTA's share of B's columns
   const int col0 = n * S.bn + static_cast<int>(rank) * bcols;
   int ready = 0;
-  for (int kb = 0; kb < S.k_iters; ++kb) {
+  for (int kb = kb0; kb < kb1; ++kb) {
     if (rank == 0 && kb == claim_at) mbar_arrive(&sc->claim_req);
     if (do_wait && !tma_wait_ready(sc, q, (kb * BK) / S.dep_bn + 1, ready, p)) return false;
     if (!wait_bar(&sc->empty[rp.slot], rp.phase ^ 1u, sc, p, 1)) return false;
@@ -327,8 +338,8 @@ __device__ bool tma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
       else
         tma_load_2d_pair(dst, map, x, y, bar_addr);
     };
-    if (kb == 0) trace_put(p, tidx, rank, CG, 4, globaltimer());
-    if (kb == S.k_iters - 1) trace_put(p, tidx, rank, CG, 5, globaltimer());
+    if (kb == kb0) trace_put(p, tidx, rank, CG, 4, globaltimer());
+    if (kb == kb1 - 1) trace_put(p, tidx, rank, CG, 5, globaltimer());
     load(sa, &p.maps[S.map_a], kb * BK, row0);
     // B operand(s): this CTA's bcols rows of N per operand; a second operand
     // (the up projection of gate|up) follows the first, so one N = 2*bn MMA
@@ -360,7 +371,9 @@ __device__ bool mma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
   if (!wait_bar(&sc->tempty[acc], acc_phase ^ 1u, sc, p, 2)) return false;
   tc_fence_after();
   const uint32_t d = sc->tmem_base + acc * static_cast<uint32_t>(p.acc_stride);
-  for (int kb = 0; kb < S.k_iters; ++kb) {
+  const int kb0 = unit_ks(unit) * S.kps;
+  const int kb1 = min(S.k_iters, kb0 + S.kps);
+  for (int kb = kb0; kb < kb1; ++kb) {
     if (!wait_bar(&sc->full[rp.slot], rp.phase, sc, p, 3)) return false;
     tc_fence_after();
     const uint32_t sa = smem_u32(ring + rp.slot * STAGE_BYTES);
@@ -373,7 +386,7 @@ __device__ bool mma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
     for (int kk = 0; kk < BK / UMMA_K; ++kk) {
       const uint64_t a = adesc + static_cast<uint64_t>(kk * 2);  // +32 bytes along K
       const uint64_t b = bdesc + static_cast<uint64_t>(S.b_major == 0 ? kk * 2 : kk * 128);  // +32 B / +16 rows
-      tc_mma_f16<CG>(d, a, b, idesc, (kb | kk) != 0 ? 1u : 0u);
+      tc_mma_f16<CG>(d, a, b, idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
     }
     tc_commit<CG>(&sc->empty[rp.slot]);
     rp.next<NS>();
@@ -473,9 +486,19 @@ __device__ void release_tile(const KParams& p, const StageP& S, int mb, int n, i
   }
 }
 
+__device__ __forceinline__ void st_global_v4f(float* p, float a, float b, float c, float d) {
+  asm volatile("st.global.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+// L2-only load (partials written by other SMs are not in this SM's L1).
+__device__ __forceinline__ float4 ld_cg_v4f(const float* p) {
+  float4 v;
+  asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+  return v;
+}
+
 template <int NS, int CG>
 __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* staging, uint32_t unit, uint32_t& acc,
-                              uint32_t& acc_phase, int& last_buf, uint32_t rank, uint32_t tidx) {
+                              uint32_t& acc_phase, int& last_buf, uint32_t rank, uint32_t tidx, uint32_t epoch1) {
   const StageP& S = p.st[unit_stage(unit)];
   const int mb = unit_m(unit) * CG + static_cast<int>(rank);  // this CTA's 128-row block
   const int n = unit_n(unit);
@@ -488,26 +511,89 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
   const uint32_t tbase =
       sc->tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * static_cast<uint32_t>(p.acc_stride);
   const int nchunks = S.bn / 64;
+  const bool split = S.splits > 1;
+  const size_t tile_floats = static_cast<size_t>(BM) * S.mma_n;
+  auto tile_partial = [&](int ks) {
+    return S.partial + (static_cast<size_t>(ks * S.m_blocks + mb) * S.n_tiles + n) * tile_floats +
+           static_cast<size_t>(row) * S.mma_n;
+  };
+  auto release_tmem = [&]() {
+    // this warp is done with the accumulator buffer: hand it back to the MMA
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+      if constexpr (CG == 1)
+        mbar_arrive(&sc->tempty[acc]);
+      else
+        mbar_arrive_cluster(mapa_shared(&sc->tempty[acc], 0));
+    }
+  };
+  if (split) {
+    // K-split: write this split's fp32 rows, count the arrival; only the last
+    // split of the tile goes on (and reduces every split in split order).
+    float* mine = tile_partial(unit_ks(unit));
+    for (int c = 0; c < S.mma_n / 32; ++c) {
+      uint32_t v[32];
+      tmem_ld32(tbase + c * 32, v);
+      tc_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 32; j += 4)
+        st_global_v4f(mine + c * 32 + j, __uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
+                      __uint_as_float(v[j + 3]));
+    }
+    release_tmem();
+    acc ^= 1u;
+    if (acc == 0u) acc_phase ^= 1u;
+    __threadfence();
+    named_bar_sync(1, EPI_THREADS);
+    if (threadIdx.x == EPI_WARP0 * 32) {
+      const uint32_t old = atomicAdd(S.split_ctr + mb * S.n_tiles + n, 1u);
+      sc->split_last = (old + 1u == epoch1 * static_cast<uint32_t>(S.splits)) ? 1 : 0;
+      __threadfence();
+    }
+    named_bar_sync(1, EPI_THREADS);
+    if (!sc->split_last) {
+      if (threadIdx.x == EPI_WARP0 * 32) trace_put(p, tidx, rank, CG, 7, globaltimer());
+      return true;
+    }
+    __threadfence();
+  }
 #pragma unroll 1
   for (int c = 0; c < nchunks; ++c) {
-    uint32_t v[2][32];
-    uint32_t u[2][32];
-    tmem_ld32(tbase + c * 64, v[0]);
-    tmem_ld32(tbase + c * 64 + 32, v[1]);
-    if (S.epi == EPI_SWIGLU) {
-      tmem_ld32(tbase + S.bn + c * 64, u[0]);
-      tmem_ld32(tbase + S.bn + c * 64 + 32, u[1]);
-    }
-    tc_wait_ld();
-    if (c == nchunks - 1) {
-      // this warp is done with the accumulator buffer: hand it back to the MMA
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if constexpr (CG == 1)
-          mbar_arrive(&sc->tempty[acc]);
-        else
-          mbar_arrive_cluster(mapa_shared(&sc->tempty[acc], 0));
+    float va[64], vu[64];
+    if (split) {
+#pragma unroll
+      for (int j = 0; j < 64; ++j) va[j] = vu[j] = 0.0f;
+      for (int ks = 0; ks < S.splits; ++ks) {
+        const float* src = tile_partial(ks);
+#pragma unroll
+        for (int j = 0; j < 64; j += 4) {
+          const float4 x = ld_cg_v4f(src + c * 64 + j);
+          va[j] += x.x, va[j + 1] += x.y, va[j + 2] += x.z, va[j + 3] += x.w;
+        }
+        if (S.epi == EPI_SWIGLU) {
+#pragma unroll
+          for (int j = 0; j < 64; j += 4) {
+            const float4 x = ld_cg_v4f(src + S.bn + c * 64 + j);
+            vu[j] += x.x, vu[j + 1] += x.y, vu[j + 2] += x.z, vu[j + 3] += x.w;
+          }
+        }
+      }
+    } else {
+      uint32_t v[2][32];
+      uint32_t u[2][32];
+      tmem_ld32(tbase + c * 64, v[0]);
+      tmem_ld32(tbase + c * 64 + 32, v[1]);
+      if (S.epi == EPI_SWIGLU) {
+        tmem_ld32(tbase + S.bn + c * 64, u[0]);
+        tmem_ld32(tbase + S.bn + c * 64 + 32, u[1]);
+      }
+      tc_wait_ld();
+      if (c == nchunks - 1) release_tmem();
+#pragma unroll
+      for (int j = 0; j < 64; ++j) {
+        va[j] = __uint_as_float(v[j >> 5][j & 31]);
+        vu[j] = S.epi == EPI_SWIGLU ? __uint_as_float(u[j >> 5][j & 31]) : 0.0f;
       }
     }
     uint32_t w[32];
@@ -516,23 +602,15 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
       float bias[64];
       load_bias64(S, col0, p.bf16, bias);
 #pragma unroll
-      for (int j = 0; j < 64; j += 2) {
-        const float a = gelu_tanh_f(__uint_as_float(v[j >> 5][j & 31]) + bias[j]);
-        const float b = gelu_tanh_f(__uint_as_float(v[(j + 1) >> 5][(j + 1) & 31]) + bias[j + 1]);
-        w[j >> 1] = pack2(a, b, p.bf16);
-      }
+      for (int j = 0; j < 64; j += 2)
+        w[j >> 1] = pack2(gelu_tanh_f(va[j] + bias[j]), gelu_tanh_f(va[j + 1] + bias[j + 1]), p.bf16);
     } else if (S.epi == EPI_SWIGLU) {
 #pragma unroll
-      for (int j = 0; j < 64; j += 2) {
-        const float a = silu_f(__uint_as_float(v[j >> 5][j & 31])) * __uint_as_float(u[j >> 5][j & 31]);
-        const float b =
-            silu_f(__uint_as_float(v[(j + 1) >> 5][(j + 1) & 31])) * __uint_as_float(u[(j + 1) >> 5][(j + 1) & 31]);
-        w[j >> 1] = pack2(a, b, p.bf16);
-      }
+      for (int j = 0; j < 64; j += 2)
+        w[j >> 1] = pack2(silu_f(va[j]) * vu[j], silu_f(va[j + 1]) * vu[j + 1], p.bf16);
     } else {
 #pragma unroll
-      for (int j = 0; j < 64; j += 2)
-        w[j >> 1] = pack2(__uint_as_float(v[j >> 5][j & 31]), __uint_as_float(v[(j + 1) >> 5][(j + 1) & 31]), p.bf16);
+      for (int j = 0; j < 64; j += 2) w[j >> 1] = pack2(va[j], va[j + 1], p.bf16);
     }
     // Two chunk buffers alternate.  Every earlier store that read this buffer
     // must be done: if the newest committed store read the other buffer, all
@@ -558,8 +636,10 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
       last_buf = buf;
     }
   }
-  acc ^= 1u;
-  if (acc == 0u) acc_phase ^= 1u;
+  if (!split) {
+    acc ^= 1u;
+    if (acc == 0u) acc_phase ^= 1u;
+  }
   if (S.rel_tile != nullptr) {
     release_tile(p, S, mb, n, lane);
     last_buf = -1;
@@ -1052,7 +1132,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
       }
       if (unit == UNIT_END) break;
       if (p.st[unit_stage(unit)].kind == STAGE_GEMM)
-        ok = epi_gemm_unit<NS, CG>(p, sc, staging, unit, acc, acc_phase, last_buf, rank, tidx);
+        ok = epi_gemm_unit<NS, CG>(p, sc, staging, unit, acc, acc_phase, last_buf, rank, tidx, epoch1);
       else if constexpr (CG == 1 && ATTN)
         ok = epi_attn_unit<NS>(p, sc, staging, unit, s_phase, o_phase, last_buf, tidx);
     }

@@ -86,7 +86,8 @@ typedef enum cs_weight_layout { CS_WEIGHTS_KN = 0, CS_WEIGHTS_NK = 1 } cs_weight
 
 typedef struct cs_chain_desc {
   int kind;            /* cs_chain_kind */
-  int M;               /* rows (tokens; for ATTN also the causal sequence length), >= 1 */
+  int M;               /* rows (tokens; for ATTN also the causal sequence length),
+                          1 .. 524160 */
   int H;               /* model width: GEMM1 K and GEMM2 N; multiple of 8 */
   int F;               /* MLP: FFN shard width (GEMM1 N, GEMM2 K), multiple of 8.
                           ATTN: heads * head_dim.                                   */
@@ -108,6 +109,12 @@ typedef struct cs_chain_desc {
   int tile_m;          /* rows per GEMM tile: 128 (one SM) or 256 (a 2-SM cluster
                           sharing one tcgen05 MMA; needs tile_n = 256); 0 = auto.
                           Semaphores stay per 128-row block either way.             */
+  int split_k;         /* K-splits per GEMM tile: 0 = auto (split when a stage has
+                          fewer tiles than the grid, small M), 1 = never, 2..15 = that
+                          many for every GEMM stage.  Splits write fp32 partial tiles
+                          to a plan-owned workspace; the last split to finish sums
+                          them in split order (bit-reproducible) and runs the
+                          epilogue and the release.                                  */
   unsigned long long spin_timeout_ns; /* per-wait limit of a consumer tile; 0 = 2 s */
 } cs_chain_desc;
 
@@ -189,7 +196,8 @@ typedef struct cs_chain_info {
   int group_m;             /* rasterisation group actually used (tile rows) */
   int tile_n[3];           /* output columns per tile of each stage */
   int tile_m;              /* rows per GEMM tile actually used (128 or 256) */
-  int sched_units[3];      /* schedule entries of each stage (tiles) */
+  int sched_units[3];      /* schedule entries of each stage (tiles x K-splits) */
+  int split_k[3];          /* K-splits of each stage */
   int stride;              /* strided-policy stride actually used */
   void* intermediate[2];   /* H (MLP) or QKV, O (ATTN): device pointers owned by the plan */
   size_t sem_words[2];     /* length of each boundary's tile-semaphore array */
@@ -198,8 +206,8 @@ typedef struct cs_chain_info {
 cs_status cs_chain_query(cs_chain_t plan, cs_chain_info* info);
 
 /* Host-only: the dispatch order a plan with this desc and grid size would use.
- * Each entry encodes one unit as (stage << 28) | (m_tile << 14) | n_tile, m_tile
- * counting tile_m-row tiles; for an ATTN stage n_tile is the head.  Row blocks are taken in groups of group_m; a
+ * Each entry encodes one unit as (stage << 30) | (k_split << 26) | (m_tile << 14) |
+ * n_tile, m_tile counting tile_m-row tiles; for an ATTN stage n_tile is the head.  Row blocks are taken in groups of group_m; a
  * stage's units of one group are listed column-tile-major; at step t, stage s
  * lists group t - s*lag, so every producer a unit waits on is listed before it.  *n_out receives the count; entries beyond cap
  * are not written (cap may be 0 to query the count).  Needs no GPU. */

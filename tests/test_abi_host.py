@@ -43,7 +43,8 @@ def test_desc_defaults(cs):
 
 
 @pytest.mark.parametrize("field,value", [("M", 0), ("H", 12), ("F", 0), ("dtype", 7), ("policy", 9),
-                                         ("kind", 5), ("weight_layout", 3), ("lag", -2), ("num_sms", -1)])
+                                         ("kind", 5), ("weight_layout", 3), ("lag", -2), ("num_sms", -1),
+                                         ("split_k", 16), ("tile_n", 192), ("tile_m", 64), ("M", 128 * 4096)])
 def test_invalid_descs_are_rejected_without_a_gpu(cs, field, value):
     d = cs.cs_chain_desc_init(M=64, H=256, F=1024)
     setattr(d, field, value)
@@ -64,35 +65,33 @@ def test_null_arguments(cs):
     assert "NULL" in cs.cs_last_error_string()
 
 
-def _deps(stage_kind, s, m, n, d, q):
-    """Producer units (stage, m, n) a unit waits on, under the plan's policy (TILE: the
-    tiles its K-slices read; every policy waits on a superset of those)."""
-    if s == 0:
-        return []
-    if stage_kind == "attn" and s == 1:
-        heads = d.heads
-        return [(0, j, t) for j in range(m + 1) for t in (n, n + heads, n + 2 * heads)]
-    ntp = q[s - 1]
-    return [(s - 1, m, t) for t in range(ntp)]
+def _check_order(dec, deps_of):
+    """Every unit appears once and after every producer unit it depends on."""
+    pos = {u: i for i, u in enumerate(dec)}
+    assert len(pos) == len(dec)
+    for u, i in pos.items():
+        for dep in deps_of(u):
+            assert pos[dep] < i, f"unit {u} at {i} precedes its producer {dep}"
 
 
 @pytest.mark.parametrize("tile_m,tile_n", [(128, 128), (128, 256), (256, 256)])
-@pytest.mark.parametrize("M,H,F,sms,lag,group", [(64, 256, 1024, 148, -1, 0), (2048, 12288, 6144, 148, -1, 0),
-                                                 (2048, 12288, 6144, 152, 0, 3), (1, 12288, 6144, 148, -1, 0),
-                                                 (1000, 8192, 2752, 148, 2, 1), (1536, 8192, 8192, 148, 5, 5)])
-def test_schedule_is_dependency_ordered(cs, M, H, F, sms, lag, group, tile_n, tile_m):
-    d = cs.cs_chain_desc_init(M=M, H=H, F=F, lag=lag, group_m=group, tile_n=tile_n, tile_m=tile_m)
-    units = cs.cs_schedule_build(d, sms)
+@pytest.mark.parametrize("M,H,F,sms,lag,group,split", [(64, 256, 1024, 148, -1, 0, 1), (2048, 12288, 6144, 148, -1, 0, 1),
+                                                       (2048, 12288, 6144, 152, 0, 3, 1), (1, 12288, 6144, 148, -1, 0, 3),
+                                                       (1000, 8192, 2752, 148, 2, 1, 2), (1536, 8192, 8192, 148, 5, 5, 1)])
+def test_schedule_is_dependency_ordered(cs, M, H, F, sms, lag, group, split, tile_n, tile_m):
+    d = cs.cs_chain_desc_init(M=M, H=H, F=F, lag=lag, group_m=group, tile_n=tile_n, tile_m=tile_m, split_k=split)
+    dec = [cs.decode_unit(u) for u in cs.cs_schedule_build(d, sms)]
     m_tiles = -(-M // tile_m)
     n0, n1 = -(-F // tile_n), -(-H // tile_n)
-    dec = [cs.decode_unit(u) for u in units]
-    # every unit exactly once
-    expect = {(0, m, n) for m in range(m_tiles) for n in range(n0)} | {(1, m, n) for m in range(m_tiles) for n in range(n1)}
+    # with an explicit split_k every GEMM stage gets that many splits (enough K-slices here)
+    expect = {(0, m, n, k) for m in range(m_tiles) for n in range(n0) for k in range(split)} | \
+             {(1, m, n, k) for m in range(m_tiles) for n in range(n1) for k in range(split)}
     assert len(dec) == len(expect) and set(dec) == expect
-    pos = {u: i for i, u in enumerate(dec)}
-    for (s, m, n), i in pos.items():
-        for dep in _deps("mlp", s, m, n, d, [n0, n1]):
-            assert pos[dep] < i, f"unit {(s, m, n)} at {i} precedes its producer {dep}"
+
+    def deps(u):
+        s, m, n, _ = u
+        return [] if s == 0 else [(0, m, t, k) for t in range(n0) for k in range(split)]
+    _check_order(dec, deps)
 
 
 @pytest.mark.parametrize("M,lag,group", [(1, -1, 0), (300, -1, 0), (2048, -1, 0), (2048, 2, 3), (1000, 0, 1)])
@@ -101,17 +100,31 @@ def test_attention_schedule_is_dependency_ordered(cs, M, lag, group):
     dec = [cs.decode_unit(u) for u in cs.cs_schedule_build(d, 148)]
     m_tiles = -(-M // 128)
     nt = [36, 12, 96]
-    expect = {(s, m, n) for s in range(3) for m in range(m_tiles) for n in range(nt[s])}
-    assert len(dec) == len(expect) and set(dec) == expect
-    pos = {u: i for i, u in enumerate(dec)}
-    for (s, m, n), i in pos.items():
-        deps = []
+    splits = {}
+    for s, m, n, k in dec:
+        splits[(s, m, n)] = max(splits.get((s, m, n), 0), k + 1)
+    assert set(splits) == {(s, m, n) for s in range(3) for m in range(m_tiles) for n in range(nt[s])}
+    assert all(v == 1 for (s, _, _), v in splits.items() if s == 1)  # attention units do not split
+
+    def deps(u):
+        s, m, n, _ = u
         if s == 1:   # causal: key blocks 0..m of head n (Q, K and V tiles)
-            deps = [(0, j, t) for j in range(m + 1) for t in (n, n + 12, n + 24)]
-        elif s == 2:  # every head of the same row block
-            deps = [(1, m, h) for h in range(12)]
-        for dep in deps:
-            assert pos[dep] < i, (s, m, n, dep)
+            return [(0, j, t, k) for j in range(m + 1) for t in (n, n + 12, n + 24) for k in range(splits[(0, j, t)])]
+        if s == 2:   # every head of the same row block
+            return [(1, m, h, 0) for h in range(12)]
+        return []
+    _check_order(dec, deps)
+
+
+def test_small_m_splits_k_automatically(cs):
+    d = cs.cs_chain_desc_init(M=64, H=12288, F=6144)
+    dec = [cs.decode_unit(u) for u in cs.cs_schedule_build(d, 152)]
+    s0 = [u for u in dec if u[0] == 0]
+    assert {u[3] for u in s0} == {0, 1, 2}        # 48 tiles < 152 SMs: three K-splits each
+    assert len(s0) == 48 * 3
+    assert {u[3] for u in dec if u[0] == 1} == {0}  # 96 consumer tiles: one split each
+    # the splits of a tile are consecutive
+    assert s0[:3] == [(0, 0, 0, 0), (0, 0, 0, 1), (0, 0, 0, 2)]
 
 
 def test_attention_desc_validation(cs):
@@ -127,7 +140,7 @@ def test_attention_desc_validation(cs):
 
 def test_schedule_rasterises_column_major_within_a_group(cs):
     d = cs.cs_chain_desc_init(M=2048, H=12288, F=6144, group_m=4, lag=1, tile_n=128)
-    dec = [cs.decode_unit(u) for u in cs.cs_schedule_build(d, 148)]
+    dec = [cs.decode_unit(u)[:3] for u in cs.cs_schedule_build(d, 148)]
     # first group of producers: (n, m) with m fastest
     assert dec[:8] == [(0, 0, 0), (0, 1, 0), (0, 2, 0), (0, 3, 0), (0, 0, 1), (0, 1, 1), (0, 2, 1), (0, 3, 1)]
     # then the second producer group, then the first consumer group

@@ -210,3 +210,48 @@ def test_stress_shape_all_policies(M):
             base = Y
             assert oracle.rel_err(Y[rows], Yref) <= TOL
         assert torch.equal(Y, base), pol
+
+
+@pytest.mark.parametrize("split", [2, 3, 5])
+@pytest.mark.parametrize("tile_m,tile_n", TILES)
+@pytest.mark.parametrize("M,H,F", [(1, 1024, 1024), (200, 968, 392), (300, 2048, 1280)])
+def test_split_k_parity(M, H, F, tile_m, tile_n, split):
+    inp = cs_inputs.make_custom("gelu", M, H, F, seed=51)
+    dev = device_tensors(inp, "nk")
+    with plan_for(inp, "tile", "nk", tile_m=tile_m, tile_n=tile_n, split_k=split) as plan:
+        q = cs.cs_chain_query(plan)
+        assert q["split_k"][0] > 1
+        Y1 = forward(plan, dev).cpu()
+        H1 = intermediate(plan, 0, inp.M, inp.F, inp.dtype).cpu()
+        Y2 = forward(plan, dev).cpu()
+        tiles, rows, epoch = cs.cs_chain_debug_read_sems(plan, 0)
+        assert epoch == 2 and all(v == 2 for r in tiles for v in r)
+    Yref, Href = _oracle(inp)
+    assert oracle.rel_err(H1, Href) <= TOL
+    assert oracle.rel_err(Y1, Yref) <= TOL
+    assert torch.equal(Y1, Y2)  # fixed split order: the same bits every time
+
+
+def test_split_k_swiglu_and_policies():
+    inp = cs_inputs.make_custom("swiglu", 100, 1024, 688, dtype=torch.bfloat16, seed=52)
+    dev = device_tensors(inp, "nk")
+    outs = {}
+    for pol in ("tile", "row", "strided", "stream"):
+        with plan_for(inp, pol, "nk", split_k=4, group_m=1) as plan:
+            outs[pol] = forward(plan, dev).cpu()
+    Yref, _ = _oracle(inp)
+    assert oracle.rel_err(outs["tile"], Yref) <= TOL
+    for k, v in outs.items():
+        assert torch.equal(v, outs["tile"]), k
+
+
+def test_split_k_delay_injection_never_changes_a_bit():
+    inp = cs_inputs.make_custom("gelu", 64, 2048, 1024, seed=53)
+    dev = device_tensors(inp, "nk")
+    with plan_for(inp, "tile", "nk", split_k=4) as plan:
+        q = cs.cs_chain_query(plan)
+        ref = forward(plan, dev).cpu()
+        for seed in range(3):
+            g = torch.Generator().manual_seed(300 + seed)
+            cs.cs_chain_debug_set_delays(plan, 0, (torch.rand(q["units"][0], generator=g) * 100_000).long().tolist())
+            assert torch.equal(forward(plan, dev).cpu(), ref), seed
