@@ -227,9 +227,22 @@ Geometry geometry(const cs_chain_desc* d, int num_sms) {
     g.splits[s] = 1;
     if (d->kind == CS_CHAIN_ATTN && s == 1) continue;  // attention units do not split
     const int tiles = g.m_tiles * g.n_tiles[s];
+    const int max_sp = std::max(1, std::min(15, g.k_iters[s] / 8));
     int sp = d->split_k;
-    if (sp == 0) sp = tiles < capacity ? capacity / tiles : 1;
-    sp = std::min(sp, std::max(1, g.k_iters[s] / 8));
+    if (sp == 0) {
+      // fewest (waves x K-slices per split): a split count that fills whole
+      // waves; a larger count must win by 10 % (each split adds a partial tile
+      // to write and to reduce)
+      sp = 1;
+      if (tiles < capacity) {
+        long best = -1;
+        for (int c = 1; c <= max_sp; ++c) {
+          const long cost = static_cast<long>(cdiv(tiles * c, capacity)) * cdiv(g.k_iters[s], c);
+          if (best < 0 || 10 * cost < 9 * best) best = cost, sp = c;
+        }
+      }
+    }
+    sp = std::min(sp, max_sp);
     sp = std::max(1, std::min(sp, 15));
     g.kps[s] = cdiv(g.k_iters[s], sp);
     g.splits[s] = cdiv(g.k_iters[s], g.kps[s]);  // no empty split

@@ -120,11 +120,14 @@ def test_small_m_splits_k_automatically(cs):
     d = cs.cs_chain_desc_init(M=64, H=12288, F=6144)
     dec = [cs.decode_unit(u) for u in cs.cs_schedule_build(d, 152)]
     s0 = [u for u in dec if u[0] == 0]
-    assert {u[3] for u in s0} == {0, 1, 2}        # 48 tiles < 152 SMs: three K-splits each
+    assert {u[3] for u in s0} == {0, 1, 2}        # 48 tiles, 152 SMs: 3 splits fill one wave
     assert len(s0) == 48 * 3
-    assert {u[3] for u in dec if u[0] == 1} == {0}  # 96 consumer tiles: one split each
+    s1 = [u for u in dec if u[0] == 1]
+    assert {u[3] for u in s1} == {0, 1, 2}        # 96 tiles: 3 splits = 2 waves of 32 K-slices
     # the splits of a tile are consecutive
     assert s0[:3] == [(0, 0, 0, 0), (0, 0, 0, 1), (0, 0, 0, 2)]
+    big = [cs.decode_unit(u) for u in cs.cs_schedule_build(cs.cs_chain_desc_init(M=2048, H=12288, F=6144), 152)]
+    assert {u[3] for u in big} == {0}             # enough tiles: no split at large M
 
 
 def test_attention_desc_validation(cs):
@@ -148,9 +151,9 @@ def test_schedule_rasterises_column_major_within_a_group(cs):
 
 
 def test_auto_tile_shape(cs):
-    big = cs.cs_schedule_build(cs.cs_chain_desc_init(M=2048, H=12288, F=6144), 148)
-    mid = cs.cs_schedule_build(cs.cs_chain_desc_init(M=640, H=12288, F=6144), 148)
-    small = cs.cs_schedule_build(cs.cs_chain_desc_init(M=256, H=12288, F=6144), 148)
+    big = cs.cs_schedule_build(cs.cs_chain_desc_init(M=2048, H=12288, F=6144, split_k=1), 148)
+    mid = cs.cs_schedule_build(cs.cs_chain_desc_init(M=640, H=12288, F=6144, split_k=1), 148)
+    small = cs.cs_schedule_build(cs.cs_chain_desc_init(M=256, H=12288, F=6144, split_k=1), 148)
     assert len(big) == 8 * 24 + 8 * 48      # 256 x 256 tiles on CTA pairs for large M
     assert len(mid) == 5 * 24 + 5 * 48      # 128 x 256 tiles on single SMs in between
     assert len(small) == 2 * 48 + 2 * 96    # 128 x 128 tiles for small M
