@@ -163,6 +163,7 @@ cs_status validate(const cs_chain_desc* d) {
     return fail(CS_ERR_INVALID_ARG, "bad weight_layout %d", d->weight_layout);
   if (d->M < 1 || d->M > 128 * 4095) return fail(CS_ERR_INVALID_ARG, "M=%d out of range [1, %d]", d->M, 128 * 4095);
   if (d->split_k < 0 || d->split_k > 15) return fail(CS_ERR_INVALID_ARG, "split_k=%d (0..15)", d->split_k);
+  if (d->prefetch < -1 || d->prefetch > 64) return fail(CS_ERR_INVALID_ARG, "prefetch=%d (-1..64)", d->prefetch);
   if (d->H < 8 || d->H % 8 != 0 || d->H > (1 << 20)) return fail(CS_ERR_INVALID_ARG, "H=%d must be a positive multiple of 8", d->H);
   if (d->F < 8 || d->F % 8 != 0 || d->F > (1 << 20)) return fail(CS_ERR_INVALID_ARG, "F=%d must be a positive multiple of 8", d->F);
   if (d->stride < 0) return fail(CS_ERR_INVALID_ARG, "stride=%d", d->stride);
@@ -381,6 +382,21 @@ void fill_common(const cs_chain_s* p, cs::KParams& kp) {
   kp.bf16 = p->d.dtype == CS_BF16;
   kp.trace = p->trace;
   kp.trace_records = p->trace_records;
+  kp.pf_dist = p->d.prefetch < 0 ? 0 : (p->d.prefetch == 0 ? 16 : p->d.prefetch);
+}
+
+// Raw pointers and strides of a GEMM stage's operands for the L2 prefetch.
+// Weight math shape [K, N]: KN storage has K rows of N, NK storage N rows of K.
+void fill_prefetch(const cs_chain_s* p, cs::StageP& s, const void* w, const void* w2, int K, int N, const void* a,
+                   int a_rows, int a_cols) {
+  const bool kn = p->d.weight_layout == CS_WEIGHTS_KN;
+  s.pf_b = static_cast<const char*>(w);
+  s.pf_b2 = static_cast<const char*>(w2);
+  s.pf_ldb = static_cast<long long>(kn ? N : K) * 2;
+  s.pf_brows = kn ? K : N;
+  s.pf_a = static_cast<const char*>(a);
+  s.pf_lda = static_cast<long long>(a_cols) * 2;
+  s.pf_arows = a_rows;
 }
 
 void fill_mlp_stages(const cs_chain_s* p, const cs_mlp_args* a, cs::KParams& kp) {
@@ -440,6 +456,10 @@ void fill_mlp_stages(const cs_chain_s* p, const cs_mlp_args* a, cs::KParams& kp)
   s1.skip_unit = -1;
   fill_split(p, 0, s0);
   fill_split(p, 1, s1);
+  if (a) {
+    fill_prefetch(p, s0, swiglu ? a->Wg : a->W1, swiglu ? a->Wu : nullptr, p->d.H, p->d.F, a->X, p->d.M, p->d.H);
+    fill_prefetch(p, s1, a->W2, nullptr, p->d.F, p->d.H, nullptr, 0, 0);
+  }
   kp.acc_stride = (s0.mma_n > 128 || s1.mma_n > 128) ? 256 : 128;
 }
 
@@ -571,6 +591,11 @@ void fill_attn_stages(const cs_chain_s* p, cs::KParams& kp) {
   kp.acc_stride = 128;
 }
 
+void fill_attn_prefetch(const cs_chain_s* p, const cs_attn_args* a, cs::KParams& kp) {
+  fill_prefetch(p, kp.st[0], a->Wqkv, nullptr, p->d.H, 3 * p->d.F, a->X, p->d.M, p->d.H);
+  fill_prefetch(p, kp.st[2], a->Wo, nullptr, p->d.F, p->d.H, nullptr, 0, 0);
+}
+
 cs_status bind_attn(cs_chain_s* p, const cs_attn_args* a) {
   if (!a) return fail(CS_ERR_INVALID_ARG, "args is NULL");
   if (!a->X || !a->Wqkv || !a->Wo || !a->Y) return fail(CS_ERR_INVALID_ARG, "X, Wqkv, Wo and Y are required");
@@ -622,6 +647,7 @@ cs_status cs_chain_desc_init(cs_chain_desc* d) {
   d->tile_n = 0;
   d->tile_m = 0;
   d->split_k = 0;
+  d->prefetch = 0;
   return CS_OK;
 }
 
@@ -791,6 +817,7 @@ cs_status cs_attn_chain_forward(cs_chain_t p, const cs_attn_args* a, void* strea
   std::memset(&kp, 0, sizeof(kp));
   fill_common(p, kp);
   fill_attn_stages(p, kp);
+  fill_attn_prefetch(p, a, kp);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (p->d.policy == CS_SYNC_STREAM) {
     kp.waits = 0;
@@ -819,6 +846,7 @@ cs_status cs_chain_forward_stage(cs_chain_t p, const void* args, int stage, void
     if ((s = bind_attn(p, a)) != CS_OK) return s;
     fill_common(p, kp);
     fill_attn_stages(p, kp);
+    fill_attn_prefetch(p, a, kp);
   } else {
     const cs_mlp_args* a = static_cast<const cs_mlp_args*>(args);
     if ((s = bind_mlp(p, a)) != CS_OK) return s;

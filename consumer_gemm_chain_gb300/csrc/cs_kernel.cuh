@@ -99,6 +99,16 @@ struct StageP {
   int splits, kps, m_blocks;
   float* partial;
   uint32_t* split_ctr;
+  // L2 prefetch of upcoming K-slices by the scheduler warp (null: none):
+  // pf_b/pf_b2 = weight base(s), pf_ldb = bytes between weight rows, pf_brows =
+  // weight rows (N if K-major, K if MN-major); pf_a/pf_lda/pf_arows likewise for A.
+  const char* pf_b;
+  const char* pf_b2;
+  long long pf_ldb;
+  int pf_brows;
+  const char* pf_a;
+  long long pf_lda;
+  int pf_arows;
   // attention (STAGE_ATTN)
   int heads;
   float softmax_scale_log2;  // log2(e) / sqrt(head_dim)
@@ -119,6 +129,7 @@ struct KParams {
   int acc_stride;  // TMEM columns between the two accumulator buffers
   unsigned long long* trace;  // optional per-unit timestamps (TRACE_WORDS per record), or null
   int trace_records;
+  int pf_dist;     // L2 prefetch distance in K-slices (0: off)
 };
 
 // Trace record of one unit on one CTA (index = dispatch index * CTAs per tile + rank):
@@ -154,6 +165,8 @@ struct SmemCtl {
   uint32_t tmem_base;
   volatile int abort;
   volatile int split_last;  // epilogue: this unit was the last split of its tile
+  volatile int tma_seq;     // TMA warp: units started so far
+  volatile int tma_kb;      // TMA warp: K-slice of its latest load
   int issued_parity[NS];  // TMA thread: parity of the last load issued into each slot (-1: none)
 };
 
@@ -338,7 +351,11 @@ __device__ bool tma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
       else
         tma_load_2d_pair(dst, map, x, y, bar_addr);
     };
-    if (kb == kb0) trace_put(p, tidx, rank, CG, 4, globaltimer());
+    if (kb == kb0) {
+      sc->tma_seq = sc->tma_seq + 1;
+      trace_put(p, tidx, rank, CG, 4, globaltimer());
+    }
+    sc->tma_kb = kb;
     if (kb == kb1 - 1) trace_put(p, tidx, rank, CG, 5, globaltimer());
     load(sa, &p.maps[S.map_a], kb * BK, row0);
     // B operand(s): this CTA's bcols rows of N per operand; a second operand
@@ -928,6 +945,78 @@ __device__ void sched_poll_attn(const KParams& p, const StageP& S, SmemCtl<NS>* 
   }
 }
 
+// ---------------------------------------------------------------- L2 prefetch
+// The scheduler warp spends the time between claims bringing the next K-slices
+// of the unit the TMA warp is loading into L2, pf_dist slices ahead of it: the
+// weight lines (and a producer's A rows), so that the TMA loads hit in L2
+// instead of each stage waiting on its slowest DRAM sector.
+struct PfState {
+  uint32_t unit = UNIT_END;
+  int seq = 0;      // sequence number of that unit in this CTA
+  int next = 0;     // next K-slice to prefetch
+  int kb0 = 0, kb1 = 0;
+};
+
+template <int CG>
+__device__ __forceinline__ void prefetch_slice(const StageP& S, uint32_t unit, int kb, uint32_t rank, int lane) {
+  const int m = unit_m(unit), n = unit_n(unit);
+  const int bcols = S.bn / CG;
+  const int col0 = n * S.bn + static_cast<int>(rank) * bcols;
+  if (S.b_major == 0) {
+    // weights [N, K]: one 128-byte line per weight row of the slice
+    for (int r = lane; r < bcols; r += 32) {
+      const int row = col0 + r;
+      if (row < S.pf_brows) {
+        const long long off = static_cast<long long>(row) * S.pf_ldb + static_cast<long long>(kb) * BK * 2;
+        prefetch_l2(S.pf_b + off);
+        if (S.pf_b2) prefetch_l2(S.pf_b2 + off);
+      }
+    }
+  } else {
+    // weights [K, N]: 64 K rows of bcols*2 bytes
+    const int lines = bcols * 2 / 128;
+    for (int i = lane; i < BK * lines; i += 32) {
+      const int row = kb * BK + i / lines;
+      if (row < S.pf_brows) {
+        const long long off = static_cast<long long>(row) * S.pf_ldb + static_cast<long long>(col0) * 2 + (i % lines) * 128;
+        prefetch_l2(S.pf_b + off);
+        if (S.pf_b2) prefetch_l2(S.pf_b2 + off);
+      }
+    }
+  }
+  if (S.pf_a) {
+    const int row0 = (m * CG + static_cast<int>(rank)) * BM;
+    for (int r = lane; r < BM; r += 32)
+      if (row0 + r < S.pf_arows)
+        prefetch_l2(S.pf_a + static_cast<long long>(row0 + r) * S.pf_lda + static_cast<long long>(kb) * BK * 2);
+  }
+}
+
+// Bounded wait for `bar`, prefetching for the latest pushed unit meanwhile.
+template <int NS, int CG, bool CLUSTER>
+__device__ bool wait_prefetching(uint64_t* bar, uint32_t parity, SmemCtl<NS>* sc, const KParams& p, PfState& pf,
+                                 uint32_t rank, int lane, uint32_t where) {
+  if (p.pf_dist <= 0 || pf.unit == UNIT_END || pf.next >= pf.kb1) return wait_bar<NS, CLUSTER>(bar, parity, sc, p, where);
+  const StageP& S = p.st[unit_stage(pf.unit)];
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    bool ready = false;
+    if (lane == 0) ready = CLUSTER ? mbar_test_wait_cluster(bar, parity) : mbar_test_wait(bar, parity);
+    if (__shfl_sync(0xFFFFFFFFu, ready ? 1 : 0, 0)) return true;
+    // the TMA warp is on an earlier unit: the first pf_dist slices; else pf_dist ahead of it
+    const int limit = min(pf.kb1, (sc->tma_seq < pf.seq ? pf.kb0 : sc->tma_kb + 1) + p.pf_dist);
+    while (pf.next < limit) prefetch_slice<CG>(S, pf.unit, pf.next++, rank, lane);
+    if (pf.next >= pf.kb1) return wait_bar<NS, CLUSTER>(bar, parity, sc, p, where);
+    if (sc->abort) return false;
+    if (globaltimer() - t0 > p.watchdog_ns) {
+      if (lane == 0) record_error(p, ERR_WATCHDOG, 0xFFFFFFFFu, where);
+      sc->abort = 1;
+      return false;
+    }
+    __nanosleep(200);
+  }
+}
+
 // ---------------------------------------------------------------- scheduler role
 template <int NS>
 __device__ __forceinline__ void push_unit(SmemCtl<NS>* sc, uint32_t q, uint32_t unit, uint32_t idx, int lane,
@@ -980,6 +1069,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
     mbar_init(&sc->o_empty, 4);
     mbar_init(&sc->drain, 1);
     sc->abort = 0;
+    sc->tma_seq = 0;
+    sc->tma_kb = 0;
     fence_mbar_init();
     for (int i = 0; i < 8; ++i) prefetch_tmap(&p.maps[i]);
   }
@@ -997,12 +1088,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
   if (warp == SCHED_WARP) {
     uint32_t q = 0, qphase = 0, req_phase = 0, mb_phase = 0;
     bool first = true;
+    PfState pf;
+    int pushed = 0;
     while (true) {
       uint32_t idx = 0xFFFFFFFFu;  // dispatch index (>= n_units: no more work)
       if (leader) {
         // claim units in schedule order, one at a time, just in time
         if (!first) {
-          if (!wait_bar(&sc->claim_req, req_phase, sc, p, 9)) break;
+          if (!wait_prefetching<NS, CG, false>(&sc->claim_req, req_phase, sc, p, pf, rank, lane, 9)) break;
           req_phase ^= 1u;
         }
         first = false;
@@ -1019,7 +1112,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
           mb_phase ^= 1u;
         }
       } else {
-        if (!wait_bar<NS, true>(&sc->mb_full, mb_phase, sc, p, 11)) break;
+        if (!wait_prefetching<NS, CG, true>(&sc->mb_full, mb_phase, sc, p, pf, rank, lane, 11)) break;
         idx = *reinterpret_cast<volatile uint32_t*>(&sc->mb_unit);
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(mapa_shared(&sc->mb_empty, 0));
@@ -1036,6 +1129,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
       const bool consumer = unit != UNIT_END && p.waits && S.wait != WAIT_NONE;
       push_unit(sc, q, unit, idx, lane, consumer);
       if (unit == UNIT_END) break;
+      ++pushed;
+      if (S.kind == STAGE_GEMM && S.pf_b != nullptr) {
+        pf.unit = unit;
+        pf.seq = pushed;
+        pf.kb0 = unit_ks(unit) * S.kps;
+        pf.kb1 = min(S.k_iters, pf.kb0 + S.kps);
+        pf.next = pf.kb0;
+      } else {
+        pf.unit = UNIT_END;
+      }
       if (consumer && S.kind == STAGE_GEMM)
         sched_poll_gemm<NS>(p, S, sc, q, unit_m(unit) * CG + static_cast<int>(rank), epoch1, unit, lane);
       else if constexpr (ATTN)

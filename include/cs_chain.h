@@ -115,6 +115,9 @@ typedef struct cs_chain_desc {
                           to a plan-owned workspace; the last split to finish sums
                           them in split order (bit-reproducible) and runs the
                           epilogue and the release.                                  */
+  int prefetch;        /* L2 prefetch distance in K-slices: the scheduler warp brings
+                          the weight lines (and producer A rows) that far ahead of
+                          the TMA loads into L2; 0 = auto (16), -1 = off            */
   unsigned long long spin_timeout_ns; /* per-wait limit of a consumer tile; 0 = 2 s */
 } cs_chain_desc;
 
