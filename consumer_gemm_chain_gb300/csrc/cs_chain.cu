@@ -382,7 +382,8 @@ void fill_common(const cs_chain_s* p, cs::KParams& kp) {
   kp.bf16 = p->d.dtype == CS_BF16;
   kp.trace = p->trace;
   kp.trace_records = p->trace_records;
-  kp.pf_dist = p->d.prefetch < 0 ? 0 : (p->d.prefetch == 0 ? 16 : p->d.prefetch);
+  // measured: extra L2 prefetch requests slow the loads down, so auto = off
+  kp.pf_dist = p->d.prefetch <= 0 ? 0 : p->d.prefetch;
 }
 
 // Raw pointers and strides of a GEMM stage's operands for the L2 prefetch.

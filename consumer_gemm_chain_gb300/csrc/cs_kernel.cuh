@@ -503,16 +503,6 @@ __device__ void release_tile(const KParams& p, const StageP& S, int mb, int n, i
   }
 }
 
-__device__ __forceinline__ void st_global_v4f(float* p, float a, float b, float c, float d) {
-  asm volatile("st.global.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
-}
-// L2-only load (partials written by other SMs are not in this SM's L1).
-__device__ __forceinline__ float4 ld_cg_v4f(const float* p) {
-  float4 v;
-  asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
-  return v;
-}
-
 template <int NS, int CG>
 __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* staging, uint32_t unit, uint32_t& acc,
                               uint32_t& acc_phase, int& last_buf, uint32_t rank, uint32_t tidx, uint32_t epoch1) {
@@ -530,9 +520,12 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
   const int nchunks = S.bn / 64;
   const bool split = S.splits > 1;
   const size_t tile_floats = static_cast<size_t>(BM) * S.mma_n;
+  // Partial tiles are stored [mma_n/4][128 rows][4 columns]: the float4 of
+  // columns 4c..4c+3 of this thread's row sits at (c * 128 + row), so a warp
+  // reads or writes 512 contiguous bytes per access.
   auto tile_partial = [&](int ks) {
-    return S.partial + (static_cast<size_t>(ks * S.m_blocks + mb) * S.n_tiles + n) * tile_floats +
-           static_cast<size_t>(row) * S.mma_n;
+    return reinterpret_cast<float4*>(S.partial + (static_cast<size_t>(ks * S.m_blocks + mb) * S.n_tiles + n) *
+                                                     tile_floats) + row;
   };
   auto release_tmem = [&]() {
     // this warp is done with the accumulator buffer: hand it back to the MMA
@@ -548,15 +541,15 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
   if (split) {
     // K-split: write this split's fp32 rows, count the arrival; only the last
     // split of the tile goes on (and reduces every split in split order).
-    float* mine = tile_partial(unit_ks(unit));
+    float4* mine = tile_partial(unit_ks(unit));
     for (int c = 0; c < S.mma_n / 32; ++c) {
       uint32_t v[32];
       tmem_ld32(tbase + c * 32, v);
       tc_wait_ld();
 #pragma unroll
       for (int j = 0; j < 32; j += 4)
-        st_global_v4f(mine + c * 32 + j, __uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
-                      __uint_as_float(v[j + 3]));
+        mine[((c * 32 + j) >> 2) * BM] = make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                                                    __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
     }
     release_tmem();
     acc ^= 1u;
@@ -581,19 +574,22 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
     if (split) {
 #pragma unroll
       for (int j = 0; j < 64; ++j) va[j] = vu[j] = 0.0f;
+      // sum the splits in split order (the same bits whichever split arrived last);
+      // loads of one split are issued together, then added
       for (int ks = 0; ks < S.splits; ++ks) {
-        const float* src = tile_partial(ks);
+        const float4* src = tile_partial(ks);
+        float4 x[16];
 #pragma unroll
-        for (int j = 0; j < 64; j += 4) {
-          const float4 x = ld_cg_v4f(src + c * 64 + j);
-          va[j] += x.x, va[j + 1] += x.y, va[j + 2] += x.z, va[j + 3] += x.w;
-        }
+        for (int j = 0; j < 16; ++j) x[j] = __ldcg(src + ((c * 64) / 4 + j) * BM);
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          va[4 * j] += x[j].x, va[4 * j + 1] += x[j].y, va[4 * j + 2] += x[j].z, va[4 * j + 3] += x[j].w;
         if (S.epi == EPI_SWIGLU) {
 #pragma unroll
-          for (int j = 0; j < 64; j += 4) {
-            const float4 x = ld_cg_v4f(src + S.bn + c * 64 + j);
-            vu[j] += x.x, vu[j + 1] += x.y, vu[j + 2] += x.z, vu[j + 3] += x.w;
-          }
+          for (int j = 0; j < 16; ++j) x[j] = __ldcg(src + ((S.bn + c * 64) / 4 + j) * BM);
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            vu[4 * j] += x[j].x, vu[4 * j + 1] += x[j].y, vu[4 * j + 2] += x[j].z, vu[4 * j + 3] += x[j].w;
         }
       }
     } else {

@@ -117,7 +117,8 @@ typedef struct cs_chain_desc {
                           epilogue and the release.                                  */
   int prefetch;        /* L2 prefetch distance in K-slices: the scheduler warp brings
                           the weight lines (and producer A rows) that far ahead of
-                          the TMA loads into L2; 0 = auto (16), -1 = off            */
+                          the TMA loads into L2; 0 = auto (off: measured slower on
+                          GB300), -1 = off                                          */
   unsigned long long spin_timeout_ns; /* per-wait limit of a consumer tile; 0 = 2 s */
 } cs_chain_desc;
 
