@@ -81,6 +81,7 @@ def parse():
     ap.add_argument("--tile-m", type=int, default=0)
     ap.add_argument("--split-k", type=int, default=0)
     ap.add_argument("--prefetch", type=int, default=0, help="L2 prefetch distance (0 auto, -1 off)")
+    ap.add_argument("--raster", type=int, default=0, help="0 auto, 1 column-major, 2 row-major in a group")
     ap.add_argument("--quick", action="store_true", help="headline kernel only (profiling runs)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU-oracle sample time")
@@ -346,7 +347,8 @@ def main():
     def make_plan(policy, MM=M):
         d = cs.cs_chain_desc_init(kind=kind, M=MM, H=inp.H, F=inp.F, dtype=inp.dtype, policy=policy,
                                   weight_layout=lay, lag=args.lag, tile_n=args.tile_n, group_m=args.group_m,
-                                  tile_m=args.tile_m, split_k=args.split_k, prefetch=args.prefetch)
+                                  tile_m=args.tile_m, split_k=args.split_k, prefetch=args.prefetch,
+                                  raster=args.raster)
         return cs.cs_chain_plan(d)
 
     plan = make_plan(args.policy)

@@ -152,6 +152,7 @@ struct Geometry {
   int splits[3] = {1, 1, 1};
   int kps[3] = {0, 0, 0};  // K-slices per split
   int lag = 1, group_m = 1, stride = 1;
+  bool row_major = false;  // tiles of a group in row-major order
 };
 
 cs_status validate(const cs_chain_desc* d) {
@@ -164,6 +165,7 @@ cs_status validate(const cs_chain_desc* d) {
   if (d->M < 1 || d->M > 128 * 4095) return fail(CS_ERR_INVALID_ARG, "M=%d out of range [1, %d]", d->M, 128 * 4095);
   if (d->split_k < 0 || d->split_k > 15) return fail(CS_ERR_INVALID_ARG, "split_k=%d (0..15)", d->split_k);
   if (d->prefetch < -1 || d->prefetch > 64) return fail(CS_ERR_INVALID_ARG, "prefetch=%d (-1..64)", d->prefetch);
+  if (d->raster < 0 || d->raster > 2) return fail(CS_ERR_INVALID_ARG, "raster=%d (0..2)", d->raster);
   if (d->H < 8 || d->H % 8 != 0 || d->H > (1 << 20)) return fail(CS_ERR_INVALID_ARG, "H=%d must be a positive multiple of 8", d->H);
   if (d->F < 8 || d->F % 8 != 0 || d->F > (1 << 20)) return fail(CS_ERR_INVALID_ARG, "F=%d must be a positive multiple of 8", d->F);
   if (d->stride < 0) return fail(CS_ERR_INVALID_ARG, "stride=%d", d->stride);
@@ -248,7 +250,10 @@ Geometry geometry(const cs_chain_desc* d, int num_sms) {
     g.kps[s] = cdiv(g.k_iters[s], sp);
     g.splits[s] = cdiv(g.k_iters[s], g.kps[s]);  // no empty split
   }
-  g.group_m = d->group_m > 0 ? d->group_m : 8 / g.cg;
+  // at most 1024 rows per group, and at least two groups when there are two
+  // tile rows, so that the lag lets consumers of one group overlap the next
+  g.group_m = d->group_m > 0 ? d->group_m : std::max(1, std::min(8 / g.cg, g.m_tiles / 2));
+  g.row_major = d->raster == 2;
   if (g.group_m > g.m_tiles) g.group_m = g.m_tiles;
   const int groups = cdiv(g.m_tiles, g.group_m);
   g.lag = d->lag >= 0 ? d->lag : 1;
@@ -263,6 +268,20 @@ Geometry geometry(const cs_chain_desc* d, int num_sms) {
 // unit a consumer waits on (same row block, or for the attention stage every
 // earlier row block) is listed at an earlier step or earlier in the same step,
 // so a dynamic in-order dispatcher cannot deadlock.
+// Units of stage s, tile rows [m0, m1): column-major (weight tiles shared by
+// the rows of the group run together) or row-major (rows complete in turn).
+void append_group(const Geometry& g, int s, int m0, int m1, std::vector<uint32_t>& v) {
+  if (g.row_major) {
+    for (int m = m0; m < m1; ++m)
+      for (int n = 0; n < g.n_tiles[s]; ++n)
+        for (int ks = 0; ks < g.splits[s]; ++ks) v.push_back(enc_unit(s, m, n, ks));
+  } else {
+    for (int n = 0; n < g.n_tiles[s]; ++n)
+      for (int m = m0; m < m1; ++m)
+        for (int ks = 0; ks < g.splits[s]; ++ks) v.push_back(enc_unit(s, m, n, ks));
+  }
+}
+
 std::vector<uint32_t> build_fused(const Geometry& g) {
   std::vector<uint32_t> v;
   const int groups = cdiv(g.m_tiles, g.group_m);
@@ -272,9 +291,7 @@ std::vector<uint32_t> build_fused(const Geometry& g) {
       const int gg = t - s * g.lag;
       if (gg < 0 || gg >= groups) continue;
       const int m0 = gg * g.group_m, m1 = std::min(g.m_tiles, m0 + g.group_m);
-      for (int n = 0; n < g.n_tiles[s]; ++n)
-        for (int m = m0; m < m1; ++m)
-          for (int ks = 0; ks < g.splits[s]; ++ks) v.push_back(enc_unit(s, m, n, ks));
+      append_group(g, s, m0, m1, v);
     }
   return v;
 }
@@ -282,10 +299,7 @@ std::vector<uint32_t> build_fused(const Geometry& g) {
 // One stage alone (two-kernel control, standalone timings): same grouping.
 std::vector<uint32_t> build_stage(const Geometry& g, int s) {
   std::vector<uint32_t> v;
-  for (int m0 = 0; m0 < g.m_tiles; m0 += g.group_m)
-    for (int n = 0; n < g.n_tiles[s]; ++n)
-      for (int m = m0; m < std::min(g.m_tiles, m0 + g.group_m); ++m)
-        for (int ks = 0; ks < g.splits[s]; ++ks) v.push_back(enc_unit(s, m, n, ks));
+  for (int m0 = 0; m0 < g.m_tiles; m0 += g.group_m) append_group(g, s, m0, std::min(g.m_tiles, m0 + g.group_m), v);
   return v;
 }
 
@@ -649,6 +663,7 @@ cs_status cs_chain_desc_init(cs_chain_desc* d) {
   d->tile_m = 0;
   d->split_k = 0;
   d->prefetch = 0;
+  d->raster = 0;
   return CS_OK;
 }
 

@@ -101,9 +101,10 @@ typedef struct cs_chain_desc {
   int num_sms;         /* persistent grid size; 0 = every SM of the device */
   int lag;             /* schedule: producer row-block groups issued before the
                           first consumer group; -1 = auto (1)                       */
-  int group_m;         /* schedule: 128-row blocks per rasterisation group (units of
-                          a group run column-tile-major so concurrent tiles share
-                          weights in L2); 0 = auto                                  */
+  int group_m;         /* schedule: tile rows per rasterisation group (units of a
+                          group run column-tile-major so concurrent tiles share
+                          weights in L2); 0 = auto (at least two groups when the
+                          rows allow, at most 1024 rows per group)                  */
   int tile_n;          /* output columns per GEMM tile: 128 or 256; 0 = auto.
                           SwiGLU producer tiles are always 128 (gate|up = 256).     */
   int tile_m;          /* rows per GEMM tile: 128 (one SM) or 256 (a 2-SM cluster
@@ -119,6 +120,10 @@ typedef struct cs_chain_desc {
                           the weight lines (and producer A rows) that far ahead of
                           the TMA loads into L2; 0 = auto (off: measured slower on
                           GB300), -1 = off                                          */
+  int raster;          /* order of a stage's tiles inside a row group: 0 = auto
+                          (column-major), 1 = column-major (tiles sharing a weight
+                          tile run together), 2 = row-major (row blocks complete one
+                          after another, so their consumers can start sooner)      */
   unsigned long long spin_timeout_ns; /* per-wait limit of a consumer tile; 0 = 2 s */
 } cs_chain_desc;
 

@@ -44,7 +44,8 @@ def test_desc_defaults(cs):
 
 @pytest.mark.parametrize("field,value", [("M", 0), ("H", 12), ("F", 0), ("dtype", 7), ("policy", 9),
                                          ("kind", 5), ("weight_layout", 3), ("lag", -2), ("num_sms", -1),
-                                         ("split_k", 16), ("tile_n", 192), ("tile_m", 64), ("M", 128 * 4096)])
+                                         ("split_k", 16), ("tile_n", 192), ("tile_m", 64), ("M", 128 * 4096),
+                                         ("raster", 3), ("prefetch", -2)])
 def test_invalid_descs_are_rejected_without_a_gpu(cs, field, value):
     d = cs.cs_chain_desc_init(M=64, H=256, F=1024)
     setattr(d, field, value)
@@ -78,8 +79,10 @@ def _check_order(dec, deps_of):
 @pytest.mark.parametrize("M,H,F,sms,lag,group,split", [(64, 256, 1024, 148, -1, 0, 1), (2048, 12288, 6144, 148, -1, 0, 1),
                                                        (2048, 12288, 6144, 152, 0, 3, 1), (1, 12288, 6144, 148, -1, 0, 3),
                                                        (1000, 8192, 2752, 148, 2, 1, 2), (1536, 8192, 8192, 148, 5, 5, 1)])
-def test_schedule_is_dependency_ordered(cs, M, H, F, sms, lag, group, split, tile_n, tile_m):
-    d = cs.cs_chain_desc_init(M=M, H=H, F=F, lag=lag, group_m=group, tile_n=tile_n, tile_m=tile_m, split_k=split)
+@pytest.mark.parametrize("raster", [1, 2])
+def test_schedule_is_dependency_ordered(cs, M, H, F, sms, lag, group, split, tile_n, tile_m, raster):
+    d = cs.cs_chain_desc_init(M=M, H=H, F=F, lag=lag, group_m=group, tile_n=tile_n, tile_m=tile_m, split_k=split,
+                              raster=raster)
     dec = [cs.decode_unit(u) for u in cs.cs_schedule_build(d, sms)]
     m_tiles = -(-M // tile_m)
     n0, n1 = -(-F // tile_n), -(-H // tile_n)
@@ -148,6 +151,12 @@ def test_schedule_rasterises_column_major_within_a_group(cs):
     assert dec[:8] == [(0, 0, 0), (0, 1, 0), (0, 2, 0), (0, 3, 0), (0, 0, 1), (0, 1, 1), (0, 2, 1), (0, 3, 1)]
     # then the second producer group, then the first consumer group
     assert dec[192] == (0, 4, 0) and dec[384] == (1, 0, 0)
+
+
+def test_row_major_raster_completes_rows_in_turn(cs):
+    d = cs.cs_chain_desc_init(M=1024, H=12288, F=6144, group_m=4, lag=1, tile_n=256, tile_m=256, raster=2)
+    dec = [cs.decode_unit(u)[:3] for u in cs.cs_schedule_build(d, 152)]
+    assert dec[:25] == [(0, 0, n) for n in range(24)] + [(0, 1, 0)]
 
 
 def test_auto_tile_shape(cs):
