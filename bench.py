@@ -438,6 +438,8 @@ def main():
 
     if rank == 0 and not args.quick:
         line["extras"] = extras(cs, torch, inp, dev, Y, make_plan, plan, M, kind, peaks, stream)
+        if args.workload == "gpt3":
+            line["extras"]["other_configs"] = other_configs(cs, torch, peaks, lay)
         fl, rows, dt, Yref = time_cpu_oracle(inp, args.cpu_seconds)
         import oracle
         Yg = Yh[:rows] if rows <= Yh.shape[0] else Yh
@@ -520,6 +522,89 @@ def extras(cs, torch, inp, dev, Y, make_plan, plan, M, kind, peaks, stream):
         sweep.append(rec)
     out["sweep"] = sweep
     return out
+
+
+def _roof_frac(fl, by, us, peaks):
+    tc, hbm = peaks["bf16_tflops"], peaks["hbm_gbs"]
+    t_roof = max(fl / (tc * 1e12), by / (hbm * 1e9))
+    return t_roof / (us * 1e-6), ("tensor" if fl / (tc * 1e12) >= by / (hbm * 1e9) else "hbm")
+
+
+def other_configs(cs, torch, peaks, lay):
+    """The other workloads of the sweep: LLaMA SwiGLU shard and the attention chain
+    vs M (fused vs two-kernel control), and the last-wave stress sweep with every
+    policy.  Rows of each M are the first M rows of the largest draw."""
+    import cs_inputs
+    dev_of = lambda t: (t if lay == "kn" else t.t().contiguous()).cuda()  # noqa: E731
+    res = {}
+    # LLaMA 65.2B 8-way SwiGLU shard, bf16
+    inp = cs_inputs.make_inputs("llama", M=2048, seed=0)
+    d = {"X": inp.X.cuda(), "Wg": dev_of(inp.Wg), "Wu": dev_of(inp.Wu), "W2": dev_of(inp.W2)}
+    rows = []
+    for m in cs_inputs.GPT3_M_SWEEP:
+        sub = dict(d, X=d["X"][:m].contiguous())
+        Ym = torch.empty(m, inp.H, dtype=inp.dtype, device="cuda")
+        rec = {"M": m}
+        for pol in ("tile", "stream"):
+            desc = cs.cs_chain_desc_init(kind="swiglu", M=m, H=inp.H, F=inp.F, dtype=inp.dtype, policy=pol,
+                                         weight_layout=lay)
+            with cs.cs_chain_plan(desc) as p:
+                rec[f"{pol}_us"] = simple_time(lambda: cs.cs_mlp_forward(p, Y=Ym, **sub), 30) * 1e3
+        fl = chain_flops("swiglu", m, inp.H, inp.F)
+        rec["tflops"] = fl / (rec["tile_us"] * 1e-6) / 1e12
+        rec["roofline_frac"], rec["bound"] = _roof_frac(fl, chain_bytes("swiglu", m, inp.H, inp.F), rec["tile_us"], peaks)
+        rec["beats_control"] = rec["tile_us"] < rec["stream_us"]
+        rows.append(rec)
+    res["llama_swiglu"] = rows
+    del d
+    # attention chain of the GPT-3 shard (12 heads x 128, causal, seq = M), fp16
+    inp = cs_inputs.make_inputs("attn", M=2048, seed=0)
+    d = {"X": inp.X.cuda(), "Wqkv": dev_of(inp.Wqkv), "Wo": dev_of(inp.Wo)}
+    rows = []
+    for m in cs_inputs.GPT3_M_SWEEP:
+        Xm = d["X"][:m].contiguous()
+        Ym = torch.empty(m, inp.H, dtype=inp.dtype, device="cuda")
+        rec = {"M": m}
+        for pol in ("row", "stream"):
+            desc = cs.cs_chain_desc_init(kind="attn", M=m, H=inp.H, F=inp.F, heads=inp.F // 128, head_dim=128,
+                                         dtype=inp.dtype, policy=pol, weight_layout=lay)
+            with cs.cs_chain_plan(desc) as p:
+                rec[f"{pol}_us"] = simple_time(lambda: cs.cs_attn_chain_forward(p, Xm, d["Wqkv"], d["Wo"], Ym), 30) * 1e3
+        F3 = 3 * inp.F
+        fl = 2.0 * m * inp.H * F3 + 2.0 * m * inp.F * inp.H + 2.0 * m * (m + 1) * inp.F
+        by = 2 * (inp.H * F3 + inp.F * inp.H + 2 * m * inp.H + 2 * m * F3 + 2 * m * inp.F)
+        rec["tflops"] = fl / (rec["row_us"] * 1e-6) / 1e12
+        rec["roofline_frac"], rec["bound"] = _roof_frac(fl, by, rec["row_us"], peaks)
+        rec["beats_control"] = rec["row_us"] < rec["stream_us"]
+        rows.append(rec)
+    res["attention_chain"] = rows
+    del d
+    # last-wave stress sweep: two-GEMM GeLU chain, K = N = 8192, every policy
+    inp = cs_inputs.make_inputs("stress", M=1536, seed=0)
+    d = {"X": inp.X.cuda(), "W1": dev_of(inp.W1), "b1": inp.b1.cuda(), "W2": dev_of(inp.W2)}
+    rows = []
+    for m in cs_inputs.STRESS_M_SWEEP:
+        sub = dict(d, X=d["X"][:m].contiguous())
+        Ym = torch.empty(m, inp.H, dtype=inp.dtype, device="cuda")
+        rec = {"M": m}
+        for pol in ("tile", "row", "strided", "stream"):
+            desc = cs.cs_chain_desc_init(kind="gelu", M=m, H=inp.H, F=inp.F, dtype=inp.dtype, policy=pol,
+                                         weight_layout=lay)
+            with cs.cs_chain_plan(desc) as p:
+                q = cs.cs_chain_query(p)
+                rec[f"{pol}_us"] = simple_time(lambda: cs.cs_mlp_forward(p, Y=Ym, **sub), 20) * 1e3
+        workers = q["num_sms"] * 128 // q["tile_m"]
+        tiles0 = q["sched_units"][0]
+        rec["stage0_units"], rec["workers"] = tiles0, workers
+        rec["waves_remainder"] = [tiles0 // workers, tiles0 % workers]
+        fl = chain_flops("gelu", m, inp.H, inp.F)
+        best = min(rec["tile_us"], rec["row_us"], rec["strided_us"])
+        rec["tflops_tile"] = fl / (rec["tile_us"] * 1e-6) / 1e12
+        rec["roofline_frac_tile"], _ = _roof_frac(fl, chain_bytes("gelu", m, inp.H, inp.F), rec["tile_us"], peaks)
+        rec["best_policy_vs_control"] = rec["stream_us"] / best
+        rows.append(rec)
+    res["stress"] = rows
+    return res
 
 
 if __name__ == "__main__":
