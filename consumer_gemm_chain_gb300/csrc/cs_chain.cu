@@ -224,13 +224,18 @@ Geometry geometry(const cs_chain_desc* d, int num_sms) {
     g.k_iters[1] = cdiv(d->F, cs::BK);
   }
   // K-splits: a stage with fewer tiles than CTAs (small M) splits K so that
-  // enough SMs stream its weights; at least 8 K-slices per split.
+  // enough SMs stream its weights (an explicit split_k: at least 8 K-slices each).
   const int capacity = num_sms / g.cg;
   for (int s = 0; s < g.stages; ++s) {
     g.splits[s] = 1;
     if (d->kind == CS_CHAIN_ATTN && s == 1) continue;  // attention units do not split
     const int tiles = g.m_tiles * g.n_tiles[s];
-    const int max_sp = std::max(1, std::min(15, g.k_iters[s] / 8));
+    // auto, several row blocks: at most 4 splits of at least 32 K-slices
+    // (measured: finer splits make the last split's reduction and the partial
+    // traffic dominate); one row block streams weights only and takes up to 15
+    const bool wide = d->split_k > 0 || g.m_tiles == 1;
+    const int max_sp = wide ? std::max(1, std::min(15, g.k_iters[s] / 8))
+                            : std::max(1, std::min(4, g.k_iters[s] / 32));
     int sp = d->split_k;
     if (sp == 0) {
       // fewest (waves x K-slices per split): a split count that fills whole

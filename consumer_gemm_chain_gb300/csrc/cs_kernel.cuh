@@ -311,6 +311,19 @@ __device__ __forceinline__ bool tma_wait_ready(SmemCtl<NS>* sc, uint32_t q, int 
   }
 }
 
+// TMA thread, out of line: wait until slice kb of a consumer unit may load
+// (the scheduler has published at least kb * BK / dep_bn + 1 complete
+// producer tiles) and return the first slice that is not yet known to be
+// loadable, or -1 after an abort or a watchdog timeout.  Kept out of the K
+// loop so that the loop itself carries only one integer compare.
+template <int NS>
+__device__ __noinline__ int tma_wait_slices(SmemCtl<NS>* sc, uint32_t q, int kb, int dep_bn, const KParams& p) {
+  int ready = 0;
+  if (!tma_wait_ready(sc, q, (kb * BK) / dep_bn + 1, ready, p)) return -1;
+  const long long lim = (static_cast<long long>(ready) * dep_bn + BK - 1) / BK;
+  return lim > 0x7FFFFFFFLL ? 0x7FFFFFFF : static_cast<int>(lim);
+}
+
 // ---------------------------------------------------------------- TMA role
 template <int NS, int STAGE_BYTES, int CG>
 __device__ bool tma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, RingPos& rp, uint32_t unit,
@@ -326,10 +339,13 @@ __device__ bool tma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
   const int row0 = (m * CG + static_cast<int>(rank)) * BM;  // this CTA's A rows
   const int bcols = S.bn / CG;                               // this CTA's share of B's columns
   const int col0 = n * S.bn + static_cast<int>(rank) * bcols;
-  int ready = 0;
+  int ready_kb = do_wait ? kb0 : kb1;  // slices below this bound may load now
   for (int kb = kb0; kb < kb1; ++kb) {
     if (rank == 0 && kb == claim_at) mbar_arrive(&sc->claim_req);
-    if (do_wait && !tma_wait_ready(sc, q, (kb * BK) / S.dep_bn + 1, ready, p)) return false;
+    if (kb >= ready_kb) {
+      ready_kb = tma_wait_slices(sc, q, kb, S.dep_bn, p);
+      if (ready_kb < 0) return false;
+    }
     if (!wait_bar(&sc->empty[rp.slot], rp.phase ^ 1u, sc, p, 1)) return false;
     uint8_t* sa = ring + rp.slot * STAGE_BYTES;
     uint8_t* sb = sa + TILE_A_BYTES;
@@ -503,6 +519,50 @@ __device__ void release_tile(const KParams& p, const StageP& S, int mb, int n, i
   }
 }
 
+// K-split reduction for a row block with few valid rows (R <= 32; from 64 rows
+// on, the row-per-thread path measured faster): the 128 epilogue threads share
+// the (row, 4-column group) elements of `np` 64-column parts and fetch every
+// split of an element at once; each element is summed in
+// split order (the same order as the row-per-thread path, so the same bits) and
+// written to the staging buffer as fp32 [part][row][16 float4], the float4 of
+// column group g of row r at slot g ^ (r & 15).  `col4[pp]` is the partial
+// tile's first 4-column group of part pp.  EB elements x KSB splits = 16 loads
+// in flight per thread.  Split ks's tile starts at tile0 + ks * kstride.
+template <int EB, int KSB>
+__device__ __forceinline__ void split_reduce_small(const StageP& S, const float4* tile0, size_t kstride, int R,
+                                                   int np, const int (&col4)[2], float4* sm) {
+  const int E = np * R * 16;
+  const int tid = threadIdx.x - EPI_WARP0 * 32;
+#pragma unroll 1
+  for (int base = tid; base < E; base += EPI_THREADS * EB) {
+    float4 x[EB][KSB];
+#pragma unroll
+    for (int u = 0; u < EB; ++u) {
+      const int e = base + u * EPI_THREADS;
+      // element e -> part pp, column group g, row r (rows fastest: coalesced)
+      const int pp = e / (R * 16), rem = e - pp * R * 16;
+      const int g = rem / R, r = rem - g * R;
+#pragma unroll
+      for (int ks = 0; ks < KSB; ++ks)
+        x[u][ks] = (e < E && ks < S.splits) ? __ldcg(tile0 + ks * kstride + (col4[pp & 1] + g) * BM + r)
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < EB; ++u) {
+      const int e = base + u * EPI_THREADS;
+      if (e < E) {
+        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int ks = 0; ks < KSB; ++ks)
+          if (ks < S.splits) s.x += x[u][ks].x, s.y += x[u][ks].y, s.z += x[u][ks].z, s.w += x[u][ks].w;
+        const int pp = e / (R * 16), rem = e - pp * R * 16;
+        const int g = rem / R, r = rem - g * R;
+        sm[(pp * R + r) * 16 + (g ^ (r & 15))] = s;
+      }
+    }
+  }
+}
+
 template <int NS, int CG>
 __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* staging, uint32_t unit, uint32_t& acc,
                               uint32_t& acc_phase, int& last_buf, uint32_t rank, uint32_t tidx, uint32_t epoch1) {
@@ -519,6 +579,8 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
       sc->tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * static_cast<uint32_t>(p.acc_stride);
   const int nchunks = S.bn / 64;
   const bool split = S.splits > 1;
+  // rows of this block inside the output (the last block may be ragged)
+  const int rows_valid = max(0, min(BM, S.m_extent - mb * BM));
   const size_t tile_floats = static_cast<size_t>(BM) * S.mma_n;
   // Partial tiles are stored [mma_n/4][128 rows][4 columns]: the float4 of
   // columns 4c..4c+3 of this thread's row sits at (c * 128 + row), so a warp
@@ -546,10 +608,12 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
       uint32_t v[32];
       tmem_ld32(tbase + c * 32, v);
       tc_wait_ld();
+      if (row < rows_valid) {
 #pragma unroll
-      for (int j = 0; j < 32; j += 4)
-        mine[((c * 32 + j) >> 2) * BM] = make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
-                                                    __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+        for (int j = 0; j < 32; j += 4)
+          mine[((c * 32 + j) >> 2) * BM] = make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                                                      __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+      }
     }
     release_tmem();
     acc ^= 1u;
@@ -571,12 +635,46 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
 #pragma unroll 1
   for (int c = 0; c < nchunks; ++c) {
     float va[64], vu[64];
-    if (split) {
+    if (split && rows_valid <= 32) {
+      // every store still reading the staging buffer is done before it is reused
+      if (lane == 0) tma_store_wait_read<0>();
+      last_buf = -1;
+      named_bar_sync(1, EPI_THREADS);
+      const float4* tile0 = tile_partial(0) - row;
+      const size_t kstride = static_cast<size_t>(S.m_blocks) * S.n_tiles * (tile_floats / 4);
+      const int np = S.epi == EPI_SWIGLU ? 2 : 1;
+      const int col4[2] = {(c * 64) / 4, (S.bn + c * 64) / 4};
+      float4* sm = reinterpret_cast<float4*>(staging);
+      if (S.splits <= 2)
+        split_reduce_small<8, 2>(S, tile0, kstride, rows_valid, np, col4, sm);
+      else if (S.splits <= 4)
+        split_reduce_small<4, 4>(S, tile0, kstride, rows_valid, np, col4, sm);
+      else if (S.splits <= 8)
+        split_reduce_small<2, 8>(S, tile0, kstride, rows_valid, np, col4, sm);
+      else
+        split_reduce_small<1, 16>(S, tile0, kstride, rows_valid, np, col4, sm);
+      named_bar_sync(1, EPI_THREADS);
+#pragma unroll
+      for (int j = 0; j < 64; ++j) va[j] = vu[j] = 0.0f;
+      if (row < rows_valid) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float4 a = sm[row * 16 + (j ^ (row & 15))];
+          va[4 * j] = a.x, va[4 * j + 1] = a.y, va[4 * j + 2] = a.z, va[4 * j + 3] = a.w;
+          if (S.epi == EPI_SWIGLU) {
+            const float4 b = sm[(rows_valid + row) * 16 + (j ^ (row & 15))];
+            vu[4 * j] = b.x, vu[4 * j + 1] = b.y, vu[4 * j + 2] = b.z, vu[4 * j + 3] = b.w;
+          }
+        }
+      }
+      // the sums are in registers; the staging buffer is free for the output rows
+      named_bar_sync(1, EPI_THREADS);
+    } else if (split) {
 #pragma unroll
       for (int j = 0; j < 64; ++j) va[j] = vu[j] = 0.0f;
       // sum the splits in split order (the same bits whichever split arrived last);
       // loads of one split are issued together, then added
-      for (int ks = 0; ks < S.splits; ++ks) {
+      for (int ks = 0; ks < S.splits && row < rows_valid; ++ks) {
         const float4* src = tile_partial(ks);
         float4 x[16];
 #pragma unroll

@@ -232,6 +232,36 @@ def test_split_k_parity(M, H, F, tile_m, tile_n, split):
     assert torch.equal(Y1, Y2)  # fixed split order: the same bits every time
 
 
+@pytest.mark.parametrize("kind,M,H,F,split", [
+    ("gelu", 24, 8192, 256, 12),    # cooperative reduction, 9..15 splits
+    ("gelu", 32, 4096, 512, 7),     # cooperative, 5..8 splits, 32 valid rows
+    ("gelu", 1, 2048, 384, 3),      # cooperative, a single row
+    ("gelu", 17, 2048, 384, 2),     # cooperative, two splits
+    ("gelu", 40, 8192, 256, 12),    # row per thread over 40 valid rows
+    ("swiglu", 32, 2048, 256, 3),   # cooperative, gate and up parts
+    ("swiglu", 33, 4096, 344, 6),   # row per thread, ragged F
+    ("swiglu", 64, 2048, 256, 3),   # row per thread, 64 valid rows
+    ("swiglu", 130, 2048, 256, 2),  # a full row block, then a cooperative block of 2 rows
+])
+def test_split_k_few_valid_rows(kind, M, H, F, split):
+    """Ragged row blocks: partials are written for the valid rows only, and a
+    block of at most 32 valid rows reduces its K-splits cooperatively (every
+    epilogue thread fetches elements of every split); the result matches the
+    oracle and is the same bits on every call."""
+    inp = cs_inputs.make_custom(kind, M, H, F, dtype=torch.bfloat16, seed=54)
+    dev = device_tensors(inp, "nk")
+    with plan_for(inp, "tile", "nk", split_k=split) as plan:
+        q = cs.cs_chain_query(plan)
+        assert q["split_k"][0] == split
+        Y1 = forward(plan, dev).cpu()
+        H1 = intermediate(plan, 0, inp.M, inp.F, inp.dtype).cpu()
+        Y2 = forward(plan, dev).cpu()
+    Yref, Href = _oracle(inp)
+    assert oracle.rel_err(H1, Href) <= TOL
+    assert oracle.rel_err(Y1, Yref) <= TOL
+    assert torch.equal(Y1, Y2)
+
+
 def test_split_k_swiglu_and_policies():
     inp = cs_inputs.make_custom("swiglu", 100, 1024, 688, dtype=torch.bfloat16, seed=52)
     dev = device_tensors(inp, "nk")
