@@ -82,6 +82,7 @@ def parse():
     ap.add_argument("--split-k", type=int, default=0)
     ap.add_argument("--prefetch", type=int, default=0, help="L2 prefetch distance (0 auto, -1 off)")
     ap.add_argument("--raster", type=int, default=0, help="0 auto, 1 column-major, 2 row-major in a group")
+    ap.add_argument("--pdl", type=int, default=0, help="programmatic dependent launch: 0 auto (on), 1 on, -1 off")
     ap.add_argument("--quick", action="store_true", help="headline kernel only (profiling runs)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU-oracle sample time")
@@ -344,11 +345,11 @@ def main():
         dev.update(Wg=w(inp.Wg), Wu=w(inp.Wu), W2=w(inp.W2))
     Y = torch.empty_like(X)
 
-    def make_plan(policy, MM=M):
+    def make_plan(policy, MM=M, pdl=None):
         d = cs.cs_chain_desc_init(kind=kind, M=MM, H=inp.H, F=inp.F, dtype=inp.dtype, policy=policy,
                                   weight_layout=lay, lag=args.lag, tile_n=args.tile_n, group_m=args.group_m,
                                   tile_m=args.tile_m, split_k=args.split_k, prefetch=args.prefetch,
-                                  raster=args.raster)
+                                  raster=args.raster, pdl=args.pdl if pdl is None else pdl)
         return cs.cs_chain_plan(d)
 
     plan = make_plan(args.policy)
@@ -414,7 +415,7 @@ def main():
         "vs_baseline": None, "dtype": "f16" if inp.dtype == torch.float16 else "bf16", "data": "synthetic",
         "config": dict(workload_config(args.workload, M, inp, args.policy, lay), parallelism=f"replicas{ws}",
                        tile_n=plan_info["tile_n"][:2], tile_m=plan_info["tile_m"], group_m=plan_info["group_m"],
-                       lag=plan_info["lag"],
+                       lag=plan_info["lag"], pdl=args.pdl >= 0,
                        grid=plan_info["num_sms"]),
         "roofline": roof, "gpu_launches": args.steps * launches_per_step,
     }
@@ -464,6 +465,11 @@ def extras(cs, torch, inp, dev, Y, make_plan, plan, M, kind, peaks, stream):
     for pol in ("row", "strided", "stream"):
         with make_plan(pol) as p:
             out[f"{pol}_ms"] = simple_time(lambda: fwd(p), 50)
+    # without programmatic dependent launch: each launch waits for the previous
+    # grid to finish before its CTAs start (the plain two-stream-kernel control)
+    for pol in ("tile", "stream"):
+        with make_plan(pol, pdl=-1) as p:
+            out[f"{'chain' if pol == 'tile' else pol}_nopdl_ms"] = simple_time(lambda: fwd(p), 50)
     # control captured in a CUDA graph (launch cost amortised)
     with make_plan("stream") as pc:
         fwd(pc)
@@ -508,10 +514,10 @@ def extras(cs, torch, inp, dev, Y, make_plan, plan, M, kind, peaks, stream):
         sub = {k: (v[:m].contiguous() if k == "X" else v) for k, v in dev.items()}
         Ym = torch.empty(m, inp.H, dtype=inp.dtype, device=X.device)
         rec = {"M": m}
-        for pol in ("tile", "stream"):
-            with make_plan(pol, m) as p:
+        for pol, pdl, key in (("tile", None, "tile"), ("stream", None, "stream"), ("stream", -1, "stream_nopdl")):
+            with make_plan(pol, m, pdl) as p:
                 ms = simple_time(lambda: cs.cs_mlp_forward(p, Y=Ym, **sub), 30)
-            rec[f"{pol}_us"] = ms * 1e3
+            rec[f"{key}_us"] = ms * 1e3
         fl = chain_flops(kind, m, inp.H, inp.F)
         by = chain_bytes(kind, m, inp.H, inp.F)
         roof_ms = max(fl / (tc * 1e12), by / (hbm * 1e9)) * 1e3

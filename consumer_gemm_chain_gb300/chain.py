@@ -47,7 +47,8 @@ class cs_chain_desc(ctypes.Structure):
                 ("stride", ctypes.c_int), ("heads", ctypes.c_int), ("head_dim", ctypes.c_int),
                 ("num_sms", ctypes.c_int), ("lag", ctypes.c_int), ("group_m", ctypes.c_int),
                 ("tile_n", ctypes.c_int), ("tile_m", ctypes.c_int), ("split_k", ctypes.c_int),
-                ("prefetch", ctypes.c_int), ("raster", ctypes.c_int), ("spin_timeout_ns", ctypes.c_ulonglong)]
+                ("prefetch", ctypes.c_int), ("raster", ctypes.c_int), ("pdl", ctypes.c_int),
+                ("spin_timeout_ns", ctypes.c_ulonglong)]
 
 
 class cs_mlp_args(ctypes.Structure):

@@ -166,6 +166,7 @@ cs_status validate(const cs_chain_desc* d) {
   if (d->split_k < 0 || d->split_k > 15) return fail(CS_ERR_INVALID_ARG, "split_k=%d (0..15)", d->split_k);
   if (d->prefetch < -1 || d->prefetch > 64) return fail(CS_ERR_INVALID_ARG, "prefetch=%d (-1..64)", d->prefetch);
   if (d->raster < 0 || d->raster > 2) return fail(CS_ERR_INVALID_ARG, "raster=%d (0..2)", d->raster);
+  if (d->pdl < -1 || d->pdl > 1) return fail(CS_ERR_INVALID_ARG, "pdl=%d (-1..1)", d->pdl);
   if (d->H < 8 || d->H % 8 != 0 || d->H > (1 << 20)) return fail(CS_ERR_INVALID_ARG, "H=%d must be a positive multiple of 8", d->H);
   if (d->F < 8 || d->F % 8 != 0 || d->F > (1 << 20)) return fail(CS_ERR_INVALID_ARG, "F=%d must be a positive multiple of 8", d->F);
   if (d->stride < 0) return fail(CS_ERR_INVALID_ARG, "stride=%d", d->stride);
@@ -498,15 +499,24 @@ cs_status launch(cs_chain_s* p, cs::KParams& kp, const uint32_t* sched, int n_un
   cfg.blockDim = dim3(cs::NUM_THREADS);
   cfg.dynamicSmemBytes = p->smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
+  unsigned n_attr = 0;
   if (p->cg == 2) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[n_attr].id = cudaLaunchAttributeClusterDimension;
+    attr[n_attr].val.clusterDim.x = 2;
+    attr[n_attr].val.clusterDim.y = 1;
+    attr[n_attr].val.clusterDim.z = 1;
+    ++n_attr;
   }
+  if (p->d.pdl >= 0) {
+    // the kernel waits for the preceding grid (griddepcontrol.wait) before it
+    // touches global memory, so it may be scheduled while that grid drains
+    attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n_attr].val.programmaticStreamSerializationAllowed = 1;
+    ++n_attr;
+  }
+  cfg.attrs = n_attr ? attr : nullptr;
+  cfg.numAttrs = n_attr;
   cudaError_t e;
   cs_status s;
   if (p->d.kind == CS_CHAIN_ATTN) {
@@ -671,6 +681,7 @@ cs_status cs_chain_desc_init(cs_chain_desc* d) {
   d->split_k = 0;
   d->prefetch = 0;
   d->raster = 0;
+  d->pdl = 0;
   return CS_OK;
 }
 

@@ -221,15 +221,21 @@ struct RingPos {
 // publish, in sc->uq_ready[q], how many leading dependency items are complete.
 // Items are producer column tiles 0..dep_ntiles-1 of 128-row block m, in the
 // order the consumer's K-loop reads them: TILE publishes the first incomplete
-// tile; ROW publishes 0 until the row counter is complete, then dep_ntiles;
-// STRIDED publishes the smallest residue class (mod stride) with an incomplete
-// tile.  Flags are read with relaxed loads (32 lanes in parallel) and each
-// observing lane fences (acquire pattern) before the CTA-scope release.
+// tile of the unit's own K range (the tiles before that range count as
+// complete: a K-split reads none of them); ROW publishes 0 until the row
+// counter is complete, then dep_ntiles; STRIDED publishes the smallest residue
+// class (mod stride) with an incomplete tile.  Flags are read with relaxed
+// loads (32 lanes in parallel) and each observing lane fences (acquire
+// pattern) before the CTA-scope release.
 template <int NS>
 __device__ void sched_poll_gemm(const KParams& p, const StageP& S, SmemCtl<NS>* sc, uint32_t q, int m,
                                 uint32_t epoch1, uint32_t unit, int lane) {
   const uint32_t* tiles = S.dep_tile + static_cast<size_t>(m) * S.dep_ntiles;
-  const int nt = S.dep_ntiles;
+  const int kb0 = unit_ks(unit) * S.kps;
+  const int kb1 = min(S.k_iters, kb0 + S.kps);
+  // TILE: the unit reads producer tiles [i0, i1)
+  const int i0 = S.wait == WAIT_TILE ? (kb0 * BK) / S.dep_bn : 0;
+  const int nt = S.wait == WAIT_TILE ? min(S.dep_ntiles, ((kb1 - 1) * BK) / S.dep_bn + 1) : S.dep_ntiles;
   int published = 0;
   const uint64_t t0 = globaltimer();
   uint32_t ns = 64;
@@ -241,7 +247,7 @@ __device__ void sched_poll_gemm(const KParams& p, const StageP& S, SmemCtl<NS>* 
       ready = static_cast<int32_t>(v - epoch1 * static_cast<uint32_t>(nt)) >= 0 ? nt : 0;
     } else {
       ready = nt;
-      for (int base = 0; base < nt; base += 32) {
+      for (int base = i0; base < nt; base += 32) {
         const int t = base + lane;
         const bool done = t >= nt || static_cast<int32_t>(ld_relaxed_gpu(tiles + t) - epoch1) >= 0;
         const uint32_t bad = __ballot_sync(0xFFFFFFFFu, !done);
@@ -1176,6 +1182,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
   __syncthreads();
   if constexpr (CG == 2) cluster_sync();  // the peer's barriers exist before anyone arrives on them
   tc_fence_after();
+  // Everything above touched only this CTA's shared and tensor memory.  Under a
+  // programmatic dependent launch the grid queued before this one may still be
+  // running: global memory (counters, inputs, outputs) waits for its completion.
+  // The next forward may then be scheduled; its CTAs take an SM only when one of
+  // this grid's CTAs has left it (each CTA needs most of an SM's shared memory).
+  grid_dep_wait();
+  grid_dep_launch_dependents();
 
   const uint32_t epoch1 = p.ctrl[CTRL_EPOCH] + 1u;
 

@@ -42,7 +42,7 @@
 extern "C" {
 #endif
 
-#define CS_ABI_VERSION 1
+#define CS_ABI_VERSION 2
 
 typedef struct cs_chain_s* cs_chain_t;
 
@@ -124,6 +124,12 @@ typedef struct cs_chain_desc {
                           (column-major), 1 = column-major (tiles sharing a weight
                           tile run together), 2 = row-major (row blocks complete one
                           after another, so their consumers can start sooner)      */
+  int pdl;             /* programmatic dependent launch: a forward queued behind another
+                          kernel on the stream starts its CTAs as the earlier grid's
+                          CTAs exit, and sets up its barriers and tensor memory while
+                          the earlier grid drains; it reads global memory only after
+                          that grid has completed (griddepcontrol.wait).  0 = auto
+                          (on), 1 = on, -1 = off (plain stream order)               */
   unsigned long long spin_timeout_ns; /* per-wait limit of a consumer tile; 0 = 2 s */
 } cs_chain_desc;
 

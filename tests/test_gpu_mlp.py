@@ -285,3 +285,48 @@ def test_split_k_delay_injection_never_changes_a_bit():
             g = torch.Generator().manual_seed(300 + seed)
             cs.cs_chain_debug_set_delays(plan, 0, (torch.rand(q["units"][0], generator=g) * 100_000).long().tolist())
             assert torch.equal(forward(plan, dev).cpu(), ref), seed
+
+
+@pytest.mark.parametrize("policy", ["tile", "stream"])
+def test_back_to_back_forwards_with_programmatic_launch(policy):
+    """Forwards queued back to back (each one's output is the next one's input,
+    no host synchronisation in between) give the same bits with programmatic
+    dependent launch on and off: a grid reads global memory only after the
+    grid before it has completed."""
+    inp = cs_inputs.make_custom("gelu", 300, 1024, 768, seed=55)
+    dev = device_tensors(inp, "nk")
+    outs = {}
+    for pdl in (1, -1):
+        with plan_for(inp, policy, "nk", pdl=pdl) as plan:
+            xs = [dev["X"].clone()]
+            for _ in range(4):
+                Y = torch.empty_like(xs[-1])
+                cs.cs_mlp_forward(plan, X=xs[-1], W1=dev["W1"], b1=dev["b1"], W2=dev["W2"], Y=Y)
+                xs.append(Y)
+            torch.cuda.synchronize()
+            assert cs.cs_chain_status(plan) == cs.CS_OK
+            outs[pdl] = [x.cpu() for x in xs[1:]]
+    Yref, _ = _oracle(inp)
+    assert oracle.rel_err(outs[1][0], Yref) <= TOL
+    for a, b in zip(outs[1], outs[-1]):
+        assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("kind,split", [("gelu", 2), ("gelu", 3), ("swiglu", 2)])
+def test_split_consumers_wait_for_their_own_producer_tiles(kind, split):
+    """A K-split consumer waits only for the producer tiles of its own K range.
+    The intermediate still holds the previous input's values, so a consumer
+    that read a tile too early would mix them in: with every producer delayed,
+    the second input's output must equal an undelayed run of it."""
+    a = cs_inputs.make_custom(kind, 64, 2048, 1536, seed=56)
+    b = cs_inputs.make_custom(kind, 64, 2048, 1536, seed=57)
+    dev_a = device_tensors(a, "nk")
+    with plan_for(a, "tile", "nk", split_k=split) as plan:
+        q = cs.cs_chain_query(plan)
+        assert q["split_k"][0] == split and q["split_k"][1] == split
+        clean_b = forward(plan, dict(dev_a, X=b.X.cuda())).cpu()
+        forward(plan, dev_a)
+        g = torch.Generator().manual_seed(58)
+        cs.cs_chain_debug_set_delays(plan, 0, (torch.rand(q["units"][0], generator=g) * 300_000).long().tolist())
+        delayed_b = forward(plan, dict(dev_a, X=b.X.cuda())).cpu()
+    assert torch.equal(delayed_b, clean_b)
