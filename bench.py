@@ -332,6 +332,9 @@ def main():
     inp = cs_inputs.make_inputs(args.workload, M=M, seed=0)
     kind = inp.kind
     lay = args.layout
+    if ws > 1 and args.tile_m in (0, 512):
+        # cluster multicast stays in single-GPU runs: several ranks use 2-SM pairs
+        args.tile_m = 256 if (kind == "gelu" and M >= 1024) else 128
 
     def w(t):
         t = t if lay == "kn" else t.t().contiguous()
@@ -402,7 +405,8 @@ def main():
         roof = {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak}
     traffic_key = f"{args.workload}_M{M}_{args.policy}_{lay}"
     roof.update({"traffic": measured_traffic(traffic_key), "peak_source": f"{peak_src} ({'sustained' if sustained else 'burst'})",
-                 "kernel": ("cs_chain_kernel<6,32768,2>" if plan_info["tile_m"] == 256 else
+                 "kernel": ("cs_chain_kernel<6,32768,2,0,4> (4-CTA clusters)" if plan_info["tile_m"] == 512 else
+                            "cs_chain_kernel<6,32768,2>" if plan_info["tile_m"] == 256 else
                             "cs_chain_kernel<4,49152,1>" if (kind == "swiglu" or 256 in plan_info["tile_n"])
                             else "cs_chain_kernel<6,32768,1>"),
                  "algorithmic_flops_per_launch": flops if launches_per_step == 1 else None,

@@ -70,7 +70,8 @@ struct cs_chain_s {
   int stride = 1;
   int bn[3] = {128, 128, 128};
   int cfg_b = 0;  // 1: 48 KB-stage kernel (256-wide one-SM tiles or gate|up)
-  int cg = 1;     // CTAs per tile (2: 256-row tiles on a 2-SM cluster)
+  int cg = 1;     // CTAs per tcgen05 MMA (2: 256-row tiles on a 2-SM pair)
+  int cl = 1;     // CTAs per unit and cluster (4: two pairs sharing weight boxes)
   int m_units = 0;   // tile rows of the schedule
   int m_blocks = 0;  // 128-row blocks (semaphore rows)
   int sched_units[3] = {0, 0, 0};
@@ -144,7 +145,8 @@ inline uint32_t enc_unit(int s, int m, int n, int ks) {
 // Geometry shared by the host-only schedule builder and the plan.
 struct Geometry {
   int stages = 0, m_tiles = 0;  // m_tiles: tile rows (tile_m each)
-  int cg = 1;                   // CTAs per tile
+  int cg = 1;                   // CTAs per MMA
+  int cl = 1;                   // CTAs per unit (128-row blocks per tile row)
   int m_blocks = 0;             // 128-row blocks
   int n_tiles[3] = {0, 0, 0};
   int k_iters[3] = {0, 0, 0};
@@ -175,15 +177,15 @@ cs_status validate(const cs_chain_desc* d) {
   if (d->group_m < 0) return fail(CS_ERR_INVALID_ARG, "group_m=%d", d->group_m);
   if (d->tile_n != 0 && d->tile_n != 128 && d->tile_n != 256)
     return fail(CS_ERR_INVALID_ARG, "tile_n=%d (0, 128 or 256)", d->tile_n);
-  if (d->tile_m != 0 && d->tile_m != 128 && d->tile_m != 256)
-    return fail(CS_ERR_INVALID_ARG, "tile_m=%d (0, 128 or 256)", d->tile_m);
-  if (d->tile_m == 256 && (d->tile_n == 128 || d->kind != CS_CHAIN_MLP_GELU))
-    return fail(CS_ERR_UNSUPPORTED, "tile_m=256 is built for 256-wide GeLU-MLP tiles only");
+  if (d->tile_m != 0 && d->tile_m != 128 && d->tile_m != 256 && d->tile_m != 512)
+    return fail(CS_ERR_INVALID_ARG, "tile_m=%d (0, 128, 256 or 512)", d->tile_m);
+  if (d->tile_m >= 256 && (d->tile_n == 128 || d->kind != CS_CHAIN_MLP_GELU))
+    return fail(CS_ERR_UNSUPPORTED, "tile_m=%d is built for 256-wide GeLU-MLP tiles only", d->tile_m);
   if (d->kind == CS_CHAIN_ATTN) {
     if (d->head_dim != 128) return fail(CS_ERR_UNSUPPORTED, "head_dim=%d (only 128 is built)", d->head_dim);
     if (d->heads < 1 || d->heads * d->head_dim != d->F)
       return fail(CS_ERR_INVALID_ARG, "ATTN needs F == heads*head_dim (F=%d heads=%d)", d->F, d->heads);
-    if (d->tile_n == 256 || d->tile_m == 256)
+    if (d->tile_n == 256 || d->tile_m >= 256)
       return fail(CS_ERR_UNSUPPORTED, "the attention chain runs 128 x 128 tiles only");
   }
   return CS_OK;
@@ -199,12 +201,22 @@ Geometry geometry(const cs_chain_desc* d, int num_sms) {
   // attention units keep S and O in TMEM next to the two 128-column accumulators
   if (d->kind == CS_CHAIN_ATTN) tn = 128;
   // A 2-SM pair per 256 x 256 tile halves them again (each SM loads half of B).
+  // Two pairs of a 4-CTA cluster (512 rows) fetch each weight box once for
+  // both (multicast): chosen when they add no padding over 256-row pairs.
   int tm = d->tile_m;
-  if (tm == 0) tm = (tn == 256 && d->kind == CS_CHAIN_MLP_GELU && blocks >= 8) ? 256 : 128;
-  if (tm == 256 && (tn != 256 || d->kind != CS_CHAIN_MLP_GELU)) tm = 128;
-  g.cg = tm / cs::BM;
+  if (tm == 0) {
+    const bool wide_gelu = tn == 256 && d->kind == CS_CHAIN_MLP_GELU;
+    tm = (wide_gelu && blocks >= 4 && 2 * cdiv(d->M, 512) == cdiv(d->M, 256)) ? 512
+         : (wide_gelu && blocks >= 8)                                        ? 256
+                                                                             : 128;
+  }
+  if (tm >= 256 && (tn != 256 || d->kind != CS_CHAIN_MLP_GELU)) tm = 128;
+  // 512-row tiles: two 2-SM pairs of one 4-CTA cluster on consecutive 256-row
+  // blocks; each weight box is fetched once and multicast to both pairs
+  g.cg = tm >= 256 ? 2 : 1;
+  g.cl = tm / cs::BM;
   g.m_tiles = cdiv(d->M, tm);
-  g.m_blocks = g.m_tiles * g.cg;
+  g.m_blocks = g.m_tiles * g.cl;
   if (d->kind == CS_CHAIN_ATTN) {
     g.stages = 3;
     g.bn[0] = 128;
@@ -226,7 +238,7 @@ Geometry geometry(const cs_chain_desc* d, int num_sms) {
   }
   // K-splits: a stage with fewer tiles than CTAs (small M) splits K so that
   // enough SMs stream its weights (an explicit split_k: at least 8 K-slices each).
-  const int capacity = num_sms / g.cg;
+  const int capacity = num_sms / g.cl;
   for (int s = 0; s < g.stages; ++s) {
     g.splits[s] = 1;
     if (d->kind == CS_CHAIN_ATTN && s == 1) continue;  // attention units do not split
@@ -234,7 +246,7 @@ Geometry geometry(const cs_chain_desc* d, int num_sms) {
     // auto, several row blocks: at most 4 splits of at least 32 K-slices
     // (measured: finer splits make the last split's reduction and the partial
     // traffic dominate); one row block streams weights only and takes up to 15
-    const bool wide = d->split_k > 0 || g.m_tiles == 1;
+    const bool wide = d->split_k > 0 || g.m_blocks == 1;
     const int max_sp = wide ? std::max(1, std::min(15, g.k_iters[s] / 8))
                             : std::max(1, std::min(4, g.k_iters[s] / 32));
     int sp = d->split_k;
@@ -258,9 +270,13 @@ Geometry geometry(const cs_chain_desc* d, int num_sms) {
   }
   // at most 1024 rows per group; with 256-row pair tiles also at least two
   // groups, so that the lag lets the consumers of one group overlap the next
-  // (measured: M=1024 pairs 0.61 -> 0.67 of peak; single-SM tiles prefer one group)
+  // (measured: M=1024 pairs 0.61 -> 0.67 of peak; single-SM tiles prefer one
+  // group); 512-row tiles: one group up to 1024 rows, else groups of 1024
+  // (measured at GPT-3 M=1024: 209 us in one group, 225 us in two)
   g.group_m = d->group_m > 0 ? d->group_m
-                             : (g.cg == 2 ? std::max(1, std::min(4, g.m_tiles / 2)) : 8);
+             : g.cl == 4   ? (g.m_tiles <= 2 ? 1 : 2)
+             : g.cg == 2   ? std::max(1, std::min(4, g.m_tiles / 2))
+                           : 8;
   g.row_major = d->raster == 2;
   if (g.group_m > g.m_tiles) g.group_m = g.m_tiles;
   const int groups = cdiv(g.m_tiles, g.group_m);
@@ -320,9 +336,9 @@ int device_sms(int* out) {
   return dev;
 }
 
-template <int NS, int SB, int CG, bool ATTN>
+template <int NS, int SB, int CG, bool ATTN, int CL = CG>
 cs_status set_smem_attr() {
-  static cudaError_t once = cudaFuncSetAttribute(cs::cs_chain_kernel<NS, SB, CG, ATTN>,
+  static cudaError_t once = cudaFuncSetAttribute(cs::cs_chain_kernel<NS, SB, CG, ATTN, CL>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes_for<NS, SB>());
   if (once != cudaSuccess) return fail(CS_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(once));
   return CS_OK;
@@ -489,11 +505,11 @@ void fill_mlp_stages(const cs_chain_s* p, const cs_mlp_args* a, cs::KParams& kp)
 cs_status launch(cs_chain_s* p, cs::KParams& kp, const uint32_t* sched, int n_units, cudaStream_t stream) {
   kp.sched = sched;
   kp.n_units = n_units;
-  // one CTA (or CTA pair) per SM; no more than there are units
-  int grid = p->num_sms / p->cg;
+  // one CTA per SM, clusters of cl CTAs per unit; no more clusters than units
+  int grid = p->num_sms / p->cl;
   if (grid > n_units) grid = n_units;
   if (grid < 1) grid = 1;
-  grid *= p->cg;
+  grid *= p->cl;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(cs::NUM_THREADS);
@@ -501,9 +517,9 @@ cs_status launch(cs_chain_s* p, cs::KParams& kp, const uint32_t* sched, int n_un
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   unsigned n_attr = 0;
-  if (p->cg == 2) {
+  if (p->cl > 1) {
     attr[n_attr].id = cudaLaunchAttributeClusterDimension;
-    attr[n_attr].val.clusterDim.x = 2;
+    attr[n_attr].val.clusterDim.x = static_cast<unsigned>(p->cl);
     attr[n_attr].val.clusterDim.y = 1;
     attr[n_attr].val.clusterDim.z = 1;
     ++n_attr;
@@ -522,6 +538,9 @@ cs_status launch(cs_chain_s* p, cs::KParams& kp, const uint32_t* sched, int n_un
   if (p->d.kind == CS_CHAIN_ATTN) {
     if ((s = set_smem_attr<NS_A, SB_A, 1, true>()) != CS_OK) return s;
     e = cudaLaunchKernelEx(&cfg, cs::cs_chain_kernel<NS_A, SB_A, 1, true>, kp);
+  } else if (p->cl == 4) {
+    if ((s = set_smem_attr<NS_A, SB_A, 2, false, 4>()) != CS_OK) return s;
+    e = cudaLaunchKernelEx(&cfg, cs::cs_chain_kernel<NS_A, SB_A, 2, false, 4>, kp);
   } else if (p->cg == 2) {
     if ((s = set_smem_attr<NS_A, SB_A, 2, false>()) != CS_OK) return s;
     e = cudaLaunchKernelEx(&cfg, cs::cs_chain_kernel<NS_A, SB_A, 2, false>, kp);
@@ -650,9 +669,12 @@ cs_status bind_mlp(cs_chain_s* p, const cs_mlp_args* a) {
   const int M = p->d.M, H = p->d.H, F = p->d.F;
   cs_status s;
   if ((s = encode_act(p, MAP_X, a->X, M, H, false)) != CS_OK) return s;
-  if ((s = encode_weight(p, MAP_W1, swiglu ? a->Wg : a->W1, H, F, p->bn[0] / p->cg)) != CS_OK) return s;
-  if (swiglu && (s = encode_weight(p, MAP_WU, a->Wu, H, F, p->bn[0] / p->cg)) != CS_OK) return s;
-  if ((s = encode_weight(p, MAP_W2, a->W2, F, H, p->bn[1] / p->cg)) != CS_OK) return s;
+  // [N, K] weights: a box holds the B columns one CTA fetches (with 4-CTA
+  // clusters, half of its pair share; the other half comes by multicast)
+  const int split_b = p->cl == 4 ? 2 : 1;
+  if ((s = encode_weight(p, MAP_W1, swiglu ? a->Wg : a->W1, H, F, p->bn[0] / p->cg / split_b)) != CS_OK) return s;
+  if (swiglu && (s = encode_weight(p, MAP_WU, a->Wu, H, F, p->bn[0] / p->cg / split_b)) != CS_OK) return s;
+  if ((s = encode_weight(p, MAP_W2, a->W2, F, H, p->bn[1] / p->cg / split_b)) != CS_OK) return s;
   if ((s = encode_act(p, MAP_Y, a->Y, M, H, true)) != CS_OK) return s;
   return CS_OK;
 }
@@ -722,6 +744,7 @@ cs_status cs_chain_plan(const cs_chain_desc* desc, cs_chain_t* out) {
   p->m_units = g.m_tiles;
   p->m_blocks = g.m_blocks;
   p->cg = g.cg;
+  p->cl = g.cl;
   p->stages = g.stages;
   for (int i = 0; i < 3; ++i) {
     p->n_tiles[i] = g.n_tiles[i];
@@ -776,7 +799,7 @@ cs_status cs_chain_plan(const cs_chain_desc* desc, cs_chain_t* out) {
   if ((s = upload(&p->sched_fused, fused)) != CS_OK) return bail(s);
   for (int st = 0; st < g.stages; ++st)
     if ((s = upload(&p->sched_stage[st], build_stage(g, st))) != CS_OK) return bail(s);
-  p->num_sms = p->num_sms / g.cg * g.cg;
+  p->num_sms = p->num_sms / g.cl * g.cl;
   // plan-owned intermediate maps (never re-encoded)
   int owned[4];
   int n_owned = 0;
@@ -937,7 +960,7 @@ cs_status cs_chain_query(cs_chain_t p, cs_chain_info* info) {
     info->sched_units[i] = p->sched_units[i];
     info->split_k[i] = p->splits[i];
   }
-  info->tile_m = cs::BM * p->cg;
+  info->tile_m = cs::BM * p->cl;
   info->stride = p->stride;
   info->intermediate[0] = p->inter[0];
   info->intermediate[1] = p->inter[1];
@@ -996,7 +1019,7 @@ cs_status cs_chain_debug_trace(cs_chain_t p, int enable) {
     p->trace_records = 0;
   }
   if (!enable) return CS_OK;
-  const int recs = p->n_fused * p->cg;
+  const int recs = p->n_fused * p->cl;
   const size_t bytes = static_cast<size_t>(recs) * cs::TRACE_WORDS * 8;
   if (cudaMalloc(reinterpret_cast<void**>(&p->trace), bytes) != cudaSuccess) return fail(CS_ERR_OOM, "cudaMalloc failed");
   CS_CUDA(cudaMemset(p->trace, 0, bytes));
@@ -1074,6 +1097,7 @@ cs_status cs_mlp_forward_noalloc(const cs_chain_desc* desc, const cs_mlp_args* a
   p.m_units = g.m_tiles;
   p.m_blocks = g.m_blocks;
   p.cg = g.cg;
+  p.cl = g.cl;
   p.stages = g.stages;
   for (int i = 0; i < 3; ++i) {
     p.n_tiles[i] = g.n_tiles[i];
@@ -1089,7 +1113,7 @@ cs_status cs_mlp_forward_noalloc(const cs_chain_desc* desc, const cs_mlp_args* a
   p.stride = g.stride;
   p.cfg_b = g.cg == 1 && (desc->kind == CS_CHAIN_MLP_SWIGLU || g.bn[0] == 256 || g.bn[1] == 256);
   p.smem = p.cfg_b ? smem_bytes_for<NS_B, SB_B>() : smem_bytes_for<NS_A, SB_A>();
-  p.num_sms = p.num_sms / g.cg * g.cg;
+  p.num_sms = p.num_sms / g.cl * g.cl;
   const std::vector<uint32_t> fused = build_fused(g);
   const std::vector<uint32_t> st0 = build_stage(g, 0), st1 = build_stage(g, 1);
   p.n_fused = static_cast<int>(fused.size());

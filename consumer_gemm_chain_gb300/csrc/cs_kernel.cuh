@@ -133,7 +133,7 @@ struct KParams {
 };
 
 // Trace record of one unit on one CTA (index = dispatch index * CTAs per tile + rank):
-//   [0] unit | dispatch index << 32   [1] smid | blockIdx << 16 | rank << 31
+//   [0] unit | dispatch index << 32   [1] smid | blockIdx << 16 | rank << 30
 //   [2] claimed   [3] dependencies published   [4] first TMA load   [5] last TMA load
 //   [6] accumulator complete (epilogue)   [7] epilogue done (stores + release)
 constexpr int TRACE_WORDS = 8;
@@ -331,7 +331,11 @@ __device__ __noinline__ int tma_wait_slices(SmemCtl<NS>* sc, uint32_t q, int kb,
 }
 
 // ---------------------------------------------------------------- TMA role
-template <int NS, int STAGE_BYTES, int CG>
+// CL = CTAs per unit: 1, 2 (a pair sharing one 256-row MMA) or 4 (two pairs
+// on consecutive 256-row blocks of the same column tile: each weight box is
+// fetched once and multicast to the CTA holding the same B columns in the
+// other pair).
+template <int NS, int STAGE_BYTES, int CG, int CL>
 __device__ bool tma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, RingPos& rp, uint32_t unit,
                               uint32_t q, uint32_t rank) {
   const uint32_t tidx = sc->uq_idx[q];
@@ -342,9 +346,10 @@ __device__ bool tma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
   const int kb0 = unit_ks(unit) * S.kps;
   const int kb1 = min(S.k_iters, kb0 + S.kps);
   const int claim_at = kb1 - kb0 > CLAIM_AHEAD ? kb1 - CLAIM_AHEAD : kb0;
-  const int row0 = (m * CG + static_cast<int>(rank)) * BM;  // this CTA's A rows
+  const int row0 = (m * CL + static_cast<int>(rank)) * BM;  // this CTA's A rows
+  const int prank = static_cast<int>(rank) & (CG - 1);        // rank inside the MMA pair
   const int bcols = S.bn / CG;                               // this CTA's share of B's columns
-  const int col0 = n * S.bn + static_cast<int>(rank) * bcols;
+  const int col0 = n * S.bn + prank * bcols;
   int ready_kb = do_wait ? kb0 : kb1;  // slices below this bound may load now
   for (int kb = kb0; kb < kb1; ++kb) {
     if (rank == 0 && kb == claim_at) mbar_arrive(&sc->claim_req);
@@ -355,9 +360,11 @@ __device__ bool tma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
     if (!wait_bar(&sc->empty[rp.slot], rp.phase ^ 1u, sc, p, 1)) return false;
     uint8_t* sa = ring + rp.slot * STAGE_BYTES;
     uint8_t* sb = sa + TILE_A_BYTES;
-    // Completion goes to the leader's full barrier (each CTA of a pair adds its bytes).
+    // Completion goes to the leader's full barrier (each CTA of a pair adds its
+    // bytes); with CL = 4 every CTA counts its own bytes (its A, and its B
+    // columns: one half fetched here, one multicast by the other pair).
     uint32_t bar_addr;
-    if constexpr (CG == 1) {
+    if constexpr (CG == 1 || CL == 4) {
       bar_addr = smem_u32(&sc->full[rp.slot]);
       mbar_arrive_expect_tx(&sc->full[rp.slot], bytes);
     } else {
@@ -368,18 +375,37 @@ __device__ bool tma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
         mbar_expect_tx_remote(bar_addr, bytes);
     }
     auto load = [&](void* dst, const CUtensorMap* map, int x, int y) {
-      if constexpr (CG == 1)
+      if constexpr (CG == 1 || CL == 4)
         tma_load_2d(dst, map, x, y, &sc->full[rp.slot]);
       else
         tma_load_2d_pair(dst, map, x, y, bar_addr);
     };
     if (kb == kb0) {
       sc->tma_seq = sc->tma_seq + 1;
-      trace_put(p, tidx, rank, CG, 4, globaltimer());
+      trace_put(p, tidx, rank, CL, 4, globaltimer());
     }
     sc->tma_kb = kb;
-    if (kb == kb1 - 1) trace_put(p, tidx, rank, CG, 5, globaltimer());
+    if (kb == kb1 - 1) trace_put(p, tidx, rank, CL, 5, globaltimer());
     load(sa, &p.maps[S.map_a], kb * BK, row0);
+    if constexpr (CL == 4) {
+      // this CTA fetches half of its B columns (the half of its pair index)
+      // for itself and for the CTA with the same pair rank in the other pair
+      const uint16_t mask = static_cast<uint16_t>((1u << prank) | (1u << (prank + 2)));
+      const int part = static_cast<int>(rank) >> 1;
+      const CUtensorMap* bm = &p.maps[S.map_b];
+      if (S.b_major == 0) {
+        // weights [N, K]: a box of 64 K x bcols/2 N rows
+        tma_load_2d_mc(sb + part * (bcols / 2) * (BK * 2), bm, kb * BK, col0 + part * (bcols / 2), &sc->full[rp.slot],
+                       mask);
+      } else {
+        // weights [K, N]: every other 64-column box (8 KB each)
+        for (int h = part; h < bcols / 64; h += 2)
+          tma_load_2d_mc(sb + h * 8192, bm, col0 + h * 64, kb * BK, &sc->full[rp.slot], mask);
+      }
+      sc->issued_parity[rp.slot] = static_cast<int>(rp.phase);
+      rp.next<NS>();
+      continue;
+    }
     // B operand(s): this CTA's bcols rows of N per operand; a second operand
     // (the up projection of gate|up) follows the first, so one N = 2*bn MMA
     // covers both.
@@ -402,9 +428,13 @@ __device__ bool tma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
 }
 
 // ---------------------------------------------------------------- MMA role
-template <int NS, int STAGE_BYTES, int CG>
+template <int NS, int STAGE_BYTES, int CG, int CL>
 __device__ bool mma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, RingPos& rp, uint32_t unit,
-                              uint32_t& acc, uint32_t& acc_phase) {
+                              uint32_t& acc, uint32_t& acc_phase, uint32_t rank) {
+  // a freed stage is refilled by this pair and (CL = 4) by the other pair's
+  // multicast: the release goes to every CTA that writes into it
+  const uint16_t empty_mask = CL == 4 ? 0xF : 0x3;
+  const uint16_t pair_mask = static_cast<uint16_t>(0x3u << (rank & 2u));
   const StageP& S = p.st[unit_stage(unit)];
   const uint32_t idesc = make_idesc_f16(p.bf16, S.b_major, BM * CG, S.mma_n);
   if (!wait_bar(&sc->tempty[acc], acc_phase ^ 1u, sc, p, 2)) return false;
@@ -427,12 +457,28 @@ __device__ bool mma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
       const uint64_t b = bdesc + static_cast<uint64_t>(S.b_major == 0 ? kk * 2 : kk * 128);  // +32 B / +16 rows
       tc_mma_f16<CG>(d, a, b, idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
     }
-    tc_commit<CG>(&sc->empty[rp.slot]);
+    tc_commit<CG>(&sc->empty[rp.slot], empty_mask);
     rp.next<NS>();
   }
-  tc_commit<CG>(&sc->tfull[acc]);
+  tc_commit<CG>(&sc->tfull[acc], pair_mask);
   acc ^= 1u;
   if (acc == 0u) acc_phase ^= 1u;
+  return true;
+}
+
+// CL = 4, the second CTA of a pair: its stage is full once its own copies and
+// the other pair's multicast have landed; pass that on to the pair's leader,
+// whose full barrier waits for both CTAs before it issues the pair MMA.
+template <int NS>
+__device__ bool fwd_gemm_unit(const KParams& p, SmemCtl<NS>* sc, RingPos& rp, uint32_t unit, uint32_t rank) {
+  const StageP& S = p.st[unit_stage(unit)];
+  const int kb0 = unit_ks(unit) * S.kps;
+  const int kb1 = min(S.k_iters, kb0 + S.kps);
+  for (int kb = kb0; kb < kb1; ++kb) {
+    if (!wait_bar(&sc->full[rp.slot], rp.phase, sc, p, 13)) return false;
+    mbar_arrive_cluster_relaxed(mapa_shared(&sc->full[rp.slot], rank & ~1u));
+    rp.next<NS>();
+  }
   return true;
 }
 
@@ -569,18 +615,18 @@ __device__ __forceinline__ void split_reduce_small(const StageP& S, const float4
   }
 }
 
-template <int NS, int CG>
+template <int NS, int CG, int CL>
 __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* staging, uint32_t unit, uint32_t& acc,
                               uint32_t& acc_phase, int& last_buf, uint32_t rank, uint32_t tidx, uint32_t epoch1) {
   const StageP& S = p.st[unit_stage(unit)];
-  const int mb = unit_m(unit) * CG + static_cast<int>(rank);  // this CTA's 128-row block
+  const int mb = unit_m(unit) * CL + static_cast<int>(rank);  // this CTA's 128-row block
   const int n = unit_n(unit);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;  // TMEM lane quadrant this warp may access
   const int row = q * 32 + lane;
   if (!wait_bar(&sc->tfull[acc], acc_phase, sc, p, 4)) return false;
   tc_fence_after();
-  if (threadIdx.x == EPI_WARP0 * 32) trace_put(p, tidx, rank, CG, 6, globaltimer());
+  if (threadIdx.x == EPI_WARP0 * 32) trace_put(p, tidx, rank, CL, 6, globaltimer());
   const uint32_t tbase =
       sc->tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * static_cast<uint32_t>(p.acc_stride);
   const int nchunks = S.bn / 64;
@@ -603,7 +649,7 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
       if constexpr (CG == 1)
         mbar_arrive(&sc->tempty[acc]);
       else
-        mbar_arrive_cluster(mapa_shared(&sc->tempty[acc], 0));
+        mbar_arrive_cluster(mapa_shared(&sc->tempty[acc], rank & ~1u));
     }
   };
   if (split) {
@@ -633,7 +679,7 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
     }
     named_bar_sync(1, EPI_THREADS);
     if (!sc->split_last) {
-      if (threadIdx.x == EPI_WARP0 * 32) trace_put(p, tidx, rank, CG, 7, globaltimer());
+      if (threadIdx.x == EPI_WARP0 * 32) trace_put(p, tidx, rank, CL, 7, globaltimer());
       return true;
     }
     __threadfence();
@@ -761,7 +807,7 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
     release_tile(p, S, mb, n, lane);
     last_buf = -1;
   }
-  if (threadIdx.x == EPI_WARP0 * 32) trace_put(p, tidx, rank, CG, 7, globaltimer());
+  if (threadIdx.x == EPI_WARP0 * 32) trace_put(p, tidx, rank, CL, 7, globaltimer());
   return true;
 }
 
@@ -1057,11 +1103,11 @@ struct PfState {
   int kb0 = 0, kb1 = 0;
 };
 
-template <int CG>
+template <int CG, int CL>
 __device__ __forceinline__ void prefetch_slice(const StageP& S, uint32_t unit, int kb, uint32_t rank, int lane) {
   const int m = unit_m(unit), n = unit_n(unit);
   const int bcols = S.bn / CG;
-  const int col0 = n * S.bn + static_cast<int>(rank) * bcols;
+  const int col0 = n * S.bn + static_cast<int>(rank & (CG - 1)) * bcols;
   if (S.b_major == 0) {
     // weights [N, K]: one 128-byte line per weight row of the slice
     for (int r = lane; r < bcols; r += 32) {
@@ -1085,7 +1131,7 @@ __device__ __forceinline__ void prefetch_slice(const StageP& S, uint32_t unit, i
     }
   }
   if (S.pf_a) {
-    const int row0 = (m * CG + static_cast<int>(rank)) * BM;
+    const int row0 = (m * CL + static_cast<int>(rank)) * BM;
     for (int r = lane; r < BM; r += 32)
       if (row0 + r < S.pf_arows)
         prefetch_l2(S.pf_a + static_cast<long long>(row0 + r) * S.pf_lda + static_cast<long long>(kb) * BK * 2);
@@ -1093,7 +1139,7 @@ __device__ __forceinline__ void prefetch_slice(const StageP& S, uint32_t unit, i
 }
 
 // Bounded wait for `bar`, prefetching for the latest pushed unit meanwhile.
-template <int NS, int CG, bool CLUSTER>
+template <int NS, int CG, int CL, bool CLUSTER>
 __device__ bool wait_prefetching(uint64_t* bar, uint32_t parity, SmemCtl<NS>* sc, const KParams& p, PfState& pf,
                                  uint32_t rank, int lane, uint32_t where) {
   if (p.pf_dist <= 0 || pf.unit == UNIT_END || pf.next >= pf.kb1) return wait_bar<NS, CLUSTER>(bar, parity, sc, p, where);
@@ -1105,7 +1151,7 @@ __device__ bool wait_prefetching(uint64_t* bar, uint32_t parity, SmemCtl<NS>* sc
     if (__shfl_sync(0xFFFFFFFFu, ready ? 1 : 0, 0)) return true;
     // the TMA warp is on an earlier unit: the first pf_dist slices; else pf_dist ahead of it
     const int limit = min(pf.kb1, (sc->tma_seq < pf.seq ? pf.kb0 : sc->tma_kb + 1) + p.pf_dist);
-    while (pf.next < limit) prefetch_slice<CG>(S, pf.unit, pf.next++, rank, lane);
+    while (pf.next < limit) prefetch_slice<CG, CL>(S, pf.unit, pf.next++, rank, lane);
     if (pf.next >= pf.kb1) return wait_bar<NS, CLUSTER>(bar, parity, sc, p, where);
     if (sc->abort) return false;
     if (globaltimer() - t0 > p.watchdog_ns) {
@@ -1133,8 +1179,11 @@ __device__ __forceinline__ void push_unit(SmemCtl<NS>* sc, uint32_t q, uint32_t 
 // ---------------------------------------------------------------- the kernel
 // ATTN: the instantiation also runs attention units (the attention chain);
 // the MLP instantiations leave that code out and keep their registers.
-template <int NS, int STAGE_BYTES, int CG, bool ATTN>
+// CG: CTAs per tcgen05 MMA (1, or 2 for a 256-row pair); CL: CTAs per unit
+// and per cluster (CG, or 4: two pairs sharing the weight boxes by multicast).
+template <int NS, int STAGE_BYTES, int CG, bool ATTN, int CL = CG>
 __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_constant__ KParams p) {
+  static_assert(CL == CG || (CG == 2 && CL == 4 && !ATTN), "unsupported cluster shape");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
@@ -1143,12 +1192,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = CG == 1 ? 0u : cluster_ctarank();
-  const bool leader = rank == 0;
+  const bool leader = rank == 0;                 // claims units for the cluster
+  const bool pair_leader = (rank & 1u) == 0u;    // issues the pair's MMAs
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
-      mbar_init(&sc->full[i], CG);  // one expect_tx arrival per CTA of the tile
-      mbar_init(&sc->empty[i], 1);
+      // CL = CG: one expect_tx arrival per CTA of the tile, on the leader's
+      // barrier; CL = 4: the own arrival, plus (pair leader) the peer's relay
+      mbar_init(&sc->full[i], CL == 4 ? (pair_leader ? 2 : 1) : CG);
+      // CL = 4: both pairs' MMAs must be done with a stage before it refills
+      mbar_init(&sc->empty[i], CL == 4 ? 2 : 1);
       sc->issued_parity[i] = -1;
     }
     for (int i = 0; i < 2; ++i) {
@@ -1161,7 +1214,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
     }
     mbar_init(&sc->claim_req, 1);
     mbar_init(&sc->mb_full, 1);
-    mbar_init(&sc->mb_empty, 1);
+    mbar_init(&sc->mb_empty, CL - 1 > 0 ? CL - 1 : 1);  // every peer CTA takes the index
     mbar_init(&sc->s_full, 1);
     mbar_init(&sc->s_empty, 4);
     mbar_init(&sc->p_full, 4);
@@ -1202,24 +1255,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
       if (leader) {
         // claim units in schedule order, one at a time, just in time
         if (!first) {
-          if (!wait_prefetching<NS, CG, false>(&sc->claim_req, req_phase, sc, p, pf, rank, lane, 9)) break;
+          if (!wait_prefetching<NS, CG, CL, false>(&sc->claim_req, req_phase, sc, p, pf, rank, lane, 9)) break;
           req_phase ^= 1u;
         }
         first = false;
         if (lane == 0 && ld_relaxed_gpu(&p.ctrl[CTRL_ABORT]) == 0u) idx = atomicAdd(&p.ctrl[CTRL_DISPATCH], 1u);
         idx = __shfl_sync(0xFFFFFFFFu, idx, 0);
         if constexpr (CG == 2) {
-          // hand the dispatch index to the peer CTA of the pair
+          // hand the dispatch index to the other CTAs of the cluster
           if (!wait_bar<NS, true>(&sc->mb_empty, mb_phase ^ 1u, sc, p, 10)) break;
-          if (lane == 0) {
-            st_cluster_u32(mapa_shared(&sc->mb_unit, 1), idx);
-            mbar_arrive_cluster(mapa_shared(&sc->mb_full, 1));
+          if (lane > 0 && lane < CL) {
+            st_cluster_u32(mapa_shared(&sc->mb_unit, static_cast<uint32_t>(lane)), idx);
+            mbar_arrive_cluster(mapa_shared(&sc->mb_full, static_cast<uint32_t>(lane)));
           }
           __syncwarp();
           mb_phase ^= 1u;
         }
       } else {
-        if (!wait_prefetching<NS, CG, true>(&sc->mb_full, mb_phase, sc, p, pf, rank, lane, 11)) break;
+        if (!wait_prefetching<NS, CG, CL, true>(&sc->mb_full, mb_phase, sc, p, pf, rank, lane, 11)) break;
         idx = *reinterpret_cast<volatile uint32_t*>(&sc->mb_unit);
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(mapa_shared(&sc->mb_empty, 0));
@@ -1227,9 +1280,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
       }
       const uint32_t unit = idx < static_cast<uint32_t>(p.n_units) ? p.sched[idx] : UNIT_END;
       if (unit != UNIT_END && lane == 0) {
-        trace_put(p, idx, rank, CG, 0, unit | (static_cast<unsigned long long>(idx) << 32));
-        trace_put(p, idx, rank, CG, 1, smid() | (blockIdx.x << 16) | (rank << 31));
-        trace_put(p, idx, rank, CG, 2, globaltimer());
+        trace_put(p, idx, rank, CL, 0, unit | (static_cast<unsigned long long>(idx) << 32));
+        trace_put(p, idx, rank, CL, 1, smid() | (blockIdx.x << 16) | (rank << 30));
+        trace_put(p, idx, rank, CL, 2, globaltimer());
       }
       if (!wait_bar(&sc->uq_empty[q], qphase ^ 1u, sc, p, 5)) break;
       const StageP& S = p.st[unit == UNIT_END ? 0 : unit_stage(unit)];
@@ -1247,11 +1300,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
         pf.unit = UNIT_END;
       }
       if (consumer && S.kind == STAGE_GEMM)
-        sched_poll_gemm<NS>(p, S, sc, q, unit_m(unit) * CG + static_cast<int>(rank), epoch1, unit, lane);
+        sched_poll_gemm<NS>(p, S, sc, q, unit_m(unit) * CL + static_cast<int>(rank), epoch1, unit, lane);
       else if constexpr (ATTN)
         if (consumer && S.kind == STAGE_ATTN)
           sched_poll_attn<NS>(p, S, sc, q, unit_m(unit), unit_n(unit), epoch1, unit, lane);
-      if (lane == 0) trace_put(p, idx, rank, CG, 3, globaltimer());
+      if (lane == 0) trace_put(p, idx, rank, CL, 3, globaltimer());
       if (++q == UQ) {
         q = 0;
         qphase ^= 1u;
@@ -1266,7 +1319,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
         if (!wait_bar(&sc->uq_full[q], qphase, sc, p, 6)) break;
         const uint32_t unit = sc->uq[q];
         if (unit != UNIT_END && p.st[unit_stage(unit)].kind == STAGE_GEMM)
-          ok = tma_gemm_unit<NS, STAGE_BYTES, CG>(p, sc, ring, rp, unit, q, rank);
+          ok = tma_gemm_unit<NS, STAGE_BYTES, CG, CL>(p, sc, ring, rp, unit, q, rank);
         else if constexpr (CG == 1 && ATTN)
           if (unit != UNIT_END) ok = tma_attn_unit<NS, STAGE_BYTES>(p, sc, ring, rp, unit, q);
         mbar_arrive(&sc->uq_empty[q]);
@@ -1279,7 +1332,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
       // Let every load this thread issued land before the CTA can exit.  In
       // pair mode the loads complete on the leader's barrier, which its MMA
       // waits for; after an abort, give in-flight copies a bounded grace time.
-      if constexpr (CG == 1) {
+      // CL = 4: each CTA's barrier counts every copy into its shared memory.
+      if constexpr (CG == 1 || CL == 4) {
         for (int i = 0; i < NS; ++i)
           if (sc->issued_parity[i] >= 0) {
             const uint64_t t0 = globaltimer();
@@ -1307,9 +1361,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
           qphase ^= 1u;
         }
         if (unit == UNIT_END) break;
-        if (leader && p.st[unit_stage(unit)].kind == STAGE_GEMM) {
-          ok = mma_gemm_unit<NS, STAGE_BYTES, CG>(p, sc, ring, rp, unit, acc, acc_phase);
+        if (pair_leader && p.st[unit_stage(unit)].kind == STAGE_GEMM) {
+          ok = mma_gemm_unit<NS, STAGE_BYTES, CG, CL>(p, sc, ring, rp, unit, acc, acc_phase, rank);
           issued = true;
+        } else if constexpr (CL == 4) {
+          if (p.st[unit_stage(unit)].kind == STAGE_GEMM) ok = fwd_gemm_unit<NS>(p, sc, rp, unit, rank);
         } else if constexpr (CG == 1 && ATTN) {
           ok = mma_attn_unit<NS, STAGE_BYTES>(p, sc, ring, staging, rp, unit, p_phase);
           issued = true;
@@ -1342,7 +1398,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
       }
       if (unit == UNIT_END) break;
       if (p.st[unit_stage(unit)].kind == STAGE_GEMM)
-        ok = epi_gemm_unit<NS, CG>(p, sc, staging, unit, acc, acc_phase, last_buf, rank, tidx, epoch1);
+        ok = epi_gemm_unit<NS, CG, CL>(p, sc, staging, unit, acc, acc_phase, last_buf, rank, tidx, epoch1);
       else if constexpr (CG == 1 && ATTN)
         ok = epi_attn_unit<NS>(p, sc, staging, unit, s_phase, o_phase, last_buf, tidx);
     }

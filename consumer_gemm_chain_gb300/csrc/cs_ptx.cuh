@@ -101,6 +101,12 @@ __device__ __forceinline__ uint32_t mapa_shared(const void* p, uint32_t rank) {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
+// Relaxed remote arrive: a relay of a completion the caller has observed on
+// its own barrier (the data it stands for is already in shared memory), so no
+// cluster-scope release (measured: the release form cost ~0.4 us per call).
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
 __device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t cluster_addr, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_addr),
                "r"(bytes)
@@ -186,6 +192,17 @@ __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorM
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster_addr)
       : "memory");
 }
+// Multicast load: the box lands at the same shared-memory offset in every CTA
+// of `cta_mask`, and each of them counts the bytes on its own mbarrier at the
+// offset of `bar`.
+__device__ __forceinline__ void tma_load_2d_mc(void* smem_dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                               uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], "
+      "[%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(cta_mask)
+      : "memory");
+}
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* smem_src, int x, int y) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
@@ -265,16 +282,16 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uin
         : "memory");
 }
 // Arrive (once) on `bar` when every tcgen05 op this thread issued so far has
-// completed.  CG = 2: arrive on `bar` at the same offset in every CTA of the
-// pair (multicast), so both SMs learn of the completion.
+// completed.  CG = 2: arrive on `bar` at the same offset in every CTA of
+// `mask` (multicast; by default the pair of cluster ranks 0 and 1), so every
+// SM that waits for the completion learns of it.
 template <int CG>
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+__device__ __forceinline__ void tc_commit(uint64_t* bar, uint16_t mask = 0x3) {
   if constexpr (CG == 1) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
                  : "memory");
   } else {
-    const uint16_t mask = 0x3;
     asm volatile(
         "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
             smem_u32(bar)),

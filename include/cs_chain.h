@@ -107,9 +107,12 @@ typedef struct cs_chain_desc {
                           with 256-row pair tiles at least two groups)              */
   int tile_n;          /* output columns per GEMM tile: 128 or 256; 0 = auto.
                           SwiGLU producer tiles are always 128 (gate|up = 256).     */
-  int tile_m;          /* rows per GEMM tile: 128 (one SM) or 256 (a 2-SM cluster
-                          sharing one tcgen05 MMA; needs tile_n = 256); 0 = auto.
-                          Semaphores stay per 128-row block either way.             */
+  int tile_m;          /* rows per GEMM tile: 128 (one SM), 256 (a 2-SM cluster
+                          sharing one tcgen05 MMA) or 512 (two such pairs in a 4-CTA
+                          cluster that fetch every weight box once and multicast it
+                          to both pairs); 256 and 512 need tile_n = 256 and the GeLU
+                          MLP.  0 = auto (512 where it adds no padding rows over 256,
+                          from M = 512).  Semaphores stay per 128-row block.         */
   int split_k;         /* K-splits per GEMM tile: 0 = auto (split when a stage has
                           fewer tiles than the grid, small M), 1 = never, 2..15 = that
                           many for every GEMM stage.  Splits write fp32 partial tiles

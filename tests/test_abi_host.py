@@ -44,7 +44,7 @@ def test_desc_defaults(cs):
 
 @pytest.mark.parametrize("field,value", [("M", 0), ("H", 12), ("F", 0), ("dtype", 7), ("policy", 9),
                                          ("kind", 5), ("weight_layout", 3), ("lag", -2), ("num_sms", -1),
-                                         ("split_k", 16), ("tile_n", 192), ("tile_m", 64), ("M", 128 * 4096),
+                                         ("split_k", 16), ("tile_n", 192), ("tile_m", 64), ("tile_m", 1024), ("M", 128 * 4096),
                                          ("raster", 3), ("prefetch", -2), ("pdl", 2), ("pdl", -2)])
 def test_invalid_descs_are_rejected_without_a_gpu(cs, field, value):
     d = cs.cs_chain_desc_init(M=64, H=256, F=1024)
@@ -75,7 +75,7 @@ def _check_order(dec, deps_of):
             assert pos[dep] < i, f"unit {u} at {i} precedes its producer {dep}"
 
 
-@pytest.mark.parametrize("tile_m,tile_n", [(128, 128), (128, 256), (256, 256)])
+@pytest.mark.parametrize("tile_m,tile_n", [(128, 128), (128, 256), (256, 256), (512, 256)])
 @pytest.mark.parametrize("M,H,F,sms,lag,group,split", [(64, 256, 1024, 148, -1, 0, 1), (2048, 12288, 6144, 148, -1, 0, 1),
                                                        (2048, 12288, 6144, 152, 0, 3, 1), (1, 12288, 6144, 148, -1, 0, 3),
                                                        (1000, 8192, 2752, 148, 2, 1, 2), (1536, 8192, 8192, 148, 5, 5, 1)])
@@ -160,12 +160,13 @@ def test_row_major_raster_completes_rows_in_turn(cs):
 
 
 def test_auto_tile_shape(cs):
-    big = cs.cs_schedule_build(cs.cs_chain_desc_init(M=2048, H=12288, F=6144, split_k=1), 148)
-    mid = cs.cs_schedule_build(cs.cs_chain_desc_init(M=640, H=12288, F=6144, split_k=1), 148)
-    small = cs.cs_schedule_build(cs.cs_chain_desc_init(M=256, H=12288, F=6144, split_k=1), 148)
-    assert len(big) == 8 * 24 + 8 * 48      # 256 x 256 tiles on CTA pairs for large M
-    assert len(mid) == 5 * 24 + 5 * 48      # 128 x 256 tiles on single SMs in between
-    assert len(small) == 2 * 48 + 2 * 96    # 128 x 128 tiles for small M
+    def units(M):
+        return len(cs.cs_schedule_build(cs.cs_chain_desc_init(M=M, H=12288, F=6144, split_k=1), 148))
+    assert units(2048) == 4 * 24 + 4 * 48   # 512 x 256 tiles: two CTA pairs sharing weight boxes
+    assert units(1536) == 3 * 24 + 3 * 48
+    assert units(1280) == 5 * 24 + 5 * 48   # 256 x 256 pairs where 512 rows would add padding
+    assert units(640) == 5 * 24 + 5 * 48    # 128 x 256 tiles on single SMs in between
+    assert units(256) == 2 * 48 + 2 * 96    # 128 x 128 tiles for small M
 
 
 def test_pair_tiles_need_wide_gelu_tiles(cs):

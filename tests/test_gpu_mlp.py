@@ -51,7 +51,9 @@ def test_tiny_chain_golden_values():
     assert np.max(np.abs(got - ref)) <= TOL * np.max(np.abs(full_ref))
 
 
-TILES = [(128, 128), (128, 256), (256, 256)]  # (tile_m, tile_n); 256 rows = a 2-SM pair
+# (tile_m, tile_n): 256 rows = a 2-SM pair; 512 rows = two pairs in a 4-CTA
+# cluster sharing every weight box by multicast
+TILES = [(128, 128), (128, 256), (256, 256), (512, 256)]
 
 
 @pytest.mark.parametrize("tile_m,tile_n", TILES)
@@ -194,6 +196,24 @@ def test_gpt3_shard_sampled_rows(M):
     rows = cs_inputs.sample_rows(M, 64)
     Yref, _ = _oracle(inp, rows)
     assert oracle.rel_err(Y[rows], Yref) <= TOL
+
+
+@pytest.mark.parametrize("M", [1024, 1536, 2048])
+def test_gpt3_shard_two_pair_clusters(M):
+    """512-row tiles (two 2-SM pairs per 4-CTA cluster, weight boxes multicast)
+    on the full GPT-3 shard: sampled rows against the oracle, and the same bits
+    as the 256-row pair tiles (same K order per output element)."""
+    inp = cs_inputs.make_inputs("gpt3", M=M, seed=0)
+    dev = device_tensors(inp)
+    outs = {}
+    for tm in (256, 512):
+        with plan_for(inp, "tile", tile_m=tm, tile_n=256) as plan:
+            assert cs.cs_chain_query(plan)["tile_m"] == tm
+            outs[tm] = forward(plan, dev).cpu()
+    rows = cs_inputs.sample_rows(M, 64)
+    Yref, _ = _oracle(inp, rows)
+    assert oracle.rel_err(outs[512][rows], Yref) <= TOL
+    assert torch.equal(outs[512], outs[256])
 
 
 @pytest.mark.parametrize("M", [128 * 3, 128 * 7, 128 * 12])
