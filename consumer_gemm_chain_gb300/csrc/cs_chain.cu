@@ -179,8 +179,8 @@ cs_status validate(const cs_chain_desc* d) {
     return fail(CS_ERR_INVALID_ARG, "tile_n=%d (0, 128 or 256)", d->tile_n);
   if (d->tile_m != 0 && d->tile_m != 128 && d->tile_m != 256 && d->tile_m != 512)
     return fail(CS_ERR_INVALID_ARG, "tile_m=%d (0, 128, 256 or 512)", d->tile_m);
-  if (d->tile_m >= 256 && (d->tile_n == 128 || d->kind != CS_CHAIN_MLP_GELU))
-    return fail(CS_ERR_UNSUPPORTED, "tile_m=%d is built for 256-wide GeLU-MLP tiles only", d->tile_m);
+  if (d->tile_m >= 256 && (d->tile_n == 128 || d->kind == CS_CHAIN_ATTN))
+    return fail(CS_ERR_UNSUPPORTED, "tile_m=%d is built for 256-wide MLP tiles only", d->tile_m);
   if (d->kind == CS_CHAIN_ATTN) {
     if (d->head_dim != 128) return fail(CS_ERR_UNSUPPORTED, "head_dim=%d (only 128 is built)", d->head_dim);
     if (d->heads < 1 || d->heads * d->head_dim != d->F)
@@ -197,20 +197,22 @@ Geometry geometry(const cs_chain_desc* d, int num_sms) {
   // 256-wide tiles need 2/3 of the operand bytes per FLOP of 128-wide ones;
   // they pay off once the producer stage alone fills half of the grid.
   int tn = d->tile_n;
+  int tm = d->tile_m;
+  const bool mlp = d->kind != CS_CHAIN_ATTN;
+  // Two 2-SM pairs of a 4-CTA cluster (512 x 256 tiles) fetch each weight box
+  // once for both pairs (multicast).  Auto from M = 512: for SwiGLU always
+  // (measured at LLaMA M=512 / 768: 76 / 104 us against 93 / 117 us with
+  // 128-row tiles), for GeLU where they add no padding rows over 256-row pairs
+  // (GPT-3 M=768: 199 us against 176 us with 128-row tiles).
+  if (tm == 0 && (tn == 0 || tn == 256) && mlp && blocks >= 4 &&
+      (d->kind == CS_CHAIN_MLP_SWIGLU || 2 * cdiv(d->M, 512) == cdiv(d->M, 256)))
+    tm = 512, tn = 256;
   if (tn == 0) tn = (2 * blocks * cdiv(d->F, 256) >= num_sms) ? 256 : 128;
   // attention units keep S and O in TMEM next to the two 128-column accumulators
   if (d->kind == CS_CHAIN_ATTN) tn = 128;
   // A 2-SM pair per 256 x 256 tile halves them again (each SM loads half of B).
-  // Two pairs of a 4-CTA cluster (512 rows) fetch each weight box once for
-  // both (multicast): chosen when they add no padding over 256-row pairs.
-  int tm = d->tile_m;
-  if (tm == 0) {
-    const bool wide_gelu = tn == 256 && d->kind == CS_CHAIN_MLP_GELU;
-    tm = (wide_gelu && blocks >= 4 && 2 * cdiv(d->M, 512) == cdiv(d->M, 256)) ? 512
-         : (wide_gelu && blocks >= 8)                                        ? 256
-                                                                             : 128;
-  }
-  if (tm >= 256 && (tn != 256 || d->kind != CS_CHAIN_MLP_GELU)) tm = 128;
+  if (tm == 0) tm = (tn == 256 && mlp && blocks >= 8) ? 256 : 128;
+  if (tm >= 256 && (tn != 256 || d->kind == CS_CHAIN_ATTN)) tm = 128;
   // 512-row tiles: two 2-SM pairs of one 4-CTA cluster on consecutive 256-row
   // blocks; each weight box is fetched once and multicast to both pairs
   g.cg = tm >= 256 ? 2 : 1;
@@ -670,10 +672,12 @@ cs_status bind_mlp(cs_chain_s* p, const cs_mlp_args* a) {
   cs_status s;
   if ((s = encode_act(p, MAP_X, a->X, M, H, false)) != CS_OK) return s;
   // [N, K] weights: a box holds the B columns one CTA fetches (with 4-CTA
-  // clusters, half of its pair share; the other half comes by multicast)
+  // clusters, half of its pair share; the other half comes by multicast).  A
+  // gate|up pair gives each CTA all bn rows of one of the two operands.
   const int split_b = p->cl == 4 ? 2 : 1;
-  if ((s = encode_weight(p, MAP_W1, swiglu ? a->Wg : a->W1, H, F, p->bn[0] / p->cg / split_b)) != CS_OK) return s;
-  if (swiglu && (s = encode_weight(p, MAP_WU, a->Wu, H, F, p->bn[0] / p->cg / split_b)) != CS_OK) return s;
+  const int box0 = (swiglu ? p->bn[0] : p->bn[0] / p->cg) / split_b;
+  if ((s = encode_weight(p, MAP_W1, swiglu ? a->Wg : a->W1, H, F, box0)) != CS_OK) return s;
+  if (swiglu && (s = encode_weight(p, MAP_WU, a->Wu, H, F, box0)) != CS_OK) return s;
   if ((s = encode_weight(p, MAP_W2, a->W2, F, H, p->bn[1] / p->cg / split_b)) != CS_OK) return s;
   if ((s = encode_act(p, MAP_Y, a->Y, M, H, true)) != CS_OK) return s;
   return CS_OK;

@@ -348,8 +348,12 @@ __device__ bool tma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
   const int claim_at = kb1 - kb0 > CLAIM_AHEAD ? kb1 - CLAIM_AHEAD : kb0;
   const int row0 = (m * CL + static_cast<int>(rank)) * BM;  // this CTA's A rows
   const int prank = static_cast<int>(rank) & (CG - 1);        // rank inside the MMA pair
-  const int bcols = S.bn / CG;                               // this CTA's share of B's columns
-  const int col0 = n * S.bn + prank * bcols;
+  // gate|up on a pair: the MMA's N = 2*bn is split over the two CTAs, so the
+  // first holds the bn gate rows of B and the second the bn up rows
+  const bool gate_up = CG == 2 && S.map_b2 >= 0;
+  const int bcols = gate_up ? S.bn : S.bn / CG;              // this CTA's share of B's rows
+  const int col0 = n * S.bn + (gate_up ? 0 : prank * bcols);
+  const int map_b = gate_up && prank == 1 ? S.map_b2 : S.map_b;
   int ready_kb = do_wait ? kb0 : kb1;  // slices below this bound may load now
   for (int kb = kb0; kb < kb1; ++kb) {
     if (rank == 0 && kb == claim_at) mbar_arrive(&sc->claim_req);
@@ -392,7 +396,7 @@ __device__ bool tma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
       // for itself and for the CTA with the same pair rank in the other pair
       const uint16_t mask = static_cast<uint16_t>((1u << prank) | (1u << (prank + 2)));
       const int part = static_cast<int>(rank) >> 1;
-      const CUtensorMap* bm = &p.maps[S.map_b];
+      const CUtensorMap* bm = &p.maps[map_b];
       if (S.b_major == 0) {
         // weights [N, K]: a box of 64 K x bcols/2 N rows
         tma_load_2d_mc(sb + part * (bcols / 2) * (BK * 2), bm, kb * BK, col0 + part * (bcols / 2), &sc->full[rp.slot],
@@ -409,9 +413,9 @@ __device__ bool tma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
     // B operand(s): this CTA's bcols rows of N per operand; a second operand
     // (the up projection of gate|up) follows the first, so one N = 2*bn MMA
     // covers both.
-    const int nops = S.map_b2 >= 0 ? 2 : 1;
+    const int nops = S.map_b2 >= 0 && !gate_up ? 2 : 1;
     for (int op = 0; op < nops; ++op) {
-      const CUtensorMap* bm = &p.maps[op == 0 ? S.map_b : S.map_b2];
+      const CUtensorMap* bm = &p.maps[op == 0 ? map_b : S.map_b2];
       uint8_t* dst = sb + op * bcols * (BK * 2);
       if (S.b_major == 0) {
         // weights [N, K]: one box of 64 K x bcols N rows
@@ -1106,8 +1110,9 @@ struct PfState {
 template <int CG, int CL>
 __device__ __forceinline__ void prefetch_slice(const StageP& S, uint32_t unit, int kb, uint32_t rank, int lane) {
   const int m = unit_m(unit), n = unit_n(unit);
-  const int bcols = S.bn / CG;
-  const int col0 = n * S.bn + static_cast<int>(rank & (CG - 1)) * bcols;
+  const bool gate_up = CG == 2 && S.pf_b2 != nullptr;
+  const int bcols = gate_up ? S.bn : S.bn / CG;
+  const int col0 = n * S.bn + (gate_up ? 0 : static_cast<int>(rank & (CG - 1)) * bcols);
   if (S.b_major == 0) {
     // weights [N, K]: one 128-byte line per weight row of the slice
     for (int r = lane; r < bcols; r += 32) {

@@ -37,6 +37,26 @@ def test_swiglu_parity(M, H, F, dtype, layout):
     assert oracle.rel_err(Y.cpu(), Yref) <= TOL
 
 
+@pytest.mark.parametrize("tile_m", [128, 256, 512])
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+@pytest.mark.parametrize("M,H,F", [(1, 512, 344), (300, 1024, 2752), (700, 768, 392)])
+def test_swiglu_tile_shapes(M, H, F, layout, tile_m):
+    """256-row tiles split the gate|up MMA over a CTA pair (gate rows of B on the
+    first CTA, up rows on the second); 512-row tiles add a second pair that
+    shares every weight box by multicast.  All shapes agree bit for bit."""
+    inp = cs_inputs.make_custom("swiglu", M, H, F, dtype=torch.bfloat16, seed=23)
+    dev = device_tensors(inp, layout)
+    with plan_for(inp, "tile", layout, tile_m=tile_m, tile_n=256) as plan:
+        assert cs.cs_chain_query(plan)["tile_m"] == tile_m
+        Y = forward(plan, dev)
+        Hid = intermediate(plan, 0, inp.M, inp.F, inp.dtype)
+    Yref, Href = _oracle(inp)
+    assert oracle.rel_err(Hid.cpu(), Href) <= TOL
+    assert oracle.rel_err(Y.cpu(), Yref) <= TOL
+    with plan_for(inp, "tile", layout, tile_m=128, tile_n=256) as plan:
+        assert torch.equal(forward(plan, dev), Y)
+
+
 def test_swiglu_policies_bit_identical():
     inp = cs_inputs.make_custom("swiglu", 384, 768, 1376, dtype=torch.bfloat16, seed=22)
     dev = device_tensors(inp, "nk")
