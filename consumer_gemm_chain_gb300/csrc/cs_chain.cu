@@ -35,7 +35,7 @@ cs_status fail(cs_status s, const char* fmt, ...) {
     if (e_ != cudaSuccess) return fail(CS_ERR_CUDA, "%s: %s", #call, cudaGetErrorString(e_));     \
   } while (0)
 
-constexpr int kMaxMaps = 8;
+constexpr int kMaxMaps = 9;
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
 
 // Kernel configurations: ring depth x stage bytes.  A stage holds the A slice
@@ -179,14 +179,16 @@ cs_status validate(const cs_chain_desc* d) {
     return fail(CS_ERR_INVALID_ARG, "tile_n=%d (0, 128 or 256)", d->tile_n);
   if (d->tile_m != 0 && d->tile_m != 128 && d->tile_m != 256 && d->tile_m != 512)
     return fail(CS_ERR_INVALID_ARG, "tile_m=%d (0, 128, 256 or 512)", d->tile_m);
-  if (d->tile_m >= 256 && (d->tile_n == 128 || d->kind == CS_CHAIN_ATTN))
-    return fail(CS_ERR_UNSUPPORTED, "tile_m=%d is built for 256-wide MLP tiles only", d->tile_m);
+  if (d->tile_m >= 256 && d->tile_n == 128)
+    return fail(CS_ERR_UNSUPPORTED, "tile_m=%d is built for 256-wide tiles only", d->tile_m);
   if (d->kind == CS_CHAIN_ATTN) {
     if (d->head_dim != 128) return fail(CS_ERR_UNSUPPORTED, "head_dim=%d (only 128 is built)", d->head_dim);
     if (d->heads < 1 || d->heads * d->head_dim != d->F)
       return fail(CS_ERR_INVALID_ARG, "ATTN needs F == heads*head_dim (F=%d heads=%d)", d->F, d->heads);
-    if (d->tile_n == 256 || d->tile_m >= 256)
-      return fail(CS_ERR_UNSUPPORTED, "the attention chain runs 128 x 128 tiles only");
+    // 128 x 128 tiles on single SMs, or 256 x 256 on CTA pairs (whose attention
+    // units then take two query blocks)
+    if (d->tile_m == 512 || (d->tile_m == 128 && d->tile_n == 256) || (d->tile_m == 256 && d->tile_n == 128))
+      return fail(CS_ERR_UNSUPPORTED, "the attention chain runs 128 x 128 or 256 x 256 (pair) tiles only");
   }
   return CS_OK;
 }
@@ -208,11 +210,17 @@ Geometry geometry(const cs_chain_desc* d, int num_sms) {
       (d->kind == CS_CHAIN_MLP_SWIGLU || 2 * cdiv(d->M, 512) == cdiv(d->M, 256)))
     tm = 512, tn = 256;
   if (tn == 0) tn = (2 * blocks * cdiv(d->F, 256) >= num_sms) ? 256 : 128;
-  // attention units keep S and O in TMEM next to the two 128-column accumulators
-  if (d->kind == CS_CHAIN_ATTN) tn = 128;
   // A 2-SM pair per 256 x 256 tile halves them again (each SM loads half of B).
   if (tm == 0) tm = (tn == 256 && mlp && blocks >= 8) ? 256 : 128;
-  if (tm >= 256 && (tn != 256 || d->kind == CS_CHAIN_ATTN)) tm = 128;
+  if (!mlp) {
+    // attention: single-SM units keep S and O in TMEM next to two 128-column
+    // accumulators; pair units borrow a 256-column accumulator buffer (auto
+    // from M = 512, measured: M=512 134 us against 156 us; M=256 110 against 102)
+    if (d->tile_m == 0) tm = blocks >= 4 ? 256 : 128;
+    if (tm == 512) tm = 256;
+    tn = tm == 256 ? 256 : 128;
+  }
+  if (tm >= 256 && tn != 256) tm = 128;
   // 512-row tiles: two 2-SM pairs of one 4-CTA cluster on consecutive 256-row
   // blocks; each weight box is fetched once and multicast to both pairs
   g.cg = tm >= 256 ? 2 : 1;
@@ -221,8 +229,8 @@ Geometry geometry(const cs_chain_desc* d, int num_sms) {
   g.m_blocks = g.m_tiles * g.cl;
   if (d->kind == CS_CHAIN_ATTN) {
     g.stages = 3;
-    g.bn[0] = 128;
-    g.n_tiles[0] = cdiv(3 * d->F, 128);
+    g.bn[0] = tn;
+    g.n_tiles[0] = cdiv(3 * d->F, tn);
     g.k_iters[0] = cdiv(d->H, cs::BK);
     g.n_tiles[1] = d->heads;
     g.k_iters[1] = 0;
@@ -537,7 +545,10 @@ cs_status launch(cs_chain_s* p, cs::KParams& kp, const uint32_t* sched, int n_un
   cfg.numAttrs = n_attr;
   cudaError_t e;
   cs_status s;
-  if (p->d.kind == CS_CHAIN_ATTN) {
+  if (p->d.kind == CS_CHAIN_ATTN && p->cg == 2) {
+    if ((s = set_smem_attr<NS_A, SB_A, 2, true>()) != CS_OK) return s;
+    e = cudaLaunchKernelEx(&cfg, cs::cs_chain_kernel<NS_A, SB_A, 2, true>, kp);
+  } else if (p->d.kind == CS_CHAIN_ATTN) {
     if ((s = set_smem_attr<NS_A, SB_A, 1, true>()) != CS_OK) return s;
     e = cudaLaunchKernelEx(&cfg, cs::cs_chain_kernel<NS_A, SB_A, 1, true>, kp);
   } else if (p->cl == 4) {
@@ -558,7 +569,9 @@ cs_status launch(cs_chain_s* p, cs::KParams& kp, const uint32_t* sched, int n_un
 }
 
 // Map indices (ATTN): 0 X, 1 Wqkv, 2 QKV store, 3 QKV load, 4 O store, 5 O load, 6 Wo, 7 Y store.
-enum { AMAP_X = 0, AMAP_WQKV = 1, AMAP_QKVST = 2, AMAP_QKVLD = 3, AMAP_OST = 4, AMAP_OLD = 5, AMAP_WO = 6, AMAP_Y = 7 };
+// 8 K half: QKV loads of 64-row boxes (half a key block, attention on CTA pairs).
+enum { AMAP_X = 0, AMAP_WQKV = 1, AMAP_QKVST = 2, AMAP_QKVLD = 3, AMAP_OST = 4, AMAP_OLD = 5, AMAP_WO = 6, AMAP_Y = 7,
+       AMAP_K64 = 8 };
 
 void fill_attn_stages(const cs_chain_s* p, cs::KParams& kp) {
   const int b_major = p->d.weight_layout == CS_WEIGHTS_KN ? 1 : 0;
@@ -575,14 +588,14 @@ void fill_attn_stages(const cs_chain_s* p, cs::KParams& kp) {
   s0.k_iters = p->k_iters[0];
   s0.n_extent = 3 * F;
   s0.m_extent = M;
-  s0.bn = 128;
-  s0.mma_n = 128;
+  s0.bn = p->bn[0];
+  s0.mma_n = p->bn[0];
   s0.b_major = b_major;
   s0.map_a = AMAP_X;
   s0.map_b = AMAP_WQKV;
   s0.map_b2 = -1;
   s0.map_out = AMAP_QKVST;
-  s0.b_bytes = 128 * cs::BK * 2;
+  s0.b_bytes = (p->bn[0] / p->cg) * cs::BK * 2;
   s0.wait = cs::WAIT_NONE;
   s0.rel_tile = p->sems[0];
   s0.rel_row = rows0;
@@ -598,6 +611,7 @@ void fill_attn_stages(const cs_chain_s* p, cs::KParams& kp) {
   s1.m_extent = M;
   s1.bn = 128;
   s1.map_a = AMAP_QKVLD;
+  s1.map_k = AMAP_K64;
   s1.map_b = -1;
   s1.map_b2 = -1;
   s1.map_out = AMAP_OST;
@@ -605,7 +619,7 @@ void fill_attn_stages(const cs_chain_s* p, cs::KParams& kp) {
   s1.dep_tile = p->sems[0];
   s1.dep_row = rows0;
   s1.dep_ntiles = p->n_tiles[0];
-  s1.dep_bn = 128;
+  s1.dep_bn = p->bn[0];
   s1.stride = p->stride;
   s1.rel_tile = p->sems[1];
   s1.rel_row = rows1;
@@ -623,14 +637,14 @@ void fill_attn_stages(const cs_chain_s* p, cs::KParams& kp) {
   s2.k_iters = p->k_iters[2];
   s2.n_extent = H;
   s2.m_extent = M;
-  s2.bn = 128;
-  s2.mma_n = 128;
+  s2.bn = p->bn[2];
+  s2.mma_n = p->bn[2];
   s2.b_major = b_major;
   s2.map_a = AMAP_OLD;
   s2.map_b = AMAP_WO;
   s2.map_b2 = -1;
   s2.map_out = AMAP_Y;
-  s2.b_bytes = 128 * cs::BK * 2;
+  s2.b_bytes = (p->bn[2] / p->cg) * cs::BK * 2;
   s2.wait = wait_kind(p);
   s2.dep_tile = p->sems[1];
   s2.dep_row = rows1;
@@ -641,7 +655,8 @@ void fill_attn_stages(const cs_chain_s* p, cs::KParams& kp) {
   fill_split(p, 0, s0);
   fill_split(p, 1, s1);
   fill_split(p, 2, s2);
-  kp.acc_stride = 128;
+  // pairs: 256-column buffers, which attention units borrow for S and O
+  kp.acc_stride = p->cg == 2 ? 256 : 128;
 }
 
 void fill_attn_prefetch(const cs_chain_s* p, const cs_attn_args* a, cs::KParams& kp) {
@@ -655,8 +670,8 @@ cs_status bind_attn(cs_chain_s* p, const cs_attn_args* a) {
   const int M = p->d.M, H = p->d.H, F = p->d.F;
   cs_status s;
   if ((s = encode_act(p, AMAP_X, a->X, M, H, false)) != CS_OK) return s;
-  if ((s = encode_weight(p, AMAP_WQKV, a->Wqkv, H, 3 * F, 128)) != CS_OK) return s;
-  if ((s = encode_weight(p, AMAP_WO, a->Wo, F, H, 128)) != CS_OK) return s;
+  if ((s = encode_weight(p, AMAP_WQKV, a->Wqkv, H, 3 * F, p->bn[0] / p->cg)) != CS_OK) return s;
+  if ((s = encode_weight(p, AMAP_WO, a->Wo, F, H, p->bn[2] / p->cg)) != CS_OK) return s;
   if ((s = encode_act(p, AMAP_Y, a->Y, M, H, true)) != CS_OK) return s;
   return CS_OK;
 }
@@ -805,15 +820,18 @@ cs_status cs_chain_plan(const cs_chain_desc* desc, cs_chain_t* out) {
     if ((s = upload(&p->sched_stage[st], build_stage(g, st))) != CS_OK) return bail(s);
   p->num_sms = p->num_sms / g.cl * g.cl;
   // plan-owned intermediate maps (never re-encoded)
-  int owned[4];
+  int owned[5];
   int n_owned = 0;
   if (attn) {
     if ((s = encode_act(p, AMAP_QKVST, p->inter[0], desc->M, 3 * desc->F, true)) != CS_OK) return bail(s);
     if ((s = encode_act(p, AMAP_QKVLD, p->inter[0], desc->M, 3 * desc->F, false)) != CS_OK) return bail(s);
     if ((s = encode_act(p, AMAP_OST, p->inter[1], desc->M, desc->F, true)) != CS_OK) return bail(s);
     if ((s = encode_act(p, AMAP_OLD, p->inter[1], desc->M, desc->F, false)) != CS_OK) return bail(s);
-    owned[0] = AMAP_QKVST, owned[1] = AMAP_QKVLD, owned[2] = AMAP_OST, owned[3] = AMAP_OLD;
-    n_owned = 4;
+    if ((s = encode_2d(&p->maps[AMAP_K64], p->inter[0], desc->dtype == CS_BF16, 3 * desc->F, desc->M, 64, 64)) !=
+        CS_OK)
+      return bail(s);
+    owned[0] = AMAP_QKVST, owned[1] = AMAP_QKVLD, owned[2] = AMAP_OST, owned[3] = AMAP_OLD, owned[4] = AMAP_K64;
+    n_owned = 5;
   } else {
     if ((s = encode_act(p, MAP_HST, p->inter[0], desc->M, desc->F, true)) != CS_OK) return bail(s);
     if ((s = encode_act(p, MAP_HLD, p->inter[0], desc->M, desc->F, false)) != CS_OK) return bail(s);

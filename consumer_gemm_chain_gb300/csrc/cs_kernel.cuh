@@ -78,6 +78,7 @@ struct StageP {
   int mma_n;       // UMMA N (bn, or 256 for gate|up with bn = 128)
   int b_major;     // 0: weights K-major ([N,K]); 1: MN-major ([K,N])
   int map_a, map_b, map_b2, map_out;
+  int map_k;  // attention on a CTA pair: QKV loads of 64-row boxes (half a key block)
   int b_bytes;     // bytes of the B operand per pipeline stage and CTA
   const __nv_bfloat16* bias_bf16;  // exactly one of these two is used (per dtype)
   const __half* bias_f16;
@@ -115,7 +116,7 @@ struct StageP {
 };
 
 struct KParams {
-  CUtensorMap maps[8];
+  CUtensorMap maps[9];
   StageP st[3];
   const uint32_t* sched;
   int n_units;
@@ -830,35 +831,59 @@ constexpr uint32_t ATT_O_COL = 384;
 
 // TMA: three 32 KB slots per key block: [Q dims 0-63 | K_j dims 0-63],
 // [Q dims 64-127 | K_j dims 64-127], [V_j dims 0-63 | V_j dims 64-127] (128 rows each).
-template <int NS, int STAGE_BYTES>
+// CG = 2: a unit is two consecutive query blocks of one head on a CTA pair; each
+// CTA loads its own Q rows, half of each K block's 128 keys (the N of Q K^T)
+// and half of V's 128 head dimensions (the N of P V); completion goes to the
+// pair leader's full barrier as in a pair GEMM.
+template <int NS, int STAGE_BYTES, int CG>
 __device__ bool tma_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, RingPos& rp, uint32_t unit,
-                              uint32_t q) {
+                              uint32_t q, uint32_t rank) {
   const StageP& S = p.st[unit_stage(unit)];
   const uint32_t tidx = sc->uq_idx[q];
   const int i = unit_m(unit), h = unit_n(unit);
   const int F = S.heads * 128;
-  const int nslots = 3 * (i + 1);
+  const int qb = i * CG + static_cast<int>(rank);  // this CTA's query block
+  const int nkb = (i + 1) * CG;                    // key blocks of the unit
+  const int nslots = 3 * nkb;
   const int claim_at = nslots > CLAIM_AHEAD ? nslots - CLAIM_AHEAD : 0;
   int ready = 0;
-  // every key block 0..i (and the query block i) must be complete first
-  if (p.waits && S.wait != WAIT_NONE && !tma_wait_ready(sc, q, i + 1, ready, p)) return false;
+  // every key block of the unit (and so every query block) must be complete first
+  if (p.waits && S.wait != WAIT_NONE && !tma_wait_ready(sc, q, nkb, ready, p)) return false;
   const CUtensorMap* m = &p.maps[S.map_a];
   int sidx = 0;
-  for (int j = 0; j <= i; ++j) {
+  for (int j = 0; j < nkb; ++j) {
     for (int part = 0; part < 3; ++part, ++sidx) {
-      if (sidx == claim_at) mbar_arrive(&sc->claim_req);
+      if (rank == 0 && sidx == claim_at) mbar_arrive(&sc->claim_req);
       if (!wait_bar(&sc->empty[rp.slot], rp.phase ^ 1u, sc, p, 1)) return false;
-      if (sidx == 0) trace_put(p, tidx, 0, 1, 4, globaltimer());
-      if (sidx == nslots - 1) trace_put(p, tidx, 0, 1, 5, globaltimer());
+      if (sidx == 0) trace_put(p, tidx, rank, CG, 4, globaltimer());
+      if (sidx == nslots - 1) trace_put(p, tidx, rank, CG, 5, globaltimer());
       uint8_t* s0 = ring + rp.slot * STAGE_BYTES;
-      uint64_t* bar = &sc->full[rp.slot];
-      mbar_arrive_expect_tx(bar, 2 * TILE_A_BYTES);
-      if (part < 2) {
-        tma_load_2d(s0, m, h * 128 + part * 64, i * BM, bar);                   // Q_i dims chunk
-        tma_load_2d(s0 + TILE_A_BYTES, m, F + h * 128 + part * 64, j * BM, bar);  // K_j dims chunk
+      if constexpr (CG == 1) {
+        uint64_t* bar = &sc->full[rp.slot];
+        mbar_arrive_expect_tx(bar, 2 * TILE_A_BYTES);
+        if (part < 2) {
+          tma_load_2d(s0, m, h * 128 + part * 64, qb * BM, bar);                   // Q_i dims chunk
+          tma_load_2d(s0 + TILE_A_BYTES, m, F + h * 128 + part * 64, j * BM, bar);  // K_j dims chunk
+        } else {
+          tma_load_2d(s0, m, 2 * F + h * 128, j * BM, bar);                       // V_j dims 0-63
+          tma_load_2d(s0 + TILE_A_BYTES, m, 2 * F + h * 128 + 64, j * BM, bar);    // V_j dims 64-127
+        }
       } else {
-        tma_load_2d(s0, m, 2 * F + h * 128, j * BM, bar);                       // V_j dims 0-63
-        tma_load_2d(s0 + TILE_A_BYTES, m, 2 * F + h * 128 + 64, j * BM, bar);    // V_j dims 64-127
+        const uint32_t bar_addr = mapa_shared(&sc->full[rp.slot], 0);
+        const uint32_t bytes = part < 2 ? TILE_A_BYTES + TILE_A_BYTES / 2 : TILE_A_BYTES;
+        if (rank == 0)
+          mbar_arrive_expect_tx(&sc->full[rp.slot], bytes);
+        else
+          mbar_expect_tx_remote(bar_addr, bytes);
+        if (part < 2) {
+          // Q rows of this CTA's query block; keys rank*64 .. +63 of block j
+          tma_load_2d_pair(s0, m, h * 128 + part * 64, qb * BM, bar_addr);
+          tma_load_2d_pair(s0 + TILE_A_BYTES, &p.maps[S.map_k], F + h * 128 + part * 64, j * BM + rank * 64,
+                           bar_addr);
+        } else {
+          // head dimensions rank*64 .. +63 of V_j, all 128 keys
+          tma_load_2d_pair(s0, m, 2 * F + h * 128 + rank * 64, j * BM, bar_addr);
+        }
       }
       sc->issued_parity[rp.slot] = static_cast<int>(rp.phase);
       rp.next<NS>();
@@ -867,15 +892,26 @@ __device__ bool tma_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
   return true;
 }
 
-template <int NS, int STAGE_BYTES>
+// CG = 2 (pair leader): S = Q K^T and O_j = P V are 256-row cta_group::2 MMAs;
+// S and O live in the accumulator buffer the unit takes like a GEMM tile
+// (S in its first 128 columns, O_j in the next 128), so 256-wide GEMM tiles
+// keep both buffers.
+template <int NS, int STAGE_BYTES, int CG>
 __device__ bool mma_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, uint8_t* pbuf, RingPos& rp,
-                              uint32_t unit, uint32_t& p_phase) {
+                              uint32_t unit, uint32_t& p_phase, uint32_t& acc, uint32_t& acc_phase) {
   const int i = unit_m(unit);
-  const uint32_t idesc_s = make_idesc_f16(p.bf16, 0, BM, 128);  // Q K^T: both operands K-major
-  const uint32_t idesc_o = make_idesc_f16(p.bf16, 1, BM, 128);  // P V: V is MN-major
-  const uint32_t s_tm = sc->tmem_base + ATT_S_COL, o_tm = sc->tmem_base + ATT_O_COL;
+  const int nkb = (i + 1) * CG;
+  const uint32_t idesc_s = make_idesc_f16(p.bf16, 0, BM * CG, 128);  // Q K^T: both operands K-major
+  const uint32_t idesc_o = make_idesc_f16(p.bf16, 1, BM * CG, 128);  // P V: V is MN-major
+  uint32_t s_tm = sc->tmem_base + ATT_S_COL, o_tm = sc->tmem_base + ATT_O_COL;
+  if constexpr (CG == 2) {
+    if (!wait_bar(&sc->tempty[acc], acc_phase ^ 1u, sc, p, 2)) return false;
+    tc_fence_after();
+    s_tm = sc->tmem_base + acc * static_cast<uint32_t>(p.acc_stride);
+    o_tm = s_tm + 128;
+  }
   const uint32_t pb = smem_u32(pbuf);
-  for (int j = 0; j <= i; ++j) {
+  for (int j = 0; j < nkb; ++j) {
     for (int part = 0; part < 2; ++part) {
       if (!wait_bar(&sc->full[rp.slot], rp.phase, sc, p, 3)) return false;
       tc_fence_after();
@@ -883,14 +919,15 @@ __device__ bool mma_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
       const uint64_t ad = smem_desc_sw128(sa, 16, 1024), bd = smem_desc_sw128(sa + TILE_A_BYTES, 16, 1024);
 #pragma unroll
       for (int kk = 0; kk < BK / UMMA_K; ++kk)
-        tc_mma_f16<1>(s_tm, ad + static_cast<uint64_t>(kk * 2), bd + static_cast<uint64_t>(kk * 2), idesc_s,
-                      (part | kk) != 0 ? 1u : 0u);
-      tc_commit<1>(&sc->empty[rp.slot]);
+        tc_mma_f16<CG>(s_tm, ad + static_cast<uint64_t>(kk * 2), bd + static_cast<uint64_t>(kk * 2), idesc_s,
+                       (part | kk) != 0 ? 1u : 0u);
+      tc_commit<CG>(&sc->empty[rp.slot]);
       rp.next<NS>();
     }
-    tc_commit<1>(&sc->s_full);
-    // P_j is in shared memory and the previous O_j has been read back
-    if (!wait_bar(&sc->p_full, p_phase, sc, p, 12)) return false;
+    tc_commit<CG>(&sc->s_full);
+    // P_j is in shared memory (of both CTAs) and the previous O_j has been read back;
+    // a pair's peer publishes its P with cluster-scope release arrivals
+    if (!wait_bar<NS, CG == 2>(&sc->p_full, p_phase, sc, p, 12)) return false;
     p_phase ^= 1u;
     tc_fence_after();
     if (!wait_bar(&sc->full[rp.slot], rp.phase, sc, p, 3)) return false;
@@ -901,27 +938,39 @@ __device__ bool mma_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
     for (int kk = 0; kk < 8; ++kk) {
       // P: chunk of 64 keys per 16 KB, +32 bytes per 16 keys; V: +16 key rows (2 KB)
       const uint64_t a = smem_desc_sw128(pb + (kk >> 2) * (BM * 128), 16, 1024) + static_cast<uint64_t>((kk & 3) * 2);
-      tc_mma_f16<1>(o_tm, a, vd + static_cast<uint64_t>(kk * 128), idesc_o, kk != 0 ? 1u : 0u);
+      tc_mma_f16<CG>(o_tm, a, vd + static_cast<uint64_t>(kk * 128), idesc_o, kk != 0 ? 1u : 0u);
     }
-    tc_commit<1>(&sc->empty[rp.slot]);
+    tc_commit<CG>(&sc->empty[rp.slot]);
     rp.next<NS>();
-    tc_commit<1>(&sc->o_full);
+    tc_commit<CG>(&sc->o_full);
+  }
+  if constexpr (CG == 2) {
+    // hand the accumulator buffer back through the GEMM protocol
+    tc_commit<CG>(&sc->tfull[acc]);
+    acc ^= 1u;
+    if (acc == 0u) acc_phase ^= 1u;
   }
   return true;
 }
 
-// Epilogue warps: online softmax for one query row per thread.
-template <int NS>
+// Epilogue warps: online softmax for one query row per thread.  CG = 2: this
+// CTA's query block is the unit's block rank; its rows see every key block of
+// the unit (the first query block's last one is entirely in its future).
+template <int NS, int CG>
 __device__ bool epi_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* staging, uint32_t unit, uint32_t& s_phase,
-                              uint32_t& o_phase, int& last_buf, uint32_t tidx) {
+                              uint32_t& o_phase, int& last_buf, uint32_t tidx, uint32_t& tacc, uint32_t& tacc_phase,
+                              uint32_t rank) {
   const StageP& S = p.st[unit_stage(unit)];
   const int i = unit_m(unit), h = unit_n(unit);
+  const int qb = i * CG + static_cast<int>(rank);  // this CTA's query block
+  const int nkb = (i + 1) * CG;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;
   const int r = q * 32 + lane;  // query row within the block
   const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-  const uint32_t s_tm = sc->tmem_base + lane_base + ATT_S_COL;
-  const uint32_t o_tm = sc->tmem_base + lane_base + ATT_O_COL;
+  const uint32_t tcols = CG == 1 ? ATT_S_COL : tacc * static_cast<uint32_t>(p.acc_stride);
+  const uint32_t s_tm = sc->tmem_base + lane_base + tcols;
+  const uint32_t o_tm = s_tm + (ATT_O_COL - ATT_S_COL);
   const float sl2 = S.softmax_scale_log2;
   float acc[128];
 #pragma unroll
@@ -931,12 +980,14 @@ __device__ bool epi_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
   if (lane == 0) tma_store_wait_read<0>();
   __syncwarp();
   last_buf = -1;
-  for (int j = 0; j <= i; ++j) {
+  for (int j = 0; j < nkb; ++j) {
     if (!wait_bar(&sc->s_full, s_phase, sc, p, 13)) return false;
     s_phase ^= 1u;
     tc_fence_after();
-    if (j == 0 && threadIdx.x == EPI_WARP0 * 32) trace_put(p, tidx, 0, 1, 6, globaltimer());
-    const bool diag = j == i;
+    if (j == 0 && threadIdx.x == EPI_WARP0 * 32) trace_put(p, tidx, rank, CG, 6, globaltimer());
+    // key column c of block j is visible to row r iff j*128 + c <= qb*128 + r
+    const bool diag = j >= qb;
+    const int lim = (qb - j) * 128 + r;
     // pass 1: row maximum of the scaled, masked logits
     float mx = -INFINITY;
 #pragma unroll
@@ -946,7 +997,7 @@ __device__ bool epi_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
       tc_wait_ld();
 #pragma unroll
       for (int t = 0; t < 32; ++t) {
-        const float s = (diag && c * 32 + t > r) ? -INFINITY : __uint_as_float(v[t]) * sl2;
+        const float s = (diag && c * 32 + t > lim) ? -INFINITY : __uint_as_float(v[t]) * sl2;
         mx = fmaxf(mx, s);
       }
     }
@@ -976,8 +1027,8 @@ __device__ bool epi_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
       uint32_t w[16];
 #pragma unroll
       for (int t = 0; t < 32; t += 2) {
-        const float p0 = (diag && c * 32 + t > r) ? 0.0f : exp2f(fmaf(__uint_as_float(v[t]), sl2, -m_new));
-        const float p1 = (diag && c * 32 + t + 1 > r) ? 0.0f : exp2f(fmaf(__uint_as_float(v[t + 1]), sl2, -m_new));
+        const float p0 = (diag && c * 32 + t > lim) ? 0.0f : exp2f(fmaf(__uint_as_float(v[t]), sl2, -m_new));
+        const float p1 = (diag && c * 32 + t + 1 > lim) ? 0.0f : exp2f(fmaf(__uint_as_float(v[t + 1]), sl2, -m_new));
         lsum += p0 + p1;
         w[t >> 1] = pack2(p0, p1, p.bf16);
       }
@@ -998,7 +1049,12 @@ __device__ bool epi_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
     fence_proxy_async_shared();
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&sc->p_full);
+    if (lane == 0) {
+      if constexpr (CG == 1)
+        mbar_arrive(&sc->p_full);
+      else
+        mbar_arrive_cluster(mapa_shared(&sc->p_full, 0));  // the pair leader issues P V
+    }
   }
   if (!wait_bar(&sc->o_full, o_phase, sc, p, 14)) return false;
   o_phase ^= 1u;
@@ -1022,7 +1078,7 @@ __device__ bool epi_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
     stage_row(staging, c, r, w);
     fence_proxy_async_shared();
     __syncwarp();
-    const int grow = i * BM + q * 32;
+    const int grow = qb * BM + q * 32;
     if (grow < S.m_extent) {
       if (lane == 0) {
         tma_store_2d(&p.maps[S.map_out], staging + c * (BM * 128) + q * 32 * 128, h * 128 + c * 64, grow);
@@ -1031,11 +1087,21 @@ __device__ bool epi_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
       last_buf = c;
     }
   }
+  if constexpr (CG == 2) {
+    // the unit's accumulator buffer goes back to the MMA (both CTAs' warps)
+    if (!wait_bar(&sc->tfull[tacc], tacc_phase, sc, p, 4)) return false;
+    tc_fence_after();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive_cluster(mapa_shared(&sc->tempty[tacc], 0));
+    tacc ^= 1u;
+    if (tacc == 0u) tacc_phase ^= 1u;
+  }
   if (S.rel_tile != nullptr) {
-    release_tile(p, S, i, h, lane);
+    release_tile(p, S, qb, h, lane);
     last_buf = -1;
   }
-  if (threadIdx.x == EPI_WARP0 * 32) trace_put(p, tidx, 0, 1, 7, globaltimer());
+  if (threadIdx.x == EPI_WARP0 * 32) trace_put(p, tidx, rank, CG, 7, globaltimer());
   return true;
 }
 
@@ -1057,10 +1123,12 @@ __device__ void sched_poll_attn(const KParams& p, const StageP& S, SmemCtl<NS>* 
         if (S.wait == WAIT_ROW) {
           done = static_cast<int32_t>(ld_relaxed_gpu(S.dep_row + j) - epoch1 * static_cast<uint32_t>(nt)) >= 0;
         } else {
+          // the producer tile holding columns (part*heads + h)*128 .. +127 (Q, K, V of head h)
 #pragma unroll
           for (int part = 0; part < 3; ++part)
-            done = done && static_cast<int32_t>(ld_relaxed_gpu(S.dep_tile + static_cast<size_t>(j) * nt + h +
-                                                               part * S.heads) - epoch1) >= 0;
+            done = done && static_cast<int32_t>(ld_relaxed_gpu(S.dep_tile + static_cast<size_t>(j) * nt +
+                                                               (part * S.heads + h) * 128 / S.dep_bn) -
+                                                epoch1) >= 0;
         }
       }
       const uint32_t bad = __ballot_sync(0xFFFFFFFFu, !done);
@@ -1222,7 +1290,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
     mbar_init(&sc->mb_empty, CL - 1 > 0 ? CL - 1 : 1);  // every peer CTA takes the index
     mbar_init(&sc->s_full, 1);
     mbar_init(&sc->s_empty, 4);
-    mbar_init(&sc->p_full, 4);
+    mbar_init(&sc->p_full, 4 * CG);  // every epilogue warp of the unit's CTAs
     mbar_init(&sc->o_full, 1);
     mbar_init(&sc->o_empty, 4);
     mbar_init(&sc->drain, 1);
@@ -1230,7 +1298,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
     sc->tma_seq = 0;
     sc->tma_kb = 0;
     fence_mbar_init();
-    for (int i = 0; i < 8; ++i) prefetch_tmap(&p.maps[i]);
+    for (int i = 0; i < 9; ++i) prefetch_tmap(&p.maps[i]);
   }
   if (warp == 1) {
     tmem_alloc<CG>(&sc->tmem_base, TMEM_COLS);
@@ -1308,7 +1376,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
         sched_poll_gemm<NS>(p, S, sc, q, unit_m(unit) * CL + static_cast<int>(rank), epoch1, unit, lane);
       else if constexpr (ATTN)
         if (consumer && S.kind == STAGE_ATTN)
-          sched_poll_attn<NS>(p, S, sc, q, unit_m(unit), unit_n(unit), epoch1, unit, lane);
+          sched_poll_attn<NS>(p, S, sc, q, (unit_m(unit) + 1) * CG - 1, unit_n(unit), epoch1, unit, lane);
       if (lane == 0) trace_put(p, idx, rank, CL, 3, globaltimer());
       if (++q == UQ) {
         q = 0;
@@ -1325,8 +1393,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
         const uint32_t unit = sc->uq[q];
         if (unit != UNIT_END && p.st[unit_stage(unit)].kind == STAGE_GEMM)
           ok = tma_gemm_unit<NS, STAGE_BYTES, CG, CL>(p, sc, ring, rp, unit, q, rank);
-        else if constexpr (CG == 1 && ATTN)
-          if (unit != UNIT_END) ok = tma_attn_unit<NS, STAGE_BYTES>(p, sc, ring, rp, unit, q);
+        else if constexpr (ATTN)
+          if (unit != UNIT_END) ok = tma_attn_unit<NS, STAGE_BYTES, CG>(p, sc, ring, rp, unit, q, rank);
         mbar_arrive(&sc->uq_empty[q]);
         if (++q == UQ) {
           q = 0;
@@ -1366,14 +1434,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
           qphase ^= 1u;
         }
         if (unit == UNIT_END) break;
-        if (pair_leader && p.st[unit_stage(unit)].kind == STAGE_GEMM) {
-          ok = mma_gemm_unit<NS, STAGE_BYTES, CG, CL>(p, sc, ring, rp, unit, acc, acc_phase, rank);
-          issued = true;
-        } else if constexpr (CL == 4) {
-          if (p.st[unit_stage(unit)].kind == STAGE_GEMM) ok = fwd_gemm_unit<NS>(p, sc, rp, unit, rank);
-        } else if constexpr (CG == 1 && ATTN) {
-          ok = mma_attn_unit<NS, STAGE_BYTES>(p, sc, ring, staging, rp, unit, p_phase);
-          issued = true;
+        if (p.st[unit_stage(unit)].kind == STAGE_GEMM) {
+          if (pair_leader) {
+            ok = mma_gemm_unit<NS, STAGE_BYTES, CG, CL>(p, sc, ring, rp, unit, acc, acc_phase, rank);
+            issued = true;
+          } else if constexpr (CL == 4) {
+            ok = fwd_gemm_unit<NS>(p, sc, rp, unit, rank);
+          }
+        } else if constexpr (ATTN) {
+          if (pair_leader) {
+            ok = mma_attn_unit<NS, STAGE_BYTES, CG>(p, sc, ring, staging, rp, unit, p_phase, acc, acc_phase);
+            issued = true;
+          }
         }
       }
       // every MMA this thread issued completes before TMEM is freed
@@ -1404,8 +1476,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
       if (unit == UNIT_END) break;
       if (p.st[unit_stage(unit)].kind == STAGE_GEMM)
         ok = epi_gemm_unit<NS, CG, CL>(p, sc, staging, unit, acc, acc_phase, last_buf, rank, tidx, epoch1);
-      else if constexpr (CG == 1 && ATTN)
-        ok = epi_attn_unit<NS>(p, sc, staging, unit, s_phase, o_phase, last_buf, tidx);
+      else if constexpr (ATTN)
+        ok = epi_attn_unit<NS, CG>(p, sc, staging, unit, s_phase, o_phase, last_buf, tidx, acc, acc_phase, rank);
     }
     if (lane == 0) tma_store_wait_all<0>();
     __syncwarp();

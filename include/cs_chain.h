@@ -112,7 +112,10 @@ typedef struct cs_chain_desc {
                           cluster that fetch every weight box once and multicast it
                           to both pairs); 256 and 512 need tile_n = 256 and the GeLU
                           MLP.  0 = auto (512 where it adds no padding rows over 256,
-                          from M = 512).  Semaphores stay per 128-row block.         */
+                          from M = 512).  The attention chain runs 128 (with
+                          tile_n 128) or 256 (with tile_n 256: attention units of
+                          two query blocks on a CTA pair); auto 256 from M = 512.
+                          Semaphores stay per 128-row block.                        */
   int split_k;         /* K-splits per GEMM tile: 0 = auto (split when a stage has
                           fewer tiles than the grid, small M), 1 = never, 2..15 = that
                           many for every GEMM stage.  Splits write fp32 partial tiles

@@ -97,12 +97,15 @@ def test_schedule_is_dependency_ordered(cs, M, H, F, sms, lag, group, split, til
     _check_order(dec, deps)
 
 
+@pytest.mark.parametrize("tile_m", [128, 256])
 @pytest.mark.parametrize("M,lag,group", [(1, -1, 0), (300, -1, 0), (2048, -1, 0), (2048, 2, 3), (1000, 0, 1)])
-def test_attention_schedule_is_dependency_ordered(cs, M, lag, group):
-    d = cs.cs_chain_desc_init(kind="attn", M=M, H=12288, F=1536, heads=12, head_dim=128, lag=lag, group_m=group)
+def test_attention_schedule_is_dependency_ordered(cs, M, lag, group, tile_m):
+    d = cs.cs_chain_desc_init(kind="attn", M=M, H=12288, F=1536, heads=12, head_dim=128, lag=lag, group_m=group,
+                              tile_m=tile_m)
     dec = [cs.decode_unit(u) for u in cs.cs_schedule_build(d, 148)]
-    m_tiles = -(-M // 128)
-    nt = [36, 12, 96]
+    m_tiles = -(-M // tile_m)
+    tn = tile_m  # 128 x 128 single-SM tiles or 256 x 256 pair tiles
+    nt = [4608 // tn, 12, 12288 // tn]
     splits = {}
     for s, m, n, k in dec:
         splits[(s, m, n)] = max(splits.get((s, m, n), 0), k + 1)
@@ -111,8 +114,9 @@ def test_attention_schedule_is_dependency_ordered(cs, M, lag, group):
 
     def deps(u):
         s, m, n, _ = u
-        if s == 1:   # causal: key blocks 0..m of head n (Q, K and V tiles)
-            return [(0, j, t, k) for j in range(m + 1) for t in (n, n + 12, n + 24) for k in range(splits[(0, j, t)])]
+        if s == 1:   # causal: key blocks up to the unit's last query block (Q, K and V tiles of head n)
+            tiles = {(p * 12 + n) * 128 // tn for p in range(3)}
+            return [(0, j, t, k) for j in range(m + 1) for t in tiles for k in range(splits[(0, j, t)])]
         if s == 2:   # every head of the same row block
             return [(1, m, h, 0) for h in range(12)]
         return []

@@ -22,12 +22,17 @@ def _oracle(inp):
     return oracle.attention_chain(inp.X, inp.Wqkv, inp.Wo, heads=inp.F // 128, head_dim=128, return_parts=True)
 
 
+@pytest.mark.parametrize("tile_m", [128, 256])
 @pytest.mark.parametrize("layout", ["nk", "kn"])
 @pytest.mark.parametrize("M,H,heads", [(1, 256, 1), (100, 256, 2), (128, 512, 1), (300, 384, 3), (513, 256, 2)])
-def test_attention_chain_parity(M, H, heads, layout):
+def test_attention_chain_parity(M, H, heads, layout, tile_m):
+    """tile_m 256: 256 x 256 GEMM tiles and attention units of two query blocks
+    on CTA pairs (each CTA holds half of every key block and half of V's head
+    dimensions; S and O borrow a 256-column accumulator buffer)."""
     inp = cs_inputs.make_custom("attn", M, H, heads * 128, seed=31)
     dev = device_tensors(inp, layout)
-    with plan_for(inp, "row", layout) as plan:
+    with plan_for(inp, "row", layout, tile_m=tile_m) as plan:
+        assert cs.cs_chain_query(plan)["tile_m"] == tile_m
         Y = forward(plan, dev)
         QKV = intermediate(plan, 0, M, 3 * inp.F, inp.dtype)
         O = intermediate(plan, 1, M, inp.F, inp.dtype)
@@ -37,12 +42,13 @@ def test_attention_chain_parity(M, H, heads, layout):
     assert oracle.rel_err(Y.cpu(), Yref) <= TOL
 
 
-def test_attention_policies_bit_identical_and_flags():
+@pytest.mark.parametrize("tile_m", [128, 256])
+def test_attention_policies_bit_identical_and_flags(tile_m):
     inp = cs_inputs.make_custom("attn", 520, 512, 256, seed=32)
     dev = device_tensors(inp, "nk")
     outs = {}
     for pol in ("tile", "row", "strided", "stream"):
-        with plan_for(inp, pol, "nk", group_m=1) as plan:
+        with plan_for(inp, pol, "nk", group_m=1, tile_m=tile_m) as plan:
             for _ in range(2):
                 outs[pol] = forward(plan, dev).cpu()
             q = cs.cs_chain_query(plan)
@@ -57,12 +63,13 @@ def test_attention_policies_bit_identical_and_flags():
         assert torch.equal(v, outs["row"]), k
 
 
-def test_attention_delay_injection_never_changes_a_bit():
+@pytest.mark.parametrize("tile_m", [128, 256])
+def test_attention_delay_injection_never_changes_a_bit(tile_m):
     inp = cs_inputs.make_custom("attn", 400, 512, 384, seed=33)
     dev = device_tensors(inp, "nk")
     ref = None
     for pol in ("row", "tile"):
-        with plan_for(inp, pol, "nk", group_m=1) as plan:
+        with plan_for(inp, pol, "nk", group_m=1, tile_m=tile_m) as plan:
             q = cs.cs_chain_query(plan)
             for seed in range(2):
                 g = torch.Generator().manual_seed(200 + seed)
@@ -75,10 +82,11 @@ def test_attention_delay_injection_never_changes_a_bit():
                 assert torch.equal(Y, ref), (pol, seed)
 
 
-def test_attention_missing_release_times_out():
+@pytest.mark.parametrize("tile_m", [128, 256])
+def test_attention_missing_release_times_out(tile_m):
     inp = cs_inputs.make_custom("attn", 256, 256, 256, seed=34)
     dev = device_tensors(inp, "nk")
-    with plan_for(inp, "tile", "nk", spin_timeout_ns=20_000_000) as plan:
+    with plan_for(inp, "tile", "nk", spin_timeout_ns=20_000_000, tile_m=tile_m) as plan:
         good = forward(plan, dev).cpu()
         cs.cs_chain_debug_skip_release(plan, 1, 0)  # attention unit (block 0, head 0)
         Y = torch.empty_like(dev["X"])
@@ -98,3 +106,22 @@ def test_gpt3_attention_shard(M):
         Y = forward(plan, dev).cpu()
     Yref, _, _ = _oracle(inp)
     assert oracle.rel_err(Y, Yref) <= TOL
+
+
+@pytest.mark.parametrize("M", (300, 1024, 2048))
+def test_attention_pair_tiles_agree_with_single_sm_tiles(M):
+    """128 x 128 single-SM tiles and 256 x 256 pair tiles (with two-query-block
+    attention units) follow the same K order per output element but different
+    tcgen05 instruction shapes, whose fp32 partial sums may round differently:
+    the two outputs agree to a few fp16 ulps (a masking or indexing slip would
+    show far above that) and each matches the oracle."""
+    inp = cs_inputs.make_inputs("attn", M=M, seed=0)
+    dev = device_tensors(inp, "nk")
+    outs = {}
+    for tm in (128, 256):
+        with plan_for(inp, "row", "nk", tile_m=tm) as plan:
+            outs[tm] = forward(plan, dev).cpu()
+    Yref, _, _ = _oracle(inp)
+    assert oracle.rel_err(outs[128], Yref) <= TOL
+    assert oracle.rel_err(outs[256], Yref) <= TOL
+    assert oracle.rel_err(outs[256], outs[128]) <= 1e-3
