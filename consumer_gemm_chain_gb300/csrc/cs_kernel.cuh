@@ -1002,7 +1002,7 @@ __device__ bool epi_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
       }
     }
     const float m_new = fmaxf(m_run, mx);
-    const float alpha = exp2f(m_run - m_new);
+    const float alpha = ex2_approx(m_run - m_new);
     if (j > 0) {
       // fold O_{j-1} (computed against m_{j-1}) into the accumulator
       if (!wait_bar(&sc->o_full, o_phase, sc, p, 14)) return false;
@@ -1027,8 +1027,8 @@ __device__ bool epi_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
       uint32_t w[16];
 #pragma unroll
       for (int t = 0; t < 32; t += 2) {
-        const float p0 = (diag && c * 32 + t > lim) ? 0.0f : exp2f(fmaf(__uint_as_float(v[t]), sl2, -m_new));
-        const float p1 = (diag && c * 32 + t + 1 > lim) ? 0.0f : exp2f(fmaf(__uint_as_float(v[t + 1]), sl2, -m_new));
+        const float p0 = (diag && c * 32 + t > lim) ? 0.0f : ex2_approx(fmaf(__uint_as_float(v[t]), sl2, -m_new));
+        const float p1 = (diag && c * 32 + t + 1 > lim) ? 0.0f : ex2_approx(fmaf(__uint_as_float(v[t + 1]), sl2, -m_new));
         lsum += p0 + p1;
         w[t >> 1] = pack2(p0, p1, p.bf16);
       }

