@@ -156,6 +156,7 @@ struct SmemCtl {
   uint64_t tfull[2], tempty[2];
   uint64_t uq_full[UQ], uq_empty[UQ];
   uint64_t s_full, s_empty, p_full, o_full, o_empty;
+  uint64_t s_full_b;  // pair attention: S of odd key blocks (its own phases)
   uint64_t drain;
   uint64_t claim_req;       // TMA warp -> scheduler: claim the next unit now
   uint64_t mb_full, mb_empty;  // pair mode: leader -> peer unit mailbox
@@ -851,8 +852,25 @@ __device__ bool tma_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
   if (p.waits && S.wait != WAIT_NONE && !tma_wait_ready(sc, q, nkb, ready, p)) return false;
   const CUtensorMap* m = &p.maps[S.map_a];
   int sidx = 0;
-  for (int j = 0; j < nkb; ++j) {
-    for (int part = 0; part < 3; ++part, ++sidx) {
+  // CG = 2: the MMA computes S for key block j+1 before P V of block j (two S
+  // buffers), so the slots go Q|K of blocks 0 and 1, V_0, Q|K_2, V_1, ...
+  for (int step = 0; step < 3 * nkb; ++step, ++sidx) {
+    int j, part;
+    if constexpr (CG == 1) {
+      j = step / 3, part = step % 3;
+    } else if (step < 4) {
+      j = step >> 1, part = step & 1;  // Q|K of key blocks 0 and 1
+    } else {
+      const int t = step - 4, jj = t / 3, r3 = t % 3;
+      if (jj <= nkb - 3) {
+        // V_jj, then Q|K of key block jj + 2
+        j = r3 == 0 ? jj : jj + 2;
+        part = r3 == 0 ? 2 : r3 - 1;
+      } else {
+        j = nkb - 2 + r3, part = 2;  // the last two V blocks
+      }
+    }
+    {
       if (rank == 0 && sidx == claim_at) mbar_arrive(&sc->claim_req);
       if (!wait_bar(&sc->empty[rp.slot], rp.phase ^ 1u, sc, p, 1)) return false;
       if (sidx == 0) trace_put(p, tidx, rank, CG, 4, globaltimer());
@@ -892,10 +910,11 @@ __device__ bool tma_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
   return true;
 }
 
-// CG = 2 (pair leader): S = Q K^T and O_j = P V are 256-row cta_group::2 MMAs;
-// S and O live in the accumulator buffer the unit takes like a GEMM tile
-// (S in its first 128 columns, O_j in the next 128), so 256-wide GEMM tiles
-// keep both buffers.
+// CG = 2 (pair leader): S = Q K^T and O_j = P V are 256-row cta_group::2 MMAs.
+// The unit takes both accumulator buffers like two GEMM tiles: S_j alternates
+// between the halves of the first, O_j uses the second, so S_{j+1} is computed
+// while the epilogue still works on S_j (the ring delivers Q|K of blocks 0 and
+// 1, then V_j followed by Q|K of block j+2).
 template <int NS, int STAGE_BYTES, int CG>
 __device__ bool mma_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, uint8_t* pbuf, RingPos& rp,
                               uint32_t unit, uint32_t& p_phase, uint32_t& acc, uint32_t& acc_phase) {
@@ -903,15 +922,10 @@ __device__ bool mma_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
   const int nkb = (i + 1) * CG;
   const uint32_t idesc_s = make_idesc_f16(p.bf16, 0, BM * CG, 128);  // Q K^T: both operands K-major
   const uint32_t idesc_o = make_idesc_f16(p.bf16, 1, BM * CG, 128);  // P V: V is MN-major
-  uint32_t s_tm = sc->tmem_base + ATT_S_COL, o_tm = sc->tmem_base + ATT_O_COL;
-  if constexpr (CG == 2) {
-    if (!wait_bar(&sc->tempty[acc], acc_phase ^ 1u, sc, p, 2)) return false;
-    tc_fence_after();
-    s_tm = sc->tmem_base + acc * static_cast<uint32_t>(p.acc_stride);
-    o_tm = s_tm + 128;
-  }
   const uint32_t pb = smem_u32(pbuf);
-  for (int j = 0; j < nkb; ++j) {
+  // one full barrier per S buffer: two S in flight must never complete two
+  // phases of one barrier before the epilogue has seen the first
+  auto mma_s = [&](uint32_t s_tm, uint64_t* s_bar) -> bool {
     for (int part = 0; part < 2; ++part) {
       if (!wait_bar(&sc->full[rp.slot], rp.phase, sc, p, 3)) return false;
       tc_fence_after();
@@ -924,9 +938,12 @@ __device__ bool mma_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
       tc_commit<CG>(&sc->empty[rp.slot]);
       rp.next<NS>();
     }
-    tc_commit<CG>(&sc->s_full);
-    // P_j is in shared memory (of both CTAs) and the previous O_j has been read back;
-    // a pair's peer publishes its P with cluster-scope release arrivals
+    tc_commit<CG>(s_bar);
+    return true;
+  };
+  auto mma_pv = [&](uint32_t o_tm) -> bool {
+    // P_j is in shared memory (of both CTAs) and the previous O_j has been read
+    // back; a pair's peer publishes its P with cluster-scope release arrivals
     if (!wait_bar<NS, CG == 2>(&sc->p_full, p_phase, sc, p, 12)) return false;
     p_phase ^= 1u;
     tc_fence_after();
@@ -943,12 +960,34 @@ __device__ bool mma_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
     tc_commit<CG>(&sc->empty[rp.slot]);
     rp.next<NS>();
     tc_commit<CG>(&sc->o_full);
-  }
-  if constexpr (CG == 2) {
-    // hand the accumulator buffer back through the GEMM protocol
-    tc_commit<CG>(&sc->tfull[acc]);
-    acc ^= 1u;
-    if (acc == 0u) acc_phase ^= 1u;
+    return true;
+  };
+  if constexpr (CG == 1) {
+    const uint32_t s_tm = sc->tmem_base + ATT_S_COL, o_tm = sc->tmem_base + ATT_O_COL;
+    for (int j = 0; j < nkb; ++j)
+      if (!mma_s(s_tm, &sc->s_full) || !mma_pv(o_tm)) return false;
+  } else {
+    uint32_t buf[2];
+    for (int b = 0; b < 2; ++b) {
+      if (!wait_bar(&sc->tempty[acc], acc_phase ^ 1u, sc, p, 2)) return false;
+      buf[b] = acc;
+      acc ^= 1u;
+      if (acc == 0u) acc_phase ^= 1u;
+    }
+    tc_fence_after();
+    const uint32_t stride = static_cast<uint32_t>(p.acc_stride);
+    const uint32_t s_base = sc->tmem_base + buf[0] * stride, o_tm = sc->tmem_base + buf[1] * stride;
+    if (!mma_s(s_base, &sc->s_full)) return false;
+    if (nkb > 1 && !mma_s(s_base + 128, &sc->s_full_b)) return false;
+    for (int j = 0; j < nkb; ++j) {
+      if (!mma_pv(o_tm)) return false;
+      // S_j's half is free once P_j is published
+      if (j + 2 < nkb && !mma_s(s_base + static_cast<uint32_t>(j & 1) * 128, (j & 1) ? &sc->s_full_b : &sc->s_full))
+        return false;
+    }
+    // hand both buffers back through the GEMM protocol
+    tc_commit<CG>(&sc->tfull[buf[0]]);
+    tc_commit<CG>(&sc->tfull[buf[1]]);
   }
   return true;
 }
@@ -968,9 +1007,11 @@ __device__ bool epi_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
   const int q = warp & 3;
   const int r = q * 32 + lane;  // query row within the block
   const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-  const uint32_t tcols = CG == 1 ? ATT_S_COL : tacc * static_cast<uint32_t>(p.acc_stride);
-  const uint32_t s_tm = sc->tmem_base + lane_base + tcols;
-  const uint32_t o_tm = s_tm + (ATT_O_COL - ATT_S_COL);
+  // CG = 1: S and O at fixed columns.  CG = 2: S_j in half (j & 1) of the
+  // unit's first accumulator buffer, O in its second (the MMA's layout)
+  const uint32_t stride = static_cast<uint32_t>(p.acc_stride);
+  const uint32_t s_base = sc->tmem_base + lane_base + (CG == 1 ? ATT_S_COL : tacc * stride);
+  const uint32_t o_tm = CG == 1 ? sc->tmem_base + lane_base + ATT_O_COL : sc->tmem_base + lane_base + (tacc ^ 1u) * stride;
   const float sl2 = S.softmax_scale_log2;
   float acc[128];
 #pragma unroll
@@ -981,10 +1022,13 @@ __device__ bool epi_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
   __syncwarp();
   last_buf = -1;
   for (int j = 0; j < nkb; ++j) {
-    if (!wait_bar(&sc->s_full, s_phase, sc, p, 13)) return false;
-    s_phase ^= 1u;
+    // s_phase: bit 0 tracks s_full, bit 1 s_full_b (odd key blocks of pair units)
+    const uint32_t sb = CG == 2 ? static_cast<uint32_t>(j & 1) : 0u;
+    if (!wait_bar(sb ? &sc->s_full_b : &sc->s_full, (s_phase >> sb) & 1u, sc, p, 13)) return false;
+    s_phase ^= 1u << sb;
     tc_fence_after();
     if (j == 0 && threadIdx.x == EPI_WARP0 * 32) trace_put(p, tidx, rank, CG, 6, globaltimer());
+    const uint32_t s_tm = CG == 1 ? s_base : s_base + static_cast<uint32_t>(j & 1) * 128;
     // key column c of block j is visible to row r iff j*128 + c <= qb*128 + r
     const bool diag = j >= qb;
     const int lim = (qb - j) * 128 + r;
@@ -1088,14 +1132,16 @@ __device__ bool epi_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
     }
   }
   if constexpr (CG == 2) {
-    // the unit's accumulator buffer goes back to the MMA (both CTAs' warps)
-    if (!wait_bar(&sc->tfull[tacc], tacc_phase, sc, p, 4)) return false;
-    tc_fence_after();
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive_cluster(mapa_shared(&sc->tempty[tacc], 0));
-    tacc ^= 1u;
-    if (tacc == 0u) tacc_phase ^= 1u;
+    // both accumulator buffers go back to the MMA (both CTAs' warps), in order
+    for (int b = 0; b < 2; ++b) {
+      if (!wait_bar(&sc->tfull[tacc], tacc_phase, sc, p, 4)) return false;
+      tc_fence_after();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(&sc->tempty[tacc], 0));
+      tacc ^= 1u;
+      if (tacc == 0u) tacc_phase ^= 1u;
+    }
   }
   if (S.rel_tile != nullptr) {
     release_tile(p, S, qb, h, lane);
@@ -1289,6 +1335,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
     mbar_init(&sc->mb_full, 1);
     mbar_init(&sc->mb_empty, CL - 1 > 0 ? CL - 1 : 1);  // every peer CTA takes the index
     mbar_init(&sc->s_full, 1);
+    mbar_init(&sc->s_full_b, 1);
     mbar_init(&sc->s_empty, 4);
     mbar_init(&sc->p_full, 4 * CG);  // every epilogue warp of the unit's CTAs
     mbar_init(&sc->o_full, 1);
