@@ -194,7 +194,7 @@ def time_loop(fn, steps, warmup, stream):
     return total, per
 
 
-def simple_time(fn, iters=50, warmup=5):
+def simple_time(fn, iters=100, warmup=20):
     import torch
     s = torch.cuda.current_stream()
     for _ in range(warmup):
@@ -464,16 +464,16 @@ def extras(cs, torch, inp, dev, Y, make_plan, plan, M, kind, peaks, stream):
     import torch.nn.functional as Fn
     out = {}
     fwd = lambda p: cs.cs_mlp_forward(p, Y=Y, **dev)  # noqa: E731
-    chain_ms = simple_time(lambda: fwd(plan), 50)
+    chain_ms = simple_time(lambda: fwd(plan))
     out["chain_ms"] = chain_ms
     for pol in ("row", "strided", "stream"):
         with make_plan(pol) as p:
-            out[f"{pol}_ms"] = simple_time(lambda: fwd(p), 50)
+            out[f"{pol}_ms"] = simple_time(lambda: fwd(p))
     # without programmatic dependent launch: each launch waits for the previous
     # grid to finish before its CTAs start (the plain two-stream-kernel control)
     for pol in ("tile", "stream"):
         with make_plan(pol, pdl=-1) as p:
-            out[f"{'chain' if pol == 'tile' else pol}_nopdl_ms"] = simple_time(lambda: fwd(p), 50)
+            out[f"{'chain' if pol == 'tile' else pol}_nopdl_ms"] = simple_time(lambda: fwd(p))
     # control captured in a CUDA graph (launch cost amortised)
     with make_plan("stream") as pc:
         fwd(pc)
@@ -481,27 +481,27 @@ def extras(cs, torch, inp, dev, Y, make_plan, plan, M, kind, peaks, stream):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             fwd(pc)
-        out["stream_graph_ms"] = simple_time(g.replay, 50)
+        out["stream_graph_ms"] = simple_time(g.replay)
         ok = cs.cs_chain_status(pc)
         out["stream_graph_status"] = cs.STATUS_NAMES.get(ok)
         del g
     # best standalone GEMMs: this library's stage kernels and cuBLAS via torch
-    solo = [simple_time(lambda s=s: cs.cs_chain_forward_stage(plan, s, Y=Y, **dev), 50) for s in (0, 1)]
+    solo = [simple_time(lambda s=s: cs.cs_chain_forward_stage(plan, s, Y=Y, **dev)) for s in (0, 1)]
     out["solo_stage_ms"] = solo
     X = dev["X"]
     if kind == "gelu":
         W1 = dev["W1"] if plan.desc.weight_layout == 0 else dev["W1"].t()
         W2 = dev["W2"] if plan.desc.weight_layout == 0 else dev["W2"].t()
         Hbuf = torch.empty(M, inp.F, dtype=inp.dtype, device=X.device)
-        c1 = simple_time(lambda: Fn.gelu(torch.addmm(dev["b1"], X, W1), approximate="tanh"), 50)
-        c2 = simple_time(lambda: torch.mm(Hbuf, W2, out=Y), 50)
+        c1 = simple_time(lambda: Fn.gelu(torch.addmm(dev["b1"], X, W1), approximate="tanh"))
+        c2 = simple_time(lambda: torch.mm(Hbuf, W2, out=Y))
     else:
         Wg = dev["Wg"] if plan.desc.weight_layout == 0 else dev["Wg"].t()
         Wu = dev["Wu"] if plan.desc.weight_layout == 0 else dev["Wu"].t()
         W2 = dev["W2"] if plan.desc.weight_layout == 0 else dev["W2"].t()
         Hbuf = torch.empty(M, inp.F, dtype=inp.dtype, device=X.device)
-        c1 = simple_time(lambda: Fn.silu(X @ Wg) * (X @ Wu), 50)
-        c2 = simple_time(lambda: torch.mm(Hbuf, W2, out=Y), 50)
+        c1 = simple_time(lambda: Fn.silu(X @ Wg) * (X @ Wu))
+        c2 = simple_time(lambda: torch.mm(Hbuf, W2, out=Y))
     out["cublas_ms"] = [c1, c2]
     best = [min(solo[0], c1), min(solo[1], c2)]
     out["best_solo_ms"] = best
@@ -520,7 +520,7 @@ def extras(cs, torch, inp, dev, Y, make_plan, plan, M, kind, peaks, stream):
         rec = {"M": m}
         for pol, pdl, key in (("tile", None, "tile"), ("stream", None, "stream"), ("stream", -1, "stream_nopdl")):
             with make_plan(pol, m, pdl) as p:
-                ms = simple_time(lambda: cs.cs_mlp_forward(p, Y=Ym, **sub), 30)
+                ms = simple_time(lambda: cs.cs_mlp_forward(p, Y=Ym, **sub))
             rec[f"{key}_us"] = ms * 1e3
         fl = chain_flops(kind, m, inp.H, inp.F)
         by = chain_bytes(kind, m, inp.H, inp.F)
@@ -559,7 +559,7 @@ def other_configs(cs, torch, peaks, lay):
             desc = cs.cs_chain_desc_init(kind="swiglu", M=m, H=inp.H, F=inp.F, dtype=inp.dtype, policy=pol,
                                          weight_layout=lay)
             with cs.cs_chain_plan(desc) as p:
-                rec[f"{pol}_us"] = simple_time(lambda: cs.cs_mlp_forward(p, Y=Ym, **sub), 30) * 1e3
+                rec[f"{pol}_us"] = simple_time(lambda: cs.cs_mlp_forward(p, Y=Ym, **sub)) * 1e3
         fl = chain_flops("swiglu", m, inp.H, inp.F)
         rec["tflops"] = fl / (rec["tile_us"] * 1e-6) / 1e12
         rec["roofline_frac"], rec["bound"] = _roof_frac(fl, chain_bytes("swiglu", m, inp.H, inp.F), rec["tile_us"], peaks)
@@ -579,7 +579,7 @@ def other_configs(cs, torch, peaks, lay):
             desc = cs.cs_chain_desc_init(kind="attn", M=m, H=inp.H, F=inp.F, heads=inp.F // 128, head_dim=128,
                                          dtype=inp.dtype, policy=pol, weight_layout=lay)
             with cs.cs_chain_plan(desc) as p:
-                rec[f"{pol}_us"] = simple_time(lambda: cs.cs_attn_chain_forward(p, Xm, d["Wqkv"], d["Wo"], Ym), 30) * 1e3
+                rec[f"{pol}_us"] = simple_time(lambda: cs.cs_attn_chain_forward(p, Xm, d["Wqkv"], d["Wo"], Ym)) * 1e3
         F3 = 3 * inp.F
         fl = 2.0 * m * inp.H * F3 + 2.0 * m * inp.F * inp.H + 2.0 * m * (m + 1) * inp.F
         by = 2 * (inp.H * F3 + inp.F * inp.H + 2 * m * inp.H + 2 * m * F3 + 2 * m * inp.F)
@@ -602,7 +602,7 @@ def other_configs(cs, torch, peaks, lay):
                                          weight_layout=lay)
             with cs.cs_chain_plan(desc) as p:
                 q = cs.cs_chain_query(p)
-                rec[f"{pol}_us"] = simple_time(lambda: cs.cs_mlp_forward(p, Y=Ym, **sub), 20) * 1e3
+                rec[f"{pol}_us"] = simple_time(lambda: cs.cs_mlp_forward(p, Y=Ym, **sub)) * 1e3
         workers = q["num_sms"] * 128 // q["tile_m"]
         tiles0 = q["sched_units"][0]
         rec["stage0_units"], rec["workers"] = tiles0, workers

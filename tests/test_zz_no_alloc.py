@@ -34,6 +34,8 @@ def _desc(inp, layout, policy):
     ("gelu", 129, 256, 392, "kn", "row"),
     ("swiglu", 200, 512, 688, "nk", "tile"),
     ("gelu", 64, 256, 1024, "nk", "stream"),
+    ("gelu", 1024, 512, 1024, "nk", "tile"),      # 512-row tiles: 4-CTA clusters, multicast weights
+    ("swiglu", 640, 512, 688, "kn", "tile"),      # gate|up pairs in 4-CTA clusters, padded rows
 ])
 def test_noalloc_matches_planned_forward_twice(kind, M, H, F, layout, policy):
     inp = cs_inputs.make_custom(kind, M, H, F, dtype=torch.float16, seed=41)
