@@ -508,6 +508,11 @@ void fill_mlp_stages(const cs_chain_s* p, const cs_mlp_args* a, cs::KParams& kp)
   if (a) {
     fill_prefetch(p, s0, swiglu ? a->Wg : a->W1, swiglu ? a->Wu : nullptr, p->d.H, p->d.F, a->X, p->d.M, p->d.H);
     fill_prefetch(p, s1, a->W2, nullptr, p->d.F, p->d.H, nullptr, 0, 0);
+    // raw outputs for the plain-store epilogue of small split tiles
+    s0.out_ptr = p->inter[0];
+    s0.out_ld = p->d.F;
+    s1.out_ptr = a->Y;
+    s1.out_ld = p->d.H;
   }
   kp.acc_stride = (s0.mma_n > 128 || s1.mma_n > 128) ? 256 : 128;
 }
@@ -662,6 +667,11 @@ void fill_attn_stages(const cs_chain_s* p, cs::KParams& kp) {
 void fill_attn_prefetch(const cs_chain_s* p, const cs_attn_args* a, cs::KParams& kp) {
   fill_prefetch(p, kp.st[0], a->Wqkv, nullptr, p->d.H, 3 * p->d.F, a->X, p->d.M, p->d.H);
   fill_prefetch(p, kp.st[2], a->Wo, nullptr, p->d.F, p->d.H, nullptr, 0, 0);
+  // raw outputs for the plain-store epilogue of small split tiles
+  kp.st[0].out_ptr = p->inter[0];
+  kp.st[0].out_ld = 3 * p->d.F;
+  kp.st[2].out_ptr = a->Y;
+  kp.st[2].out_ld = p->d.H;
 }
 
 cs_status bind_attn(cs_chain_s* p, const cs_attn_args* a) {

@@ -79,6 +79,8 @@ struct StageP {
   int b_major;     // 0: weights K-major ([N,K]); 1: MN-major ([K,N])
   int map_a, map_b, map_b2, map_out;
   int map_k;  // attention on a CTA pair: QKV loads of 64-row boxes (half a key block)
+  void* out_ptr;   // the output (row-major, out_ld elements per row) for plain stores, or null
+  long long out_ld;
   int b_bytes;     // bytes of the B operand per pipeline stage and CTA
   const __nv_bfloat16* bias_bf16;  // exactly one of these two is used (per dtype)
   const __half* bias_f16;
@@ -170,6 +172,7 @@ struct SmemCtl {
   volatile int tma_seq;     // TMA warp: units started so far
   volatile int tma_kb;      // TMA warp: K-slice of its latest load
   int issued_parity[NS];  // TMA thread: parity of the last load issued into each slot (-1: none)
+  uint4 bias_s[32];       // epilogue: the bias of one tile (up to 256 values)
 };
 
 __device__ __forceinline__ void record_error(const KParams& p, uint32_t code, uint32_t unit, uint32_t where) {
@@ -579,17 +582,17 @@ __device__ void release_tile(const KParams& p, const StageP& S, int mb, int n, i
 
 // K-split reduction for a row block with few valid rows (R <= 32; from 64 rows
 // on, the row-per-thread path measured faster): the 128 epilogue threads share
-// the (row, 4-column group) elements of `np` 64-column parts and fetch every
-// split of an element at once; each element is summed in
-// split order (the same order as the row-per-thread path, so the same bits) and
-// written to the staging buffer as fp32 [part][row][16 float4], the float4 of
-// column group g of row r at slot g ^ (r & 15).  `col4[pp]` is the partial
-// tile's first 4-column group of part pp.  EB elements x KSB splits = 16 loads
-// in flight per thread.  Split ks's tile starts at tile0 + ks * kstride.
+// the (row, 4-column group) elements of the tile's `npc` 64-column parts (the
+// value chunks, then for SwiGLU the up chunks) and fetch every split of an
+// element at once; each element is summed in split order (the same order as
+// the row-per-thread path, so the same bits) and written to the staging buffer
+// as fp32 [part][row][16 float4], the float4 of column group g of row r at
+// slot g ^ (r & 15).  EB elements x KSB splits = 16 loads in flight per
+// thread.  Split ks's tile starts at tile0 + ks * kstride.
 template <int EB, int KSB>
 __device__ __forceinline__ void split_reduce_small(const StageP& S, const float4* tile0, size_t kstride, int R,
-                                                   int np, const int (&col4)[2], float4* sm) {
-  const int E = np * R * 16;
+                                                   int npc, int nchunks, float4* sm) {
+  const int E = npc * R * 16;
   const int tid = threadIdx.x - EPI_WARP0 * 32;
 #pragma unroll 1
   for (int base = tid; base < E; base += EPI_THREADS * EB) {
@@ -597,12 +600,13 @@ __device__ __forceinline__ void split_reduce_small(const StageP& S, const float4
 #pragma unroll
     for (int u = 0; u < EB; ++u) {
       const int e = base + u * EPI_THREADS;
-      // element e -> part pp, column group g, row r (rows fastest: coalesced)
-      const int pp = e / (R * 16), rem = e - pp * R * 16;
+      // element e -> part pc, column group g, row r (rows fastest: coalesced)
+      const int pc = e / (R * 16), rem = e - pc * R * 16;
       const int g = rem / R, r = rem - g * R;
+      const int col4 = ((pc / nchunks) * S.bn + (pc % nchunks) * 64) / 4 + g;
 #pragma unroll
       for (int ks = 0; ks < KSB; ++ks)
-        x[u][ks] = (e < E && ks < S.splits) ? __ldcg(tile0 + ks * kstride + (col4[pp & 1] + g) * BM + r)
+        x[u][ks] = (e < E && ks < S.splits) ? __ldcg(tile0 + ks * kstride + col4 * BM + r)
                                             : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
@@ -613,12 +617,96 @@ __device__ __forceinline__ void split_reduce_small(const StageP& S, const float4
 #pragma unroll
         for (int ks = 0; ks < KSB; ++ks)
           if (ks < S.splits) s.x += x[u][ks].x, s.y += x[u][ks].y, s.z += x[u][ks].z, s.w += x[u][ks].w;
-        const int pp = e / (R * 16), rem = e - pp * R * 16;
+        const int pc = e / (R * 16), rem = e - pc * R * 16;
         const int g = rem / R, r = rem - g * R;
-        sm[(pp * R + r) * 16 + (g ^ (r & 15))] = s;
+        sm[(pc * R + r) * 16 + (g ^ (r & 15))] = s;
       }
     }
   }
+}
+
+// The last K-split of a tile with at most 32 valid rows: one cooperative pass
+// brings every split of every 64-column part (and the bias) on chip, then each
+// row thread finishes its row and writes it with plain 16-byte stores, so no
+// staging, TMA store or per-chunk round trip stays on the hand-off to the
+// consumers (measured at GPT-3 M=1: 13 us from accumulator to release with the
+// per-chunk path).  The caller fences and releases.
+template <int NS>
+__device__ void epi_split_rows32(const KParams& p, const StageP& S, SmemCtl<NS>* sc, uint8_t* staging,
+                                 const float4* tile0, size_t kstride, int R, int mb, int n, int row, int lane) {
+  const int nchunks = S.bn / 64;
+  const int npc = (S.epi == EPI_SWIGLU ? 2 : 1) * nchunks;
+  // every store still reading the staging buffer is done before it is reused
+  if (lane == 0) tma_store_wait_read<0>();
+  named_bar_sync(1, EPI_THREADS);
+  const int tid = threadIdx.x - EPI_WARP0 * 32;
+  if (S.epi == EPI_BIAS_GELU && tid < S.bn / 8) {
+    const int col = n * S.bn + tid * 8;  // 16-byte groups, zero past the extent (a multiple of 8)
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (col < S.n_extent)
+      v = ldg_nc_v4(p.bf16 ? static_cast<const void*>(S.bias_bf16 + col) : static_cast<const void*>(S.bias_f16 + col));
+    sc->bias_s[tid] = v;
+  }
+  float4* sm = reinterpret_cast<float4*>(staging);
+  if (S.splits <= 2)
+    split_reduce_small<8, 2>(S, tile0, kstride, R, npc, nchunks, sm);
+  else if (S.splits <= 4)
+    split_reduce_small<4, 4>(S, tile0, kstride, R, npc, nchunks, sm);
+  else if (S.splits <= 8)
+    split_reduce_small<2, 8>(S, tile0, kstride, R, npc, nchunks, sm);
+  else
+    split_reduce_small<1, 16>(S, tile0, kstride, R, npc, nchunks, sm);
+  named_bar_sync(1, EPI_THREADS);
+  if (row < R) {
+    char* out_row = static_cast<char*>(S.out_ptr) + (static_cast<long long>(mb) * BM + row) * S.out_ld * 2;
+#pragma unroll 1
+    for (int c = 0; c < nchunks; ++c) {
+      float va[64], vu[64];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float4 a = sm[(c * R + row) * 16 + (j ^ (row & 15))];
+        va[4 * j] = a.x, va[4 * j + 1] = a.y, va[4 * j + 2] = a.z, va[4 * j + 3] = a.w;
+        if (S.epi == EPI_SWIGLU) {
+          const float4 b = sm[((nchunks + c) * R + row) * 16 + (j ^ (row & 15))];
+          vu[4 * j] = b.x, vu[4 * j + 1] = b.y, vu[4 * j + 2] = b.z, vu[4 * j + 3] = b.w;
+        } else {
+          vu[4 * j] = vu[4 * j + 1] = vu[4 * j + 2] = vu[4 * j + 3] = 0.0f;
+        }
+      }
+      uint32_t w[32];
+      if (S.epi == EPI_BIAS_GELU) {
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          const uint4 bv = sc->bias_s[c * 8 + g];
+          const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+          for (int i2 = 0; i2 < 4; ++i2) {
+            float2 f;
+            if (p.bf16)
+              f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bw[i2]));
+            else
+              f = __half22float2(*reinterpret_cast<const __half2*>(&bw[i2]));
+            const int j = g * 8 + 2 * i2;
+            w[j >> 1] = pack2(gelu_tanh_f(va[j] + f.x), gelu_tanh_f(va[j + 1] + f.y), p.bf16);
+          }
+        }
+      } else if (S.epi == EPI_SWIGLU) {
+#pragma unroll
+        for (int j = 0; j < 64; j += 2)
+          w[j >> 1] = pack2(silu_f(va[j]) * vu[j], silu_f(va[j + 1]) * vu[j + 1], p.bf16);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 64; j += 2) w[j >> 1] = pack2(va[j], va[j + 1], p.bf16);
+      }
+      const int col0 = n * S.bn + c * 64;
+#pragma unroll
+      for (int g = 0; g < 8; ++g)
+        if (col0 + g * 8 < S.n_extent)
+          *reinterpret_cast<uint4*>(out_row + static_cast<long long>(col0 + g * 8) * 2) =
+              make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
+    }
+  }
+  __threadfence();
 }
 
 template <int NS, int CG, int CL>
@@ -690,44 +778,18 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
     }
     __threadfence();
   }
+  // at most 32 valid rows (the last split of the tile): one cooperative pass
+  // and plain row stores; the loop below is skipped
+  const bool rows32 = split && rows_valid <= 32 && S.out_ptr != nullptr;
+  if (rows32) {
+    const size_t kstride = static_cast<size_t>(S.m_blocks) * S.n_tiles * (tile_floats / 4);
+    epi_split_rows32<NS>(p, S, sc, staging, tile_partial(0) - row, kstride, rows_valid, mb, n, row, lane);
+    last_buf = -1;
+  }
 #pragma unroll 1
-  for (int c = 0; c < nchunks; ++c) {
+  for (int c = 0; c < (rows32 ? 0 : nchunks); ++c) {
     float va[64], vu[64];
-    if (split && rows_valid <= 32) {
-      // every store still reading the staging buffer is done before it is reused
-      if (lane == 0) tma_store_wait_read<0>();
-      last_buf = -1;
-      named_bar_sync(1, EPI_THREADS);
-      const float4* tile0 = tile_partial(0) - row;
-      const size_t kstride = static_cast<size_t>(S.m_blocks) * S.n_tiles * (tile_floats / 4);
-      const int np = S.epi == EPI_SWIGLU ? 2 : 1;
-      const int col4[2] = {(c * 64) / 4, (S.bn + c * 64) / 4};
-      float4* sm = reinterpret_cast<float4*>(staging);
-      if (S.splits <= 2)
-        split_reduce_small<8, 2>(S, tile0, kstride, rows_valid, np, col4, sm);
-      else if (S.splits <= 4)
-        split_reduce_small<4, 4>(S, tile0, kstride, rows_valid, np, col4, sm);
-      else if (S.splits <= 8)
-        split_reduce_small<2, 8>(S, tile0, kstride, rows_valid, np, col4, sm);
-      else
-        split_reduce_small<1, 16>(S, tile0, kstride, rows_valid, np, col4, sm);
-      named_bar_sync(1, EPI_THREADS);
-#pragma unroll
-      for (int j = 0; j < 64; ++j) va[j] = vu[j] = 0.0f;
-      if (row < rows_valid) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float4 a = sm[row * 16 + (j ^ (row & 15))];
-          va[4 * j] = a.x, va[4 * j + 1] = a.y, va[4 * j + 2] = a.z, va[4 * j + 3] = a.w;
-          if (S.epi == EPI_SWIGLU) {
-            const float4 b = sm[(rows_valid + row) * 16 + (j ^ (row & 15))];
-            vu[4 * j] = b.x, vu[4 * j + 1] = b.y, vu[4 * j + 2] = b.z, vu[4 * j + 3] = b.w;
-          }
-        }
-      }
-      // the sums are in registers; the staging buffer is free for the output rows
-      named_bar_sync(1, EPI_THREADS);
-    } else if (split) {
+    if (split) {
 #pragma unroll
       for (int j = 0; j < 64; ++j) va[j] = vu[j] = 0.0f;
       // sum the splits in split order (the same bits whichever split arrived last);
