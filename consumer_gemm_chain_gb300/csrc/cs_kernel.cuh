@@ -580,18 +580,17 @@ __device__ void release_tile(const KParams& p, const StageP& S, int mb, int n, i
   }
 }
 
-// K-split reduction for a row block with few valid rows (R <= 32; from 64 rows
-// on, the row-per-thread path measured faster): the 128 epilogue threads share
-// the (row, 4-column group) elements of the tile's `npc` 64-column parts (the
-// value chunks, then for SwiGLU the up chunks) and fetch every split of an
-// element at once; each element is summed in split order (the same order as
-// the row-per-thread path, so the same bits) and written to the staging buffer
-// as fp32 [part][row][16 float4], the float4 of column group g of row r at
-// slot g ^ (r & 15).  EB elements x KSB splits = 16 loads in flight per
-// thread.  Split ks's tile starts at tile0 + ks * kstride.
+// K-split reduction for a row block with few valid rows (R <= 48): the 128
+// epilogue threads share the (row, 4-column group) elements of `npc` 64-column
+// parts (the value chunks c0 .. c0+nc-1, then for SwiGLU the same up chunks)
+// and fetch every split of an element at once; each element is summed in split
+// order (the same order as the row-per-thread path, so the same bits) and
+// written to the staging buffer as fp32 [part][row][16 float4], the float4 of
+// column group g of row r at slot g ^ (r & 15).  EB elements x KSB splits = 16
+// loads in flight per thread.  Split ks's tile starts at tile0 + ks * kstride.
 template <int EB, int KSB>
 __device__ __forceinline__ void split_reduce_small(const StageP& S, const float4* tile0, size_t kstride, int R,
-                                                   int npc, int nchunks, float4* sm) {
+                                                   int npc, int nc, int c0, float4* sm) {
   const int E = npc * R * 16;
   const int tid = threadIdx.x - EPI_WARP0 * 32;
 #pragma unroll 1
@@ -603,7 +602,7 @@ __device__ __forceinline__ void split_reduce_small(const StageP& S, const float4
       // element e -> part pc, column group g, row r (rows fastest: coalesced)
       const int pc = e / (R * 16), rem = e - pc * R * 16;
       const int g = rem / R, r = rem - g * R;
-      const int col4 = ((pc / nchunks) * S.bn + (pc % nchunks) * 64) / 4 + g;
+      const int col4 = ((pc / nc) * S.bn + (c0 + pc % nc) * 64) / 4 + g;
 #pragma unroll
       for (int ks = 0; ks < KSB; ++ks)
         x[u][ks] = (e < E && ks < S.splits) ? __ldcg(tile0 + ks * kstride + col4 * BM + r)
@@ -625,17 +624,21 @@ __device__ __forceinline__ void split_reduce_small(const StageP& S, const float4
   }
 }
 
-// The last K-split of a tile with at most 32 valid rows: one cooperative pass
-// brings every split of every 64-column part (and the bias) on chip, then each
-// row thread finishes its row and writes it with plain 16-byte stores, so no
-// staging, TMA store or per-chunk round trip stays on the hand-off to the
-// consumers (measured at GPT-3 M=1: 13 us from accumulator to release with the
-// per-chunk path).  The caller fences and releases.
+// The last K-split of a tile with at most 48 valid rows: cooperative passes
+// bring every split of the tile's 64-column parts (as many per pass as the
+// staging buffer holds: all of them up to 32 rows) and, once, the bias on chip;
+// each row thread finishes its rows' chunks and writes them with plain 16-byte
+// stores, so no staging output, TMA store or per-chunk round trip stays on the
+// hand-off to the consumers (measured at GPT-3 M=1: 13 us from accumulator to
+// release with the per-chunk path).  The caller fences and releases.
 template <int NS>
-__device__ void epi_split_rows32(const KParams& p, const StageP& S, SmemCtl<NS>* sc, uint8_t* staging,
-                                 const float4* tile0, size_t kstride, int R, int mb, int n, int row, int lane) {
+__device__ void epi_split_rows_small(const KParams& p, const StageP& S, SmemCtl<NS>* sc, uint8_t* staging,
+                                     const float4* tile0, size_t kstride, int R, int mb, int n, int row, int lane) {
   const int nchunks = S.bn / 64;
-  const int npc = (S.epi == EPI_SWIGLU ? 2 : 1) * nchunks;
+  const int np = S.epi == EPI_SWIGLU ? 2 : 1;
+  // chunks per pass: np parts each, R rows of 256 bytes per part
+  const int cap = (STAGING_BYTES / 256) / R / np;
+  const int cpp = cap < nchunks ? cap : nchunks;
   // every store still reading the staging buffer is done before it is reused
   if (lane == 0) tma_store_wait_read<0>();
   named_bar_sync(1, EPI_THREADS);
@@ -648,31 +651,37 @@ __device__ void epi_split_rows32(const KParams& p, const StageP& S, SmemCtl<NS>*
     sc->bias_s[tid] = v;
   }
   float4* sm = reinterpret_cast<float4*>(staging);
-  if (S.splits <= 2)
-    split_reduce_small<8, 2>(S, tile0, kstride, R, npc, nchunks, sm);
-  else if (S.splits <= 4)
-    split_reduce_small<4, 4>(S, tile0, kstride, R, npc, nchunks, sm);
-  else if (S.splits <= 8)
-    split_reduce_small<2, 8>(S, tile0, kstride, R, npc, nchunks, sm);
-  else
-    split_reduce_small<1, 16>(S, tile0, kstride, R, npc, nchunks, sm);
-  named_bar_sync(1, EPI_THREADS);
-  if (row < R) {
-    char* out_row = static_cast<char*>(S.out_ptr) + (static_cast<long long>(mb) * BM + row) * S.out_ld * 2;
+  char* out_row = static_cast<char*>(S.out_ptr) + (static_cast<long long>(mb) * BM + row) * S.out_ld * 2;
 #pragma unroll 1
-    for (int c = 0; c < nchunks; ++c) {
+  for (int c0 = 0; c0 < nchunks; c0 += cpp) {
+    const int nc = nchunks - c0 < cpp ? nchunks - c0 : cpp;
+    // the row threads are done with the previous pass's sums
+    if (c0 > 0) named_bar_sync(1, EPI_THREADS);
+    if (S.splits <= 2)
+      split_reduce_small<8, 2>(S, tile0, kstride, R, np * nc, nc, c0, sm);
+    else if (S.splits <= 4)
+      split_reduce_small<4, 4>(S, tile0, kstride, R, np * nc, nc, c0, sm);
+    else if (S.splits <= 8)
+      split_reduce_small<2, 8>(S, tile0, kstride, R, np * nc, nc, c0, sm);
+    else
+      split_reduce_small<1, 16>(S, tile0, kstride, R, np * nc, nc, c0, sm);
+    named_bar_sync(1, EPI_THREADS);
+    if (row >= R) continue;
+#pragma unroll 1
+    for (int cc = 0; cc < nc; ++cc) {
       float va[64], vu[64];
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        const float4 a = sm[(c * R + row) * 16 + (j ^ (row & 15))];
+        const float4 a = sm[(cc * R + row) * 16 + (j ^ (row & 15))];
         va[4 * j] = a.x, va[4 * j + 1] = a.y, va[4 * j + 2] = a.z, va[4 * j + 3] = a.w;
         if (S.epi == EPI_SWIGLU) {
-          const float4 b = sm[((nchunks + c) * R + row) * 16 + (j ^ (row & 15))];
+          const float4 b = sm[((nc + cc) * R + row) * 16 + (j ^ (row & 15))];
           vu[4 * j] = b.x, vu[4 * j + 1] = b.y, vu[4 * j + 2] = b.z, vu[4 * j + 3] = b.w;
         } else {
           vu[4 * j] = vu[4 * j + 1] = vu[4 * j + 2] = vu[4 * j + 3] = 0.0f;
         }
       }
+      const int c = c0 + cc;
       uint32_t w[32];
       if (S.epi == EPI_BIAS_GELU) {
 #pragma unroll
@@ -778,16 +787,18 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
     }
     __threadfence();
   }
-  // at most 32 valid rows (the last split of the tile): one cooperative pass
-  // and plain row stores; the loop below is skipped
-  const bool rows32 = split && rows_valid <= 32 && S.out_ptr != nullptr;
-  if (rows32) {
+  // at most 48 valid rows (the last split of the tile): cooperative passes
+  // and plain row stores; the loop below is skipped (measured against the
+  // row-per-thread path: LLaMA 33 rows 77 -> 58 us, 48 rows 60 -> 57 us, but
+  // 64 rows 59 -> 62 us)
+  const bool rows_small = split && rows_valid <= 48 && S.out_ptr != nullptr;
+  if (rows_small) {
     const size_t kstride = static_cast<size_t>(S.m_blocks) * S.n_tiles * (tile_floats / 4);
-    epi_split_rows32<NS>(p, S, sc, staging, tile_partial(0) - row, kstride, rows_valid, mb, n, row, lane);
+    epi_split_rows_small<NS>(p, S, sc, staging, tile_partial(0) - row, kstride, rows_valid, mb, n, row, lane);
     last_buf = -1;
   }
 #pragma unroll 1
-  for (int c = 0; c < (rows32 ? 0 : nchunks); ++c) {
+  for (int c = 0; c < (rows_small ? 0 : nchunks); ++c) {
     float va[64], vu[64];
     if (split) {
 #pragma unroll
