@@ -210,6 +210,11 @@ Geometry geometry(const cs_chain_desc* d, int num_sms) {
       (d->kind == CS_CHAIN_MLP_SWIGLU || 2 * cdiv(d->M, 512) == cdiv(d->M, 256)))
     tm = 512, tn = 256;
   if (tn == 0) tn = (2 * blocks * cdiv(d->F, 256) >= num_sms) ? 256 : 128;
+  // A few rows only stream weights: 256-wide single-SM tiles keep 128 KB of
+  // weights in flight per SM (96 KB with 128-wide ones); their doubled K-splits
+  // cost more in the reduction once rows add up (measured, GPT-3 / LLaMA:
+  // M=1 82 -> 71 / 55 -> 49 us, M=32 73 -> 80 / 51 -> 53 us)
+  if (d->tile_n == 0 && mlp && d->M <= 8) tn = 256;
   // A 2-SM pair per 256 x 256 tile halves them again (each SM loads half of B).
   if (tm == 0) tm = (tn == 256 && mlp && blocks >= 8) ? 256 : 128;
   if (!mlp) {
@@ -253,10 +258,12 @@ Geometry geometry(const cs_chain_desc* d, int num_sms) {
     g.splits[s] = 1;
     if (d->kind == CS_CHAIN_ATTN && s == 1) continue;  // attention units do not split
     const int tiles = g.m_tiles * g.n_tiles[s];
-    // auto, several row blocks: at most 4 splits of at least 32 K-slices
+    // auto, more than 32 rows: at most 4 splits of at least 32 K-slices
     // (measured: finer splits make the last split's reduction and the partial
-    // traffic dominate); one row block streams weights only and takes up to 15
-    const bool wide = d->split_k > 0 || g.m_blocks == 1;
+    // traffic dominate); up to 32 rows stream weights only and take up to 15
+    // (measured: seven splits of a full 128-row block, stress M=128, 141 us
+    // against 99 us with four)
+    const bool wide = d->split_k > 0 || d->M <= 32;
     const int max_sp = wide ? std::max(1, std::min(15, g.k_iters[s] / 8))
                             : std::max(1, std::min(4, g.k_iters[s] / 32));
     int sp = d->split_k;
