@@ -43,11 +43,18 @@ constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
 // gate|up).  Both rings keep 192 KB of operands in flight per SM.
 constexpr int NS_A = 6, SB_A = cs::TILE_A_BYTES + 128 * cs::BK * 2;      // 32 KB stages
 constexpr int NS_B = 4, SB_B = cs::TILE_A_BYTES + 2 * 128 * cs::BK * 2;  // 48 KB stages
+// up to 8 rows: 8-row A tiles (1 KB) leave room for deeper rings of weights
+constexpr int NS_S = 11, SB_S = 8 * cs::BK * 2 + 128 * cs::BK * 2;      // 17 KB stages
+constexpr int NS_T = 5, SB_T = 8 * cs::BK * 2 + 2 * 128 * cs::BK * 2;   // 33 KB stages
 
 template <int NS, int SB>
 constexpr int smem_bytes_for() {
   return NS * SB + cs::STAGING_BYTES + static_cast<int>(sizeof(cs::SmemCtl<NS>)) + 1024;
 }
+// every configuration fits the 227 KB a CTA may use
+static_assert(smem_bytes_for<NS_A, SB_A>() <= 232448 && smem_bytes_for<NS_B, SB_B>() <= 232448 &&
+                  smem_bytes_for<NS_S, SB_S>() <= 232448 && smem_bytes_for<NS_T, SB_T>() <= 232448,
+              "shared memory");
 
 struct MapSlot {
   const void* ptr = nullptr;  // caller pointer the map was encoded for (nullptr: plan-owned or unset)
@@ -70,6 +77,7 @@ struct cs_chain_s {
   int stride = 1;
   int bn[3] = {128, 128, 128};
   int cfg_b = 0;  // 1: 48 KB-stage kernel (256-wide one-SM tiles or gate|up)
+  int cfg_s = 0;  // up to 8 rows: 1 = 11 x 17 KB stages (128-wide B), 2 = 5 x 33 KB (256 rows of B)
   int cg = 1;     // CTAs per tcgen05 MMA (2: 256-row tiles on a 2-SM pair)
   int cl = 1;     // CTAs per unit and cluster (4: two pairs sharing weight boxes)
   int m_units = 0;   // tile rows of the schedule
@@ -210,11 +218,6 @@ Geometry geometry(const cs_chain_desc* d, int num_sms) {
       (d->kind == CS_CHAIN_MLP_SWIGLU || 2 * cdiv(d->M, 512) == cdiv(d->M, 256)))
     tm = 512, tn = 256;
   if (tn == 0) tn = (2 * blocks * cdiv(d->F, 256) >= num_sms) ? 256 : 128;
-  // A few rows only stream weights: 256-wide single-SM tiles keep 128 KB of
-  // weights in flight per SM (96 KB with 128-wide ones); their doubled K-splits
-  // cost more in the reduction once rows add up (measured, GPT-3 / LLaMA:
-  // M=1 82 -> 71 / 55 -> 49 us, M=32 73 -> 80 / 51 -> 53 us)
-  if (d->tile_n == 0 && mlp && d->M <= 8) tn = 256;
   // A 2-SM pair per 256 x 256 tile halves them again (each SM loads half of B).
   if (tm == 0) tm = (tn == 256 && mlp && blocks >= 8) ? 256 : 128;
   if (!mlp) {
@@ -353,9 +356,9 @@ int device_sms(int* out) {
   return dev;
 }
 
-template <int NS, int SB, int CG, bool ATTN, int CL = CG>
+template <int NS, int SB, int CG, bool ATTN, int CL = CG, int AR = cs::BM>
 cs_status set_smem_attr() {
-  static cudaError_t once = cudaFuncSetAttribute(cs::cs_chain_kernel<NS, SB, CG, ATTN, CL>,
+  static cudaError_t once = cudaFuncSetAttribute(cs::cs_chain_kernel<NS, SB, CG, ATTN, CL, AR>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes_for<NS, SB>());
   if (once != cudaSuccess) return fail(CS_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(once));
   return CS_OK;
@@ -405,9 +408,9 @@ cs_status encode_weight(cs_chain_s* p, int slot, const void* ptr, int K, int N, 
 }
 
 // Activation-side map: row-major [rows, cols]; box 64 cols x (128 rows for loads / 32 for stores).
-cs_status encode_act(cs_chain_s* p, int slot, const void* ptr, int rows, int cols, bool store) {
+cs_status encode_act(cs_chain_s* p, int slot, const void* ptr, int rows, int cols, bool store, int load_rows = 128) {
   if (p->slots[slot].valid && p->slots[slot].ptr == ptr) return CS_OK;
-  cs_status s = encode_2d(&p->maps[slot], ptr, p->d.dtype == CS_BF16, cols, rows, 64, store ? 32 : 128);
+  cs_status s = encode_2d(&p->maps[slot], ptr, p->d.dtype == CS_BF16, cols, rows, 64, store ? 32 : load_rows);
   if (s != CS_OK) return s;
   p->slots[slot].ptr = ptr;
   p->slots[slot].valid = true;
@@ -569,6 +572,12 @@ cs_status launch(cs_chain_s* p, cs::KParams& kp, const uint32_t* sched, int n_un
   } else if (p->cg == 2) {
     if ((s = set_smem_attr<NS_A, SB_A, 2, false>()) != CS_OK) return s;
     e = cudaLaunchKernelEx(&cfg, cs::cs_chain_kernel<NS_A, SB_A, 2, false>, kp);
+  } else if (p->cfg_s == 1) {
+    if ((s = set_smem_attr<NS_S, SB_S, 1, false, 1, 8>()) != CS_OK) return s;
+    e = cudaLaunchKernelEx(&cfg, cs::cs_chain_kernel<NS_S, SB_S, 1, false, 1, 8>, kp);
+  } else if (p->cfg_s == 2) {
+    if ((s = set_smem_attr<NS_T, SB_T, 1, false, 1, 8>()) != CS_OK) return s;
+    e = cudaLaunchKernelEx(&cfg, cs::cs_chain_kernel<NS_T, SB_T, 1, false, 1, 8>, kp);
   } else if (p->cfg_b) {
     if ((s = set_smem_attr<NS_B, SB_B, 1, false>()) != CS_OK) return s;
     e = cudaLaunchKernelEx(&cfg, cs::cs_chain_kernel<NS_B, SB_B, 1, false>, kp);
@@ -702,7 +711,7 @@ cs_status bind_mlp(cs_chain_s* p, const cs_mlp_args* a) {
   if (!swiglu && reinterpret_cast<uintptr_t>(a->b1) % 16 != 0) return fail(CS_ERR_INVALID_ARG, "b1 is not 16-byte aligned");
   const int M = p->d.M, H = p->d.H, F = p->d.F;
   cs_status s;
-  if ((s = encode_act(p, MAP_X, a->X, M, H, false)) != CS_OK) return s;
+  if ((s = encode_act(p, MAP_X, a->X, M, H, false, p->cfg_s ? 8 : 128)) != CS_OK) return s;
   // [N, K] weights: a box holds the B columns one CTA fetches (with 4-CTA
   // clusters, half of its pair share; the other half comes by multicast).  A
   // gate|up pair gives each CTA all bn rows of one of the two operands.
@@ -794,8 +803,13 @@ cs_status cs_chain_plan(const cs_chain_desc* desc, cs_chain_t* out) {
   p->group_m = g.group_m;
   p->stride = g.stride;
   for (int i = 0; i < 3; ++i) p->bn[i] = g.bn[i];
-  p->cfg_b = g.cg == 1 && (desc->kind == CS_CHAIN_MLP_SWIGLU || g.bn[0] == 256 || g.bn[1] == 256 || g.bn[2] == 256);
-  p->smem = p->cfg_b ? smem_bytes_for<NS_B, SB_B>() : smem_bytes_for<NS_A, SB_A>();
+  const bool wide_b = desc->kind == CS_CHAIN_MLP_SWIGLU || g.bn[0] == 256 || g.bn[1] == 256 || g.bn[2] == 256;
+  p->cfg_s = (g.cg == 1 && desc->kind != CS_CHAIN_ATTN && desc->M <= 8) ? (wide_b ? 2 : 1) : 0;
+  p->cfg_b = g.cg == 1 && !p->cfg_s && wide_b;
+  p->smem = p->cfg_s == 1 ? smem_bytes_for<NS_S, SB_S>()
+            : p->cfg_s == 2 ? smem_bytes_for<NS_T, SB_T>()
+            : p->cfg_b      ? smem_bytes_for<NS_B, SB_B>()
+                            : smem_bytes_for<NS_A, SB_A>();
 
   auto bail = [&](cs_status st) {
     free_plan(p);
@@ -851,7 +865,8 @@ cs_status cs_chain_plan(const cs_chain_desc* desc, cs_chain_t* out) {
     n_owned = 5;
   } else {
     if ((s = encode_act(p, MAP_HST, p->inter[0], desc->M, desc->F, true)) != CS_OK) return bail(s);
-    if ((s = encode_act(p, MAP_HLD, p->inter[0], desc->M, desc->F, false)) != CS_OK) return bail(s);
+    if ((s = encode_act(p, MAP_HLD, p->inter[0], desc->M, desc->F, false, p->cfg_s ? 8 : 128)) != CS_OK)
+      return bail(s);
     owned[0] = MAP_HST, owned[1] = MAP_HLD;
     n_owned = 2;
   }
@@ -1150,8 +1165,13 @@ cs_status cs_mlp_forward_noalloc(const cs_chain_desc* desc, const cs_mlp_args* a
   p.lag = g.lag;
   p.group_m = g.group_m;
   p.stride = g.stride;
-  p.cfg_b = g.cg == 1 && (desc->kind == CS_CHAIN_MLP_SWIGLU || g.bn[0] == 256 || g.bn[1] == 256);
-  p.smem = p.cfg_b ? smem_bytes_for<NS_B, SB_B>() : smem_bytes_for<NS_A, SB_A>();
+  const bool wide_b = desc->kind == CS_CHAIN_MLP_SWIGLU || g.bn[0] == 256 || g.bn[1] == 256;
+  p.cfg_s = (g.cg == 1 && desc->M <= 8) ? (wide_b ? 2 : 1) : 0;
+  p.cfg_b = g.cg == 1 && !p.cfg_s && wide_b;
+  p.smem = p.cfg_s == 1 ? smem_bytes_for<NS_S, SB_S>()
+           : p.cfg_s == 2 ? smem_bytes_for<NS_T, SB_T>()
+           : p.cfg_b      ? smem_bytes_for<NS_B, SB_B>()
+                          : smem_bytes_for<NS_A, SB_A>();
   p.num_sms = p.num_sms / g.cl * g.cl;
   const std::vector<uint32_t> fused = build_fused(g);
   const std::vector<uint32_t> st0 = build_stage(g, 0), st1 = build_stage(g, 1);
@@ -1187,7 +1207,7 @@ cs_status cs_mlp_forward_noalloc(const cs_chain_desc* desc, const cs_mlp_args* a
 
   // Tensor maps of the intermediate (in the array) and of the caller's tensors.
   if ((s = encode_act(&p, MAP_HST, p.inter[0], desc->M, desc->F, true)) != CS_OK) return s;
-  if ((s = encode_act(&p, MAP_HLD, p.inter[0], desc->M, desc->F, false)) != CS_OK) return s;
+  if ((s = encode_act(&p, MAP_HLD, p.inter[0], desc->M, desc->F, false, p.cfg_s ? 8 : 128)) != CS_OK) return s;
   for (int i = 0; i < kMaxMaps; ++i)
     if (i != MAP_HST && i != MAP_HLD) std::memcpy(&p.maps[i], &p.maps[MAP_HLD], sizeof(CUtensorMap));
   if ((s = bind_mlp(&p, args)) != CS_OK) return s;

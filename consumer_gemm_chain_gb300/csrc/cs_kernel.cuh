@@ -340,13 +340,17 @@ __device__ __noinline__ int tma_wait_slices(SmemCtl<NS>* sc, uint32_t q, int kb,
 // on consecutive 256-row blocks of the same column tile: each weight box is
 // fetched once and multicast to the CTA holding the same B columns in the
 // other pair).
-template <int NS, int STAGE_BYTES, int CG, int CL>
+// AR: A rows held in shared memory per stage: 128, or 8 for up to 8 valid rows
+// (the MMA then reads the one 8-row group for every 8-row group of its 128
+// rows, and the rows past the valid ones are never stored).
+template <int NS, int STAGE_BYTES, int CG, int CL, int AR>
 __device__ bool tma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, RingPos& rp, uint32_t unit,
                               uint32_t q, uint32_t rank) {
   const uint32_t tidx = sc->uq_idx[q];
   const StageP& S = p.st[unit_stage(unit)];
   const int m = unit_m(unit), n = unit_n(unit);
-  const uint32_t bytes = TILE_A_BYTES + S.b_bytes;
+  constexpr int A_BYTES = AR * BK * 2;
+  const uint32_t bytes = A_BYTES + S.b_bytes;
   const bool do_wait = p.waits && S.wait != WAIT_NONE;
   const int kb0 = unit_ks(unit) * S.kps;
   const int kb1 = min(S.k_iters, kb0 + S.kps);
@@ -368,7 +372,7 @@ __device__ bool tma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
     }
     if (!wait_bar(&sc->empty[rp.slot], rp.phase ^ 1u, sc, p, 1)) return false;
     uint8_t* sa = ring + rp.slot * STAGE_BYTES;
-    uint8_t* sb = sa + TILE_A_BYTES;
+    uint8_t* sb = sa + A_BYTES;
     // Completion goes to the leader's full barrier (each CTA of a pair adds its
     // bytes); with CL = 4 every CTA counts its own bytes (its A, and its B
     // columns: one half fetched here, one multicast by the other pair).
@@ -437,7 +441,7 @@ __device__ bool tma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
 }
 
 // ---------------------------------------------------------------- MMA role
-template <int NS, int STAGE_BYTES, int CG, int CL>
+template <int NS, int STAGE_BYTES, int CG, int CL, int AR>
 __device__ bool mma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, RingPos& rp, uint32_t unit,
                               uint32_t& acc, uint32_t& acc_phase, uint32_t rank) {
   // a freed stage is refilled by this pair and (CL = 4) by the other pair's
@@ -455,8 +459,9 @@ __device__ bool mma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
     if (!wait_bar(&sc->full[rp.slot], rp.phase, sc, p, 3)) return false;
     tc_fence_after();
     const uint32_t sa = smem_u32(ring + rp.slot * STAGE_BYTES);
-    const uint32_t sb = sa + TILE_A_BYTES;
-    const uint64_t adesc = smem_desc_sw128(sa, 16, 1024);
+    const uint32_t sb = sa + AR * BK * 2;
+    // AR = 8: stride 0 between 8-row groups, so every group reads the one loaded
+    const uint64_t adesc = smem_desc_sw128(sa, 16, AR >= 16 ? 1024 : 0);
     // K-major B: 8-row groups 1024 B apart.  MN-major B: 64-column atoms 8 KB
     // apart (LBO), 8-row K groups 1024 B apart (SBO).
     const uint64_t bdesc = S.b_major == 0 ? smem_desc_sw128(sb, 16, 1024) : smem_desc_sw128(sb, 8192, 1024);
@@ -1373,9 +1378,10 @@ __device__ __forceinline__ void push_unit(SmemCtl<NS>* sc, uint32_t q, uint32_t 
 // the MLP instantiations leave that code out and keep their registers.
 // CG: CTAs per tcgen05 MMA (1, or 2 for a 256-row pair); CL: CTAs per unit
 // and per cluster (CG, or 4: two pairs sharing the weight boxes by multicast).
-template <int NS, int STAGE_BYTES, int CG, bool ATTN, int CL = CG>
+template <int NS, int STAGE_BYTES, int CG, bool ATTN, int CL = CG, int AR = BM>
 __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_constant__ KParams p) {
   static_assert(CL == CG || (CG == 2 && CL == 4 && !ATTN), "unsupported cluster shape");
+  static_assert(AR == BM || (AR == 8 && CG == 1 && !ATTN), "8-row A tiles are built for single-SM MLP tiles");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
@@ -1512,7 +1518,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
         if (!wait_bar(&sc->uq_full[q], qphase, sc, p, 6)) break;
         const uint32_t unit = sc->uq[q];
         if (unit != UNIT_END && p.st[unit_stage(unit)].kind == STAGE_GEMM)
-          ok = tma_gemm_unit<NS, STAGE_BYTES, CG, CL>(p, sc, ring, rp, unit, q, rank);
+          ok = tma_gemm_unit<NS, STAGE_BYTES, CG, CL, AR>(p, sc, ring, rp, unit, q, rank);
         else if constexpr (ATTN)
           if (unit != UNIT_END) ok = tma_attn_unit<NS, STAGE_BYTES, CG>(p, sc, ring, rp, unit, q, rank);
         mbar_arrive(&sc->uq_empty[q]);
@@ -1556,7 +1562,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
         if (unit == UNIT_END) break;
         if (p.st[unit_stage(unit)].kind == STAGE_GEMM) {
           if (pair_leader) {
-            ok = mma_gemm_unit<NS, STAGE_BYTES, CG, CL>(p, sc, ring, rp, unit, acc, acc_phase, rank);
+            ok = mma_gemm_unit<NS, STAGE_BYTES, CG, CL, AR>(p, sc, ring, rp, unit, acc, acc_phase, rank);
             issued = true;
           } else if constexpr (CL == 4) {
             ok = fwd_gemm_unit<NS>(p, sc, rp, unit, rank);

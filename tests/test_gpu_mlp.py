@@ -355,3 +355,28 @@ def test_split_consumers_wait_for_their_own_producer_tiles(kind, split):
         cs.cs_chain_debug_set_delays(plan, 0, (torch.rand(q["units"][0], generator=g) * 300_000).long().tolist())
         delayed_b = forward(plan, dict(dev_a, X=b.X.cuda())).cpu()
     assert torch.equal(delayed_b, clean_b)
+
+
+@pytest.mark.parametrize("kind,tile_n", [("gelu", 128), ("gelu", 256), ("swiglu", 0)])
+@pytest.mark.parametrize("layout", ["nk", "kn"])
+@pytest.mark.parametrize("M", [2, 5, 8])
+def test_up_to_eight_rows_use_one_a_row_group(M, layout, kind, tile_n):
+    """Up to 8 rows, a stage holds only the one 8-row group of A (the MMA reads it
+    for all of its 128 rows; the rows past M are never stored), which leaves room
+    for 11 (or 5 with 256 rows of B) stages of weights: parity against the oracle,
+    every policy the same bits, producer delays change nothing."""
+    inp = cs_inputs.make_custom(kind, M, 2048, 1280 if kind == "gelu" else 688, seed=59)
+    dev = device_tensors(inp, layout)
+    outs = {}
+    for pol in ("tile", "row", "stream"):
+        with plan_for(inp, pol, layout, tile_n=tile_n) as plan:
+            q = cs.cs_chain_query(plan)
+            outs[pol] = forward(plan, dev).cpu()
+            if pol == "tile":
+                g = torch.Generator().manual_seed(60)
+                cs.cs_chain_debug_set_delays(plan, 0, (torch.rand(q["units"][0], generator=g) * 100_000).long().tolist())
+                assert torch.equal(forward(plan, dev).cpu(), outs[pol])
+    Yref, _ = _oracle(inp)
+    assert oracle.rel_err(outs["tile"], Yref) <= TOL
+    for k, v in outs.items():
+        assert torch.equal(v, outs["tile"]), k
