@@ -1,29 +1,34 @@
 // Persistent tile-synchronised GEMM-chain kernel for sm_103a.
 //
-// CTAs (or CTA pairs) pull work units from a dependency-ordered schedule
+// CTAs (or clusters) pull work units from a dependency-ordered schedule
 // through a global atomic counter (a megakernel-style task queue: a dependent
 // task starts once the slice it reads is done, not when the whole producer op
 // is done).  Roles inside a CTA (224 threads):
 //   warp 6      : scheduler.  Claims the next unit just in time (when the TMA
 //                 warp is a few K-slices from the end of its current unit),
-//                 and for consumer units polls the producer tile semaphores with
-//                 all 32 lanes at once, publishing how many leading producer
-//                 tiles are complete in shared memory (acquire at gpu scope,
-//                 release at CTA scope).
+//                 and for consumer units polls the producer tile semaphores of
+//                 the unit's K range with all 32 lanes at once, publishing how
+//                 many leading producer tiles are complete in shared memory
+//                 (acquire at gpu scope, release at CTA scope).
 //   warp 0      : TMA producer (lane 0).  Before loading a K-slice of the
-//                 intermediate it checks the published readiness (shared
-//                 memory only) and fences the async proxy.
+//                 intermediate it checks the published readiness (a compare in
+//                 the loop, an out-of-line wait at the bound) and fences the
+//                 async proxy.
 //   warp 1      : TMEM allocator (whole warp) and tcgen05.mma issuer (lane 0).
 //   warps 2..5  : epilogue: tcgen05.ld of the fp32 accumulator, bias + GeLU /
 //                 SiLU*up / none, downcast, swizzled smem staging, TMA store,
 //                 then (producer stages) release-increment of the tile
-//                 semaphore and of the row counter.
+//                 semaphore and of the row counter; the last K-split of a
+//                 small tile sums the splits' partials first.
 // CG = 2 (pair mode): a 2-CTA cluster shares one 256 x 256 tile.  Each CTA
 // loads its 128 rows of A and its half of B's columns; the leader (rank 0)
 // issues tcgen05.mma.cta_group::2, whose accumulator rows 0-127 land in the
 // leader's TMEM and rows 128-255 in the peer's; commits are multicast to both.
-// Semaphores stay per 128-row block, so each CTA of a consumer pair waits only
-// for the producer rows it reads.
+// CL = 4: two such pairs on consecutive 256-row blocks form a 4-CTA cluster
+// and share every weight box by TMA multicast.  Attention on pairs runs two
+// query blocks per unit.  AR = 8: up to 8 rows, one 8-row A group per stage.
+// Semaphores stay per 128-row block, so each CTA of a consumer cluster waits
+// only for the producer rows it reads.
 // Every wait is bounded: semaphore polls by the plan's timeout (error word +
 // global abort flag), mbarrier waits by a watchdog (error word + CTA abort).
 #pragma once
@@ -157,7 +162,7 @@ struct SmemCtl {
   uint64_t full[NS], empty[NS];
   uint64_t tfull[2], tempty[2];
   uint64_t uq_full[UQ], uq_empty[UQ];
-  uint64_t s_full, s_empty, p_full, o_full, o_empty;
+  uint64_t s_full, p_full, o_full;  // attention: S ready, P written, O_j ready
   uint64_t s_full_b;  // pair attention: S of odd key blocks (its own phases)
   uint64_t drain;
   uint64_t claim_req;       // TMA warp -> scheduler: claim the next unit now
@@ -1415,10 +1420,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
     mbar_init(&sc->mb_empty, CL - 1 > 0 ? CL - 1 : 1);  // every peer CTA takes the index
     mbar_init(&sc->s_full, 1);
     mbar_init(&sc->s_full_b, 1);
-    mbar_init(&sc->s_empty, 4);
     mbar_init(&sc->p_full, 4 * CG);  // every epilogue warp of the unit's CTAs
     mbar_init(&sc->o_full, 1);
-    mbar_init(&sc->o_empty, 4);
     mbar_init(&sc->drain, 1);
     sc->abort = 0;
     sc->tma_seq = 0;
