@@ -21,12 +21,14 @@ from .chain import (  # noqa: F401
     cs_chain_desc_init,
     cs_chain_destroy,
     cs_chain_forward_stage,
+    cs_chain_host_join,
     cs_chain_plan,
     cs_chain_query,
     cs_chain_reset,
     cs_chain_status,
     cs_last_error_string,
     cs_mlp_forward,
+    cs_mlp_forward_host,
     cs_mlp_forward_noalloc,
     cs_noalloc_status,
     cs_schedule_build,

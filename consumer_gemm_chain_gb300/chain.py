@@ -33,7 +33,8 @@ POLICIES = {"tile": CS_SYNC_TILE, "row": CS_SYNC_ROW, "strided": CS_SYNC_STRIDED
 KINDS = {"gelu": CS_CHAIN_MLP_GELU, "swiglu": CS_CHAIN_MLP_SWIGLU, "attn": CS_CHAIN_ATTN}
 
 EXPORTED = (
-    "cs_chain_desc_init", "cs_chain_plan", "cs_chain_destroy", "cs_mlp_forward", "cs_attn_chain_forward",
+    "cs_chain_desc_init", "cs_chain_plan", "cs_chain_destroy", "cs_mlp_forward", "cs_mlp_forward_host",
+    "cs_chain_host_join", "cs_attn_chain_forward",
     "cs_chain_forward_stage", "cs_chain_status", "cs_chain_reset", "cs_last_error_string", "cs_chain_query",
     "cs_schedule_build", "cs_chain_debug_read_sems", "cs_chain_debug_set_delays", "cs_chain_debug_skip_release",
     "cs_chain_debug_copy_intermediate", "cs_chain_debug_trace", "cs_chain_debug_read_trace", "cs_abi_version",
@@ -80,6 +81,8 @@ def _load() -> ctypes.CDLL:
         "cs_chain_plan": (I, [ctypes.POINTER(cs_chain_desc), ctypes.POINTER(V)]),
         "cs_chain_destroy": (I, [V]),
         "cs_mlp_forward": (I, [V, ctypes.POINTER(cs_mlp_args), V]),
+        "cs_mlp_forward_host": (I, [V, ctypes.POINTER(cs_mlp_args), V]),
+        "cs_chain_host_join": (I, [V, V]),
         "cs_attn_chain_forward": (I, [V, ctypes.POINTER(cs_attn_args), V]),
         "cs_chain_forward_stage": (I, [V, V, I, V]),
         "cs_chain_status": (I, [V]),
@@ -197,14 +200,16 @@ def _stream_ptr(stream) -> int | None:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
-def _ptr(t, shape, dtype, name):
-    """Device pointer of tensor t after checking shape/dtype/contiguity/device."""
+def _ptr(t, shape, dtype, name, host=False):
+    """Device (host=True: host) pointer of tensor t after checking shape/dtype/contiguity/device."""
     if t is None:
         return None
     import torch
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if not t.is_cuda:
+    if host and t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if not host and not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
     if t.dtype != dtype:
         raise ValueError(f"{name} has dtype {t.dtype}, the plan uses {dtype}")
@@ -243,6 +248,23 @@ def cs_mlp_forward(plan: Plan, X, W1=None, b1=None, W2=None, Y=None, Wg=None, Wu
     """Enqueue Y = GeLU(X W1 + b1) W2 (or the SwiGLU chain with Wg, Wu, W2=Wd) on ``stream``."""
     a = _mlp_args(plan, X, W1, b1, W2, Y, Wg, Wu)
     _check(_lib.cs_mlp_forward(plan.handle, ctypes.byref(a), _stream_ptr(stream)), "cs_mlp_forward")
+
+
+def cs_mlp_forward_host(plan: Plan, X, W1=None, b1=None, W2=None, Y=None, Wg=None, Wu=None, stream=None) -> None:
+    """Like cs_mlp_forward with X and Y in host memory (CPU tensors, pinned for
+    the copies to overlap the kernels); Y holds the result after
+    cs_chain_host_join on a stream and a synchronisation of that stream."""
+    d = plan.desc
+    dt = _torch_dtype(d)
+    a = _mlp_args(plan, None, W1, b1, W2, None, Wg, Wu)
+    a.X = _ptr(X, (d.M, d.H), dt, "X", host=True)
+    a.Y = _ptr(Y, (d.M, d.H), dt, "Y", host=True)
+    _check(_lib.cs_mlp_forward_host(plan.handle, ctypes.byref(a), _stream_ptr(stream)), "cs_mlp_forward_host")
+
+
+def cs_chain_host_join(plan: Plan, stream=None) -> None:
+    """Make ``stream`` wait for every Y read-back of cs_mlp_forward_host so far."""
+    _check(_lib.cs_chain_host_join(plan.handle, _stream_ptr(stream)), "cs_chain_host_join")
 
 
 def _attn_args(plan: Plan, X, Wqkv, Wo, Y) -> cs_attn_args:

@@ -78,6 +78,12 @@ struct cs_chain_s {
   int bn[3] = {128, 128, 128};
   int cfg_b = 0;  // 1: 48 KB-stage kernel (256-wide one-SM tiles or gate|up)
   int cfg_s = 0;  // up to 8 rows: 1 = 11 x 17 KB stages (128-wide B), 2 = 5 x 33 KB (256 rows of B)
+  // cs_mlp_forward_host: double-buffered device X / Y, copy streams and events
+  void* host_x[2] = {nullptr, nullptr};
+  void* host_y[2] = {nullptr, nullptr};
+  cudaStream_t s_h2d = nullptr, s_d2h = nullptr;
+  cudaEvent_t ev_x[2] = {nullptr, nullptr}, ev_k[2] = {nullptr, nullptr}, ev_y[2] = {nullptr, nullptr};
+  unsigned long long host_calls = 0;
   int cg = 1;     // CTAs per tcgen05 MMA (2: 256-row tiles on a 2-SM pair)
   int cl = 1;     // CTAs per unit and cluster (4: two pairs sharing weight boxes)
   int m_units = 0;   // tile rows of the schedule
@@ -375,6 +381,12 @@ void free_plan(cs_chain_s* p) {
   if (p->trace) cudaFree(p->trace);
   for (auto& b : p->partial) if (b) cudaFree(b);
   for (auto& b : p->split_ctr) if (b) cudaFree(b);
+  for (auto& b : p->host_x) if (b) cudaFree(b);
+  for (auto& b : p->host_y) if (b) cudaFree(b);
+  for (cudaEvent_t* evs : {p->ev_x, p->ev_k, p->ev_y})
+    for (int i = 0; i < 2; ++i) if (evs[i]) cudaEventDestroy(evs[i]);
+  if (p->s_h2d) cudaStreamDestroy(p->s_h2d);
+  if (p->s_d2h) cudaStreamDestroy(p->s_d2h);
   delete p;
 }
 
@@ -916,6 +928,53 @@ cs_status cs_mlp_forward(cs_chain_t p, const cs_mlp_args* a, void* stream) {
   kp.release = 1;
   kp.bump_epoch = 1;
   return launch(p, kp, p->sched_fused, p->n_fused, st);
+}
+
+cs_status cs_mlp_forward_host(cs_chain_t p, const cs_mlp_args* a, void* stream) {
+  if (!p) return fail(CS_ERR_INVALID_ARG, "plan is NULL");
+  if (!a || !a->X || !a->Y) return fail(CS_ERR_INVALID_ARG, "host X and Y are required");
+  if (p->d.kind == CS_CHAIN_ATTN) return fail(CS_ERR_INVALID_ARG, "plan is an attention chain");
+  const size_t bytes = static_cast<size_t>(p->d.M) * p->d.H * 2;
+  CS_CUDA(cudaSetDevice(p->device));
+  if (!p->s_h2d) {
+    for (int b = 0; b < 2; ++b)
+      if (cudaMalloc(&p->host_x[b], bytes) != cudaSuccess || cudaMalloc(&p->host_y[b], bytes) != cudaSuccess)
+        return fail(CS_ERR_OOM, "cudaMalloc of the host-path buffers failed");
+    for (cudaEvent_t* evs : {p->ev_x, p->ev_k, p->ev_y})
+      for (int i = 0; i < 2; ++i)
+        if (cudaEventCreateWithFlags(&evs[i], cudaEventDisableTiming) != cudaSuccess)
+          return fail(CS_ERR_CUDA, "cudaEventCreate failed");
+    if (cudaStreamCreateWithFlags(&p->s_h2d, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&p->s_d2h, cudaStreamNonBlocking) != cudaSuccess)
+      return fail(CS_ERR_CUDA, "cudaStreamCreate failed");
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int b = static_cast<int>(p->host_calls & 1u);
+  // X[b] was last read by the forward of call i-2; Y[b] last copied out by its read-back
+  // (waits on events not yet recorded complete at once)
+  CS_CUDA(cudaStreamWaitEvent(p->s_h2d, p->ev_k[b], 0));
+  CS_CUDA(cudaMemcpyAsync(p->host_x[b], a->X, bytes, cudaMemcpyHostToDevice, p->s_h2d));
+  CS_CUDA(cudaEventRecord(p->ev_x[b], p->s_h2d));
+  CS_CUDA(cudaStreamWaitEvent(st, p->ev_x[b], 0));
+  CS_CUDA(cudaStreamWaitEvent(st, p->ev_y[b], 0));
+  cs_mlp_args dev = *a;
+  dev.X = p->host_x[b];
+  dev.Y = p->host_y[b];
+  cs_status s = cs_mlp_forward(p, &dev, stream);
+  if (s != CS_OK) return s;
+  CS_CUDA(cudaEventRecord(p->ev_k[b], st));
+  CS_CUDA(cudaStreamWaitEvent(p->s_d2h, p->ev_k[b], 0));
+  CS_CUDA(cudaMemcpyAsync(a->Y, p->host_y[b], bytes, cudaMemcpyDeviceToHost, p->s_d2h));
+  CS_CUDA(cudaEventRecord(p->ev_y[b], p->s_d2h));
+  ++p->host_calls;
+  return CS_OK;
+}
+
+cs_status cs_chain_host_join(cs_chain_t p, void* stream) {
+  if (!p) return fail(CS_ERR_INVALID_ARG, "plan is NULL");
+  if (!p->s_h2d) return CS_OK;
+  for (int b = 0; b < 2; ++b) CS_CUDA(cudaStreamWaitEvent(static_cast<cudaStream_t>(stream), p->ev_y[b], 0));
+  return CS_OK;
 }
 
 cs_status cs_attn_chain_forward(cs_chain_t p, const cs_attn_args* a, void* stream) {

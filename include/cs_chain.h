@@ -171,6 +171,24 @@ typedef struct cs_mlp_args {
  * reported a device error that has not been cleared. */
 cs_status cs_mlp_forward(cs_chain_t plan, const cs_mlp_args* args, void* stream);
 
+/* End-to-end forward from host memory (no counterpart on the pages): args->X
+ * (M x H) and args->Y (M x H) are HOST pointers, page-locked for the copies to
+ * run asynchronously; weights and bias are device pointers as above.  The plan
+ * owns two device buffers for X and two for Y (allocated on the first call)
+ * and two copy streams: call i copies X on the first copy stream, runs the
+ * forward on `stream` once that copy has landed (and once the read-back of
+ * call i-2, which used the same Y buffer, is done), and copies Y back on the
+ * second copy stream, so consecutive calls overlap their copies with the
+ * kernels.  args->X may be reused or changed as soon as the call's copy has
+ * run; args->Y holds the result once cs_chain_host_join has made a stream wait
+ * for it and that stream has been synchronised.  The host buffers are the
+ * caller's and must stay valid until then. */
+cs_status cs_mlp_forward_host(cs_chain_t plan, const cs_mlp_args* args, void* stream);
+
+/* Make `stream` wait until every Y read-back issued by cs_mlp_forward_host on
+ * this plan so far has landed in host memory. */
+cs_status cs_chain_host_join(cs_chain_t plan, void* stream);
+
 /* Device pointers of one attention-chain forward, caller-owned.
  *  X [M,H]; Wqkv: KN [H, 3F] / NK [3F, H], columns (KN) [Q | K | V], head-major;
  *  Wo: KN [F, H] / NK [H, F]; Y [M,H] (written). */

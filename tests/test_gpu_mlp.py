@@ -380,3 +380,28 @@ def test_up_to_eight_rows_use_one_a_row_group(M, layout, kind, tile_n):
     assert oracle.rel_err(outs["tile"], Yref) <= TOL
     for k, v in outs.items():
         assert torch.equal(v, outs["tile"]), k
+
+
+@pytest.mark.parametrize("kind", ["gelu", "swiglu"])
+def test_host_memory_forward_matches_device_forward(kind):
+    """cs_mlp_forward_host: inputs and outputs in pinned host memory, four calls
+    back to back with different inputs (the plan's two device buffers each serve
+    two calls, the copies overlap the kernels); after the join every output
+    equals the device-memory forward bit for bit."""
+    inp = cs_inputs.make_custom(kind, 300, 1024, 768 if kind == "gelu" else 688, seed=61)
+    dev = device_tensors(inp, "nk")
+    wts = {k: v for k, v in dev.items() if k != "X"}
+    g = torch.Generator().manual_seed(62)
+    xs = [(torch.randn(inp.M, inp.H, generator=g) * 0.02).to(inp.dtype).pin_memory() for _ in range(4)]
+    ys = [torch.full((inp.M, inp.H), float("nan"), dtype=inp.dtype).pin_memory() for _ in range(4)]
+    with plan_for(inp, "tile", "nk") as plan:
+        refs = [forward(plan, dict(dev, X=x.cuda())).cpu() for x in xs]
+        for x, y in zip(xs, ys):
+            cs.cs_mlp_forward_host(plan, X=x, Y=y, **wts)
+        cs.cs_chain_host_join(plan)
+        torch.cuda.synchronize()
+        assert cs.cs_chain_status(plan) == cs.CS_OK
+        for y, r in zip(ys, refs):
+            assert torch.equal(y, r)
+        with pytest.raises(ValueError):
+            cs.cs_mlp_forward_host(plan, X=xs[0].cuda(), Y=ys[0], **wts)
