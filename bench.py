@@ -200,19 +200,25 @@ def time_loop(fn, steps, warmup, stream, finish=None):
     return total, per
 
 
-def simple_time(fn, iters=100, warmup=20):
+def simple_time(fn, iters=100, warmup=20, repeats=3):
+    """Median over `repeats` of the mean ms per call of fn over `iters` back-to-back
+    calls (CUDA events on the current stream, after `warmup` calls); the median
+    keeps a momentary clock dip out of difference metrics such as the overhead."""
     import torch
     s = torch.cuda.current_stream()
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(s)
-    for _ in range(iters):
-        fn()
-    b.record(s)
-    torch.cuda.synchronize()
-    return a.elapsed_time(b) / iters
+    runs = []
+    for _ in range(repeats):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        for _ in range(iters):
+            fn()
+        b.record(s)
+        torch.cuda.synchronize()
+        runs.append(a.elapsed_time(b) / iters)
+    return statistics.median(runs)
 
 
 # ------------------------------------------------------------------ CPU oracle timing

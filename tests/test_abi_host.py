@@ -170,7 +170,8 @@ def test_auto_tile_shape(cs):
     assert units(1536) == 3 * 24 + 3 * 48
     assert units(1280) == 5 * 24 + 5 * 48   # 256 x 256 pairs where 512 rows would add padding
     assert units(640) == 5 * 24 + 5 * 48    # 128 x 256 tiles on single SMs in between
-    assert units(256) == 2 * 48 + 2 * 96    # 128 x 128 tiles for small M
+    assert units(256) == 1 * 24 + 1 * 48    # two row blocks: one 256 x 256 pair tile row
+    assert units(128) == 1 * 48 + 1 * 96    # one row block: 128 x 128 tiles
     # SwiGLU (gate|up split over each pair): 512 x 256 tiles from M = 512, padding or not
     swiglu = cs.cs_chain_desc_init(kind="swiglu", M=768, H=8192, F=2752, split_k=1)
     assert len(cs.cs_schedule_build(swiglu, 148)) == 2 * 22 + 2 * 32
