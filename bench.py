@@ -19,6 +19,7 @@ Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload gpt3|str
 from __future__ import annotations
 
 import argparse
+import contextlib
 import json
 import os
 import statistics
@@ -219,6 +220,16 @@ def simple_time(fn, iters=100, warmup=20, repeats=3):
         torch.cuda.synchronize()
         runs.append(a.elapsed_time(b) / iters)
     return statistics.median(runs)
+
+
+def interleaved_times(fns, rounds=3):
+    """Median ms per call of each fn, timed in interleaved rounds (all of them
+    then see the same clock under the power cap)."""
+    runs = {name: [] for name in fns}
+    for _ in range(rounds):
+        for name, fn in fns.items():
+            runs[name].append(simple_time(fn, repeats=1))
+    return {name: statistics.median(v) for name, v in runs.items()}
 
 
 # ------------------------------------------------------------------ CPU oracle timing
@@ -545,10 +556,13 @@ def extras(cs, torch, inp, dev, Y, make_plan, plan, M, kind, peaks, stream):
         sub = {k: (v[:m].contiguous() if k == "X" else v) for k, v in dev.items()}
         Ym = torch.empty(m, inp.H, dtype=inp.dtype, device=X.device)
         rec = {"M": m}
-        for pol, pdl, key in (("tile", None, "tile"), ("stream", None, "stream"), ("stream", -1, "stream_nopdl")):
-            with make_plan(pol, m, pdl) as p:
-                ms = simple_time(lambda: cs.cs_mlp_forward(p, Y=Ym, **sub))
-            rec[f"{key}_us"] = ms * 1e3
+        with contextlib.ExitStack() as es:
+            fns = {}
+            for pol, pdl, key in (("tile", None, "tile"), ("stream", None, "stream"), ("stream", -1, "stream_nopdl")):
+                p = es.enter_context(make_plan(pol, m, pdl))
+                fns[key] = (lambda p=p: cs.cs_mlp_forward(p, Y=Ym, **sub))
+            for key, ms in interleaved_times(fns).items():
+                rec[f"{key}_us"] = ms * 1e3
         fl = chain_flops(kind, m, inp.H, inp.F)
         by = chain_bytes(kind, m, inp.H, inp.F)
         roof_ms = max(fl / (tc * 1e12), by / (hbm * 1e9)) * 1e3
@@ -582,11 +596,15 @@ def other_configs(cs, torch, peaks, lay):
         sub = dict(d, X=d["X"][:m].contiguous())
         Ym = torch.empty(m, inp.H, dtype=inp.dtype, device="cuda")
         rec = {"M": m}
-        for pol in ("tile", "stream"):
-            desc = cs.cs_chain_desc_init(kind="swiglu", M=m, H=inp.H, F=inp.F, dtype=inp.dtype, policy=pol,
-                                         weight_layout=lay)
-            with cs.cs_chain_plan(desc) as p:
-                rec[f"{pol}_us"] = simple_time(lambda: cs.cs_mlp_forward(p, Y=Ym, **sub)) * 1e3
+        with contextlib.ExitStack() as es:
+            fns = {}
+            for pol in ("tile", "stream"):
+                desc = cs.cs_chain_desc_init(kind="swiglu", M=m, H=inp.H, F=inp.F, dtype=inp.dtype, policy=pol,
+                                             weight_layout=lay)
+                p = es.enter_context(cs.cs_chain_plan(desc))
+                fns[pol] = (lambda p=p: cs.cs_mlp_forward(p, Y=Ym, **sub))
+            for pol, ms in interleaved_times(fns).items():
+                rec[f"{pol}_us"] = ms * 1e3
         fl = chain_flops("swiglu", m, inp.H, inp.F)
         rec["tflops"] = fl / (rec["tile_us"] * 1e-6) / 1e12
         rec["roofline_frac"], rec["bound"] = _roof_frac(fl, chain_bytes("swiglu", m, inp.H, inp.F), rec["tile_us"], peaks)
@@ -602,11 +620,15 @@ def other_configs(cs, torch, peaks, lay):
         Xm = d["X"][:m].contiguous()
         Ym = torch.empty(m, inp.H, dtype=inp.dtype, device="cuda")
         rec = {"M": m}
-        for pol in ("row", "stream"):
-            desc = cs.cs_chain_desc_init(kind="attn", M=m, H=inp.H, F=inp.F, heads=inp.F // 128, head_dim=128,
-                                         dtype=inp.dtype, policy=pol, weight_layout=lay)
-            with cs.cs_chain_plan(desc) as p:
-                rec[f"{pol}_us"] = simple_time(lambda: cs.cs_attn_chain_forward(p, Xm, d["Wqkv"], d["Wo"], Ym)) * 1e3
+        with contextlib.ExitStack() as es:
+            fns = {}
+            for pol in ("row", "stream"):
+                desc = cs.cs_chain_desc_init(kind="attn", M=m, H=inp.H, F=inp.F, heads=inp.F // 128, head_dim=128,
+                                             dtype=inp.dtype, policy=pol, weight_layout=lay)
+                p = es.enter_context(cs.cs_chain_plan(desc))
+                fns[pol] = (lambda p=p: cs.cs_attn_chain_forward(p, Xm, d["Wqkv"], d["Wo"], Ym))
+            for pol, ms in interleaved_times(fns).items():
+                rec[f"{pol}_us"] = ms * 1e3
         F3 = 3 * inp.F
         fl = 2.0 * m * inp.H * F3 + 2.0 * m * inp.F * inp.H + 2.0 * m * (m + 1) * inp.F
         by = 2 * (inp.H * F3 + inp.F * inp.H + 2 * m * inp.H + 2 * m * F3 + 2 * m * inp.F)
@@ -624,12 +646,17 @@ def other_configs(cs, torch, peaks, lay):
         sub = dict(d, X=d["X"][:m].contiguous())
         Ym = torch.empty(m, inp.H, dtype=inp.dtype, device="cuda")
         rec = {"M": m}
-        for pol in ("tile", "row", "strided", "stream"):
-            desc = cs.cs_chain_desc_init(kind="gelu", M=m, H=inp.H, F=inp.F, dtype=inp.dtype, policy=pol,
-                                         weight_layout=lay)
-            with cs.cs_chain_plan(desc) as p:
-                q = cs.cs_chain_query(p)
-                rec[f"{pol}_us"] = simple_time(lambda: cs.cs_mlp_forward(p, Y=Ym, **sub)) * 1e3
+        with contextlib.ExitStack() as es:
+            fns = {}
+            for pol in ("tile", "row", "strided", "stream"):
+                desc = cs.cs_chain_desc_init(kind="gelu", M=m, H=inp.H, F=inp.F, dtype=inp.dtype, policy=pol,
+                                             weight_layout=lay)
+                p = es.enter_context(cs.cs_chain_plan(desc))
+                if pol == "tile":
+                    q = cs.cs_chain_query(p)
+                fns[pol] = (lambda p=p: cs.cs_mlp_forward(p, Y=Ym, **sub))
+            for pol, ms in interleaved_times(fns).items():
+                rec[f"{pol}_us"] = ms * 1e3
         workers = q["num_sms"] * 128 // q["tile_m"]
         tiles0 = q["sched_units"][0]
         rec["stage0_units"], rec["workers"] = tiles0, workers
