@@ -256,10 +256,17 @@ def _oracle_rows(oracle, inp, rows):
 
 
 def cpu_cores():
+    """Host threads the oracle's BLAS may use: the CPUs this process may run on,
+    capped by an explicit thread limit (torchrun sets OMP_NUM_THREADS=1)."""
     try:
-        return len(os.sched_getaffinity(0))
+        n = len(os.sched_getaffinity(0))
     except AttributeError:
-        return os.cpu_count()
+        n = os.cpu_count() or 1
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        v = os.environ.get(var, "")
+        if v.isdigit() and int(v) > 0:
+            return min(n, int(v))
+    return n
 
 
 # ------------------------------------------------------------------ distributed
@@ -272,6 +279,21 @@ def dist_setup(args):
         backend = "nccl" if args.impl == "ours" else "gloo"
         dist.init_process_group(backend=backend)
     return ws, rank, local
+
+
+def replica_tile_m(ws, tile_m, kind, M):
+    """Tile rows for an N-rank replica run.  Cluster multicast of weight boxes
+    (512-row tiles on 4-CTA clusters) is kept to single-GPU runs, so with several
+    ranks the automatic and 512-row choices become 2-SM pairs or single SMs."""
+    if ws > 1 and tile_m in (0, 512):
+        return 256 if (kind == "gelu" and M >= 1024) else 128
+    return tile_m
+
+
+def whole_job_tflops(flops_per_rank, ms_max, ws):
+    """Whole-job throughput of N replicas: every rank does the same work, and the
+    slowest rank's time per step bounds the job."""
+    return ws * flops_per_rank / (ms_max * 1e-3) / 1e12
 
 
 def barrier(ws):
@@ -294,8 +316,16 @@ def max_over_ranks(v, ws, device=None):
 def run_reference(args):
     """The fp64 CPU oracle as the reference arm: same metric, workload and unit."""
     ws, rank, _ = dist_setup(args)
-    if rank != 0:
-        return
+    try:
+        if rank == 0:
+            _reference_line(args)
+    finally:
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+def _reference_line(args):
     import cs_inputs
     import oracle
     M = args.M or cs_inputs.WORKLOADS[args.workload][4]
@@ -355,9 +385,7 @@ def main():
     inp = cs_inputs.make_inputs(args.workload, M=M, seed=0)
     kind = inp.kind
     lay = args.layout
-    if ws > 1 and args.tile_m in (0, 512):
-        # cluster multicast stays in single-GPU runs: several ranks use 2-SM pairs
-        args.tile_m = 256 if (kind == "gelu" and M >= 1024) else 128
+    args.tile_m = replica_tile_m(ws, args.tile_m, kind, M)
 
     def w(t):
         t = t if lay == "kn" else t.t().contiguous()
@@ -411,7 +439,7 @@ def main():
     if st != cs.CS_OK:
         raise RuntimeError(f"device status {cs.STATUS_NAMES.get(st)}: {cs.cs_last_error_string()}")
     ms_step = max_over_ranks(ms_total, ws, device)
-    value = ws * flops / (ms_step * 1e-3) / 1e12
+    value = whole_job_tflops(flops, ms_step, ws)
 
     timed_s = ms_total * args.steps / 1e3
     sustained = timed_s >= 1.0
@@ -463,7 +491,7 @@ def main():
     e2e_ms, _ = time_loop(e2e_step, max(3, min(args.steps, 200)), 3, stream,
                           finish=lambda: cs.cs_chain_host_join(plan, stream))
     e2e_ms = max_over_ranks(e2e_ms, ws, device)
-    line["e2e"] = {"value": ws * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+    line["e2e"] = {"value": whole_job_tflops(flops, e2e_ms, ws), "unit": "TFLOP/s",
                    "h2d_bytes_per_step": Xh.numel() * Xh.element_size(),
                    "d2h_bytes_per_step": Yh.numel() * Yh.element_size(), "ms_per_step": e2e_ms,
                    "api": "cs_mlp_forward_host (double-buffered copies on two copy streams)"}
