@@ -84,6 +84,9 @@ def parse():
     ap.add_argument("--prefetch", type=int, default=0, help="L2 prefetch distance (0 auto, -1 off)")
     ap.add_argument("--raster", type=int, default=0, help="0 auto, 1 column-major, 2 row-major in a group")
     ap.add_argument("--pdl", type=int, default=0, help="programmatic dependent launch: 0 auto (on), 1 on, -1 off")
+    ap.add_argument("--tuning", default="default",
+                    help="tuning table for the plans' auto fields: 'default' (the package's table, when "
+                         "present), 'none' (built-in rules only) or a path")
     ap.add_argument("--quick", action="store_true", help="headline kernel only (profiling runs)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU-oracle sample time")
@@ -312,6 +315,19 @@ def max_over_ranks(v, ws, device=None):
     return float(t.item())
 
 
+def load_tuning(cs, which):
+    """Loads the tuning table the plans' auto fields come from; returns a record
+    for the JSON line."""
+    cs.cs_tune_clear()
+    if which == "none":
+        return {"table": None, "entries": 0}
+    path = cs.chain.TUNE_TABLE if which == "default" else which
+    if which == "default" and not os.path.exists(path):
+        return {"table": None, "entries": 0}
+    n = cs.cs_tune_load(path)
+    return {"table": os.path.relpath(path, ROOT), "entries": n}
+
+
 # ------------------------------------------------------------------ reference arm
 def run_reference(args):
     """The fp64 CPU oracle as the reference arm: same metric, workload and unit."""
@@ -379,6 +395,7 @@ def main():
 
     ws, rank, local = dist_setup(args)
     torch.cuda.set_device(local)
+    tuning = load_tuning(cs, args.tuning)
     device = torch.device("cuda", local)
     peaks, peak_src = load_peaks()
     M = args.M or cs_inputs.WORKLOADS[args.workload][4]
@@ -399,11 +416,11 @@ def main():
         dev.update(Wg=w(inp.Wg), Wu=w(inp.Wu), W2=w(inp.W2))
     Y = torch.empty_like(X)
 
-    def make_plan(policy, MM=M, pdl=None):
+    def make_plan(policy, MM=M, pdl=None, tuned=0):
         d = cs.cs_chain_desc_init(kind=kind, M=MM, H=inp.H, F=inp.F, dtype=inp.dtype, policy=policy,
                                   weight_layout=lay, lag=args.lag, tile_n=args.tile_n, group_m=args.group_m,
                                   tile_m=args.tile_m, split_k=args.split_k, prefetch=args.prefetch,
-                                  raster=args.raster, pdl=args.pdl if pdl is None else pdl)
+                                  raster=args.raster, pdl=args.pdl if pdl is None else pdl, tuned=tuned)
         return cs.cs_chain_plan(d)
 
     plan = make_plan(args.policy)
@@ -470,8 +487,8 @@ def main():
         "vs_baseline": None, "dtype": "f16" if inp.dtype == torch.float16 else "bf16", "data": "synthetic",
         "config": dict(workload_config(args.workload, M, inp, args.policy, lay), parallelism=f"replicas{ws}",
                        tile_n=plan_info["tile_n"][:2], tile_m=plan_info["tile_m"], group_m=plan_info["group_m"],
-                       lag=plan_info["lag"], pdl=args.pdl >= 0,
-                       grid=plan_info["num_sms"]),
+                       lag=plan_info["lag"], pdl=args.pdl >= 0, split_k=plan_info["split_k"][:2],
+                       grid=plan_info["num_sms"], tuning=dict(tuning, entry=plan_info["tuned_entry"])),
         "roofline": roof, "gpu_launches": args.steps * launches_per_step,
     }
     if sampler:
@@ -586,8 +603,11 @@ def extras(cs, torch, inp, dev, Y, make_plan, plan, M, kind, peaks, stream):
         rec = {"M": m}
         with contextlib.ExitStack() as es:
             fns = {}
-            for pol, pdl, key in (("tile", None, "tile"), ("stream", None, "stream"), ("stream", -1, "stream_nopdl")):
-                p = es.enter_context(make_plan(pol, m, pdl))
+            for pol, pdl, key, tuned in (("tile", None, "tile", 0), ("stream", None, "stream", 0),
+                                         ("stream", -1, "stream_nopdl", 0), ("tile", None, "tile_builtin", -1)):
+                p = es.enter_context(make_plan(pol, m, pdl, tuned))
+                if key == "tile":
+                    rec["plan"] = plan_record(cs.cs_chain_query(p))
                 fns[key] = (lambda p=p: cs.cs_mlp_forward(p, Y=Ym, **sub))
             for key, ms in interleaved_times(fns).items():
                 rec[f"{key}_us"] = ms * 1e3
@@ -601,6 +621,12 @@ def extras(cs, torch, inp, dev, Y, make_plan, plan, M, kind, peaks, stream):
         sweep.append(rec)
     out["sweep"] = sweep
     return out
+
+
+def plan_record(q):
+    """Tile shape, K-splits and tuning entry of a plan, for the sweep records."""
+    return {"tile_m": q["tile_m"], "tile_n": q["tile_n"][q["stages"] - 1], "split_k": max(q["split_k"]),
+            "tuned_entry": q["tuned_entry"]}
 
 
 def _roof_frac(fl, by, us, peaks):
@@ -626,13 +652,15 @@ def other_configs(cs, torch, peaks, lay):
         rec = {"M": m}
         with contextlib.ExitStack() as es:
             fns = {}
-            for pol in ("tile", "stream"):
+            for key, pol, tuned in (("tile", "tile", 0), ("stream", "stream", 0), ("tile_builtin", "tile", -1)):
                 desc = cs.cs_chain_desc_init(kind="swiglu", M=m, H=inp.H, F=inp.F, dtype=inp.dtype, policy=pol,
-                                             weight_layout=lay)
+                                             weight_layout=lay, tuned=tuned)
                 p = es.enter_context(cs.cs_chain_plan(desc))
-                fns[pol] = (lambda p=p: cs.cs_mlp_forward(p, Y=Ym, **sub))
-            for pol, ms in interleaved_times(fns).items():
-                rec[f"{pol}_us"] = ms * 1e3
+                if key == "tile":
+                    rec["plan"] = plan_record(cs.cs_chain_query(p))
+                fns[key] = (lambda p=p: cs.cs_mlp_forward(p, Y=Ym, **sub))
+            for key, ms in interleaved_times(fns).items():
+                rec[f"{key}_us"] = ms * 1e3
         fl = chain_flops("swiglu", m, inp.H, inp.F)
         rec["tflops"] = fl / (rec["tile_us"] * 1e-6) / 1e12
         rec["roofline_frac"], rec["bound"] = _roof_frac(fl, chain_bytes("swiglu", m, inp.H, inp.F), rec["tile_us"], peaks)
@@ -650,13 +678,15 @@ def other_configs(cs, torch, peaks, lay):
         rec = {"M": m}
         with contextlib.ExitStack() as es:
             fns = {}
-            for pol in ("row", "stream"):
+            for key, pol, tuned in (("row", "row", 0), ("stream", "stream", 0), ("row_builtin", "row", -1)):
                 desc = cs.cs_chain_desc_init(kind="attn", M=m, H=inp.H, F=inp.F, heads=inp.F // 128, head_dim=128,
-                                             dtype=inp.dtype, policy=pol, weight_layout=lay)
+                                             dtype=inp.dtype, policy=pol, weight_layout=lay, tuned=tuned)
                 p = es.enter_context(cs.cs_chain_plan(desc))
-                fns[pol] = (lambda p=p: cs.cs_attn_chain_forward(p, Xm, d["Wqkv"], d["Wo"], Ym))
-            for pol, ms in interleaved_times(fns).items():
-                rec[f"{pol}_us"] = ms * 1e3
+                if key == "row":
+                    rec["plan"] = plan_record(cs.cs_chain_query(p))
+                fns[key] = (lambda p=p: cs.cs_attn_chain_forward(p, Xm, d["Wqkv"], d["Wo"], Ym))
+            for key, ms in interleaved_times(fns).items():
+                rec[f"{key}_us"] = ms * 1e3
         F3 = 3 * inp.F
         fl = 2.0 * m * inp.H * F3 + 2.0 * m * inp.F * inp.H + 2.0 * m * (m + 1) * inp.F
         by = 2 * (inp.H * F3 + inp.F * inp.H + 2 * m * inp.H + 2 * m * F3 + 2 * m * inp.F)
@@ -676,15 +706,17 @@ def other_configs(cs, torch, peaks, lay):
         rec = {"M": m}
         with contextlib.ExitStack() as es:
             fns = {}
-            for pol in ("tile", "row", "strided", "stream"):
+            for key, pol, tuned in (("tile", "tile", 0), ("row", "row", 0), ("strided", "strided", 0),
+                                    ("stream", "stream", 0), ("tile_builtin", "tile", -1)):
                 desc = cs.cs_chain_desc_init(kind="gelu", M=m, H=inp.H, F=inp.F, dtype=inp.dtype, policy=pol,
-                                             weight_layout=lay)
+                                             weight_layout=lay, tuned=tuned)
                 p = es.enter_context(cs.cs_chain_plan(desc))
-                if pol == "tile":
+                if key == "tile":
                     q = cs.cs_chain_query(p)
-                fns[pol] = (lambda p=p: cs.cs_mlp_forward(p, Y=Ym, **sub))
-            for pol, ms in interleaved_times(fns).items():
-                rec[f"{pol}_us"] = ms * 1e3
+                    rec["plan"] = plan_record(q)
+                fns[key] = (lambda p=p: cs.cs_mlp_forward(p, Y=Ym, **sub))
+            for key, ms in interleaved_times(fns).items():
+                rec[f"{key}_us"] = ms * 1e3
         workers = q["num_sms"] * 128 // q["tile_m"]
         tiles0 = q["sched_units"][0]
         rec["stage0_units"], rec["workers"] = tiles0, workers

@@ -32,5 +32,9 @@ from .chain import (  # noqa: F401
     cs_mlp_forward_noalloc,
     cs_noalloc_status,
     cs_schedule_build,
+    cs_tune_clear,
+    cs_tune_load,
+    cs_tune_match,
+    cs_tune_size,
     decode_unit,
 )

@@ -11,8 +11,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libcs_chain.so")
-SOURCES = ["cs_chain.cu"]
-DEPS = ["cs_chain.cu", "cs_kernel.cuh", "cs_ptx.cuh", "cs_attn.cuh"]
+SOURCES = ["cs_chain.cu", "cs_tune.cpp"]
+DEPS = ["cs_chain.cu", "cs_kernel.cuh", "cs_ptx.cuh", "cs_tune.cpp", "cs_tune.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -27,9 +27,14 @@ STATUS_NAMES = {0: "CS_OK", 1: "CS_ERR_INVALID_ARG", 2: "CS_ERR_UNSUPPORTED", 3:
 # enums
 CS_F16, CS_BF16 = 0, 1
 CS_CHAIN_MLP_GELU, CS_CHAIN_MLP_SWIGLU, CS_CHAIN_ATTN = 0, 1, 2
-CS_SYNC_TILE, CS_SYNC_ROW, CS_SYNC_STRIDED, CS_SYNC_STREAM = 0, 1, 2, 3
+CS_SYNC_AUTO, CS_SYNC_TILE, CS_SYNC_ROW, CS_SYNC_STRIDED, CS_SYNC_STREAM = -1, 0, 1, 2, 3
 CS_WEIGHTS_KN, CS_WEIGHTS_NK = 0, 1
-POLICIES = {"tile": CS_SYNC_TILE, "row": CS_SYNC_ROW, "strided": CS_SYNC_STRIDED, "stream": CS_SYNC_STREAM}
+POLICIES = {"auto": CS_SYNC_AUTO, "tile": CS_SYNC_TILE, "row": CS_SYNC_ROW, "strided": CS_SYNC_STRIDED,
+            "stream": CS_SYNC_STREAM}
+POLICY_NAMES = {v: k for k, v in POLICIES.items()}
+# the tuning table measured on this package's target GPU (written by the tuner,
+# consumer_gemm_chain_gb300.tune); cs_tune_load() reads it
+TUNE_TABLE = os.path.join(PKG, "tuning", "gb300.json")
 KINDS = {"gelu": CS_CHAIN_MLP_GELU, "swiglu": CS_CHAIN_MLP_SWIGLU, "attn": CS_CHAIN_ATTN}
 
 EXPORTED = (
@@ -38,7 +43,8 @@ EXPORTED = (
     "cs_chain_forward_stage", "cs_chain_status", "cs_chain_reset", "cs_last_error_string", "cs_chain_query",
     "cs_schedule_build", "cs_chain_debug_read_sems", "cs_chain_debug_set_delays", "cs_chain_debug_skip_release",
     "cs_chain_debug_copy_intermediate", "cs_chain_debug_trace", "cs_chain_debug_read_trace", "cs_abi_version",
-    "cs_mlp_forward_noalloc", "cs_noalloc_status",
+    "cs_mlp_forward_noalloc", "cs_noalloc_status", "cs_tune_load", "cs_tune_clear", "cs_tune_size",
+    "cs_tune_match",
 )
 
 
@@ -49,7 +55,7 @@ class cs_chain_desc(ctypes.Structure):
                 ("num_sms", ctypes.c_int), ("lag", ctypes.c_int), ("group_m", ctypes.c_int),
                 ("tile_n", ctypes.c_int), ("tile_m", ctypes.c_int), ("split_k", ctypes.c_int),
                 ("prefetch", ctypes.c_int), ("raster", ctypes.c_int), ("pdl", ctypes.c_int),
-                ("spin_timeout_ns", ctypes.c_ulonglong)]
+                ("tuned", ctypes.c_int), ("spin_timeout_ns", ctypes.c_ulonglong)]
 
 
 class cs_mlp_args(ctypes.Structure):
@@ -68,7 +74,8 @@ class cs_chain_info(ctypes.Structure):
                 ("tile_n", ctypes.c_int * 3), ("tile_m", ctypes.c_int), ("sched_units", ctypes.c_int * 3),
                 ("split_k", ctypes.c_int * 3),
                 ("stride", ctypes.c_int),
-                ("intermediate", ctypes.c_void_p * 2), ("sem_words", ctypes.c_size_t * 2)]
+                ("intermediate", ctypes.c_void_p * 2), ("sem_words", ctypes.c_size_t * 2),
+                ("policy", ctypes.c_int), ("tuned_entry", ctypes.c_int)]
 
 
 def _load() -> ctypes.CDLL:
@@ -100,6 +107,10 @@ def _load() -> ctypes.CDLL:
         "cs_abi_version": (I, []),
         "cs_mlp_forward_noalloc": (I, [ctypes.POINTER(cs_chain_desc), ctypes.POINTER(cs_mlp_args), V]),
         "cs_noalloc_status": (I, []),
+        "cs_tune_load": (I, [ctypes.c_char_p, ctypes.POINTER(I)]),
+        "cs_tune_clear": (I, []),
+        "cs_tune_size": (I, []),
+        "cs_tune_match": (I, [ctypes.POINTER(cs_chain_desc), I, ctypes.POINTER(I), ctypes.POINTER(cs_chain_desc)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -311,7 +322,8 @@ def cs_chain_query(plan: Plan) -> dict:
             "group_m": i.group_m, "tile_n": list(i.tile_n), "tile_m": i.tile_m,
             "sched_units": list(i.sched_units), "split_k": list(i.split_k),
             "stride": i.stride, "intermediate": [i.intermediate[0], i.intermediate[1]],
-            "sem_words": [i.sem_words[0], i.sem_words[1]]}
+            "sem_words": [i.sem_words[0], i.sem_words[1]], "policy": POLICY_NAMES.get(i.policy, i.policy),
+            "tuned_entry": i.tuned_entry}
 
 
 def cs_schedule_build(desc: cs_chain_desc, num_sms: int) -> list[int]:
@@ -320,6 +332,33 @@ def cs_schedule_build(desc: cs_chain_desc, num_sms: int) -> list[int]:
     buf = (ctypes.c_uint32 * max(1, n.value))()
     _check(_lib.cs_schedule_build(ctypes.byref(desc), num_sms, buf, n.value, ctypes.byref(n)), "cs_schedule_build")
     return list(buf[: n.value])
+
+
+def cs_tune_load(path: str | None = None) -> int:
+    """Replace the process-wide tuning table with a JSON file (default: the
+    table measured for this package's target GPU); returns the entry count.
+    Plans made afterwards take their auto fields from it (cs_chain_desc.tuned)."""
+    n = ctypes.c_int()
+    path = TUNE_TABLE if path is None else os.fspath(path)
+    _check(_lib.cs_tune_load(path.encode(), ctypes.byref(n)), "cs_tune_load")
+    return n.value
+
+
+def cs_tune_clear() -> None:
+    _check(_lib.cs_tune_clear(), "cs_tune_clear")
+
+
+def cs_tune_size() -> int:
+    return _lib.cs_tune_size()
+
+
+def cs_tune_match(desc: cs_chain_desc, num_sms: int) -> tuple[int, cs_chain_desc]:
+    """(index of the table entry a plan of ``desc`` on ``num_sms`` SMs applies, or -1;
+    the desc as that plan runs it).  Needs no GPU."""
+    e = ctypes.c_int()
+    r = cs_chain_desc()
+    _check(_lib.cs_tune_match(ctypes.byref(desc), num_sms, ctypes.byref(e), ctypes.byref(r)), "cs_tune_match")
+    return e.value, r
 
 
 def decode_unit(u: int) -> tuple[int, int, int, int]:

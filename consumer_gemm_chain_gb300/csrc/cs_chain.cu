@@ -16,6 +16,7 @@
 
 #include "../../include/cs_chain.h"
 #include "cs_kernel.cuh"
+#include "cs_tune.h"
 
 namespace {
 
@@ -63,8 +64,17 @@ struct MapSlot {
 
 }  // namespace
 
+cs_status cs_fail(cs_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
 struct cs_chain_s {
-  cs_chain_desc d{};
+  cs_chain_desc d{};  // as run: tuning-table choices applied, policy AUTO resolved
+  int tuned_entry = -1;
   int device = 0;
   int num_sms = 0;
   int m_tiles = 0;
@@ -175,7 +185,8 @@ cs_status validate(const cs_chain_desc* d) {
   if (!d) return fail(CS_ERR_INVALID_ARG, "desc is NULL");
   if (d->kind < CS_CHAIN_MLP_GELU || d->kind > CS_CHAIN_ATTN) return fail(CS_ERR_INVALID_ARG, "bad kind %d", d->kind);
   if (d->dtype != CS_F16 && d->dtype != CS_BF16) return fail(CS_ERR_INVALID_ARG, "bad dtype %d", d->dtype);
-  if (d->policy < CS_SYNC_TILE || d->policy > CS_SYNC_STREAM) return fail(CS_ERR_INVALID_ARG, "bad policy %d", d->policy);
+  if (d->policy < CS_SYNC_AUTO || d->policy > CS_SYNC_STREAM) return fail(CS_ERR_INVALID_ARG, "bad policy %d", d->policy);
+  if (d->tuned < -1 || d->tuned > 0) return fail(CS_ERR_INVALID_ARG, "tuned=%d (0 or -1)", d->tuned);
   if (d->weight_layout != CS_WEIGHTS_KN && d->weight_layout != CS_WEIGHTS_NK)
     return fail(CS_ERR_INVALID_ARG, "bad weight_layout %d", d->weight_layout);
   if (d->M < 1 || d->M > 128 * 4095) return fail(CS_ERR_INVALID_ARG, "M=%d out of range [1, %d]", d->M, 128 * 4095);
@@ -205,6 +216,22 @@ cs_status validate(const cs_chain_desc* d) {
       return fail(CS_ERR_UNSUPPORTED, "the attention chain runs 128 x 128 or 256 x 256 (pair) tiles only");
   }
   return CS_OK;
+}
+
+// The desc a plan runs: the tuning table's choices for the fields left on auto
+// (an entry whose choices this desc rejects is ignored), policy AUTO resolved.
+cs_chain_desc resolve_desc(const cs_chain_desc* d, int num_sms, int* entry) {
+  cs_chain_desc t;
+  int e = cs_tune_apply(d, num_sms, &t);
+  if (e >= 0) {
+    char saved[sizeof(g_err)];
+    std::memcpy(saved, g_err, sizeof(g_err));
+    if (validate(&t) != CS_OK) e = -1, t = *d;
+    std::memcpy(g_err, saved, sizeof(g_err));
+  }
+  if (t.policy == CS_SYNC_AUTO) t.policy = CS_SYNC_TILE;
+  *entry = e;
+  return t;
 }
 
 Geometry geometry(const cs_chain_desc* d, int num_sms) {
@@ -764,6 +791,7 @@ cs_status cs_chain_desc_init(cs_chain_desc* d) {
   d->prefetch = 0;
   d->raster = 0;
   d->pdl = 0;
+  d->tuned = 0;
   return CS_OK;
 }
 
@@ -773,7 +801,9 @@ cs_status cs_schedule_build(const cs_chain_desc* desc, int num_sms, uint32_t* un
   if (num_sms < 1) return fail(CS_ERR_INVALID_ARG, "num_sms=%d", num_sms);
   if (!n_out) return fail(CS_ERR_INVALID_ARG, "n_out is NULL");
   if (cap > 0 && !units) return fail(CS_ERR_INVALID_ARG, "units is NULL");
-  Geometry g = geometry(desc, num_sms);
+  int entry = -1;
+  const cs_chain_desc rd = resolve_desc(desc, num_sms, &entry);
+  Geometry g = geometry(&rd, num_sms);
   std::vector<uint32_t> v = build_fused(g);
   *n_out = v.size();
   for (size_t i = 0; i < v.size() && i < cap; ++i) units[i] = v[i];
@@ -796,10 +826,10 @@ cs_status cs_chain_plan(const cs_chain_desc* desc, cs_chain_t* out) {
 
   cs_chain_s* p = new (std::nothrow) cs_chain_s();
   if (!p) return fail(CS_ERR_OOM, "host allocation failed");
-  p->d = *desc;
   p->device = dev;
   p->num_sms = desc->num_sms > 0 && desc->num_sms < sms ? desc->num_sms : sms;
-  Geometry g = geometry(desc, p->num_sms);
+  p->d = resolve_desc(desc, p->num_sms, &p->tuned_entry);
+  Geometry g = geometry(&p->d, p->num_sms);
   p->m_tiles = g.m_blocks;
   p->m_units = g.m_tiles;
   p->m_blocks = g.m_blocks;
@@ -1082,6 +1112,19 @@ cs_status cs_chain_query(cs_chain_t p, cs_chain_info* info) {
   info->intermediate[1] = p->inter[1];
   info->sem_words[0] = p->sem_words[0];
   info->sem_words[1] = p->sem_words[1];
+  info->policy = p->d.policy;
+  info->tuned_entry = p->tuned_entry;
+  return CS_OK;
+}
+
+cs_status cs_tune_match(const cs_chain_desc* desc, int num_sms, int* entry, cs_chain_desc* resolved) {
+  if (!entry) return fail(CS_ERR_INVALID_ARG, "entry is NULL");
+  *entry = -1;
+  cs_status s = validate(desc);
+  if (s != CS_OK) return s;
+  if (num_sms < 1) return fail(CS_ERR_INVALID_ARG, "num_sms=%d", num_sms);
+  const cs_chain_desc rd = resolve_desc(desc, num_sms, entry);
+  if (resolved) *resolved = rd;
   return CS_OK;
 }
 
@@ -1206,6 +1249,7 @@ cs_status cs_mlp_forward_noalloc(const cs_chain_desc* desc, const cs_mlp_args* a
   cs_chain_s p;
   p.d = *desc;
   p.d.split_k = 1;  // no split-K workspace in the fixed array
+  if (p.d.policy == CS_SYNC_AUTO) p.d.policy = CS_SYNC_TILE;  // no tuning table here
   p.device = dev;
   p.num_sms = desc->num_sms > 0 && desc->num_sms < sms ? desc->num_sms : sms;
   Geometry g = geometry(&p.d, p.num_sms);

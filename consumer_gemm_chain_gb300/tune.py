@@ -1,0 +1,233 @@
+"""Tuner for the plan's automatic choices: measures tile shape x K-split
+candidates under every sync policy for a chain shape and a list of row counts
+M, and writes the fastest per (M, policy) as a tuning table that
+``cs_tune_load`` reads (Flux summary, idea I4: one kernel code base, tuned per
+GPU and environment).
+
+    python -m consumer_gemm_chain_gb300.tune --preset gpt3 [--M 1,16,...] [--out FILE] [--merge]
+
+Per M: every candidate runs under TileSync (RowSync for the attention chain);
+the three fastest are timed again under every policy, including the
+two-kernel control (so that the control, too, runs its best tiles); the best
+candidate of each policy is re-timed against the built-in rules in
+interleaved rounds, and an entry is written per policy.  Each candidate's
+output is checked against the built-in plan's output before it is timed.
+Inputs are random device tensors of the shape (N(0, 0.02)); timing uses CUDA
+events on the current stream, after warm-up, with weights larger than L2.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import sys
+
+from . import chain as cs
+
+PRESETS = {
+    # name: (kind, H, F, dtype name, heads, default M list)
+    "gpt3": ("gelu", 12288, 6144, "f16", 0, (1, 16, 64, 256, 512, 1024, 2048)),
+    "llama": ("swiglu", 8192, 2752, "bf16", 0, (1, 16, 64, 256, 512, 1024, 2048)),
+    "attn": ("attn", 12288, 1536, "f16", 12, (1, 16, 64, 256, 512, 1024, 2048)),
+    "stress": ("gelu", 8192, 8192, "f16", 0, tuple(128 * b for b in range(1, 13))),
+}
+MLP_TILES = ((128, 128), (128, 256), (256, 256), (512, 256))
+ATTN_TILES = ((128, 128), (256, 256))
+POLICIES = ("tile", "row", "strided", "stream")
+
+
+def _inputs(torch, kind, M, H, F, dtype, dev, seed=0):
+    g = torch.Generator(device=dev).manual_seed(seed)
+
+    def r(*shape):
+        return (torch.randn(*shape, generator=g, device=dev, dtype=torch.float32) * 0.02).to(dtype)
+
+    t = {"X": r(M, H)}
+    if kind == "gelu":
+        t.update(W1=r(F, H), b1=r(F), W2=r(H, F))
+    elif kind == "swiglu":
+        t.update(Wg=r(F, H), Wu=r(F, H), W2=r(H, F))
+    else:
+        t.update(Wqkv=r(3 * F, H), Wo=r(H, F))
+    return t
+
+
+def _time(torch, fn, target_ms=12.0, warmup=3, repeats=1):
+    s = torch.cuda.current_stream()
+    for _ in range(warmup):
+        fn()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s)
+    fn()
+    b.record(s)
+    torch.cuda.synchronize()
+    iters = max(5, min(400, int(target_ms / max(a.elapsed_time(b), 1e-3))))
+    runs = []
+    for _ in range(repeats):
+        a.record(s)
+        for _ in range(iters):
+            fn()
+        b.record(s)
+        torch.cuda.synchronize()
+        runs.append(a.elapsed_time(b) / iters * 1e3)
+    return statistics.median(runs)
+
+
+class Candidate:
+    def __init__(self, kind, shape, policy, tile_m=0, tile_n=0, split_k=0, tuned=-1):
+        self.key = (tile_m, tile_n, split_k)
+        self.policy = policy
+        self.desc = cs.cs_chain_desc_init(kind=kind, M=shape["M"], H=shape["H"], F=shape["F"],
+                                          dtype=shape["dtype"], policy=policy, weight_layout="nk",
+                                          heads=shape["heads"] or 12, tile_m=tile_m, tile_n=tile_n,
+                                          split_k=split_k, tuned=tuned)
+
+
+def _forward(plan, kind, t, Y):
+    if kind == "attn":
+        return lambda: cs.cs_attn_chain_forward(plan, t["X"], t["Wqkv"], t["Wo"], Y)
+    w = {k: v for k, v in t.items() if k != "X"}
+    return lambda: cs.cs_mlp_forward(plan, t["X"], Y=Y, **w)
+
+
+def _rel(torch, a, b):
+    return float((a.float() - b.float()).abs().max() / b.float().abs().max().clamp_min(1e-30))
+
+
+def tune_shape(torch, kind, H, F, dtype, heads, Ms, log=print):
+    dev = torch.device("cuda", torch.cuda.current_device())
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    tiles = ATTN_TILES if kind == "attn" else MLP_TILES
+    base = "row" if kind == "attn" else "tile"
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
+    entries = []
+    for M in Ms:
+        shape = {"M": M, "H": H, "F": F, "dtype": tdt, "heads": heads}
+        t = _inputs(torch, kind, M, H, F, tdt, dev)
+        Y = torch.empty(M, H, dtype=tdt, device=dev)
+        splits = (1, 2, 3, 4) + ((6, 8, 12) if M <= 32 else ())
+
+        def run(c):
+            """(us, plan info) of one candidate; checks its status and its output
+            against the built-in plan's."""
+            with cs.cs_chain_plan(c.desc) as plan:
+                info = cs.cs_chain_query(plan)
+                fwd = _forward(plan, kind, t, Y)
+                fwd()
+                torch.cuda.synchronize()
+                if cs.cs_chain_status(plan) != cs.CS_OK:
+                    raise RuntimeError(f"M={M} {c.policy} {c.key}: device status {cs.cs_chain_status(plan)}")
+                if ref is not None:
+                    err = _rel(torch, Y, ref)
+                    if not err <= 5e-3:
+                        raise RuntimeError(f"M={M} {c.policy} {c.key}: output differs from the built-in plan's "
+                                           f"by {err:.2e}")
+                return _time(torch, fwd), info
+
+        ref = None
+        auto = Candidate(kind, shape, base)
+        with cs.cs_chain_plan(auto.desc) as plan:
+            _forward(plan, kind, t, Y)()
+            torch.cuda.synchronize()
+            ref = Y.clone()
+        # 1: every tile shape x split under the base policy
+        first = {}
+        for tm, tn in tiles:
+            for sp in splits:
+                if sp > 4 and tm > 128:
+                    continue  # many-way splits pay off only where single SMs stream the weights
+                c = Candidate(kind, shape, base, tm, tn, sp)
+                try:
+                    us, info = run(c)
+                except cs.CSError:
+                    continue  # a shape this desc rejects
+                # the last stage's tiles (SwiGLU producer tiles are always 128 wide)
+                real = (info["tile_m"], info["tile_n"][info["stages"] - 1], max(info["split_k"]))
+                if real != (tm, tn, sp):
+                    continue  # clamped to another candidate (too few K-slices for the split)
+                first[c.key] = us
+        top = sorted(first, key=first.get)[:3]
+        # 2: the three fastest under every policy (the control included)
+        best = {}
+        for pol in POLICIES:
+            for key in top:
+                us = first[key] if pol == base else run(Candidate(kind, shape, pol, *key))[0]
+                if pol not in best or us < best[pol][1]:
+                    best[pol] = (key, us)
+        # 3: each policy's best against the built-in rules, interleaved rounds
+        finals = {pol: Candidate(kind, shape, pol, *best[pol][0]) for pol in POLICIES}
+        builtin = {pol: Candidate(kind, shape, pol) for pol in POLICIES}
+        times, builtin_key = {}, {}
+        for _ in range(3):
+            for pol in POLICIES:
+                for name, c in (("tuned", finals[pol]), ("builtin", builtin[pol])):
+                    us, info = run(c)
+                    times.setdefault((pol, name), []).append(us)
+                    if name == "builtin":
+                        # the built-in tiles, with the built-in (auto) split rule
+                        builtin_key[pol] = (info["tile_m"], info["tile_n"][info["stages"] - 1], 0)
+        for pol in POLICIES:
+            us = statistics.median(times[(pol, "tuned")])
+            us_auto = statistics.median(times[(pol, "builtin")])
+            tm, tn, sp = finals[pol].key if us < us_auto else builtin_key[pol]
+            us = min(us, us_auto)
+            entries.append({"kind": kind, "dtype": dtype, "H": H, "F": F, "M": M, "sms": sms, "layout": "nk",
+                            "policy": pol, "tile_m": tm, "tile_n": tn, "split_k": sp, "group_m": 0,
+                            "us": round(us, 2), "builtin_us": round(us_auto, 2)})
+            log(f"{kind} M={M:5d} {pol:8s} tile {tm}x{tn} split {sp:2d}: {us:8.1f} us "
+                f"(built-in rules {us_auto:8.1f} us)")
+        del t, Y, ref
+        torch.cuda.empty_cache()
+    return entries
+
+
+def _key(e):
+    return (e["kind"], e["dtype"], e["H"], e["F"], e["M"], e["sms"], e.get("layout", "any"), e.get("policy", "any"))
+
+
+def write_table(path, entries, merge, device):
+    old = []
+    if merge and os.path.exists(path):
+        with open(path) as f:
+            old = json.load(f).get("entries", [])
+    keys = {_key(e) for e in entries}
+    merged = [e for e in old if _key(e) not in keys] + entries
+    merged.sort(key=lambda e: (e["kind"], e["H"], e["F"], e["dtype"], e["M"], e.get("policy", "")))
+    doc = {"format": "cs_chain_tuning", "version": 1, "device": device,
+           "written_by": "python -m consumer_gemm_chain_gb300.tune", "entries": merged}
+    os.makedirs(os.path.dirname(os.path.abspath(path)), exist_ok=True)
+    with open(path, "w") as f:
+        f.write("{\n")
+        f.write(f'  "format": "cs_chain_tuning", "version": 1, "device": {json.dumps(device)},\n')
+        f.write(f'  "written_by": {json.dumps(doc["written_by"])},\n  "entries": [\n')
+        f.write(",\n".join("    " + json.dumps(e) for e in merged))
+        f.write("\n  ]\n}\n")
+    return len(merged)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--preset", action="append", choices=sorted(PRESETS), required=True)
+    ap.add_argument("--M", default="", help="comma-separated row counts (default: the preset's list)")
+    ap.add_argument("--out", default=cs.TUNE_TABLE)
+    ap.add_argument("--merge", action="store_true", help="keep the file's entries for other shapes / M")
+    args = ap.parse_args(argv)
+    import torch
+    if not torch.cuda.is_available():
+        raise SystemExit("the tuner times kernels on a GPU; none is visible")
+    props = torch.cuda.get_device_properties(0)
+    device = {"name": props.name, "sms": props.multi_processor_count, "cc": f"{props.major}.{props.minor}"}
+    entries = []
+    n = 0
+    for name in args.preset:
+        kind, H, F, dtype, heads, Ms = PRESETS[name]
+        if args.M:
+            Ms = tuple(int(v) for v in args.M.split(","))
+        entries += tune_shape(torch, kind, H, F, dtype, heads, Ms, log=lambda s: print(s, file=sys.stderr, flush=True))
+        n = write_table(args.out, entries, args.merge, device)  # after every shape: keep what is measured
+    print(json.dumps({"out": args.out, "entries": n}))
+
+
+if __name__ == "__main__":
+    main()

@@ -42,7 +42,7 @@
 extern "C" {
 #endif
 
-#define CS_ABI_VERSION 2
+#define CS_ABI_VERSION 3
 
 typedef struct cs_chain_s* cs_chain_t;
 
@@ -76,8 +76,18 @@ typedef enum cs_chain_kind { CS_CHAIN_MLP_GELU = 0, CS_CHAIN_MLP_SWIGLU = 1, CS_
  *            is congruent (mod stride) to the one that wrote the K-slice.  With
  *            stride = heads this is "the Q, K and V tiles of one head".
  *  STREAM  : two-kernel control: all producer tiles in one launch, all consumer
- *            tiles in a second launch on the same stream, no tile waits.        */
-typedef enum cs_policy { CS_SYNC_TILE = 0, CS_SYNC_ROW = 1, CS_SYNC_STRIDED = 2, CS_SYNC_STREAM = 3 } cs_policy;
+ *            tiles in a second launch on the same stream, no tile waits.
+ *  AUTO    : (desc only) the fastest fused policy (TILE, ROW or STRIDED) that the
+ *            loaded tuning table recorded for this chain shape at the nearest
+ *            measured M; TILE when the table has no entry.  All policies give the
+ *            same bits; only the timing differs.                               */
+typedef enum cs_policy {
+  CS_SYNC_AUTO = -1,
+  CS_SYNC_TILE = 0,
+  CS_SYNC_ROW = 1,
+  CS_SYNC_STRIDED = 2,
+  CS_SYNC_STREAM = 3
+} cs_policy;
 
 /* Storage layout of every weight matrix of the chain.
  *  KN : W stored as in the maths, [K, N] row-major (W1 is [H, F]).
@@ -136,6 +146,12 @@ typedef struct cs_chain_desc {
                           the earlier grid drains; it reads global memory only after
                           that grid has completed (griddepcontrol.wait).  0 = auto
                           (on), 1 = on, -1 = off (plain stream order)               */
+  int tuned;           /* 0 = consult the loaded tuning table (cs_tune_load): when
+                          tile_m, tile_n, split_k and group_m are all auto, they are
+                          taken from the entry of the nearest measured M for this
+                          chain shape, dtype, layout and grid size, and policy AUTO
+                          is resolved from it; an entry whose choices do not fit the
+                          desc is ignored.  -1 = never (built-in rules only).       */
   unsigned long long spin_timeout_ns; /* per-wait limit of a consumer tile; 0 = 2 s */
 } cs_chain_desc;
 
@@ -240,6 +256,8 @@ typedef struct cs_chain_info {
   int stride;              /* strided-policy stride actually used */
   void* intermediate[2];   /* H (MLP) or QKV, O (ATTN): device pointers owned by the plan */
   size_t sem_words[2];     /* length of each boundary's tile-semaphore array */
+  int policy;              /* cs_policy the plan runs (AUTO resolved) */
+  int tuned_entry;         /* index of the tuning-table entry applied, -1 = none */
 } cs_chain_info;
 
 cs_status cs_chain_query(cs_chain_t plan, cs_chain_info* info);
@@ -252,6 +270,43 @@ cs_status cs_chain_query(cs_chain_t plan, cs_chain_info* info);
  * are not written (cap may be 0 to query the count).  Needs no GPU. */
 cs_status cs_schedule_build(const cs_chain_desc* desc, int num_sms, uint32_t* units, size_t cap,
                             size_t* n_out);
+
+/* Tuning table. ------------------------------------------------------------ */
+/* Per-shape tuning of the plan's automatic choices (Flux summary, idea I4: one
+ * kernel code base auto-tuned per GPU and environment).  A process-wide table
+ * of measured best choices, applied by cs_chain_plan and cs_schedule_build to
+ * descs that leave them on auto (see cs_chain_desc.tuned).
+ *
+ * File format (JSON, written by the package's tuner, consumer_gemm_chain_gb300.tune):
+ *   {"format": "cs_chain_tuning", "version": 1, "entries": [ENTRY, ...], ...}
+ *   ENTRY = {"kind": "gelu"|"swiglu"|"attn", "dtype": "f16"|"bf16", "H": int,
+ *            "F": int, "M": int, "sms": int (grid the entry was measured on),
+ *            "tile_m": 0|128|256|512, "tile_n": 0|128|256, "split_k": 0..15,
+ *            optional "group_m": int >= 0 (default 0 = auto),
+ *            optional "layout": "kn"|"nk"|"any", "policy": "tile"|"row"|
+ *            "strided"|"stream"|"any" (default any), "us": time per chain (> 0)}
+ * Other keys are ignored.  Matching: entries of the same kind, dtype, H, F and
+ * sms whose layout and policy fit the desc; of those, the ones at the measured
+ * M nearest to desc.M on a log2 scale (ties: the smaller M); among those, for
+ * policy AUTO the smallest "us", otherwise the entry naming the most of layout
+ * and policy, then the smallest "us", then the first in the file. */
+
+/* Replace the table with the entries of a JSON file.  On any error (unreadable
+ * file, bad JSON, missing or out-of-range field: the message names the entry)
+ * the table is left as it was.  *n_entries (may be NULL) receives the count.
+ * Thread-safe; plans made earlier keep their choices. */
+cs_status cs_tune_load(const char* path, int* n_entries);
+
+/* Empty the table (the built-in rules then decide every auto field). */
+cs_status cs_tune_clear(void);
+
+/* Entries in the table. */
+int cs_tune_size(void);
+
+/* Host-only: the index of the entry a plan with this desc on num_sms SMs would
+ * apply, or -1 (into *entry); *resolved (may be NULL) receives the desc with the
+ * entry applied and policy AUTO resolved.  Needs no GPU. */
+cs_status cs_tune_match(const cs_chain_desc* desc, int num_sms, int* entry, cs_chain_desc* resolved);
 
 /* Testing aids. ------------------------------------------------------------ */
 

@@ -1,0 +1,60 @@
+"""GPU parity of plans whose tile shape, K-splits and policy come from the
+shipped tuning table (desc fields on auto, policy AUTO), against the fp64
+oracle, through the C ABI.  The table only changes how the chain is tiled and
+synchronised, never what it computes."""
+from __future__ import annotations
+
+import os
+
+import pytest
+import torch
+
+import cs_inputs
+import oracle
+from tests.gpu_util import TOL, device_tensors, forward, plan_for
+
+pytestmark = pytest.mark.gpu
+
+cs = pytest.importorskip("consumer_gemm_chain_gb300")
+
+
+@pytest.fixture(scope="module")
+def tuned_table():
+    if not os.path.exists(cs.chain.TUNE_TABLE):
+        pytest.skip("no tuning table shipped")
+    n = cs.cs_tune_load()
+    assert n > 0
+    yield n
+    cs.cs_tune_clear()
+
+
+def _oracle_rows(inp, rows):
+    if inp.kind == "gelu":
+        return oracle.mlp_gelu(inp.X[rows], inp.W1, inp.b1, inp.W2)
+    if inp.kind == "swiglu":
+        return oracle.mlp_swiglu(inp.X[rows], inp.Wg, inp.Wu, inp.W2)
+    Y = oracle.attention_chain(inp.X, inp.Wqkv, inp.Wo, heads=inp.F // 128, head_dim=128)
+    return Y[rows]
+
+
+@pytest.mark.parametrize("workload,M", [("gpt3", 1), ("gpt3", 256), ("gpt3", 2048), ("llama", 64), ("llama", 1024),
+                                        ("attn", 16), ("attn", 512), ("stress", 384), ("stress", 1152)])
+def test_tuned_plans_match_the_oracle(tuned_table, workload, M):
+    inp = cs_inputs.make_inputs(workload, M=M, seed=0)
+    dev = device_tensors(inp, "nk")
+    outs = {}
+    for tuned in (0, -1):
+        with plan_for(inp, "auto", "nk", tuned=tuned) as plan:
+            q = cs.cs_chain_query(plan)
+            if tuned == 0:
+                assert q["tuned_entry"] >= 0, "the shipped table has an entry for this shape"
+                assert q["policy"] in ("tile", "row", "strided")
+            else:
+                assert q["tuned_entry"] == -1 and q["policy"] == "tile"
+            outs[tuned] = forward(plan, dev).cpu()
+    rows = cs_inputs.sample_rows(M, 64)
+    Yref = _oracle_rows(inp, rows)
+    for tuned, Y in outs.items():
+        assert oracle.rel_err(Y[rows], Yref) <= TOL, tuned
+    # tiled differently, the same sums up to fp32 rounding order
+    assert oracle.rel_err(outs[0], outs[-1]) <= 2e-3
