@@ -119,8 +119,10 @@ def tune_shape(torch, kind, H, F, dtype, heads, Ms, log=print):
                 if cs.cs_chain_status(plan) != cs.CS_OK:
                     raise RuntimeError(f"M={M} {c.policy} {c.key}: device status {cs.cs_chain_status(plan)}")
                 if ref is not None:
+                    # both plans lie within 5e-3 of the exact chain (max-normalised),
+                    # so within 1e-2 of each other; more means a broken candidate
                     err = _rel(torch, Y, ref)
-                    if not err <= 5e-3:
+                    if not err <= 1e-2:
                         raise RuntimeError(f"M={M} {c.policy} {c.key}: output differs from the built-in plan's "
                                            f"by {err:.2e}")
                 return _time(torch, fwd), info

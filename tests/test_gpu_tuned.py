@@ -56,5 +56,6 @@ def test_tuned_plans_match_the_oracle(tuned_table, workload, M):
     Yref = _oracle_rows(inp, rows)
     for tuned, Y in outs.items():
         assert oracle.rel_err(Y[rows], Yref) <= TOL, tuned
-    # tiled differently, the same sums up to fp32 rounding order
-    assert oracle.rel_err(outs[0], outs[-1]) <= 2e-3
+    # tiled differently, the same sums up to fp32 rounding order and the
+    # rounding of the intermediate to the input type (one bf16 ulp is 2^-8)
+    assert oracle.rel_err(outs[0], outs[-1]) <= (2e-3 if inp.dtype == torch.float16 else 1e-2)
