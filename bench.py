@@ -204,15 +204,35 @@ def time_loop(fn, steps, warmup, stream, finish=None):
     return total, per
 
 
-def simple_time(fn, iters=100, warmup=20, repeats=3):
-    """Median over `repeats` of the mean ms per call of fn over `iters` back-to-back
-    calls (CUDA events on the current stream, after `warmup` calls); the median
-    keeps a momentary clock dip out of difference metrics such as the overhead."""
+def warm_up(fn, warm_ms=100.0, min_calls=3):
+    """Back-to-back calls of fn for at least warm_ms of device time.  Under the
+    power cap the SM clock follows the power drawn over the last tens of
+    milliseconds (measured: a fused chain timed right after the lighter
+    two-kernel control ran 4-6 % faster than the same plan timed after another
+    fused chain), so every timing starts from fn's own steady state."""
     import torch
     s = torch.cuda.current_stream()
-    for _ in range(warmup):
-        fn()
-    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n, spent = min_calls, 0.0
+    while True:
+        a.record(s)
+        for _ in range(n):
+            fn()
+        b.record(s)
+        torch.cuda.synchronize()
+        spent += a.elapsed_time(b)
+        if spent >= warm_ms:
+            return
+        n = min(2 * n, 4096)
+
+
+def simple_time(fn, iters=100, warm_ms=100.0, repeats=3):
+    """Median over `repeats` of the mean ms per call of fn over `iters` back-to-back
+    calls (CUDA events on the current stream, after warm_up); the median keeps a
+    momentary clock dip out of difference metrics such as the overhead."""
+    import torch
+    s = torch.cuda.current_stream()
+    warm_up(fn, warm_ms)
     runs = []
     for _ in range(repeats):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -225,13 +245,16 @@ def simple_time(fn, iters=100, warmup=20, repeats=3):
     return statistics.median(runs)
 
 
-def interleaved_times(fns, rounds=3):
+def interleaved_times(fns, rounds=5):
     """Median ms per call of each fn, timed in interleaved rounds (all of them
-    then see the same clock under the power cap)."""
-    runs = {name: [] for name in fns}
-    for _ in range(rounds):
-        for name, fn in fns.items():
-            runs[name].append(simple_time(fn, repeats=1))
+    then see the same drift of the clock under the power cap); round r starts
+    at the r-th fn, and each timing starts with its own warm_up."""
+    names = list(fns)
+    runs = {name: [] for name in names}
+    for r in range(rounds):
+        for i in range(len(names)):
+            name = names[(r + i) % len(names)]
+            runs[name].append(simple_time(fns[name], repeats=1))
     return {name: statistics.median(v) for name, v in runs.items()}
 
 
@@ -436,13 +459,13 @@ def main():
 
     # ---- headline timed region
     sampler = ClockSampler(local) if rank == 0 else None
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    barrier(ws)
     if sampler:
         sampler.start()
         time.sleep(0.3)
+    # the warm-up steps run right before the timed ones (no idle gap between
+    # them, in which the clock would rise above its level under load)
+    for _ in range(args.warmup):
+        step()
     torch.cuda.synchronize()
     barrier(ws)
     t_wall0 = time.monotonic()
@@ -575,11 +598,7 @@ def extras(cs, torch, inp, dev, Y, make_plan, plan, M, kind, peaks, stream):
              "stage1": lambda: cs.cs_chain_forward_stage(plan, 1, Y=Y, **dev),
              "cublas0": cub1,
              "cublas1": lambda: torch.mm(Hbuf, W2, out=Y)}
-    rounds = {name: [] for name in terms}
-    for _ in range(3):
-        for name, fn in terms.items():
-            rounds[name].append(simple_time(fn, repeats=1))
-    med = {name: statistics.median(v) for name, v in rounds.items()}
+    med = interleaved_times(terms)
     chain_ms = med["chain"]
     out["chain_ms"] = chain_ms
     solo = [med["stage0"], med["stage1"]]

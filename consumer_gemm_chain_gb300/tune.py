@@ -10,7 +10,8 @@ Per M: every candidate runs under TileSync (RowSync for the attention chain);
 the three fastest are timed again under every policy, including the
 two-kernel control (so that the control, too, runs its best tiles); the best
 candidate of each policy is re-timed against the built-in rules in
-interleaved rounds, and an entry is written per policy.  Each candidate's
+interleaved rounds, and an entry is written per policy: the candidate's
+choices if it wins by at least 2 %, else zeros (the built-in rules).  Each candidate's
 output is checked against the built-in plan's output before it is timed.
 Inputs are random device tensors of the shape (N(0, 0.02)); timing uses CUDA
 events on the current stream, after warm-up, with weights larger than L2.
@@ -35,6 +36,8 @@ PRESETS = {
 MLP_TILES = ((128, 128), (128, 256), (256, 256), (512, 256))
 ATTN_TILES = ((128, 128), (256, 256))
 POLICIES = ("tile", "row", "strided", "stream")
+ROUNDS = 5      # interleaved rounds of the final comparison
+MARGIN = 0.02   # a tuned choice must beat the built-in rules by 2 %
 
 
 def _inputs(torch, kind, M, H, F, dtype, dev, seed=0):
@@ -53,16 +56,24 @@ def _inputs(torch, kind, M, H, F, dtype, dev, seed=0):
     return t
 
 
-def _time(torch, fn, target_ms=12.0, warmup=3, repeats=1):
+def _time(torch, fn, target_ms=12.0, warm_ms=60.0, repeats=1):
+    """Mean us per call over about target_ms of back-to-back calls, after at
+    least warm_ms of calls: under the power cap the SM clock follows the power
+    drawn over the last tens of milliseconds, so the timing of a candidate must
+    not start in the clock its predecessor left behind."""
     s = torch.cuda.current_stream()
-    for _ in range(warmup):
-        fn()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(s)
-    fn()
-    b.record(s)
-    torch.cuda.synchronize()
-    iters = max(5, min(400, int(target_ms / max(a.elapsed_time(b), 1e-3))))
+    n, spent, calls = 3, 0.0, 0
+    while spent < warm_ms:
+        a.record(s)
+        for _ in range(n):
+            fn()
+        b.record(s)
+        torch.cuda.synchronize()
+        spent += a.elapsed_time(b)
+        calls += n
+        n = min(2 * n, 4096)
+    iters = max(5, min(400, int(target_ms / max(spent / calls, 1e-3))))
     runs = []
     for _ in range(repeats):
         a.record(s)
@@ -157,28 +168,30 @@ def tune_shape(torch, kind, H, F, dtype, heads, Ms, log=print):
                 us = first[key] if pol == base else run(Candidate(kind, shape, pol, *key))[0]
                 if pol not in best or us < best[pol][1]:
                     best[pol] = (key, us)
-        # 3: each policy's best against the built-in rules, interleaved rounds
+        # 3: each policy's best against the built-in rules, interleaved rounds;
+        # a candidate replaces the built-in rules only when it wins by MARGIN
+        # (an entry of zeros keeps them: the timings of one configuration
+        # spread by a few per cent under the power cap)
         finals = {pol: Candidate(kind, shape, pol, *best[pol][0]) for pol in POLICIES}
         builtin = {pol: Candidate(kind, shape, pol) for pol in POLICIES}
-        times, builtin_key = {}, {}
-        for _ in range(3):
-            for pol in POLICIES:
-                for name, c in (("tuned", finals[pol]), ("builtin", builtin[pol])):
-                    us, info = run(c)
-                    times.setdefault((pol, name), []).append(us)
-                    if name == "builtin":
-                        # the built-in tiles, with the built-in (auto) split rule
-                        builtin_key[pol] = (info["tile_m"], info["tile_n"][info["stages"] - 1], 0)
+        times = {}
+        order = [(pol, name, c) for pol in POLICIES for name, c in (("tuned", finals[pol]), ("builtin", builtin[pol]))]
+        for r in range(ROUNDS):
+            for i in range(len(order)):  # each round starts one place later
+                pol, name, c = order[(r + i) % len(order)]
+                times.setdefault((pol, name), []).append(run(c)[0])
         for pol in POLICIES:
             us = statistics.median(times[(pol, "tuned")])
             us_auto = statistics.median(times[(pol, "builtin")])
-            tm, tn, sp = finals[pol].key if us < us_auto else builtin_key[pol]
-            us = min(us, us_auto)
+            if us < (1.0 - MARGIN) * us_auto:
+                tm, tn, sp = finals[pol].key
+            else:
+                tm, tn, sp, us = 0, 0, 0, us_auto
             entries.append({"kind": kind, "dtype": dtype, "H": H, "F": F, "M": M, "sms": sms, "layout": "nk",
                             "policy": pol, "tile_m": tm, "tile_n": tn, "split_k": sp, "group_m": 0,
                             "us": round(us, 2), "builtin_us": round(us_auto, 2)})
-            log(f"{kind} M={M:5d} {pol:8s} tile {tm}x{tn} split {sp:2d}: {us:8.1f} us "
-                f"(built-in rules {us_auto:8.1f} us)")
+            choice = f"tile {tm}x{tn} split {sp:2d}" if tm else "built-in rules    "
+            log(f"{kind} M={M:5d} {pol:8s} {choice}: {us:8.1f} us (built-in rules {us_auto:8.1f} us)")
         del t, Y, ref
         torch.cuda.empty_cache()
     return entries
