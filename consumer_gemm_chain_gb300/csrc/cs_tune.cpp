@@ -123,10 +123,10 @@ class JReader {
       if (p_ >= e_ || !isdigit(static_cast<unsigned char>(*p_))) return error("bad exponent");
       while (p_ < e_ && isdigit(static_cast<unsigned char>(*p_))) ++p_;
     }
+    // underflow (a subnormal or zero result) is a valid reading; overflow is not
     const std::string text(s, p_);
-    errno = 0;
     d = strtod(text.c_str(), nullptr);
-    if (errno == ERANGE || !std::isfinite(d)) return error("number out of range");
+    if (!std::isfinite(d)) return error("number out of range");
     return true;
   }
   bool value(JVal& v, int depth) {

@@ -160,6 +160,16 @@ def test_reader_accepts_json_details(cs, table):
     assert n == 1
 
 
+def test_number_edges(cs, table, tmp_path):
+    # an underflowing number is read (as a subnormal or zero), an overflowing one refused
+    assert table([dict(E(64), us=1e-320, extra=2.2e-311)]) == 1
+    bad = tmp_path / "big.json"
+    bad.write_text('{"format": "cs_chain_tuning", "version": 1, "entries": [], "x": 1e400}')
+    with pytest.raises(cs.CSError) as err:
+        cs.cs_tune_load(str(bad))
+    assert "number out of range" in str(err.value)
+
+
 def test_missing_file(cs, tmp_path):
     with pytest.raises(cs.CSError) as err:
         cs.cs_tune_load(str(tmp_path / "nope.json"))
