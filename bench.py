@@ -43,14 +43,40 @@ def load_peaks():
     return dict(PEAKS_FALLBACK), "fallback"
 
 
+def strip_comments(src: str) -> str:
+    """C/C++ source without its comments and with runs of whitespace collapsed
+    (string and character literals kept as written)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            out.append(" ")
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_sha():
-    """sha256[:16] of the kernel sources; DRAM-traffic counters are reported only
-    while the sources still match the ones they were taken with."""
+    """sha256[:16] of the kernel sources (device code and the host code that
+    plans and launches it) without comments; DRAM-traffic counters are reported
+    only while the code still matches the code they were taken with."""
     import hashlib
     h = hashlib.sha256()
     for f in ("cs_kernel.cuh", "cs_ptx.cuh", "cs_chain.cu"):
-        with open(os.path.join(ROOT, "consumer_gemm_chain_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "consumer_gemm_chain_gb300", "csrc", f), encoding="utf-8") as fh:
+            h.update(strip_comments(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

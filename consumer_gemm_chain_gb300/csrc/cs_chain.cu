@@ -324,11 +324,12 @@ Geometry geometry(const cs_chain_desc* d, int num_sms) {
     g.kps[s] = cdiv(g.k_iters[s], sp);
     g.splits[s] = cdiv(g.k_iters[s], g.kps[s]);  // no empty split
   }
-  // at most 1024 rows per group; with 256-row pair tiles also at least two
-  // groups, so that the lag lets the consumers of one group overlap the next
-  // (measured: M=1024 pairs 0.61 -> 0.67 of peak; single-SM tiles prefer one
-  // group); 512-row tiles: one group up to 1024 rows, else groups of 1024
-  // (measured at GPT-3 M=1024: 209 us in one group, 225 us in two)
+  // group_m counts tile rows.  At most 1024 rows per group; with 256-row pair
+  // tiles also at least two groups, so that the lag lets the consumers of one
+  // group overlap the next (measured: M=1024 pairs 0.61 -> 0.67 of peak;
+  // single-SM tiles prefer one group); 512-row tiles: groups of one tile row
+  // up to M = 1024, else of two (1024 rows) (measured at GPT-3 M=1024: 209 us
+  // with two 512-row groups, 225 us with one group of 1024 rows)
   g.group_m = d->group_m > 0 ? d->group_m
              : g.cl == 4   ? (g.m_tiles <= 2 ? 1 : 2)
              : g.cg == 2   ? std::max(1, std::min(4, g.m_tiles / 2))
