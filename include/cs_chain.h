@@ -120,12 +120,18 @@ typedef struct cs_chain_desc {
   int tile_m;          /* rows per GEMM tile: 128 (one SM), 256 (a 2-SM cluster
                           sharing one tcgen05 MMA) or 512 (two such pairs in a 4-CTA
                           cluster that fetch every weight box once and multicast it
-                          to both pairs); 256 and 512 need tile_n = 256 and the GeLU
-                          MLP.  0 = auto (512 where it adds no padding rows over 256,
-                          from M = 512).  The attention chain runs 128 (with
-                          tile_n 128) or 256 (with tile_n 256: attention units of
-                          two query blocks on a CTA pair); auto 256 from M = 512.
-                          Semaphores stay per 128-row block.                        */
+                          to both pairs).  256 and 512 run 256-wide tiles: tile_n =
+                          128 is refused, and with tile_n = 0 they fall back to 128
+                          rows where the automatic tile_n is 128.  SwiGLU pairs hold
+                          the gate rows of B on one CTA and the up rows on the other.
+                          0 = auto: MLPs take 512 from four 128-row blocks (M > 384;
+                          GeLU only where it adds no padding rows over 256), else
+                          256 (with 256-wide tiles) for exactly two
+                          128-row blocks or from eight, else 128.
+                          The attention chain runs 128 (with tile_n 128) or 256 (with
+                          tile_n 256: attention units of two query blocks on a CTA
+                          pair); auto 256 from four 128-row blocks.  Semaphores stay
+                          per 128-row block.                                        */
   int split_k;         /* K-splits per GEMM tile: 0 = auto (split when a stage has
                           fewer tiles than the grid, small M), 1 = never, 2..15 = that
                           many for every GEMM stage.  Splits write fp32 partial tiles
