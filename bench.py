@@ -114,6 +114,9 @@ def parse():
                     help="tuning table for the plans' auto fields: 'default' (the package's table, when "
                          "present), 'none' (built-in rules only) or a path")
     ap.add_argument("--quick", action="store_true", help="headline kernel only (profiling runs)")
+    ap.add_argument("--solo-vs-cublas", type=int, default=None, metavar="STAGE",
+                    help="profiling aid: launch stage STAGE of the chain alone once, then the cuBLAS GEMM "
+                         "of the same shape (via torch) once, and exit; no other kernel runs")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU-oracle sample time")
     return ap.parse_args()
@@ -475,6 +478,9 @@ def main():
     plan = make_plan(args.policy)
     plan_info = cs.cs_chain_query(plan)
     stream = torch.cuda.current_stream()
+    if args.solo_vs_cublas is not None:
+        solo_vs_cublas(cs, torch, plan, plan_info, dev, Y, inp, lay, args.solo_vs_cublas)
+        return
 
     def step():
         cs.cs_mlp_forward(plan, Y=Y, **dev)
@@ -578,6 +584,28 @@ def main():
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def solo_vs_cublas(cs, torch, plan, info, dev, Y, inp, lay, stage):
+    """One launch of an MLP chain's stage alone and one of cuBLAS's GEMM of that
+    stage's shape (stage 0 as addmm + GeLU), for an ncu capture of both kernels.
+    The inputs are copied from the host, so no other kernel runs before them."""
+    import torch.nn.functional as Fn
+    if inp.kind != "gelu" or stage not in (0, 1):
+        raise SystemExit("--solo-vs-cublas: stage 0 or 1 of a GeLU MLP workload")
+    cs.cs_chain_forward_stage(plan, stage, Y=Y, **dev)
+    t = (lambda w: w) if lay == "kn" else (lambda w: w.t())
+    if stage == 0:
+        Fn.gelu(torch.addmm(dev["b1"], dev["X"], t(dev["W1"])), approximate="tanh")
+    else:
+        Hbuf = torch.empty(inp.M, inp.F, dtype=inp.dtype, device=Y.device)
+        torch.mm(Hbuf, t(dev["W2"]), out=Y)
+    torch.cuda.synchronize()
+    st = cs.cs_chain_status(plan)
+    print(json.dumps({"solo_vs_cublas": stage, "M": inp.M, "tile_m": info["tile_m"], "tile_n": info["tile_n"][:2],
+                      "status": cs.STATUS_NAMES.get(st)}))
+    if st != cs.CS_OK:
+        raise SystemExit(1)
 
 
 def extras(cs, torch, inp, dev, Y, make_plan, plan, M, kind, peaks, stream):
