@@ -124,23 +124,28 @@ def parse():
 
 # ------------------------------------------------------------------ workload arithmetic
 def chain_flops(kind, M, H, F):
+    """Algorithmic flops of one chain forward (a multiply-add counts 2)."""
     if kind == "gelu":
         return 4.0 * M * H * F
     if kind == "swiglu":
         return 6.0 * M * H * F
+    if kind == "attn":
+        # QKV projection, Q K^T and P V over the causal half (key j <= query i),
+        # output projection; F = heads x head_dim
+        return 2.0 * M * H * 3 * F + 2.0 * M * (M + 1) * F + 2.0 * M * F * H
     raise ValueError(kind)
 
 
 def chain_bytes(kind, M, H, F, esz=2):
     """Algorithmic HBM bytes of one chain forward: weights once, X, Y, bias, and
-    the intermediate written once and read once."""
+    every intermediate (H; for attention QKV and O) written once and read once."""
     if kind == "gelu":
-        w = 2 * H * F
-        b = F
-    else:
-        w = 3 * H * F
-        b = 0
-    return esz * (w + b + 2 * M * H + 2 * M * F)
+        return esz * (2 * H * F + F + 2 * M * H + 2 * M * F)
+    if kind == "swiglu":
+        return esz * (3 * H * F + 2 * M * H + 2 * M * F)
+    if kind == "attn":
+        return esz * (4 * H * F + 2 * M * H + 2 * M * 3 * F + 2 * M * F)
+    raise ValueError(kind)
 
 
 # ------------------------------------------------------------------ clocks
@@ -760,9 +765,8 @@ def other_configs(cs, torch, peaks, lay):
                 fns[key] = (lambda p=p: cs.cs_attn_chain_forward(p, Xm, d["Wqkv"], d["Wo"], Ym))
             for key, ms in interleaved_times(fns).items():
                 rec[f"{key}_us"] = ms * 1e3
-        F3 = 3 * inp.F
-        fl = 2.0 * m * inp.H * F3 + 2.0 * m * inp.F * inp.H + 2.0 * m * (m + 1) * inp.F
-        by = 2 * (inp.H * F3 + inp.F * inp.H + 2 * m * inp.H + 2 * m * F3 + 2 * m * inp.F)
+        fl = chain_flops("attn", m, inp.H, inp.F)
+        by = chain_bytes("attn", m, inp.H, inp.F)
         rec["tflops"] = fl / (rec["row_us"] * 1e-6) / 1e12
         rec["roofline_frac"], rec["bound"] = _roof_frac(fl, by, rec["row_us"], peaks)
         rec["beats_control"] = rec["row_us"] < rec["stream_us"]

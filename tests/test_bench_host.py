@@ -1,0 +1,76 @@
+"""The bench's own arithmetic and timing order, on the host: the algorithmic
+flops and bytes behind every roofline fraction, the interleaving of timings,
+and the comment-insensitive source hash that gates the recorded DRAM traffic."""
+from __future__ import annotations
+
+import pytest
+
+import bench
+
+
+def test_flops_per_row_and_per_chain():
+    # GPT-3 MLP shard: 4 H F flops per row = 302 MFLOP; 618 GFLOP at M = 2048
+    assert bench.chain_flops("gelu", 1, 12288, 6144) == pytest.approx(302.0e6, rel=1e-3)
+    assert bench.chain_flops("gelu", 2048, 12288, 6144) == pytest.approx(618.5e9, rel=1e-3)
+    # LLaMA SwiGLU shard: gate, up and down projections, 135 MFLOP per row
+    assert bench.chain_flops("swiglu", 1, 8192, 2752) == pytest.approx(135.3e6, rel=1e-3)
+    # stress chain: 4 M 8192^2
+    assert bench.chain_flops("gelu", 1536, 8192, 8192) == 4.0 * 1536 * 8192 ** 2
+
+
+def test_attention_flops_count_the_causal_half():
+    M, H, F = 7, 12288, 1536
+    proj = 2.0 * M * H * 3 * F + 2.0 * M * F * H
+    # Q K^T and P V: 2 * head_dim flops per (query, key <= query) pair and head, twice
+    pairs = sum(i + 1 for i in range(M))
+    assert bench.chain_flops("attn", M, H, F) == pytest.approx(proj + 2 * 2 * pairs * F)
+
+
+def test_weight_bytes_of_the_workloads():
+    # weights once: GPT-3 302 MB, LLaMA 135 MB, attention 151 MB, stress 268 MB
+    w = lambda kind, H, F: bench.chain_bytes(kind, 0, H, F)  # noqa: E731
+    assert w("gelu", 12288, 6144) == pytest.approx(302e6, rel=1e-3)
+    assert w("swiglu", 8192, 2752) == pytest.approx(135.3e6, rel=1e-3)
+    assert w("attn", 12288, 1536) == pytest.approx(151e6, rel=1e-2)
+    assert w("gelu", 8192, 8192) == pytest.approx(268.5e6, rel=1e-3)
+    # per row: X read and Y written (2 H), the intermediate written and read (2 F)
+    assert bench.chain_bytes("gelu", 1, 12288, 6144) - w("gelu", 12288, 6144) == 2 * (2 * 12288 + 2 * 6144)
+    assert bench.chain_bytes("attn", 1, 12288, 1536) - w("attn", 12288, 1536) == 2 * (2 * 12288 + 8 * 1536)
+    with pytest.raises(ValueError):
+        bench.chain_bytes("conv", 1, 8, 8)
+
+
+def test_interleaved_rounds_put_every_fn_in_every_place(monkeypatch):
+    order = []
+    monkeypatch.setattr(bench, "simple_time", lambda fn, repeats=1: (order.append(fn()), 1.0)[1])
+    fns = {c: (lambda c=c: c) for c in "abcd"}
+    med = bench.interleaved_times(fns, rounds=4)
+    assert med == {c: 1.0 for c in "abcd"}
+    rounds = [order[i:i + 4] for i in range(0, 16, 4)]
+    assert rounds == [list("abcd"), list("bcda"), list("cdab"), list("dabc")]
+    for pos in range(4):
+        assert sorted(r[pos] for r in rounds) == list("abcd")
+
+
+@pytest.mark.parametrize("src,want", [
+    ("int a; // note\nint b;", "int a; int b;"),
+    ("int a; /* one\n two */ int b;", "int a; int b;"),
+    ('const char* s = "// not a comment";', 'const char* s = "// not a comment";'),
+    ("char c = '/'; char d = '*'; // x", "char c = '/'; char d = '*';"),
+    ('const char* e = "a\\"/*b";  int x;', 'const char* e = "a\\"/*b"; int x;'),
+])
+def test_strip_comments(src, want):
+    assert bench.strip_comments(src) == want
+
+
+def test_kernel_sha_ignores_comments_only(tmp_path, monkeypatch):
+    d = tmp_path / "consumer_gemm_chain_gb300" / "csrc"
+    d.mkdir(parents=True)
+    for f in ("cs_kernel.cuh", "cs_ptx.cuh", "cs_chain.cu"):
+        (d / f).write_text("int x = 1;\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    a = bench.kernel_sha()
+    (d / "cs_chain.cu").write_text("// a comment\nint   x = 1; /* another */\n")
+    assert bench.kernel_sha() == a
+    (d / "cs_chain.cu").write_text("int x = 2;\n")
+    assert bench.kernel_sha() != a
