@@ -69,27 +69,44 @@ def strip_comments(src: str) -> str:
 
 
 def kernel_sha():
-    """sha256[:16] of the kernel sources (device code and the host code that
-    plans and launches it) without comments; DRAM-traffic counters are reported
-    only while the code still matches the code they were taken with."""
+    """sha256[:16] of what fixes the kernel's memory traffic apart from the
+    schedule: the device code (comments removed) and the kernel configurations
+    the host instantiates (ring depths and stage sizes)."""
     import hashlib
+    import re
     h = hashlib.sha256()
-    for f in ("cs_kernel.cuh", "cs_ptx.cuh", "cs_chain.cu"):
-        with open(os.path.join(ROOT, "consumer_gemm_chain_gb300", "csrc", f), encoding="utf-8") as fh:
+    csrc = os.path.join(ROOT, "consumer_gemm_chain_gb300", "csrc")
+    for f in ("cs_kernel.cuh", "cs_ptx.cuh"):
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
             h.update(strip_comments(fh.read()).encode())
+    with open(os.path.join(csrc, "cs_chain.cu"), encoding="utf-8") as fh:
+        for m in re.finditer(r"constexpr int NS_\w+ = [^;]*;", strip_comments(fh.read())):
+            h.update(m.group(0).encode())
     return h.hexdigest()[:16]
 
 
-def measured_traffic(key):
+def schedule_sha(cs, desc, num_sms):
+    """sha256[:16] of the dispatch order a plan of `desc` runs on num_sms SMs
+    (tiles, K-splits, groups and their order: the rest of what fixes traffic)."""
+    import hashlib
+    import struct
+    units = cs.cs_schedule_build(desc, num_sms)
+    return hashlib.sha256(struct.pack(f"<{len(units)}I", *units)).hexdigest()[:16]
+
+
+def measured_traffic(key, sched_sha):
+    """DRAM bytes per launch recorded by ncu for this workload, while the kernel
+    and the plan's schedule are still the ones the counters were taken with."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
     except (OSError, ValueError):
         return None
-    if d.get("kernel_sha") != kernel_sha():
+    rec = d.get("records", {}).get(key)
+    if d.get("kernel_sha") != kernel_sha() or not rec or rec.get("schedule_sha") != sched_sha:
         return None
-    return d.get(key)
+    return rec.get("bytes_per_launch")
 
 
 def parse():
@@ -473,11 +490,12 @@ def main():
         dev.update(Wg=w(inp.Wg), Wu=w(inp.Wu), W2=w(inp.W2))
     Y = torch.empty_like(X)
 
-    def make_plan(policy, MM=M, pdl=None, tuned=0):
+    def make_plan(policy, MM=M, pdl=None, tuned=0, out_release=0):
         d = cs.cs_chain_desc_init(kind=kind, M=MM, H=inp.H, F=inp.F, dtype=inp.dtype, policy=policy,
                                   weight_layout=lay, lag=args.lag, tile_n=args.tile_n, group_m=args.group_m,
                                   tile_m=args.tile_m, split_k=args.split_k, prefetch=args.prefetch,
-                                  raster=args.raster, pdl=args.pdl if pdl is None else pdl, tuned=tuned)
+                                  raster=args.raster, pdl=args.pdl if pdl is None else pdl, tuned=tuned,
+                                  out_release=out_release)
         return cs.cs_chain_plan(d)
 
     plan = make_plan(args.policy)
@@ -532,7 +550,8 @@ def main():
         gbs = nbytes / (ms_launch * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak}
     traffic_key = f"{args.workload}_M{M}_{args.policy}_{lay}"
-    roof.update({"traffic": measured_traffic(traffic_key), "peak_source": f"{peak_src} ({'sustained' if sustained else 'burst'})",
+    roof.update({"traffic": measured_traffic(traffic_key, schedule_sha(cs, plan.desc, plan_info["num_sms"])),
+                 "peak_source": f"{peak_src} ({'sustained' if sustained else 'burst'})",
                  "kernel": ("cs_chain_kernel<6,32768,2,0,4> (4-CTA clusters)" if plan_info["tile_m"] == 512 else
                             "cs_chain_kernel<6,32768,2>" if plan_info["tile_m"] == 256 else
                             "cs_chain_kernel<4,49152,1>" if (kind == "swiglu" or 256 in plan_info["tile_n"])
@@ -613,6 +632,52 @@ def solo_vs_cublas(cs, torch, plan, info, dev, Y, inp, lay, stage):
         raise SystemExit(1)
 
 
+def rs_standin(cs, torch, make_plan, Y, dev, M, chunks=8):
+    """Single-GPU stand-in for a GEMM + reduce-scatter fusion (Flux summary): the
+    chain with its output released per 128-row block (desc.out_release), timed
+    against the plain chain, and the per-unit timeline of one traced forward:
+    when each of `chunks` row chunks of Y (one per destination rank) is complete,
+    as a fraction of the kernel's span from the first unit claimed to the last
+    tile stored.  A chunk-wise collective could send chunk r from then on."""
+    fwd = lambda p: cs.cs_mlp_forward(p, Y=Y, **dev)  # noqa: E731
+    with make_plan("tile") as p0, make_plan("tile", out_release=1) as p1:
+        t = interleaved_times({"plain": lambda: fwd(p0), "out_release": lambda: fwd(p1)})
+        cs.cs_chain_debug_trace(p1, True)
+        fwd(p1)
+        torch.cuda.synchronize()
+        recs = cs.cs_chain_debug_read_trace(p1)
+        q = cs.cs_chain_query(p1)
+        cs.cs_chain_debug_trace(p1, False)
+        st = cs.cs_chain_status(p1)
+    if st != cs.CS_OK:
+        return {"error": f"device status {cs.STATUS_NAMES.get(st)}"}
+    rec = chunk_ready(recs, q["stages"] - 1, q["tile_m"], M, chunks, cs.decode_unit)
+    rec.update({"chain_ms": t["plain"], "chain_out_release_ms": t["out_release"],
+                "release_cost_frac": t["out_release"] / t["plain"] - 1.0})
+    return rec
+
+
+def chunk_ready(recs, last, tile_m, M, chunks, decode):
+    """From trace records (8 integers: unit | index << 32, SM, then ns at claim,
+    ..., epilogue done): the time each of `chunks` equal row chunks of the output
+    is complete (its last tile of the last stage stored), as a fraction of the
+    span from the first claim to the last epilogue."""
+    ready = {}
+    for r in recs:
+        stage, m_tile, _, _ = decode(r[0] & 0xFFFFFFFF)
+        if stage == last and r[7]:
+            ready[m_tile] = max(ready.get(m_tile, 0), r[7])
+    start = min(r[2] for r in recs if r[2])
+    end = max(r[7] for r in recs if r[7])
+    frac = []
+    for c in range(chunks):
+        lo, hi = c * M // chunks, (c + 1) * M // chunks
+        tiles = range(lo // tile_m, (hi - 1) // tile_m + 1) if hi > lo else []
+        frac.append(max(((ready[m] - start) / (end - start) for m in tiles), default=0.0))
+    return {"chunks": chunks, "chunk_ready_frac": [round(f, 3) for f in frac],
+            "overlap_window_frac": sum(1.0 - f for f in frac) / chunks, "kernel_span_us": (end - start) / 1e3}
+
+
 def extras(cs, torch, inp, dev, Y, make_plan, plan, M, kind, peaks, stream):
     """Control, graph control, solo stages, cuBLAS solo GEMMs, sync overhead, M sweep."""
     import torch.nn.functional as Fn
@@ -669,6 +734,10 @@ def extras(cs, torch, inp, dev, Y, make_plan, plan, M, kind, peaks, stream):
     out["sync_overhead_ms"] = chain_ms - sum(best)
     out["sync_overhead_frac"] = (chain_ms - sum(best)) / chain_ms
     out["beats_control"] = chain_ms < out["stream_ms"]
+    try:
+        out["reduce_scatter_standin"] = rs_standin(cs, torch, make_plan, Y, dev, M)
+    except Exception as e:  # a side measurement that fails must not cost the bench line
+        out["reduce_scatter_standin"] = {"error": repr(e)[:300]}
     # sweep over M (first M rows of the same draw)
     sweep = []
     tc, hbm = peaks["bf16_tflops"], peaks["hbm_gbs"]

@@ -55,7 +55,7 @@ class cs_chain_desc(ctypes.Structure):
                 ("num_sms", ctypes.c_int), ("lag", ctypes.c_int), ("group_m", ctypes.c_int),
                 ("tile_n", ctypes.c_int), ("tile_m", ctypes.c_int), ("split_k", ctypes.c_int),
                 ("prefetch", ctypes.c_int), ("raster", ctypes.c_int), ("pdl", ctypes.c_int),
-                ("tuned", ctypes.c_int), ("spin_timeout_ns", ctypes.c_ulonglong)]
+                ("tuned", ctypes.c_int), ("out_release", ctypes.c_int), ("spin_timeout_ns", ctypes.c_ulonglong)]
 
 
 class cs_mlp_args(ctypes.Structure):
@@ -75,7 +75,8 @@ class cs_chain_info(ctypes.Structure):
                 ("split_k", ctypes.c_int * 3),
                 ("stride", ctypes.c_int),
                 ("intermediate", ctypes.c_void_p * 2), ("sem_words", ctypes.c_size_t * 2),
-                ("policy", ctypes.c_int), ("tuned_entry", ctypes.c_int)]
+                ("policy", ctypes.c_int), ("tuned_entry", ctypes.c_int),
+                ("out_tile_sems", ctypes.c_void_p), ("out_row_sems", ctypes.c_void_p), ("out_sem_words", ctypes.c_size_t)]
 
 
 def _load() -> ctypes.CDLL:
@@ -323,7 +324,8 @@ def cs_chain_query(plan: Plan) -> dict:
             "sched_units": list(i.sched_units), "split_k": list(i.split_k),
             "stride": i.stride, "intermediate": [i.intermediate[0], i.intermediate[1]],
             "sem_words": [i.sem_words[0], i.sem_words[1]], "policy": POLICY_NAMES.get(i.policy, i.policy),
-            "tuned_entry": i.tuned_entry}
+            "tuned_entry": i.tuned_entry, "out_tile_sems": i.out_tile_sems, "out_row_sems": i.out_row_sems,
+            "out_sem_words": i.out_sem_words}
 
 
 def cs_schedule_build(desc: cs_chain_desc, num_sms: int) -> list[int]:
@@ -369,7 +371,8 @@ def decode_unit(u: int) -> tuple[int, int, int, int]:
 def cs_chain_debug_read_sems(plan: Plan, boundary: int):
     """(tile semaphores as a [m_tiles, n_tiles] list of lists, row counters, epoch)."""
     q = cs_chain_query(plan)
-    words = q["sem_words"][boundary] + q["m_tiles"]
+    sem_words = q["out_sem_words"] if boundary == q["stages"] - 1 else q["sem_words"][boundary]
+    words = sem_words + q["m_tiles"]
     buf = (ctypes.c_uint32 * words)()
     ep = ctypes.c_uint32()
     _check(_lib.cs_chain_debug_read_sems(plan.handle, boundary, buf, words, ctypes.byref(ep)),
@@ -377,7 +380,7 @@ def cs_chain_debug_read_sems(plan: Plan, boundary: int):
     vals = list(buf)
     nt = q["n_tiles"][boundary]
     tiles = [vals[m * nt:(m + 1) * nt] for m in range(q["m_tiles"])]
-    rows = vals[q["sem_words"][boundary]:]
+    rows = vals[sem_words:]
     return tiles, rows, ep.value
 
 

@@ -106,8 +106,10 @@ struct cs_chain_s {
   int smem = 0;
   // device memory owned by the plan
   void* inter[2] = {nullptr, nullptr};
-  uint32_t* sems[2] = {nullptr, nullptr};
-  size_t sem_words[2] = {0, 0};
+  // tile semaphores then row counters of each boundary; sems[stages - 1] (the
+  // output, for desc.out_release) only when asked for
+  uint32_t* sems[3] = {nullptr, nullptr, nullptr};
+  size_t sem_words[3] = {0, 0, 0};
   size_t inter_bytes[2] = {0, 0};
   uint32_t* ctrl = nullptr;
   uint32_t* sched_fused = nullptr;
@@ -187,6 +189,7 @@ cs_status validate(const cs_chain_desc* d) {
   if (d->dtype != CS_F16 && d->dtype != CS_BF16) return fail(CS_ERR_INVALID_ARG, "bad dtype %d", d->dtype);
   if (d->policy < CS_SYNC_AUTO || d->policy > CS_SYNC_STREAM) return fail(CS_ERR_INVALID_ARG, "bad policy %d", d->policy);
   if (d->tuned < -1 || d->tuned > 0) return fail(CS_ERR_INVALID_ARG, "tuned=%d (0 or -1)", d->tuned);
+  if (d->out_release < 0 || d->out_release > 1) return fail(CS_ERR_INVALID_ARG, "out_release=%d (0 or 1)", d->out_release);
   if (d->weight_layout != CS_WEIGHTS_KN && d->weight_layout != CS_WEIGHTS_NK)
     return fail(CS_ERR_INVALID_ARG, "bad weight_layout %d", d->weight_layout);
   if (d->M < 1 || d->M > 128 * 4095) return fail(CS_ERR_INVALID_ARG, "M=%d out of range [1, %d]", d->M, 128 * 4095);
@@ -553,8 +556,9 @@ void fill_mlp_stages(const cs_chain_s* p, const cs_mlp_args* a, cs::KParams& kp)
   s1.dep_ntiles = p->n_tiles[0];
   s1.dep_bn = p->bn[0];
   s1.stride = p->stride;
-  s1.rel_tile = nullptr;
-  s1.rel_row = nullptr;
+  // the output's own semaphores when the plan releases Y (desc.out_release)
+  s1.rel_tile = p->sems[1];
+  s1.rel_row = p->sems[1] ? p->sems[1] + p->sem_words[1] : nullptr;
   s1.skip_unit = -1;
   fill_split(p, 0, s0);
   fill_split(p, 1, s1);
@@ -715,6 +719,8 @@ void fill_attn_stages(const cs_chain_s* p, cs::KParams& kp) {
   s2.dep_ntiles = p->n_tiles[1];
   s2.dep_bn = 128;
   s2.stride = p->stride;
+  s2.rel_tile = p->sems[2];
+  s2.rel_row = p->sems[2] ? p->sems[2] + p->sem_words[2] : nullptr;
   s2.skip_unit = -1;
   fill_split(p, 0, s0);
   fill_split(p, 1, s1);
@@ -793,6 +799,7 @@ cs_status cs_chain_desc_init(cs_chain_desc* d) {
   d->raster = 0;
   d->pdl = 0;
   d->tuned = 0;
+  d->out_release = 0;
   return CS_OK;
 }
 
@@ -870,7 +877,7 @@ cs_status cs_chain_plan(const cs_chain_desc* desc, cs_chain_t* out) {
   for (int b = 0; b < 2; ++b)
     if (p->inter_bytes[b] && cudaMalloc(&p->inter[b], p->inter_bytes[b]) != cudaSuccess)
       return bail(fail(CS_ERR_OOM, "cudaMalloc of the intermediate failed"));
-  for (int b = 0; b < g.stages - 1; ++b) {
+  for (int b = 0; b < g.stages - (desc->out_release ? 0 : 1); ++b) {
     p->sem_words[b] = static_cast<size_t>(g.m_blocks) * g.n_tiles[b];
     const size_t words = p->sem_words[b] + g.m_blocks;
     if (cudaMalloc(reinterpret_cast<void**>(&p->sems[b]), words * 4) != cudaSuccess)
@@ -1077,8 +1084,8 @@ cs_status cs_chain_status(cs_chain_t p) {
 cs_status cs_chain_reset(cs_chain_t p) {
   if (!p) return fail(CS_ERR_INVALID_ARG, "plan is NULL");
   CS_CUDA(cudaDeviceSynchronize());
-  for (int b = 0; b < p->stages - 1; ++b)
-    CS_CUDA(cudaMemset(p->sems[b], 0, (p->sem_words[b] + p->m_tiles) * 4));
+  for (int b = 0; b < 3; ++b)
+    if (p->sems[b]) CS_CUDA(cudaMemset(p->sems[b], 0, (p->sem_words[b] + p->m_tiles) * 4));
   CS_CUDA(cudaMemset(p->ctrl, 0, cs::CTRL_WORDS * 4));
   for (int st = 0; st < p->stages; ++st)
     if (p->split_ctr[st])
@@ -1115,6 +1122,10 @@ cs_status cs_chain_query(cs_chain_t p, cs_chain_info* info) {
   info->sem_words[1] = p->sem_words[1];
   info->policy = p->d.policy;
   info->tuned_entry = p->tuned_entry;
+  const int last = p->stages - 1;
+  info->out_tile_sems = p->sems[last];
+  info->out_row_sems = p->sems[last] ? p->sems[last] + p->sem_words[last] : nullptr;
+  info->out_sem_words = p->sems[last] ? p->sem_words[last] : 0;
   return CS_OK;
 }
 
@@ -1131,7 +1142,8 @@ cs_status cs_tune_match(const cs_chain_desc* desc, int num_sms, int* entry, cs_c
 
 cs_status cs_chain_debug_read_sems(cs_chain_t p, int boundary, uint32_t* host, size_t n, uint32_t* epoch) {
   if (!p || !host) return fail(CS_ERR_INVALID_ARG, "NULL argument");
-  if (boundary < 0 || boundary >= p->stages - 1) return fail(CS_ERR_INVALID_ARG, "boundary %d", boundary);
+  if (boundary < 0 || boundary >= p->stages || !p->sems[boundary])
+    return fail(CS_ERR_INVALID_ARG, "boundary %d has no semaphores", boundary);
   const size_t words = p->sem_words[boundary] + p->m_tiles;
   if (n < words) return fail(CS_ERR_INVALID_ARG, "need %zu words, got %zu", words, n);
   CS_CUDA(cudaMemcpy(host, p->sems[boundary], words * 4, cudaMemcpyDeviceToHost));
@@ -1237,6 +1249,7 @@ cs_status cs_mlp_forward_noalloc(const cs_chain_desc* desc, const cs_mlp_args* a
   cs_status s = validate(desc);
   if (s != CS_OK) return s;
   if (desc->kind == CS_CHAIN_ATTN) return fail(CS_ERR_UNSUPPORTED, "the allocation-free forward runs MLP chains only");
+  if (desc->out_release) return fail(CS_ERR_UNSUPPORTED, "the allocation-free forward has no output semaphores");
   int sms = 0;
   const int dev = device_sms(&sms);
   if (dev < 0) return fail(CS_ERR_CUDA, "no CUDA device available");

@@ -42,7 +42,7 @@
 extern "C" {
 #endif
 
-#define CS_ABI_VERSION 3
+#define CS_ABI_VERSION 4
 
 typedef struct cs_chain_s* cs_chain_t;
 
@@ -158,6 +158,16 @@ typedef struct cs_chain_desc {
                           chain shape, dtype, layout and grid size, and policy AUTO
                           is resolved from it; an entry whose choices do not fit the
                           desc is ignored.  -1 = never (built-in rules only).       */
+  int out_release;     /* 1: the last stage releases Y the way producers release the
+                          intermediate: once a tile of Y is stored, its tile
+                          semaphore and its 128-row block's counter are
+                          release-incremented (device pointers in cs_chain_info), so
+                          that a following consumer of Y -- a collective that sends
+                          blocks of rows as they complete, as in the Flux summary's
+                          GEMM + reduce-scatter fusion -- may acquire-read a block
+                          once its counter reaches epoch * (tiles per row block).
+                          Each Y tile then waits for its store to complete before
+                          the epilogue moves on.  0 = off.                          */
   unsigned long long spin_timeout_ns; /* per-wait limit of a consumer tile; 0 = 2 s */
 } cs_chain_desc;
 
@@ -264,6 +274,16 @@ typedef struct cs_chain_info {
   size_t sem_words[2];     /* length of each boundary's tile-semaphore array */
   int policy;              /* cs_policy the plan runs (AUTO resolved) */
   int tuned_entry;         /* index of the tuning-table entry applied, -1 = none */
+  /* desc.out_release: device uint32 arrays of the output Y (NULL otherwise).
+   * out_tile_sems[m_tiles * n_tiles[stages-1]] (128-row block-major) count the
+   * forwards that stored each Y tile; out_row_sems[m_tiles] count the Y tiles
+   * stored in each 128-row block, n_tiles[stages-1] per forward.  After the
+   * e-th forward (e = the epoch cs_chain_debug_read_sems reports), a block of
+   * rows is complete once its counter is >= e * n_tiles[stages-1]; the
+   * counters are zeroed by cs_chain_reset only. */
+  uint32_t* out_tile_sems;
+  uint32_t* out_row_sems;
+  size_t out_sem_words;    /* length of out_tile_sems */
 } cs_chain_info;
 
 cs_status cs_chain_query(cs_chain_t plan, cs_chain_info* info);
@@ -316,8 +336,9 @@ cs_status cs_tune_match(const cs_chain_desc* desc, int num_sms, int* entry, cs_c
 
 /* Testing aids. ------------------------------------------------------------ */
 
-/* Copy boundary b's tile semaphores (b = 0: stage0->stage1, b = 1: stage1->stage2)
- * to host[0..n), then the boundary's row counters after them (m_tiles words).
+/* Copy boundary b's tile semaphores (b = 0: stage0->stage1, b = 1: stage1->stage2;
+ * b = stages - 1: the output Y of a plan made with desc.out_release) to
+ * host[0..n), then the boundary's row counters after them (m_tiles words).
  * *epoch receives the number of completed forwards.  Blocking. */
 cs_status cs_chain_debug_read_sems(cs_chain_t plan, int boundary, uint32_t* host, size_t n,
                                    uint32_t* epoch);

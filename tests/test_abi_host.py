@@ -33,7 +33,7 @@ def test_every_declared_symbol_is_exported(cs):
     for n in names:
         assert hasattr(lib, n), f"{n} declared in cs_chain.h but not exported"
     assert set(cs.chain.EXPORTED) == set(names)
-    assert cs.cs_abi_version() == 3
+    assert cs.cs_abi_version() == 4
 
 
 def test_desc_defaults(cs):
@@ -46,7 +46,8 @@ def test_desc_defaults(cs):
                                          ("kind", 5), ("weight_layout", 3), ("lag", -2), ("num_sms", -1),
                                          ("split_k", 16), ("tile_n", 192), ("tile_m", 64), ("tile_m", 1024), ("M", 128 * 4096),
                                          ("raster", 3), ("prefetch", -2), ("pdl", 2), ("pdl", -2),
-                                         ("policy", -2), ("tuned", 1), ("tuned", -2)])
+                                         ("policy", -2), ("tuned", 1), ("tuned", -2), ("out_release", 2),
+                                         ("out_release", -1)])
 def test_invalid_descs_are_rejected_without_a_gpu(cs, field, value):
     d = cs.cs_chain_desc_init(M=64, H=256, F=1024)
     setattr(d, field, value)

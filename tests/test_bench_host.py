@@ -63,14 +63,48 @@ def test_strip_comments(src, want):
     assert bench.strip_comments(src) == want
 
 
-def test_kernel_sha_ignores_comments_only(tmp_path, monkeypatch):
+def test_kernel_sha_follows_device_code_and_ring_configurations(tmp_path, monkeypatch):
     d = tmp_path / "consumer_gemm_chain_gb300" / "csrc"
     d.mkdir(parents=True)
-    for f in ("cs_kernel.cuh", "cs_ptx.cuh", "cs_chain.cu"):
-        (d / f).write_text("int x = 1;\n")
+    (d / "cs_kernel.cuh").write_text("int x = 1;\n")
+    (d / "cs_ptx.cuh").write_text("int y = 1;\n")
+    (d / "cs_chain.cu").write_text("constexpr int NS_A = 6, SB_A = 32768;\nint host = 1;\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     a = bench.kernel_sha()
-    (d / "cs_chain.cu").write_text("// a comment\nint   x = 1; /* another */\n")
+    # comments, and host code other than the ring configurations, do not count
+    (d / "cs_kernel.cuh").write_text("// a comment\nint   x = 1; /* another */\n")
+    (d / "cs_chain.cu").write_text("constexpr int NS_A = 6, SB_A = 32768; // ring\nint host = 2;\n")
     assert bench.kernel_sha() == a
-    (d / "cs_chain.cu").write_text("int x = 2;\n")
+    # device code and ring depths do
+    (d / "cs_ptx.cuh").write_text("int y = 2;\n")
     assert bench.kernel_sha() != a
+    (d / "cs_ptx.cuh").write_text("int y = 1;\n")
+    assert bench.kernel_sha() == a
+    (d / "cs_chain.cu").write_text("constexpr int NS_A = 7, SB_A = 32768;\nint host = 2;\n")
+    assert bench.kernel_sha() != a
+
+
+def test_schedule_sha_follows_the_plans_tiles():
+    import consumer_gemm_chain_gb300 as cs
+    cs.cs_tune_clear()
+    d = cs.cs_chain_desc_init(kind="gelu", M=2048, H=12288, F=6144, weight_layout="nk")
+    a = bench.schedule_sha(cs, d, 152)
+    assert bench.schedule_sha(cs, d, 152) == a
+    d.tile_m, d.tile_n = 256, 256
+    assert bench.schedule_sha(cs, d, 152) != a
+
+
+def test_chunk_ready_from_a_timeline():
+    decode = lambda u: (u >> 30, (u >> 14) & 0xFFF, u & 0x3FFF, (u >> 26) & 0xF)  # noqa: E731
+    enc = lambda s, m, n: (s << 30) | (m << 14) | n  # noqa: E731
+    # 2 tile rows of 512 (M = 1024): producers claimed from 100 ns, done at 140; row 0's
+    # consumers done at 160, row 1's at 200
+    recs = [[enc(0, m, n), 0, 100 + n, 0, 0, 0, 0, 140] for m in (0, 1) for n in (0, 1)]
+    recs += [[enc(1, 0, n), 0, 140, 0, 0, 0, 0, 150 + 10 * n] for n in (0, 1)]
+    recs += [[enc(1, 1, n), 0, 160, 0, 0, 0, 0, 190 + 10 * n] for n in (0, 1)]
+    recs += [[enc(1, 1, 2), 0, 0, 0, 0, 0, 0, 0]]  # a record of a unit never reached
+    r = bench.chunk_ready(recs, 1, 512, 1024, 4, decode)
+    # chunks of 256 rows: the first two lie in tile row 0 (ready at 60), the others in row 1 (100)
+    assert r["chunk_ready_frac"] == [0.6, 0.6, 1.0, 1.0]
+    assert r["overlap_window_frac"] == pytest.approx(0.2)
+    assert r["kernel_span_us"] == pytest.approx(0.1)
