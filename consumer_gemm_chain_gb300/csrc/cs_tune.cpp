@@ -6,6 +6,7 @@
 // JSON, written by the package's tuner; this file reads them.
 #include <cctype>
 #include <cerrno>
+#include <charconv>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
@@ -13,6 +14,7 @@
 #include <limits>
 #include <mutex>
 #include <string>
+#include <system_error>
 #include <utility>
 #include <vector>
 
@@ -123,10 +125,19 @@ class JReader {
       if (p_ >= e_ || !isdigit(static_cast<unsigned char>(*p_))) return error("bad exponent");
       while (p_ < e_ && isdigit(static_cast<unsigned char>(*p_))) ++p_;
     }
-    // underflow (a subnormal or zero result) is a valid reading; overflow is not
-    const std::string text(s, p_);
-    d = strtod(text.c_str(), nullptr);
-    if (!std::isfinite(d)) return error("number out of range");
+    // std::from_chars reads the C format whatever the process's locale is (strtod
+    // would stop at the '.' under a locale with a decimal comma).  Underflow (a
+    // subnormal or zero result) is a valid reading; overflow is not.
+    const std::from_chars_result r = std::from_chars(s, p_, d);
+    if (r.ec == std::errc::result_out_of_range) {
+      const char* e = s;
+      while (e < p_ && *e != 'e' && *e != 'E') ++e;
+      const bool tiny = (e < p_ && e + 1 < p_ && e[1] == '-');
+      if (!tiny) return error("number out of range");
+      d = 0.0;
+      return true;
+    }
+    if (r.ec != std::errc() || r.ptr != p_ || !std::isfinite(d)) return error("number out of range");
     return true;
   }
   bool value(JVal& v, int depth) {
