@@ -6,7 +6,6 @@
 // JSON, written by the package's tuner; this file reads them.
 #include <cctype>
 #include <cerrno>
-#include <charconv>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
@@ -14,7 +13,6 @@
 #include <limits>
 #include <mutex>
 #include <string>
-#include <system_error>
 #include <utility>
 #include <vector>
 
@@ -125,19 +123,41 @@ class JReader {
       if (p_ >= e_ || !isdigit(static_cast<unsigned char>(*p_))) return error("bad exponent");
       while (p_ < e_ && isdigit(static_cast<unsigned char>(*p_))) ++p_;
     }
-    // std::from_chars reads the C format whatever the process's locale is (strtod
-    // would stop at the '.' under a locale with a decimal comma).  Underflow (a
-    // subnormal or zero result) is a valid reading; overflow is not.
-    const std::from_chars_result r = std::from_chars(s, p_, d);
-    if (r.ec == std::errc::result_out_of_range) {
-      const char* e = s;
-      while (e < p_ && *e != 'e' && *e != 'E') ++e;
-      const bool tiny = (e < p_ && e + 1 < p_ && e[1] == '-');
-      if (!tiny) return error("number out of range");
-      d = 0.0;
-      return true;
+    // The value, read by hand (strtod follows the process's locale and would stop
+    // at the '.' under one with a decimal comma): integers of up to 18 digits
+    // exactly, anything else as mantissa x 10^exponent in long double.
+    // Underflow reads as zero; overflow is refused.
+    const char* q = s;
+    const bool neg = *q == '-';
+    if (neg) ++q;
+    long double mant = 0.0L;
+    long exp10 = 0;
+    int kept = 0;  // significant digits taken into the mantissa
+    for (; q < p_ && isdigit(static_cast<unsigned char>(*q)); ++q) {
+      if (kept < 30) mant = mant * 10.0L + (*q - '0'), kept += (mant != 0.0L);
+      else ++exp10;
     }
-    if (r.ec != std::errc() || r.ptr != p_ || !std::isfinite(d)) return error("number out of range");
+    if (q < p_ && *q == '.')
+      for (++q; q < p_ && isdigit(static_cast<unsigned char>(*q)); ++q)
+        if (kept < 30) mant = mant * 10.0L + (*q - '0'), kept += (mant != 0.0L), --exp10;
+    if (q < p_ && (*q == 'e' || *q == 'E')) {
+      ++q;
+      const bool eneg = *q == '-';
+      if (*q == '+' || *q == '-') ++q;
+      long e = 0;
+      for (; q < p_ && isdigit(static_cast<unsigned char>(*q)); ++q)
+        if (e < 100000) e = e * 10 + (*q - '0');
+      exp10 += eneg ? -e : e;
+    }
+    if (mant == 0.0L || exp10 < -4000) {
+      d = 0.0;
+    } else {
+      if (exp10 > 4000) return error("number out of range");
+      const long double v = mant * std::pow(10.0L, static_cast<long double>(exp10));
+      if (!(v <= static_cast<long double>(std::numeric_limits<double>::max()))) return error("number out of range");
+      d = static_cast<double>(v);
+    }
+    if (neg) d = -d;
     return true;
   }
   bool value(JVal& v, int depth) {

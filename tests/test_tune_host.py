@@ -170,6 +170,21 @@ def test_number_edges(cs, table, tmp_path):
     assert "number out of range" in str(err.value)
 
 
+@pytest.mark.parametrize("text,ok", [("128", True), ("128.0", True), ("1.28e2", True), ("12.8e1", True),
+                                     ("128.5", False), ("1e2", False)])
+def test_integer_fields_in_any_json_number_form(cs, table, tmp_path, text, ok):
+    """Integer fields are read exactly whatever form the number takes (the reader
+    does not go through the C library's locale-dependent conversion)."""
+    path = tmp_path / "t.json"
+    path.write_text('{"format": "cs_chain_tuning", "version": 1, "entries": [' +
+                    json.dumps(E(64))[:-1].replace('"tile_m": 128', '"tile_m": ' + text) + '}]}')
+    if ok:
+        assert cs.cs_tune_load(str(path)) == 1
+    else:
+        with pytest.raises(cs.CSError):
+            cs.cs_tune_load(str(path))
+
+
 def test_missing_file(cs, tmp_path):
     with pytest.raises(cs.CSError) as err:
         cs.cs_tune_load(str(tmp_path / "nope.json"))
