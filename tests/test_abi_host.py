@@ -184,3 +184,21 @@ def test_pair_tiles_need_wide_gelu_tiles(cs):
     with pytest.raises(cs.CSError) as e:
         cs.cs_schedule_build(d, 148)
     assert e.value.status == cs.CS_ERR_UNSUPPORTED
+
+
+def test_the_abi_from_plain_c99(cs, tmp_path):
+    """tests/c/abi_host_check.c includes only include/cs_chain.h, compiles as
+    strict C99 and links the library: the boundary is a C ABI, usable without
+    Python (host-only entry points, no GPU)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    libdir = os.path.dirname(cs.chain.LIB_PATH)
+    exe = str(tmp_path / "abi_host_check")
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    os.path.join(ROOT, "tests", "c", "abi_host_check.c"), "-o", exe, "-L", libdir, "-lcs_chain",
+                    f"-Wl,-rpath,{libdir}"], check=True)
+    p = subprocess.run([exe, cs.chain.TUNE_TABLE], capture_output=True, text=True, timeout=60)
+    assert p.returncode == 0 and p.stdout.strip() == "ok", p.stderr
