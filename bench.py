@@ -224,28 +224,36 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ timing helpers
+def sampled_calls(steps, most=200):
+    """{call index: event-pair slot} for about `most` calls spread evenly over `steps`."""
+    every = max(1, steps // most)
+    return {i: k for k, i in enumerate(range(0, steps, every))}
+
+
 def time_loop(fn, steps, warmup, stream, finish=None):
     """Mean ms per call of fn over `steps` calls (after `warmup`), CUDA events on `stream`,
-    plus the mean of per-call event pairs (the kernel's average launch duration).
-    `finish` (if any) runs after the last call, before the end event (e.g. to make
-    `stream` wait for work queued on other streams)."""
+    plus the mean of per-call event pairs (the kernel's average launch duration) on up
+    to 200 calls spread evenly over the timed region (the clock under the power cap
+    drifts during it).  `finish` (if any) runs after the last call, before the end
+    event (e.g. to make `stream` wait for work queued on other streams)."""
     import torch
     for _ in range(warmup):
         fn()
     if finish is not None:
         finish()
     torch.cuda.synchronize()
-    n_pairs = min(steps, 200)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_pairs)]
+    slot = sampled_calls(steps)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in slot]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     start.record(stream)
     for i in range(steps):
-        if i < n_pairs:
-            ev[i][0].record(stream)
+        k = slot.get(i)
+        if k is not None:
+            ev[k][0].record(stream)
         fn()
-        if i < n_pairs:
-            ev[i][1].record(stream)
+        if k is not None:
+            ev[k][1].record(stream)
     if finish is not None:
         finish()
     end.record(stream)

@@ -108,3 +108,11 @@ def test_chunk_ready_from_a_timeline():
     assert r["chunk_ready_frac"] == [0.6, 0.6, 1.0, 1.0]
     assert r["overlap_window_frac"] == pytest.approx(0.2)
     assert r["kernel_span_us"] == pytest.approx(0.1)
+
+
+@pytest.mark.parametrize("steps", [1, 3, 200, 201, 2000, 4000])
+def test_launch_samples_spread_over_the_timed_region(steps):
+    slot = bench.sampled_calls(steps)
+    assert sorted(slot.values()) == list(range(len(slot)))
+    assert 0 in slot and len(slot) <= 201
+    assert max(slot) >= steps - max(1, steps // 200)  # the last calls are sampled too
