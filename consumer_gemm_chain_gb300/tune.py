@@ -5,6 +5,7 @@ M, and writes the fastest per (M, policy) as a tuning table that
 GPU and environment).
 
     python -m consumer_gemm_chain_gb300.tune --preset gpt3 [--M 1,16,...] [--out FILE] [--merge]
+    python -m consumer_gemm_chain_gb300.tune --shape gelu,8192,4096,bf16 --layout kn --M 64,512,4096
 
 Per M: every candidate runs under TileSync (RowSync for the attention chain);
 the three fastest are timed again under every policy, including the
@@ -40,19 +41,38 @@ ROUNDS = 5      # interleaved rounds of the final comparison
 MARGIN = 0.02   # a tuned choice must beat the built-in rules by 2 %
 
 
-def _inputs(torch, kind, M, H, F, dtype, dev, seed=0):
+def parse_shape(text):
+    """KIND,H,F,DTYPE[,HEADS] -> (kind, H, F, dtype, heads) of a chain to tune."""
+    parts = [p.strip() for p in text.split(",")]
+    if len(parts) not in (4, 5):
+        raise ValueError(f"--shape {text!r}: KIND,H,F,DTYPE[,HEADS]")
+    kind, H, F, dtype = parts[0], int(parts[1]), int(parts[2]), parts[3]
+    heads = int(parts[4]) if len(parts) == 5 else 0
+    if kind not in ("gelu", "swiglu", "attn") or dtype not in ("f16", "bf16"):
+        raise ValueError(f"--shape {text!r}: KIND is gelu, swiglu or attn; DTYPE f16 or bf16")
+    if H < 8 or F < 8 or H % 8 or F % 8:
+        raise ValueError(f"--shape {text!r}: H and F are positive multiples of 8")
+    if kind == "attn" and heads * 128 != F:
+        raise ValueError(f"--shape {text!r}: the attention chain needs HEADS with F = HEADS x 128")
+    return kind, H, F, dtype, heads
+
+
+def _inputs(torch, kind, M, H, F, dtype, dev, layout="nk", seed=0):
     g = torch.Generator(device=dev).manual_seed(seed)
 
     def r(*shape):
         return (torch.randn(*shape, generator=g, device=dev, dtype=torch.float32) * 0.02).to(dtype)
 
+    def w(K, N):  # a weight of math shape [K, N] in the storage layout
+        return r(N, K) if layout == "nk" else r(K, N)
+
     t = {"X": r(M, H)}
     if kind == "gelu":
-        t.update(W1=r(F, H), b1=r(F), W2=r(H, F))
+        t.update(W1=w(H, F), b1=r(F), W2=w(F, H))
     elif kind == "swiglu":
-        t.update(Wg=r(F, H), Wu=r(F, H), W2=r(H, F))
+        t.update(Wg=w(H, F), Wu=w(H, F), W2=w(F, H))
     else:
-        t.update(Wqkv=r(3 * F, H), Wo=r(H, F))
+        t.update(Wqkv=w(H, 3 * F), Wo=w(F, H))
     return t
 
 
@@ -90,7 +110,7 @@ class Candidate:
         self.key = (tile_m, tile_n, split_k)
         self.policy = policy
         self.desc = cs.cs_chain_desc_init(kind=kind, M=shape["M"], H=shape["H"], F=shape["F"],
-                                          dtype=shape["dtype"], policy=policy, weight_layout="nk",
+                                          dtype=shape["dtype"], policy=policy, weight_layout=shape["layout"],
                                           heads=shape["heads"] or 12, tile_m=tile_m, tile_n=tile_n,
                                           split_k=split_k, tuned=tuned)
 
@@ -106,7 +126,7 @@ def _rel(torch, a, b):
     return float((a.float() - b.float()).abs().max() / b.float().abs().max().clamp_min(1e-30))
 
 
-def tune_shape(torch, kind, H, F, dtype, heads, Ms, log=print):
+def tune_shape(torch, kind, H, F, dtype, heads, Ms, log=print, layout="nk"):
     dev = torch.device("cuda", torch.cuda.current_device())
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     tiles = ATTN_TILES if kind == "attn" else MLP_TILES
@@ -114,8 +134,8 @@ def tune_shape(torch, kind, H, F, dtype, heads, Ms, log=print):
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
     entries = []
     for M in Ms:
-        shape = {"M": M, "H": H, "F": F, "dtype": tdt, "heads": heads}
-        t = _inputs(torch, kind, M, H, F, tdt, dev)
+        shape = {"M": M, "H": H, "F": F, "dtype": tdt, "heads": heads, "layout": layout}
+        t = _inputs(torch, kind, M, H, F, tdt, dev, layout)
         Y = torch.empty(M, H, dtype=tdt, device=dev)
         splits = (1, 2, 3, 4) + ((6, 8, 12) if M <= 32 else ())
 
@@ -187,7 +207,7 @@ def tune_shape(torch, kind, H, F, dtype, heads, Ms, log=print):
                 tm, tn, sp = finals[pol].key
             else:
                 tm, tn, sp, us = 0, 0, 0, us_auto
-            entries.append({"kind": kind, "dtype": dtype, "H": H, "F": F, "M": M, "sms": sms, "layout": "nk",
+            entries.append({"kind": kind, "dtype": dtype, "H": H, "F": F, "M": M, "sms": sms, "layout": layout,
                             "policy": pol, "tile_m": tm, "tile_n": tn, "split_k": sp, "group_m": 0,
                             "us": round(us, 2), "builtin_us": round(us_auto, 2)})
             choice = f"tile {tm}x{tn} split {sp:2d}" if tm else "built-in rules    "
@@ -223,11 +243,21 @@ def write_table(path, entries, merge, device):
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
-    ap.add_argument("--preset", action="append", choices=sorted(PRESETS), required=True)
+    ap.add_argument("--preset", action="append", default=[], choices=sorted(PRESETS))
+    ap.add_argument("--shape", action="append", default=[], metavar="KIND,H,F,DTYPE[,HEADS]",
+                    help="a chain shape of your own (its default M list is the presets' 1 .. 2048)")
+    ap.add_argument("--layout", default="nk", choices=["nk", "kn"], help="weight storage layout")
     ap.add_argument("--M", default="", help="comma-separated row counts (default: the preset's list)")
     ap.add_argument("--out", default=cs.TUNE_TABLE)
     ap.add_argument("--merge", action="store_true", help="keep the file's entries for other shapes / M")
     args = ap.parse_args(argv)
+    shapes = [PRESETS[name] for name in args.preset]
+    try:
+        shapes += [parse_shape(t) + (PRESETS["gpt3"][5],) for t in args.shape]
+    except ValueError as e:
+        ap.error(str(e))
+    if not shapes:
+        ap.error("give at least one --preset or --shape")
     import torch
     if not torch.cuda.is_available():
         raise SystemExit("the tuner times kernels on a GPU; none is visible")
@@ -235,11 +265,11 @@ def main(argv=None):
     device = {"name": props.name, "sms": props.multi_processor_count, "cc": f"{props.major}.{props.minor}"}
     entries = []
     n = 0
-    for name in args.preset:
-        kind, H, F, dtype, heads, Ms = PRESETS[name]
+    for kind, H, F, dtype, heads, Ms in shapes:
         if args.M:
             Ms = tuple(int(v) for v in args.M.split(","))
-        entries += tune_shape(torch, kind, H, F, dtype, heads, Ms, log=lambda s: print(s, file=sys.stderr, flush=True))
+        entries += tune_shape(torch, kind, H, F, dtype, heads, Ms, layout=args.layout,
+                              log=lambda s: print(s, file=sys.stderr, flush=True))
         n = write_table(args.out, entries, args.merge, device)  # after every shape: keep what is measured
     print(json.dumps({"out": args.out, "entries": n}))
 

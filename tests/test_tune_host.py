@@ -212,3 +212,18 @@ def test_packaged_table_matches_its_own_entries(cs):
             assert e["us"] <= e["builtin_us"] * 1.0001
     finally:
         cs.cs_tune_clear()
+
+
+def test_tuner_shapes_of_ones_own():
+    from consumer_gemm_chain_gb300 import tune
+    assert tune.parse_shape("gelu, 8192, 4096, bf16") == ("gelu", 8192, 4096, "bf16", 0)
+    assert tune.parse_shape("attn,12288,1536,f16,12") == ("attn", 12288, 1536, "f16", 12)
+    for bad in ("gelu,8192,4096", "conv,8,8,f16", "gelu,8190,4096,f16", "attn,12288,1536,f16",
+                "gelu,8,8,f32", "gelu,x,8,f16"):
+        with pytest.raises(ValueError):
+            tune.parse_shape(bad)
+    # the command line refuses before it looks for a GPU
+    for argv in ([], ["--shape", "gelu,1,2"], ["--preset", "gpt3", "--layout", "mk"]):
+        with pytest.raises(SystemExit) as e:
+            tune.main(argv)
+        assert e.value.code == 2
