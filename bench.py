@@ -109,7 +109,7 @@ def measured_traffic(key, sched_sha):
     return rec.get("bytes_per_launch")
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
@@ -136,7 +136,7 @@ def parse():
                          "of the same shape (via torch) once, and exit; no other kernel runs")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU-oracle sample time")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 # ------------------------------------------------------------------ workload arithmetic
@@ -203,8 +203,12 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self, t0, t1):
+        """Median SM clock, max clock and throttle reasons of the samples taken
+        inside [t0, t1]; with none inside (a timed region shorter than the
+        sampling period), sm_mhz is None: samples of the idle GPU around the
+        region would not show the clock under load."""
         inside = [s for t, s in self.samples if t0 <= t <= t1]
-        used = inside if inside else [s for _, s in self.samples]
+        used = inside
 
         def num(x):
             try:
@@ -219,8 +223,13 @@ class ClockSampler:
             for name, v in zip(names, s[4:8]):
                 if v.strip().lower() == "active":
                     reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(used), "samples_in_timed_region": len(inside)}
+        mx_all = [num(s[1]) for _, s in self.samples if num(s[1]) is not None]
+        out = {"sm_mhz": statistics.median(sm) if sm else None,
+               "sm_max_mhz": max(mx) if mx else (max(mx_all) if mx_all else None),
+               "reasons": sorted(reasons), "samples_in_timed_region": len(inside)}
+        if not inside:
+            out["note"] = "no clock sample fell inside the timed region (shorter than the 100 ms sampling period)"
+        return out
 
 
 # ------------------------------------------------------------------ timing helpers
@@ -366,13 +375,18 @@ def dist_setup(args):
     return ws, rank, local
 
 
-def replica_tile_m(ws, tile_m, kind, M):
-    """Tile rows for an N-rank replica run.  Cluster multicast of weight boxes
-    (512-row tiles on 4-CTA clusters) is kept to single-GPU runs, so with several
-    ranks the automatic and 512-row choices become 2-SM pairs or single SMs."""
-    if ws > 1 and tile_m in (0, 512):
-        return 256 if (kind == "gelu" and M >= 1024) else 128
-    return tile_m
+def runs_extras(ws, quick):
+    """The side measurements (controls, solo stages, cuBLAS, sweeps, the CPU
+    oracle) run on one GPU only: an N-rank run times the headline chain alone."""
+    return ws == 1 and not quick
+
+
+def check_replica_library(cs, ws):
+    """An N-rank run must have loaded the replica build (no TMA cluster
+    multicast in it); the binding picks it from WORLD_SIZE."""
+    if ws > 1 and cs.cs_library_features() & cs.CS_FEATURE_CLUSTER_MULTICAST:
+        raise SystemExit(f"{ws} ranks but {os.path.basename(cs.chain.LIB_PATH)} has cluster multicast; "
+                         "the replica build libcs_chain_nomc.so must be loaded")
 
 
 def whole_job_tflops(flops_per_rank, ms_max, ws):
@@ -452,6 +466,7 @@ def _reference_line(args):
 
 
 METRIC = "MLP-chain TFLOP/s & % roofline vs M on 1 GB300; sync overhead vs best solo GEMMs"
+STEADY_S = 1.5  # seconds of the steady-state timing beside a short timed region
 
 
 def workload_config(name, M, inp, policy, layout="nk"):
@@ -465,6 +480,16 @@ def workload_config(name, M, inp, policy, layout="nk"):
 
 
 # ------------------------------------------------------------------ our arm
+def plan_desc(cs, args, inp, policy, M, pdl=None, tuned=0, out_release=0):
+    """The desc of a plan of the bench's MLP workload `inp` with M rows, the
+    command line's choices applied."""
+    return cs.cs_chain_desc_init(kind=inp.kind, M=M, H=inp.H, F=inp.F, dtype=inp.dtype, policy=policy,
+                                 weight_layout=args.layout, lag=args.lag, tile_n=args.tile_n, group_m=args.group_m,
+                                 tile_m=args.tile_m, split_k=args.split_k, prefetch=args.prefetch,
+                                 raster=args.raster, pdl=args.pdl if pdl is None else pdl, tuned=tuned,
+                                 out_release=out_release)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -484,7 +509,7 @@ def main():
     inp = cs_inputs.make_inputs(args.workload, M=M, seed=0)
     kind = inp.kind
     lay = args.layout
-    args.tile_m = replica_tile_m(ws, args.tile_m, kind, M)
+    check_replica_library(cs, ws)
 
     def w(t):
         t = t if lay == "kn" else t.t().contiguous()
@@ -499,12 +524,7 @@ def main():
     Y = torch.empty_like(X)
 
     def make_plan(policy, MM=M, pdl=None, tuned=0, out_release=0):
-        d = cs.cs_chain_desc_init(kind=kind, M=MM, H=inp.H, F=inp.F, dtype=inp.dtype, policy=policy,
-                                  weight_layout=lay, lag=args.lag, tile_n=args.tile_n, group_m=args.group_m,
-                                  tile_m=args.tile_m, split_k=args.split_k, prefetch=args.prefetch,
-                                  raster=args.raster, pdl=args.pdl if pdl is None else pdl, tuned=tuned,
-                                  out_release=out_release)
-        return cs.cs_chain_plan(d)
+        return cs.cs_chain_plan(plan_desc(cs, args, inp, policy, MM, pdl, tuned, out_release))
 
     plan = make_plan(args.policy)
     plan_info = cs.cs_chain_query(plan)
@@ -535,9 +555,22 @@ def main():
     ms_total, ms_launch = time_loop(step, args.steps, 0, stream)
     t_wall1 = time.monotonic()
     barrier(ws)
+    # A timed region shorter than a second is a burst: the SM clock has not yet
+    # settled under the power cap.  Beside it, one GPU also times the same step
+    # for at least STEADY_S seconds (reported apart; `value` stays the K steps).
+    steady = None
+    if ws == 1 and ms_total * args.steps < 1000.0 * STEADY_S and not args.quick:
+        n_steady = max(args.steps, int(STEADY_S * 1e3 / max(ms_total, 1e-3)) + 1)
+        t_s0 = time.monotonic()
+        ms_s, ms_s_launch = time_loop(step, n_steady, 0, stream)
+        t_s1 = time.monotonic()
+        steady = {"value": flops / (ms_s * 1e-3) / 1e12, "unit": "TFLOP/s", "steps": n_steady, "ms_per_step": ms_s,
+                  "launch_ms": ms_s_launch, "seconds": ms_s * n_steady / 1e3}
     if sampler:
         time.sleep(0.15)
         sampler.stop()
+        if steady is not None:
+            steady["clocks"] = sampler.summary(t_s0, t_s1)
     st = cs.cs_chain_status(plan)
     if st != cs.CS_OK:
         raise RuntimeError(f"device status {cs.STATUS_NAMES.get(st)}: {cs.cs_last_error_string()}")
@@ -580,6 +613,12 @@ def main():
     }
     if sampler:
         line["clocks"] = sampler.summary(t_wall0, t_wall1)
+    if steady is not None:
+        tc_s = peaks["bf16_tflops_sustained"]
+        steady["roofline"] = {"achieved": flops / (steady["launch_ms"] * 1e-3) / 1e12, "peak": tc_s,
+                              "frac": flops / (steady["launch_ms"] * 1e-3) / 1e12 / tc_s,
+                              "peak_source": f"{peak_src} (sustained)"} if bound == "tensor" else None
+        line["steady_state"] = steady
 
     # ---- end to end through the C ABI with host buffers
     Xh = inp.X.pin_memory()
@@ -600,7 +639,7 @@ def main():
                    "d2h_bytes_per_step": Yh.numel() * Yh.element_size(), "ms_per_step": e2e_ms,
                    "api": "cs_mlp_forward_host (double-buffered copies on two copy streams)"}
 
-    if rank == 0 and not args.quick:
+    if rank == 0 and runs_extras(ws, args.quick):
         line["extras"] = extras(cs, torch, inp, dev, Y, make_plan, plan, M, kind, peaks, stream)
         if args.workload == "gpt3":
             line["extras"]["other_configs"] = other_configs(cs, torch, peaks, lay)

@@ -13,6 +13,10 @@ from .chain import (  # noqa: F401
     cs_abi_version,
     cs_attn_chain_forward,
     cs_chain_debug_copy_intermediate,
+    cs_chain_debug_poison_intermediate,
+    cs_chain_debug_set_epoch,
+    cs_chain_plan_info,
+    cs_library_features,
     cs_chain_debug_read_sems,
     cs_chain_debug_read_trace,
     cs_chain_debug_set_delays,

@@ -11,7 +11,22 @@ import ctypes
 import os
 
 PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(PKG, "_lib", "libcs_chain.so")
+
+
+def library_path(environ=os.environ) -> str:
+    """The build this process loads.  A process that shares a node with other
+    GPUs' ranks (WORLD_SIZE > 1, as torchrun sets it) loads the replica build,
+    which contains no TMA cluster-multicast load; CS_CHAIN_LIBRARY=full|nomc
+    overrides the choice."""
+    want = environ.get("CS_CHAIN_LIBRARY", "")
+    if want not in ("", "full", "nomc"):
+        raise ImportError(f"CS_CHAIN_LIBRARY={want!r}: expected 'full' or 'nomc'")
+    ws = environ.get("WORLD_SIZE", "1")
+    nomc = want == "nomc" or (want == "" and ws.isdigit() and int(ws) > 1)
+    return os.path.join(PKG, "_lib", "libcs_chain_nomc.so" if nomc else "libcs_chain.so")
+
+
+LIB_PATH = library_path()
 
 # cs_status
 CS_OK = 0
@@ -44,8 +59,10 @@ EXPORTED = (
     "cs_schedule_build", "cs_chain_debug_read_sems", "cs_chain_debug_set_delays", "cs_chain_debug_skip_release",
     "cs_chain_debug_copy_intermediate", "cs_chain_debug_trace", "cs_chain_debug_read_trace", "cs_abi_version",
     "cs_mlp_forward_noalloc", "cs_noalloc_status", "cs_tune_load", "cs_tune_clear", "cs_tune_size",
-    "cs_tune_match",
+    "cs_tune_match", "cs_chain_plan_info", "cs_library_features", "cs_chain_debug_poison_intermediate",
+    "cs_chain_debug_set_epoch",
 )
+CS_FEATURE_CLUSTER_MULTICAST = 1
 
 
 class cs_chain_desc(ctypes.Structure):
@@ -112,6 +129,10 @@ def _load() -> ctypes.CDLL:
         "cs_tune_clear": (I, []),
         "cs_tune_size": (I, []),
         "cs_tune_match": (I, [ctypes.POINTER(cs_chain_desc), I, ctypes.POINTER(I), ctypes.POINTER(cs_chain_desc)]),
+        "cs_chain_plan_info": (I, [ctypes.POINTER(cs_chain_desc), I, ctypes.POINTER(cs_chain_info)]),
+        "cs_library_features": (I, []),
+        "cs_chain_debug_poison_intermediate": (I, [V, I, V]),
+        "cs_chain_debug_set_epoch": (I, [V, ctypes.c_uint32]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -318,6 +339,23 @@ def cs_chain_reset(plan: Plan) -> None:
 def cs_chain_query(plan: Plan) -> dict:
     i = cs_chain_info()
     _check(_lib.cs_chain_query(plan.handle, ctypes.byref(i)), "cs_chain_query")
+    return _info_dict(i)
+
+
+def cs_chain_plan_info(desc: cs_chain_desc, num_sms: int) -> dict:
+    """The geometry a plan of ``desc`` would get on ``num_sms`` SMs (keys as
+    cs_chain_query; pointers are None).  Needs no GPU."""
+    i = cs_chain_info()
+    _check(_lib.cs_chain_plan_info(ctypes.byref(desc), num_sms, ctypes.byref(i)), "cs_chain_plan_info")
+    return _info_dict(i)
+
+
+def cs_library_features() -> int:
+    """Bit flags of the loaded build (CS_FEATURE_CLUSTER_MULTICAST)."""
+    return _lib.cs_library_features()
+
+
+def _info_dict(i: cs_chain_info) -> dict:
     return {"stages": i.stages, "m_tiles": i.m_tiles, "n_tiles": list(i.n_tiles), "units": list(i.units),
             "n_units": i.n_units, "num_sms": i.num_sms, "smem_bytes": i.smem_bytes, "lag": i.lag,
             "group_m": i.group_m, "tile_n": list(i.tile_n), "tile_m": i.tile_m,
@@ -401,6 +439,19 @@ def cs_chain_debug_copy_intermediate(plan: Plan, which: int, out) -> None:
     nbytes = out.numel() * out.element_size()
     _check(_lib.cs_chain_debug_copy_intermediate(plan.handle, which, out.data_ptr(), nbytes),
            "cs_chain_debug_copy_intermediate")
+
+
+def cs_chain_debug_poison_intermediate(plan: Plan, which: int = -1, stream=None) -> None:
+    """Enqueue a NaN fill of plan-owned scratch (0: H or QKV, 1: O, 2: split-K
+    partial tiles, -1: all): a consumer that read before its producer released
+    would then produce NaN."""
+    _check(_lib.cs_chain_debug_poison_intermediate(plan.handle, which, _stream_ptr(stream)),
+           "cs_chain_debug_poison_intermediate")
+
+
+def cs_chain_debug_set_epoch(plan: Plan, epoch: int) -> None:
+    """Set the epoch and every counter to their values after ``epoch`` forwards (mod 2^32)."""
+    _check(_lib.cs_chain_debug_set_epoch(plan.handle, epoch & 0xFFFFFFFF), "cs_chain_debug_set_epoch")
 
 
 def cs_chain_debug_trace(plan: Plan, enable: bool = True) -> None:

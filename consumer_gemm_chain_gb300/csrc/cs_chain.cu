@@ -16,6 +16,7 @@
 
 #include "../../include/cs_chain.h"
 #include "cs_kernel.cuh"
+#include "cs_sched.cuh"
 #include "cs_tune.h"
 
 namespace {
@@ -38,6 +39,14 @@ cs_status fail(cs_status s, const char* fmt, ...) {
 
 constexpr int kMaxMaps = 9;
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
+// The replica build (CS_NO_CLUSTER_MULTICAST), which processes that share a
+// node with other GPUs' ranks load, has no 512-row tiles: those are the only
+// ones whose weight boxes travel by TMA cluster multicast.
+#ifdef CS_NO_CLUSTER_MULTICAST
+constexpr bool kClusterMulticast = false;
+#else
+constexpr bool kClusterMulticast = true;
+#endif
 
 // Kernel configurations: ring depth x stage bytes.  A stage holds the A slice
 // (128 x 64) and the B slice (128 x 64; or 256 x 64 for 256-wide tiles and for
@@ -163,11 +172,6 @@ cs_status encode_2d(CUtensorMap* map, const void* ptr, int bf16, uint64_t inner,
 
 inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 
-inline uint32_t enc_unit(int s, int m, int n, int ks) {
-  return (static_cast<uint32_t>(s) << 30) | (static_cast<uint32_t>(ks) << 26) | (static_cast<uint32_t>(m) << 14) |
-         static_cast<uint32_t>(n);
-}
-
 // Geometry shared by the host-only schedule builder and the plan.
 struct Geometry {
   int stages = 0, m_tiles = 0;  // m_tiles: tile rows (tile_m each)
@@ -209,6 +213,8 @@ cs_status validate(const cs_chain_desc* d) {
     return fail(CS_ERR_INVALID_ARG, "tile_m=%d (0, 128, 256 or 512)", d->tile_m);
   if (d->tile_m >= 256 && d->tile_n == 128)
     return fail(CS_ERR_UNSUPPORTED, "tile_m=%d is built for 256-wide tiles only", d->tile_m);
+  if (d->tile_m == 512 && !kClusterMulticast)
+    return fail(CS_ERR_UNSUPPORTED, "tile_m=512 needs cluster multicast, which the replica build leaves out");
   if (d->kind == CS_CHAIN_ATTN) {
     if (d->head_dim != 128) return fail(CS_ERR_UNSUPPORTED, "head_dim=%d (only 128 is built)", d->head_dim);
     if (d->heads < 1 || d->heads * d->head_dim != d->F)
@@ -250,7 +256,7 @@ Geometry geometry(const cs_chain_desc* d, int num_sms) {
   // (measured at LLaMA M=512 / 768: 76 / 104 us against 93 / 117 us with
   // 128-row tiles), for GeLU where they add no padding rows over 256-row pairs
   // (GPT-3 M=768: 199 us against 176 us with 128-row tiles).
-  if (tm == 0 && (tn == 0 || tn == 256) && mlp && blocks >= 4 &&
+  if (kClusterMulticast && tm == 0 && (tn == 0 || tn == 256) && mlp && blocks >= 4 &&
       (d->kind == CS_CHAIN_MLP_SWIGLU || 2 * cdiv(d->M, 512) == cdiv(d->M, 256)))
     tm = 512, tn = 256;
   if (tn == 0) tn = (2 * blocks * cdiv(d->F, 256) >= num_sms) ? 256 : 128;
@@ -346,45 +352,93 @@ Geometry geometry(const cs_chain_desc* d, int num_sms) {
   return g;
 }
 
-// Dependency-respecting dispatch order.  Row blocks form groups of group_m; at
-// step t, stage s lists every unit of group t - s*lag, column-tile-major so that
-// the tiles running at the same time share their weight tiles in L2.  Every
-// unit a consumer waits on (same row block, or for the attention stage every
-// earlier row block) is listed at an earlier step or earlier in the same step,
-// so a dynamic in-order dispatcher cannot deadlock.
-// Units of stage s, tile rows [m0, m1): column-major (weight tiles shared by
-// the rows of the group run together) or row-major (rows complete in turn).
-void append_group(const Geometry& g, int s, int m0, int m1, std::vector<uint32_t>& v) {
-  if (g.row_major) {
-    for (int m = m0; m < m1; ++m)
-      for (int n = 0; n < g.n_tiles[s]; ++n)
-        for (int ks = 0; ks < g.splits[s]; ++ks) v.push_back(enc_unit(s, m, n, ks));
-  } else {
-    for (int n = 0; n < g.n_tiles[s]; ++n)
-      for (int m = m0; m < m1; ++m)
-        for (int ks = 0; ks < g.splits[s]; ++ks) v.push_back(enc_unit(s, m, n, ks));
+// Dispatch order (closed form in cs_sched.cuh, shared with the device-side
+// builder of the allocation-free forward): row tiles in groups of group_m; at
+// step t, stage s lists the units of group t - s*lag, so every producer unit a
+// consumer waits on is listed before it and an in-order dispatcher cannot
+// deadlock.
+cs::SchedGeo sched_geo(const Geometry& g) {
+  cs::SchedGeo sg;
+  sg.stages = g.stages;
+  sg.m_tiles = g.m_tiles;
+  sg.group_m = g.group_m;
+  sg.lag = g.lag;
+  sg.row_major = g.row_major ? 1 : 0;
+  for (int s = 0; s < 3; ++s) {
+    sg.n_tiles[s] = g.n_tiles[s];
+    sg.splits[s] = g.splits[s];
   }
+  return sg;
 }
 
 std::vector<uint32_t> build_fused(const Geometry& g) {
-  std::vector<uint32_t> v;
-  const int groups = cdiv(g.m_tiles, g.group_m);
-  const int steps = groups + (g.stages - 1) * g.lag;
-  for (int t = 0; t < steps; ++t)
-    for (int s = 0; s < g.stages; ++s) {
-      const int gg = t - s * g.lag;
-      if (gg < 0 || gg >= groups) continue;
-      const int m0 = gg * g.group_m, m1 = std::min(g.m_tiles, m0 + g.group_m);
-      append_group(g, s, m0, m1, v);
-    }
+  const cs::SchedGeo sg = sched_geo(g);
+  std::vector<uint32_t> v(static_cast<size_t>(cs::sched_fused_count(sg)));
+  for (size_t i = 0; i < v.size(); ++i) v[i] = cs::sched_fused_entry(sg, static_cast<long long>(i));
   return v;
 }
 
 // One stage alone (two-kernel control, standalone timings): same grouping.
 std::vector<uint32_t> build_stage(const Geometry& g, int s) {
-  std::vector<uint32_t> v;
-  for (int m0 = 0; m0 < g.m_tiles; m0 += g.group_m) append_group(g, s, m0, std::min(g.m_tiles, m0 + g.group_m), v);
+  const cs::SchedGeo sg = sched_geo(g);
+  std::vector<uint32_t> v(static_cast<size_t>(cs::sched_stage_count(sg, s)));
+  for (size_t i = 0; i < v.size(); ++i) v[i] = cs::sched_stage_entry(sg, s, static_cast<long long>(i));
   return v;
+}
+
+// Everything a plan takes from its geometry: tile counts, K-splits, the kernel
+// configuration (ring depth and stage size) and its shared memory.  The grid
+// is rounded down to whole clusters.
+void shape_plan(cs_chain_s* p, const Geometry& g, int kind, int M) {
+  p->m_tiles = g.m_blocks;
+  p->m_units = g.m_tiles;
+  p->m_blocks = g.m_blocks;
+  p->cg = g.cg;
+  p->cl = g.cl;
+  p->stages = g.stages;
+  for (int i = 0; i < 3; ++i) {
+    p->n_tiles[i] = g.n_tiles[i];
+    p->k_iters[i] = g.k_iters[i];
+    p->units[i] = g.m_blocks * g.n_tiles[i];
+    p->sched_units[i] = g.m_tiles * g.n_tiles[i] * g.splits[i];
+    p->splits[i] = g.splits[i];
+    p->kps[i] = g.kps[i];
+    p->bn[i] = g.bn[i];
+  }
+  p->lag = g.lag;
+  p->group_m = g.group_m;
+  p->stride = g.stride;
+  const bool wide_b = kind == CS_CHAIN_MLP_SWIGLU || g.bn[0] == 256 || g.bn[1] == 256 || g.bn[2] == 256;
+  p->cfg_s = (g.cg == 1 && kind != CS_CHAIN_ATTN && M <= 8) ? (wide_b ? 2 : 1) : 0;
+  p->cfg_b = g.cg == 1 && !p->cfg_s && wide_b;
+  p->smem = p->cfg_s == 1 ? smem_bytes_for<NS_S, SB_S>()
+            : p->cfg_s == 2 ? smem_bytes_for<NS_T, SB_T>()
+            : p->cfg_b      ? smem_bytes_for<NS_B, SB_B>()
+                            : smem_bytes_for<NS_A, SB_A>();
+  p->num_sms = p->num_sms / g.cl * g.cl;
+}
+
+// The geometry fields of cs_chain_info (no device pointers).
+void info_geometry(const cs_chain_s* p, int n_fused, cs_chain_info* info) {
+  std::memset(info, 0, sizeof(*info));
+  info->stages = p->stages;
+  info->m_tiles = p->m_tiles;
+  for (int i = 0; i < 3; ++i) {
+    info->n_tiles[i] = p->n_tiles[i];
+    info->units[i] = p->units[i];
+    info->tile_n[i] = p->bn[i];
+    info->sched_units[i] = p->sched_units[i];
+    info->split_k[i] = p->splits[i];
+  }
+  info->n_units = n_fused;
+  info->num_sms = p->num_sms;
+  info->smem_bytes = p->smem;
+  info->lag = p->lag;
+  info->group_m = p->group_m;
+  info->tile_m = cs::BM * p->cl;
+  info->stride = p->stride;
+  info->policy = p->d.policy;
+  info->tuned_entry = p->tuned_entry;
 }
 
 int device_sms(int* out) {
@@ -461,6 +515,16 @@ cs_status encode_act(cs_chain_s* p, int slot, const void* ptr, int rows, int col
   p->slots[slot].ptr = ptr;
   p->slots[slot].valid = true;
   return CS_OK;
+}
+
+// Two-kernel control: the launch of the next stage records its units after
+// those of stage `done` in the trace buffer (each launch counts its dispatch
+// indices from 0).
+void next_trace_segment(const cs_chain_s* p, cs::KParams& kp, int done) {
+  if (!kp.trace) return;
+  const int recs = p->sched_units[done] * p->cl;
+  kp.trace += static_cast<size_t>(recs) * cs::TRACE_WORDS;
+  kp.trace_records -= recs;
 }
 
 int wait_kind(const cs_chain_s* p) {
@@ -613,9 +677,11 @@ cs_status launch(cs_chain_s* p, cs::KParams& kp, const uint32_t* sched, int n_un
   } else if (p->d.kind == CS_CHAIN_ATTN) {
     if ((s = set_smem_attr<NS_A, SB_A, 1, true>()) != CS_OK) return s;
     e = cudaLaunchKernelEx(&cfg, cs::cs_chain_kernel<NS_A, SB_A, 1, true>, kp);
+#ifndef CS_NO_CLUSTER_MULTICAST
   } else if (p->cl == 4) {
     if ((s = set_smem_attr<NS_A, SB_A, 2, false, 4>()) != CS_OK) return s;
     e = cudaLaunchKernelEx(&cfg, cs::cs_chain_kernel<NS_A, SB_A, 2, false, 4>, kp);
+#endif
   } else if (p->cg == 2) {
     if ((s = set_smem_attr<NS_A, SB_A, 2, false>()) != CS_OK) return s;
     e = cudaLaunchKernelEx(&cfg, cs::cs_chain_kernel<NS_A, SB_A, 2, false>, kp);
@@ -838,31 +904,7 @@ cs_status cs_chain_plan(const cs_chain_desc* desc, cs_chain_t* out) {
   p->num_sms = desc->num_sms > 0 && desc->num_sms < sms ? desc->num_sms : sms;
   p->d = resolve_desc(desc, p->num_sms, &p->tuned_entry);
   Geometry g = geometry(&p->d, p->num_sms);
-  p->m_tiles = g.m_blocks;
-  p->m_units = g.m_tiles;
-  p->m_blocks = g.m_blocks;
-  p->cg = g.cg;
-  p->cl = g.cl;
-  p->stages = g.stages;
-  for (int i = 0; i < 3; ++i) {
-    p->n_tiles[i] = g.n_tiles[i];
-    p->k_iters[i] = g.k_iters[i];
-    p->units[i] = g.m_blocks * g.n_tiles[i];
-    p->sched_units[i] = g.m_tiles * g.n_tiles[i] * g.splits[i];
-    p->splits[i] = g.splits[i];
-    p->kps[i] = g.kps[i];
-  }
-  p->lag = g.lag;
-  p->group_m = g.group_m;
-  p->stride = g.stride;
-  for (int i = 0; i < 3; ++i) p->bn[i] = g.bn[i];
-  const bool wide_b = desc->kind == CS_CHAIN_MLP_SWIGLU || g.bn[0] == 256 || g.bn[1] == 256 || g.bn[2] == 256;
-  p->cfg_s = (g.cg == 1 && desc->kind != CS_CHAIN_ATTN && desc->M <= 8) ? (wide_b ? 2 : 1) : 0;
-  p->cfg_b = g.cg == 1 && !p->cfg_s && wide_b;
-  p->smem = p->cfg_s == 1 ? smem_bytes_for<NS_S, SB_S>()
-            : p->cfg_s == 2 ? smem_bytes_for<NS_T, SB_T>()
-            : p->cfg_b      ? smem_bytes_for<NS_B, SB_B>()
-                            : smem_bytes_for<NS_A, SB_A>();
+  shape_plan(p, g, desc->kind, desc->M);
 
   auto bail = [&](cs_status st) {
     free_plan(p);
@@ -902,7 +944,6 @@ cs_status cs_chain_plan(const cs_chain_desc* desc, cs_chain_t* out) {
   if ((s = upload(&p->sched_fused, fused)) != CS_OK) return bail(s);
   for (int st = 0; st < g.stages; ++st)
     if ((s = upload(&p->sched_stage[st], build_stage(g, st))) != CS_OK) return bail(s);
-  p->num_sms = p->num_sms / g.cl * g.cl;
   // plan-owned intermediate maps (never re-encoded)
   int owned[5];
   int n_owned = 0;
@@ -963,6 +1004,7 @@ cs_status cs_mlp_forward(cs_chain_t p, const cs_mlp_args* a, void* stream) {
     kp.bump_epoch = 0;
     if ((s = launch(p, kp, p->sched_stage[0], p->sched_units[0], st)) != CS_OK) return s;
     kp.bump_epoch = 1;
+    next_trace_segment(p, kp, 0);
     return launch(p, kp, p->sched_stage[1], p->sched_units[1], st);
   }
   kp.waits = 1;
@@ -1035,6 +1077,7 @@ cs_status cs_attn_chain_forward(cs_chain_t p, const cs_attn_args* a, void* strea
     kp.release = 1;
     for (int stg = 0; stg < 3; ++stg) {
       kp.bump_epoch = stg == 2;
+      if (stg > 0) next_trace_segment(p, kp, stg - 1);
       if ((s = launch(p, kp, p->sched_stage[stg], p->sched_units[stg], st)) != CS_OK) return s;
     }
     return CS_OK;
@@ -1097,31 +1140,11 @@ cs_status cs_chain_reset(cs_chain_t p) {
 
 cs_status cs_chain_query(cs_chain_t p, cs_chain_info* info) {
   if (!p || !info) return fail(CS_ERR_INVALID_ARG, "NULL argument");
-  std::memset(info, 0, sizeof(*info));
-  info->stages = p->stages;
-  info->m_tiles = p->m_tiles;
-  for (int i = 0; i < 3; ++i) {
-    info->n_tiles[i] = p->n_tiles[i];
-    info->units[i] = p->units[i];
-  }
-  info->n_units = p->n_fused;
-  info->num_sms = p->num_sms;
-  info->smem_bytes = p->smem;
-  info->lag = p->lag;
-  info->group_m = p->group_m;
-  for (int i = 0; i < 3; ++i) {
-    info->tile_n[i] = p->bn[i];
-    info->sched_units[i] = p->sched_units[i];
-    info->split_k[i] = p->splits[i];
-  }
-  info->tile_m = cs::BM * p->cl;
-  info->stride = p->stride;
+  info_geometry(p, p->n_fused, info);
   info->intermediate[0] = p->inter[0];
   info->intermediate[1] = p->inter[1];
   info->sem_words[0] = p->sem_words[0];
   info->sem_words[1] = p->sem_words[1];
-  info->policy = p->d.policy;
-  info->tuned_entry = p->tuned_entry;
   const int last = p->stages - 1;
   info->out_tile_sems = p->sems[last];
   info->out_row_sems = p->sems[last] ? p->sems[last] + p->sem_words[last] : nullptr;
@@ -1139,6 +1162,22 @@ cs_status cs_tune_match(const cs_chain_desc* desc, int num_sms, int* entry, cs_c
   if (resolved) *resolved = rd;
   return CS_OK;
 }
+
+cs_status cs_chain_plan_info(const cs_chain_desc* desc, int num_sms, cs_chain_info* info) {
+  if (!info) return fail(CS_ERR_INVALID_ARG, "info is NULL");
+  cs_status s = validate(desc);
+  if (s != CS_OK) return s;
+  if (num_sms < 1) return fail(CS_ERR_INVALID_ARG, "num_sms=%d", num_sms);
+  cs_chain_s p;
+  p.num_sms = desc->num_sms > 0 && desc->num_sms < num_sms ? desc->num_sms : num_sms;
+  p.d = resolve_desc(desc, p.num_sms, &p.tuned_entry);
+  const Geometry g = geometry(&p.d, p.num_sms);
+  shape_plan(&p, g, desc->kind, desc->M);
+  info_geometry(&p, static_cast<int>(build_fused(g).size()), info);
+  return CS_OK;
+}
+
+int cs_library_features(void) { return kClusterMulticast ? CS_FEATURE_CLUSTER_MULTICAST : 0; }
 
 cs_status cs_chain_debug_read_sems(cs_chain_t p, int boundary, uint32_t* host, size_t n, uint32_t* epoch) {
   if (!p || !host) return fail(CS_ERR_INVALID_ARG, "NULL argument");
@@ -1180,6 +1219,44 @@ cs_status cs_chain_debug_copy_intermediate(cs_chain_t p, int which, void* dst, s
   if (bytes > p->inter_bytes[which]) return fail(CS_ERR_INVALID_ARG, "%zu bytes > buffer (%zu)", bytes, p->inter_bytes[which]);
   CS_CUDA(cudaDeviceSynchronize());
   CS_CUDA(cudaMemcpy(dst, p->inter[which], bytes, cudaMemcpyDeviceToDevice));
+  return CS_OK;
+}
+
+cs_status cs_chain_debug_poison_intermediate(cs_chain_t p, int which, void* stream) {
+  if (!p) return fail(CS_ERR_INVALID_ARG, "plan is NULL");
+  if (which < -1 || which > 2) return fail(CS_ERR_INVALID_ARG, "which=%d (-1..2)", which);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // all-ones bytes: NaN as fp16, bf16 and fp32
+  for (int b = 0; b < 2; ++b)
+    if ((which == -1 || which == b) && p->inter[b]) CS_CUDA(cudaMemsetAsync(p->inter[b], 0xFF, p->inter_bytes[b], st));
+  if (which == -1 || which == 2)
+    for (int stg = 0; stg < p->stages; ++stg)
+      if (p->partial[stg]) {
+        const int acc_n = (p->d.kind == CS_CHAIN_MLP_SWIGLU && stg == 0) ? 256 : p->bn[stg];
+        const size_t bytes = static_cast<size_t>(p->splits[stg]) * p->m_blocks * p->n_tiles[stg] * cs::BM * acc_n * 4;
+        CS_CUDA(cudaMemsetAsync(p->partial[stg], 0xFF, bytes, st));
+      }
+  return CS_OK;
+}
+
+cs_status cs_chain_debug_set_epoch(cs_chain_t p, uint32_t epoch) {
+  if (!p) return fail(CS_ERR_INVALID_ARG, "plan is NULL");
+  CS_CUDA(cudaDeviceSynchronize());
+  // every counter as it stands after `epoch` complete forwards, modulo 2^32
+  for (int b = 0; b < 3; ++b) {
+    if (!p->sems[b]) continue;
+    std::vector<uint32_t> v(p->sem_words[b] + p->m_tiles, epoch);
+    for (int m = 0; m < p->m_tiles; ++m) v[p->sem_words[b] + m] = epoch * static_cast<uint32_t>(p->n_tiles[b]);
+    CS_CUDA(cudaMemcpy(p->sems[b], v.data(), v.size() * 4, cudaMemcpyHostToDevice));
+  }
+  for (int stg = 0; stg < p->stages; ++stg)
+    if (p->split_ctr[stg]) {
+      std::vector<uint32_t> v(static_cast<size_t>(p->m_blocks) * p->n_tiles[stg],
+                              epoch * static_cast<uint32_t>(p->splits[stg]));
+      CS_CUDA(cudaMemcpy(p->split_ctr[stg], v.data(), v.size() * 4, cudaMemcpyHostToDevice));
+    }
+  CS_CUDA(cudaMemcpy(p->ctrl + cs::CTRL_EPOCH, &epoch, 4, cudaMemcpyHostToDevice));
+  CS_CUDA(cudaDeviceSynchronize());
   return CS_OK;
 }
 
@@ -1241,6 +1318,34 @@ cs_status noalloc_scratch(int dev, unsigned char** out) {
 
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
+// Per call, in stream order before the chain: zero the control block and the
+// semaphores, and write the fused and per-stage schedules from the closed form,
+// one thread per word (nothing is copied from host memory).
+__global__ void noalloc_prep_kernel(cs::SchedGeo g, uint32_t* zero, long long n_zero, uint32_t* fused,
+                                    long long n_fused, uint32_t* st0, long long n0, uint32_t* st1, long long n1) {
+  const long long total = n_zero + n_fused + n0 + n1;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    long long j = i;
+    if (j < n_zero) {
+      zero[j] = 0u;
+      continue;
+    }
+    j -= n_zero;
+    if (j < n_fused) {
+      fused[j] = cs::sched_fused_entry(g, j);
+      continue;
+    }
+    j -= n_fused;
+    if (j < n0) {
+      st0[j] = cs::sched_stage_entry(g, 0, j);
+      continue;
+    }
+    j -= n0;
+    st1[j] = cs::sched_stage_entry(g, 1, j);
+  }
+}
+
 }  // namespace
 
 extern "C" {
@@ -1250,6 +1355,9 @@ cs_status cs_mlp_forward_noalloc(const cs_chain_desc* desc, const cs_mlp_args* a
   if (s != CS_OK) return s;
   if (desc->kind == CS_CHAIN_ATTN) return fail(CS_ERR_UNSUPPORTED, "the allocation-free forward runs MLP chains only");
   if (desc->out_release) return fail(CS_ERR_UNSUPPORTED, "the allocation-free forward has no output semaphores");
+  if (desc->split_k > 1)
+    return fail(CS_ERR_UNSUPPORTED, "split_k=%d: the allocation-free forward runs unsplit tiles (split_k 0 or 1)",
+                desc->split_k);
   int sms = 0;
   const int dev = device_sms(&sms);
   if (dev < 0) return fail(CS_ERR_CUDA, "no CUDA device available");
@@ -1260,48 +1368,25 @@ cs_status cs_mlp_forward_noalloc(const cs_chain_desc* desc, const cs_mlp_args* a
     return fail(CS_ERR_UNSUPPORTED, "device is sm_%d%d; this library is built for sm_103a only", major, minor);
 
   // A plan on the host stack whose buffers all point into the scratch array.
+  // The tuning table is not consulted; policy AUTO runs TILE.
   cs_chain_s p;
   p.d = *desc;
   p.d.split_k = 1;  // no split-K workspace in the fixed array
-  if (p.d.policy == CS_SYNC_AUTO) p.d.policy = CS_SYNC_TILE;  // no tuning table here
+  if (p.d.policy == CS_SYNC_AUTO) p.d.policy = CS_SYNC_TILE;
   p.device = dev;
   p.num_sms = desc->num_sms > 0 && desc->num_sms < sms ? desc->num_sms : sms;
   Geometry g = geometry(&p.d, p.num_sms);
-  p.m_tiles = g.m_blocks;
-  p.m_units = g.m_tiles;
-  p.m_blocks = g.m_blocks;
-  p.cg = g.cg;
-  p.cl = g.cl;
-  p.stages = g.stages;
-  for (int i = 0; i < 3; ++i) {
-    p.n_tiles[i] = g.n_tiles[i];
-    p.k_iters[i] = g.k_iters[i];
-    p.units[i] = g.m_blocks * g.n_tiles[i];
-    p.sched_units[i] = g.m_tiles * g.n_tiles[i] * g.splits[i];
-    p.splits[i] = g.splits[i];
-    p.kps[i] = g.kps[i];
-    p.bn[i] = g.bn[i];
-  }
-  p.lag = g.lag;
-  p.group_m = g.group_m;
-  p.stride = g.stride;
-  const bool wide_b = desc->kind == CS_CHAIN_MLP_SWIGLU || g.bn[0] == 256 || g.bn[1] == 256;
-  p.cfg_s = (g.cg == 1 && desc->M <= 8) ? (wide_b ? 2 : 1) : 0;
-  p.cfg_b = g.cg == 1 && !p.cfg_s && wide_b;
-  p.smem = p.cfg_s == 1 ? smem_bytes_for<NS_S, SB_S>()
-           : p.cfg_s == 2 ? smem_bytes_for<NS_T, SB_T>()
-           : p.cfg_b      ? smem_bytes_for<NS_B, SB_B>()
-                          : smem_bytes_for<NS_A, SB_A>();
-  p.num_sms = p.num_sms / g.cl * g.cl;
-  const std::vector<uint32_t> fused = build_fused(g);
-  const std::vector<uint32_t> st0 = build_stage(g, 0), st1 = build_stage(g, 1);
-  p.n_fused = static_cast<int>(fused.size());
+  shape_plan(&p, g, desc->kind, desc->M);
+  const cs::SchedGeo sg = sched_geo(g);
+  const long long n_fused = cs::sched_fused_count(sg);
+  const long long n_st0 = cs::sched_stage_count(sg, 0), n_st1 = cs::sched_stage_count(sg, 1);
+  p.n_fused = static_cast<int>(n_fused);
 
   // Carve the array: control block and semaphores (cleared every call), then
   // the schedules, then the intermediate H [M, F].
   p.sem_words[0] = static_cast<size_t>(g.m_blocks) * g.n_tiles[0];
   const size_t zero_words = cs::CTRL_WORDS + p.sem_words[0] + g.m_blocks;
-  const size_t sched_words = fused.size() + st0.size() + st1.size();
+  const size_t sched_words = static_cast<size_t>(n_fused + n_st0 + n_st1);
   const size_t h_off = align256((zero_words + sched_words) * 4);
   p.inter_bytes[0] = static_cast<size_t>(desc->M) * desc->F * 2;
   const size_t need = h_off + p.inter_bytes[0];
@@ -1315,15 +1400,9 @@ cs_status cs_mlp_forward_noalloc(const cs_chain_desc* desc, const cs_mlp_args* a
   p.ctrl = words;
   p.sems[0] = words + cs::CTRL_WORDS;
   p.sched_fused = words + zero_words;
-  p.sched_stage[0] = p.sched_fused + fused.size();
-  p.sched_stage[1] = p.sched_stage[0] + st0.size();
+  p.sched_stage[0] = p.sched_fused + n_fused;
+  p.sched_stage[1] = p.sched_stage[0] + n_st0;
   p.inter[0] = base + h_off;
-
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  CS_CUDA(cudaMemsetAsync(words, 0, zero_words * 4, st));
-  CS_CUDA(cudaMemcpyAsync(p.sched_fused, fused.data(), fused.size() * 4, cudaMemcpyHostToDevice, st));
-  CS_CUDA(cudaMemcpyAsync(p.sched_stage[0], st0.data(), st0.size() * 4, cudaMemcpyHostToDevice, st));
-  CS_CUDA(cudaMemcpyAsync(p.sched_stage[1], st1.data(), st1.size() * 4, cudaMemcpyHostToDevice, st));
 
   // Tensor maps of the intermediate (in the array) and of the caller's tensors.
   if ((s = encode_act(&p, MAP_HST, p.inter[0], desc->M, desc->F, true)) != CS_OK) return s;
@@ -1331,6 +1410,16 @@ cs_status cs_mlp_forward_noalloc(const cs_chain_desc* desc, const cs_mlp_args* a
   for (int i = 0; i < kMaxMaps; ++i)
     if (i != MAP_HST && i != MAP_HLD) std::memcpy(&p.maps[i], &p.maps[MAP_HLD], sizeof(CUtensorMap));
   if ((s = bind_mlp(&p, args)) != CS_OK) return s;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  {
+    const long long total = static_cast<long long>(zero_words) + n_fused + n_st0 + n_st1;
+    const int threads = 256;
+    const int blocks = static_cast<int>(std::min<long long>((total + threads - 1) / threads, 4 * sms));
+    noalloc_prep_kernel<<<blocks, threads, 0, st>>>(sg, words, static_cast<long long>(zero_words), p.sched_fused,
+                                                     n_fused, p.sched_stage[0], n_st0, p.sched_stage[1], n_st1);
+    CS_CUDA(cudaGetLastError());
+  }
 
   cs::KParams kp;
   std::memset(&kp, 0, sizeof(kp));

@@ -405,6 +405,7 @@ __device__ bool tma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
     sc->tma_kb = kb;
     if (kb == kb1 - 1) trace_put(p, tidx, rank, CL, 5, globaltimer());
     load(sa, &p.maps[S.map_a], kb * BK, row0);
+#ifndef CS_NO_CLUSTER_MULTICAST
     if constexpr (CL == 4) {
       // this CTA fetches half of its B columns (the half of its pair index)
       // for itself and for the CTA with the same pair rank in the other pair
@@ -424,6 +425,7 @@ __device__ bool tma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
       rp.next<NS>();
       continue;
     }
+#endif  // CS_NO_CLUSTER_MULTICAST
     // B operand(s): this CTA's bcols rows of N per operand; a second operand
     // (the up projection of gate|up) follows the first, so one N = 2*bn MMA
     // covers both.
@@ -1386,6 +1388,9 @@ __device__ __forceinline__ void push_unit(SmemCtl<NS>* sc, uint32_t q, uint32_t 
 template <int NS, int STAGE_BYTES, int CG, bool ATTN, int CL = CG, int AR = BM>
 __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_constant__ KParams p) {
   static_assert(CL == CG || (CG == 2 && CL == 4 && !ATTN), "unsupported cluster shape");
+#ifdef CS_NO_CLUSTER_MULTICAST
+  static_assert(CL != 4, "the replica build has no 4-CTA multicast tiles");
+#endif
   static_assert(AR == BM || (AR == 8 && CG == 1 && !ATTN), "8-row A tiles are built for single-SM MLP tiles");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));

@@ -200,9 +200,11 @@ __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorM
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster_addr)
       : "memory");
 }
+#ifndef CS_NO_CLUSTER_MULTICAST
 // Multicast load: the box lands at the same shared-memory offset in every CTA
 // of `cta_mask`, and each of them counts the bytes on its own mbarrier at the
-// offset of `bar`.
+// offset of `bar`.  Left out of the replica build (CS_NO_CLUSTER_MULTICAST),
+// the one that processes sharing a node with other GPUs' ranks load.
 __device__ __forceinline__ void tma_load_2d_mc(void* smem_dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
                                                uint16_t cta_mask) {
   asm volatile(
@@ -211,6 +213,7 @@ __device__ __forceinline__ void tma_load_2d_mc(void* smem_dst, const CUtensorMap
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(cta_mask)
       : "memory");
 }
+#endif  // CS_NO_CLUSTER_MULTICAST
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* smem_src, int x, int y) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),

@@ -1,0 +1,119 @@
+// Dependency-ordered dispatch order of a chain's tile units, as a closed form
+// that host and device code share: entry i of a schedule is computed on its
+// own, so a schedule can be written by one thread per entry.
+//
+// Row tiles form groups of group_m.  The fused order takes steps t = 0, 1, ...;
+// at step t, stage s lists every unit of group t - s*lag (column-tile-major
+// inside the group, or row-major), so every producer unit a consumer waits on
+// is listed at an earlier step or earlier in the same step, and an in-order
+// dispatcher cannot deadlock.  A stage alone lists its groups in turn.
+#pragma once
+#include <cstdint>
+
+namespace cs {
+
+struct SchedGeo {
+  int stages = 2;
+  int m_tiles = 1;    // tile rows
+  int group_m = 1;    // tile rows per group
+  int lag = 1;        // groups between consecutive stages
+  int row_major = 0;  // units of a group row by row instead of column by column
+  int n_tiles[3] = {0, 0, 0};
+  int splits[3] = {1, 1, 1};
+};
+
+__host__ __device__ inline uint32_t sched_enc(int s, int m, int n, int ks) {
+  return (static_cast<uint32_t>(s) << 30) | (static_cast<uint32_t>(ks) << 26) | (static_cast<uint32_t>(m) << 14) |
+         static_cast<uint32_t>(n);
+}
+
+__host__ __device__ inline int sched_groups(const SchedGeo& g) { return (g.m_tiles + g.group_m - 1) / g.group_m; }
+
+// tile rows in groups [0, k), k clamped to [0, groups]
+__host__ __device__ inline long long sched_rows_before(const SchedGeo& g, int k) {
+  if (k <= 0) return 0;
+  const long long r = static_cast<long long>(k) * g.group_m;
+  return r < g.m_tiles ? r : g.m_tiles;
+}
+
+// tile rows of group k (0 outside the valid groups)
+__host__ __device__ inline long long sched_rows_of(const SchedGeo& g, int k) {
+  if (k < 0 || k >= sched_groups(g)) return 0;
+  return sched_rows_before(g, k + 1) - sched_rows_before(g, k);
+}
+
+__host__ __device__ inline long long sched_units_per_row(const SchedGeo& g, int s) {
+  return static_cast<long long>(g.n_tiles[s]) * g.splits[s];
+}
+
+// Entries of the fused order before step t.
+__host__ __device__ inline long long sched_fused_before(const SchedGeo& g, int t) {
+  long long o = 0;
+  for (int s = 0; s < g.stages; ++s) o += sched_units_per_row(g, s) * sched_rows_before(g, t - s * g.lag);
+  return o;
+}
+
+__host__ __device__ inline int sched_fused_steps(const SchedGeo& g) { return sched_groups(g) + (g.stages - 1) * g.lag; }
+
+__host__ __device__ inline long long sched_fused_count(const SchedGeo& g) {
+  return sched_fused_before(g, sched_fused_steps(g));
+}
+
+__host__ __device__ inline long long sched_stage_count(const SchedGeo& g, int s) {
+  return sched_units_per_row(g, s) * g.m_tiles;
+}
+
+// Entry j of stage s's units in the group of tile rows [m0, m0 + rows).
+__host__ __device__ inline uint32_t sched_in_group(const SchedGeo& g, int s, int m0, int rows, long long j) {
+  const int sp = g.splits[s];
+  int m, n, ks;
+  if (g.row_major) {
+    const long long per_row = sched_units_per_row(g, s);
+    m = m0 + static_cast<int>(j / per_row);
+    const long long r = j % per_row;
+    n = static_cast<int>(r / sp);
+    ks = static_cast<int>(r % sp);
+  } else {
+    const long long per_col = static_cast<long long>(rows) * sp;
+    n = static_cast<int>(j / per_col);
+    const long long r = j % per_col;
+    m = m0 + static_cast<int>(r / sp);
+    ks = static_cast<int>(r % sp);
+  }
+  return sched_enc(s, m, n, ks);
+}
+
+// Entry i (0 <= i < sched_fused_count) of the fused order.
+__host__ __device__ inline uint32_t sched_fused_entry(const SchedGeo& g, long long i) {
+  // the step holding entry i: the last t with sched_fused_before(t) <= i
+  int lo = 0, hi = sched_fused_steps(g) - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) / 2;
+    if (sched_fused_before(g, mid) <= i)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  const int t = lo;
+  long long j = i - sched_fused_before(g, t);
+  for (int s = 0; s < g.stages; ++s) {
+    const int k = t - s * g.lag;
+    const long long rows = sched_rows_of(g, k);
+    const long long c = rows * sched_units_per_row(g, s);
+    if (j < c) return sched_in_group(g, s, static_cast<int>(sched_rows_before(g, k)), static_cast<int>(rows), j);
+    j -= c;
+  }
+  return 0xFFFFFFFFu;  // i out of range
+}
+
+// Entry i (0 <= i < sched_stage_count) of stage s run alone.
+__host__ __device__ inline uint32_t sched_stage_entry(const SchedGeo& g, int s, long long i) {
+  const long long per_group = static_cast<long long>(g.group_m) * sched_units_per_row(g, s);
+  int k = static_cast<int>(i / per_group);
+  if (k >= sched_groups(g)) k = sched_groups(g) - 1;
+  const long long base = sched_rows_before(g, k) * sched_units_per_row(g, s);
+  return sched_in_group(g, s, static_cast<int>(sched_rows_before(g, k)), static_cast<int>(sched_rows_of(g, k)),
+                        i - base);
+}
+
+}  // namespace cs

@@ -42,7 +42,7 @@
 extern "C" {
 #endif
 
-#define CS_ABI_VERSION 4
+#define CS_ABI_VERSION 5
 
 typedef struct cs_chain_s* cs_chain_t;
 
@@ -288,6 +288,23 @@ typedef struct cs_chain_info {
 
 cs_status cs_chain_query(cs_chain_t plan, cs_chain_info* info);
 
+/* Host-only: the geometry fields of cs_chain_info (stages .. tuned_entry) that
+ * cs_chain_plan would give a plan of this desc on a device of num_sms SMs, with
+ * the loaded tuning table applied; the pointer and semaphore fields are zero.
+ * Needs no GPU. */
+cs_status cs_chain_plan_info(const cs_chain_desc* desc, int num_sms, cs_chain_info* info);
+
+/* What this build of the library contains (bit flags).
+ *  CS_FEATURE_CLUSTER_MULTICAST: 512-row tiles, whose two CTA pairs share every
+ *  weight box by TMA multicast inside a 4-CTA cluster (tile_m = 512, and the
+ *  automatic choice for large M).  The package ships two builds of this ABI:
+ *  libcs_chain.so has it; libcs_chain_nomc.so, the replica build that a process
+ *  sharing a node with other GPUs' ranks loads, is compiled without any
+ *  multicast load, refuses tile_m = 512 (CS_ERR_UNSUPPORTED), ignores
+ *  tuning-table entries that name it and never picks it automatically. */
+#define CS_FEATURE_CLUSTER_MULTICAST 1
+int cs_library_features(void);
+
 /* Host-only: the dispatch order a plan with this desc and grid size would use.
  * Each entry encodes one unit as (stage << 30) | (k_split << 26) | (m_tile << 14) |
  * n_tile, m_tile counting tile_m-row tiles; for an ATTN stage n_tile is the head.  Row blocks are taken in groups of group_m; a
@@ -358,6 +375,21 @@ cs_status cs_chain_debug_skip_release(cs_chain_t plan, int stage, int unit);
  * (M * F * 2 for H and O, M * 3F * 2 for QKV).  For stage-by-stage parity tests. */
 cs_status cs_chain_debug_copy_intermediate(cs_chain_t plan, int which, void* dst, size_t bytes);
 
+/* Enqueue on `stream` a fill of plan-owned scratch with all-ones bytes (NaN as
+ * fp16, bf16 and fp32): which = 0: H or QKV, 1: O, 2: the split-K partial
+ * tiles of every stage, -1: all of them.  A forward overwrites each of them
+ * before any consumer may read it, so a consumer that read a K-slice before
+ * its producer released it would turn its output NaN: the delay-injection
+ * tests fill before every delayed forward. */
+cs_status cs_chain_debug_poison_intermediate(cs_chain_t plan, int which, void* stream);
+
+/* Blocking: set the plan's epoch to `epoch` and every counter to the value it
+ * has after `epoch` forwards, modulo 2^32 (tile semaphores = epoch, row
+ * counters = epoch * tiles per row block, split-K arrival counters = epoch *
+ * splits, and the output counters of desc.out_release alike), so that a test
+ * can run forwards across the 2^32 wrap of the epoch-counted semaphores. */
+cs_status cs_chain_debug_set_epoch(cs_chain_t plan, uint32_t epoch);
+
 /* Allocation-free MLP forward.  The pages have no counterpart to this call.
  *
  * Some callers may not allocate device memory: code running inside another
@@ -371,12 +403,17 @@ cs_status cs_chain_debug_copy_intermediate(cs_chain_t plan, int which, void* dst
  * loads the library holds until the process exits.  It calls no cudaMalloc,
  * cudaFree or other allocating routine.
  *
- * desc: as for cs_chain_plan (kind MLP_GELU or MLP_SWIGLU).  args and stream: as
- * for cs_mlp_forward; the caller still owns and passes X, the weights, b1 and Y.
+ * desc: as for cs_chain_plan (kind MLP_GELU or MLP_SWIGLU), except that tiles
+ * are never split along K (split_k 0 runs unsplit tiles; split_k > 1 is refused
+ * with CS_ERR_UNSUPPORTED), the tuning table is not consulted (policy AUTO runs
+ * TILE) and out_release is refused.  args and stream: as for cs_mlp_forward;
+ * the caller still owns and passes X, the weights, b1 and Y.
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
- * capture.  Each call clears the semaphores and counters it needs, so results
- * never depend on an earlier call, but the array is shared by every call on the
+ * capture.  Every call then enqueues two kernels on `stream`: a small one that
+ * clears the semaphores and counters and writes the schedule into the array
+ * (nothing is copied from host memory), and the chain.  So results never
+ * depend on an earlier call, but the array is shared by every call on the
  * device: calls that overlap on the GPU (other streams, other threads) race
  * and must not be issued.  A shape whose intermediate, semaphores and schedule
  * need more than the array holds is rejected with CS_ERR_INVALID_ARG before any

@@ -33,7 +33,7 @@ def test_every_declared_symbol_is_exported(cs):
     for n in names:
         assert hasattr(lib, n), f"{n} declared in cs_chain.h but not exported"
     assert set(cs.chain.EXPORTED) == set(names)
-    assert cs.cs_abi_version() == 4
+    assert cs.cs_abi_version() == 5
 
 
 def test_desc_defaults(cs):
@@ -202,3 +202,41 @@ def test_the_abi_from_plain_c99(cs, tmp_path):
                     f"-Wl,-rpath,{libdir}"], check=True)
     p = subprocess.run([exe, cs.chain.TUNE_TABLE], capture_output=True, text=True, timeout=60)
     assert p.returncode == 0 and p.stdout.strip() == "ok", p.stderr
+
+
+def _loop_order(stages, m_tiles, group_m, lag, n_tiles, splits, row_major):
+    """The fused dispatch order written as nested loops (steps, stages, a
+    group's tiles), independently of the library's closed form."""
+    groups = -(-m_tiles // group_m)
+    out = []
+    for t in range(groups + (stages - 1) * lag):
+        for s in range(stages):
+            g = t - s * lag
+            if not 0 <= g < groups:
+                continue
+            rows = range(g * group_m, min(m_tiles, (g + 1) * group_m))
+            if row_major:
+                out += [(s, m, n, k) for m in rows for n in range(n_tiles[s]) for k in range(splits[s])]
+            else:
+                out += [(s, m, n, k) for n in range(n_tiles[s]) for m in rows for k in range(splits[s])]
+    return out
+
+
+@pytest.mark.parametrize("kind,M,H,F,lag,group,split,tile_m,raster", [
+    ("gelu", 2048, 12288, 6144, -1, 0, 0, 0, 0), ("gelu", 1, 12288, 6144, -1, 0, 0, 0, 0),
+    ("gelu", 1000, 8192, 2752, 2, 1, 2, 128, 1), ("gelu", 1536, 8192, 8192, 5, 5, 1, 256, 2),
+    ("swiglu", 777, 8192, 2752, 0, 3, 3, 128, 2), ("gelu", 130000, 256, 512, 3, 7, 1, 128, 1),
+    ("attn", 2048, 12288, 1536, -1, 0, 0, 256, 0), ("attn", 300, 12288, 1536, 2, 1, 0, 128, 2)])
+def test_closed_form_schedule_equals_the_loop_order(cs, kind, M, H, F, lag, group, split, tile_m, raster):
+    """The schedule entries are computed one by one from a closed form (so the
+    allocation-free forward can write them on the device, one thread each):
+    they must equal the nested-loop order entry for entry."""
+    extra = dict(heads=F // 128, head_dim=128) if kind == "attn" else {}
+    d = cs.cs_chain_desc_init(kind=kind, M=M, H=H, F=F, lag=lag, group_m=group, split_k=split, tile_m=tile_m,
+                              raster=raster, weight_layout="nk", tuned=-1, **extra)
+    q = cs.cs_chain_plan_info(d, 152)
+    m_tiles = -(-M // q["tile_m"])
+    want = _loop_order(q["stages"], m_tiles, q["group_m"], q["lag"], q["n_tiles"], q["split_k"], raster == 2)
+    got = [cs.decode_unit(u) for u in cs.cs_schedule_build(d, 152)]
+    assert got == [(s, m, n, k) for s, m, n, k in want]
+    assert q["n_units"] == len(got)

@@ -65,10 +65,14 @@ def test_attention_policies_bit_identical_and_flags(tile_m):
 
 @pytest.mark.parametrize("tile_m", [128, 256])
 def test_attention_delay_injection_never_changes_a_bit(tile_m):
+    """Random delays before the QKV tiles' and the attention units' releases,
+    QKV and O poisoned with NaN before every forward: an attention unit that
+    read a QKV row block, or a Wo tile that read an O block, before it was
+    released would turn Y NaN."""
     inp = cs_inputs.make_custom("attn", 400, 512, 384, seed=33)
     dev = device_tensors(inp, "nk")
     ref = None
-    for pol in ("row", "tile"):
+    for pol in ("row", "tile", "strided"):
         with plan_for(inp, pol, "nk", group_m=1, tile_m=tile_m) as plan:
             q = cs.cs_chain_query(plan)
             for seed in range(2):
@@ -76,10 +80,56 @@ def test_attention_delay_injection_never_changes_a_bit(tile_m):
                 for stage in (0, 1):
                     d = (torch.rand(q["units"][stage], generator=g) * 200_000).to(torch.int64).tolist()
                     cs.cs_chain_debug_set_delays(plan, stage, d)
+                cs.cs_chain_debug_poison_intermediate(plan, -1)
                 Y = forward(plan, dev).cpu()
+                assert not torch.isnan(Y).any(), (pol, seed)
                 if ref is None:
                     ref = Y
+                    Yref, _, _ = _oracle(inp)
+                    assert oracle.rel_err(Y, Yref) <= TOL
                 assert torch.equal(Y, ref), (pol, seed)
+
+
+@pytest.mark.parametrize("tile_m", [128, 256])
+def test_attention_poison_reaches_stages_run_without_producers(tile_m):
+    """Positive control of the poisoned attention tests: run alone after a
+    poison, the attention stage reads NaN QKV and the Wo stage NaN O."""
+    inp = cs_inputs.make_custom("attn", 300, 512, 256, seed=35)
+    dev = device_tensors(inp, "nk")
+    with plan_for(inp, "row", "nk", tile_m=tile_m) as plan:
+        good = forward(plan, dev).cpu()
+        Y = torch.zeros_like(dev["X"])
+        cs.cs_chain_debug_poison_intermediate(plan, 0)
+        cs.cs_chain_forward_stage(plan, 1, Y=Y, **dev)  # attention from poisoned QKV
+        O = intermediate(plan, 1, inp.M, inp.F, inp.dtype).cpu()
+        assert torch.isnan(O).all()
+        cs.cs_chain_debug_poison_intermediate(plan, 1)
+        cs.cs_chain_forward_stage(plan, 2, Y=Y, **dev)  # Wo from poisoned O
+        torch.cuda.synchronize()
+        assert torch.isnan(Y.cpu()).all()
+        assert torch.equal(forward(plan, dev).cpu(), good)
+
+
+@pytest.mark.parametrize("tile_m", [128, 256])
+@pytest.mark.parametrize("policy", ["row", "tile", "stream"])
+def test_attention_epoch_counters_wrap(policy, tile_m):
+    """Both boundaries' counters (and the output's) across the 2^32 wrap."""
+    inp = cs_inputs.make_custom("attn", 300, 512, 256, seed=36)
+    dev = device_tensors(inp, "nk")
+    with plan_for(inp, policy, "nk", tile_m=tile_m, out_release=1) as fresh:
+        ref = forward(fresh, dev).cpu()
+    with plan_for(inp, policy, "nk", tile_m=tile_m, out_release=1) as plan:
+        q = cs.cs_chain_query(plan)
+        start = 0xFFFFFFFF
+        cs.cs_chain_debug_set_epoch(plan, start)
+        for i in range(1, 4):
+            cs.cs_chain_debug_poison_intermediate(plan, -1)
+            assert torch.equal(forward(plan, dev).cpu(), ref), i
+            e = (start + i) & 0xFFFFFFFF
+            for b in (0, 1, 2):
+                tiles, rows, epoch = cs.cs_chain_debug_read_sems(plan, b)
+                assert epoch == e and all(v == e for r in tiles for v in r), (i, b)
+                assert rows == [(e * q["n_tiles"][b]) & 0xFFFFFFFF] * q["m_tiles"], (i, b)
 
 
 @pytest.mark.parametrize("tile_m", [128, 256])

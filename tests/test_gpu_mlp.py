@@ -112,8 +112,37 @@ def test_policies_and_control_keep_flags_consistent():
             assert epoch == 3 and all(v == 3 for r in tiles for v in r) and rows == [3 * 4] * 2
 
 
+def poisoned_forward(plan, dev, Y=None):
+    """A forward whose plan-owned intermediate (and split-K partials) hold NaN
+    when it starts: every element a consumer reads before its producer has
+    stored and released it is NaN, and NaN reaches the output through the
+    MMA, so one premature read anywhere turns Y NaN."""
+    cs.cs_chain_debug_poison_intermediate(plan, -1)
+    Y = forward(plan, dev, Y)
+    return Y
+
+
+def test_poison_reaches_a_consumer_that_reads_without_its_producer():
+    """The positive control of the poisoned delay tests: the consumer stage run
+    alone after a poison (no producer in between) reads NaN and writes NaN."""
+    inp = cs_inputs.make_custom("gelu", 300, 512, 1024, seed=12)
+    dev = device_tensors(inp)
+    with plan_for(inp, "tile") as plan:
+        good = forward(plan, dev).cpu()
+        assert not torch.isnan(good).any()
+        cs.cs_chain_debug_poison_intermediate(plan, 0)
+        Y = torch.zeros_like(dev["X"])
+        cs.cs_chain_forward_stage(plan, 1, Y=Y, **dev)
+        torch.cuda.synchronize()
+        assert torch.isnan(Y.cpu()).all(dim=1).all()  # every row read poisoned K-slices
+        assert torch.equal(poisoned_forward(plan, dev).cpu(), good)
+
+
 @pytest.mark.parametrize("tile_m,tile_n", TILES)
 def test_delay_injection_never_changes_a_bit(tile_m, tile_n):
+    """Random producer delays (up to 200 us) before each release, the
+    intermediate poisoned before every forward: a consumer that loaded any
+    K-slice before its producer tile was released would produce NaN."""
     inp = cs_inputs.make_custom("gelu", 640, 1024, 2048, seed=8)
     dev = device_tensors(inp)
     ref = None
@@ -124,7 +153,8 @@ def test_delay_injection_never_changes_a_bit(tile_m, tile_n):
                 g = torch.Generator().manual_seed(100 + seed)
                 delays = (torch.rand(q["units"][0], generator=g) * 200_000).to(torch.int64).tolist()
                 cs.cs_chain_debug_set_delays(plan, 0, delays)
-                Y = forward(plan, dev).cpu()
+                Y = poisoned_forward(plan, dev).cpu()
+                assert not torch.isnan(Y).any(), (pol, seed)
                 if ref is None:
                     ref = Y
                     Yref, _ = _oracle(inp)
@@ -133,6 +163,35 @@ def test_delay_injection_never_changes_a_bit(tile_m, tile_n):
             cs.cs_chain_debug_set_delays(plan, 0, None)
             tiles, rows, epoch = cs.cs_chain_debug_read_sems(plan, 0)
             assert epoch == 3 and all(v == 3 for r in tiles for v in r)
+
+
+@pytest.mark.parametrize("tile_m,tile_n,split", [(128, 128, 1), (256, 256, 2), (512, 256, 1), (128, 256, 3)])
+@pytest.mark.parametrize("policy", ["tile", "row", "strided", "stream"])
+def test_epoch_counters_wrap_at_two_to_the_32(policy, tile_m, tile_n, split):
+    """Semaphores are epoch-counted and never reset: a forward waits for
+    counts of epoch + 1 (times the tiles per row block, or the splits per tile),
+    compared modulo 2^32.  Seeded two forwards before the wrap, four forwards
+    (with the output released per tile too) cross it: every counter ends at its
+    expected value modulo 2^32 and every output has the bits of a fresh plan."""
+    inp = cs_inputs.make_custom("gelu", 520, 2048, 1280, seed=13)
+    dev = device_tensors(inp, "nk")
+    kw = dict(tile_m=tile_m, tile_n=tile_n, split_k=split, out_release=1)
+    with plan_for(inp, policy, "nk", **kw) as fresh:
+        ref = forward(fresh, dev).cpu()
+    with plan_for(inp, policy, "nk", **kw) as plan:
+        q = cs.cs_chain_query(plan)
+        assert q["split_k"][0] == split
+        start = 0xFFFFFFFE
+        cs.cs_chain_debug_set_epoch(plan, start)
+        for i in range(1, 5):
+            Y = poisoned_forward(plan, dev).cpu()
+            assert torch.equal(Y, ref), i
+            e = (start + i) & 0xFFFFFFFF
+            for b in (0, 1):  # the intermediate's counters, then the output's
+                tiles, rows, epoch = cs.cs_chain_debug_read_sems(plan, b)
+                assert epoch == e
+                assert all(v == e for r in tiles for v in r), (i, b)
+                assert rows == [(e * q["n_tiles"][b]) & 0xFFFFFFFF] * q["m_tiles"], (i, b)
 
 
 @pytest.mark.parametrize("tile_m,tile_n", TILES)
@@ -309,7 +368,7 @@ def test_split_k_delay_injection_never_changes_a_bit():
         for seed in range(3):
             g = torch.Generator().manual_seed(300 + seed)
             cs.cs_chain_debug_set_delays(plan, 0, (torch.rand(q["units"][0], generator=g) * 100_000).long().tolist())
-            assert torch.equal(forward(plan, dev).cpu(), ref), seed
+            assert torch.equal(poisoned_forward(plan, dev).cpu(), ref), seed
 
 
 @pytest.mark.parametrize("policy", ["tile", "stream"])
@@ -375,7 +434,7 @@ def test_up_to_eight_rows_use_one_a_row_group(M, layout, kind, tile_n):
             if pol == "tile":
                 g = torch.Generator().manual_seed(60)
                 cs.cs_chain_debug_set_delays(plan, 0, (torch.rand(q["units"][0], generator=g) * 100_000).long().tolist())
-                assert torch.equal(forward(plan, dev).cpu(), outs[pol])
+                assert torch.equal(poisoned_forward(plan, dev).cpu(), outs[pol])
     Yref, _ = _oracle(inp)
     assert oracle.rel_err(outs["tile"], Yref) <= TOL
     for k, v in outs.items():
@@ -405,3 +464,45 @@ def test_host_memory_forward_matches_device_forward(kind):
             assert torch.equal(y, r)
         with pytest.raises(ValueError):
             cs.cs_mlp_forward_host(plan, X=xs[0].cuda(), Y=ys[0], **wts)
+
+
+REPLICA_CHECK = r"""
+import sys, torch
+sys.path.insert(0, sys.argv[1])
+import consumer_gemm_chain_gb300 as cs, cs_inputs, oracle
+from tests.gpu_util import device_tensors, forward, plan_for
+assert cs.chain.LIB_PATH.endswith("libcs_chain_nomc.so"), cs.chain.LIB_PATH
+assert cs.cs_library_features() & cs.CS_FEATURE_CLUSTER_MULTICAST == 0
+inp = cs_inputs.make_custom("gelu", 1024, 512, 1024, seed=14)
+dev = device_tensors(inp, "nk")
+with plan_for(inp, "tile", "nk") as plan:
+    tm = cs.cs_chain_query(plan)["tile_m"]
+    Y = forward(plan, dev).cpu()
+try:
+    plan_for(inp, "tile", "nk", tile_m=512, tile_n=256)
+    raise SystemExit("tile_m=512 accepted")
+except cs.CSError as e:
+    assert e.status == cs.CS_ERR_UNSUPPORTED
+Yref = oracle.mlp_gelu(inp.X, inp.W1, inp.b1, inp.W2)
+print(tm, oracle.rel_err(Y, Yref))
+"""
+
+
+def test_replica_build_runs_the_chain_without_multicast():
+    """The replica build (no TMA cluster multicast; what N-rank processes load)
+    in a process of its own: the shape that takes 512-row 4-CTA tiles in the
+    full build runs on 256-row pairs there, matches the oracle, and an explicit
+    tile_m = 512 is refused."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, CS_CHAIN_LIBRARY="nomc")
+    p = subprocess.run([sys.executable, "-c", REPLICA_CHECK, root], cwd=root, env=env, capture_output=True,
+                       text=True, timeout=600)
+    assert p.returncode == 0, p.stderr[-3000:]
+    tm, err = p.stdout.split()[-2:]
+    assert int(tm) == 256
+    assert float(err) <= TOL
+    full = cs.cs_chain_desc_init(kind="gelu", M=1024, H=512, F=1024, weight_layout="nk", tuned=-1)
+    assert cs.cs_chain_plan_info(full, 152)["tile_m"] == 512  # this process: the full build

@@ -13,6 +13,7 @@ import os
 import socket
 import subprocess
 import sys
+import types
 
 import pytest
 import torch.distributed as dist
@@ -63,14 +64,73 @@ def test_whole_job_throughput_is_linear_in_ranks_at_fixed_step_time():
     assert bench.whole_job_tflops(1.0e12, 4.0, 8) == pytest.approx(8 * one)
 
 
-@pytest.mark.parametrize("kind,M,tile_m,expect", [
-    ("gelu", 2048, 0, 256), ("gelu", 2048, 512, 256), ("gelu", 512, 0, 128),
-    ("swiglu", 2048, 0, 128), ("swiglu", 2048, 512, 128), ("gelu", 2048, 128, 128),
-    ("gelu", 2048, 256, 256)])
-def test_replicas_use_no_cluster_multicast(kind, M, tile_m, expect):
-    assert bench.replica_tile_m(2, tile_m, kind, M) == expect
-    # one rank keeps whatever was asked, multicast tiles included
-    assert bench.replica_tile_m(1, tile_m, kind, M) == tile_m
+def _replica_rank(rank, ws, port, out):
+    """One rank of an N-rank bench run, up to its plans: the environment torchrun
+    gives it, then the binding (which picks the library build from WORLD_SIZE),
+    then every plan desc the bench makes with ws ranks, resolved host-side."""
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(ws), LOCAL_RANK=str(rank))
+    os.environ.pop("CS_CHAIN_LIBRARY", None)
+    got_ws, _, _ = bench.dist_setup(argparse.Namespace(impl="reference"))  # gloo: no GPU here
+    try:
+        import cs_inputs
+        import consumer_gemm_chain_gb300 as cs
+        bench.check_replica_library(cs, got_ws)
+        rec = {"lib": os.path.basename(cs.chain.LIB_PATH), "features": cs.cs_library_features(),
+               "extras": bench.runs_extras(got_ws, False), "plans": [], "refused": []}
+        cs.cs_tune_load()  # the bench's default: the shipped table, whose entries may name 512-row tiles
+        for workload in ("gpt3", "llama", "stress", "tiny"):
+            for M in sorted({cs_inputs.WORKLOADS[workload][4], 512, 1024, 2048}):
+                for extra in ([], ["--tile-m", "512"], ["--tile-m", "256"], ["--policy", "stream"]):
+                    args = bench.parse(["--workload", workload, "--M", str(M), "--gpus", str(got_ws)] + extra)
+                    kind, H, F, dtype, _ = cs_inputs.WORKLOADS[workload]
+                    inp = types.SimpleNamespace(kind=kind, H=H, F=F, dtype=dtype)
+                    desc = bench.plan_desc(cs, args, inp, args.policy, M)
+                    try:
+                        q = cs.cs_chain_plan_info(desc, 152)
+                        rec["plans"].append((workload, M, tuple(extra), q["tile_m"]))
+                    except cs.CSError as e:
+                        rec["refused"].append((workload, M, tuple(extra), e.status))
+        out.put((rank, rec))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_replica_ranks_load_the_build_without_cluster_multicast():
+    import __graft_entry__
+    __graft_entry__._build_module().build()
+    ws = 2
+    ctx = mp.get_context("spawn")
+    out = ctx.SimpleQueue()
+    mp.start_processes(_replica_rank, args=(ws, _free_port(), out), nprocs=ws, start_method="spawn", join=True)
+    res = dict(out.get() for _ in range(ws))
+    assert sorted(res) == [0, 1]
+    for rank, rec in res.items():
+        assert rec["lib"] == "libcs_chain_nomc.so", rec["lib"]
+        assert rec["features"] & 1 == 0  # CS_FEATURE_CLUSTER_MULTICAST
+        assert rec["extras"] is False  # an N-rank run makes the headline plan only
+        assert rec["plans"], "no plan resolved"
+        # no plan of any workload resolves to 512-row (4-CTA multicast) tiles ...
+        assert all(tm in (128, 256) for *_, tm in rec["plans"]), rec["plans"]
+        # ... and asking for them is refused by the library, not silently changed
+        assert rec["refused"] and all(extra == ("--tile-m", "512") and st == 2 for _, _, extra, st in rec["refused"])
+        assert len(rec["refused"]) == len({(w, m) for w, m, _, _ in rec["plans"]})
+
+
+def test_one_gpu_loads_the_full_build_and_keeps_its_tiles():
+    import consumer_gemm_chain_gb300 as cs
+    assert cs.chain.library_path({"WORLD_SIZE": "1"}).endswith("libcs_chain.so")
+    assert cs.chain.library_path({}).endswith("libcs_chain.so")
+    assert cs.chain.library_path({"WORLD_SIZE": "8"}).endswith("libcs_chain_nomc.so")
+    assert cs.chain.library_path({"WORLD_SIZE": "8", "CS_CHAIN_LIBRARY": "full"}).endswith("libcs_chain.so")
+    assert cs.chain.library_path({"CS_CHAIN_LIBRARY": "nomc"}).endswith("libcs_chain_nomc.so")
+    with pytest.raises(ImportError):
+        cs.chain.library_path({"CS_CHAIN_LIBRARY": "other"})
+    assert bench.runs_extras(1, False) and not bench.runs_extras(1, True)
+    if os.path.basename(cs.chain.LIB_PATH) == "libcs_chain.so":
+        assert cs.cs_library_features() & cs.CS_FEATURE_CLUSTER_MULTICAST
+        d = cs.cs_chain_desc_init(kind="gelu", M=2048, H=12288, F=6144, weight_layout="nk", tuned=-1)
+        assert cs.cs_chain_plan_info(d, 152)["tile_m"] == 512
 
 
 def test_reference_arm_under_torchrun_prints_one_line_from_rank_zero():

@@ -12,9 +12,11 @@ import os
 
 import pytest
 
-hyp = pytest.importorskip("hypothesis")
-from hypothesis import HealthCheck, given, settings  # noqa: E402
-from hypothesis import strategies as st  # noqa: E402
+try:
+    from hypothesis import HealthCheck, given, settings
+    from hypothesis import strategies as st
+except ImportError:  # the property tests need hypothesis; the plain tests below run without it
+    given = None
 
 
 @pytest.fixture(scope="module")
@@ -24,8 +26,6 @@ def cs():
     import consumer_gemm_chain_gb300 as cs
     return cs
 
-
-SETTINGS = settings(max_examples=300, deadline=None, suppress_health_check=[HealthCheck.function_scoped_fixture])
 
 BASE = {"kind": "gelu", "dtype": "f16", "H": 12288, "F": 6144, "M": 64, "sms": 152,
         "tile_m": 128, "tile_n": 128, "split_k": 1}
@@ -37,64 +37,72 @@ def _load_text(cs, tmp_path, text: bytes):
     return cs.cs_tune_load(str(p))
 
 
-@SETTINGS
-@given(st.binary(max_size=400))
-def test_random_bytes_never_crash(cs, tmp_path, data):
-    cs.cs_tune_clear()
-    try:
-        n = _load_text(cs, tmp_path, data)
-    except cs.CSError as e:
-        assert e.status == cs.CS_ERR_INVALID_ARG and str(e)
-        assert cs.cs_tune_size() == 0
-    else:  # only a well-formed table with an empty entry list can come out of noise
-        assert n == cs.cs_tune_size()
+if given is not None:
+    SETTINGS = settings(max_examples=300, deadline=None, suppress_health_check=[HealthCheck.function_scoped_fixture])
+
+    @SETTINGS
+    @given(st.binary(max_size=400))
+    def test_random_bytes_never_crash(cs, tmp_path, data):
+        cs.cs_tune_clear()
+        try:
+            n = _load_text(cs, tmp_path, data)
+        except cs.CSError as e:
+            assert e.status == cs.CS_ERR_INVALID_ARG and str(e)
+            assert cs.cs_tune_size() == 0
+        else:  # only a well-formed table with an empty entry list can come out of noise
+            assert n == cs.cs_tune_size()
 
 
-json_scalars = st.none() | st.booleans() | st.integers(-10**6, 10**6) | st.floats(allow_nan=False, allow_infinity=False) \
-    | st.text(max_size=12)
-json_values = st.recursive(json_scalars, lambda c: st.lists(c, max_size=4) | st.dictionaries(st.text(max_size=6), c, max_size=4),
-                           max_leaves=20)
+    json_scalars = st.none() | st.booleans() | st.integers(-10**6, 10**6) | st.floats(allow_nan=False, allow_infinity=False) \
+        | st.text(max_size=12)
+    json_values = st.recursive(json_scalars, lambda c: st.lists(c, max_size=4) | st.dictionaries(st.text(max_size=6), c, max_size=4),
+                               max_leaves=20)
 
 
-@SETTINGS
-@given(extra=st.dictionaries(st.text(max_size=8), json_values, max_size=4), ws=st.sampled_from(["", " ", "\n\t", "  \r\n"]))
-def test_valid_tables_with_unknown_keys_load(cs, tmp_path, extra, ws):
-    entry = dict(extra)
-    entry.update(BASE)  # the required fields win over random ones of the same name
-    doc = {"format": "cs_chain_tuning", "version": 1, "entries": [entry, dict(BASE, M=128)], "notes": extra}
-    text = json.dumps(doc, indent=1 if ws else None).replace("\n", "\n" + ws)
-    assert _load_text(cs, tmp_path, text.encode()) == 2
-    cs.cs_tune_clear()
+    @SETTINGS
+    @given(extra=st.dictionaries(st.text(max_size=8), json_values, max_size=4), ws=st.sampled_from(["", " ", "\n\t", "  \r\n"]))
+    def test_valid_tables_with_unknown_keys_load(cs, tmp_path, extra, ws):
+        entry = dict(extra)
+        entry.update(BASE)  # the required fields win over random ones of the same name
+        doc = {"format": "cs_chain_tuning", "version": 1, "entries": [entry, dict(BASE, M=128)], "notes": extra}
+        text = json.dumps(doc, indent=1 if ws else None).replace("\n", "\n" + ws)
+        assert _load_text(cs, tmp_path, text.encode()) == 2
+        cs.cs_tune_clear()
 
 
-@SETTINGS
-@given(field=st.sampled_from(sorted(BASE)), value=json_values)
-def test_random_field_values_load_or_name_the_field(cs, tmp_path, field, value):
-    cs.cs_tune_clear()
-    keep = {"format": "cs_chain_tuning", "version": 1, "entries": [BASE]}
-    assert _load_text(cs, tmp_path, json.dumps(keep).encode()) == 1
-    entry = dict(BASE)
-    entry[field] = value
-    doc = {"format": "cs_chain_tuning", "version": 1, "entries": [entry]}
-    try:
-        n = _load_text(cs, tmp_path, json.dumps(doc).encode())
-    except cs.CSError as e:
-        assert e.status == cs.CS_ERR_INVALID_ARG and f'"{field}"' in str(e)
-        assert cs.cs_tune_size() == 1  # the earlier table stays
-    else:
-        assert n == 1
-    cs.cs_tune_clear()
+    @SETTINGS
+    @given(field=st.sampled_from(sorted(BASE)), value=json_values)
+    def test_random_field_values_load_or_name_the_field(cs, tmp_path, field, value):
+        cs.cs_tune_clear()
+        keep = {"format": "cs_chain_tuning", "version": 1, "entries": [BASE]}
+        assert _load_text(cs, tmp_path, json.dumps(keep).encode()) == 1
+        entry = dict(BASE)
+        entry[field] = value
+        doc = {"format": "cs_chain_tuning", "version": 1, "entries": [entry]}
+        try:
+            n = _load_text(cs, tmp_path, json.dumps(doc).encode())
+        except cs.CSError as e:
+            assert e.status == cs.CS_ERR_INVALID_ARG and f'"{field}"' in str(e)
+            assert cs.cs_tune_size() == 1  # the earlier table stays
+        else:
+            assert n == 1
+        cs.cs_tune_clear()
 
 
-@SETTINGS
-@given(cut=st.integers(0, 200))
-def test_truncated_files_are_refused(cs, tmp_path, cut):
-    cs.cs_tune_clear()
-    text = json.dumps({"format": "cs_chain_tuning", "version": 1, "entries": [BASE, dict(BASE, M=2)]})
-    cut = min(cut, len(text) - 1)
-    with pytest.raises(cs.CSError) as e:
-        _load_text(cs, tmp_path, text[:cut].encode())
-    assert e.value.status == cs.CS_ERR_INVALID_ARG
+    @SETTINGS
+    @given(cut=st.integers(0, 200))
+    def test_truncated_files_are_refused(cs, tmp_path, cut):
+        cs.cs_tune_clear()
+        text = json.dumps({"format": "cs_chain_tuning", "version": 1, "entries": [BASE, dict(BASE, M=2)]})
+        cut = min(cut, len(text) - 1)
+        with pytest.raises(cs.CSError) as e:
+            _load_text(cs, tmp_path, text[:cut].encode())
+        assert e.value.status == cs.CS_ERR_INVALID_ARG
+
+else:
+    @pytest.mark.skip(reason="hypothesis is not installed")
+    def test_property_tests_need_hypothesis():
+        pass
 
 
 def test_deep_nesting_is_refused_not_overflowed(cs, tmp_path):

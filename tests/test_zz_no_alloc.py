@@ -7,7 +7,8 @@ cudaFree would synchronise the device.  It keeps its intermediate, semaphores
 and schedule in a fixed array inside the library instead of a plan.  Each test
 runs it twice in a row (the array keeps the previous call's contents, which the
 second call must not depend on) and compares Y with cs_chain_plan +
-cs_mlp_forward within the parity tolerance the other GPU tests use.  This file
+cs_mlp_forward (unsplit, like the allocation-free forward) and with the fp64
+oracle, within the parity tolerance the other GPU tests use.  This file
 runs last, and also passes on its own in a fresh process.
 """
 from __future__ import annotations
@@ -40,8 +41,13 @@ def _desc(inp, layout, policy):
 def test_noalloc_matches_planned_forward_twice(kind, M, H, F, layout, policy):
     inp = cs_inputs.make_custom(kind, M, H, F, dtype=torch.float16, seed=41)
     dev = device_tensors(inp, layout)
-    with plan_for(inp, policy, layout) as plan:
+    with plan_for(inp, policy, layout, split_k=1) as plan:
         ref = forward(plan, dev).cpu()
+    if kind == "gelu":
+        truth = oracle.mlp_gelu(inp.X, inp.W1, inp.b1, inp.W2)
+    else:
+        truth = oracle.mlp_swiglu(inp.X, inp.Wg, inp.Wu, inp.W2)
+    assert oracle.rel_err(ref, truth) <= TOL
     desc = _desc(inp, layout, policy)
     for call in range(2):
         Y = torch.full_like(dev["X"], float("nan"))
@@ -50,7 +56,19 @@ def test_noalloc_matches_planned_forward_twice(kind, M, H, F, layout, policy):
         assert cs.cs_noalloc_status() == cs.CS_OK, cs.cs_last_error_string()
         Yc = Y.cpu()
         assert not torch.isnan(Yc).any(), call
-        assert oracle.rel_err(Yc, ref) <= TOL, call
+        assert oracle.rel_err(Yc, ref) <= TOL, call   # against the planned forward
+        assert oracle.rel_err(Yc, truth) <= TOL, call  # and against the fp64 oracle
+
+
+def test_noalloc_refuses_k_splits():
+    """The array holds no split-K workspace: split_k > 1 is refused, not ignored."""
+    inp = cs_inputs.make_custom("gelu", 64, 256, 512, dtype=torch.float16, seed=42)
+    dev = device_tensors(inp, "nk")
+    desc = _desc(inp, "nk", "tile")
+    desc.split_k = 2
+    with pytest.raises(cs.CSError) as e:
+        cs.cs_mlp_forward_noalloc(desc, Y=torch.empty_like(dev["X"]), **dev)
+    assert e.value.status == cs.CS_ERR_UNSUPPORTED
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
