@@ -21,7 +21,7 @@ LIB_NOMC = os.path.join(LIBDIR, "libcs_chain_nomc.so")
 # (library, extra nvcc defines)
 VARIANTS = ((LIB, []), (LIB_NOMC, ["-DCS_NO_CLUSTER_MULTICAST"]))
 SOURCES = ["cs_chain.cu", "cs_tune.cpp"]
-DEPS = ["cs_chain.cu", "cs_kernel.cuh", "cs_ptx.cuh", "cs_tune.cpp", "cs_tune.h"]
+DEPS = ["cs_chain.cu", "cs_kernel.cuh", "cs_ptx.cuh", "cs_sched.cuh", "cs_tune.cpp", "cs_tune.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

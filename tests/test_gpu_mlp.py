@@ -491,8 +491,8 @@ print(tm, oracle.rel_err(Y, Yref))
 def test_replica_build_runs_the_chain_without_multicast():
     """The replica build (no TMA cluster multicast; what N-rank processes load)
     in a process of its own: the shape that takes 512-row 4-CTA tiles in the
-    full build runs on 256-row pairs there, matches the oracle, and an explicit
-    tile_m = 512 is refused."""
+    full build runs on single-SM or 256-row pair tiles there, matches the
+    oracle, and an explicit tile_m = 512 is refused."""
     import os
     import subprocess
     import sys
@@ -502,7 +502,7 @@ def test_replica_build_runs_the_chain_without_multicast():
                        text=True, timeout=600)
     assert p.returncode == 0, p.stderr[-3000:]
     tm, err = p.stdout.split()[-2:]
-    assert int(tm) == 256
+    assert int(tm) in (128, 256)
     assert float(err) <= TOL
     full = cs.cs_chain_desc_init(kind="gelu", M=1024, H=512, F=1024, weight_layout="nk", tuned=-1)
     assert cs.cs_chain_plan_info(full, 152)["tile_m"] == 512  # this process: the full build
