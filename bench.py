@@ -679,6 +679,84 @@ def solo_vs_cublas(cs, torch, plan, info, dev, Y, inp, lay, stage):
         raise SystemExit(1)
 
 
+def _union_len(iv, lo=None, hi=None):
+    """Length of the union of intervals iv, clipped to [lo, hi]."""
+    total, cur = 0, None
+    for a, b in sorted(iv):
+        if lo is not None:
+            a, b = max(a, lo), min(b, hi)
+            if b <= a:
+                continue
+        if cur is None or a > cur[1]:
+            if cur is not None:
+                total += cur[1] - cur[0]
+            cur = [a, b]
+        else:
+            cur[1] = max(cur[1], b)
+    return total + (cur[1] - cur[0] if cur else 0)
+
+
+def sm_busy_stats(recs, n_sm):
+    """Tensor-pipe occupancy of one kernel launch from its trace records (8
+    integers: unit | index << 32, SM | ..., then ns at claim, dependencies
+    published, first TMA load, last TMA load, accumulator complete, epilogue
+    done).  An SM counts as busy while one of its units is between its first
+    load and its accumulator (the mainloop: the span in which its MMAs run).
+    The tail is the window from the moment the first SM has finished the
+    mainloop of its last unit to the end of the launch: the last wave, in which
+    SMs fall idle while others still work."""
+    per_sm = {}
+    t0 = min(r[2] for r in recs if r[2])
+    t1 = max(r[7] for r in recs if r[7])
+    for r in recs:
+        if r[4] and r[6]:
+            per_sm.setdefault(r[1] & 0xFFFF, []).append((r[4], r[6]))
+    span = t1 - t0
+    busy = sum(_union_len(iv) for iv in per_sm.values())
+    # SMs without any unit are idle from the start
+    last = [max(b for _, b in iv) for iv in per_sm.values()] + [t0] * max(0, n_sm - len(per_sm))
+    tail0 = min(last)
+    tail = t1 - tail0
+    tail_busy = sum(_union_len(iv, tail0, t1) for iv in per_sm.values())
+    return {"span_us": span / 1e3, "busy_frac": busy / (n_sm * span) if span else None,
+            "idle_sm_us": (n_sm * span - busy) / 1e3, "tail_us": tail / 1e3,
+            "tail_busy_frac": tail_busy / (n_sm * tail) if tail > 0 else None,
+            "tail_idle_sm_us": (n_sm * tail - tail_busy) / 1e3, "sms_used": len(per_sm), "t_start": t0, "t_end": t1}
+
+
+def traced_forward(cs, torch, plan, fwd):
+    """Trace records of one forward of `plan` (fwd runs it)."""
+    cs.cs_chain_debug_trace(plan, True)
+    fwd()
+    torch.cuda.synchronize()
+    recs = cs.cs_chain_debug_read_trace(plan)
+    cs.cs_chain_debug_trace(plan, False)
+    return recs
+
+
+def tail_stats(cs, torch, plan, fwd):
+    """SM occupancy of one traced forward: per launch (one for a fused policy;
+    the producer and the consumer launch of the two-kernel control) and for the
+    whole forward, with the gap between the control's launches."""
+    q = cs.cs_chain_query(plan)
+    n_sm = q["num_sms"]
+    recs = [r for r in traced_forward(cs, torch, plan, fwd) if r[2]]
+    if q["policy"] != "stream":
+        st = sm_busy_stats(recs, n_sm)
+        st.pop("t_start"), st.pop("t_end")
+        return {"launches": [st], "whole": st}
+    by_stage = {}
+    for r in recs:
+        by_stage.setdefault(cs.decode_unit(r[0] & 0xFFFFFFFF)[0], []).append(r)
+    launches = [sm_busy_stats(by_stage[s], n_sm) for s in sorted(by_stage)]
+    whole = sm_busy_stats(recs, n_sm)
+    gaps = [(b["t_start"] - a["t_end"]) / 1e3 for a, b in zip(launches, launches[1:])]
+    for st in launches + [whole]:
+        st.pop("t_start"), st.pop("t_end")
+    whole["gaps_us"] = gaps
+    return {"launches": launches, "whole": whole}
+
+
 def rs_standin(cs, torch, make_plan, Y, dev, M, chunks=8):
     """Single-GPU stand-in for a GEMM + reduce-scatter fusion (Flux summary): the
     chain with its output released per 128-row block (desc.out_release), timed
@@ -898,7 +976,7 @@ def other_configs(cs, torch, peaks, lay):
         Ym = torch.empty(m, inp.H, dtype=inp.dtype, device="cuda")
         rec = {"M": m}
         with contextlib.ExitStack() as es:
-            fns = {}
+            fns, plans = {}, {}
             for key, pol, tuned in (("tile", "tile", 0), ("row", "row", 0), ("strided", "strided", 0),
                                     ("stream", "stream", 0), ("tile_builtin", "tile", -1)):
                 desc = cs.cs_chain_desc_init(kind="gelu", M=m, H=inp.H, F=inp.F, dtype=inp.dtype, policy=pol,
@@ -908,8 +986,14 @@ def other_configs(cs, torch, peaks, lay):
                     q = cs.cs_chain_query(p)
                     rec["plan"] = plan_record(q)
                 fns[key] = (lambda p=p: cs.cs_mlp_forward(p, Y=Ym, **sub))
+                plans[key] = p
             for key, ms in interleaved_times(fns).items():
                 rec[f"{key}_us"] = ms * 1e3
+            # SM occupancy of one traced forward of the fused chain and of the control
+            try:
+                rec["tail"] = {k: tail_stats(cs, torch, plans[k], fns[k]) for k in ("tile", "stream")}
+            except Exception as e:  # a side measurement that fails must not cost the bench line
+                rec["tail"] = {"error": repr(e)[:200]}
         workers = q["num_sms"] * 128 // q["tile_m"]
         tiles0 = q["sched_units"][0]
         rec["stage0_units"], rec["workers"] = tiles0, workers

@@ -124,6 +124,10 @@ struct cs_chain_s {
   uint32_t* sched_fused = nullptr;
   int n_fused = 0;
   uint32_t* sched_stage[3] = {nullptr, nullptr, nullptr};
+  int n_stage[3] = {0, 0, 0};  // entries of each stage-alone schedule (Stream-K units included)
+  // Stream-K tail of the last stage (geometry in sk_*; partial tiles owned here)
+  int sk_tiles = 0, sk_units = 0, sk_q = 0, sk_max_nc = 0;
+  float* sk_partial = nullptr;
   uint32_t* delays[3] = {nullptr, nullptr, nullptr};
   unsigned long long* trace = nullptr;
   int trace_records = 0;
@@ -185,7 +189,15 @@ struct Geometry {
   int kps[3] = {0, 0, 0};  // K-slices per split
   int lag = 1, group_m = 1, stride = 1;
   bool row_major = false;  // tiles of a group in row-major order
+  // Stream-K tail of the last stage: its last sk_tiles tiles in dispatch order
+  // become sk_units units of sk_q consecutive K-slices each (the last shorter)
+  int sk_tiles = 0, sk_units = 0, sk_q = 0, sk_max_nc = 0;
 };
+
+// Smallest Stream-K share in K-slices, and the most contributors a tile may
+// have (the part word holds 7 bits).
+constexpr int kSkMinSlices = 8;
+constexpr int kSkMaxContrib = 120;
 
 cs_status validate(const cs_chain_desc* d) {
   if (!d) return fail(CS_ERR_INVALID_ARG, "desc is NULL");
@@ -201,6 +213,8 @@ cs_status validate(const cs_chain_desc* d) {
   if (d->prefetch < -1 || d->prefetch > 64) return fail(CS_ERR_INVALID_ARG, "prefetch=%d (-1..64)", d->prefetch);
   if (d->raster < 0 || d->raster > 2) return fail(CS_ERR_INVALID_ARG, "raster=%d (0..2)", d->raster);
   if (d->pdl < -1 || d->pdl > 1) return fail(CS_ERR_INVALID_ARG, "pdl=%d (-1..1)", d->pdl);
+  if (d->sk_tiles < -1 || d->sk_tiles > 65534) return fail(CS_ERR_INVALID_ARG, "sk_tiles=%d (-1..65534)", d->sk_tiles);
+  if (d->sk_units < 0 || d->sk_units > 16383) return fail(CS_ERR_INVALID_ARG, "sk_units=%d (0..16383)", d->sk_units);
   if (d->H < 8 || d->H % 8 != 0 || d->H > (1 << 20)) return fail(CS_ERR_INVALID_ARG, "H=%d must be a positive multiple of 8", d->H);
   if (d->F < 8 || d->F % 8 != 0 || d->F > (1 << 20)) return fail(CS_ERR_INVALID_ARG, "F=%d must be a positive multiple of 8", d->F);
   if (d->stride < 0) return fail(CS_ERR_INVALID_ARG, "stride=%d", d->stride);
@@ -349,6 +363,25 @@ Geometry geometry(const cs_chain_desc* d, int num_sms) {
   g.lag = d->lag >= 0 ? d->lag : 1;
   if (g.lag > groups) g.lag = groups;
   g.stride = d->stride > 0 ? d->stride : (d->kind == CS_CHAIN_ATTN ? d->heads : 4);
+  // Stream-K tail: the last stage's trailing tiles (at most those of the last
+  // row group, all listed at the schedule's end) shared out in equal K-ranges
+  const int fs = g.stages - 1;
+  if (d->sk_tiles > 0 && g.splits[fs] == 1 && g.k_iters[fs] >= 2) {
+    const int last_rows = g.m_tiles - (groups - 1) * g.group_m;
+    const int tiles = std::min(d->sk_tiles, last_rows * g.n_tiles[fs]);
+    const long long K = g.k_iters[fs];
+    const long long work = static_cast<long long>(tiles) * K;
+    const int units = d->sk_units > 0 ? d->sk_units : capacity;
+    long long q = (work + units - 1) / units;
+    q = std::max<long long>(q, std::min<long long>(kSkMinSlices, K));
+    q = std::max<long long>(q, (K + kSkMaxContrib - 2) / (kSkMaxContrib - 1));
+    g.sk_tiles = tiles;
+    g.sk_q = static_cast<int>(q);
+    g.sk_units = static_cast<int>((work + q - 1) / q);
+    g.sk_max_nc = 0;
+    for (int j = 0; j < tiles; ++j)
+      g.sk_max_nc = std::max(g.sk_max_nc, static_cast<int>(((j + 1) * K - 1) / q - (j * K) / q + 1));
+  }
   return g;
 }
 
@@ -371,19 +404,47 @@ cs::SchedGeo sched_geo(const Geometry& g) {
   return sg;
 }
 
-std::vector<uint32_t> build_fused(const Geometry& g) {
+// A schedule as uploaded: n_units dispatch entries, then (with a Stream-K
+// tail) the unit encodings of the sk_tiles tiles the Stream-K units share.
+struct Sched {
+  std::vector<uint32_t> v;
+  int n_units = 0;
+};
+
+// The last g.sk_tiles entries (the last stage's trailing tiles) become the
+// Stream-K table; Stream-K units (K-split field 15, unit index in the column
+// field) take their place.
+Sched with_stream_k(const Geometry& g, std::vector<uint32_t> v, bool last_stage) {
+  Sched r;
+  if (!last_stage || g.sk_units == 0 || static_cast<int>(v.size()) < g.sk_tiles) {
+    r.n_units = static_cast<int>(v.size());
+    r.v = std::move(v);
+    return r;
+  }
+  const size_t keep = v.size() - static_cast<size_t>(g.sk_tiles);
+  std::vector<uint32_t> table(v.begin() + static_cast<long>(keep), v.end());
+  v.resize(keep);
+  for (int u = 0; u < g.sk_units; ++u) v.push_back(cs::sched_enc(g.stages - 1, 0, u, cs::SK_KS));
+  r.n_units = static_cast<int>(v.size());
+  v.insert(v.end(), table.begin(), table.end());
+  r.v = std::move(v);
+  return r;
+}
+
+Sched build_fused(const Geometry& g) {
   const cs::SchedGeo sg = sched_geo(g);
   std::vector<uint32_t> v(static_cast<size_t>(cs::sched_fused_count(sg)));
   for (size_t i = 0; i < v.size(); ++i) v[i] = cs::sched_fused_entry(sg, static_cast<long long>(i));
-  return v;
+  return with_stream_k(g, std::move(v), true);
 }
 
-// One stage alone (two-kernel control, standalone timings): same grouping.
-std::vector<uint32_t> build_stage(const Geometry& g, int s) {
+// One stage alone (two-kernel control, standalone timings): same grouping, and
+// the same Stream-K tail on the last stage (so its bits equal the fused chain's).
+Sched build_stage(const Geometry& g, int s) {
   const cs::SchedGeo sg = sched_geo(g);
   std::vector<uint32_t> v(static_cast<size_t>(cs::sched_stage_count(sg, s)));
   for (size_t i = 0; i < v.size(); ++i) v[i] = cs::sched_stage_entry(sg, s, static_cast<long long>(i));
-  return v;
+  return with_stream_k(g, std::move(v), s == g.stages - 1);
 }
 
 // Everything a plan takes from its geometry: tile counts, K-splits, the kernel
@@ -408,6 +469,10 @@ void shape_plan(cs_chain_s* p, const Geometry& g, int kind, int M) {
   p->lag = g.lag;
   p->group_m = g.group_m;
   p->stride = g.stride;
+  p->sk_tiles = g.sk_tiles;
+  p->sk_units = g.sk_units;
+  p->sk_q = g.sk_q;
+  p->sk_max_nc = g.sk_max_nc;
   const bool wide_b = kind == CS_CHAIN_MLP_SWIGLU || g.bn[0] == 256 || g.bn[1] == 256 || g.bn[2] == 256;
   p->cfg_s = (g.cg == 1 && kind != CS_CHAIN_ATTN && M <= 8) ? (wide_b ? 2 : 1) : 0;
   p->cfg_b = g.cg == 1 && !p->cfg_s && wide_b;
@@ -439,6 +504,9 @@ void info_geometry(const cs_chain_s* p, int n_fused, cs_chain_info* info) {
   info->stride = p->stride;
   info->policy = p->d.policy;
   info->tuned_entry = p->tuned_entry;
+  info->sk_tiles = p->sk_tiles;
+  info->sk_units = p->sk_units;
+  info->sk_q = p->sk_q;
 }
 
 int device_sms(int* out) {
@@ -469,6 +537,7 @@ void free_plan(cs_chain_s* p) {
   if (p->trace) cudaFree(p->trace);
   for (auto& b : p->partial) if (b) cudaFree(b);
   for (auto& b : p->split_ctr) if (b) cudaFree(b);
+  if (p->sk_partial) cudaFree(p->sk_partial);
   for (auto& b : p->host_x) if (b) cudaFree(b);
   for (auto& b : p->host_y) if (b) cudaFree(b);
   for (cudaEvent_t* evs : {p->ev_x, p->ev_k, p->ev_y})
@@ -522,7 +591,7 @@ cs_status encode_act(cs_chain_s* p, int slot, const void* ptr, int rows, int col
 // indices from 0).
 void next_trace_segment(const cs_chain_s* p, cs::KParams& kp, int done) {
   if (!kp.trace) return;
-  const int recs = p->sched_units[done] * p->cl;
+  const int recs = p->n_stage[done] * p->cl;
   kp.trace += static_cast<size_t>(recs) * cs::TRACE_WORDS;
   kp.trace_records -= recs;
 }
@@ -540,6 +609,13 @@ void fill_split(const cs_chain_s* p, int st, cs::StageP& s) {
   s.m_blocks = p->m_blocks;
   s.partial = p->partial[st];
   s.split_ctr = p->split_ctr[st];
+  if (st == p->stages - 1 && p->sk_units > 0) {
+    s.sk_tiles = p->sk_tiles;
+    s.sk_units = p->sk_units;
+    s.sk_q = p->sk_q;
+    s.sk_max_nc = p->sk_max_nc;
+    s.sk_partial = p->sk_partial;
+  }
 }
 
 void fill_common(const cs_chain_s* p, cs::KParams& kp) {
@@ -641,6 +717,8 @@ void fill_mlp_stages(const cs_chain_s* p, const cs_mlp_args* a, cs::KParams& kp)
 cs_status launch(cs_chain_s* p, cs::KParams& kp, const uint32_t* sched, int n_units, cudaStream_t stream) {
   kp.sched = sched;
   kp.n_units = n_units;
+  // a schedule with Stream-K units is followed by the table of their tiles
+  kp.st[p->stages - 1].sk_tile = sched + n_units;
   // one CTA per SM, clusters of cl CTAs per unit; no more clusters than units
   int grid = p->num_sms / p->cl;
   if (grid > n_units) grid = n_units;
@@ -878,9 +956,9 @@ cs_status cs_schedule_build(const cs_chain_desc* desc, int num_sms, uint32_t* un
   int entry = -1;
   const cs_chain_desc rd = resolve_desc(desc, num_sms, &entry);
   Geometry g = geometry(&rd, num_sms);
-  std::vector<uint32_t> v = build_fused(g);
-  *n_out = v.size();
-  for (size_t i = 0; i < v.size() && i < cap; ++i) units[i] = v[i];
+  const Sched f = build_fused(g);
+  *n_out = static_cast<size_t>(f.n_units);
+  for (size_t i = 0; i < *n_out && i < cap; ++i) units[i] = f.v[i];
   return CS_OK;
 }
 
@@ -929,6 +1007,16 @@ cs_status cs_chain_plan(const cs_chain_desc* desc, cs_chain_t* out) {
   if (cudaMalloc(reinterpret_cast<void**>(&p->ctrl), cs::CTRL_WORDS * 4) != cudaSuccess)
     return bail(fail(CS_ERR_OOM, "cudaMalloc of the control block failed"));
   for (int st = 0; st < g.stages; ++st) {
+    const bool sk = st == g.stages - 1 && g.sk_units > 0;
+    if (sk) {
+      // Stream-K partial tiles: [sk_tiles][sk_max_nc][CTAs per unit][128][tile_n]
+      const size_t pf = static_cast<size_t>(g.sk_tiles) * g.sk_max_nc * g.cl * cs::BM * g.bn[st];
+      const size_t words = static_cast<size_t>(g.m_blocks) * g.n_tiles[st];
+      if (cudaMalloc(reinterpret_cast<void**>(&p->sk_partial), pf * 4) != cudaSuccess ||
+          cudaMalloc(reinterpret_cast<void**>(&p->split_ctr[st]), words * 4) != cudaSuccess)
+        return bail(fail(CS_ERR_OOM, "cudaMalloc of the Stream-K workspace failed"));
+      if (cudaMemset(p->split_ctr[st], 0, words * 4) != cudaSuccess) return bail(fail(CS_ERR_CUDA, "cudaMemset failed"));
+    }
     if (g.splits[st] <= 1) continue;
     const int acc_n = (desc->kind == CS_CHAIN_MLP_SWIGLU && st == 0) ? 256 : g.bn[st];
     const size_t pf = static_cast<size_t>(g.splits[st]) * g.m_blocks * g.n_tiles[st] * cs::BM * acc_n;
@@ -939,11 +1027,14 @@ cs_status cs_chain_plan(const cs_chain_desc* desc, cs_chain_t* out) {
     if (cudaMemset(p->split_ctr[st], 0, words * 4) != cudaSuccess) return bail(fail(CS_ERR_CUDA, "cudaMemset failed"));
   }
   if (cudaMemset(p->ctrl, 0, cs::CTRL_WORDS * 4) != cudaSuccess) return bail(fail(CS_ERR_CUDA, "cudaMemset failed"));
-  std::vector<uint32_t> fused = build_fused(g);
-  p->n_fused = static_cast<int>(fused.size());
-  if ((s = upload(&p->sched_fused, fused)) != CS_OK) return bail(s);
-  for (int st = 0; st < g.stages; ++st)
-    if ((s = upload(&p->sched_stage[st], build_stage(g, st))) != CS_OK) return bail(s);
+  const Sched fused = build_fused(g);
+  p->n_fused = fused.n_units;
+  if ((s = upload(&p->sched_fused, fused.v)) != CS_OK) return bail(s);
+  for (int st = 0; st < g.stages; ++st) {
+    const Sched one = build_stage(g, st);
+    p->n_stage[st] = one.n_units;
+    if ((s = upload(&p->sched_stage[st], one.v)) != CS_OK) return bail(s);
+  }
   // plan-owned intermediate maps (never re-encoded)
   int owned[5];
   int n_owned = 0;
@@ -1002,10 +1093,10 @@ cs_status cs_mlp_forward(cs_chain_t p, const cs_mlp_args* a, void* stream) {
     kp.waits = 0;
     kp.release = 1;
     kp.bump_epoch = 0;
-    if ((s = launch(p, kp, p->sched_stage[0], p->sched_units[0], st)) != CS_OK) return s;
+    if ((s = launch(p, kp, p->sched_stage[0], p->n_stage[0], st)) != CS_OK) return s;
     kp.bump_epoch = 1;
     next_trace_segment(p, kp, 0);
-    return launch(p, kp, p->sched_stage[1], p->sched_units[1], st);
+    return launch(p, kp, p->sched_stage[1], p->n_stage[1], st);
   }
   kp.waits = 1;
   kp.release = 1;
@@ -1078,7 +1169,7 @@ cs_status cs_attn_chain_forward(cs_chain_t p, const cs_attn_args* a, void* strea
     for (int stg = 0; stg < 3; ++stg) {
       kp.bump_epoch = stg == 2;
       if (stg > 0) next_trace_segment(p, kp, stg - 1);
-      if ((s = launch(p, kp, p->sched_stage[stg], p->sched_units[stg], st)) != CS_OK) return s;
+      if ((s = launch(p, kp, p->sched_stage[stg], p->n_stage[stg], st)) != CS_OK) return s;
     }
     return CS_OK;
   }
@@ -1110,7 +1201,7 @@ cs_status cs_chain_forward_stage(cs_chain_t p, const void* args, int stage, void
   kp.waits = 0;
   kp.release = 0;
   kp.bump_epoch = 0;
-  return launch(p, kp, p->sched_stage[stage], p->sched_units[stage], static_cast<cudaStream_t>(stream));
+  return launch(p, kp, p->sched_stage[stage], p->n_stage[stage], static_cast<cudaStream_t>(stream));
 }
 
 cs_status cs_chain_status(cs_chain_t p) {
@@ -1173,7 +1264,7 @@ cs_status cs_chain_plan_info(const cs_chain_desc* desc, int num_sms, cs_chain_in
   p.d = resolve_desc(desc, p.num_sms, &p.tuned_entry);
   const Geometry g = geometry(&p.d, p.num_sms);
   shape_plan(&p, g, desc->kind, desc->M);
-  info_geometry(&p, static_cast<int>(build_fused(g).size()), info);
+  info_geometry(&p, build_fused(g).n_units, info);
   return CS_OK;
 }
 
@@ -1229,6 +1320,10 @@ cs_status cs_chain_debug_poison_intermediate(cs_chain_t p, int which, void* stre
   // all-ones bytes: NaN as fp16, bf16 and fp32
   for (int b = 0; b < 2; ++b)
     if ((which == -1 || which == b) && p->inter[b]) CS_CUDA(cudaMemsetAsync(p->inter[b], 0xFF, p->inter_bytes[b], st));
+  if ((which == -1 || which == 2) && p->sk_partial) {
+    const size_t bytes = static_cast<size_t>(p->sk_tiles) * p->sk_max_nc * p->cl * cs::BM * p->bn[p->stages - 1] * 4;
+    CS_CUDA(cudaMemsetAsync(p->sk_partial, 0xFF, bytes, st));
+  }
   if (which == -1 || which == 2)
     for (int stg = 0; stg < p->stages; ++stg)
       if (p->partial[stg]) {
@@ -1253,6 +1348,17 @@ cs_status cs_chain_debug_set_epoch(cs_chain_t p, uint32_t epoch) {
     if (p->split_ctr[stg]) {
       std::vector<uint32_t> v(static_cast<size_t>(p->m_blocks) * p->n_tiles[stg],
                               epoch * static_cast<uint32_t>(p->splits[stg]));
+      if (stg == p->stages - 1 && p->sk_units > 0) {
+        // a Stream-K tile counts one arrival per contributing unit (per 128-row block)
+        std::vector<uint32_t> table(static_cast<size_t>(p->sk_tiles));
+        CS_CUDA(cudaMemcpy(table.data(), p->sched_fused + p->n_fused, table.size() * 4, cudaMemcpyDeviceToHost));
+        const long long K = p->k_iters[stg], q = p->sk_q;
+        for (int j = 0; j < p->sk_tiles; ++j) {
+          const uint32_t nc = static_cast<uint32_t>(((j + 1) * K - 1) / q - (j * K) / q + 1);
+          const int m = static_cast<int>((table[j] >> 14) & 0xFFFu), n = static_cast<int>(table[j] & 0x3FFFu);
+          for (int r = 0; r < p->cl; ++r) v[static_cast<size_t>(m * p->cl + r) * p->n_tiles[stg] + n] = epoch * nc;
+        }
+      }
       CS_CUDA(cudaMemcpy(p->split_ctr[stg], v.data(), v.size() * 4, cudaMemcpyHostToDevice));
     }
   CS_CUDA(cudaMemcpy(p->ctrl + cs::CTRL_EPOCH, &epoch, 4, cudaMemcpyHostToDevice));
@@ -1268,7 +1374,9 @@ cs_status cs_chain_debug_trace(cs_chain_t p, int enable) {
     p->trace_records = 0;
   }
   if (!enable) return CS_OK;
-  const int recs = p->n_fused * p->cl;
+  int per_stage = 0;
+  for (int st = 0; st < p->stages; ++st) per_stage += p->n_stage[st];
+  const int recs = std::max(p->n_fused, per_stage) * p->cl;
   const size_t bytes = static_cast<size_t>(recs) * cs::TRACE_WORDS * 8;
   if (cudaMalloc(reinterpret_cast<void**>(&p->trace), bytes) != cudaSuccess) return fail(CS_ERR_OOM, "cudaMalloc failed");
   CS_CUDA(cudaMemset(p->trace, 0, bytes));
@@ -1358,6 +1466,9 @@ cs_status cs_mlp_forward_noalloc(const cs_chain_desc* desc, const cs_mlp_args* a
   if (desc->split_k > 1)
     return fail(CS_ERR_UNSUPPORTED, "split_k=%d: the allocation-free forward runs unsplit tiles (split_k 0 or 1)",
                 desc->split_k);
+  if (desc->sk_tiles > 0)
+    return fail(CS_ERR_UNSUPPORTED, "sk_tiles=%d: the allocation-free forward has no Stream-K workspace",
+                desc->sk_tiles);
   int sms = 0;
   const int dev = device_sms(&sms);
   if (dev < 0) return fail(CS_ERR_CUDA, "no CUDA device available");
@@ -1372,6 +1483,7 @@ cs_status cs_mlp_forward_noalloc(const cs_chain_desc* desc, const cs_mlp_args* a
   cs_chain_s p;
   p.d = *desc;
   p.d.split_k = 1;  // no split-K workspace in the fixed array
+  p.d.sk_tiles = -1;
   if (p.d.policy == CS_SYNC_AUTO) p.d.policy = CS_SYNC_TILE;
   p.device = dev;
   p.num_sms = desc->num_sms > 0 && desc->num_sms < sms ? desc->num_sms : sms;

@@ -107,6 +107,16 @@ struct StageP {
   int splits, kps, m_blocks;
   float* partial;
   uint32_t* split_ctr;
+  // Stream-K tail (the last GEMM stage only): the stage's last sk_tiles tiles
+  // in dispatch order are replaced by sk_units units that each cover sk_q
+  // consecutive K-slices of the tiles' concatenated K ranges (crossing tile
+  // boundaries); a tile's contributors write fp32 partials
+  // [sk_tiles][sk_max_nc][CTAs per unit][128][mma_n] and count their arrival
+  // on split_ctr; the last to arrive sums them in K order, runs the epilogue
+  // and releases.  sk_tile[j] is the unit encoding of tile j.
+  int sk_tiles, sk_units, sk_q, sk_max_nc;
+  float* sk_partial;
+  const uint32_t* sk_tile;
   // L2 prefetch of upcoming K-slices by the scheduler warp (null: none):
   // pf_b/pf_b2 = weight base(s), pf_ldb = bytes between weight rows, pf_brows =
   // weight rows (N if K-major, K if MN-major); pf_a/pf_lda/pf_arows likewise for A.
@@ -170,6 +180,9 @@ struct SmemCtl {
   uint32_t uq[UQ];
   uint32_t uq_idx[UQ];      // dispatch index of each queued unit (trace records)
   uint32_t uq_ready[UQ];    // per queued unit: leading producer items known complete
+  uint32_t uq_kb[UQ];       // per queued piece: first K-slice | end K-slice << 16
+  uint32_t uq_part[UQ];     // per queued piece: contributor | contributors << 8 | last of its claim << 15 |
+                            // Stream-K tile << 16 (0xFFFF: a tile unit)
   uint32_t mb_unit;         // pair mode: dispatch index handed to the peer
   uint32_t tmem_base;
   volatile int abort;
@@ -215,6 +228,18 @@ __device__ __forceinline__ uint32_t unit_stage(uint32_t u) { return u >> 30; }
 __device__ __forceinline__ int unit_ks(uint32_t u) { return static_cast<int>((u >> 26) & 0xFu); }
 __device__ __forceinline__ int unit_m(uint32_t u) { return static_cast<int>((u >> 14) & 0xFFFu); }
 __device__ __forceinline__ int unit_n(uint32_t u) { return static_cast<int>(u & 0x3FFFu); }
+// A schedule entry with K-split field SK_KS is Stream-K unit unit_n(u) of its stage.
+constexpr int SK_KS = 15;
+
+// A queued piece of work: a tile unit, or one tile's share of a Stream-K unit.
+__device__ __forceinline__ int piece_kb0(uint32_t kb) { return static_cast<int>(kb & 0xFFFFu); }
+__device__ __forceinline__ int piece_kb1(uint32_t kb) { return static_cast<int>(kb >> 16); }
+__device__ __forceinline__ int part_c(uint32_t x) { return static_cast<int>(x & 0xFFu); }
+__device__ __forceinline__ int part_nc(uint32_t x) { return static_cast<int>((x >> 8) & 0x7Fu); }
+__device__ __forceinline__ bool part_last(uint32_t x) { return ((x >> 15) & 1u) != 0u; }
+__device__ __forceinline__ int part_sk(uint32_t x) { return static_cast<int>(x >> 16); }
+constexpr uint32_t PART_TILE = 0xFFFFu << 16;  // not a Stream-K tile
+constexpr uint32_t PART_LAST = 1u << 15;
 
 struct RingPos {
   uint32_t slot = 0, phase = 0;
@@ -239,10 +264,8 @@ struct RingPos {
 // pattern) before the CTA-scope release.
 template <int NS>
 __device__ void sched_poll_gemm(const KParams& p, const StageP& S, SmemCtl<NS>* sc, uint32_t q, int m,
-                                uint32_t epoch1, uint32_t unit, int lane) {
+                                uint32_t epoch1, uint32_t unit, int kb0, int kb1, int lane) {
   const uint32_t* tiles = S.dep_tile + static_cast<size_t>(m) * S.dep_ntiles;
-  const int kb0 = unit_ks(unit) * S.kps;
-  const int kb1 = min(S.k_iters, kb0 + S.kps);
   // TILE: the unit reads producer tiles [i0, i1)
   const int i0 = S.wait == WAIT_TILE ? (kb0 * BK) / S.dep_bn : 0;
   const int nt = S.wait == WAIT_TILE ? min(S.dep_ntiles, ((kb1 - 1) * BK) / S.dep_bn + 1) : S.dep_ntiles;
@@ -357,9 +380,10 @@ __device__ bool tma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
   constexpr int A_BYTES = AR * BK * 2;
   const uint32_t bytes = A_BYTES + S.b_bytes;
   const bool do_wait = p.waits && S.wait != WAIT_NONE;
-  const int kb0 = unit_ks(unit) * S.kps;
-  const int kb1 = min(S.k_iters, kb0 + S.kps);
-  const int claim_at = kb1 - kb0 > CLAIM_AHEAD ? kb1 - CLAIM_AHEAD : kb0;
+  const int kb0 = piece_kb0(sc->uq_kb[q]);
+  const int kb1 = piece_kb1(sc->uq_kb[q]);
+  // the next unit is claimed near the end of the last piece of this claim
+  const int claim_at = !part_last(sc->uq_part[q]) ? -1 : kb1 - kb0 > CLAIM_AHEAD ? kb1 - CLAIM_AHEAD : kb0;
   const int row0 = (m * CL + static_cast<int>(rank)) * BM;  // this CTA's A rows
   const int prank = static_cast<int>(rank) & (CG - 1);        // rank inside the MMA pair
   // gate|up on a pair: the MMA's N = 2*bn is split over the two CTAs, so the
@@ -450,7 +474,7 @@ __device__ bool tma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
 // ---------------------------------------------------------------- MMA role
 template <int NS, int STAGE_BYTES, int CG, int CL, int AR>
 __device__ bool mma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, RingPos& rp, uint32_t unit,
-                              uint32_t& acc, uint32_t& acc_phase, uint32_t rank) {
+                              int kb0, int kb1, uint32_t& acc, uint32_t& acc_phase, uint32_t rank) {
   // a freed stage is refilled by this pair and (CL = 4) by the other pair's
   // multicast: the release goes to every CTA that writes into it
   const uint16_t empty_mask = CL == 4 ? 0xF : 0x3;
@@ -460,8 +484,6 @@ __device__ bool mma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
   if (!wait_bar(&sc->tempty[acc], acc_phase ^ 1u, sc, p, 2)) return false;
   tc_fence_after();
   const uint32_t d = sc->tmem_base + acc * static_cast<uint32_t>(p.acc_stride);
-  const int kb0 = unit_ks(unit) * S.kps;
-  const int kb1 = min(S.k_iters, kb0 + S.kps);
   for (int kb = kb0; kb < kb1; ++kb) {
     if (!wait_bar(&sc->full[rp.slot], rp.phase, sc, p, 3)) return false;
     tc_fence_after();
@@ -491,10 +513,7 @@ __device__ bool mma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
 // the other pair's multicast have landed; pass that on to the pair's leader,
 // whose full barrier waits for both CTAs before it issues the pair MMA.
 template <int NS>
-__device__ bool fwd_gemm_unit(const KParams& p, SmemCtl<NS>* sc, RingPos& rp, uint32_t unit, uint32_t rank) {
-  const StageP& S = p.st[unit_stage(unit)];
-  const int kb0 = unit_ks(unit) * S.kps;
-  const int kb1 = min(S.k_iters, kb0 + S.kps);
+__device__ bool fwd_gemm_unit(const KParams& p, SmemCtl<NS>* sc, RingPos& rp, int kb0, int kb1, uint32_t rank) {
   for (int kb = kb0; kb < kb1; ++kb) {
     if (!wait_bar(&sc->full[rp.slot], rp.phase, sc, p, 13)) return false;
     mbar_arrive_cluster_relaxed(mapa_shared(&sc->full[rp.slot], rank & ~1u));
@@ -731,8 +750,9 @@ __device__ void epi_split_rows_small(const KParams& p, const StageP& S, SmemCtl<
 }
 
 template <int NS, int CG, int CL>
-__device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* staging, uint32_t unit, uint32_t& acc,
-                              uint32_t& acc_phase, int& last_buf, uint32_t rank, uint32_t tidx, uint32_t epoch1) {
+__device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* staging, uint32_t unit, uint32_t part,
+                              uint32_t& acc, uint32_t& acc_phase, int& last_buf, uint32_t rank, uint32_t tidx,
+                              uint32_t epoch1) {
   const StageP& S = p.st[unit_stage(unit)];
   const int mb = unit_m(unit) * CL + static_cast<int>(rank);  // this CTA's 128-row block
   const int n = unit_n(unit);
@@ -745,7 +765,10 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
   const uint32_t tbase =
       sc->tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * static_cast<uint32_t>(p.acc_stride);
   const int nchunks = S.bn / 64;
-  const bool split = S.splits > 1;
+  // contributors of this tile: its K-splits, or the Stream-K units whose K
+  // ranges touch it (this piece is contributor c of nc, in K order)
+  const int nc = part_nc(part), skj = part_sk(part);
+  const bool split = nc > 1;
   // rows of this block inside the output (the last block may be ragged)
   const int rows_valid = max(0, min(BM, S.m_extent - mb * BM));
   const size_t tile_floats = static_cast<size_t>(BM) * S.mma_n;
@@ -753,6 +776,10 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
   // columns 4c..4c+3 of this thread's row sits at (c * 128 + row), so a warp
   // reads or writes 512 contiguous bytes per access.
   auto tile_partial = [&](int ks) {
+    if (skj != 0xFFFF)
+      return reinterpret_cast<float4*>(
+                 S.sk_partial +
+                 (static_cast<size_t>(skj * S.sk_max_nc + ks) * CL + rank) * tile_floats) + row;
     return reinterpret_cast<float4*>(S.partial + (static_cast<size_t>(ks * S.m_blocks + mb) * S.n_tiles + n) *
                                                      tile_floats) + row;
   };
@@ -770,7 +797,7 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
   if (split) {
     // K-split: write this split's fp32 rows, count the arrival; only the last
     // split of the tile goes on (and reduces every split in split order).
-    float4* mine = tile_partial(unit_ks(unit));
+    float4* mine = tile_partial(part_c(part));
     for (int c = 0; c < S.mma_n / 32; ++c) {
       uint32_t v[32];
       tmem_ld32(tbase + c * 32, v);
@@ -789,7 +816,7 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
     named_bar_sync(1, EPI_THREADS);
     if (threadIdx.x == EPI_WARP0 * 32) {
       const uint32_t old = atomicAdd(S.split_ctr + mb * S.n_tiles + n, 1u);
-      sc->split_last = (old + 1u == epoch1 * static_cast<uint32_t>(S.splits)) ? 1 : 0;
+      sc->split_last = (old + 1u == epoch1 * static_cast<uint32_t>(nc)) ? 1 : 0;
       __threadfence();
     }
     named_bar_sync(1, EPI_THREADS);
@@ -803,7 +830,7 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
   // and plain row stores; the loop below is skipped (measured against the
   // row-per-thread path: LLaMA 33 rows 77 -> 58 us, 48 rows 60 -> 57 us, but
   // 64 rows 59 -> 62 us)
-  const bool rows_small = split && rows_valid <= 48 && S.out_ptr != nullptr;
+  const bool rows_small = split && skj == 0xFFFF && rows_valid <= 48 && S.out_ptr != nullptr;
   if (rows_small) {
     const size_t kstride = static_cast<size_t>(S.m_blocks) * S.n_tiles * (tile_floats / 4);
     epi_split_rows_small<NS>(p, S, sc, staging, tile_partial(0) - row, kstride, rows_valid, mb, n, row, lane);
@@ -817,7 +844,7 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
       for (int j = 0; j < 64; ++j) va[j] = vu[j] = 0.0f;
       // sum the splits in split order (the same bits whichever split arrived last);
       // loads of one split are issued together, then added
-      for (int ks = 0; ks < S.splits && row < rows_valid; ++ks) {
+      for (int ks = 0; ks < nc && row < rows_valid; ++ks) {
         const float4* src = tile_partial(ks);
         float4 x[16];
 #pragma unroll
@@ -1370,10 +1397,12 @@ __device__ bool wait_prefetching(uint64_t* bar, uint32_t parity, SmemCtl<NS>* sc
 // ---------------------------------------------------------------- scheduler role
 template <int NS>
 __device__ __forceinline__ void push_unit(SmemCtl<NS>* sc, uint32_t q, uint32_t unit, uint32_t idx, int lane,
-                                          bool consumer) {
+                                          bool consumer, uint32_t kb, uint32_t part) {
   if (lane == 0) {
     sc->uq[q] = unit;
     sc->uq_idx[q] = idx;
+    sc->uq_kb[q] = kb;
+    sc->uq_part[q] = part;
     sc->uq_ready[q] = consumer ? 0u : READY_ALL;
     mbar_arrive(&sc->uq_full[q]);
   }
@@ -1491,31 +1520,66 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
         trace_put(p, idx, rank, CL, 1, smid() | (blockIdx.x << 16) | (rank << 30));
         trace_put(p, idx, rank, CL, 2, globaltimer());
       }
-      if (!wait_bar(&sc->uq_empty[q], qphase ^ 1u, sc, p, 5)) break;
-      const StageP& S = p.st[unit == UNIT_END ? 0 : unit_stage(unit)];
-      const bool consumer = unit != UNIT_END && p.waits && S.wait != WAIT_NONE;
-      push_unit(sc, q, unit, idx, lane, consumer);
-      if (unit == UNIT_END) break;
-      ++pushed;
-      if (S.kind == STAGE_GEMM && S.pf_b != nullptr) {
-        pf.unit = unit;
-        pf.seq = pushed;
-        pf.kb0 = unit_ks(unit) * S.kps;
-        pf.kb1 = min(S.k_iters, pf.kb0 + S.kps);
-        pf.next = pf.kb0;
-      } else {
-        pf.unit = UNIT_END;
+      if (unit == UNIT_END) {
+        if (wait_bar(&sc->uq_empty[q], qphase ^ 1u, sc, p, 5))
+          push_unit(sc, q, UNIT_END, idx, lane, false, 0u, PART_TILE | PART_LAST);
+        break;
       }
-      if (consumer && S.kind == STAGE_GEMM)
-        sched_poll_gemm<NS>(p, S, sc, q, unit_m(unit) * CL + static_cast<int>(rank), epoch1, unit, lane);
-      else if constexpr (ATTN)
-        if (consumer && S.kind == STAGE_ATTN)
-          sched_poll_attn<NS>(p, S, sc, q, (unit_m(unit) + 1) * CG - 1, unit_n(unit), epoch1, unit, lane);
-      if (lane == 0) trace_put(p, idx, rank, CL, 3, globaltimer());
-      if (++q == UQ) {
-        q = 0;
-        qphase ^= 1u;
+      const StageP& S = p.st[unit_stage(unit)];
+      const bool consumer = p.waits && S.wait != WAIT_NONE;
+      // The claimed unit's pieces: one for a tile unit; for Stream-K unit u,
+      // one per tile that its K-slices [u*q, (u+1)*q) of the SK tiles'
+      // concatenated K ranges touch (contributor u - first of that tile).
+      const bool sk = S.kind == STAGE_GEMM && unit_ks(unit) == SK_KS;
+      const long long K = S.k_iters;
+      const long long sk_a = sk ? static_cast<long long>(unit_n(unit)) * S.sk_q : 0;
+      const long long sk_b = sk ? min(static_cast<long long>(S.sk_tiles) * K, sk_a + S.sk_q) : 0;
+      int j = sk ? static_cast<int>(sk_a / K) : 0;
+      const int j_end = sk ? static_cast<int>((sk_b - 1) / K) + 1 : 1;
+      bool ok = true;
+      for (; j < j_end; ++j) {
+        uint32_t pu = unit, kb = 0u, part = PART_TILE | PART_LAST | (1u << 8);
+        if (sk) {
+          pu = S.sk_tile[j];
+          const long long t0 = j * K;
+          const int kb0 = static_cast<int>(max(sk_a, t0) - t0), kb1 = static_cast<int>(min(sk_b, t0 + K) - t0);
+          const int first = static_cast<int>(t0 / S.sk_q), last = static_cast<int>((t0 + K - 1) / S.sk_q);
+          kb = static_cast<uint32_t>(kb0) | (static_cast<uint32_t>(kb1) << 16);
+          part = static_cast<uint32_t>(unit_n(unit) - first) | (static_cast<uint32_t>(last - first + 1) << 8) |
+                 (j + 1 == j_end ? PART_LAST : 0u) | (static_cast<uint32_t>(j) << 16);
+        } else if (S.kind == STAGE_GEMM) {
+          const int kb0 = unit_ks(unit) * S.kps, kb1 = min(S.k_iters, kb0 + S.kps);
+          kb = static_cast<uint32_t>(kb0) | (static_cast<uint32_t>(kb1) << 16);
+          part = static_cast<uint32_t>(unit_ks(unit)) | (static_cast<uint32_t>(S.splits) << 8) | PART_LAST | PART_TILE;
+        }
+        if (!wait_bar(&sc->uq_empty[q], qphase ^ 1u, sc, p, 5)) {
+          ok = false;
+          break;
+        }
+        push_unit(sc, q, pu, idx, lane, consumer, kb, part);
+        ++pushed;
+        if (S.kind == STAGE_GEMM && S.pf_b != nullptr) {
+          pf.unit = pu;
+          pf.seq = pushed;
+          pf.kb0 = piece_kb0(kb);
+          pf.kb1 = piece_kb1(kb);
+          pf.next = pf.kb0;
+        } else {
+          pf.unit = UNIT_END;
+        }
+        if (consumer && S.kind == STAGE_GEMM)
+          sched_poll_gemm<NS>(p, S, sc, q, unit_m(pu) * CL + static_cast<int>(rank), epoch1, pu, piece_kb0(kb),
+                              piece_kb1(kb), lane);
+        else if constexpr (ATTN)
+          if (consumer && S.kind == STAGE_ATTN)
+            sched_poll_attn<NS>(p, S, sc, q, (unit_m(pu) + 1) * CG - 1, unit_n(pu), epoch1, pu, lane);
+        if (lane == 0) trace_put(p, idx, rank, CL, 3, globaltimer());
+        if (++q == UQ) {
+          q = 0;
+          qphase ^= 1u;
+        }
       }
+      if (!ok) break;
     }
   } else if (warp == 0) {
     if (lane == 0) {
@@ -1562,6 +1626,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
       while (ok) {
         if (!wait_bar(&sc->uq_full[q], qphase, sc, p, 6)) break;
         const uint32_t unit = sc->uq[q];
+        const uint32_t kb = sc->uq_kb[q];
         mbar_arrive(&sc->uq_empty[q]);
         if (++q == UQ) {
           q = 0;
@@ -1570,10 +1635,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
         if (unit == UNIT_END) break;
         if (p.st[unit_stage(unit)].kind == STAGE_GEMM) {
           if (pair_leader) {
-            ok = mma_gemm_unit<NS, STAGE_BYTES, CG, CL, AR>(p, sc, ring, rp, unit, acc, acc_phase, rank);
+            ok = mma_gemm_unit<NS, STAGE_BYTES, CG, CL, AR>(p, sc, ring, rp, unit, piece_kb0(kb), piece_kb1(kb), acc,
+                                                            acc_phase, rank);
             issued = true;
           } else if constexpr (CL == 4) {
-            ok = fwd_gemm_unit<NS>(p, sc, rp, unit, rank);
+            ok = fwd_gemm_unit<NS>(p, sc, rp, piece_kb0(kb), piece_kb1(kb), rank);
           }
         } else if constexpr (ATTN) {
           if (pair_leader) {
@@ -1601,6 +1667,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
       if (!wait_bar(&sc->uq_full[q], qphase, sc, p, 7)) break;
       const uint32_t unit = sc->uq[q];
       const uint32_t tidx = sc->uq_idx[q];
+      const uint32_t part = sc->uq_part[q];
       __syncwarp();
       if (lane == 0) mbar_arrive(&sc->uq_empty[q]);
       if (++q == UQ) {
@@ -1609,7 +1676,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
       }
       if (unit == UNIT_END) break;
       if (p.st[unit_stage(unit)].kind == STAGE_GEMM)
-        ok = epi_gemm_unit<NS, CG, CL>(p, sc, staging, unit, acc, acc_phase, last_buf, rank, tidx, epoch1);
+        ok = epi_gemm_unit<NS, CG, CL>(p, sc, staging, unit, part, acc, acc_phase, last_buf, rank, tidx, epoch1);
       else if constexpr (ATTN)
         ok = epi_attn_unit<NS, CG>(p, sc, staging, unit, s_phase, o_phase, last_buf, tidx, acc, acc_phase, rank);
     }

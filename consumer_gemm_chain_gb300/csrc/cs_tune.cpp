@@ -214,6 +214,7 @@ struct TuneEntry {
   int layout = -1;  // cs_weight_layout, -1 = any
   int policy = -1;  // cs_policy, -1 = any
   int tile_m = 0, tile_n = 0, split_k = 0, group_m = 0;
+  int sk_tiles = 0, sk_units = 0;  // Stream-K tail of the last stage (0: none)
   double us = std::numeric_limits<double>::infinity();  // measured time per chain
 };
 
@@ -267,7 +268,9 @@ bool read_entry(const JVal& o, TuneEntry& e, std::string& err) {
       !int_field(o, "M", 1, 128 * 4095, true, &e.M, err) || !int_field(o, "sms", 1, 1 << 16, true, &e.sms, err) ||
       !int_field(o, "tile_m", 0, 512, true, &e.tile_m, err) || !int_field(o, "tile_n", 0, 256, true, &e.tile_n, err) ||
       !int_field(o, "split_k", 0, 15, true, &e.split_k, err) ||
-      !int_field(o, "group_m", 0, 4095, false, &e.group_m, err))
+      !int_field(o, "group_m", 0, 4095, false, &e.group_m, err) ||
+      !int_field(o, "sk_tiles", 0, 65534, false, &e.sk_tiles, err) ||
+      !int_field(o, "sk_units", 0, 16383, false, &e.sk_units, err))
     return false;
   if (e.tile_m != 0 && e.tile_m != 128 && e.tile_m != 256 && e.tile_m != 512) return err = "bad \"tile_m\"", false;
   if (e.tile_n != 0 && e.tile_n != 128 && e.tile_n != 256) return err = "bad \"tile_n\"", false;
@@ -324,6 +327,10 @@ int cs_tune_apply(const cs_chain_desc* in, int num_sms, cs_chain_desc* out) {
     out->tile_n = e.tile_n;
     out->split_k = e.split_k;
     out->group_m = e.group_m;
+    if (in->sk_tiles == 0 && in->sk_units == 0) {  // the desc leaves the Stream-K tail on auto
+      out->sk_tiles = e.sk_tiles;
+      out->sk_units = e.sk_units;
+    }
   }
   return best;
 }

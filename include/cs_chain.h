@@ -169,6 +169,22 @@ typedef struct cs_chain_desc {
                           Each Y tile then waits for its store to complete before
                           the epilogue moves on.  0 = off.                          */
   unsigned long long spin_timeout_ns; /* per-wait limit of a consumer tile; 0 = 2 s */
+  int sk_tiles;        /* Stream-K tail of the last GEMM stage (CuSync README, MLP
+                          paragraph: Stream-K as the other fix of the last
+                          thread-block wave).  The last sk_tiles tiles of that
+                          stage in dispatch order (at most those of the last row
+                          group) are not run as tiles; sk_units units instead
+                          each take an equal run of their concatenated K-slices,
+                          crossing tile boundaries.  A tile's contributing units
+                          write fp32 partial tiles to a plan-owned workspace; the
+                          last to finish sums them in K order (the same bits on
+                          every call and under every policy) and runs the
+                          epilogue.  Needs an unsplit last stage (split_k 1 there).
+                          0 = auto (the tuning table's choice, else none),
+                          -1 = none, n = that many tiles.                          */
+  int sk_units;        /* Stream-K units for those tiles; 0 = one per worker (SM,
+                          pair or cluster of the grid).  Each takes at least 8
+                          K-slices (fewer units then).                              */
 } cs_chain_desc;
 
 /* Fill *desc with defaults (kind MLP_GELU, F16, TILE, KN, auto everything else). */
@@ -284,6 +300,9 @@ typedef struct cs_chain_info {
   uint32_t* out_tile_sems;
   uint32_t* out_row_sems;
   size_t out_sem_words;    /* length of out_tile_sems */
+  int sk_tiles;            /* Stream-K tail actually used: tiles of the last stage, */
+  int sk_units;            /* units sharing their K-slices (0: none),               */
+  int sk_q;                /* K-slices per unit (the last one may hold fewer)       */
 } cs_chain_info;
 
 cs_status cs_chain_query(cs_chain_t plan, cs_chain_info* info);
@@ -307,7 +326,8 @@ int cs_library_features(void);
 
 /* Host-only: the dispatch order a plan with this desc and grid size would use.
  * Each entry encodes one unit as (stage << 30) | (k_split << 26) | (m_tile << 14) |
- * n_tile, m_tile counting tile_m-row tiles; for an ATTN stage n_tile is the head.  Row blocks are taken in groups of group_m; a
+ * n_tile, m_tile counting tile_m-row tiles; for an ATTN stage n_tile is the head;
+ * k_split 15 marks Stream-K unit n_tile of the last stage (desc.sk_tiles).  Row blocks are taken in groups of group_m; a
  * stage's units of one group are listed column-tile-major; at step t, stage s
  * lists group t - s*lag, so every producer a unit waits on is listed before it.  *n_out receives the count; entries beyond cap
  * are not written (cap may be 0 to query the count).  Needs no GPU. */
@@ -326,6 +346,8 @@ cs_status cs_schedule_build(const cs_chain_desc* desc, int num_sms, uint32_t* un
  *            "F": int, "M": int, "sms": int (grid the entry was measured on),
  *            "tile_m": 0|128|256|512, "tile_n": 0|128|256, "split_k": 0..15,
  *            optional "group_m": int >= 0 (default 0 = auto),
+ *            optional "sk_tiles": 0..65534, "sk_units": 0..16383 (Stream-K
+ *            tail, applied when the desc leaves both on 0; default 0 = none),
  *            optional "layout": "kn"|"nk"|"any", "policy": "tile"|"row"|
  *            "strided"|"stream"|"any" (default any), "us": time per chain (> 0)}
  * Other keys are ignored.  Matching: entries of the same kind, dtype, H, F and

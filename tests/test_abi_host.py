@@ -240,3 +240,66 @@ def test_closed_form_schedule_equals_the_loop_order(cs, kind, M, H, F, lag, grou
     got = [cs.decode_unit(u) for u in cs.cs_schedule_build(d, 152)]
     assert got == [(s, m, n, k) for s, m, n, k in want]
     assert q["n_units"] == len(got)
+
+
+def _sk_pieces(u, q, K, tiles):
+    """(tile, first slice, end slice, contributor, contributors) of Stream-K unit u."""
+    a, b = u * q, min(tiles * K, (u + 1) * q)
+    out = []
+    for j in range(a // K, (b - 1) // K + 1):
+        first, last = (j * K) // q, ((j + 1) * K - 1) // q
+        out.append((j, max(a, j * K) - j * K, min(b, (j + 1) * K) - j * K, u - first, last - first + 1))
+    return out
+
+
+@pytest.mark.parametrize("M,H,F,tile_m,sk_tiles,sk_units", [
+    (1024, 8192, 8192, 512, 14, 0), (1024, 8192, 8192, 512, 52, 0), (896, 8192, 8192, 512, 100, 0),
+    (1536, 8192, 8192, 256, 20, 76), (700, 1024, 2048, 128, 9, 40), (300, 512, 1024, 128, 3, 1000)])
+def test_stream_k_tail_schedule(cs, M, H, F, tile_m, sk_tiles, sk_units):
+    """The last sk_tiles tiles of the last stage leave the dispatch order and
+    Stream-K units (K-split field 15) take their place at its end; their K
+    ranges cover every K-slice of those tiles exactly once, each unit's share
+    is contiguous and at least 8 slices (or all of a shorter K), and each
+    tile's contributors are numbered in K order."""
+    d = cs.cs_chain_desc_init(M=M, H=H, F=F, tile_m=tile_m, tile_n=256 if tile_m > 128 else 128,
+                              sk_tiles=sk_tiles, sk_units=sk_units, weight_layout="nk", tuned=-1)
+    q = cs.cs_chain_plan_info(d, 152)
+    K = -(-F // 64)  # K-slices of the last stage (H = X W2: K = F)
+    tn = q["tile_n"][1]
+    last_group_tiles = (-(-M // tile_m) - (q["group_m"] * (-(-(-(-M // tile_m)) // q["group_m"]) - 1))) * -(-H // tn)
+    assert q["sk_tiles"] == min(sk_tiles, last_group_tiles)
+    assert q["sk_q"] >= min(8, K)
+    plain = cs.cs_chain_desc_init(M=M, H=H, F=F, tile_m=tile_m, tile_n=d.tile_n, sk_tiles=-1, weight_layout="nk",
+                                  tuned=-1)
+    base = [cs.decode_unit(u) for u in cs.cs_schedule_build(plain, 152)]
+    got = [cs.decode_unit(u) for u in cs.cs_schedule_build(d, 152)]
+    t, U = q["sk_tiles"], q["sk_units"]
+    assert got[:len(base) - t] == base[:len(base) - t]
+    assert got[len(base) - t:] == [(1, 0, u, 15) for u in range(U)]
+    assert q["n_units"] == len(got)
+    assert all(s == 1 and k == 0 for s, _, _, k in base[len(base) - t:])  # the replaced entries: last-stage tiles
+    cover = {}
+    for u in range(U):
+        pieces = _sk_pieces(u, q["sk_q"], K, t)
+        assert sum(e - b for _, b, e, _, _ in pieces) == min(q["sk_q"], t * K - u * q["sk_q"])
+        for j, b, e, c, nc in pieces:
+            assert 0 <= b < e <= K and 0 <= c < nc
+            cover.setdefault(j, []).append((b, e, c, nc))
+    for j in range(t):
+        parts = sorted(cover[j])
+        assert parts[0][0] == 0 and parts[-1][1] == K
+        assert all(a[1] == b[0] for a, b in zip(parts, parts[1:]))  # contiguous, no overlap
+        assert [c for _, _, c, _ in parts] == list(range(len(parts)))
+        assert all(nc == len(parts) for _, _, _, nc in parts)
+
+
+def test_stream_k_needs_an_unsplit_last_stage(cs):
+    d = cs.cs_chain_desc_init(M=64, H=4096, F=4096, split_k=4, sk_tiles=8, tuned=-1)
+    q = cs.cs_chain_plan_info(d, 152)
+    assert q["split_k"][1] == 4 and q["sk_tiles"] == 0 and q["sk_units"] == 0
+    for field, value in (("sk_tiles", -2), ("sk_tiles", 70000), ("sk_units", -1), ("sk_units", 20000)):
+        bad = cs.cs_chain_desc_init(M=64, H=256, F=1024)
+        setattr(bad, field, value)
+        with pytest.raises(cs.CSError) as e:
+            cs.cs_chain_plan_info(bad, 152)
+        assert e.value.status == cs.CS_ERR_INVALID_ARG

@@ -116,3 +116,30 @@ def test_launch_samples_spread_over_the_timed_region(steps):
     assert sorted(slot.values()) == list(range(len(slot)))
     assert 0 in slot and len(slot) <= 201
     assert max(slot) >= steps - max(1, steps // 200)  # the last calls are sampled too
+
+
+def _rec(sm, claim, first, acc, done, unit=0):
+    # timestamps are ns of the global timer; 0 means "not reached", so offset them
+    return [unit, sm, 1000 + claim, 1000 + claim, 1000 + first, 1000 + acc, 1000 + acc, 1000 + done]
+
+
+def test_sm_busy_stats_on_a_hand_made_timeline():
+    # SM 0 runs two units back to back over [0, 10]; SM 1 one unit over [0, 4];
+    # SM 2 gets no unit.  The tail starts when the first SM has finished: at 0
+    # for the idle SM 2.
+    recs = [_rec(0, 0, 0, 5, 6), _rec(0, 4, 5, 10, 10), _rec(1, 0, 0, 4, 4)]
+    st = bench.sm_busy_stats(recs, 3)
+    assert st["span_us"] == pytest.approx(10 / 1e3)
+    assert st["busy_frac"] == pytest.approx(14 / 30)
+    assert st["tail_us"] == pytest.approx(10 / 1e3) and st["tail_busy_frac"] == pytest.approx(14 / 30)
+    # with every SM used, the tail opens when SM 1 finishes at 4
+    st = bench.sm_busy_stats(recs, 2)
+    assert st["busy_frac"] == pytest.approx(14 / 20)
+    assert st["tail_us"] == pytest.approx(6 / 1e3)
+    assert st["tail_busy_frac"] == pytest.approx(6 / 12)
+    assert st["tail_idle_sm_us"] == pytest.approx(6 / 1e3)
+
+
+def test_union_of_overlapping_intervals():
+    assert bench._union_len([(0, 5), (3, 8), (10, 12)]) == 10
+    assert bench._union_len([(0, 5), (3, 8), (10, 12)], 4, 11) == 5

@@ -175,3 +175,20 @@ def test_attention_pair_tiles_agree_with_single_sm_tiles(M):
     assert oracle.rel_err(outs[128], Yref) <= TOL
     assert oracle.rel_err(outs[256], Yref) <= TOL
     assert oracle.rel_err(outs[256], outs[128]) <= 1e-3
+
+
+@pytest.mark.parametrize("tile_m", [128, 256])
+def test_attention_stream_k_tail_on_the_output_projection(tile_m):
+    inp = cs_inputs.make_custom("attn", 520, 512, 384, seed=37)
+    dev = device_tensors(inp, "nk")
+    outs = {}
+    for pol in ("row", "tile", "stream"):
+        with plan_for(inp, pol, "nk", tile_m=tile_m, sk_tiles=6, group_m=1) as plan:
+            q = cs.cs_chain_query(plan)
+            assert q["sk_units"] > 0
+            cs.cs_chain_debug_poison_intermediate(plan, -1)
+            outs[pol] = forward(plan, dev).cpu()
+    Yref, _, _ = _oracle(inp)
+    assert oracle.rel_err(outs["row"], Yref) <= TOL
+    for k, v in outs.items():
+        assert torch.equal(v, outs["row"]), k

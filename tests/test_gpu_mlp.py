@@ -506,3 +506,55 @@ def test_replica_build_runs_the_chain_without_multicast():
     assert float(err) <= TOL
     full = cs.cs_chain_desc_init(kind="gelu", M=1024, H=512, F=1024, weight_layout="nk", tuned=-1)
     assert cs.cs_chain_plan_info(full, 152)["tile_m"] == 512  # this process: the full build
+
+
+@pytest.mark.parametrize("kind,tile_m,tile_n,sk_tiles,sk_units", [
+    ("gelu", 128, 128, 9, 40), ("gelu", 128, 256, 20, 0), ("gelu", 256, 256, 13, 76), ("gelu", 512, 256, 14, 0),
+    ("gelu", 512, 256, 52, 0), ("swiglu", 512, 256, 20, 0), ("swiglu", 128, 128, 30, 7)])
+def test_stream_k_tail(kind, tile_m, tile_n, sk_tiles, sk_units):
+    """The last stage's trailing tiles shared out as Stream-K units (K ranges
+    crossing tile boundaries, partial tiles summed in K order by the last
+    contributor): parity with the oracle, the same bits under every policy
+    (the two-kernel control's last launch carries the same tail), under
+    producer delays with the intermediate and every partial poisoned, and
+    across the 2^32 wrap of the arrival counters."""
+    inp = cs_inputs.make_custom(kind, 1000, 1024, 2048 if kind == "gelu" else 1376, seed=15)
+    dev = device_tensors(inp, "nk")
+    kw = dict(tile_m=tile_m, tile_n=tile_n, sk_tiles=sk_tiles, sk_units=sk_units, group_m=1)
+    outs = {}
+    for pol in ("tile", "row", "strided", "stream"):
+        with plan_for(inp, pol, "nk", **kw) as plan:
+            q = cs.cs_chain_query(plan)
+            assert q["sk_tiles"] > 0 and q["sk_units"] > 0, q
+            outs[pol] = forward(plan, dev).cpu()
+            if pol == "tile":
+                g = torch.Generator().manual_seed(16)
+                cs.cs_chain_debug_set_delays(plan, 0, (torch.rand(q["units"][0], generator=g) * 100_000).long().tolist())
+                for _ in range(2):
+                    assert torch.equal(poisoned_forward(plan, dev).cpu(), outs[pol])
+                cs.cs_chain_debug_set_delays(plan, 0, None)
+                cs.cs_chain_debug_set_epoch(plan, 0xFFFFFFFE)
+                for _ in range(3):
+                    assert torch.equal(poisoned_forward(plan, dev).cpu(), outs[pol])
+    Yref, _ = _oracle(inp)
+    assert oracle.rel_err(outs["tile"], Yref) <= TOL
+    for k, v in outs.items():
+        assert torch.equal(v, outs["tile"]), k
+    with plan_for(inp, "tile", "nk", tile_m=tile_m, tile_n=tile_n, sk_tiles=-1, group_m=1) as plain:
+        assert cs.cs_chain_query(plain)["sk_units"] == 0
+        Yplain = forward(plain, dev).cpu()
+    assert oracle.rel_err(outs["tile"], Yplain) <= 1e-3  # only the tail tiles' summation order differs
+
+
+@pytest.mark.parametrize("M", [896, 1024, 1408, 1536])
+def test_stream_k_on_the_stress_shape(M):
+    inp = cs_inputs.make_inputs("stress", M=M, seed=0)
+    dev = device_tensors(inp, "nk")
+    rows = cs_inputs.sample_rows(M, 32)
+    Yref, _ = _oracle(inp, rows)
+    with plan_for(inp, "tile", "nk", sk_tiles=64, tuned=-1) as plan:
+        q = cs.cs_chain_query(plan)
+        assert q["sk_units"] > 0
+        Y = poisoned_forward(plan, dev).cpu()
+        assert torch.equal(poisoned_forward(plan, dev).cpu(), Y)
+    assert oracle.rel_err(Y[rows], Yref) <= TOL
