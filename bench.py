@@ -713,15 +713,20 @@ def sm_busy_stats(recs, n_sm):
             per_sm.setdefault(r[1] & 0xFFFF, []).append((r[4], r[6]))
     span = t1 - t0
     busy = sum(_union_len(iv) for iv in per_sm.values())
-    # SMs without any unit are idle from the start
-    last = [max(b for _, b in iv) for iv in per_sm.values()] + [t0] * max(0, n_sm - len(per_sm))
-    tail0 = min(last)
+    # The tail is measured over the SMs that ran units: SMs that host no CTA
+    # of a cluster shape (a GPC whose SM count is not a multiple of the
+    # cluster size) are idle for the whole launch and are reported apart.
+    used = len(per_sm)
+    last = [max(b for _, b in iv) for iv in per_sm.values()]
+    tail0 = min(last) if last else t1
     tail = t1 - tail0
     tail_busy = sum(_union_len(iv, tail0, t1) for iv in per_sm.values())
     return {"span_us": span / 1e3, "busy_frac": busy / (n_sm * span) if span else None,
+            "busy_frac_used_sms": busy / (used * span) if span and used else None,
             "idle_sm_us": (n_sm * span - busy) / 1e3, "tail_us": tail / 1e3,
-            "tail_busy_frac": tail_busy / (n_sm * tail) if tail > 0 else None,
-            "tail_idle_sm_us": (n_sm * tail - tail_busy) / 1e3, "sms_used": len(per_sm), "t_start": t0, "t_end": t1}
+            "tail_busy_frac": tail_busy / (used * tail) if tail > 0 and used else None,
+            "tail_idle_sm_us": (used * tail - tail_busy) / 1e3, "sms_used": used, "sms_unused": n_sm - used,
+            "t_start": t0, "t_end": t1}
 
 
 def traced_forward(cs, torch, plan, fwd):
@@ -994,7 +999,7 @@ def other_configs(cs, torch, peaks, lay):
                 rec["tail"] = {k: tail_stats(cs, torch, plans[k], fns[k]) for k in ("tile", "stream")}
             except Exception as e:  # a side measurement that fails must not cost the bench line
                 rec["tail"] = {"error": repr(e)[:200]}
-        workers = q["num_sms"] * 128 // q["tile_m"]
+        workers = q["workers"]
         tiles0 = q["sched_units"][0]
         rec["stage0_units"], rec["workers"] = tiles0, workers
         rec["waves_remainder"] = [tiles0 // workers, tiles0 % workers]

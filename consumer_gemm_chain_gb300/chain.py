@@ -95,7 +95,8 @@ class cs_chain_info(ctypes.Structure):
                 ("intermediate", ctypes.c_void_p * 2), ("sem_words", ctypes.c_size_t * 2),
                 ("policy", ctypes.c_int), ("tuned_entry", ctypes.c_int),
                 ("out_tile_sems", ctypes.c_void_p), ("out_row_sems", ctypes.c_void_p), ("out_sem_words", ctypes.c_size_t),
-                ("sk_tiles", ctypes.c_int), ("sk_units", ctypes.c_int), ("sk_q", ctypes.c_int)]
+                ("sk_tiles", ctypes.c_int), ("sk_units", ctypes.c_int), ("sk_q", ctypes.c_int),
+                ("workers", ctypes.c_int)]
 
 
 def _load() -> ctypes.CDLL:
@@ -365,7 +366,8 @@ def _info_dict(i: cs_chain_info) -> dict:
             "stride": i.stride, "intermediate": [i.intermediate[0], i.intermediate[1]],
             "sem_words": [i.sem_words[0], i.sem_words[1]], "policy": POLICY_NAMES.get(i.policy, i.policy),
             "tuned_entry": i.tuned_entry, "out_tile_sems": i.out_tile_sems, "out_row_sems": i.out_row_sems,
-            "out_sem_words": i.out_sem_words, "sk_tiles": i.sk_tiles, "sk_units": i.sk_units, "sk_q": i.sk_q}
+            "out_sem_words": i.out_sem_words, "sk_tiles": i.sk_tiles, "sk_units": i.sk_units, "sk_q": i.sk_q,
+            "workers": i.workers}
 
 
 def cs_schedule_build(desc: cs_chain_desc, num_sms: int) -> list[int]:

@@ -125,6 +125,7 @@ struct cs_chain_s {
   int n_fused = 0;
   uint32_t* sched_stage[3] = {nullptr, nullptr, nullptr};
   int n_stage[3] = {0, 0, 0};  // entries of each stage-alone schedule (Stream-K units included)
+  int workers = 0;             // clusters (or CTAs) of the plan's shape resident at once
   // Stream-K tail of the last stage (geometry in sk_*; partial tiles owned here)
   int sk_tiles = 0, sk_units = 0, sk_q = 0, sk_max_nc = 0;
   float* sk_partial = nullptr;
@@ -257,7 +258,7 @@ cs_chain_desc resolve_desc(const cs_chain_desc* d, int num_sms, int* entry) {
   return t;
 }
 
-Geometry geometry(const cs_chain_desc* d, int num_sms) {
+Geometry geometry(const cs_chain_desc* d, int num_sms, int workers = 0) {
   Geometry g;
   const int blocks = cdiv(d->M, cs::BM);
   // 256-wide tiles need 2/3 of the operand bytes per FLOP of 128-wide ones;
@@ -371,7 +372,7 @@ Geometry geometry(const cs_chain_desc* d, int num_sms) {
     const int tiles = std::min(d->sk_tiles, last_rows * g.n_tiles[fs]);
     const long long K = g.k_iters[fs];
     const long long work = static_cast<long long>(tiles) * K;
-    const int units = d->sk_units > 0 ? d->sk_units : capacity;
+    const int units = d->sk_units > 0 ? d->sk_units : (workers > 0 ? workers : capacity);
     long long q = (work + units - 1) / units;
     q = std::max<long long>(q, std::min<long long>(kSkMinSlices, K));
     q = std::max<long long>(q, (K + kSkMaxContrib - 2) / (kSkMaxContrib - 1));
@@ -507,6 +508,7 @@ void info_geometry(const cs_chain_s* p, int n_fused, cs_chain_info* info) {
   info->sk_tiles = p->sk_tiles;
   info->sk_units = p->sk_units;
   info->sk_q = p->sk_q;
+  info->workers = p->workers > 0 ? p->workers : p->num_sms / p->cl;
 }
 
 int device_sms(int* out) {
@@ -714,13 +716,62 @@ void fill_mlp_stages(const cs_chain_s* p, const cs_mlp_args* a, cs::KParams& kp)
   kp.acc_stride = (s0.mma_n > 128 || s1.mma_n > 128) ? 256 : 128;
 }
 
+// The kernel instantiation a plan runs (its shared-memory size set once).
+cs_status kernel_for(const cs_chain_s* p, const void** fn) {
+  cs_status s;
+#define CS_KERNEL(...)                                                                  \
+  do {                                                                                  \
+    if ((s = set_smem_attr<__VA_ARGS__>()) != CS_OK) return s;                           \
+    *fn = reinterpret_cast<const void*>(cs::cs_chain_kernel<__VA_ARGS__>);              \
+    return CS_OK;                                                                       \
+  } while (0)
+  if (p->d.kind == CS_CHAIN_ATTN && p->cg == 2) CS_KERNEL(NS_A, SB_A, 2, true);
+  if (p->d.kind == CS_CHAIN_ATTN) CS_KERNEL(NS_A, SB_A, 1, true);
+#ifndef CS_NO_CLUSTER_MULTICAST
+  if (p->cl == 4) CS_KERNEL(NS_A, SB_A, 2, false, 4);
+#endif
+  if (p->cg == 2) CS_KERNEL(NS_A, SB_A, 2, false);
+  if (p->cfg_s == 1) CS_KERNEL(NS_S, SB_S, 1, false, 1, 8);
+  if (p->cfg_s == 2) CS_KERNEL(NS_T, SB_T, 1, false, 1, 8);
+  if (p->cfg_b) CS_KERNEL(NS_B, SB_B, 1, false);
+  CS_KERNEL(NS_A, SB_A, 1, false);
+#undef CS_KERNEL
+}
+
+// Clusters of the plan's shape that can be resident at once: a GPC whose SM
+// count is not a multiple of the cluster size leaves SMs idle (on a 152-SM
+// GB300, 36 clusters of 4 CTAs, 144 SMs).
+cs_status resident_workers(const cs_chain_s* p, int* workers) {
+  *workers = p->num_sms / p->cl;
+  if (p->cl == 1) return CS_OK;
+  const void* fn = nullptr;
+  cs_status s = kernel_for(p, &fn);
+  if (s != CS_OK) return s;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(p->num_sms);
+  cfg.blockDim = dim3(cs::NUM_THREADS);
+  cfg.dynamicSmemBytes = p->smem;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = static_cast<unsigned>(p->cl);
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  CS_CUDA(cudaOccupancyMaxActiveClusters(&n, fn, &cfg));
+  if (n >= 1 && n < *workers) *workers = n;
+  return CS_OK;
+}
+
 cs_status launch(cs_chain_s* p, cs::KParams& kp, const uint32_t* sched, int n_units, cudaStream_t stream) {
   kp.sched = sched;
   kp.n_units = n_units;
   // a schedule with Stream-K units is followed by the table of their tiles
   kp.st[p->stages - 1].sk_tile = sched + n_units;
-  // one CTA per SM, clusters of cl CTAs per unit; no more clusters than units
-  int grid = p->num_sms / p->cl;
+  // one CTA per SM, clusters of cl CTAs per unit: as many clusters as can be
+  // resident at once, and no more than units
+  int grid = p->workers > 0 ? p->workers : p->num_sms / p->cl;
   if (grid > n_units) grid = n_units;
   if (grid < 1) grid = 1;
   grid *= p->cl;
@@ -747,35 +798,11 @@ cs_status launch(cs_chain_s* p, cs::KParams& kp, const uint32_t* sched, int n_un
   }
   cfg.attrs = n_attr ? attr : nullptr;
   cfg.numAttrs = n_attr;
-  cudaError_t e;
-  cs_status s;
-  if (p->d.kind == CS_CHAIN_ATTN && p->cg == 2) {
-    if ((s = set_smem_attr<NS_A, SB_A, 2, true>()) != CS_OK) return s;
-    e = cudaLaunchKernelEx(&cfg, cs::cs_chain_kernel<NS_A, SB_A, 2, true>, kp);
-  } else if (p->d.kind == CS_CHAIN_ATTN) {
-    if ((s = set_smem_attr<NS_A, SB_A, 1, true>()) != CS_OK) return s;
-    e = cudaLaunchKernelEx(&cfg, cs::cs_chain_kernel<NS_A, SB_A, 1, true>, kp);
-#ifndef CS_NO_CLUSTER_MULTICAST
-  } else if (p->cl == 4) {
-    if ((s = set_smem_attr<NS_A, SB_A, 2, false, 4>()) != CS_OK) return s;
-    e = cudaLaunchKernelEx(&cfg, cs::cs_chain_kernel<NS_A, SB_A, 2, false, 4>, kp);
-#endif
-  } else if (p->cg == 2) {
-    if ((s = set_smem_attr<NS_A, SB_A, 2, false>()) != CS_OK) return s;
-    e = cudaLaunchKernelEx(&cfg, cs::cs_chain_kernel<NS_A, SB_A, 2, false>, kp);
-  } else if (p->cfg_s == 1) {
-    if ((s = set_smem_attr<NS_S, SB_S, 1, false, 1, 8>()) != CS_OK) return s;
-    e = cudaLaunchKernelEx(&cfg, cs::cs_chain_kernel<NS_S, SB_S, 1, false, 1, 8>, kp);
-  } else if (p->cfg_s == 2) {
-    if ((s = set_smem_attr<NS_T, SB_T, 1, false, 1, 8>()) != CS_OK) return s;
-    e = cudaLaunchKernelEx(&cfg, cs::cs_chain_kernel<NS_T, SB_T, 1, false, 1, 8>, kp);
-  } else if (p->cfg_b) {
-    if ((s = set_smem_attr<NS_B, SB_B, 1, false>()) != CS_OK) return s;
-    e = cudaLaunchKernelEx(&cfg, cs::cs_chain_kernel<NS_B, SB_B, 1, false>, kp);
-  } else {
-    if ((s = set_smem_attr<NS_A, SB_A, 1, false>()) != CS_OK) return s;
-    e = cudaLaunchKernelEx(&cfg, cs::cs_chain_kernel<NS_A, SB_A, 1, false>, kp);
-  }
+  const void* fn = nullptr;
+  cs_status s = kernel_for(p, &fn);
+  if (s != CS_OK) return s;
+  void* args[] = {&kp};
+  const cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
   if (e != cudaSuccess) return fail(CS_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
   return CS_OK;
 }
@@ -979,10 +1006,21 @@ cs_status cs_chain_plan(const cs_chain_desc* desc, cs_chain_t* out) {
   cs_chain_s* p = new (std::nothrow) cs_chain_s();
   if (!p) return fail(CS_ERR_OOM, "host allocation failed");
   p->device = dev;
-  p->num_sms = desc->num_sms > 0 && desc->num_sms < sms ? desc->num_sms : sms;
+  const int grid_sms = desc->num_sms > 0 && desc->num_sms < sms ? desc->num_sms : sms;
+  p->num_sms = grid_sms;
   p->d = resolve_desc(desc, p->num_sms, &p->tuned_entry);
   Geometry g = geometry(&p->d, p->num_sms);
   shape_plan(p, g, desc->kind, desc->M);
+  if ((s = resident_workers(p, &p->workers)) != CS_OK) {
+    delete p;
+    return s;
+  }
+  if (g.sk_units > 0 && p->d.sk_units == 0 && p->workers != p->num_sms / g.cl) {
+    // one Stream-K unit per resident worker
+    p->num_sms = grid_sms;
+    g = geometry(&p->d, grid_sms, p->workers);
+    shape_plan(p, g, desc->kind, desc->M);
+  }
 
   auto bail = [&](cs_status st) {
     free_plan(p);
@@ -1489,6 +1527,7 @@ cs_status cs_mlp_forward_noalloc(const cs_chain_desc* desc, const cs_mlp_args* a
   p.num_sms = desc->num_sms > 0 && desc->num_sms < sms ? desc->num_sms : sms;
   Geometry g = geometry(&p.d, p.num_sms);
   shape_plan(&p, g, desc->kind, desc->M);
+  if ((s = resident_workers(&p, &p.workers)) != CS_OK) return s;
   const cs::SchedGeo sg = sched_geo(g);
   const long long n_fused = cs::sched_fused_count(sg);
   const long long n_st0 = cs::sched_stage_count(sg, 0), n_st1 = cs::sched_stage_count(sg, 1);

@@ -392,29 +392,43 @@ __device__ bool tma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
   const int bcols = gate_up ? S.bn : S.bn / CG;              // this CTA's share of B's rows
   const int col0 = n * S.bn + (gate_up ? 0 : prank * bcols);
   const int map_b = gate_up && prank == 1 ? S.map_b2 : S.map_b;
-  // Stage completion goes to the leader's full barrier (each CTA of a pair adds
-  // its bytes); with CL = 4 every CTA counts its own bytes (its A, and its B
-  // columns: one half fetched here, one multicast by the other pair).
-  auto expect = [&](const RingPos& r) {
-    if constexpr (CG == 1 || CL == 4) {
-      mbar_arrive_expect_tx(&sc->full[r.slot], bytes);
-    } else {
-      if (rank == 0)
-        mbar_arrive_expect_tx(&sc->full[r.slot], bytes);
-      else
-        mbar_expect_tx_remote(mapa_shared(&sc->full[r.slot], 0), bytes);
+  int ready_kb = do_wait ? kb0 : kb1;  // slices below this bound may load now
+  for (int kb = kb0; kb < kb1; ++kb) {
+    if (rank == 0 && kb == claim_at) mbar_arrive(&sc->claim_req);
+    if (kb >= ready_kb) {
+      ready_kb = tma_wait_slices(sc, q, kb, S.dep_bn, p);
+      if (ready_kb < 0) return false;
     }
-  };
-  auto load = [&](const RingPos& r, void* dst, const CUtensorMap* map, int x, int y) {
-    if constexpr (CG == 1 || CL == 4)
-      tma_load_2d(dst, map, x, y, &sc->full[r.slot]);
-    else
-      tma_load_2d_pair(dst, map, x, y, mapa_shared(&sc->full[r.slot], 0));
-  };
-  // The weight slice of K-slice k into stage r (after the stage's expect_tx).
-  auto issue_b = [&](int k, const RingPos& r) {
-    expect(r);
-    uint8_t* sb = ring + r.slot * STAGE_BYTES + A_BYTES;
+    if (!wait_bar(&sc->empty[rp.slot], rp.phase ^ 1u, sc, p, 1)) return false;
+    uint8_t* sa = ring + rp.slot * STAGE_BYTES;
+    uint8_t* sb = sa + A_BYTES;
+    // Completion goes to the pair leader's full barrier: each CTA of a pair adds
+    // its bytes (with CL = 4 its A, and its B columns: one half fetched here,
+    // one multicast by the other pair, which counts them on this pair's leader).
+    uint32_t bar_addr;
+    if constexpr (CG == 1) {
+      bar_addr = smem_u32(&sc->full[rp.slot]);
+      mbar_arrive_expect_tx(&sc->full[rp.slot], bytes);
+    } else {
+      bar_addr = mapa_shared(&sc->full[rp.slot], rank & ~1u);
+      if ((rank & 1u) == 0u)
+        mbar_arrive_expect_tx(&sc->full[rp.slot], bytes);
+      else
+        mbar_expect_tx_remote(bar_addr, bytes);
+    }
+    auto load = [&](void* dst, const CUtensorMap* map, int x, int y) {
+      if constexpr (CG == 1)
+        tma_load_2d(dst, map, x, y, &sc->full[rp.slot]);
+      else
+        tma_load_2d_pair(dst, map, x, y, bar_addr);
+    };
+    if (kb == kb0) {
+      sc->tma_seq = sc->tma_seq + 1;
+      trace_put(p, tidx, rank, CL, 4, globaltimer());
+    }
+    sc->tma_kb = kb;
+    if (kb == kb1 - 1) trace_put(p, tidx, rank, CL, 5, globaltimer());
+    load(sa, &p.maps[S.map_a], kb * BK, row0);
 #ifndef CS_NO_CLUSTER_MULTICAST
     if constexpr (CL == 4) {
       // this CTA fetches half of its B columns (the half of its pair index)
@@ -424,15 +438,16 @@ __device__ bool tma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
       const CUtensorMap* bm = &p.maps[map_b];
       if (S.b_major == 0) {
         // weights [N, K]: a box of 64 K x bcols/2 N rows
-        tma_load_2d_mc(sb + part * (bcols / 2) * (BK * 2), bm, k * BK, col0 + part * (bcols / 2), &sc->full[r.slot],
-                       mask);
+        tma_load_2d_mc_pair(sb + part * (bcols / 2) * (BK * 2), bm, kb * BK, col0 + part * (bcols / 2), bar_addr,
+                            mask);
       } else {
         // weights [K, N]: every other 64-column box (8 KB each)
         for (int h = part; h < bcols / 64; h += 2)
-          tma_load_2d_mc(sb + h * 8192, bm, col0 + h * 64, k * BK, &sc->full[r.slot], mask);
+          tma_load_2d_mc_pair(sb + h * 8192, bm, col0 + h * 64, kb * BK, bar_addr, mask);
       }
-      sc->issued_parity[r.slot] = static_cast<int>(r.phase);
-      return;
+      sc->issued_parity[rp.slot] = static_cast<int>(rp.phase);
+      rp.next<NS>();
+      continue;
     }
 #endif  // CS_NO_CLUSTER_MULTICAST
     // B operand(s): this CTA's bcols rows of N per operand; a second operand
@@ -444,54 +459,13 @@ __device__ bool tma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
       uint8_t* dst = sb + op * bcols * (BK * 2);
       if (S.b_major == 0) {
         // weights [N, K]: one box of 64 K x bcols N rows
-        load(r, dst, bm, k * BK, col0);
+        load(dst, bm, kb * BK, col0);
       } else {
         // weights [K, N]: boxes of 64 N (contiguous) x 64 K rows (8 KB), one per 64 columns
-        for (int h = 0; h < bcols / 64; ++h) load(r, dst + h * 8192, bm, col0 + h * 64, k * BK);
+        for (int h = 0; h < bcols / 64; ++h) load(dst + h * 8192, bm, col0 + h * 64, kb * BK);
       }
     }
-    sc->issued_parity[r.slot] = static_cast<int>(r.phase);
-  };
-  auto issue_a = [&](int k, const RingPos& r) { load(r, ring + r.slot * STAGE_BYTES, &p.maps[S.map_a], k * BK, row0); };
-  // A consumer whose next K-slice is not yet released streams the weight
-  // slices of the following K-slices into the free stages while it waits (the
-  // weights do not depend on the producers): slices [kb, kb_b) have their B
-  // (and their stage's expect_tx) issued, B-only, at ring positions from rp.
-  int kb_b = kb0;
-  RingPos rpb = rp;
-  int ready_kb = do_wait ? kb0 : kb1;  // slices below this bound may load now
-  for (int kb = kb0; kb < kb1; ++kb) {
-    if (rank == 0 && kb == claim_at) mbar_arrive(&sc->claim_req);
-    if (kb >= ready_kb) {
-      const int need = (kb * BK) / S.dep_bn + 1;
-      while (kb_b < kb1 && kb_b < kb + NS && static_cast<int>(ld_acquire_cta_shared(&sc->uq_ready[q])) < need &&
-             mbar_test_wait(&sc->empty[rpb.slot], rpb.phase ^ 1u)) {
-        issue_b(kb_b, rpb);
-        ++kb_b;
-        rpb.next<NS>();
-      }
-      ready_kb = tma_wait_slices(sc, q, kb, S.dep_bn, p);
-      if (ready_kb < 0) {
-        // the forward is void; complete the stages that already hold B so that
-        // no copy stays in flight on an incomplete barrier
-        for (RingPos r = rp; kb < kb_b; ++kb, r.next<NS>()) issue_a(kb, r);
-        return false;
-      }
-    }
-    if (kb >= kb_b) {
-      if (!wait_bar(&sc->empty[rp.slot], rp.phase ^ 1u, sc, p, 1)) return false;
-      issue_b(kb, rp);
-      kb_b = kb + 1;
-      rpb = rp;
-      rpb.next<NS>();
-    }
-    if (kb == kb0) {
-      sc->tma_seq = sc->tma_seq + 1;
-      trace_put(p, tidx, rank, CL, 4, globaltimer());
-    }
-    sc->tma_kb = kb;
-    if (kb == kb1 - 1) trace_put(p, tidx, rank, CL, 5, globaltimer());
-    issue_a(kb, rp);
+    sc->issued_parity[rp.slot] = static_cast<int>(rp.phase);
     rp.next<NS>();
   }
   return true;
@@ -532,19 +506,6 @@ __device__ bool mma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
   tc_commit<CG>(&sc->tfull[acc], pair_mask);
   acc ^= 1u;
   if (acc == 0u) acc_phase ^= 1u;
-  return true;
-}
-
-// CL = 4, the second CTA of a pair: its stage is full once its own copies and
-// the other pair's multicast have landed; pass that on to the pair's leader,
-// whose full barrier waits for both CTAs before it issues the pair MMA.
-template <int NS>
-__device__ bool fwd_gemm_unit(const KParams& p, SmemCtl<NS>* sc, RingPos& rp, int kb0, int kb1, uint32_t rank) {
-  for (int kb = kb0; kb < kb1; ++kb) {
-    if (!wait_bar(&sc->full[rp.slot], rp.phase, sc, p, 13)) return false;
-    mbar_arrive_cluster_relaxed(mapa_shared(&sc->full[rp.slot], rank & ~1u));
-    rp.next<NS>();
-  }
   return true;
 }
 
@@ -1460,9 +1421,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
-      // CL = CG: one expect_tx arrival per CTA of the tile, on the leader's
-      // barrier; CL = 4: the own arrival, plus (pair leader) the peer's relay
-      mbar_init(&sc->full[i], CL == 4 ? (pair_leader ? 2 : 1) : CG);
+      // one expect_tx arrival per CTA of the pair, on the pair leader's barrier
+      // (CL = 4: each pair's leader counts its own pair's bytes)
+      mbar_init(&sc->full[i], CG);
       // CL = 4: both pairs' MMAs must be done with a stage before it refills
       mbar_init(&sc->empty[i], CL == 4 ? 2 : 1);
       sc->issued_parity[i] = -1;
@@ -1627,10 +1588,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
         if (unit == UNIT_END) break;
       }
       // Let every load this thread issued land before the CTA can exit.  In
-      // pair mode the loads complete on the leader's barrier, which its MMA
-      // waits for; after an abort, give in-flight copies a bounded grace time.
-      // CL = 4: each CTA's barrier counts every copy into its shared memory.
-      if constexpr (CG == 1 || CL == 4) {
+      // pair mode (and CL = 4) the loads complete on the pair leader's barrier,
+      // which its MMA waits for; after an abort, give in-flight copies a bounded
+      // grace time.
+      if constexpr (CG == 1) {
         for (int i = 0; i < NS; ++i)
           if (sc->issued_parity[i] >= 0) {
             const uint64_t t0 = globaltimer();
@@ -1664,8 +1625,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
             ok = mma_gemm_unit<NS, STAGE_BYTES, CG, CL, AR>(p, sc, ring, rp, unit, piece_kb0(kb), piece_kb1(kb), acc,
                                                             acc_phase, rank);
             issued = true;
-          } else if constexpr (CL == 4) {
-            ok = fwd_gemm_unit<NS>(p, sc, rp, piece_kb0(kb), piece_kb1(kb), rank);
           }
         } else if constexpr (ATTN) {
           if (pair_leader) {

@@ -101,12 +101,6 @@ __device__ __forceinline__ uint32_t mapa_shared(const void* p, uint32_t rank) {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
-// Relaxed remote arrive: a relay of a completion the caller has observed on
-// its own barrier (the data it stands for is already in shared memory), so no
-// cluster-scope release (measured: the release form cost ~0.4 us per call).
-__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
 __device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t cluster_addr, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_addr),
                "r"(bytes)
@@ -211,6 +205,18 @@ __device__ __forceinline__ void tma_load_2d_mc(void* smem_dst, const CUtensorMap
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], "
       "[%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(cta_mask)
+      : "memory");
+}
+// Multicast load of a CTA pair (cta_group::2): the box lands at the same
+// shared-memory offset in every CTA of `cta_mask`, and each destination counts
+// the bytes on the mbarrier at that offset in the leader (even rank) of its own
+// CTA pair; `bar_cluster_addr` names that barrier in the issuing CTA's pair.
+__device__ __forceinline__ void tma_load_2d_mc_pair(void* smem_dst, const CUtensorMap* map, int x, int y,
+                                                    uint32_t bar_cluster_addr, uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::"
+      "cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster_addr), "h"(cta_mask)
       : "memory");
 }
 #endif  // CS_NO_CLUSTER_MULTICAST

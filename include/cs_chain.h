@@ -303,6 +303,11 @@ typedef struct cs_chain_info {
   int sk_tiles;            /* Stream-K tail actually used: tiles of the last stage, */
   int sk_units;            /* units sharing their K-slices (0: none),               */
   int sk_q;                /* K-slices per unit (the last one may hold fewer)       */
+  int workers;             /* units the grid runs at once: CTAs, or clusters of
+                              tile_m / 128 CTAs that can be resident together (a
+                              GPC whose SM count is not a multiple of the cluster
+                              size leaves SMs out); cs_chain_plan_info, which needs
+                              no GPU, reports num_sms / (tile_m / 128)          */
 } cs_chain_info;
 
 cs_status cs_chain_query(cs_chain_t plan, cs_chain_info* info);

@@ -125,14 +125,15 @@ def _rec(sm, claim, first, acc, done, unit=0):
 
 def test_sm_busy_stats_on_a_hand_made_timeline():
     # SM 0 runs two units back to back over [0, 10]; SM 1 one unit over [0, 4];
-    # SM 2 gets no unit.  The tail starts when the first SM has finished: at 0
-    # for the idle SM 2.
+    # SM 2 gets no unit: it counts against the whole-launch busy fraction and
+    # is reported as unused, while the tail (from SM 1's end at 4) is measured
+    # over the two SMs that ran units.
     recs = [_rec(0, 0, 0, 5, 6), _rec(0, 4, 5, 10, 10), _rec(1, 0, 0, 4, 4)]
     st = bench.sm_busy_stats(recs, 3)
     assert st["span_us"] == pytest.approx(10 / 1e3)
-    assert st["busy_frac"] == pytest.approx(14 / 30)
-    assert st["tail_us"] == pytest.approx(10 / 1e3) and st["tail_busy_frac"] == pytest.approx(14 / 30)
-    # with every SM used, the tail opens when SM 1 finishes at 4
+    assert st["busy_frac"] == pytest.approx(14 / 30) and st["busy_frac_used_sms"] == pytest.approx(14 / 20)
+    assert st["sms_used"] == 2 and st["sms_unused"] == 1
+    assert st["tail_us"] == pytest.approx(6 / 1e3) and st["tail_busy_frac"] == pytest.approx(6 / 12)
     st = bench.sm_busy_stats(recs, 2)
     assert st["busy_frac"] == pytest.approx(14 / 20)
     assert st["tail_us"] == pytest.approx(6 / 1e3)
