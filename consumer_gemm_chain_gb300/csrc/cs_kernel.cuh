@@ -392,6 +392,9 @@ __device__ bool tma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
   const int bcols = gate_up ? S.bn : S.bn / CG;              // this CTA's share of B's rows
   const int col0 = n * S.bn + (gate_up ? 0 : prank * bcols);
   const int map_b = gate_up && prank == 1 ? S.map_b2 : S.map_b;
+  // activations and the intermediate stay in L2, the weights stream through
+  const uint64_t pol_a = policy_evict_last();
+  const uint64_t pol_b = policy_evict_first();
   int ready_kb = do_wait ? kb0 : kb1;  // slices below this bound may load now
   for (int kb = kb0; kb < kb1; ++kb) {
     if (rank == 0 && kb == claim_at) mbar_arrive(&sc->claim_req);
@@ -416,11 +419,11 @@ __device__ bool tma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
       else
         mbar_expect_tx_remote(bar_addr, bytes);
     }
-    auto load = [&](void* dst, const CUtensorMap* map, int x, int y) {
+    auto load = [&](void* dst, const CUtensorMap* map, int x, int y, uint64_t pol) {
       if constexpr (CG == 1)
-        tma_load_2d(dst, map, x, y, &sc->full[rp.slot]);
+        tma_load_2d_h(dst, map, x, y, &sc->full[rp.slot], pol);
       else
-        tma_load_2d_pair(dst, map, x, y, bar_addr);
+        tma_load_2d_pair_h(dst, map, x, y, bar_addr, pol);
     };
     if (kb == kb0) {
       sc->tma_seq = sc->tma_seq + 1;
@@ -428,7 +431,7 @@ __device__ bool tma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
     }
     sc->tma_kb = kb;
     if (kb == kb1 - 1) trace_put(p, tidx, rank, CL, 5, globaltimer());
-    load(sa, &p.maps[S.map_a], kb * BK, row0);
+    load(sa, &p.maps[S.map_a], kb * BK, row0, pol_a);
 #ifndef CS_NO_CLUSTER_MULTICAST
     if constexpr (CL == 4) {
       // this CTA fetches half of its B columns (the half of its pair index)
@@ -438,12 +441,12 @@ __device__ bool tma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
       const CUtensorMap* bm = &p.maps[map_b];
       if (S.b_major == 0) {
         // weights [N, K]: a box of 64 K x bcols/2 N rows
-        tma_load_2d_mc_pair(sb + part * (bcols / 2) * (BK * 2), bm, kb * BK, col0 + part * (bcols / 2), bar_addr,
-                            mask);
+        tma_load_2d_mc_pair_h(sb + part * (bcols / 2) * (BK * 2), bm, kb * BK, col0 + part * (bcols / 2), bar_addr,
+                              mask, pol_b);
       } else {
         // weights [K, N]: every other 64-column box (8 KB each)
         for (int h = part; h < bcols / 64; h += 2)
-          tma_load_2d_mc_pair(sb + h * 8192, bm, col0 + h * 64, kb * BK, bar_addr, mask);
+          tma_load_2d_mc_pair_h(sb + h * 8192, bm, col0 + h * 64, kb * BK, bar_addr, mask, pol_b);
       }
       sc->issued_parity[rp.slot] = static_cast<int>(rp.phase);
       rp.next<NS>();
@@ -459,10 +462,10 @@ __device__ bool tma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
       uint8_t* dst = sb + op * bcols * (BK * 2);
       if (S.b_major == 0) {
         // weights [N, K]: one box of 64 K x bcols N rows
-        load(dst, bm, kb * BK, col0);
+        load(dst, bm, kb * BK, col0, pol_b);
       } else {
         // weights [K, N]: boxes of 64 N (contiguous) x 64 K rows (8 KB), one per 64 columns
-        for (int h = 0; h < bcols / 64; ++h) load(dst + h * 8192, bm, col0 + h * 64, kb * BK);
+        for (int h = 0; h < bcols / 64; ++h) load(dst + h * 8192, bm, col0 + h * 64, kb * BK, pol_b);
       }
     }
     sc->issued_parity[rp.slot] = static_cast<int>(rp.phase);

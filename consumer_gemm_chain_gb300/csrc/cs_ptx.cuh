@@ -194,29 +194,53 @@ __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorM
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster_addr)
       : "memory");
 }
-#ifndef CS_NO_CLUSTER_MULTICAST
-// Multicast load: the box lands at the same shared-memory offset in every CTA
-// of `cta_mask`, and each of them counts the bytes on its own mbarrier at the
-// offset of `bar`.  Left out of the replica build (CS_NO_CLUSTER_MULTICAST),
-// the one that processes sharing a node with other GPUs' ranks load.
-__device__ __forceinline__ void tma_load_2d_mc(void* smem_dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
-                                               uint16_t cta_mask) {
+
+// L2 eviction policies for the cache_hint loads below (createpolicy, the whole
+// access range at that priority).  Measured on the chains: the weights stream
+// through once per forward (evict_first) while the activations, the
+// intermediate and the partial tiles stay (evict_last) -- GPT-3 M=1 71 -> 67.5
+// us, attention M=16 77 -> 64 us, large M unchanged.
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+// tma_load_2d / tma_load_2d_pair with an L2 eviction policy.
+__device__ __forceinline__ void tma_load_2d_h(void* smem_dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                              uint64_t pol) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], "
-      "[%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(cta_mask)
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, "
+      "{%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(pol)
       : "memory");
 }
-// Multicast load of a CTA pair (cta_group::2): the box lands at the same
-// shared-memory offset in every CTA of `cta_mask`, and each destination counts
-// the bytes on the mbarrier at that offset in the leader (even rank) of its own
-// CTA pair; `bar_cluster_addr` names that barrier in the issuing CTA's pair.
-__device__ __forceinline__ void tma_load_2d_mc_pair(void* smem_dst, const CUtensorMap* map, int x, int y,
-                                                    uint32_t bar_cluster_addr, uint16_t cta_mask) {
+__device__ __forceinline__ void tma_load_2d_pair_h(void* smem_dst, const CUtensorMap* map, int x, int y,
+                                                   uint32_t bar_cluster_addr, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster_addr), "l"(pol)
+      : "memory");
+}
+#ifndef CS_NO_CLUSTER_MULTICAST
+// Multicast load of a CTA pair (cta_group::2) with an L2 eviction policy: the
+// box lands at the same shared-memory offset in every CTA of `cta_mask`, and
+// each destination counts the bytes on the mbarrier at that offset in the
+// leader (even rank) of its own CTA pair; `bar_cluster_addr` names that
+// barrier in the issuing CTA's pair.  Left out of the replica build
+// (CS_NO_CLUSTER_MULTICAST), the one that processes sharing a node with other
+// GPUs' ranks load.
+__device__ __forceinline__ void tma_load_2d_mc_pair_h(void* smem_dst, const CUtensorMap* map, int x, int y,
+                                                      uint32_t bar_cluster_addr, uint16_t cta_mask, uint64_t pol) {
   asm volatile(
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::"
-      "cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster_addr), "h"(cta_mask)
+      "cluster.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster_addr), "h"(cta_mask), "l"(pol)
       : "memory");
 }
 #endif  // CS_NO_CLUSTER_MULTICAST
