@@ -594,7 +594,8 @@ __device__ void release_tile(const KParams& p, const StageP& S, int mb, int n, i
       }
     }
     if (p.release && S.rel_tile != nullptr && u != S.skip_unit) {
-      __threadfence();
+      // the barrier above ordered every epilogue thread's stores (the TMA
+      // stores waited for and fenced to the generic proxy) before this release
       red_release_gpu_add(S.rel_tile + u, 1u);
       red_release_gpu_add(S.rel_row + mb, 1u);
     }
@@ -736,7 +737,6 @@ __device__ void epi_split_rows_small(const KParams& p, const StageP& S, SmemCtl<
               make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
     }
   }
-  __threadfence();
 }
 
 template <int NS, int CG, int CL>
@@ -802,19 +802,19 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
     release_tmem();
     acc ^= 1u;
     if (acc == 0u) acc_phase ^= 1u;
-    __threadfence();
+    // the CTA barrier orders every thread's partial stores before the one
+    // acq_rel arrival (release: this split's partial; acquire, for the last
+    // split: every other split's, read after the next barrier)
     named_bar_sync(1, EPI_THREADS);
     if (threadIdx.x == EPI_WARP0 * 32) {
-      const uint32_t old = atomicAdd(S.split_ctr + mb * S.n_tiles + n, 1u);
+      const uint32_t old = atom_add_acq_rel_gpu(S.split_ctr + mb * S.n_tiles + n, 1u);
       sc->split_last = (old + 1u == epoch1 * static_cast<uint32_t>(nc)) ? 1 : 0;
-      __threadfence();
     }
     named_bar_sync(1, EPI_THREADS);
     if (!sc->split_last) {
       if (threadIdx.x == EPI_WARP0 * 32) trace_put(p, tidx, rank, CL, 7, globaltimer());
       return true;
     }
-    __threadfence();
   }
   // at most 48 valid rows (the last split of the tile): cooperative passes
   // and plain row stores; the loop below is skipped (measured against the
