@@ -900,6 +900,16 @@ def extras(cs, torch, inp, dev, Y, make_plan, plan, M, kind, peaks, stream):
     return out
 
 
+def stream_k_remainder(q):
+    """Tiles of the last stage left over after whole waves of a plan's units
+    (0 when the plan splits its last stage or fills its waves)."""
+    last = q["stages"] - 1
+    if q["split_k"][last] != 1:
+        return 0
+    rem = sum(q["sched_units"][: q["stages"]]) % q["workers"]
+    return rem if rem <= q["sched_units"][last] else 0
+
+
 def plan_record(q):
     """Tile shape, K-splits and tuning entry of a plan, for the sweep records."""
     return {"tile_m": q["tile_m"], "tile_n": q["tile_n"][q["stages"] - 1], "split_k": max(q["split_k"]),
@@ -992,6 +1002,17 @@ def other_configs(cs, torch, peaks, lay):
                     rec["plan"] = plan_record(q)
                 fns[key] = (lambda p=p: cs.cs_mlp_forward(p, Y=Ym, **sub))
                 plans[key] = p
+            # Stream-K tail of the TileSync plan's tiles: the last stage's tiles
+            # left over after whole waves, shared by one unit per resident worker
+            sk = stream_k_remainder(q)
+            if sk:
+                d = cs.cs_chain_desc_init(kind="gelu", M=m, H=inp.H, F=inp.F, dtype=inp.dtype, policy="tile",
+                                          weight_layout=lay, tile_m=q["tile_m"], tile_n=q["tile_n"][1],
+                                          split_k=1, group_m=q["group_m"], sk_tiles=sk)
+                p = es.enter_context(cs.cs_chain_plan(d))
+                rec["stream_k_plan"] = {"sk_tiles": cs.cs_chain_query(p)["sk_tiles"],
+                                        "sk_units": cs.cs_chain_query(p)["sk_units"]}
+                fns["tile_sk"] = (lambda p=p: cs.cs_mlp_forward(p, Y=Ym, **sub))
             for key, ms in interleaved_times(fns).items():
                 rec[f"{key}_us"] = ms * 1e3
             # SM occupancy of one traced forward of the fused chain and of the control
@@ -1008,6 +1029,8 @@ def other_configs(cs, torch, peaks, lay):
         rec["tflops_tile"] = fl / (rec["tile_us"] * 1e-6) / 1e12
         rec["roofline_frac_tile"], _ = _roof_frac(fl, chain_bytes("gelu", m, inp.H, inp.F), rec["tile_us"], peaks)
         rec["best_policy_vs_control"] = rec["stream_us"] / best
+        if "tile_sk_us" in rec:
+            rec["stream_k_vs_tile"] = rec["tile_us"] / rec["tile_sk_us"]
         rows.append(rec)
     res["stress"] = rows
     return res

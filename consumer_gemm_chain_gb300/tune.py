@@ -7,7 +7,8 @@ GPU and environment).
     python -m consumer_gemm_chain_gb300.tune --preset gpt3 [--M 1,16,...] [--out FILE] [--merge]
     python -m consumer_gemm_chain_gb300.tune --shape gelu,8192,4096,bf16 --layout kn --M 64,512,4096
 
-Per M: every candidate runs under TileSync (RowSync for the attention chain);
+Per M: every candidate runs under TileSync (RowSync for the attention chain),
+and Stream-K tails of the last stage on the two fastest unsplit tile shapes;
 the three fastest are timed again under every policy, including the
 two-kernel control (so that the control, too, runs its best tiles); the best
 candidate of each policy is re-timed against the built-in rules in
@@ -106,13 +107,32 @@ def _time(torch, fn, target_ms=12.0, warm_ms=60.0, repeats=1):
 
 
 class Candidate:
-    def __init__(self, kind, shape, policy, tile_m=0, tile_n=0, split_k=0, tuned=-1):
-        self.key = (tile_m, tile_n, split_k)
+    def __init__(self, kind, shape, policy, tile_m=0, tile_n=0, split_k=0, sk_tiles=0, sk_units=0, tuned=-1):
+        self.key = (tile_m, tile_n, split_k, sk_tiles, sk_units)
         self.policy = policy
         self.desc = cs.cs_chain_desc_init(kind=kind, M=shape["M"], H=shape["H"], F=shape["F"],
                                           dtype=shape["dtype"], policy=policy, weight_layout=shape["layout"],
                                           heads=shape["heads"] or 12, tile_m=tile_m, tile_n=tile_n,
-                                          split_k=split_k, tuned=tuned)
+                                          split_k=split_k, sk_tiles=sk_tiles if sk_tiles else -1,
+                                          sk_units=sk_units, tuned=tuned)
+
+
+def stream_k_candidates(info):
+    """Stream-K tails worth timing for a plan of unsplit tiles: the last stage's
+    tiles left over after whole waves of all the plan's units (the last wave),
+    that remainder plus half a wave, each shared by one or two units per worker
+    (the resident workers the plan reports)."""
+    last = info["stages"] - 1
+    if info["split_k"][last] != 1:
+        return []
+    w = info["workers"]
+    total = sum(info["sched_units"][: info["stages"]])
+    rem = total % w
+    out = []
+    for tiles in (rem, rem + w // 2):
+        if 0 < tiles <= info["sched_units"][last]:
+            out += [(tiles, w), (tiles, 2 * w)]
+    return out
 
 
 def _forward(plan, kind, t, Y):
@@ -165,7 +185,7 @@ def tune_shape(torch, kind, H, F, dtype, heads, Ms, log=print, layout="nk"):
             torch.cuda.synchronize()
             ref = Y.clone()
         # 1: every tile shape x split under the base policy
-        first = {}
+        first, infos = {}, {}
         for tm, tn in tiles:
             for sp in splits:
                 if sp > 4 and tm > 128:
@@ -180,6 +200,18 @@ def tune_shape(torch, kind, H, F, dtype, heads, Ms, log=print, layout="nk"):
                 if real != (tm, tn, sp):
                     continue  # clamped to another candidate (too few K-slices for the split)
                 first[c.key] = us
+                infos[c.key] = info
+        # 1b: Stream-K tails on the two fastest unsplit tile shapes
+        unsplit = sorted((k for k in first if k[2] == 1), key=first.get)[:2]
+        for key in unsplit:
+            for skt, sku in stream_k_candidates(infos[key]):
+                c = Candidate(kind, shape, base, key[0], key[1], key[2], skt, sku)
+                try:
+                    us, info = run(c)
+                except cs.CSError:
+                    continue
+                if info["sk_tiles"] == skt:
+                    first[c.key] = us
         top = sorted(first, key=first.get)[:3]
         # 2: the three fastest under every policy (the control included)
         best = {}
@@ -204,13 +236,17 @@ def tune_shape(torch, kind, H, F, dtype, heads, Ms, log=print, layout="nk"):
             us = statistics.median(times[(pol, "tuned")])
             us_auto = statistics.median(times[(pol, "builtin")])
             if us < (1.0 - MARGIN) * us_auto:
-                tm, tn, sp = finals[pol].key
+                tm, tn, sp, skt, sku = finals[pol].key
             else:
-                tm, tn, sp, us = 0, 0, 0, us_auto
-            entries.append({"kind": kind, "dtype": dtype, "H": H, "F": F, "M": M, "sms": sms, "layout": layout,
-                            "policy": pol, "tile_m": tm, "tile_n": tn, "split_k": sp, "group_m": 0,
-                            "us": round(us, 2), "builtin_us": round(us_auto, 2)})
-            choice = f"tile {tm}x{tn} split {sp:2d}" if tm else "built-in rules    "
+                tm, tn, sp, skt, sku, us = 0, 0, 0, 0, 0, us_auto
+            entry = {"kind": kind, "dtype": dtype, "H": H, "F": F, "M": M, "sms": sms, "layout": layout,
+                     "policy": pol, "tile_m": tm, "tile_n": tn, "split_k": sp, "group_m": 0,
+                     "us": round(us, 2), "builtin_us": round(us_auto, 2)}
+            if skt:
+                entry.update(sk_tiles=skt, sk_units=sku)
+            entries.append(entry)
+            choice = (f"tile {tm}x{tn} split {sp:2d}" + (f" stream-K {skt}/{sku}" if skt else "")) if tm else \
+                "built-in rules    "
             log(f"{kind} M={M:5d} {pol:8s} {choice}: {us:8.1f} us (built-in rules {us_auto:8.1f} us)")
         del t, Y, ref
         torch.cuda.empty_cache()

@@ -144,3 +144,11 @@ def test_sm_busy_stats_on_a_hand_made_timeline():
 def test_union_of_overlapping_intervals():
     assert bench._union_len([(0, 5), (3, 8), (10, 12)]) == 10
     assert bench._union_len([(0, 5), (3, 8), (10, 12)], 4, 11) == 5
+
+
+def test_stream_k_remainder_is_the_last_wave_of_the_last_stage():
+    q = {"stages": 2, "split_k": [1, 1, 1], "sched_units": [96, 96, 0], "workers": 36}
+    assert bench.stream_k_remainder(q) == (96 + 96) % 36  # 12 tiles after five whole waves
+    assert bench.stream_k_remainder(dict(q, sched_units=[90, 90, 0])) == 0  # whole waves
+    assert bench.stream_k_remainder(dict(q, split_k=[1, 3, 1])) == 0  # a split last stage takes no tail
+    assert bench.stream_k_remainder(dict(q, sched_units=[70, 10, 0], workers=40)) == 0  # remainder > last stage
