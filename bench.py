@@ -114,7 +114,7 @@ def parse(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="gpt3", choices=["gpt3", "stress", "llama", "tiny"])
+    ap.add_argument("--workload", default="gpt3", choices=["gpt3", "stress", "llama", "tiny", "attn"])
     ap.add_argument("--M", type=int, default=None)
     ap.add_argument("--policy", default="tile", choices=["tile", "row", "strided", "stream"])
     ap.add_argument("--layout", default="nk", choices=["kn", "nk"],
@@ -346,6 +346,10 @@ def time_cpu_oracle(inp, target_s):
 def _oracle_rows(oracle, inp, rows):
     if inp.kind == "gelu":
         return oracle.mlp_gelu(inp.X[rows], inp.W1, inp.b1, inp.W2)
+    if inp.kind == "attn":
+        # causal: the first r output rows depend on the first r input rows only
+        assert rows == list(range(len(rows)))
+        return oracle.attention_chain(inp.X[: len(rows)], inp.Wqkv, inp.Wo, heads=inp.F // 128, head_dim=128)
     return oracle.mlp_swiglu(inp.X[rows], inp.Wg, inp.Wu, inp.W2)
 
 
@@ -471,7 +475,8 @@ STEADY_S = 1.5  # seconds of the steady-state timing beside a short timed region
 
 def workload_config(name, M, inp, policy, layout="nk"):
     desc = {"gpt3": "GPT-3 175B 8-way TP MLP shard", "stress": "last-wave stress two-GEMM GeLU chain",
-            "llama": "LLaMA 65.2B 8-way TP SwiGLU shard", "tiny": "tiny MLP chain"}[name]
+            "llama": "LLaMA 65.2B 8-way TP SwiGLU shard", "tiny": "tiny MLP chain",
+            "attn": "GPT-3 attention shard (QKV GEMM, 12-head causal attention, output projection)"}[name]
     return {"workload": f"{desc}: X[{M},{inp.H}] -> F={inp.F} -> H={inp.H}, {str(inp.dtype).split('.')[-1]}, "
                         f"policy={policy}",
             "M": M, "H": inp.H, "F": inp.F, "policy": policy, "accumulate": "fp32",
@@ -481,13 +486,14 @@ def workload_config(name, M, inp, policy, layout="nk"):
 
 # ------------------------------------------------------------------ our arm
 def plan_desc(cs, args, inp, policy, M, pdl=None, tuned=0, out_release=0):
-    """The desc of a plan of the bench's MLP workload `inp` with M rows, the
-    command line's choices applied."""
+    """The desc of a plan of the bench's workload `inp` with M rows, the command
+    line's choices applied."""
+    extra = dict(heads=inp.F // 128, head_dim=128) if inp.kind == "attn" else {}
     return cs.cs_chain_desc_init(kind=inp.kind, M=M, H=inp.H, F=inp.F, dtype=inp.dtype, policy=policy,
                                  weight_layout=args.layout, lag=args.lag, tile_n=args.tile_n, group_m=args.group_m,
                                  tile_m=args.tile_m, split_k=args.split_k, prefetch=args.prefetch,
                                  raster=args.raster, pdl=args.pdl if pdl is None else pdl, tuned=tuned,
-                                 out_release=out_release)
+                                 out_release=out_release, **extra)
 
 
 def main():
@@ -519,8 +525,10 @@ def main():
     dev = {"X": X}
     if kind == "gelu":
         dev.update(W1=w(inp.W1), b1=inp.b1.to(device), W2=w(inp.W2))
-    else:
+    elif kind == "swiglu":
         dev.update(Wg=w(inp.Wg), Wu=w(inp.Wu), W2=w(inp.W2))
+    else:
+        dev.update(Wqkv=w(inp.Wqkv), Wo=w(inp.Wo))
     Y = torch.empty_like(X)
 
     def make_plan(policy, MM=M, pdl=None, tuned=0, out_release=0):
@@ -534,7 +542,10 @@ def main():
         return
 
     def step():
-        cs.cs_mlp_forward(plan, Y=Y, **dev)
+        if kind == "attn":
+            cs.cs_attn_chain_forward(plan, X, dev["Wqkv"], dev["Wo"], Y)
+        else:
+            cs.cs_mlp_forward(plan, Y=Y, **dev)
 
     flops = chain_flops(kind, M, inp.H, inp.F)
     nbytes = chain_bytes(kind, M, inp.H, inp.F)
@@ -593,7 +604,8 @@ def main():
     traffic_key = f"{args.workload}_M{M}_{args.policy}_{lay}"
     roof.update({"traffic": measured_traffic(traffic_key, schedule_sha(cs, plan.desc, plan_info["num_sms"])),
                  "peak_source": f"{peak_src} ({'sustained' if sustained else 'burst'})",
-                 "kernel": ("cs_chain_kernel<6,32768,2,0,4> (4-CTA clusters)" if plan_info["tile_m"] == 512 else
+                 "kernel": (f"cs_chain_kernel<6,32768,{plan_info['tile_m'] // 128},1> (attention)" if kind == "attn" else
+                            "cs_chain_kernel<6,32768,2,0,4> (4-CTA clusters)" if plan_info["tile_m"] == 512 else
                             "cs_chain_kernel<6,32768,2>" if plan_info["tile_m"] == 256 else
                             "cs_chain_kernel<4,49152,1>" if (kind == "swiglu" or 256 in plan_info["tile_n"])
                             else "cs_chain_kernel<6,32768,1>"),
@@ -628,18 +640,27 @@ def main():
     # out (pinned buffers); the copies of consecutive steps overlap the kernels
     wts = {k: v for k, v in dev.items() if k != "X"}
 
-    def e2e_step():
-        cs.cs_mlp_forward_host(plan, X=Xh, Y=Yh, **wts)
+    if kind == "attn":
+        # the attention chain has no host-memory entry point: each step copies
+        # X in, runs the chain and copies Y out on the stream, in series
+        def e2e_step():
+            X.copy_(Xh, non_blocking=True)
+            step()
+            Yh.copy_(Y, non_blocking=True)
+        finish, api = None, "cs_attn_chain_forward with the X upload and Y read-back on the same stream"
+    else:
+        def e2e_step():
+            cs.cs_mlp_forward_host(plan, X=Xh, Y=Yh, **wts)
+        finish, api = (lambda: cs.cs_chain_host_join(plan, stream)), \
+            "cs_mlp_forward_host (double-buffered copies on two copy streams)"
 
-    e2e_ms, _ = time_loop(e2e_step, max(3, min(args.steps, 200)), 3, stream,
-                          finish=lambda: cs.cs_chain_host_join(plan, stream))
+    e2e_ms, _ = time_loop(e2e_step, max(3, min(args.steps, 200)), 3, stream, finish=finish)
     e2e_ms = max_over_ranks(e2e_ms, ws, device)
     line["e2e"] = {"value": whole_job_tflops(flops, e2e_ms, ws), "unit": "TFLOP/s",
                    "h2d_bytes_per_step": Xh.numel() * Xh.element_size(),
-                   "d2h_bytes_per_step": Yh.numel() * Yh.element_size(), "ms_per_step": e2e_ms,
-                   "api": "cs_mlp_forward_host (double-buffered copies on two copy streams)"}
+                   "d2h_bytes_per_step": Yh.numel() * Yh.element_size(), "ms_per_step": e2e_ms, "api": api}
 
-    if rank == 0 and runs_extras(ws, args.quick):
+    if rank == 0 and runs_extras(ws, args.quick) and kind != "attn":
         line["extras"] = extras(cs, torch, inp, dev, Y, make_plan, plan, M, kind, peaks, stream)
         if args.workload == "gpt3":
             line["extras"]["other_configs"] = other_configs(cs, torch, peaks, lay)
