@@ -1027,10 +1027,10 @@ def other_configs(cs, torch, peaks, lay):
             # left over after whole waves, shared by one unit per resident worker
             sk = stream_k_remainder(q)
             if sk:
-                d = cs.cs_chain_desc_init(kind="gelu", M=m, H=inp.H, F=inp.F, dtype=inp.dtype, policy="tile",
-                                          weight_layout=lay, tile_m=q["tile_m"], tile_n=q["tile_n"][1],
-                                          split_k=1, group_m=q["group_m"], sk_tiles=sk)
-                p = es.enter_context(cs.cs_chain_plan(d))
+                dsk = cs.cs_chain_desc_init(kind="gelu", M=m, H=inp.H, F=inp.F, dtype=inp.dtype, policy="tile",
+                                            weight_layout=lay, tile_m=q["tile_m"], tile_n=q["tile_n"][1],
+                                            split_k=1, group_m=q["group_m"], sk_tiles=sk)
+                p = es.enter_context(cs.cs_chain_plan(dsk))
                 rec["stream_k_plan"] = {"sk_tiles": cs.cs_chain_query(p)["sk_tiles"],
                                         "sk_units": cs.cs_chain_query(p)["sk_units"]}
                 fns["tile_sk"] = (lambda p=p: cs.cs_mlp_forward(p, Y=Ym, **sub))
