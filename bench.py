@@ -234,8 +234,8 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ timing helpers
 def sampled_calls(steps, most=200):
-    """{call index: event-pair slot} for about `most` calls spread evenly over `steps`."""
-    every = max(1, steps // most)
+    """{call index: event-pair slot} for at most `most` calls spread evenly over `steps`."""
+    every = max(1, -(-steps // most))
     return {i: k for k, i in enumerate(range(0, steps, every))}
 
 

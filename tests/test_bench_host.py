@@ -152,3 +152,14 @@ def test_stream_k_remainder_is_the_last_wave_of_the_last_stage():
     assert bench.stream_k_remainder(dict(q, sched_units=[90, 90, 0])) == 0  # whole waves
     assert bench.stream_k_remainder(dict(q, split_k=[1, 3, 1])) == 0  # a split last stage takes no tail
     assert bench.stream_k_remainder(dict(q, sched_units=[70, 10, 0], workers=40)) == 0  # remainder > last stage
+
+
+@pytest.mark.parametrize("steps", [1, 5, 199, 200, 201, 250, 399, 400, 401, 2000, 3875])
+def test_sampled_calls_never_exceed_the_limit_and_spread_evenly(steps):
+    s = bench.sampled_calls(steps)
+    assert 1 <= len(s) <= 200
+    assert sorted(s.values()) == list(range(len(s)))
+    idx = sorted(s)
+    assert idx[0] == 0 and all(i < steps for i in idx)
+    gaps = {b - a for a, b in zip(idx, idx[1:])}
+    assert len(gaps) <= 1  # one stride
