@@ -37,7 +37,8 @@ def _oracle_rows(inp, rows):
     return Y[rows]
 
 
-@pytest.mark.parametrize("workload,M", [("gpt3", 1), ("gpt3", 256), ("gpt3", 2048), ("llama", 64), ("llama", 1024),
+@pytest.mark.parametrize("workload,M", [("gpt3", 1), ("gpt3", 256), ("gpt3", 512), ("gpt3", 2048), ("llama", 64),
+                                        ("llama", 1024),
                                         ("attn", 16), ("attn", 512), ("stress", 384), ("stress", 1152)])
 def test_tuned_plans_match_the_oracle(tuned_table, workload, M):
     inp = cs_inputs.make_inputs(workload, M=M, seed=0)
@@ -59,3 +60,21 @@ def test_tuned_plans_match_the_oracle(tuned_table, workload, M):
     # tiled differently, the same sums up to fp32 rounding order and the
     # rounding of the intermediate to the input type (one bf16 ulp is 2^-8)
     assert oracle.rel_err(outs[0], outs[-1]) <= (2e-3 if inp.dtype == torch.float16 else 1e-2)
+
+
+def test_the_table_selects_a_stream_k_tail_where_it_won(tuned_table):
+    """Entries that recorded a Stream-K tail give plans that run it (and match
+    the oracle through the tuned-plan test above); the plan reports the tail."""
+    import json
+    with open(cs.chain.TUNE_TABLE) as f:
+        entries = [e for e in json.load(f)["entries"] if e.get("sk_tiles")]
+    if not entries:
+        pytest.skip("no entry of the shipped table chose a Stream-K tail")
+    e = entries[0]
+    desc = cs.cs_chain_desc_init(kind=e["kind"], M=e["M"], H=e["H"], F=e["F"],
+                                 dtype=torch.float16 if e["dtype"] == "f16" else torch.bfloat16,
+                                 policy=e["policy"], weight_layout=e.get("layout", "nk"))
+    with cs.cs_chain_plan(desc) as plan:
+        q = cs.cs_chain_query(plan)
+    assert q["tuned_entry"] >= 0
+    assert q["sk_tiles"] == e["sk_tiles"] and q["sk_units"] == e["sk_units"]
