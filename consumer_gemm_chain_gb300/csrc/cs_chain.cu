@@ -352,10 +352,15 @@ Geometry geometry(const cs_chain_desc* d, int num_sms, int workers = 0) {
   // tiles also at least two groups, so that the lag lets the consumers of one
   // group overlap the next (measured: M=1024 pairs 0.61 -> 0.67 of peak;
   // single-SM tiles prefer one group); 512-row tiles: groups of one tile row
-  // up to M = 1024, else of two (1024 rows) (measured at GPT-3 M=1024: 209 us
-  // with two 512-row groups, 225 us with one group of 1024 rows)
+  // up to M = 1024 (measured at GPT-3 M=1024: 209 us with two 512-row groups,
+  // 225 us with one group of 1024 rows), beyond that as below
+  // GeLU chains on 512-row tiles from three tile rows: one group of up to four
+  // tile rows, so every weight box is read once per 2048 rows (measured in
+  // steady state: GPT-3 M=1536 322 -> 313 us, M=2048 430 -> 428 us with 680 ->
+  // 442 MB of DRAM traffic per launch, stress M=1536 298 -> 286 us; SwiGLU at
+  // M=2048 185 -> 196 us, so it keeps groups of two)
   g.group_m = d->group_m > 0 ? d->group_m
-             : g.cl == 4   ? (g.m_tiles <= 2 ? 1 : 2)
+             : g.cl == 4   ? (g.m_tiles <= 2 ? 1 : d->kind == CS_CHAIN_MLP_GELU ? std::min(4, g.m_tiles) : 2)
              : g.cg == 2   ? std::max(1, std::min(4, g.m_tiles / 2))
                            : 8;
   g.row_major = d->raster == 2;

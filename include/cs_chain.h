@@ -114,7 +114,8 @@ typedef struct cs_chain_desc {
   int group_m;         /* schedule: tile rows per rasterisation group (units of a
                           group run column-tile-major so concurrent tiles share
                           weights in L2); 0 = auto (at most 1024 rows per group;
-                          with 256-row pair tiles at least two groups)              */
+                          with 256-row pair tiles at least two groups; GeLU chains
+                          on 512-row tiles from three tile rows: up to 2048 rows)   */
   int tile_n;          /* output columns per GEMM tile: 128 or 256; 0 = auto.
                           SwiGLU producer tiles are always 128 (gate|up = 256).     */
   int tile_m;          /* rows per GEMM tile: 128 (one SM), 256 (a 2-SM cluster
