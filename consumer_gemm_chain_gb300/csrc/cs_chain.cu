@@ -129,6 +129,10 @@ struct cs_chain_s {
   // Stream-K tail of the last stage (geometry in sk_*; partial tiles owned here)
   int sk_tiles = 0, sk_units = 0, sk_q = 0, sk_max_nc = 0;
   float* sk_partial = nullptr;
+  // attention pieces (kv key groups each, at most kv_max per row); their
+  // partial states live in partial[1], their arrivals in split_ctr[1]
+  int kv = 0, kv_max = 0;
+  size_t partial_bytes[3] = {0, 0, 0};
   uint32_t* delays[3] = {nullptr, nullptr, nullptr};
   unsigned long long* trace = nullptr;
   int trace_records = 0;
@@ -193,6 +197,9 @@ struct Geometry {
   // Stream-K tail of the last stage: its last sk_tiles tiles in dispatch order
   // become sk_units units of sk_q consecutive K-slices each (the last shorter)
   int sk_tiles = 0, sk_units = 0, sk_q = 0, sk_max_nc = 0;
+  // attention: units of tile row m cover key groups 0..m (tile_m / 128 key
+  // blocks each); with kv > 0 they run as ceil((m + 1) / kv) pieces of kv groups
+  int kv = 0, kv_max = 0;
 };
 
 // Smallest Stream-K share in K-slices, and the most contributors a tile may
@@ -216,6 +223,7 @@ cs_status validate(const cs_chain_desc* d) {
   if (d->pdl < -1 || d->pdl > 1) return fail(CS_ERR_INVALID_ARG, "pdl=%d (-1..1)", d->pdl);
   if (d->sk_tiles < -1 || d->sk_tiles > 65534) return fail(CS_ERR_INVALID_ARG, "sk_tiles=%d (-1..65534)", d->sk_tiles);
   if (d->sk_units < 0 || d->sk_units > 16383) return fail(CS_ERR_INVALID_ARG, "sk_units=%d (0..16383)", d->sk_units);
+  if (d->kv_chunk < -1 || d->kv_chunk > 4095) return fail(CS_ERR_INVALID_ARG, "kv_chunk=%d (-1..4095)", d->kv_chunk);
   if (d->H < 8 || d->H % 8 != 0 || d->H > (1 << 20)) return fail(CS_ERR_INVALID_ARG, "H=%d must be a positive multiple of 8", d->H);
   if (d->F < 8 || d->F % 8 != 0 || d->F > (1 << 20)) return fail(CS_ERR_INVALID_ARG, "F=%d must be a positive multiple of 8", d->F);
   if (d->stride < 0) return fail(CS_ERR_INVALID_ARG, "stride=%d", d->stride);
@@ -305,6 +313,18 @@ Geometry geometry(const cs_chain_desc* d, int num_sms, int workers = 0) {
     g.bn[2] = tn;
     g.n_tiles[2] = cdiv(d->H, tn);
     g.k_iters[2] = cdiv(d->F, cs::BK);
+    // Causal units grow with their row: the last rows' units set the chain's
+    // critical path once the QKV GEMM ends.  Pieces of kv key groups run them
+    // on several SMs at once; auto: at most four pieces per row from four tile
+    // rows.  At most 15 pieces per row (the unit's K-split field).
+    int kv = d->kv_chunk > 0 ? d->kv_chunk : (d->kv_chunk == 0 && g.m_tiles >= 4 ? cdiv(g.m_tiles, 4) : 0);
+    if (kv > 0) {
+      kv = std::max(kv, cdiv(g.m_tiles, 15));
+      if (kv < g.m_tiles) {
+        g.kv = kv;
+        g.kv_max = cdiv(g.m_tiles, kv);
+      }
+    }
   } else {
     g.stages = 2;
     g.bn[0] = d->kind == CS_CHAIN_MLP_SWIGLU ? 128 : tn;
@@ -407,6 +427,7 @@ cs::SchedGeo sched_geo(const Geometry& g) {
     sg.n_tiles[s] = g.n_tiles[s];
     sg.splits[s] = g.splits[s];
   }
+  if (g.stages == 3) sg.kv[1] = g.kv;
   return sg;
 }
 
@@ -467,7 +488,7 @@ void shape_plan(cs_chain_s* p, const Geometry& g, int kind, int M) {
     p->n_tiles[i] = g.n_tiles[i];
     p->k_iters[i] = g.k_iters[i];
     p->units[i] = g.m_blocks * g.n_tiles[i];
-    p->sched_units[i] = g.m_tiles * g.n_tiles[i] * g.splits[i];
+    p->sched_units[i] = i < g.stages ? static_cast<int>(cs::sched_stage_count(sched_geo(g), i)) : 0;
     p->splits[i] = g.splits[i];
     p->kps[i] = g.kps[i];
     p->bn[i] = g.bn[i];
@@ -479,6 +500,8 @@ void shape_plan(cs_chain_s* p, const Geometry& g, int kind, int M) {
   p->sk_units = g.sk_units;
   p->sk_q = g.sk_q;
   p->sk_max_nc = g.sk_max_nc;
+  p->kv = g.kv;
+  p->kv_max = g.kv_max;
   const bool wide_b = kind == CS_CHAIN_MLP_SWIGLU || g.bn[0] == 256 || g.bn[1] == 256 || g.bn[2] == 256;
   p->cfg_s = (g.cg == 1 && kind != CS_CHAIN_ATTN && M <= 8) ? (wide_b ? 2 : 1) : 0;
   p->cfg_b = g.cg == 1 && !p->cfg_s && wide_b;
@@ -514,6 +537,7 @@ void info_geometry(const cs_chain_s* p, int n_fused, cs_chain_info* info) {
   info->sk_units = p->sk_units;
   info->sk_q = p->sk_q;
   info->workers = p->workers > 0 ? p->workers : p->num_sms / p->cl;
+  info->kv_chunk = p->kv;
 }
 
 int device_sms(int* out) {
@@ -901,6 +925,8 @@ void fill_attn_stages(const cs_chain_s* p, cs::KParams& kp) {
   fill_split(p, 0, s0);
   fill_split(p, 1, s1);
   fill_split(p, 2, s2);
+  s1.kv_chunk = p->kv;
+  s1.kv_max = p->kv_max;
   // pairs: 256-column buffers, which attention units borrow for S and O
   kp.acc_stride = p->cg == 2 ? 256 : 128;
 }
@@ -1060,9 +1086,16 @@ cs_status cs_chain_plan(const cs_chain_desc* desc, cs_chain_t* out) {
         return bail(fail(CS_ERR_OOM, "cudaMalloc of the Stream-K workspace failed"));
       if (cudaMemset(p->split_ctr[st], 0, words * 4) != cudaSuccess) return bail(fail(CS_ERR_CUDA, "cudaMemset failed"));
     }
-    if (g.splits[st] <= 1) continue;
-    const int acc_n = (desc->kind == CS_CHAIN_MLP_SWIGLU && st == 0) ? 256 : g.bn[st];
-    const size_t pf = static_cast<size_t>(g.splits[st]) * g.m_blocks * g.n_tiles[st] * cs::BM * acc_n;
+    size_t pf = 0;
+    if (attn && st == 1 && g.kv > 0) {
+      // attention pieces: [query block][head][piece][ATT_PART_COLS][128 rows]
+      pf = static_cast<size_t>(g.m_blocks) * g.n_tiles[st] * g.kv_max * cs::ATT_PART_COLS * cs::BM;
+    } else if (g.splits[st] > 1) {
+      const int acc_n = (desc->kind == CS_CHAIN_MLP_SWIGLU && st == 0) ? 256 : g.bn[st];
+      pf = static_cast<size_t>(g.splits[st]) * g.m_blocks * g.n_tiles[st] * cs::BM * acc_n;
+    }
+    if (pf == 0) continue;
+    p->partial_bytes[st] = pf * 4;
     const size_t words = static_cast<size_t>(g.m_blocks) * g.n_tiles[st];
     if (cudaMalloc(reinterpret_cast<void**>(&p->partial[st]), pf * 4) != cudaSuccess ||
         cudaMalloc(reinterpret_cast<void**>(&p->split_ctr[st]), words * 4) != cudaSuccess)
@@ -1369,11 +1402,7 @@ cs_status cs_chain_debug_poison_intermediate(cs_chain_t p, int which, void* stre
   }
   if (which == -1 || which == 2)
     for (int stg = 0; stg < p->stages; ++stg)
-      if (p->partial[stg]) {
-        const int acc_n = (p->d.kind == CS_CHAIN_MLP_SWIGLU && stg == 0) ? 256 : p->bn[stg];
-        const size_t bytes = static_cast<size_t>(p->splits[stg]) * p->m_blocks * p->n_tiles[stg] * cs::BM * acc_n * 4;
-        CS_CUDA(cudaMemsetAsync(p->partial[stg], 0xFF, bytes, st));
-      }
+      if (p->partial[stg]) CS_CUDA(cudaMemsetAsync(p->partial[stg], 0xFF, p->partial_bytes[stg], st));
   return CS_OK;
 }
 
@@ -1391,6 +1420,12 @@ cs_status cs_chain_debug_set_epoch(cs_chain_t p, uint32_t epoch) {
     if (p->split_ctr[stg]) {
       std::vector<uint32_t> v(static_cast<size_t>(p->m_blocks) * p->n_tiles[stg],
                               epoch * static_cast<uint32_t>(p->splits[stg]));
+      if (p->d.kind == CS_CHAIN_ATTN && stg == 1 && p->kv > 0) {
+        // one arrival per piece of the query block's tile row
+        for (int qb = 0; qb < p->m_blocks; ++qb)
+          for (int h = 0; h < p->n_tiles[stg]; ++h)
+            v[static_cast<size_t>(qb) * p->n_tiles[stg] + h] = epoch * static_cast<uint32_t>((qb / p->cg + p->kv) / p->kv);
+      }
       if (stg == p->stages - 1 && p->sk_units > 0) {
         // a Stream-K tile counts one arrival per contributing unit (per 128-row block)
         std::vector<uint32_t> table(static_cast<size_t>(p->sk_tiles));

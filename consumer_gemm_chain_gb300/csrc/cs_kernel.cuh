@@ -128,6 +128,11 @@ struct StageP {
   long long pf_lda;
   int pf_arows;
   // attention (STAGE_ATTN)
+  // kv_chunk > 0: the units of tile row m run as ceil((m + 1) / kv_chunk)
+  // pieces of at most kv_chunk key groups (CTAs-per-unit key blocks each); a
+  // piece writes its fp32 state [query block][head][piece][ATT_PART_COLS][128]
+  // to `partial` and counts its arrival on split_ctr[query block * heads + head]
+  int kv_chunk, kv_max;
   int heads;
   float softmax_scale_log2;  // log2(e) / sqrt(head_dim)
 };
@@ -926,11 +931,35 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
 //   S = Q_i K_j^T            tcgen05, fp32 in TMEM columns [ATT_S_COL, +128)
 //   P = exp2(S*c - m)         epilogue warps (one query row per thread), fp16/bf16
 //                             into the staging buffers as a K-major SW128 operand
-//   O_j = P V_j               tcgen05 (V is an MN-major B operand), TMEM [ATT_O_COL, +128)
-//   acc = acc*alpha + O_j     in registers, alpha = exp2(m_old - m_new)
-// then O = acc / l is stored like a GEMM tile and the (i, h) semaphore released.
+//   O += P V_j                tcgen05 (V is an MN-major B operand), accumulated in
+//                             TMEM [ATT_O_COL, +128) across the unit's key blocks
+// P is taken against a reference maximum m that is raised only when a row's
+// maximum exceeds it by more than 2^ATT_RESCALE_LOG2 (so P <= 2^8); then O and
+// l are rescaled by exp2(m_old - m_new) in TMEM first.  O / l is stored like a
+// GEMM tile and the (i, h) semaphore released.
 constexpr uint32_t ATT_S_COL = 256;
 constexpr uint32_t ATT_O_COL = 384;
+// fp32 columns of a piece's state per query row: 128 output dims, max, sum, 2 unused
+constexpr int ATT_PART_COLS = 132;
+// log2 of the largest P the reference maximum allows before O is rescaled
+constexpr float ATT_RESCALE_LOG2 = 8.0f;
+
+// Key blocks [j0, j1) of an attention unit; returns the pieces of its tile
+// row.  Tile row i sees key groups 0..i (CG key blocks each); with kv_chunk
+// = c, piece k (the unit's K-split field) takes groups [k c, min((k + 1) c, i + 1)).
+template <int CG>
+__device__ __forceinline__ int attn_keys(const StageP& S, uint32_t unit, int& j0, int& j1) {
+  const int i = unit_m(unit);
+  if (S.kv_chunk <= 0) {
+    j0 = 0;
+    j1 = (i + 1) * CG;
+    return 1;
+  }
+  const int c = unit_ks(unit);
+  j0 = c * S.kv_chunk * CG;
+  j1 = min((c + 1) * S.kv_chunk, i + 1) * CG;
+  return (i + S.kv_chunk) / S.kv_chunk;
+}
 
 // TMA: three 32 KB slots per key block: [Q dims 0-63 | K_j dims 0-63],
 // [Q dims 64-127 | K_j dims 64-127], [V_j dims 0-63 | V_j dims 64-127] (128 rows each).
@@ -946,12 +975,15 @@ __device__ bool tma_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
   const int i = unit_m(unit), h = unit_n(unit);
   const int F = S.heads * 128;
   const int qb = i * CG + static_cast<int>(rank);  // this CTA's query block
-  const int nkb = (i + 1) * CG;                    // key blocks of the unit
+  int j0, j1;
+  attn_keys<CG>(S, unit, j0, j1);
+  const int nkb = j1 - j0;                         // key blocks of the unit
   const int nslots = 3 * nkb;
   const int claim_at = nslots > CLAIM_AHEAD ? nslots - CLAIM_AHEAD : 0;
   int ready = 0;
-  // every key block of the unit (and so every query block) must be complete first
-  if (p.waits && S.wait != WAIT_NONE && !tma_wait_ready(sc, q, nkb, ready, p)) return false;
+  // every row block up to the unit's query blocks (and so every key block it
+  // reads) must be complete first
+  if (p.waits && S.wait != WAIT_NONE && !tma_wait_ready(sc, q, (i + 1) * CG, ready, p)) return false;
   const CUtensorMap* m = &p.maps[S.map_a];
   int sidx = 0;
   // CG = 2: the MMA computes S for key block j+1 before P V of block j (two S
@@ -978,15 +1010,16 @@ __device__ bool tma_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
       if (sidx == 0) trace_put(p, tidx, rank, CG, 4, globaltimer());
       if (sidx == nslots - 1) trace_put(p, tidx, rank, CG, 5, globaltimer());
       uint8_t* s0 = ring + rp.slot * STAGE_BYTES;
+      const int jb = j0 + j;  // key block
       if constexpr (CG == 1) {
         uint64_t* bar = &sc->full[rp.slot];
         mbar_arrive_expect_tx(bar, 2 * TILE_A_BYTES);
         if (part < 2) {
-          tma_load_2d(s0, m, h * 128 + part * 64, qb * BM, bar);                   // Q_i dims chunk
-          tma_load_2d(s0 + TILE_A_BYTES, m, F + h * 128 + part * 64, j * BM, bar);  // K_j dims chunk
+          tma_load_2d(s0, m, h * 128 + part * 64, qb * BM, bar);                    // Q_i dims chunk
+          tma_load_2d(s0 + TILE_A_BYTES, m, F + h * 128 + part * 64, jb * BM, bar);  // K_j dims chunk
         } else {
-          tma_load_2d(s0, m, 2 * F + h * 128, j * BM, bar);                       // V_j dims 0-63
-          tma_load_2d(s0 + TILE_A_BYTES, m, 2 * F + h * 128 + 64, j * BM, bar);    // V_j dims 64-127
+          tma_load_2d(s0, m, 2 * F + h * 128, jb * BM, bar);                        // V_j dims 0-63
+          tma_load_2d(s0 + TILE_A_BYTES, m, 2 * F + h * 128 + 64, jb * BM, bar);     // V_j dims 64-127
         }
       } else {
         const uint32_t bar_addr = mapa_shared(&sc->full[rp.slot], 0);
@@ -998,11 +1031,11 @@ __device__ bool tma_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
         if (part < 2) {
           // Q rows of this CTA's query block; keys rank*64 .. +63 of block j
           tma_load_2d_pair(s0, m, h * 128 + part * 64, qb * BM, bar_addr);
-          tma_load_2d_pair(s0 + TILE_A_BYTES, &p.maps[S.map_k], F + h * 128 + part * 64, j * BM + rank * 64,
+          tma_load_2d_pair(s0 + TILE_A_BYTES, &p.maps[S.map_k], F + h * 128 + part * 64, jb * BM + rank * 64,
                            bar_addr);
         } else {
           // head dimensions rank*64 .. +63 of V_j, all 128 keys
-          tma_load_2d_pair(s0, m, 2 * F + h * 128 + rank * 64, j * BM, bar_addr);
+          tma_load_2d_pair(s0, m, 2 * F + h * 128 + rank * 64, jb * BM, bar_addr);
         }
       }
       sc->issued_parity[rp.slot] = static_cast<int>(rp.phase);
@@ -1020,8 +1053,9 @@ __device__ bool tma_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
 template <int NS, int STAGE_BYTES, int CG>
 __device__ bool mma_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, uint8_t* pbuf, RingPos& rp,
                               uint32_t unit, uint32_t& p_phase, uint32_t& acc, uint32_t& acc_phase) {
-  const int i = unit_m(unit);
-  const int nkb = (i + 1) * CG;
+  int j0, j1;
+  attn_keys<CG>(p.st[unit_stage(unit)], unit, j0, j1);
+  const int nkb = j1 - j0;  // key blocks of the unit (even for CG = 2)
   const uint32_t idesc_s = make_idesc_f16(p.bf16, 0, BM * CG, 128);  // Q K^T: both operands K-major
   const uint32_t idesc_o = make_idesc_f16(p.bf16, 1, BM * CG, 128);  // P V: V is MN-major
   const uint32_t pb = smem_u32(pbuf);
@@ -1043,7 +1077,7 @@ __device__ bool mma_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
     tc_commit<CG>(s_bar);
     return true;
   };
-  auto mma_pv = [&](uint32_t o_tm) -> bool {
+  auto mma_pv = [&](uint32_t o_tm, bool accumulate) -> bool {
     // P_j is in shared memory (of both CTAs) and the previous O_j has been read
     // back; a pair's peer publishes its P with cluster-scope release arrivals
     if (!wait_bar<NS, CG == 2>(&sc->p_full, p_phase, sc, p, 12)) return false;
@@ -1057,7 +1091,7 @@ __device__ bool mma_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
     for (int kk = 0; kk < 8; ++kk) {
       // P: chunk of 64 keys per 16 KB, +32 bytes per 16 keys; V: +16 key rows (2 KB)
       const uint64_t a = smem_desc_sw128(pb + (kk >> 2) * (BM * 128), 16, 1024) + static_cast<uint64_t>((kk & 3) * 2);
-      tc_mma_f16<CG>(o_tm, a, vd + static_cast<uint64_t>(kk * 128), idesc_o, kk != 0 ? 1u : 0u);
+      tc_mma_f16<CG>(o_tm, a, vd + static_cast<uint64_t>(kk * 128), idesc_o, (accumulate || kk != 0) ? 1u : 0u);
     }
     tc_commit<CG>(&sc->empty[rp.slot]);
     rp.next<NS>();
@@ -1067,7 +1101,7 @@ __device__ bool mma_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
   if constexpr (CG == 1) {
     const uint32_t s_tm = sc->tmem_base + ATT_S_COL, o_tm = sc->tmem_base + ATT_O_COL;
     for (int j = 0; j < nkb; ++j)
-      if (!mma_s(s_tm, &sc->s_full) || !mma_pv(o_tm)) return false;
+      if (!mma_s(s_tm, &sc->s_full) || !mma_pv(o_tm, j > 0)) return false;
   } else {
     uint32_t buf[2];
     for (int b = 0; b < 2; ++b) {
@@ -1082,7 +1116,7 @@ __device__ bool mma_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
     if (!mma_s(s_base, &sc->s_full)) return false;
     if (nkb > 1 && !mma_s(s_base + 128, &sc->s_full_b)) return false;
     for (int j = 0; j < nkb; ++j) {
-      if (!mma_pv(o_tm)) return false;
+      if (!mma_pv(o_tm, j > 0)) return false;
       // S_j's half is free once P_j is published
       if (j + 2 < nkb && !mma_s(s_base + static_cast<uint32_t>(j & 1) * 128, (j & 1) ? &sc->s_full_b : &sc->s_full))
         return false;
@@ -1097,14 +1131,18 @@ __device__ bool mma_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
 // Epilogue warps: online softmax for one query row per thread.  CG = 2: this
 // CTA's query block is the unit's block rank; its rows see every key block of
 // the unit (the first query block's last one is entirely in its future).
+// A piece of a split row ends with its state (m, l and the output scaled by
+// 2^-m) in the workspace; the last piece of this query block and head to
+// arrive merges all of them in piece order and stores O.
 template <int NS, int CG>
 __device__ bool epi_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* staging, uint32_t unit, uint32_t& s_phase,
                               uint32_t& o_phase, int& last_buf, uint32_t tidx, uint32_t& tacc, uint32_t& tacc_phase,
-                              uint32_t rank) {
+                              uint32_t rank, uint32_t epoch1) {
   const StageP& S = p.st[unit_stage(unit)];
   const int i = unit_m(unit), h = unit_n(unit);
   const int qb = i * CG + static_cast<int>(rank);  // this CTA's query block
-  const int nkb = (i + 1) * CG;
+  int j0, j1;
+  const int np = attn_keys<CG>(S, unit, j0, j1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;
   const int r = q * 32 + lane;  // query row within the block
@@ -1115,67 +1153,79 @@ __device__ bool epi_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
   const uint32_t s_base = sc->tmem_base + lane_base + (CG == 1 ? ATT_S_COL : tacc * stride);
   const uint32_t o_tm = CG == 1 ? sc->tmem_base + lane_base + ATT_O_COL : sc->tmem_base + lane_base + (tacc ^ 1u) * stride;
   const float sl2 = S.softmax_scale_log2;
-  float acc[128];
-#pragma unroll
-  for (int t = 0; t < 128; ++t) acc[t] = 0.0f;
-  float m_run = -INFINITY, l_run = 0.0f, alpha_prev = 0.0f;
+  float m_ref = -INFINITY, l_run = 0.0f;
   // the staging buffers double as the P operand: earlier stores must be done reading them
   if (lane == 0) tma_store_wait_read<0>();
   __syncwarp();
   last_buf = -1;
-  for (int j = 0; j < nkb; ++j) {
-    // s_phase: bit 0 tracks s_full, bit 1 s_full_b (odd key blocks of pair units)
+  for (int j = j0; j < j1; ++j) {
+    // s_phase: bit 0 tracks s_full, bit 1 s_full_b (odd key blocks of pair
+    // units; j0 is even there)
     const uint32_t sb = CG == 2 ? static_cast<uint32_t>(j & 1) : 0u;
     if (!wait_bar(sb ? &sc->s_full_b : &sc->s_full, (s_phase >> sb) & 1u, sc, p, 13)) return false;
     s_phase ^= 1u << sb;
     tc_fence_after();
-    if (j == 0 && threadIdx.x == EPI_WARP0 * 32) trace_put(p, tidx, rank, CG, 6, globaltimer());
+    if (j == j0 && threadIdx.x == EPI_WARP0 * 32) trace_put(p, tidx, rank, CG, 6, globaltimer());
     const uint32_t s_tm = CG == 1 ? s_base : s_base + static_cast<uint32_t>(j & 1) * 128;
-    // key column c of block j is visible to row r iff j*128 + c <= qb*128 + r
+    // this row of S_j, read once
+    uint32_t v[4][32];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tmem_ld32(s_tm + c * 32, v[c]);
+    tc_wait_ld();
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tc_wait_ld_regs(v[c]);
+    // scaled logits, -inf where masked: key column c of block j is visible to
+    // row r iff j*128 + c <= qb*128 + r
     const bool diag = j >= qb;
     const int lim = (qb - j) * 128 + r;
-    // pass 1: row maximum of the scaled, masked logits
-    float mx = -INFINITY;
+    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint32_t v[32];
-      tmem_ld32(s_tm + c * 32, v);
-      tc_wait_ld();
+    for (int c = 0; c < 4; ++c)
 #pragma unroll
       for (int t = 0; t < 32; ++t) {
-        const float s = (diag && c * 32 + t > lim) ? -INFINITY : __uint_as_float(v[t]) * sl2;
-        mx = fmaxf(mx, s);
+        const float x = (diag && c * 32 + t > lim) ? -INFINITY : __uint_as_float(v[c][t]) * sl2;
+        v[c][t] = __float_as_uint(x);
+        mx[t & 3] = fmaxf(mx[t & 3], x);
       }
-    }
-    const float m_new = fmaxf(m_run, mx);
-    const float alpha = ex2_approx(m_run - m_new);
-    if (j > 0) {
-      // fold O_{j-1} (computed against m_{j-1}) into the accumulator
+    const float m_blk = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+    // every row sees a key of the unit's first block (j0 <= qb), so m_ref is
+    // finite from then on
+    const bool raise = m_blk > m_ref + ATT_RESCALE_LOG2;
+    const float m_new = raise ? m_blk : m_ref;
+    if (j > j0) {
+      // P V of block j-1 has read P_{j-1} and added into O
       if (!wait_bar(&sc->o_full, o_phase, sc, p, 14)) return false;
       o_phase ^= 1u;
       tc_fence_after();
+      if (__any_sync(0xFFFFFFFFu, raise)) {
+        // O and l against the raised maximum (tcgen05.ld/st are warp-wide)
+        const float f = raise ? ex2_approx(m_ref - m_new) : 1.0f;
+        l_run *= f;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tmem_ld32(o_tm + c * 32, o);
+          tc_wait_ld();
+          tc_wait_ld_regs(o);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(o_tm + c * 32, v);
-        tc_wait_ld();
-#pragma unroll
-        for (int t = 0; t < 32; ++t) acc[c * 32 + t] = fmaf(acc[c * 32 + t], alpha_prev, __uint_as_float(v[t]));
+          for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * f);
+          tmem_st32(o_tm + c * 32, o);
+        }
+        tc_wait_st();
       }
     }
-    // pass 2: P = exp2(s - m_new), row sum, write P_j as the A operand of P V
-    float lsum = 0.0f;
+    m_ref = m_new;
+    // P = exp2(s - m_ref) (0 where masked), its row sum, P_j written as the A operand of P V
+    float ls[2] = {0.0f, 0.0f};
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      uint32_t v[32];
-      tmem_ld32(s_tm + c * 32, v);
-      tc_wait_ld();
       uint32_t w[16];
 #pragma unroll
       for (int t = 0; t < 32; t += 2) {
-        const float p0 = (diag && c * 32 + t > lim) ? 0.0f : ex2_approx(fmaf(__uint_as_float(v[t]), sl2, -m_new));
-        const float p1 = (diag && c * 32 + t + 1 > lim) ? 0.0f : ex2_approx(fmaf(__uint_as_float(v[t + 1]), sl2, -m_new));
-        lsum += p0 + p1;
+        const float p0 = ex2_approx(__uint_as_float(v[c][t]) - m_ref);
+        const float p1 = ex2_approx(__uint_as_float(v[c][t + 1]) - m_ref);
+        ls[0] += p0;
+        ls[1] += p1;
         w[t >> 1] = pack2(p0, p1, p.bf16);
       }
       // keys c*32 .. c*32+31 live in 64-key chunk c/2, 16-byte pieces (c%2)*4 .. +3 of row r
@@ -1189,9 +1239,7 @@ __device__ bool epi_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
                      : "memory");
       }
     }
-    l_run = fmaf(l_run, alpha, lsum);
-    m_run = m_new;
-    alpha_prev = alpha;
+    l_run += ls[0] + ls[1];
     fence_proxy_async_shared();
     tc_fence_before();
     __syncwarp();
@@ -1202,18 +1250,89 @@ __device__ bool epi_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
         mbar_arrive_cluster(mapa_shared(&sc->p_full, 0));  // the pair leader issues P V
     }
   }
+  // the last P V, then O (against m_ref) into registers
   if (!wait_bar(&sc->o_full, o_phase, sc, p, 14)) return false;
   o_phase ^= 1u;
   tc_fence_after();
+  float acc[128];
+  {
+    uint32_t o[4][32];
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    uint32_t v[32];
-    tmem_ld32(o_tm + c * 32, v);
+    for (int c = 0; c < 4; ++c) tmem_ld32(o_tm + c * 32, o[c]);
     tc_wait_ld();
 #pragma unroll
-    for (int t = 0; t < 32; ++t) acc[c * 32 + t] = fmaf(acc[c * 32 + t], alpha_prev, __uint_as_float(v[t]));
+    for (int c = 0; c < 4; ++c) {
+      tc_wait_ld_regs(o[c]);
+#pragma unroll
+      for (int t = 0; t < 32; ++t) acc[c * 32 + t] = __uint_as_float(o[c][t]);
+    }
   }
+  const float m_run = m_ref;
   tc_fence_before();
+  if constexpr (CG == 2) {
+    // every TMEM read of the unit is done: both accumulator buffers go back to
+    // the MMA (both CTAs' warps), in order
+    for (int b = 0; b < 2; ++b) {
+      if (!wait_bar(&sc->tfull[tacc], tacc_phase, sc, p, 4)) return false;
+      tc_fence_after();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(&sc->tempty[tacc], 0));
+      tacc ^= 1u;
+      if (tacc == 0u) tacc_phase ^= 1u;
+    }
+  }
+  if (np > 1) {
+    // [piece][ATT_PART_COLS / 4][128 rows] float4: a warp moves 512 contiguous bytes per access
+    const size_t piece_floats = static_cast<size_t>(ATT_PART_COLS) * BM;
+    float* ws = S.partial + (static_cast<size_t>(qb) * S.n_tiles + h) * S.kv_max * piece_floats;
+    float4* mine = reinterpret_cast<float4*>(ws + unit_ks(unit) * piece_floats) + r;
+#pragma unroll
+    for (int t = 0; t < 32; ++t)
+      mine[t * BM] = make_float4(acc[4 * t], acc[4 * t + 1], acc[4 * t + 2], acc[4 * t + 3]);
+    mine[32 * BM] = make_float4(m_run, l_run, 0.0f, 0.0f);
+    // as for K-splits: the CTA barrier orders every thread's stores before the
+    // one acq_rel arrival; the last piece reads the others' after the next one
+    named_bar_sync(1, EPI_THREADS);
+    if (threadIdx.x == EPI_WARP0 * 32) {
+      const uint32_t old = atom_add_acq_rel_gpu(S.split_ctr + static_cast<size_t>(qb) * S.n_tiles + h, 1u);
+      sc->split_last = (old + 1u == epoch1 * static_cast<uint32_t>(np)) ? 1 : 0;
+    }
+    named_bar_sync(1, EPI_THREADS);
+    if (!sc->split_last) {
+      if (threadIdx.x == EPI_WARP0 * 32) trace_put(p, tidx, rank, CG, 7, globaltimer());
+      return true;
+    }
+    // O = sum_k 2^(m_k - M) acc_k / sum_k 2^(m_k - M) l_k, M = max_k m_k,
+    // summed in piece order
+    float mx = -INFINITY;
+    for (int k = 0; k < np; ++k)
+      mx = fmaxf(mx, __ldcg(reinterpret_cast<const float4*>(ws + k * piece_floats) + 32 * BM + r).x);
+#pragma unroll
+    for (int t = 0; t < 128; ++t) acc[t] = 0.0f;
+    float l_sum = 0.0f;
+    for (int k = 0; k < np; ++k) {
+      const float4* src = reinterpret_cast<const float4*>(ws + k * piece_floats) + r;
+      const float4 ml = __ldcg(src + 32 * BM);
+      const float w = ex2_approx(ml.x - mx);
+      l_sum = fmaf(ml.y, w, l_sum);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float4 x[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) x[t] = __ldcg(src + (c * 8 + t) * BM);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          float* a = &acc[(c * 8 + t) * 4];
+          a[0] = fmaf(x[t].x, w, a[0]);
+          a[1] = fmaf(x[t].y, w, a[1]);
+          a[2] = fmaf(x[t].z, w, a[2]);
+          a[3] = fmaf(x[t].w, w, a[3]);
+        }
+      }
+    }
+    l_run = l_sum;
+  }
   const float inv = 1.0f / l_run;
   // O tile rows of this warp -> staging (the last P V has completed) -> TMA store
 #pragma unroll
@@ -1231,18 +1350,6 @@ __device__ bool epi_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
         tma_store_commit();
       }
       last_buf = c;
-    }
-  }
-  if constexpr (CG == 2) {
-    // both accumulator buffers go back to the MMA (both CTAs' warps), in order
-    for (int b = 0; b < 2; ++b) {
-      if (!wait_bar(&sc->tfull[tacc], tacc_phase, sc, p, 4)) return false;
-      tc_fence_after();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(mapa_shared(&sc->tempty[tacc], 0));
-      tacc ^= 1u;
-      if (tacc == 0u) tacc_phase ^= 1u;
     }
   }
   if (S.rel_tile != nullptr) {
@@ -1666,7 +1773,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
       if (p.st[unit_stage(unit)].kind == STAGE_GEMM)
         ok = epi_gemm_unit<NS, CG, CL>(p, sc, staging, unit, part, acc, acc_phase, last_buf, rank, tidx, epoch1);
       else if constexpr (ATTN)
-        ok = epi_attn_unit<NS, CG>(p, sc, staging, unit, s_phase, o_phase, last_buf, tidx, acc, acc_phase, rank);
+        ok = epi_attn_unit<NS, CG>(p, sc, staging, unit, s_phase, o_phase, last_buf, tidx, acc, acc_phase, rank,
+                                   epoch1);
     }
     if (lane == 0) tma_store_wait_all<0>();
     __syncwarp();

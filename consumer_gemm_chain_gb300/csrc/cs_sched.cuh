@@ -7,6 +7,11 @@
 // inside the group, or row-major), so every producer unit a consumer waits on
 // is listed at an earlier step or earlier in the same step, and an in-order
 // dispatcher cannot deadlock.  A stage alone lists its groups in turn.
+//
+// A causal stage split into key-range pieces (kv[s] > 0: the attention units
+// of tile row m cover key groups 0..m, in pieces of kv[s] groups) lists
+// n_tiles[s] * ceil((m + 1) / kv[s]) units in row m, row by row, each row's
+// units by column tile and then piece.
 #pragma once
 #include <cstdint>
 
@@ -20,6 +25,7 @@ struct SchedGeo {
   int row_major = 0;  // units of a group row by row instead of column by column
   int n_tiles[3] = {0, 0, 0};
   int splits[3] = {1, 1, 1};
+  int kv[3] = {0, 0, 0};  // key groups per piece of a causal stage (0: none)
 };
 
 __host__ __device__ inline uint32_t sched_enc(int s, int m, int n, int ks) {
@@ -46,10 +52,23 @@ __host__ __device__ inline long long sched_units_per_row(const SchedGeo& g, int 
   return static_cast<long long>(g.n_tiles[s]) * g.splits[s];
 }
 
+// Units of stage s per column tile in tile row m: its K-splits, or its pieces.
+__host__ __device__ inline int sched_pieces(const SchedGeo& g, int s, int m) {
+  return g.kv[s] > 0 ? (m + g.kv[s]) / g.kv[s] : g.splits[s];
+}
+
+// Units of stage s in tile rows [0, r): with pieces, sum over k = 1..r of
+// ceil(k / kv) = kv * a * (a + 1) / 2 + b * (a + 1) for r = a * kv + b.
+__host__ __device__ inline long long sched_units_rows(const SchedGeo& g, int s, long long r) {
+  if (g.kv[s] <= 0) return sched_units_per_row(g, s) * r;
+  const long long a = r / g.kv[s], b = r % g.kv[s];
+  return static_cast<long long>(g.n_tiles[s]) * (g.kv[s] * a * (a + 1) / 2 + b * (a + 1));
+}
+
 // Entries of the fused order before step t.
 __host__ __device__ inline long long sched_fused_before(const SchedGeo& g, int t) {
   long long o = 0;
-  for (int s = 0; s < g.stages; ++s) o += sched_units_per_row(g, s) * sched_rows_before(g, t - s * g.lag);
+  for (int s = 0; s < g.stages; ++s) o += sched_units_rows(g, s, sched_rows_before(g, t - s * g.lag));
   return o;
 }
 
@@ -60,14 +79,26 @@ __host__ __device__ inline long long sched_fused_count(const SchedGeo& g) {
 }
 
 __host__ __device__ inline long long sched_stage_count(const SchedGeo& g, int s) {
-  return sched_units_per_row(g, s) * g.m_tiles;
+  return sched_units_rows(g, s, g.m_tiles);
 }
 
 // Entry j of stage s's units in the group of tile rows [m0, m0 + rows).
 __host__ __device__ inline uint32_t sched_in_group(const SchedGeo& g, int s, int m0, int rows, long long j) {
   const int sp = g.splits[s];
   int m, n, ks;
-  if (g.row_major) {
+  if (g.kv[s] > 0) {
+    // row by row; in a row, column tile then piece
+    m = m0;
+    long long c = static_cast<long long>(g.n_tiles[s]) * sched_pieces(g, s, m);
+    while (j >= c && m + 1 < m0 + rows) {
+      j -= c;
+      ++m;
+      c = static_cast<long long>(g.n_tiles[s]) * sched_pieces(g, s, m);
+    }
+    const int np = sched_pieces(g, s, m);
+    n = static_cast<int>(j / np);
+    ks = static_cast<int>(j % np);
+  } else if (g.row_major) {
     const long long per_row = sched_units_per_row(g, s);
     m = m0 + static_cast<int>(j / per_row);
     const long long r = j % per_row;
@@ -99,7 +130,7 @@ __host__ __device__ inline uint32_t sched_fused_entry(const SchedGeo& g, long lo
   for (int s = 0; s < g.stages; ++s) {
     const int k = t - s * g.lag;
     const long long rows = sched_rows_of(g, k);
-    const long long c = rows * sched_units_per_row(g, s);
+    const long long c = sched_units_rows(g, s, sched_rows_before(g, k + 1)) - sched_units_rows(g, s, sched_rows_before(g, k));
     if (j < c) return sched_in_group(g, s, static_cast<int>(sched_rows_before(g, k)), static_cast<int>(rows), j);
     j -= c;
   }
@@ -108,10 +139,24 @@ __host__ __device__ inline uint32_t sched_fused_entry(const SchedGeo& g, long lo
 
 // Entry i (0 <= i < sched_stage_count) of stage s run alone.
 __host__ __device__ inline uint32_t sched_stage_entry(const SchedGeo& g, int s, long long i) {
-  const long long per_group = static_cast<long long>(g.group_m) * sched_units_per_row(g, s);
-  int k = static_cast<int>(i / per_group);
-  if (k >= sched_groups(g)) k = sched_groups(g) - 1;
-  const long long base = sched_rows_before(g, k) * sched_units_per_row(g, s);
+  int k;
+  if (g.kv[s] > 0) {
+    // the group holding entry i: the last k with sched_units_rows(rows before k) <= i
+    int lo = 0, hi = sched_groups(g) - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) / 2;
+      if (sched_units_rows(g, s, sched_rows_before(g, mid)) <= i)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    k = lo;
+  } else {
+    const long long per_group = static_cast<long long>(g.group_m) * sched_units_per_row(g, s);
+    k = static_cast<int>(i / per_group);
+    if (k >= sched_groups(g)) k = sched_groups(g) - 1;
+  }
+  const long long base = sched_units_rows(g, s, sched_rows_before(g, k));
   return sched_in_group(g, s, static_cast<int>(sched_rows_before(g, k)), static_cast<int>(sched_rows_of(g, k)),
                         i - base);
 }

@@ -42,7 +42,7 @@
 extern "C" {
 #endif
 
-#define CS_ABI_VERSION 5
+#define CS_ABI_VERSION 6
 
 typedef struct cs_chain_s* cs_chain_t;
 
@@ -186,6 +186,19 @@ typedef struct cs_chain_desc {
   int sk_units;        /* Stream-K units for those tiles; 0 = one per worker (SM,
                           pair or cluster of the grid).  Each takes at least 8
                           K-slices (fewer units then).                              */
+  int kv_chunk;        /* ATTN: key-range pieces of the causal attention units.  A
+                          unit of tile row m (tile_m query rows of one head) sees
+                          key groups 0..m (tile_m keys each), so the last rows'
+                          units are the longest.  With kv_chunk = c the row runs
+                          as ceil((m + 1) / c) pieces of at most c key groups, on
+                          as many SMs (or pairs) at once; each piece writes its
+                          fp32 softmax state (row maximum, row sum, unnormalised
+                          output) to a plan-owned workspace, and the last piece of
+                          a query block and head to finish merges every piece in
+                          piece order (the same bits whichever finishes last),
+                          stores O and releases it.  0 = auto (four pieces for the
+                          longest row from four tile rows), -1 = whole rows.  At
+                          most 15 pieces per row (c is raised to fit).           */
 } cs_chain_desc;
 
 /* Fill *desc with defaults (kind MLP_GELU, F16, TILE, KN, auto everything else). */
@@ -309,6 +322,7 @@ typedef struct cs_chain_info {
                               GPC whose SM count is not a multiple of the cluster
                               size leaves SMs out); cs_chain_plan_info, which needs
                               no GPU, reports num_sms / (tile_m / 128)          */
+  int kv_chunk;            /* ATTN: key groups per attention piece (0: whole rows) */
 } cs_chain_info;
 
 cs_status cs_chain_query(cs_chain_t plan, cs_chain_info* info);

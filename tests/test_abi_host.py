@@ -33,7 +33,7 @@ def test_every_declared_symbol_is_exported(cs):
     for n in names:
         assert hasattr(lib, n), f"{n} declared in cs_chain.h but not exported"
     assert set(cs.chain.EXPORTED) == set(names)
-    assert cs.cs_abi_version() == 5
+    assert cs.cs_abi_version() == 6
 
 
 def test_desc_defaults(cs):
@@ -101,26 +101,32 @@ def test_schedule_is_dependency_ordered(cs, M, H, F, sms, lag, group, split, til
 
 @pytest.mark.parametrize("tile_m", [128, 256])
 @pytest.mark.parametrize("M,lag,group", [(1, -1, 0), (300, -1, 0), (2048, -1, 0), (2048, 2, 3), (1000, 0, 1)])
-def test_attention_schedule_is_dependency_ordered(cs, M, lag, group, tile_m):
+@pytest.mark.parametrize("kv", [-1, 0, 2])
+def test_attention_schedule_is_dependency_ordered(cs, M, lag, group, tile_m, kv):
     d = cs.cs_chain_desc_init(kind="attn", M=M, H=12288, F=1536, heads=12, head_dim=128, lag=lag, group_m=group,
-                              tile_m=tile_m)
+                              tile_m=tile_m, kv_chunk=kv)
     dec = [cs.decode_unit(u) for u in cs.cs_schedule_build(d, 148)]
+    kv_arg, kv = kv, cs.cs_chain_plan_info(d, 148)["kv_chunk"]
     m_tiles = -(-M // tile_m)
     tn = tile_m  # 128 x 128 single-SM tiles or 256 x 256 pair tiles
     nt = [4608 // tn, 12, 12288 // tn]
     splits = {}
     for s, m, n, k in dec:
         splits[(s, m, n)] = max(splits.get((s, m, n), 0), k + 1)
+    assert len(dec) == len(set(dec))
     assert set(splits) == {(s, m, n) for s in range(3) for m in range(m_tiles) for n in range(nt[s])}
-    assert all(v == 1 for (s, _, _), v in splits.items() if s == 1)  # attention units do not split
+    # attention units: one per row and head, or ceil((m + 1) / kv) key-range pieces
+    assert all(v == (-(-(m + 1) // kv) if kv else 1) for (s, m, _), v in splits.items() if s == 1)
+    if kv_arg == 0:
+        assert (kv > 0) == (m_tiles >= 4)  # auto: pieces from four tile rows
 
     def deps(u):
         s, m, n, _ = u
         if s == 1:   # causal: key blocks up to the unit's last query block (Q, K and V tiles of head n)
             tiles = {(p * 12 + n) * 128 // tn for p in range(3)}
             return [(0, j, t, k) for j in range(m + 1) for t in tiles for k in range(splits[(0, j, t)])]
-        if s == 2:   # every head of the same row block
-            return [(1, m, h, 0) for h in range(12)]
+        if s == 2:   # every piece of every head of the same row block
+            return [(1, m, h, k) for h in range(12) for k in range(splits[(1, m, h)])]
         return []
     _check_order(dec, deps)
 
@@ -204,9 +210,11 @@ def test_the_abi_from_plain_c99(cs, tmp_path):
     assert p.returncode == 0 and p.stdout.strip() == "ok", p.stderr
 
 
-def _loop_order(stages, m_tiles, group_m, lag, n_tiles, splits, row_major):
+def _loop_order(stages, m_tiles, group_m, lag, n_tiles, splits, row_major, kv=0):
     """The fused dispatch order written as nested loops (steps, stages, a
-    group's tiles), independently of the library's closed form."""
+    group's tiles), independently of the library's closed form.  kv > 0: the
+    attention stage's units of tile row m are ceil((m + 1) / kv) key-range
+    pieces per head, listed row by row, head, then piece."""
     groups = -(-m_tiles // group_m)
     out = []
     for t in range(groups + (stages - 1) * lag):
@@ -215,31 +223,47 @@ def _loop_order(stages, m_tiles, group_m, lag, n_tiles, splits, row_major):
             if not 0 <= g < groups:
                 continue
             rows = range(g * group_m, min(m_tiles, (g + 1) * group_m))
-            if row_major:
+            if kv > 0 and stages == 3 and s == 1:
+                out += [(s, m, n, k) for m in rows for n in range(n_tiles[s]) for k in range(-(-(m + 1) // kv))]
+            elif row_major:
                 out += [(s, m, n, k) for m in rows for n in range(n_tiles[s]) for k in range(splits[s])]
             else:
                 out += [(s, m, n, k) for n in range(n_tiles[s]) for m in rows for k in range(splits[s])]
     return out
 
 
-@pytest.mark.parametrize("kind,M,H,F,lag,group,split,tile_m,raster", [
+_ORDER_CASES = [
     ("gelu", 2048, 12288, 6144, -1, 0, 0, 0, 0), ("gelu", 1, 12288, 6144, -1, 0, 0, 0, 0),
     ("gelu", 1000, 8192, 2752, 2, 1, 2, 128, 1), ("gelu", 1536, 8192, 8192, 5, 5, 1, 256, 2),
     ("swiglu", 777, 8192, 2752, 0, 3, 3, 128, 2), ("gelu", 130000, 256, 512, 3, 7, 1, 128, 1),
-    ("attn", 2048, 12288, 1536, -1, 0, 0, 256, 0), ("attn", 300, 12288, 1536, 2, 1, 0, 128, 2)])
-def test_closed_form_schedule_equals_the_loop_order(cs, kind, M, H, F, lag, group, split, tile_m, raster):
+    ("attn", 2048, 12288, 1536, -1, 0, 0, 256, 0), ("attn", 300, 12288, 1536, 2, 1, 0, 128, 2),
+    ("attn", 2048, 12288, 1536, -1, 3, 0, 128, 0), ("attn", 1900, 1024, 512, 1, 2, 0, 256, 2),
+    ("attn", 640, 1024, 256, 0, 1, 0, 128, 0)]
+
+
+# attention cases also with key-range pieces: auto, every group alone, three groups
+@pytest.mark.parametrize("kind,M,H,F,lag,group,split,tile_m,raster,kv",
+                         [c + (kv,) for c in _ORDER_CASES for kv in ((-1, 0, 1, 3) if c[0] == "attn" else (-1,))])
+def test_closed_form_schedule_equals_the_loop_order(cs, kind, M, H, F, lag, group, split, tile_m, raster, kv):
     """The schedule entries are computed one by one from a closed form (so the
     allocation-free forward can write them on the device, one thread each):
     they must equal the nested-loop order entry for entry."""
-    extra = dict(heads=F // 128, head_dim=128) if kind == "attn" else {}
+    extra = dict(heads=F // 128, head_dim=128, kv_chunk=kv) if kind == "attn" else {}
     d = cs.cs_chain_desc_init(kind=kind, M=M, H=H, F=F, lag=lag, group_m=group, split_k=split, tile_m=tile_m,
                               raster=raster, weight_layout="nk", tuned=-1, **extra)
     q = cs.cs_chain_plan_info(d, 152)
     m_tiles = -(-M // q["tile_m"])
-    want = _loop_order(q["stages"], m_tiles, q["group_m"], q["lag"], q["n_tiles"], q["split_k"], raster == 2)
+    if kind == "attn":
+        want_kv = kv if kv > 0 else (-(-m_tiles // 4) if kv == 0 and m_tiles >= 4 else 0)
+        want_kv = max(want_kv, -(-m_tiles // 15)) if want_kv else 0
+        assert q["kv_chunk"] == (want_kv if want_kv < m_tiles else 0)
+    want = _loop_order(q["stages"], m_tiles, q["group_m"], q["lag"], q["n_tiles"], q["split_k"], raster == 2,
+                       q.get("kv_chunk", 0))
     got = [cs.decode_unit(u) for u in cs.cs_schedule_build(d, 152)]
     assert got == [(s, m, n, k) for s, m, n, k in want]
     assert q["n_units"] == len(got)
+    for s in range(q["stages"]):
+        assert q["sched_units"][s] == sum(1 for e in got if e[0] == s)
 
 
 def _sk_pieces(u, q, K, tiles):
@@ -303,3 +327,20 @@ def test_stream_k_needs_an_unsplit_last_stage(cs):
         with pytest.raises(cs.CSError) as e:
             cs.cs_chain_plan_info(bad, 152)
         assert e.value.status == cs.CS_ERR_INVALID_ARG
+
+
+def test_attention_piece_bounds(cs):
+    """kv_chunk is refused outside -1..4095, raised so that no row has more than
+    15 pieces (the unit's K-split field), and pieces never cover a whole row."""
+    for v in (-2, 4096):
+        d = cs.cs_chain_desc_init(kind="attn", M=2048, H=12288, F=1536, heads=12, head_dim=128, kv_chunk=v)
+        with pytest.raises(cs.CSError) as e:
+            cs.cs_chain_plan_info(d, 152)
+        assert e.value.status == cs.CS_ERR_INVALID_ARG
+    d = cs.cs_chain_desc_init(kind="attn", M=128 * 40, H=1024, F=256, heads=2, head_dim=128, tile_m=128, kv_chunk=1)
+    q = cs.cs_chain_plan_info(d, 152)
+    assert q["kv_chunk"] == 3  # ceil(40 / 15)
+    assert max(cs.decode_unit(u)[3] for u in cs.cs_schedule_build(d, 152) if cs.decode_unit(u)[0] == 1) == 13
+    for M, kv in ((512, 2), (512, 5), (128, 1)):  # two 256-row tile rows, one 128-row row: nothing to split
+        d = cs.cs_chain_desc_init(kind="attn", M=M, H=1024, F=256, heads=2, head_dim=128, kv_chunk=kv)
+        assert cs.cs_chain_plan_info(d, 152)["kv_chunk"] == 0

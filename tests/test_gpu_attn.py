@@ -63,18 +63,21 @@ def test_attention_policies_bit_identical_and_flags(tile_m):
         assert torch.equal(v, outs["row"]), k
 
 
+@pytest.mark.parametrize("kv", [-1, 1])
 @pytest.mark.parametrize("tile_m", [128, 256])
-def test_attention_delay_injection_never_changes_a_bit(tile_m):
+def test_attention_delay_injection_never_changes_a_bit(tile_m, kv):
     """Random delays before the QKV tiles' and the attention units' releases,
-    QKV and O poisoned with NaN before every forward: an attention unit that
-    read a QKV row block, or a Wo tile that read an O block, before it was
-    released would turn Y NaN."""
-    inp = cs_inputs.make_custom("attn", 400, 512, 384, seed=33)
+    QKV, O and the pieces' workspace poisoned with NaN before every forward: an
+    attention unit that read a QKV row block, a Wo tile that read an O block,
+    or a merging piece that read another piece's state, before it was released
+    would turn Y NaN.  kv 1: every key group its own piece."""
+    inp = cs_inputs.make_custom("attn", 400 if tile_m == 128 else 800, 512, 384, seed=33)
     dev = device_tensors(inp, "nk")
     ref = None
     for pol in ("row", "tile", "strided"):
-        with plan_for(inp, pol, "nk", group_m=1, tile_m=tile_m) as plan:
+        with plan_for(inp, pol, "nk", group_m=1, tile_m=tile_m, kv_chunk=kv) as plan:
             q = cs.cs_chain_query(plan)
+            assert q["kv_chunk"] == (1 if kv == 1 else 0)
             for seed in range(2):
                 g = torch.Generator().manual_seed(200 + seed)
                 for stage in (0, 1):
@@ -110,21 +113,25 @@ def test_attention_poison_reaches_stages_run_without_producers(tile_m):
         assert torch.equal(forward(plan, dev).cpu(), good)
 
 
+@pytest.mark.parametrize("kv", [-1, 1])
 @pytest.mark.parametrize("tile_m", [128, 256])
 @pytest.mark.parametrize("policy", ["row", "tile", "stream"])
-def test_attention_epoch_counters_wrap(policy, tile_m):
-    """Both boundaries' counters (and the output's) across the 2^32 wrap."""
-    inp = cs_inputs.make_custom("attn", 300, 512, 256, seed=36)
+def test_attention_epoch_counters_wrap(policy, tile_m, kv):
+    """Both boundaries' counters (and the output's) across the 2^32 wrap; kv 1:
+    also the pieces' arrival counters (a piece that miscounted would never
+    merge, and the forward would time out)."""
+    inp = cs_inputs.make_custom("attn", 300 if tile_m == 128 else 600, 512, 256, seed=36)
     dev = device_tensors(inp, "nk")
-    with plan_for(inp, policy, "nk", tile_m=tile_m, out_release=1) as fresh:
+    with plan_for(inp, policy, "nk", tile_m=tile_m, out_release=1, kv_chunk=kv) as fresh:
         ref = forward(fresh, dev).cpu()
-    with plan_for(inp, policy, "nk", tile_m=tile_m, out_release=1) as plan:
+    with plan_for(inp, policy, "nk", tile_m=tile_m, out_release=1, kv_chunk=kv) as plan:
         q = cs.cs_chain_query(plan)
         start = 0xFFFFFFFF
         cs.cs_chain_debug_set_epoch(plan, start)
         for i in range(1, 4):
             cs.cs_chain_debug_poison_intermediate(plan, -1)
             assert torch.equal(forward(plan, dev).cpu(), ref), i
+            assert cs.cs_chain_status(plan) == cs.CS_OK
             e = (start + i) & 0xFFFFFFFF
             for b in (0, 1, 2):
                 tiles, rows, epoch = cs.cs_chain_debug_read_sems(plan, b)
@@ -192,3 +199,38 @@ def test_attention_stream_k_tail_on_the_output_projection(tile_m):
     assert oracle.rel_err(outs["row"], Yref) <= TOL
     for k, v in outs.items():
         assert torch.equal(v, outs["row"]), k
+
+
+@pytest.mark.parametrize("tile_m", [128, 256])
+@pytest.mark.parametrize("M,heads,kv", [(700, 2, 1), (700, 2, 2), (1000, 1, 3), (1280, 3, 4), (2048, 2, 0)])
+def test_attention_key_range_pieces(M, heads, kv, tile_m):
+    """The causal units split into key-range pieces of kv key groups (tile_m
+    keys each), merged by the last piece in piece order: O and Y against the
+    oracle, against whole-row units (the merge reorders the fp32 sums, so to a
+    few fp16 ulps, not bit for bit), and the same bits on a second forward and
+    under another policy."""
+    inp = cs_inputs.make_custom("attn", M, 384, heads * 128, seed=38)
+    dev = device_tensors(inp, "nk")
+    outs = {}
+    for pol, k in (("row", kv), ("tile", kv), ("row", -1)):
+        with plan_for(inp, pol, "nk", tile_m=tile_m, kv_chunk=k) as plan:
+            q = cs.cs_chain_query(plan)
+            m_tiles = -(-M // tile_m)
+            if k == -1:
+                assert q["kv_chunk"] == 0
+            else:
+                assert 0 < q["kv_chunk"] < m_tiles
+                assert q["sched_units"][1] == heads * sum(-(-(m + 1) // q["kv_chunk"]) for m in range(m_tiles))
+            cs.cs_chain_debug_poison_intermediate(plan, -1)
+            Y = forward(plan, dev).cpu()
+            O = intermediate(plan, 1, M, inp.F, inp.dtype).cpu()
+            cs.cs_chain_debug_poison_intermediate(plan, -1)
+            assert torch.equal(forward(plan, dev).cpu(), Y)
+            outs[(pol, k)] = (Y, O)
+    Yref, _, Oref = _oracle(inp)
+    Y, O = outs[("row", kv)]
+    assert oracle.rel_err(O, Oref) <= TOL
+    assert oracle.rel_err(Y, Yref) <= TOL
+    assert torch.equal(outs[("tile", kv)][0], Y)
+    assert oracle.rel_err(O, outs[("row", -1)][1]) <= 1e-3
+    assert oracle.rel_err(Y, outs[("row", -1)][0]) <= 1e-3
