@@ -313,11 +313,14 @@ Geometry geometry(const cs_chain_desc* d, int num_sms, int workers = 0) {
     g.bn[2] = tn;
     g.n_tiles[2] = cdiv(d->H, tn);
     g.k_iters[2] = cdiv(d->F, cs::BK);
-    // Causal units grow with their row: the last rows' units set the chain's
-    // critical path once the QKV GEMM ends.  Pieces of kv key groups run them
-    // on several SMs at once; auto: at most four pieces per row from four tile
-    // rows.  At most 15 pieces per row (the unit's K-split field).
-    int kv = d->kv_chunk > 0 ? d->kv_chunk : (d->kv_chunk == 0 && g.m_tiles >= 4 ? cdiv(g.m_tiles, 4) : 0);
+    // Causal units grow with their row: the last rows' units lie on the
+    // chain's critical path once the QKV GEMM ends.  Pieces of kv key groups
+    // run them on several SMs at once, at the price of a state write and a
+    // merge per piece; auto: whole rows (measured with the tensor-memory
+    // accumulator, GPT-3 shard: M=1024 142 us whole against 143-147 in
+    // pieces, M=2048 256 against 258-286, M=4096 543 against 553-596).  At
+    // most 15 pieces per row (the unit's K-split field).
+    int kv = d->kv_chunk > 0 ? d->kv_chunk : 0;
     if (kv > 0) {
       kv = std::max(kv, cdiv(g.m_tiles, 15));
       if (kv < g.m_tiles) {

@@ -196,9 +196,10 @@ typedef struct cs_chain_desc {
                           output) to a plan-owned workspace, and the last piece of
                           a query block and head to finish merges every piece in
                           piece order (the same bits whichever finishes last),
-                          stores O and releases it.  0 = auto (four pieces for the
-                          longest row from four tile rows), -1 = whole rows.  At
-                          most 15 pieces per row (c is raised to fit).           */
+                          stores O and releases it.  0 = auto (whole rows: the
+                          merge costs more than the shorter critical path saves
+                          on GB300), -1 = whole rows.  At most 15 pieces per row
+                          (c is raised to fit).                                   */
 } cs_chain_desc;
 
 /* Fill *desc with defaults (kind MLP_GELU, F16, TILE, KN, auto everything else). */

@@ -117,8 +117,8 @@ def test_attention_schedule_is_dependency_ordered(cs, M, lag, group, tile_m, kv)
     assert set(splits) == {(s, m, n) for s in range(3) for m in range(m_tiles) for n in range(nt[s])}
     # attention units: one per row and head, or ceil((m + 1) / kv) key-range pieces
     assert all(v == (-(-(m + 1) // kv) if kv else 1) for (s, m, _), v in splits.items() if s == 1)
-    if kv_arg == 0:
-        assert (kv > 0) == (m_tiles >= 4)  # auto: pieces from four tile rows
+    if kv_arg <= 0:
+        assert kv == 0  # auto and -1: whole rows
 
     def deps(u):
         s, m, n, _ = u
@@ -254,8 +254,7 @@ def test_closed_form_schedule_equals_the_loop_order(cs, kind, M, H, F, lag, grou
     q = cs.cs_chain_plan_info(d, 152)
     m_tiles = -(-M // q["tile_m"])
     if kind == "attn":
-        want_kv = kv if kv > 0 else (-(-m_tiles // 4) if kv == 0 and m_tiles >= 4 else 0)
-        want_kv = max(want_kv, -(-m_tiles // 15)) if want_kv else 0
+        want_kv = max(kv, -(-m_tiles // 15)) if kv > 0 else 0  # auto: whole rows
         assert q["kv_chunk"] == (want_kv if want_kv < m_tiles else 0)
     want = _loop_order(q["stages"], m_tiles, q["group_m"], q["lag"], q["n_tiles"], q["split_k"], raster == 2,
                        q.get("kv_chunk", 0))

@@ -202,7 +202,7 @@ def test_attention_stream_k_tail_on_the_output_projection(tile_m):
 
 
 @pytest.mark.parametrize("tile_m", [128, 256])
-@pytest.mark.parametrize("M,heads,kv", [(700, 2, 1), (700, 2, 2), (1000, 1, 3), (1280, 3, 4), (2048, 2, 0)])
+@pytest.mark.parametrize("M,heads,kv", [(700, 2, 1), (700, 2, 2), (1000, 1, 3), (1280, 3, 4), (2048, 2, 2)])
 def test_attention_key_range_pieces(M, heads, kv, tile_m):
     """The causal units split into key-range pieces of kv key groups (tile_m
     keys each), merged by the last piece in piece order: O and Y against the
