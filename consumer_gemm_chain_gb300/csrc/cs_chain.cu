@@ -770,6 +770,12 @@ cs_status kernel_for(const cs_chain_s* p, const void** fn) {
 #undef CS_KERNEL
 }
 
+// Threads per CTA: the attention instantiations run two epilogue warps per TMEM
+// lane quadrant.
+unsigned block_threads(const cs_chain_s* p) {
+  return static_cast<unsigned>(p->d.kind == CS_CHAIN_ATTN ? cs::Roles<true>::THREADS : cs::Roles<false>::THREADS);
+}
+
 // Clusters of the plan's shape that can be resident at once: a GPC whose SM
 // count is not a multiple of the cluster size leaves SMs idle (on a 152-SM
 // GB300, 36 clusters of 4 CTAs, 144 SMs).
@@ -781,7 +787,7 @@ cs_status resident_workers(const cs_chain_s* p, int* workers) {
   if (s != CS_OK) return s;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(p->num_sms);
-  cfg.blockDim = dim3(cs::NUM_THREADS);
+  cfg.blockDim = dim3(block_threads(p));
   cfg.dynamicSmemBytes = p->smem;
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeClusterDimension;
@@ -809,7 +815,7 @@ cs_status launch(cs_chain_s* p, cs::KParams& kp, const uint32_t* sched, int n_un
   grid *= p->cl;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(cs::NUM_THREADS);
+  cfg.blockDim = dim3(block_threads(p));
   cfg.dynamicSmemBytes = p->smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];

@@ -45,10 +45,17 @@ constexpr int UMMA_K = 16;        // K per tcgen05.mma (kind::f16)
 constexpr int TILE_A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int STAGING_BYTES = 2 * BM * 128;  // two 64-column chunk buffers of 128 rows
 constexpr int UQ = 4;             // unit-queue depth (scheduler -> TMA/MMA/epilogue)
-constexpr int NUM_THREADS = 224;
+// Warp roles: 0 TMA, 1 MMA, EPI_WARP0 .. EPI_WARP0 + EPI - 1 epilogue, then the
+// scheduler.  Epilogue warp w reads TMEM lane quadrant w % 4; the attention
+// instantiations run two epilogue warps per quadrant, each on half of a tile's
+// columns (the softmax of a 128-key block is then split over two warps).
 constexpr int EPI_WARP0 = 2;
-constexpr int EPI_THREADS = 128;
-constexpr int SCHED_WARP = 6;
+template <bool ATTN>
+struct Roles {
+  static constexpr int EPI = ATTN ? 8 : 4;
+  static constexpr int SCHED = EPI_WARP0 + EPI;
+  static constexpr int THREADS = (SCHED + 1) * 32;
+};
 constexpr int CLAIM_AHEAD = 12;   // K-slices before a unit's end at which the next unit is claimed
 constexpr uint32_t READY_ALL = 0x7FFFFFFFu;
 constexpr uint32_t TMEM_COLS = 512;
@@ -196,6 +203,7 @@ struct SmemCtl {
   volatile int tma_kb;      // TMA warp: K-slice of its latest load
   int issued_parity[NS];  // TMA thread: parity of the last load issued into each slot (-1: none)
   uint4 bias_s[32];       // epilogue: the bias of one tile (up to 256 values)
+  float xchg[2][BM];      // attention epilogue: the two warps of a row exchange row maxima and sums
 };
 
 __device__ __forceinline__ void record_error(const KParams& p, uint32_t code, uint32_t unit, uint32_t where) {
@@ -583,12 +591,13 @@ __device__ __forceinline__ void stage_row(uint8_t* staging, int chunk, int row, 
 
 // Producer release: all epilogue threads have their stores complete; one thread
 // publishes the 128-row block's tile (and its row) with gpu-scope release.
+template <int NE>
 __device__ void release_tile(const KParams& p, const StageP& S, int mb, int n, int lane) {
   if (lane == 0) {
     tma_store_wait_all<0>();
     fence_proxy_async_global();
   }
-  named_bar_sync(1, EPI_THREADS);
+  named_bar_sync(1, NE * 32);
   if (threadIdx.x == EPI_WARP0 * 32) {
     const int u = mb * S.n_tiles + n;
     if (S.delay_ns != nullptr) {
@@ -607,7 +616,7 @@ __device__ void release_tile(const KParams& p, const StageP& S, int mb, int n, i
   }
 }
 
-// K-split reduction for a row block with few valid rows (R <= 48): the 128
+// K-split reduction for a row block with few valid rows (R <= 48): the NE * 32
 // epilogue threads share the (row, 4-column group) elements of `npc` 64-column
 // parts (the value chunks c0 .. c0+nc-1, then for SwiGLU the same up chunks)
 // and fetch every split of an element at once; each element is summed in split
@@ -615,17 +624,17 @@ __device__ void release_tile(const KParams& p, const StageP& S, int mb, int n, i
 // written to the staging buffer as fp32 [part][row][16 float4], the float4 of
 // column group g of row r at slot g ^ (r & 15).  EB elements x KSB splits = 16
 // loads in flight per thread.  Split ks's tile starts at tile0 + ks * kstride.
-template <int EB, int KSB>
+template <int EB, int KSB, int NE>
 __device__ __forceinline__ void split_reduce_small(const StageP& S, const float4* tile0, size_t kstride, int R,
                                                    int npc, int nc, int c0, float4* sm) {
   const int E = npc * R * 16;
   const int tid = threadIdx.x - EPI_WARP0 * 32;
 #pragma unroll 1
-  for (int base = tid; base < E; base += EPI_THREADS * EB) {
+  for (int base = tid; base < E; base += NE * 32 * EB) {
     float4 x[EB][KSB];
 #pragma unroll
     for (int u = 0; u < EB; ++u) {
-      const int e = base + u * EPI_THREADS;
+      const int e = base + u * NE * 32;
       // element e -> part pc, column group g, row r (rows fastest: coalesced)
       const int pc = e / (R * 16), rem = e - pc * R * 16;
       const int g = rem / R, r = rem - g * R;
@@ -637,7 +646,7 @@ __device__ __forceinline__ void split_reduce_small(const StageP& S, const float4
     }
 #pragma unroll
     for (int u = 0; u < EB; ++u) {
-      const int e = base + u * EPI_THREADS;
+      const int e = base + u * NE * 32;
       if (e < E) {
         float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -657,8 +666,9 @@ __device__ __forceinline__ void split_reduce_small(const StageP& S, const float4
 // each row thread finishes its rows' chunks and writes them with plain 16-byte
 // stores, so no staging output, TMA store or per-chunk round trip stays on the
 // hand-off to the consumers (measured at GPT-3 M=1: 13 us from accumulator to
-// release with the per-chunk path).  The caller fences and releases.
-template <int NS>
+// release with the per-chunk path).  With two warps per lane quadrant each
+// takes every other chunk of its rows.  The caller fences and releases.
+template <int NS, int NE, bool ACT>
 __device__ void epi_split_rows_small(const KParams& p, const StageP& S, SmemCtl<NS>* sc, uint8_t* staging,
                                      const float4* tile0, size_t kstride, int R, int mb, int n, int row, int lane) {
   const int nchunks = S.bn / 64;
@@ -668,9 +678,11 @@ __device__ void epi_split_rows_small(const KParams& p, const StageP& S, SmemCtl<
   const int cpp = cap < nchunks ? cap : nchunks;
   // every store still reading the staging buffer is done before it is reused
   if (lane == 0) tma_store_wait_read<0>();
-  named_bar_sync(1, EPI_THREADS);
+  named_bar_sync(1, NE * 32);
   const int tid = threadIdx.x - EPI_WARP0 * 32;
-  if (S.epi == EPI_BIAS_GELU && tid < S.bn / 8) {
+  constexpr int NH = NE / 4;
+  const int half = tid >> 7;  // which of the quadrant's warps
+  if (ACT && S.epi == EPI_BIAS_GELU && tid < S.bn / 8) {
     const int col = n * S.bn + tid * 8;  // 16-byte groups, zero past the extent (a multiple of 8)
     uint4 v = make_uint4(0, 0, 0, 0);
     if (col < S.n_extent)
@@ -683,25 +695,25 @@ __device__ void epi_split_rows_small(const KParams& p, const StageP& S, SmemCtl<
   for (int c0 = 0; c0 < nchunks; c0 += cpp) {
     const int nc = nchunks - c0 < cpp ? nchunks - c0 : cpp;
     // the row threads are done with the previous pass's sums
-    if (c0 > 0) named_bar_sync(1, EPI_THREADS);
+    if (c0 > 0) named_bar_sync(1, NE * 32);
     if (S.splits <= 2)
-      split_reduce_small<8, 2>(S, tile0, kstride, R, np * nc, nc, c0, sm);
+      split_reduce_small<8, 2, NE>(S, tile0, kstride, R, np * nc, nc, c0, sm);
     else if (S.splits <= 4)
-      split_reduce_small<4, 4>(S, tile0, kstride, R, np * nc, nc, c0, sm);
+      split_reduce_small<4, 4, NE>(S, tile0, kstride, R, np * nc, nc, c0, sm);
     else if (S.splits <= 8)
-      split_reduce_small<2, 8>(S, tile0, kstride, R, np * nc, nc, c0, sm);
+      split_reduce_small<2, 8, NE>(S, tile0, kstride, R, np * nc, nc, c0, sm);
     else
-      split_reduce_small<1, 16>(S, tile0, kstride, R, np * nc, nc, c0, sm);
-    named_bar_sync(1, EPI_THREADS);
+      split_reduce_small<1, 16, NE>(S, tile0, kstride, R, np * nc, nc, c0, sm);
+    named_bar_sync(1, NE * 32);
     if (row >= R) continue;
 #pragma unroll 1
-    for (int cc = 0; cc < nc; ++cc) {
+    for (int cc = half; cc < nc; cc += NH) {
       float va[64], vu[64];
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const float4 a = sm[(cc * R + row) * 16 + (j ^ (row & 15))];
         va[4 * j] = a.x, va[4 * j + 1] = a.y, va[4 * j + 2] = a.z, va[4 * j + 3] = a.w;
-        if (S.epi == EPI_SWIGLU) {
+        if (ACT && S.epi == EPI_SWIGLU) {
           const float4 b = sm[((nc + cc) * R + row) * 16 + (j ^ (row & 15))];
           vu[4 * j] = b.x, vu[4 * j + 1] = b.y, vu[4 * j + 2] = b.z, vu[4 * j + 3] = b.w;
         } else {
@@ -710,7 +722,7 @@ __device__ void epi_split_rows_small(const KParams& p, const StageP& S, SmemCtl<
       }
       const int c = c0 + cc;
       uint32_t w[32];
-      if (S.epi == EPI_BIAS_GELU) {
+      if (ACT && S.epi == EPI_BIAS_GELU) {
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
           const uint4 bv = sc->bias_s[c * 8 + g];
@@ -726,7 +738,7 @@ __device__ void epi_split_rows_small(const KParams& p, const StageP& S, SmemCtl<
             w[j >> 1] = pack2(gelu_tanh_f(va[j] + f.x), gelu_tanh_f(va[j + 1] + f.y), p.bf16);
           }
         }
-      } else if (S.epi == EPI_SWIGLU) {
+      } else if (ACT && S.epi == EPI_SWIGLU) {
 #pragma unroll
         for (int j = 0; j < 64; j += 2)
           w[j >> 1] = pack2(silu_f(va[j]) * vu[j], silu_f(va[j + 1]) * vu[j + 1], p.bf16);
@@ -742,9 +754,16 @@ __device__ void epi_split_rows_small(const KParams& p, const StageP& S, SmemCtl<
               make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
     }
   }
+  // every thread is done reading the sums in the staging buffer before any
+  // warp's next unit writes it (attention P, output staging)
+  named_bar_sync(1, NE * 32);
 }
 
-template <int NS, int CG, int CL>
+// NE epilogue warps: with 8, the two warps of a TMEM lane quadrant take every
+// other 64-column chunk (and every other 32-column part of a K-split's
+// partial).  ACT: the bias + GeLU and SiLU-up epilogues are compiled in (the
+// attention instantiations' GEMMs have none).
+template <int NS, int CG, int CL, int NE, bool ACT>
 __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* staging, uint32_t unit, uint32_t part,
                               uint32_t& acc, uint32_t& acc_phase, int& last_buf, uint32_t rank, uint32_t tidx,
                               uint32_t epoch1) {
@@ -754,6 +773,8 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;  // TMEM lane quadrant this warp may access
   const int row = q * 32 + lane;
+  constexpr int NH = NE / 4;
+  const int half = (warp - EPI_WARP0) >> 2;  // which of the quadrant's warps
   if (!wait_bar(&sc->tfull[acc], acc_phase, sc, p, 4)) return false;
   tc_fence_after();
   if (threadIdx.x == EPI_WARP0 * 32) trace_put(p, tidx, rank, CL, 6, globaltimer());
@@ -793,7 +814,7 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
     // K-split: write this split's fp32 rows, count the arrival; only the last
     // split of the tile goes on (and reduces every split in split order).
     float4* mine = tile_partial(part_c(part));
-    for (int c = 0; c < S.mma_n / 32; ++c) {
+    for (int c = half; c < S.mma_n / 32; c += NH) {
       uint32_t v[32];
       tmem_ld32(tbase + c * 32, v);
       tc_wait_ld();
@@ -810,12 +831,12 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
     // the CTA barrier orders every thread's partial stores before the one
     // acq_rel arrival (release: this split's partial; acquire, for the last
     // split: every other split's, read after the next barrier)
-    named_bar_sync(1, EPI_THREADS);
+    named_bar_sync(1, NE * 32);
     if (threadIdx.x == EPI_WARP0 * 32) {
       const uint32_t old = atom_add_acq_rel_gpu(S.split_ctr + mb * S.n_tiles + n, 1u);
       sc->split_last = (old + 1u == epoch1 * static_cast<uint32_t>(nc)) ? 1 : 0;
     }
-    named_bar_sync(1, EPI_THREADS);
+    named_bar_sync(1, NE * 32);
     if (!sc->split_last) {
       if (threadIdx.x == EPI_WARP0 * 32) trace_put(p, tidx, rank, CL, 7, globaltimer());
       return true;
@@ -828,11 +849,12 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
   const bool rows_small = split && skj == 0xFFFF && rows_valid <= 48 && S.out_ptr != nullptr;
   if (rows_small) {
     const size_t kstride = static_cast<size_t>(S.m_blocks) * S.n_tiles * (tile_floats / 4);
-    epi_split_rows_small<NS>(p, S, sc, staging, tile_partial(0) - row, kstride, rows_valid, mb, n, row, lane);
+    epi_split_rows_small<NS, NE, ACT>(p, S, sc, staging, tile_partial(0) - row, kstride, rows_valid, mb, n, row,
+                                      lane);
     last_buf = -1;
   }
 #pragma unroll 1
-  for (int c = 0; c < (rows_small ? 0 : nchunks); ++c) {
+  for (int c = half; c < (rows_small ? 0 : nchunks); c += NH) {
     float va[64], vu[64];
     if (split) {
 #pragma unroll
@@ -847,7 +869,7 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
 #pragma unroll
         for (int j = 0; j < 16; ++j)
           va[4 * j] += x[j].x, va[4 * j + 1] += x[j].y, va[4 * j + 2] += x[j].z, va[4 * j + 3] += x[j].w;
-        if (S.epi == EPI_SWIGLU) {
+        if (ACT && S.epi == EPI_SWIGLU) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) x[j] = __ldcg(src + ((S.bn + c * 64) / 4 + j) * BM);
 #pragma unroll
@@ -860,27 +882,27 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
       uint32_t u[2][32];
       tmem_ld32(tbase + c * 64, v[0]);
       tmem_ld32(tbase + c * 64 + 32, v[1]);
-      if (S.epi == EPI_SWIGLU) {
+      if (ACT && S.epi == EPI_SWIGLU) {
         tmem_ld32(tbase + S.bn + c * 64, u[0]);
         tmem_ld32(tbase + S.bn + c * 64 + 32, u[1]);
       }
       tc_wait_ld();
-      if (c == nchunks - 1) release_tmem();
+      if (c + NH >= nchunks) release_tmem();  // this warp's last chunk
 #pragma unroll
       for (int j = 0; j < 64; ++j) {
         va[j] = __uint_as_float(v[j >> 5][j & 31]);
-        vu[j] = S.epi == EPI_SWIGLU ? __uint_as_float(u[j >> 5][j & 31]) : 0.0f;
+        vu[j] = (ACT && S.epi == EPI_SWIGLU) ? __uint_as_float(u[j >> 5][j & 31]) : 0.0f;
       }
     }
     uint32_t w[32];
     const int col0 = n * S.bn + c * 64;
-    if (S.epi == EPI_BIAS_GELU) {
+    if (ACT && S.epi == EPI_BIAS_GELU) {
       float bias[64];
       load_bias64(S, col0, p.bf16, bias);
 #pragma unroll
       for (int j = 0; j < 64; j += 2)
         w[j >> 1] = pack2(gelu_tanh_f(va[j] + bias[j]), gelu_tanh_f(va[j + 1] + bias[j + 1]), p.bf16);
-    } else if (S.epi == EPI_SWIGLU) {
+    } else if (ACT && S.epi == EPI_SWIGLU) {
 #pragma unroll
       for (int j = 0; j < 64; j += 2)
         w[j >> 1] = pack2(silu_f(va[j]) * vu[j], silu_f(va[j + 1]) * vu[j + 1], p.bf16);
@@ -888,7 +910,8 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
 #pragma unroll
       for (int j = 0; j < 64; j += 2) w[j >> 1] = pack2(va[j], va[j + 1], p.bf16);
     }
-    // Two chunk buffers alternate.  Every earlier store that read this buffer
+    // Two chunk buffers alternate (with two warps per quadrant each warp keeps
+    // one: its chunks all have the same parity).  Every earlier store that read this buffer
     // must be done: if the newest committed store read the other buffer, all
     // but that one group suffice; if it read this buffer, wait for all.
     const int buf = c & 1;
@@ -917,7 +940,7 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
     if (acc == 0u) acc_phase ^= 1u;
   }
   if (S.rel_tile != nullptr) {
-    release_tile(p, S, mb, n, lane);
+    release_tile<NE>(p, S, mb, n, lane);
     last_buf = -1;
   }
   if (threadIdx.x == EPI_WARP0 * 32) trace_put(p, tidx, rank, CL, 7, globaltimer());
@@ -1131,10 +1154,13 @@ __device__ bool mma_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
 // Epilogue warps: online softmax for one query row per thread.  CG = 2: this
 // CTA's query block is the unit's block rank; its rows see every key block of
 // the unit (the first query block's last one is entirely in its future).
+// NE = 8: the two warps of a TMEM lane quadrant share each row, one taking keys
+// 0-63 and output dimensions 0-63, the other the rest; they exchange their row
+// maxima (and at the end their row sums) through shared memory.
 // A piece of a split row ends with its state (m, l and the output scaled by
 // 2^-m) in the workspace; the last piece of this query block and head to
 // arrive merges all of them in piece order and stores O.
-template <int NS, int CG>
+template <int NS, int CG, int NE>
 __device__ bool epi_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* staging, uint32_t unit, uint32_t& s_phase,
                               uint32_t& o_phase, int& last_buf, uint32_t tidx, uint32_t& tacc, uint32_t& tacc_phase,
                               uint32_t rank, uint32_t epoch1) {
@@ -1146,6 +1172,19 @@ __device__ bool epi_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;
   const int r = q * 32 + lane;  // query row within the block
+  constexpr int NH = NE / 4;    // warps per row
+  constexpr int CPW = 4 / NH;   // 32-column chunks of S (keys) and of O (dimensions) per warp
+  const int half = (warp - EPI_WARP0) >> 2;
+  const int cb = half * CPW;    // this warp's first chunk
+  // NE = 8: the other warp of the row's value of x; both have read before
+  // either writes the exchange slots again
+  auto other = [&](float x) -> float {
+    sc->xchg[half][r] = x;
+    named_bar_sync(2 + q, 64);
+    const float y = sc->xchg[half ^ 1][r];
+    named_bar_sync(2 + q, 64);
+    return y;
+  };
   const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
   // CG = 1: S and O at fixed columns.  CG = 2: S_j in half (j & 1) of the
   // unit's first accumulator buffer, O in its second (the MMA's layout)
@@ -1153,7 +1192,7 @@ __device__ bool epi_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
   const uint32_t s_base = sc->tmem_base + lane_base + (CG == 1 ? ATT_S_COL : tacc * stride);
   const uint32_t o_tm = CG == 1 ? sc->tmem_base + lane_base + ATT_O_COL : sc->tmem_base + lane_base + (tacc ^ 1u) * stride;
   const float sl2 = S.softmax_scale_log2;
-  float m_ref = -INFINITY, l_run = 0.0f;
+  float m_ref = -INFINITY, l_run = 0.0f;  // l_run: this warp's keys
   // the staging buffers double as the P operand: earlier stores must be done reading them
   if (lane == 0) tma_store_wait_read<0>();
   __syncwarp();
@@ -1167,29 +1206,30 @@ __device__ bool epi_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
     tc_fence_after();
     if (j == j0 && threadIdx.x == EPI_WARP0 * 32) trace_put(p, tidx, rank, CG, 6, globaltimer());
     const uint32_t s_tm = CG == 1 ? s_base : s_base + static_cast<uint32_t>(j & 1) * 128;
-    // this row of S_j, read once
-    uint32_t v[4][32];
+    // this warp's part of the row of S_j, read once
+    uint32_t v[CPW][32];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) tmem_ld32(s_tm + c * 32, v[c]);
+    for (int c = 0; c < CPW; ++c) tmem_ld32(s_tm + (cb + c) * 32, v[c]);
     tc_wait_ld();
 #pragma unroll
-    for (int c = 0; c < 4; ++c) tc_wait_ld_regs(v[c]);
-    // scaled logits, -inf where masked: key column c of block j is visible to
-    // row r iff j*128 + c <= qb*128 + r
+    for (int c = 0; c < CPW; ++c) tc_wait_ld_regs(v[c]);
+    // scaled logits, -inf where masked: key column k of block j is visible to
+    // row r iff j*128 + k <= qb*128 + r
     const bool diag = j >= qb;
     const int lim = (qb - j) * 128 + r;
     float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
+    for (int c = 0; c < CPW; ++c)
 #pragma unroll
       for (int t = 0; t < 32; ++t) {
-        const float x = (diag && c * 32 + t > lim) ? -INFINITY : __uint_as_float(v[c][t]) * sl2;
+        const float x = (diag && (cb + c) * 32 + t > lim) ? -INFINITY : __uint_as_float(v[c][t]) * sl2;
         v[c][t] = __float_as_uint(x);
         mx[t & 3] = fmaxf(mx[t & 3], x);
       }
-    const float m_blk = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+    float m_blk = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+    if constexpr (NH > 1) m_blk = fmaxf(m_blk, other(m_blk));
     // every row sees a key of the unit's first block (j0 <= qb), so m_ref is
-    // finite from then on
+    // finite from then on; both warps of a row take the same decisions
     const bool raise = m_blk > m_ref + ATT_RESCALE_LOG2;
     const float m_new = raise ? m_blk : m_ref;
     if (j > j0) {
@@ -1202,14 +1242,14 @@ __device__ bool epi_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
         const float f = raise ? ex2_approx(m_ref - m_new) : 1.0f;
         l_run *= f;
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < CPW; ++c) {
           uint32_t o[32];
-          tmem_ld32(o_tm + c * 32, o);
+          tmem_ld32(o_tm + (cb + c) * 32, o);
           tc_wait_ld();
           tc_wait_ld_regs(o);
 #pragma unroll
           for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * f);
-          tmem_st32(o_tm + c * 32, o);
+          tmem_st32(o_tm + (cb + c) * 32, o);
         }
         tc_wait_st();
       }
@@ -1218,7 +1258,7 @@ __device__ bool epi_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
     // P = exp2(s - m_ref) (0 where masked), its row sum, P_j written as the A operand of P V
     float ls[2] = {0.0f, 0.0f};
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < CPW; ++c) {
       uint32_t w[16];
 #pragma unroll
       for (int t = 0; t < 32; t += 2) {
@@ -1228,11 +1268,12 @@ __device__ bool epi_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
         ls[1] += p1;
         w[t >> 1] = pack2(p0, p1, p.bf16);
       }
-      // keys c*32 .. c*32+31 live in 64-key chunk c/2, 16-byte pieces (c%2)*4 .. +3 of row r
-      uint8_t* rowp = staging + (c >> 1) * (BM * 128) + r * 128;
+      // keys k*32 .. k*32+31 live in 64-key chunk k/2, 16-byte pieces (k%2)*4 .. +3 of row r
+      const int k = cb + c;
+      uint8_t* rowp = staging + (k >> 1) * (BM * 128) + r * 128;
 #pragma unroll
       for (int pc = 0; pc < 4; ++pc) {
-        const int piece = (c & 1) * 4 + pc;
+        const int piece = (k & 1) * 4 + pc;
         const uint32_t addr = smem_u32(rowp + ((piece ^ (r & 7)) << 4));
         asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[pc * 4 + 0]),
                      "r"(w[pc * 4 + 1]), "r"(w[pc * 4 + 2]), "r"(w[pc * 4 + 3])
@@ -1250,24 +1291,26 @@ __device__ bool epi_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
         mbar_arrive_cluster(mapa_shared(&sc->p_full, 0));  // the pair leader issues P V
     }
   }
-  // the last P V, then O (against m_ref) into registers
+  // the last P V, then this warp's O dimensions (against m_ref) into registers
   if (!wait_bar(&sc->o_full, o_phase, sc, p, 14)) return false;
   o_phase ^= 1u;
   tc_fence_after();
-  float acc[128];
+  constexpr int DW = CPW * 32;  // output dimensions of this warp: [cb*32, cb*32 + DW)
+  float acc[DW];
   {
-    uint32_t o[4][32];
+    uint32_t o[CPW][32];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) tmem_ld32(o_tm + c * 32, o[c]);
+    for (int c = 0; c < CPW; ++c) tmem_ld32(o_tm + (cb + c) * 32, o[c]);
     tc_wait_ld();
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < CPW; ++c) {
       tc_wait_ld_regs(o[c]);
 #pragma unroll
       for (int t = 0; t < 32; ++t) acc[c * 32 + t] = __uint_as_float(o[c][t]);
     }
   }
   const float m_run = m_ref;
+  if constexpr (NH > 1) l_run += other(l_run);  // the row's sum over all 128 keys of every block
   tc_fence_before();
   if constexpr (CG == 2) {
     // every TMEM read of the unit is done: both accumulator buffers go back to
@@ -1288,17 +1331,17 @@ __device__ bool epi_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
     float* ws = S.partial + (static_cast<size_t>(qb) * S.n_tiles + h) * S.kv_max * piece_floats;
     float4* mine = reinterpret_cast<float4*>(ws + unit_ks(unit) * piece_floats) + r;
 #pragma unroll
-    for (int t = 0; t < 32; ++t)
-      mine[t * BM] = make_float4(acc[4 * t], acc[4 * t + 1], acc[4 * t + 2], acc[4 * t + 3]);
-    mine[32 * BM] = make_float4(m_run, l_run, 0.0f, 0.0f);
+    for (int t = 0; t < DW / 4; ++t)
+      mine[(cb * 8 + t) * BM] = make_float4(acc[4 * t], acc[4 * t + 1], acc[4 * t + 2], acc[4 * t + 3]);
+    if (half == 0) mine[32 * BM] = make_float4(m_run, l_run, 0.0f, 0.0f);
     // as for K-splits: the CTA barrier orders every thread's stores before the
     // one acq_rel arrival; the last piece reads the others' after the next one
-    named_bar_sync(1, EPI_THREADS);
+    named_bar_sync(1, NE * 32);
     if (threadIdx.x == EPI_WARP0 * 32) {
       const uint32_t old = atom_add_acq_rel_gpu(S.split_ctr + static_cast<size_t>(qb) * S.n_tiles + h, 1u);
       sc->split_last = (old + 1u == epoch1 * static_cast<uint32_t>(np)) ? 1 : 0;
     }
-    named_bar_sync(1, EPI_THREADS);
+    named_bar_sync(1, NE * 32);
     if (!sc->split_last) {
       if (threadIdx.x == EPI_WARP0 * 32) trace_put(p, tidx, rank, CG, 7, globaltimer());
       return true;
@@ -1309,7 +1352,7 @@ __device__ bool epi_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
     for (int k = 0; k < np; ++k)
       mx = fmaxf(mx, __ldcg(reinterpret_cast<const float4*>(ws + k * piece_floats) + 32 * BM + r).x);
 #pragma unroll
-    for (int t = 0; t < 128; ++t) acc[t] = 0.0f;
+    for (int t = 0; t < DW; ++t) acc[t] = 0.0f;
     float l_sum = 0.0f;
     for (int k = 0; k < np; ++k) {
       const float4* src = reinterpret_cast<const float4*>(ws + k * piece_floats) + r;
@@ -1317,10 +1360,10 @@ __device__ bool epi_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
       const float w = ex2_approx(ml.x - mx);
       l_sum = fmaf(ml.y, w, l_sum);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < DW / 32; ++c) {
         float4 x[8];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) x[t] = __ldcg(src + (c * 8 + t) * BM);
+        for (int t = 0; t < 8; ++t) x[t] = __ldcg(src + (cb * 8 + c * 8 + t) * BM);
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
           float* a = &acc[(c * 8 + t) * 4];
@@ -1334,12 +1377,14 @@ __device__ bool epi_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
     l_run = l_sum;
   }
   const float inv = 1.0f / l_run;
-  // O tile rows of this warp -> staging (the last P V has completed) -> TMA store
+  // this warp's O dimensions of its rows -> staging (the last P V has completed:
+  // P's buffers are free) -> TMA store, 64 dimensions per staging chunk
 #pragma unroll
-  for (int c = 0; c < 2; ++c) {
+  for (int cc = 0; cc < DW / 64; ++cc) {
+    const int c = cb / 2 + cc;
     uint32_t w[32];
 #pragma unroll
-    for (int t = 0; t < 64; t += 2) w[t >> 1] = pack2(acc[c * 64 + t] * inv, acc[c * 64 + t + 1] * inv, p.bf16);
+    for (int t = 0; t < 64; t += 2) w[t >> 1] = pack2(acc[cc * 64 + t] * inv, acc[cc * 64 + t + 1] * inv, p.bf16);
     stage_row(staging, c, r, w);
     fence_proxy_async_shared();
     __syncwarp();
@@ -1353,7 +1398,7 @@ __device__ bool epi_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
     }
   }
   if (S.rel_tile != nullptr) {
-    release_tile(p, S, qb, h, lane);
+    release_tile<NE>(p, S, qb, h, lane);
     last_buf = -1;
   }
   if (threadIdx.x == EPI_WARP0 * 32) trace_put(p, tidx, rank, CG, 7, globaltimer());
@@ -1512,7 +1557,8 @@ __device__ __forceinline__ void push_unit(SmemCtl<NS>* sc, uint32_t q, uint32_t 
 // CG: CTAs per tcgen05 MMA (1, or 2 for a 256-row pair); CL: CTAs per unit
 // and per cluster (CG, or 4: two pairs sharing the weight boxes by multicast).
 template <int NS, int STAGE_BYTES, int CG, bool ATTN, int CL = CG, int AR = BM>
-__global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_constant__ KParams p) {
+__global__ void __launch_bounds__(Roles<ATTN>::THREADS, 1) cs_chain_kernel(const __grid_constant__ KParams p) {
+  constexpr int NE = Roles<ATTN>::EPI;
   static_assert(CL == CG || (CG == 2 && CL == 4 && !ATTN), "unsupported cluster shape");
 #ifdef CS_NO_CLUSTER_MULTICAST
   static_assert(CL != 4, "the replica build has no 4-CTA multicast tiles");
@@ -1540,18 +1586,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sc->tfull[i], 1);
-      mbar_init(&sc->tempty[i], 4 * CG);  // every epilogue warp of the tile
+      mbar_init(&sc->tempty[i], NE * CG);  // every epilogue warp of the tile
     }
     for (int i = 0; i < UQ; ++i) {
       mbar_init(&sc->uq_full[i], 1);
-      mbar_init(&sc->uq_empty[i], 6);  // TMA + MMA + 4 epilogue warps
+      mbar_init(&sc->uq_empty[i], 2 + NE);  // TMA + MMA + the epilogue warps
     }
     mbar_init(&sc->claim_req, 1);
     mbar_init(&sc->mb_full, 1);
     mbar_init(&sc->mb_empty, CL - 1 > 0 ? CL - 1 : 1);  // every peer CTA takes the index
     mbar_init(&sc->s_full, 1);
     mbar_init(&sc->s_full_b, 1);
-    mbar_init(&sc->p_full, 4 * CG);  // every epilogue warp of the unit's CTAs
+    mbar_init(&sc->p_full, NE * CG);  // every epilogue warp of the unit's CTAs
     mbar_init(&sc->o_full, 1);
     mbar_init(&sc->drain, 1);
     sc->abort = 0;
@@ -1578,7 +1624,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
 
   const uint32_t epoch1 = p.ctrl[CTRL_EPOCH] + 1u;
 
-  if (warp == SCHED_WARP) {
+  if (warp == Roles<ATTN>::SCHED) {
     uint32_t q = 0, qphase = 0, req_phase = 0, mb_phase = 0;
     bool first = true;
     PfState pf;
@@ -1771,10 +1817,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cs_chain_kernel(const __grid_c
       }
       if (unit == UNIT_END) break;
       if (p.st[unit_stage(unit)].kind == STAGE_GEMM)
-        ok = epi_gemm_unit<NS, CG, CL>(p, sc, staging, unit, part, acc, acc_phase, last_buf, rank, tidx, epoch1);
+        ok = epi_gemm_unit<NS, CG, CL, NE, !ATTN>(p, sc, staging, unit, part, acc, acc_phase, last_buf, rank, tidx,
+                                                  epoch1);
       else if constexpr (ATTN)
-        ok = epi_attn_unit<NS, CG>(p, sc, staging, unit, s_phase, o_phase, last_buf, tidx, acc, acc_phase, rank,
-                                   epoch1);
+        ok = epi_attn_unit<NS, CG, NE>(p, sc, staging, unit, s_phase, o_phase, last_buf, tidx, acc, acc_phase, rank,
+                                       epoch1);
     }
     if (lane == 0) tma_store_wait_all<0>();
     __syncwarp();
