@@ -1283,12 +1283,15 @@ __device__ bool epi_attn_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
     l_run += ls[0] + ls[1];
     fence_proxy_async_shared();
     tc_fence_before();
-    __syncwarp();
-    if (lane == 0) {
-      if constexpr (CG == 1)
-        mbar_arrive(&sc->p_full);
-      else
-        mbar_arrive_cluster(mapa_shared(&sc->p_full, 0));  // the pair leader issues P V
+    if (CG == 1 || rank == 0) {
+      // the pair leader's own warps (or a single SM's): one CTA-scope arrival each
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sc->p_full);
+    } else {
+      // the pair's second CTA: every epilogue warp's P is written, then one
+      // cluster-scope arrival on the leader's barrier (the leader issues P V)
+      named_bar_sync(1, NE * 32);
+      if (threadIdx.x == EPI_WARP0 * 32) mbar_arrive_cluster(mapa_shared(&sc->p_full, 0));
     }
   }
   // the last P V, then this warp's O dimensions (against m_ref) into registers
@@ -1597,7 +1600,7 @@ __global__ void __launch_bounds__(Roles<ATTN>::THREADS, 1) cs_chain_kernel(const
     mbar_init(&sc->mb_empty, CL - 1 > 0 ? CL - 1 : 1);  // every peer CTA takes the index
     mbar_init(&sc->s_full, 1);
     mbar_init(&sc->s_full_b, 1);
-    mbar_init(&sc->p_full, NE * CG);  // every epilogue warp of the unit's CTAs
+    mbar_init(&sc->p_full, CG == 1 ? NE : NE + 1);  // the leader's epilogue warps, one arrival from the peer
     mbar_init(&sc->o_full, 1);
     mbar_init(&sc->drain, 1);
     sc->abort = 0;
