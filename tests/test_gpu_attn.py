@@ -234,3 +234,64 @@ def test_attention_key_range_pieces(M, heads, kv, tile_m):
     assert torch.equal(outs[("tile", kv)][0], Y)
     assert oracle.rel_err(O, outs[("row", -1)][1]) <= 1e-3
     assert oracle.rel_err(Y, outs[("row", -1)][0]) <= 1e-3
+
+
+def _rising_logits(M, H, heads, dtype, a=8.0, seed=40):
+    """Inputs whose causal logits rise with the key index: Q = a in every
+    dimension (X column 1 is 1, Wq row 1 is a), K = x0 in every dimension (X
+    column 0 is floor(j/4)/256, Wk row 0 is 1), so S_ij = 128 a x0_j, exact in
+    fp32 from fp16 or bf16 operands.  Scaled by 1/sqrt(128) the logit grows by
+    11.3 a / 8 per 128 keys: with a = 8 about 16 powers of two per key block,
+    more than the 2^8 a row's maximum may rise before the kernel rescales the
+    output it accumulates in tensor memory, so every block rescales.  V and Wo
+    are random."""
+    F = heads * 128
+    g = torch.Generator().manual_seed(seed)
+    X = torch.randn(M, H, generator=g) * 0.02
+    X[:, 0] = torch.div(torch.arange(M), 4, rounding_mode="floor").float() / 256.0
+    X[:, 1] = 1.0
+    Wqkv = torch.randn(H, 3 * F, generator=g) * 0.02
+    Wqkv[:, :2 * F] = 0.0
+    Wqkv[1, :F] = a          # Q
+    Wqkv[0, F:2 * F] = 1.0   # K
+    Wo = torch.randn(F, H, generator=g) * 0.02
+    return cs_inputs.ChainInputs("rising", "attn", M, H, F, dtype, X.to(dtype), Wqkv=Wqkv.to(dtype), Wo=Wo.to(dtype))
+
+
+@pytest.mark.parametrize("kv", [-1, 1])
+@pytest.mark.parametrize("tile_m", [128, 256])
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_attention_rescales_the_tensor_memory_output(dtype, tile_m, kv):
+    """Logits that rise by more than 2^8 from one key block to the next make
+    every block raise the reference maximum and rescale O in TMEM (and l):
+    O and Y still match the oracle, under two policies, also split into
+    pieces whose merge takes different maxima."""
+    inp = _rising_logits(1024, 256, 2, dtype)
+    dev = device_tensors(inp, "nk")
+    Yref, _, Oref = _oracle(inp)
+    outs = {}
+    for pol in ("row", "tile"):
+        with plan_for(inp, pol, "nk", tile_m=tile_m, kv_chunk=kv) as plan:
+            cs.cs_chain_debug_poison_intermediate(plan, -1)
+            outs[pol] = forward(plan, dev).cpu()
+            O = intermediate(plan, 1, inp.M, inp.F, inp.dtype).cpu()
+            assert cs.cs_chain_status(plan) == cs.CS_OK
+    assert oracle.rel_err(O, Oref) <= TOL
+    assert oracle.rel_err(outs["row"], Yref) <= TOL
+    assert torch.equal(outs["row"], outs["tile"])
+
+
+@pytest.mark.parametrize("tile_m", [128, 256])
+@pytest.mark.parametrize("M,H,heads", [(300, 384, 3), (513, 256, 2), (1100, 256, 1)])
+def test_attention_chain_parity_bf16(M, H, heads, tile_m):
+    """The attention chain in bf16 (P and O rounded to bf16) against the oracle."""
+    inp = cs_inputs.make_custom("attn", M, H, heads * 128, dtype=torch.bfloat16, seed=39)
+    dev = device_tensors(inp, "nk")
+    with plan_for(inp, "row", "nk", tile_m=tile_m) as plan:
+        Y = forward(plan, dev)
+        QKV = intermediate(plan, 0, M, 3 * inp.F, inp.dtype)
+        O = intermediate(plan, 1, M, inp.F, inp.dtype)
+    Yref, QKVref, Oref = _oracle(inp)
+    assert oracle.rel_err(QKV.cpu(), QKVref) <= TOL
+    assert oracle.rel_err(O.cpu(), Oref) <= TOL
+    assert oracle.rel_err(Y.cpu(), Yref) <= TOL
