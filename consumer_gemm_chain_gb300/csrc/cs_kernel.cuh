@@ -3,8 +3,9 @@
 // CTAs (or clusters) pull work units from a dependency-ordered schedule
 // through a global atomic counter (a megakernel-style task queue: a dependent
 // task starts once the slice it reads is done, not when the whole producer op
-// is done).  Roles inside a CTA (224 threads):
-//   warp 6      : scheduler.  Claims the next unit just in time (when the TMA
+// is done).  Roles inside a CTA (224 threads; 352 in the attention
+// instantiations, which have eight epilogue warps):
+//   last warp   : scheduler (warp 6, or 10).  Claims the next unit just in time (when the TMA
 //                 warp is a few K-slices from the end of its current unit),
 //                 and for consumer units polls the producer tile semaphores of
 //                 the unit's K range with all 32 lanes at once, publishing how
@@ -15,11 +16,14 @@
 //                 the loop, an out-of-line wait at the bound) and fences the
 //                 async proxy.
 //   warp 1      : TMEM allocator (whole warp) and tcgen05.mma issuer (lane 0).
-//   warps 2..5  : epilogue: tcgen05.ld of the fp32 accumulator, bias + GeLU /
-//                 SiLU*up / none, downcast, swizzled smem staging, TMA store,
-//                 then (producer stages) release-increment of the tile
-//                 semaphore and of the row counter; the last K-split of a
-//                 small tile sums the splits' partials first.
+//   warps 2..5  : epilogue (2..9 for attention: two warps per TMEM lane
+//                 quadrant, each on half of a tile's columns): tcgen05.ld of
+//                 the fp32 accumulator, bias + GeLU / SiLU*up / none,
+//                 downcast, swizzled smem staging, TMA store, then (producer
+//                 stages) release-increment of the tile semaphore and of the
+//                 row counter; the last K-split of a small tile sums the
+//                 splits' partials first.  Attention units run their softmax
+//                 here, between the S = QK^T and P V MMAs.
 // CG = 2 (pair mode): a 2-CTA cluster shares one 256 x 256 tile.  Each CTA
 // loads its 128 rows of A and its half of B's columns; the leader (rank 0)
 // issues tcgen05.mma.cta_group::2, whose accumulator rows 0-127 land in the
