@@ -368,6 +368,9 @@ Geometry geometry(const cs_chain_desc* d, int num_sms, int workers = 0) {
     }
     sp = std::min(sp, max_sp);
     sp = std::max(1, std::min(sp, 15));
+    // a Stream-K tail asked for with automatic K-splits: the last stage stays
+    // unsplit (its tail's units share K-slices instead)
+    if (d->split_k == 0 && d->sk_tiles > 0 && s == g.stages - 1) sp = 1;
     g.kps[s] = cdiv(g.k_iters[s], sp);
     g.splits[s] = cdiv(g.k_iters[s], g.kps[s]);  // no empty split
   }

@@ -212,6 +212,25 @@ def tune_shape(torch, kind, H, F, dtype, heads, Ms, log=print, layout="nk"):
                     continue
                 if info["sk_tiles"] == skt:
                     first[c.key] = us
+        # 1c: at small M, the two fastest tile shapes with automatic K-splits for
+        # the producers and a Stream-K last stage (all of its tiles shared out
+        # over the resident workers)
+        if M <= 256:
+            shapes = []
+            for key in sorted(first, key=first.get):
+                if key[3] == 0 and key[:2] not in shapes:
+                    shapes.append(key[:2])
+            for tm, tn in shapes[:2]:
+                info0 = infos[next(k for k in infos if k[:2] == (tm, tn))]
+                last = info0["stages"] - 1
+                skt = info0["n_tiles"][last] * -(-M // info0["tile_m"])
+                c = Candidate(kind, shape, base, tm, tn, 0, skt, 0)
+                try:
+                    us, info = run(c)
+                except cs.CSError:
+                    continue
+                if info["sk_tiles"] == skt:
+                    first[c.key] = us
         top = sorted(first, key=first.get)[:3]
         # 2: the three fastest under every policy (the control included)
         best = {}

@@ -180,7 +180,9 @@ typedef struct cs_chain_desc {
                           write fp32 partial tiles to a plan-owned workspace; the
                           last to finish sums them in K order (the same bits on
                           every call and under every policy) and runs the
-                          epilogue.  Needs an unsplit last stage (split_k 1 there).
+                          epilogue.  Needs an unsplit last stage: with split_k
+                          0 (auto) the last stage then takes no K-splits, with
+                          split_k > 1 the tail is not applied.
                           0 = auto (the tuning table's choice, else none),
                           -1 = none, n = that many tiles.                          */
   int sk_units;        /* Stream-K units for those tiles; 0 = one per worker (SM,

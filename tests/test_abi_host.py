@@ -316,6 +316,21 @@ def test_stream_k_tail_schedule(cs, M, H, F, tile_m, sk_tiles, sk_units):
         assert all(nc == len(parts) for _, _, _, nc in parts)
 
 
+def test_stream_k_with_automatic_splits_leaves_the_last_stage_unsplit(cs):
+    """At small M the automatic rule splits every stage; asking for a Stream-K
+    tail with split_k 0 keeps the producers' splits and leaves the last stage
+    unsplit, its tiles shared out as Stream-K units."""
+    for kind, H, F, M in (("gelu", 12288, 6144, 1), ("swiglu", 8192, 2752, 16), ("gelu", 12288, 6144, 256)):
+        plain = cs.cs_chain_plan_info(cs.cs_chain_desc_init(kind=kind, M=M, H=H, F=F, tuned=-1), 152)
+        assert plain["split_k"][1] > 1
+        d = cs.cs_chain_desc_init(kind=kind, M=M, H=H, F=F, tuned=-1, sk_tiles=4096)
+        q = cs.cs_chain_plan_info(d, 152)
+        assert q["split_k"][0] == plain["split_k"][0] and q["split_k"][1] == 1
+        assert q["sk_tiles"] == q["n_tiles"][1] * -(-M // q["tile_m"]) and q["sk_units"] > 0
+        units = [cs.decode_unit(u) for u in cs.cs_schedule_build(d, 152)]
+        assert sum(1 for s, _, _, k in units if s == 1 and k == 15) == q["sk_units"]
+
+
 def test_stream_k_needs_an_unsplit_last_stage(cs):
     d = cs.cs_chain_desc_init(M=64, H=4096, F=4096, split_k=4, sk_tiles=8, tuned=-1)
     q = cs.cs_chain_plan_info(d, 152)

@@ -70,11 +70,17 @@ def test_the_table_selects_a_stream_k_tail_where_it_won(tuned_table):
         entries = [e for e in json.load(f)["entries"] if e.get("sk_tiles")]
     if not entries:
         pytest.skip("no entry of the shipped table chose a Stream-K tail")
-    e = entries[0]
-    desc = cs.cs_chain_desc_init(kind=e["kind"], M=e["M"], H=e["H"], F=e["F"],
-                                 dtype=torch.float16 if e["dtype"] == "f16" else torch.bfloat16,
-                                 policy=e["policy"], weight_layout=e.get("layout", "nk"))
-    with cs.cs_chain_plan(desc) as plan:
-        q = cs.cs_chain_query(plan)
-    assert q["tuned_entry"] >= 0
-    assert q["sk_tiles"] == e["sk_tiles"] and q["sk_units"] == e["sk_units"]
+    for e in entries:
+        extra = dict(heads=e["F"] // 128, head_dim=128) if e["kind"] == "attn" else {}
+        desc = cs.cs_chain_desc_init(kind=e["kind"], M=e["M"], H=e["H"], F=e["F"],
+                                     dtype=torch.float16 if e["dtype"] == "f16" else torch.bfloat16,
+                                     policy=e["policy"], weight_layout=e.get("layout", "nk"), **extra)
+        with cs.cs_chain_plan(desc) as plan:
+            q = cs.cs_chain_query(plan)
+        assert q["tuned_entry"] >= 0, e
+        assert q["sk_tiles"] == e["sk_tiles"], e
+        # sk_units 0: one Stream-K unit per resident worker
+        assert q["sk_units"] == e["sk_units"] if e["sk_units"] else 0 < q["sk_units"] <= q["workers"], e
+        if e["split_k"] == 0:
+            # automatic K-splits: the last stage unsplit, its tiles shared out
+            assert q["split_k"][q["stages"] - 1] == 1, e
