@@ -125,7 +125,8 @@ def parse(argv=None):
     ap.add_argument("--tile-m", type=int, default=0)
     ap.add_argument("--split-k", type=int, default=0)
     ap.add_argument("--prefetch", type=int, default=0, help="L2 prefetch distance (0 auto, -1 off)")
-    ap.add_argument("--raster", type=int, default=0, help="0 auto, 1 column-major, 2 row-major in a group")
+    ap.add_argument("--raster", type=int, default=0,
+                    help="0 auto, 1 column-major, 2 row-major in a group, 3 K-range-major split consumers")
     ap.add_argument("--pdl", type=int, default=0, help="programmatic dependent launch: 0 auto (on), 1 on, -1 off")
     ap.add_argument("--tuning", default="default",
                     help="tuning table for the plans' auto fields: 'default' (the package's table, when "
@@ -932,9 +933,9 @@ def stream_k_remainder(q):
 
 
 def plan_record(q):
-    """Tile shape, K-splits and tuning entry of a plan, for the sweep records."""
+    """Tile shape, K-splits, unit order and tuning entry of a plan, for the sweep records."""
     return {"tile_m": q["tile_m"], "tile_n": q["tile_n"][q["stages"] - 1], "split_k": max(q["split_k"]),
-            "tuned_entry": q["tuned_entry"]}
+            "splits": q["split_k"][: q["stages"]], "raster": q["raster"], "tuned_entry": q["tuned_entry"]}
 
 
 def _roof_frac(fl, by, us, peaks):

@@ -73,7 +73,8 @@ class cs_chain_desc(ctypes.Structure):
                 ("tile_n", ctypes.c_int), ("tile_m", ctypes.c_int), ("split_k", ctypes.c_int),
                 ("prefetch", ctypes.c_int), ("raster", ctypes.c_int), ("pdl", ctypes.c_int),
                 ("tuned", ctypes.c_int), ("out_release", ctypes.c_int), ("spin_timeout_ns", ctypes.c_ulonglong),
-                ("sk_tiles", ctypes.c_int), ("sk_units", ctypes.c_int), ("kv_chunk", ctypes.c_int)]
+                ("sk_tiles", ctypes.c_int), ("sk_units", ctypes.c_int), ("kv_chunk", ctypes.c_int),
+                ("split_k_first", ctypes.c_int)]
 
 
 class cs_mlp_args(ctypes.Structure):
@@ -96,7 +97,7 @@ class cs_chain_info(ctypes.Structure):
                 ("policy", ctypes.c_int), ("tuned_entry", ctypes.c_int),
                 ("out_tile_sems", ctypes.c_void_p), ("out_row_sems", ctypes.c_void_p), ("out_sem_words", ctypes.c_size_t),
                 ("sk_tiles", ctypes.c_int), ("sk_units", ctypes.c_int), ("sk_q", ctypes.c_int),
-                ("workers", ctypes.c_int), ("kv_chunk", ctypes.c_int)]
+                ("workers", ctypes.c_int), ("kv_chunk", ctypes.c_int), ("raster", ctypes.c_int)]
 
 
 def _load() -> ctypes.CDLL:
@@ -367,7 +368,7 @@ def _info_dict(i: cs_chain_info) -> dict:
             "sem_words": [i.sem_words[0], i.sem_words[1]], "policy": POLICY_NAMES.get(i.policy, i.policy),
             "tuned_entry": i.tuned_entry, "out_tile_sems": i.out_tile_sems, "out_row_sems": i.out_row_sems,
             "out_sem_words": i.out_sem_words, "sk_tiles": i.sk_tiles, "sk_units": i.sk_units, "sk_q": i.sk_q,
-            "workers": i.workers, "kv_chunk": i.kv_chunk}
+            "workers": i.workers, "kv_chunk": i.kv_chunk, "raster": i.raster}
 
 
 def cs_schedule_build(desc: cs_chain_desc, num_sms: int) -> list[int]:

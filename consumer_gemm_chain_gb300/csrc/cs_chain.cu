@@ -93,6 +93,7 @@ struct cs_chain_s {
   int units[3] = {0, 0, 0};
   int lag = 0;
   int group_m = 1;
+  int raster = 1;  // order used: 1 column-major, 2 row-major, 3 K-range-major split consumers
   int stride = 1;
   int bn[3] = {128, 128, 128};
   int cfg_b = 0;  // 1: 48 KB-stage kernel (256-wide one-SM tiles or gate|up)
@@ -194,6 +195,7 @@ struct Geometry {
   int kps[3] = {0, 0, 0};  // K-slices per split
   int lag = 1, group_m = 1, stride = 1;
   bool row_major = false;  // tiles of a group in row-major order
+  bool ks_major = false;   // a split later stage's units of a group by K range first
   // Stream-K tail of the last stage: its last sk_tiles tiles in dispatch order
   // become sk_units units of sk_q consecutive K-slices each (the last shorter)
   int sk_tiles = 0, sk_units = 0, sk_q = 0, sk_max_nc = 0;
@@ -221,7 +223,9 @@ cs_status validate(const cs_chain_desc* d) {
   if (d->M < 1 || d->M > 128 * 4095) return fail(CS_ERR_INVALID_ARG, "M=%d out of range [1, %d]", d->M, 128 * 4095);
   if (d->split_k < 0 || d->split_k > 15) return fail(CS_ERR_INVALID_ARG, "split_k=%d (0..15)", d->split_k);
   if (d->prefetch < -1 || d->prefetch > 64) return fail(CS_ERR_INVALID_ARG, "prefetch=%d (-1..64)", d->prefetch);
-  if (d->raster < 0 || d->raster > 2) return fail(CS_ERR_INVALID_ARG, "raster=%d (0..2)", d->raster);
+  if (d->raster < 0 || d->raster > 3) return fail(CS_ERR_INVALID_ARG, "raster=%d (0..3)", d->raster);
+  if (d->split_k_first < 0 || d->split_k_first > 15)
+    return fail(CS_ERR_INVALID_ARG, "split_k_first=%d (0..15)", d->split_k_first);
   if (d->pdl < -1 || d->pdl > 1) return fail(CS_ERR_INVALID_ARG, "pdl=%d (-1..1)", d->pdl);
   if (d->sk_tiles < -1 || d->sk_tiles > 65534) return fail(CS_ERR_INVALID_ARG, "sk_tiles=%d (-1..65534)", d->sk_tiles);
   if (d->sk_units < 0 || d->sk_units > 16383) return fail(CS_ERR_INVALID_ARG, "sk_units=%d (0..16383)", d->sk_units);
@@ -351,10 +355,12 @@ Geometry geometry(const cs_chain_desc* d, int num_sms, int workers = 0) {
     // traffic dominate); up to 32 rows stream weights only and take up to 15
     // (measured: seven splits of a full 128-row block, stress M=128, 141 us
     // against 99 us with four)
-    const bool wide = d->split_k > 0 || d->M <= 32;
+    // an explicit count for the first stage (split_k_first) overrides split_k there
+    const int want = (s == 0 && d->split_k_first > 0) ? d->split_k_first : d->split_k;
+    const bool wide = want > 0 || d->M <= 32;
     const int max_sp = wide ? std::max(1, std::min(15, g.k_iters[s] / 8))
                             : std::max(1, std::min(4, g.k_iters[s] / 32));
-    int sp = d->split_k;
+    int sp = want;
     if (sp == 0) {
       // fewest (waves x K-slices per split): a split count that fills whole
       // waves; a larger count must win by 10 % (each split adds a partial tile
@@ -392,6 +398,7 @@ Geometry geometry(const cs_chain_desc* d, int num_sms, int workers = 0) {
              : g.cg == 2   ? std::max(1, std::min(4, g.m_tiles / 2))
                            : 8;
   g.row_major = d->raster == 2;
+  g.ks_major = d->raster == 3;
   if (g.group_m > g.m_tiles) g.group_m = g.m_tiles;
   const int groups = cdiv(g.m_tiles, g.group_m);
   g.lag = d->lag >= 0 ? d->lag : 1;
@@ -431,6 +438,7 @@ cs::SchedGeo sched_geo(const Geometry& g) {
   sg.group_m = g.group_m;
   sg.lag = g.lag;
   sg.row_major = g.row_major ? 1 : 0;
+  sg.ks_major = g.ks_major ? 1 : 0;
   for (int s = 0; s < 3; ++s) {
     sg.n_tiles[s] = g.n_tiles[s];
     sg.splits[s] = g.splits[s];
@@ -503,6 +511,7 @@ void shape_plan(cs_chain_s* p, const Geometry& g, int kind, int M) {
   }
   p->lag = g.lag;
   p->group_m = g.group_m;
+  p->raster = g.row_major ? 2 : g.ks_major ? 3 : 1;
   p->stride = g.stride;
   p->sk_tiles = g.sk_tiles;
   p->sk_units = g.sk_units;
@@ -546,6 +555,7 @@ void info_geometry(const cs_chain_s* p, int n_fused, cs_chain_info* info) {
   info->sk_q = p->sk_q;
   info->workers = p->workers > 0 ? p->workers : p->num_sms / p->cl;
   info->kv_chunk = p->kv;
+  info->raster = p->raster;
 }
 
 int device_sms(int* out) {
@@ -1564,6 +1574,10 @@ cs_status cs_mlp_forward_noalloc(const cs_chain_desc* desc, const cs_mlp_args* a
   if (desc->split_k > 1)
     return fail(CS_ERR_UNSUPPORTED, "split_k=%d: the allocation-free forward runs unsplit tiles (split_k 0 or 1)",
                 desc->split_k);
+  if (desc->split_k_first > 1)
+    return fail(CS_ERR_UNSUPPORTED,
+                "split_k_first=%d: the allocation-free forward runs unsplit tiles (split_k_first 0 or 1)",
+                desc->split_k_first);
   if (desc->sk_tiles > 0)
     return fail(CS_ERR_UNSUPPORTED, "sk_tiles=%d: the allocation-free forward has no Stream-K workspace",
                 desc->sk_tiles);
@@ -1581,6 +1595,7 @@ cs_status cs_mlp_forward_noalloc(const cs_chain_desc* desc, const cs_mlp_args* a
   cs_chain_s p;
   p.d = *desc;
   p.d.split_k = 1;  // no split-K workspace in the fixed array
+  p.d.split_k_first = 0;
   p.d.sk_tiles = -1;
   if (p.d.policy == CS_SYNC_AUTO) p.d.policy = CS_SYNC_TILE;
   p.device = dev;

@@ -4,9 +4,11 @@
 //
 // Row tiles form groups of group_m.  The fused order takes steps t = 0, 1, ...;
 // at step t, stage s lists every unit of group t - s*lag (column-tile-major
-// inside the group, or row-major), so every producer unit a consumer waits on
-// is listed at an earlier step or earlier in the same step, and an in-order
-// dispatcher cannot deadlock.  A stage alone lists its groups in turn.
+// inside the group, or row-major; a split stage after the first may instead
+// list K-split 0 of every tile of the group, then K-split 1, ...), so every
+// producer unit a consumer waits on is listed at an earlier step or earlier in
+// the same step, and an in-order dispatcher cannot deadlock.  A stage alone
+// lists its groups in turn.
 //
 // A causal stage split into key-range pieces (kv[s] > 0: the attention units
 // of tile row m cover key groups 0..m, in pieces of kv[s] groups) lists
@@ -23,6 +25,7 @@ struct SchedGeo {
   int group_m = 1;    // tile rows per group
   int lag = 1;        // groups between consecutive stages
   int row_major = 0;  // units of a group row by row instead of column by column
+  int ks_major = 0;   // stages after the first: units of a group by K-split, then column, then row
   int n_tiles[3] = {0, 0, 0};
   int splits[3] = {1, 1, 1};
   int kv[3] = {0, 0, 0};  // key groups per piece of a causal stage (0: none)
@@ -104,6 +107,14 @@ __host__ __device__ inline uint32_t sched_in_group(const SchedGeo& g, int s, int
     const long long r = j % per_row;
     n = static_cast<int>(r / sp);
     ks = static_cast<int>(r % sp);
+  } else if (g.ks_major && s > 0 && sp > 1) {
+    // K range first: a consumer's K range waits only on the producer column
+    // tiles of that range, which a producer stage in several waves finishes first
+    const long long per_ks = static_cast<long long>(rows) * g.n_tiles[s];
+    ks = static_cast<int>(j / per_ks);
+    const long long r = j % per_ks;
+    n = static_cast<int>(r / rows);
+    m = m0 + static_cast<int>(r % rows);
   } else {
     const long long per_col = static_cast<long long>(rows) * sp;
     n = static_cast<int>(j / per_col);

@@ -214,6 +214,8 @@ struct TuneEntry {
   int layout = -1;  // cs_weight_layout, -1 = any
   int policy = -1;  // cs_policy, -1 = any
   int tile_m = 0, tile_n = 0, split_k = 0, group_m = 0;
+  int split_k_first = 0;           // K-splits of the first stage (0: as split_k)
+  int raster = 0;                  // unit order inside a row group (0: the built-in rule)
   int sk_tiles = 0, sk_units = 0;  // Stream-K tail of the last stage (0: none)
   double us = std::numeric_limits<double>::infinity();  // measured time per chain
 };
@@ -269,6 +271,8 @@ bool read_entry(const JVal& o, TuneEntry& e, std::string& err) {
       !int_field(o, "tile_m", 0, 512, true, &e.tile_m, err) || !int_field(o, "tile_n", 0, 256, true, &e.tile_n, err) ||
       !int_field(o, "split_k", 0, 15, true, &e.split_k, err) ||
       !int_field(o, "group_m", 0, 4095, false, &e.group_m, err) ||
+      !int_field(o, "split_k_first", 0, 15, false, &e.split_k_first, err) ||
+      !int_field(o, "raster", 0, 3, false, &e.raster, err) ||
       !int_field(o, "sk_tiles", 0, 65534, false, &e.sk_tiles, err) ||
       !int_field(o, "sk_units", 0, 16383, false, &e.sk_units, err))
     return false;
@@ -286,7 +290,8 @@ bool read_entry(const JVal& o, TuneEntry& e, std::string& err) {
 int cs_tune_apply(const cs_chain_desc* in, int num_sms, cs_chain_desc* out) {
   *out = *in;
   if (in->tuned < 0) return -1;
-  const bool tiles_auto = in->tile_m == 0 && in->tile_n == 0 && in->split_k == 0 && in->group_m == 0;
+  const bool tiles_auto =
+      in->tile_m == 0 && in->tile_n == 0 && in->split_k == 0 && in->split_k_first == 0 && in->group_m == 0;
   const bool policy_auto = in->policy == CS_SYNC_AUTO;
   if (!tiles_auto && !policy_auto) return -1;
   std::lock_guard<std::mutex> lock(g_mu);
@@ -326,7 +331,9 @@ int cs_tune_apply(const cs_chain_desc* in, int num_sms, cs_chain_desc* out) {
     out->tile_m = e.tile_m;
     out->tile_n = e.tile_n;
     out->split_k = e.split_k;
+    out->split_k_first = e.split_k_first;
     out->group_m = e.group_m;
+    if (in->raster == 0) out->raster = e.raster;  // the desc leaves the order on auto
     if (in->sk_tiles == 0 && in->sk_units == 0) {  // the desc leaves the Stream-K tail on auto
       out->sk_tiles = e.sk_tiles;
       out->sk_units = e.sk_units;

@@ -9,8 +9,12 @@ GPU and environment).
 
 Per M: every candidate runs under TileSync (RowSync for the attention chain),
 and Stream-K tails of the last stage on the two fastest unsplit tile shapes;
-the three fastest are timed again under every policy, including the
-two-kernel control (so that the control, too, runs its best tiles); the best
+up to 64 rows also the two fastest split tile shapes with the later stages'
+units in K-range order (raster 3), with uniform splits and with more splits
+for the first stage (split_k_first); the four fastest are timed again in
+interleaved rounds, and the three fastest of those under every policy,
+including the two-kernel control (so that the control, too, runs its best
+tiles); the best
 candidate of each policy is re-timed against the built-in rules in
 interleaved rounds, and an entry is written per policy: the candidate's
 choices if it wins by at least 2 %, else zeros (the built-in rules).  Each candidate's
@@ -107,14 +111,16 @@ def _time(torch, fn, target_ms=12.0, warm_ms=60.0, repeats=1):
 
 
 class Candidate:
-    def __init__(self, kind, shape, policy, tile_m=0, tile_n=0, split_k=0, sk_tiles=0, sk_units=0, tuned=-1):
-        self.key = (tile_m, tile_n, split_k, sk_tiles, sk_units)
+    def __init__(self, kind, shape, policy, tile_m=0, tile_n=0, split_k=0, sk_tiles=0, sk_units=0,
+                 split_k_first=0, raster=0, tuned=-1):
+        self.key = (tile_m, tile_n, split_k, sk_tiles, sk_units, split_k_first, raster)
         self.policy = policy
         self.desc = cs.cs_chain_desc_init(kind=kind, M=shape["M"], H=shape["H"], F=shape["F"],
                                           dtype=shape["dtype"], policy=policy, weight_layout=shape["layout"],
                                           heads=shape["heads"] or 12, tile_m=tile_m, tile_n=tile_n,
                                           split_k=split_k, sk_tiles=sk_tiles if sk_tiles else -1,
-                                          sk_units=sk_units, tuned=tuned)
+                                          sk_units=sk_units, split_k_first=split_k_first, raster=raster,
+                                          tuned=tuned)
 
 
 def stream_k_candidates(info):
@@ -146,7 +152,7 @@ def _rel(torch, a, b):
     return float((a.float() - b.float()).abs().max() / b.float().abs().max().clamp_min(1e-30))
 
 
-def tune_shape(torch, kind, H, F, dtype, heads, Ms, log=print, layout="nk"):
+def tune_shape(torch, kind, H, F, dtype, heads, Ms, log=print, layout="nk", verbose=False):
     dev = torch.device("cuda", torch.cuda.current_device())
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     tiles = ATTN_TILES if kind == "attn" else MLP_TILES
@@ -176,7 +182,11 @@ def tune_shape(torch, kind, H, F, dtype, heads, Ms, log=print, layout="nk"):
                     if not err <= 1e-2:
                         raise RuntimeError(f"M={M} {c.policy} {c.key}: output differs from the built-in plan's "
                                            f"by {err:.2e}")
-                return _time(torch, fwd), info
+                us = _time(torch, fwd)
+                if verbose:
+                    log(f"  {kind} M={M:5d} {c.policy:8s} {c.key} splits {info['split_k'][:info['stages']]}: "
+                        f"{us:8.2f} us")
+                return us, info
 
         ref = None
         auto = Candidate(kind, shape, base)
@@ -231,12 +241,46 @@ def tune_shape(torch, kind, H, F, dtype, heads, Ms, log=print, layout="nk"):
                     continue
                 if info["sk_tiles"] == skt:
                     first[c.key] = us
-        top = sorted(first, key=first.get)[:3]
-        # 2: the three fastest under every policy (the control included)
+        # 1d: up to 64 rows, the two fastest split tile shapes with the later
+        # stages' units in K-range order (raster 3), under uniform splits and
+        # with more splits for the first stage: producers in several waves
+        # finish their column tiles in turn, which K-range-major consumers use
+        if M <= 64:
+            shapes = []
+            for key in sorted(first, key=first.get):
+                if key[2] != 1 and key[3] == 0 and key[:2] not in [k[:2] for k in shapes]:
+                    shapes.append(key)
+            seen = set()
+            for tm, tn, sp, *_ in shapes[:2]:
+                combos = [(s, 0) for s in (0, sp, 4, 6, 8)] + [(sp, f) for f in (2 * sp, 6, 8, 12) if f != sp]
+                for s, f in dict.fromkeys(combos):
+                    c = Candidate(kind, shape, base, tm, tn, s, 0, 0, f, 3)
+                    try:
+                        us, info = run(c)
+                    except cs.CSError:
+                        continue
+                    real = (info["tile_m"], tuple(info["tile_n"]), tuple(info["split_k"]))
+                    want_first = f or s
+                    if real in seen or info["raster"] != 3 or (want_first and info["split_k"][0] != want_first):
+                        continue  # clamped onto another candidate, or a repeat
+                    seen.add(real)
+                    first[c.key] = us
+        # 2a: the four fastest again under the base policy, in interleaved
+        # rounds (at small M single timings of near candidates differ by more
+        # than their real gaps), keeping the three fastest medians
+        top = sorted(first, key=first.get)[:4]
+        again = {key: [] for key in top}
+        for r in range(3):
+            for i in range(len(top)):
+                key = top[(r + i) % len(top)]
+                again[key].append(run(Candidate(kind, shape, base, *key))[0])
+        base_us = {key: statistics.median(v) for key, v in again.items()}
+        top = sorted(top, key=base_us.get)[:3]
+        # 2b: the three fastest under every policy (the control included)
         best = {}
         for pol in POLICIES:
             for key in top:
-                us = first[key] if pol == base else run(Candidate(kind, shape, pol, *key))[0]
+                us = base_us[key] if pol == base else run(Candidate(kind, shape, pol, *key))[0]
                 if pol not in best or us < best[pol][1]:
                     best[pol] = (key, us)
         # 3: each policy's best against the built-in rules, interleaved rounds;
@@ -255,16 +299,21 @@ def tune_shape(torch, kind, H, F, dtype, heads, Ms, log=print, layout="nk"):
             us = statistics.median(times[(pol, "tuned")])
             us_auto = statistics.median(times[(pol, "builtin")])
             if us < (1.0 - MARGIN) * us_auto:
-                tm, tn, sp, skt, sku = finals[pol].key
+                tm, tn, sp, skt, sku, spf, ras = finals[pol].key
             else:
-                tm, tn, sp, skt, sku, us = 0, 0, 0, 0, 0, us_auto
+                tm, tn, sp, skt, sku, spf, ras, us = 0, 0, 0, 0, 0, 0, 0, us_auto
             entry = {"kind": kind, "dtype": dtype, "H": H, "F": F, "M": M, "sms": sms, "layout": layout,
                      "policy": pol, "tile_m": tm, "tile_n": tn, "split_k": sp, "group_m": 0,
                      "us": round(us, 2), "builtin_us": round(us_auto, 2)}
             if skt:
                 entry.update(sk_tiles=skt, sk_units=sku)
+            if spf:
+                entry.update(split_k_first=spf)
+            if ras:
+                entry.update(raster=ras)
             entries.append(entry)
-            choice = (f"tile {tm}x{tn} split {sp:2d}" + (f" stream-K {skt}/{sku}" if skt else "")) if tm else \
+            choice = (f"tile {tm}x{tn} split {sp:2d}" + (f" first {spf}" if spf else "") +
+                      (f" raster {ras}" if ras else "") + (f" stream-K {skt}/{sku}" if skt else "")) if tm else \
                 "built-in rules    "
             log(f"{kind} M={M:5d} {pol:8s} {choice}: {us:8.1f} us (built-in rules {us_auto:8.1f} us)")
         del t, Y, ref
@@ -305,6 +354,7 @@ def main(argv=None):
     ap.add_argument("--M", default="", help="comma-separated row counts (default: the preset's list)")
     ap.add_argument("--out", default=cs.TUNE_TABLE)
     ap.add_argument("--merge", action="store_true", help="keep the file's entries for other shapes / M")
+    ap.add_argument("--verbose", action="store_true", help="log every candidate's timing")
     args = ap.parse_args(argv)
     shapes = [PRESETS[name] for name in args.preset]
     try:
@@ -323,7 +373,7 @@ def main(argv=None):
     for kind, H, F, dtype, heads, Ms in shapes:
         if args.M:
             Ms = tuple(int(v) for v in args.M.split(","))
-        entries += tune_shape(torch, kind, H, F, dtype, heads, Ms, layout=args.layout,
+        entries += tune_shape(torch, kind, H, F, dtype, heads, Ms, layout=args.layout, verbose=args.verbose,
                               log=lambda s: print(s, file=sys.stderr, flush=True))
         n = write_table(args.out, entries, args.merge, device)  # after every shape: keep what is measured
     print(json.dumps({"out": args.out, "entries": n}))

@@ -42,7 +42,7 @@
 extern "C" {
 #endif
 
-#define CS_ABI_VERSION 6
+#define CS_ABI_VERSION 7
 
 typedef struct cs_chain_s* cs_chain_t;
 
@@ -144,9 +144,18 @@ typedef struct cs_chain_desc {
                           the TMA loads into L2; 0 = auto (off: measured slower on
                           GB300), -1 = off                                          */
   int raster;          /* order of a stage's tiles inside a row group: 0 = auto
-                          (column-major), 1 = column-major (tiles sharing a weight
-                          tile run together), 2 = row-major (row blocks complete one
-                          after another, so their consumers can start sooner)      */
+                          (column-major, or the tuning table's choice), 1 =
+                          column-major (tiles sharing a weight tile run together,
+                          a tile's K-splits one after another), 2 = row-major (row
+                          blocks complete one after another, so their consumers
+                          can start sooner), 3 = column-major for the first stage
+                          and K-range-major for a split later stage: K-split 0 of
+                          every tile of the group, then K-split 1, ... A split
+                          consumer's K range needs only the producer tiles of that
+                          range, so when the producers run in more than one wave
+                          (they finish in column-tile order) the first consumers
+                          start while the later producer tiles still stream their
+                          weights.                                                 */
   int pdl;             /* programmatic dependent launch: a forward queued behind another
                           kernel on the stream starts its CTAs as the earlier grid's
                           CTAs exit, and sets up its barriers and tensor memory while
@@ -154,11 +163,13 @@ typedef struct cs_chain_desc {
                           that grid has completed (griddepcontrol.wait).  0 = auto
                           (on), 1 = on, -1 = off (plain stream order)               */
   int tuned;           /* 0 = consult the loaded tuning table (cs_tune_load): when
-                          tile_m, tile_n, split_k and group_m are all auto, they are
-                          taken from the entry of the nearest measured M for this
-                          chain shape, dtype, layout and grid size, and policy AUTO
-                          is resolved from it; an entry whose choices do not fit the
-                          desc is ignored.  -1 = never (built-in rules only).       */
+                          tile_m, tile_n, split_k, split_k_first and group_m are
+                          all auto, they are taken from the entry of the nearest
+                          measured M for this chain shape, dtype, layout and grid
+                          size (and raster, where the desc leaves it on auto), and
+                          policy AUTO is resolved from it; an entry whose choices
+                          do not fit the desc is ignored.  -1 = never (built-in
+                          rules only).                                              */
   int out_release;     /* 1: the last stage releases Y the way producers release the
                           intermediate: once a tile of Y is stored, its tile
                           semaphore and its 128-row block's counter are
@@ -202,6 +213,13 @@ typedef struct cs_chain_desc {
                           merge costs more than the shorter critical path saves
                           on GB300), -1 = whole rows.  At most 15 pieces per row
                           (c is raised to fit).                                   */
+  int split_k_first;   /* K-splits of the first GEMM stage (GEMM1 of an MLP, the
+                          QKV GEMM of the attention chain): 0 = as split_k,
+                          1..15 = that many (at least 8 K-slices each; with
+                          split_k 0 the other stages keep the automatic rule).  A
+                          first stage split into more units than the grid runs at
+                          once finishes its column tiles in waves, which raster 3
+                          lets the consumers use.                                 */
 } cs_chain_desc;
 
 /* Fill *desc with defaults (kind MLP_GELU, F16, TILE, KN, auto everything else). */
@@ -326,6 +344,8 @@ typedef struct cs_chain_info {
                               size leaves SMs out); cs_chain_plan_info, which needs
                               no GPU, reports num_sms / (tile_m / 128)          */
   int kv_chunk;            /* ATTN: key groups per attention piece (0: whole rows) */
+  int raster;              /* order actually used: 1 column-major, 2 row-major,
+                              3 K-range-major split consumers (desc.raster)    */
 } cs_chain_info;
 
 cs_status cs_chain_query(cs_chain_t plan, cs_chain_info* info);
@@ -369,6 +389,9 @@ cs_status cs_schedule_build(const cs_chain_desc* desc, int num_sms, uint32_t* un
  *            "F": int, "M": int, "sms": int (grid the entry was measured on),
  *            "tile_m": 0|128|256|512, "tile_n": 0|128|256, "split_k": 0..15,
  *            optional "group_m": int >= 0 (default 0 = auto),
+ *            optional "split_k_first": 0..15 (default 0 = as split_k),
+ *            optional "raster": 0..3 (applied when the desc leaves raster on 0;
+ *            default 0 = the built-in order),
  *            optional "sk_tiles": 0..65534, "sk_units": 0..16383 (Stream-K
  *            tail, applied when the desc leaves both on 0; default 0 = none),
  *            optional "layout": "kn"|"nk"|"any", "policy": "tile"|"row"|

@@ -33,7 +33,7 @@ def test_every_declared_symbol_is_exported(cs):
     for n in names:
         assert hasattr(lib, n), f"{n} declared in cs_chain.h but not exported"
     assert set(cs.chain.EXPORTED) == set(names)
-    assert cs.cs_abi_version() == 6
+    assert cs.cs_abi_version() == 7
 
 
 def test_desc_defaults(cs):
@@ -45,7 +45,8 @@ def test_desc_defaults(cs):
 @pytest.mark.parametrize("field,value", [("M", 0), ("H", 12), ("F", 0), ("dtype", 7), ("policy", 9),
                                          ("kind", 5), ("weight_layout", 3), ("lag", -2), ("num_sms", -1),
                                          ("split_k", 16), ("tile_n", 192), ("tile_m", 64), ("tile_m", 1024), ("M", 128 * 4096),
-                                         ("raster", 3), ("prefetch", -2), ("pdl", 2), ("pdl", -2),
+                                         ("raster", 4), ("raster", -1), ("split_k_first", 16),
+                                         ("split_k_first", -1), ("prefetch", -2), ("pdl", 2), ("pdl", -2),
                                          ("policy", -2), ("tuned", 1), ("tuned", -2), ("out_release", 2),
                                          ("out_release", -1)])
 def test_invalid_descs_are_rejected_without_a_gpu(cs, field, value):
@@ -81,7 +82,7 @@ def _check_order(dec, deps_of):
 @pytest.mark.parametrize("M,H,F,sms,lag,group,split", [(64, 256, 1024, 148, -1, 0, 1), (2048, 12288, 6144, 148, -1, 0, 1),
                                                        (2048, 12288, 6144, 152, 0, 3, 1), (1, 12288, 6144, 148, -1, 0, 3),
                                                        (1000, 8192, 2752, 148, 2, 1, 2), (1536, 8192, 8192, 148, 5, 5, 1)])
-@pytest.mark.parametrize("raster", [1, 2])
+@pytest.mark.parametrize("raster", [1, 2, 3])
 def test_schedule_is_dependency_ordered(cs, M, H, F, sms, lag, group, split, tile_n, tile_m, raster):
     d = cs.cs_chain_desc_init(M=M, H=H, F=F, lag=lag, group_m=group, tile_n=tile_n, tile_m=tile_m, split_k=split,
                               raster=raster)
@@ -143,6 +144,23 @@ def test_small_m_splits_k_automatically(cs):
     assert s0[:3] == [(0, 0, 0, 0), (0, 0, 0, 1), (0, 0, 0, 2)]
     big = [cs.decode_unit(u) for u in cs.cs_schedule_build(cs.cs_chain_desc_init(M=2048, H=12288, F=6144), 152)]
     assert {u[3] for u in big} == {0}             # enough tiles: no split at large M
+
+
+@pytest.mark.parametrize("kind,M,H,F,split,first", [
+    ("gelu", 1, 12288, 6144, 6, 9), ("gelu", 1, 12288, 6144, 0, 6), ("swiglu", 16, 8192, 2752, 4, 6),
+    ("attn", 16, 12288, 1536, 3, 8), ("gelu", 64, 12288, 6144, 3, 1)])
+def test_split_k_first_sets_the_first_stage_only(cs, kind, M, H, F, split, first):
+    """split_k_first replaces split_k (explicit or automatic) for the first
+    GEMM stage alone; the later stages keep what split_k gives them."""
+    extra = dict(heads=F // 128, head_dim=128) if kind == "attn" else {}
+    base = cs.cs_chain_desc_init(kind=kind, M=M, H=H, F=F, split_k=split, tile_m=128, tile_n=128, tuned=-1, **extra)
+    d = cs.cs_chain_desc_init(kind=kind, M=M, H=H, F=F, split_k=split, split_k_first=first, tile_m=128, tile_n=128,
+                              tuned=-1, **extra)
+    qb, q = cs.cs_chain_plan_info(base, 152), cs.cs_chain_plan_info(d, 152)
+    assert q["split_k"][0] == first and q["split_k"][1:] == qb["split_k"][1:]
+    units = [cs.decode_unit(u) for u in cs.cs_schedule_build(d, 152)]
+    assert {k for s, _, _, k in units if s == 0} == set(range(first))
+    assert q["sched_units"][0] == q["n_tiles"][0] * -(-M // 128) * first
 
 
 def test_attention_desc_validation(cs):
@@ -210,11 +228,12 @@ def test_the_abi_from_plain_c99(cs, tmp_path):
     assert p.returncode == 0 and p.stdout.strip() == "ok", p.stderr
 
 
-def _loop_order(stages, m_tiles, group_m, lag, n_tiles, splits, row_major, kv=0):
+def _loop_order(stages, m_tiles, group_m, lag, n_tiles, splits, row_major, kv=0, ks_major=False):
     """The fused dispatch order written as nested loops (steps, stages, a
     group's tiles), independently of the library's closed form.  kv > 0: the
     attention stage's units of tile row m are ceil((m + 1) / kv) key-range
-    pieces per head, listed row by row, head, then piece."""
+    pieces per head, listed row by row, head, then piece.  ks_major: a split
+    stage after the first lists K-split, then column tile, then row."""
     groups = -(-m_tiles // group_m)
     out = []
     for t in range(groups + (stages - 1) * lag):
@@ -227,6 +246,8 @@ def _loop_order(stages, m_tiles, group_m, lag, n_tiles, splits, row_major, kv=0)
                 out += [(s, m, n, k) for m in rows for n in range(n_tiles[s]) for k in range(-(-(m + 1) // kv))]
             elif row_major:
                 out += [(s, m, n, k) for m in rows for n in range(n_tiles[s]) for k in range(splits[s])]
+            elif ks_major and s > 0:
+                out += [(s, m, n, k) for k in range(splits[s]) for n in range(n_tiles[s]) for m in rows]
             else:
                 out += [(s, m, n, k) for n in range(n_tiles[s]) for m in rows for k in range(splits[s])]
     return out
@@ -238,7 +259,11 @@ _ORDER_CASES = [
     ("swiglu", 777, 8192, 2752, 0, 3, 3, 128, 2), ("gelu", 130000, 256, 512, 3, 7, 1, 128, 1),
     ("attn", 2048, 12288, 1536, -1, 0, 0, 256, 0), ("attn", 300, 12288, 1536, 2, 1, 0, 128, 2),
     ("attn", 2048, 12288, 1536, -1, 3, 0, 128, 0), ("attn", 1900, 1024, 512, 1, 2, 0, 256, 2),
-    ("attn", 640, 1024, 256, 0, 1, 0, 128, 0)]
+    ("attn", 640, 1024, 256, 0, 1, 0, 128, 0),
+    # K-range-major split consumers
+    ("gelu", 1, 12288, 6144, -1, 0, 6, 0, 3), ("swiglu", 16, 8192, 2752, -1, 0, 4, 128, 3),
+    ("gelu", 1000, 8192, 2752, 2, 1, 2, 128, 3), ("gelu", 700, 4096, 1024, 1, 2, 3, 256, 3),
+    ("attn", 16, 12288, 1536, -1, 0, 3, 128, 3), ("attn", 900, 1024, 512, 1, 2, 2, 256, 3)]
 
 
 # attention cases also with key-range pieces: auto, every group alone, three groups
@@ -257,7 +282,8 @@ def test_closed_form_schedule_equals_the_loop_order(cs, kind, M, H, F, lag, grou
         want_kv = max(kv, -(-m_tiles // 15)) if kv > 0 else 0  # auto: whole rows
         assert q["kv_chunk"] == (want_kv if want_kv < m_tiles else 0)
     want = _loop_order(q["stages"], m_tiles, q["group_m"], q["lag"], q["n_tiles"], q["split_k"], raster == 2,
-                       q.get("kv_chunk", 0))
+                       q.get("kv_chunk", 0), raster == 3)
+    assert q["raster"] == (raster or 1)
     got = [cs.decode_unit(u) for u in cs.cs_schedule_build(d, 152)]
     assert got == [(s, m, n, k) for s, m, n, k in want]
     assert q["n_units"] == len(got)

@@ -165,6 +165,31 @@ def test_gpt3_attention_shard(M):
     assert oracle.rel_err(Y, Yref) <= TOL
 
 
+@pytest.mark.parametrize("M,tile_m", [(16, 128), (300, 128), (600, 256)])
+def test_attention_k_range_major_output_projection(M, tile_m):
+    """raster 3 with split_k_first: the QKV GEMM takes its own (larger) split
+    count and the split Wo stage runs K range by K range; with the QKV units
+    delayed and QKV / O poisoned before every forward the output keeps its
+    bits, equals raster 1 with the same splits, and matches the oracle."""
+    inp = cs_inputs.make_custom("attn", M, 4096, 1024, seed=57)
+    dev = device_tensors(inp, "nk")
+    outs = {}
+    for raster in (1, 3):
+        with plan_for(inp, "row", "nk", tile_m=tile_m, split_k=2, split_k_first=4, raster=raster) as plan:
+            q = cs.cs_chain_query(plan)
+            assert q["raster"] == raster and q["split_k"] == [4, 1, 2]
+            cs.cs_chain_debug_poison_intermediate(plan, -1)
+            outs[raster] = forward(plan, dev).cpu()
+            if raster == 3:
+                g = torch.Generator().manual_seed(410)
+                cs.cs_chain_debug_set_delays(plan, 0, (torch.rand(q["units"][0], generator=g) * 100_000).long().tolist())
+                cs.cs_chain_debug_poison_intermediate(plan, -1)
+                assert torch.equal(forward(plan, dev).cpu(), outs[3])
+    Yref, _, _ = _oracle(inp)
+    assert oracle.rel_err(outs[3], Yref) <= TOL
+    assert torch.equal(outs[1], outs[3])
+
+
 @pytest.mark.parametrize("M", (300, 1024, 2048))
 def test_attention_pair_tiles_agree_with_single_sm_tiles(M):
     """128 x 128 single-SM tiles and 256 x 256 pair tiles (with two-query-block

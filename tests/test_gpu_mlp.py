@@ -371,6 +371,37 @@ def test_split_k_delay_injection_never_changes_a_bit():
             assert torch.equal(poisoned_forward(plan, dev).cpu(), ref), seed
 
 
+@pytest.mark.parametrize("kind,M,H,F,split,first", [
+    ("gelu", 1, 12288, 6144, 6, 6),    # GPT-3 shard at one row: producers in two waves
+    ("gelu", 16, 4096, 2048, 3, 8),    # more producer splits than consumer splits
+    ("swiglu", 16, 8192, 2752, 4, 6),  # LLaMA shard: gate and up, a ragged consumer K
+    ("gelu", 200, 2048, 1024, 2, 4),   # two row blocks, row-per-thread reductions
+])
+def test_k_range_major_consumers_and_first_stage_splits(kind, M, H, F, split, first):
+    """raster 3 lists a split consumer stage K-split by K-split, and
+    split_k_first gives the producers their own split count: every consumer
+    still waits for exactly the producer tiles of its K range (delayed
+    producers, the intermediate poisoned before each forward), the output
+    matches the oracle, and the order changes no bit (raster 1, same splits)."""
+    inp = cs_inputs.make_custom(kind, M, H, F, seed=56)
+    dev = device_tensors(inp, "nk")
+    outs = {}
+    for raster in (1, 3):
+        with plan_for(inp, "tile", "nk", split_k=split, split_k_first=first, raster=raster) as plan:
+            q = cs.cs_chain_query(plan)
+            assert q["raster"] == raster and q["split_k"][:2] == [first, split]
+            outs[raster] = poisoned_forward(plan, dev).cpu()
+            if raster == 3:
+                for seed in range(2):
+                    g = torch.Generator().manual_seed(400 + seed)
+                    delays = (torch.rand(q["units"][0], generator=g) * 100_000).long().tolist()
+                    cs.cs_chain_debug_set_delays(plan, 0, delays)
+                    assert torch.equal(poisoned_forward(plan, dev).cpu(), outs[3]), seed
+    Yref, _ = _oracle(inp)
+    assert oracle.rel_err(outs[3], Yref) <= TOL
+    assert torch.equal(outs[1], outs[3])
+
+
 @pytest.mark.parametrize("policy", ["tile", "stream"])
 def test_back_to_back_forwards_with_programmatic_launch(policy):
     """Forwards queued back to back (each one's output is the next one's input,

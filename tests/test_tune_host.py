@@ -88,8 +88,8 @@ def test_policy_rules(cs, table):
 
 def test_fields_set_by_the_caller_are_kept(cs, table):
     table([E(512, 256, 256, split_k=3, policy="row", us=1.0)])
-    # any of the four tile fields given: the table does not touch them
-    for field, value in [("tile_m", 128), ("tile_n", 128), ("split_k", 1), ("group_m", 2)]:
+    # any of the five tile fields given: the table does not touch them
+    for field, value in [("tile_m", 128), ("tile_n", 128), ("split_k", 1), ("split_k_first", 2), ("group_m", 2)]:
         e, r = cs.cs_tune_match(gpt3(cs, 512, policy="row", **{field: value}), 152)
         assert e == -1 and getattr(r, field) == value
     # ... but an auto policy is still resolved from it
@@ -108,6 +108,21 @@ def test_entry_the_desc_rejects_is_ignored(cs, table):
     e, r = cs.cs_tune_match(d, 152)
     assert e == -1 and r.tile_m == 0 and r.policy == cs.CS_SYNC_TILE
     assert cs.cs_last_error_string() == ""  or "attention" not in cs.cs_last_error_string()
+
+
+def test_first_stage_splits_and_order_come_from_the_entry(cs, table):
+    """split_k_first and raster are optional keys: applied with the tile fields,
+    the order only where the desc leaves it on auto."""
+    table([E(1, split_k=6, split_k_first=8, raster=3, us=1.0), E(16, split_k=3, us=1.0)])
+    e, r = cs.cs_tune_match(gpt3(cs, 1), 152)
+    assert e == 0 and (r.split_k, r.split_k_first, r.raster) == (6, 8, 3)
+    q = cs.cs_chain_plan_info(gpt3(cs, 1), 152)
+    assert q["split_k"][:2] == [8, 6] and q["raster"] == 3
+    e, r = cs.cs_tune_match(gpt3(cs, 1, raster=2), 152)
+    assert e == 0 and r.raster == 2 and r.split_k_first == 8
+    e, r = cs.cs_tune_match(gpt3(cs, 16), 152)   # keys absent: defaults
+    assert e == 1 and (r.split_k, r.split_k_first, r.raster) == (3, 0, 0)
+    assert cs.cs_chain_plan_info(gpt3(cs, 16), 152)["raster"] == 1
 
 
 def test_schedule_follows_the_tuned_tiles(cs, table):
@@ -143,7 +158,8 @@ def test_malformed_files_are_rejected_and_keep_the_table(cs, table, tmp_path, te
 
 @pytest.mark.parametrize("field,value", [("tile_m", 384), ("tile_n", 64), ("split_k", 16), ("M", 0),
                                          ("H", 12.5), ("kind", "conv"), ("dtype", "f32"), ("policy", "none"),
-                                         ("layout", "mk"), ("us", -1), ("group_m", -1), ("sms", "152")])
+                                         ("layout", "mk"), ("us", -1), ("group_m", -1), ("sms", "152"),
+                                         ("split_k_first", 16), ("raster", 4), ("raster", -1)])
 def test_bad_entries_name_their_field(cs, table, field, value):
     bad = E(128)
     bad[field] = value

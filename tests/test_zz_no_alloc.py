@@ -61,14 +61,16 @@ def test_noalloc_matches_planned_forward_twice(kind, M, H, F, layout, policy):
 
 
 def test_noalloc_refuses_k_splits():
-    """The array holds no split-K workspace: split_k > 1 is refused, not ignored."""
+    """The array holds no split-K workspace: split_k > 1 or split_k_first > 1
+    is refused, not ignored."""
     inp = cs_inputs.make_custom("gelu", 64, 256, 512, dtype=torch.float16, seed=42)
     dev = device_tensors(inp, "nk")
-    desc = _desc(inp, "nk", "tile")
-    desc.split_k = 2
-    with pytest.raises(cs.CSError) as e:
-        cs.cs_mlp_forward_noalloc(desc, Y=torch.empty_like(dev["X"]), **dev)
-    assert e.value.status == cs.CS_ERR_UNSUPPORTED
+    for field in ("split_k", "split_k_first"):
+        desc = _desc(inp, "nk", "tile")
+        setattr(desc, field, 2)
+        with pytest.raises(cs.CSError) as e:
+            cs.cs_mlp_forward_noalloc(desc, Y=torch.empty_like(dev["X"]), **dev)
+        assert e.value.status == cs.CS_ERR_UNSUPPORTED and field in str(e.value)
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
