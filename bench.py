@@ -605,11 +605,7 @@ def main():
     traffic_key = f"{args.workload}_M{M}_{args.policy}_{lay}"
     roof.update({"traffic": measured_traffic(traffic_key, schedule_sha(cs, plan.desc, plan_info["num_sms"])),
                  "peak_source": f"{peak_src} ({'sustained' if sustained else 'burst'})",
-                 "kernel": (f"cs_chain_kernel<6,32768,{plan_info['tile_m'] // 128},1> (attention)" if kind == "attn" else
-                            "cs_chain_kernel<6,32768,2,0,4> (4-CTA clusters)" if plan_info["tile_m"] == 512 else
-                            "cs_chain_kernel<6,32768,2>" if plan_info["tile_m"] == 256 else
-                            "cs_chain_kernel<4,49152,1>" if (kind == "swiglu" or 256 in plan_info["tile_n"])
-                            else "cs_chain_kernel<6,32768,1>"),
+                 "kernel": kernel_label(kind, M, plan_info),
                  "algorithmic_flops_per_launch": flops if launches_per_step == 1 else None,
                  "algorithmic_bytes_per_launch": nbytes if launches_per_step == 1 else None,
                  "launch_ms": ms_launch, "roofline_time_ms": t_roof_ms})
@@ -932,10 +928,27 @@ def stream_k_remainder(q):
     return rem if rem <= q["sched_units"][last] else 0
 
 
+def kernel_label(kind, M, q):
+    """The instantiation a plan launches (the library's configuration rules:
+    up to 8 rows on single SMs, 11 stages of 17 KB or, with 256-wide B, 5 of
+    33 KB; 256-wide B otherwise 4 stages of 48 KB; else 6 of 32 KB)."""
+    wide_b = kind == "swiglu" or 256 in q["tile_n"][: q["stages"]]
+    if kind == "attn":
+        return f"cs_chain_kernel<6,32768,{q['tile_m'] // 128},1> (attention)"
+    if q["tile_m"] == 512:
+        return "cs_chain_kernel<6,32768,2,0,4> (4-CTA clusters)"
+    if q["tile_m"] == 256:
+        return "cs_chain_kernel<6,32768,2>"
+    if M <= 8:
+        return "cs_chain_kernel<5,33792,1,0,1,8>" if wide_b else "cs_chain_kernel<11,17408,1,0,1,8>"
+    return "cs_chain_kernel<4,49152,1>" if wide_b else "cs_chain_kernel<6,32768,1>"
+
+
 def plan_record(q):
     """Tile shape, K-splits, unit order and tuning entry of a plan, for the sweep records."""
     return {"tile_m": q["tile_m"], "tile_n": q["tile_n"][q["stages"] - 1], "split_k": max(q["split_k"]),
-            "splits": q["split_k"][: q["stages"]], "raster": q["raster"], "tuned_entry": q["tuned_entry"]}
+            "splits": q["split_k"][: q["stages"]], "raster": q["raster"], "sk_tiles": q["sk_tiles"],
+            "tuned_entry": q["tuned_entry"]}
 
 
 def _roof_frac(fl, by, us, peaks):
