@@ -402,6 +402,29 @@ def test_k_range_major_consumers_and_first_stage_splits(kind, M, H, F, split, fi
     assert torch.equal(outs[1], outs[3])
 
 
+@pytest.mark.parametrize("layout", ["nk", "kn"])
+@pytest.mark.parametrize("policy", ["row", "strided", "stream"])
+def test_k_range_order_under_every_policy(policy, layout):
+    """The K-range order is a dispatch order only: under RowSync, Strided and the
+    two-kernel control, in both weight layouts, with the output release on,
+    it gives raster 1's bits and the oracle's values, and every Y tile and row
+    block is released once per forward."""
+    inp = cs_inputs.make_custom("swiglu", 24, 4096, 2048, dtype=torch.bfloat16, seed=58)
+    dev = device_tensors(inp, layout)
+    outs = {}
+    for raster in (1, 3):
+        with plan_for(inp, policy, layout, split_k=3, split_k_first=5, raster=raster, out_release=1) as plan:
+            q = cs.cs_chain_query(plan)
+            assert q["raster"] == raster and q["split_k"][:2] == [5, 3]
+            outs[raster] = poisoned_forward(plan, dev).cpu()
+            assert torch.equal(poisoned_forward(plan, dev).cpu(), outs[raster])
+            tiles, rows, epoch = cs.cs_chain_debug_read_sems(plan, 1)  # the output's counters
+            assert epoch == 2 and all(v == 2 for r in tiles for v in r)
+    Yref, _ = _oracle(inp)
+    assert oracle.rel_err(outs[3], Yref) <= TOL
+    assert torch.equal(outs[1], outs[3])
+
+
 @pytest.mark.parametrize("policy", ["tile", "stream"])
 def test_back_to_back_forwards_with_programmatic_launch(policy):
     """Forwards queued back to back (each one's output is the next one's input,
