@@ -141,6 +141,21 @@ def stream_k_candidates(info):
     return out
 
 
+def k_range_combos(sp):
+    """(split_k, split_k_first) pairs timed with the K-range order (raster 3) on
+    a tile shape whose fastest split count is sp: uniform splits (0: the
+    automatic rule) and more splits for the first stage, each pair once."""
+    combos = [(s, 0) for s in (0, sp, 4, 6, 8)] + [(sp, f) for f in (2 * sp, 6, 8, 12) if f != sp]
+    return list(dict.fromkeys(combos))
+
+
+def plan_key(info):
+    """What makes two plans the same candidate: the tile shape of every stage
+    and the K-splits of every stage (tile_m alone does not tell 128 x 128 from
+    128 x 256 tiles)."""
+    return (info["tile_m"], tuple(info["tile_n"]), tuple(info["split_k"]))
+
+
 def _forward(plan, kind, t, Y):
     if kind == "attn":
         return lambda: cs.cs_attn_chain_forward(plan, t["X"], t["Wqkv"], t["Wo"], Y)
@@ -252,14 +267,13 @@ def tune_shape(torch, kind, H, F, dtype, heads, Ms, log=print, layout="nk", verb
                     shapes.append(key)
             seen = set()
             for tm, tn, sp, *_ in shapes[:2]:
-                combos = [(s, 0) for s in (0, sp, 4, 6, 8)] + [(sp, f) for f in (2 * sp, 6, 8, 12) if f != sp]
-                for s, f in dict.fromkeys(combos):
+                for s, f in k_range_combos(sp):
                     c = Candidate(kind, shape, base, tm, tn, s, 0, 0, f, 3)
                     try:
                         us, info = run(c)
                     except cs.CSError:
                         continue
-                    real = (info["tile_m"], tuple(info["tile_n"]), tuple(info["split_k"]))
+                    real = plan_key(info)
                     want_first = f or s
                     if real in seen or info["raster"] != 3 or (want_first and info["split_k"][0] != want_first):
                         continue  # clamped onto another candidate, or a repeat

@@ -225,9 +225,26 @@ def test_packaged_table_matches_its_own_entries(cs):
             idx, r = cs.cs_tune_match(d, e["sms"])
             assert idx >= 0, e
             assert (r.tile_m, r.tile_n, r.split_k) == (e["tile_m"], e["tile_n"], e["split_k"]), e
+            assert (r.split_k_first, r.raster) == (e.get("split_k_first", 0), e.get("raster", 0)), e
             assert e["us"] <= e["builtin_us"] * 1.0001
     finally:
         cs.cs_tune_clear()
+
+
+def test_tuner_k_range_candidates(cs):
+    """The K-range phase times each (split, first-stage split) pair once, and
+    tells candidates apart by every stage's tile width and splits: 128 x 128 and
+    128 x 256 tiles with the same splits are two candidates."""
+    from consumer_gemm_chain_gb300 import tune
+    assert tune.k_range_combos(3) == [(0, 0), (3, 0), (4, 0), (6, 0), (8, 0), (3, 6), (3, 8), (3, 12)]
+    c6 = tune.k_range_combos(6)
+    assert len(c6) == len(set(c6)) and (6, 12) in c6 and (6, 6) not in c6
+    keys = set()
+    for tn in (128, 256):
+        d = cs.cs_chain_desc_init(kind="gelu", M=1, H=12288, F=6144, tile_m=128, tile_n=tn, split_k=6, raster=3,
+                                  tuned=-1)
+        keys.add(tune.plan_key(cs.cs_chain_plan_info(d, 152)))
+    assert len(keys) == 2
 
 
 def test_tuner_shapes_of_ones_own():
