@@ -144,8 +144,11 @@ def stream_k_candidates(info):
 def k_range_combos(sp):
     """(split_k, split_k_first) pairs timed with the K-range order (raster 3) on
     a tile shape whose fastest split count is sp: uniform splits (0: the
-    automatic rule) and more splits for the first stage, each pair once."""
+    automatic rule), more splits for the first stage, and the first stage's
+    splits with unsplit later stages (no reduction there; measured faster for
+    the attention chain's short Wo GEMM at up to 16 rows), each pair once."""
     combos = [(s, 0) for s in (0, sp, 4, 6, 8)] + [(sp, f) for f in (2 * sp, 6, 8, 12) if f != sp]
+    combos += [(1, f) for f in (sp, 2 * sp) if sp > 1]
     return list(dict.fromkeys(combos))
 
 

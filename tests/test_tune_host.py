@@ -236,7 +236,7 @@ def test_tuner_k_range_candidates(cs):
     tells candidates apart by every stage's tile width and splits: 128 x 128 and
     128 x 256 tiles with the same splits are two candidates."""
     from consumer_gemm_chain_gb300 import tune
-    assert tune.k_range_combos(3) == [(0, 0), (3, 0), (4, 0), (6, 0), (8, 0), (3, 6), (3, 8), (3, 12)]
+    assert tune.k_range_combos(3) == [(0, 0), (3, 0), (4, 0), (6, 0), (8, 0), (3, 6), (3, 8), (3, 12), (1, 3), (1, 6)]
     c6 = tune.k_range_combos(6)
     assert len(c6) == len(set(c6)) and (6, 12) in c6 and (6, 6) not in c6
     keys = set()
