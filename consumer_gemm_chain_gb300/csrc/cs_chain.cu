@@ -236,11 +236,11 @@ cs_status validate(const cs_chain_desc* d) {
   if (d->num_sms < 0) return fail(CS_ERR_INVALID_ARG, "num_sms=%d", d->num_sms);
   if (d->lag < -1) return fail(CS_ERR_INVALID_ARG, "lag=%d", d->lag);
   if (d->group_m < 0) return fail(CS_ERR_INVALID_ARG, "group_m=%d", d->group_m);
-  if (d->tile_n != 0 && d->tile_n != 128 && d->tile_n != 256)
-    return fail(CS_ERR_INVALID_ARG, "tile_n=%d (0, 128 or 256)", d->tile_n);
+  if (d->tile_n != 0 && d->tile_n != 64 && d->tile_n != 128 && d->tile_n != 256)
+    return fail(CS_ERR_INVALID_ARG, "tile_n=%d (0, 64, 128 or 256)", d->tile_n);
   if (d->tile_m != 0 && d->tile_m != 128 && d->tile_m != 256 && d->tile_m != 512)
     return fail(CS_ERR_INVALID_ARG, "tile_m=%d (0, 128, 256 or 512)", d->tile_m);
-  if (d->tile_m >= 256 && d->tile_n == 128)
+  if (d->tile_m >= 256 && (d->tile_n == 64 || d->tile_n == 128))
     return fail(CS_ERR_UNSUPPORTED, "tile_m=%d is built for 256-wide tiles only", d->tile_m);
   if (d->tile_m == 512 && !kClusterMulticast)
     return fail(CS_ERR_UNSUPPORTED, "tile_m=512 needs cluster multicast, which the replica build leaves out");
@@ -250,7 +250,8 @@ cs_status validate(const cs_chain_desc* d) {
       return fail(CS_ERR_INVALID_ARG, "ATTN needs F == heads*head_dim (F=%d heads=%d)", d->F, d->heads);
     // 128 x 128 tiles on single SMs, or 256 x 256 on CTA pairs (whose attention
     // units then take two query blocks)
-    if (d->tile_m == 512 || (d->tile_m == 128 && d->tile_n == 256) || (d->tile_m == 256 && d->tile_n == 128))
+    if (d->tile_m == 512 || d->tile_n == 64 || (d->tile_m == 128 && d->tile_n == 256) ||
+        (d->tile_m == 256 && d->tile_n == 128))
       return fail(CS_ERR_UNSUPPORTED, "the attention chain runs 128 x 128 or 256 x 256 (pair) tiles only");
   }
   return CS_OK;

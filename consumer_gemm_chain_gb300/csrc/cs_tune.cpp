@@ -277,7 +277,7 @@ bool read_entry(const JVal& o, TuneEntry& e, std::string& err) {
       !int_field(o, "sk_units", 0, 16383, false, &e.sk_units, err))
     return false;
   if (e.tile_m != 0 && e.tile_m != 128 && e.tile_m != 256 && e.tile_m != 512) return err = "bad \"tile_m\"", false;
-  if (e.tile_n != 0 && e.tile_n != 128 && e.tile_n != 256) return err = "bad \"tile_n\"", false;
+  if (e.tile_n != 0 && e.tile_n != 64 && e.tile_n != 128 && e.tile_n != 256) return err = "bad \"tile_n\"", false;
   if (const JVal* us = o.get("us")) {
     if (us->kind != JVal::Num || !(us->num > 0.0)) return err = "\"us\" must be a positive number", false;
     e.us = us->num;

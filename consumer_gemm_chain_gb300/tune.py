@@ -39,7 +39,7 @@ PRESETS = {
     "attn": ("attn", 12288, 1536, "f16", 12, (1, 16, 64, 256, 512, 1024, 2048)),
     "stress": ("gelu", 8192, 8192, "f16", 0, tuple(128 * b for b in range(1, 13))),
 }
-MLP_TILES = ((128, 128), (128, 256), (256, 256), (512, 256))
+MLP_TILES = ((128, 64), (128, 128), (128, 256), (256, 256), (512, 256))
 ATTN_TILES = ((128, 128), (256, 256))
 POLICIES = ("tile", "row", "strided", "stream")
 ROUNDS = 5      # interleaved rounds of the final comparison

@@ -116,8 +116,11 @@ typedef struct cs_chain_desc {
                           weights in L2); 0 = auto (at most 1024 rows per group;
                           with 256-row pair tiles at least two groups; GeLU chains
                           on 512-row tiles from three tile rows: up to 2048 rows)   */
-  int tile_n;          /* output columns per GEMM tile: 128 or 256; 0 = auto.
-                          SwiGLU producer tiles are always 128 (gate|up = 256).     */
+  int tile_n;          /* output columns per GEMM tile: 64, 128 or 256; 0 = auto
+                          (never 64).  SwiGLU producer tiles are always 128
+                          (gate|up = 256).  64 runs on single SMs only (tile_m
+                          128, MLP chains): twice the tiles of 128 for a stage
+                          with fewer tiles than SMs, without K-splits.            */
   int tile_m;          /* rows per GEMM tile: 128 (one SM), 256 (a 2-SM cluster
                           sharing one tcgen05 MMA) or 512 (two such pairs in a 4-CTA
                           cluster that fetch every weight box once and multicast it
@@ -387,7 +390,7 @@ cs_status cs_schedule_build(const cs_chain_desc* desc, int num_sms, uint32_t* un
  *   {"format": "cs_chain_tuning", "version": 1, "entries": [ENTRY, ...], ...}
  *   ENTRY = {"kind": "gelu"|"swiglu"|"attn", "dtype": "f16"|"bf16", "H": int,
  *            "F": int, "M": int, "sms": int (grid the entry was measured on),
- *            "tile_m": 0|128|256|512, "tile_n": 0|128|256, "split_k": 0..15,
+ *            "tile_m": 0|128|256|512, "tile_n": 0|64|128|256, "split_k": 0..15,
  *            optional "group_m": int >= 0 (default 0 = auto),
  *            optional "split_k_first": 0..15 (default 0 = as split_k),
  *            optional "raster": 0..3 (applied when the desc leaves raster on 0;

@@ -78,7 +78,7 @@ def _check_order(dec, deps_of):
             assert pos[dep] < i, f"unit {u} at {i} precedes its producer {dep}"
 
 
-@pytest.mark.parametrize("tile_m,tile_n", [(128, 128), (128, 256), (256, 256), (512, 256)])
+@pytest.mark.parametrize("tile_m,tile_n", [(128, 64), (128, 128), (128, 256), (256, 256), (512, 256)])
 @pytest.mark.parametrize("M,H,F,sms,lag,group,split", [(64, 256, 1024, 148, -1, 0, 1), (2048, 12288, 6144, 148, -1, 0, 1),
                                                        (2048, 12288, 6144, 152, 0, 3, 1), (1, 12288, 6144, 148, -1, 0, 3),
                                                        (1000, 8192, 2752, 148, 2, 1, 2), (1536, 8192, 8192, 148, 5, 5, 1)])
@@ -161,6 +161,28 @@ def test_split_k_first_sets_the_first_stage_only(cs, kind, M, H, F, split, first
     units = [cs.decode_unit(u) for u in cs.cs_schedule_build(d, 152)]
     assert {k for s, _, _, k in units if s == 0} == set(range(first))
     assert q["sched_units"][0] == q["n_tiles"][0] * -(-M // 128) * first
+
+
+def test_64_wide_tiles_on_single_sms_only(cs):
+    """tile_n = 64: single-SM MLP tiles (twice the tiles of 128, the SwiGLU
+    producer keeping its 128-wide gate|up tiles); refused for pairs, clusters
+    and the attention chain, and never chosen automatically."""
+    for kind, F, n0 in (("gelu", 6144, 96), ("swiglu", 2752, 22)):
+        d = cs.cs_chain_desc_init(kind=kind, M=64, H=8192, F=F, tile_m=128, tile_n=64, tuned=-1)
+        q = cs.cs_chain_plan_info(d, 152)
+        assert q["tile_n"][:2] == [64 if kind == "gelu" else 128, 64] and q["n_tiles"][:2] == [n0, 128]
+    for tm in (256, 512):
+        with pytest.raises(cs.CSError) as e:
+            cs.cs_schedule_build(cs.cs_chain_desc_init(M=1024, H=8192, F=8192, tile_m=tm, tile_n=64), 152)
+        assert e.value.status == cs.CS_ERR_UNSUPPORTED
+    with pytest.raises(cs.CSError) as e:
+        cs.cs_schedule_build(cs.cs_chain_desc_init(kind="attn", M=64, H=1024, F=512, heads=4, head_dim=128,
+                                                   tile_m=128, tile_n=64), 152)
+    assert e.value.status == cs.CS_ERR_UNSUPPORTED
+    for M in (1, 64, 1024, 8192):
+        for kind in ("gelu", "swiglu"):
+            q = cs.cs_chain_plan_info(cs.cs_chain_desc_init(kind=kind, M=M, H=8192, F=2752, tuned=-1), 152)
+            assert 64 not in q["tile_n"]
 
 
 def test_attention_desc_validation(cs):

@@ -403,6 +403,37 @@ def test_k_range_major_consumers_and_first_stage_splits(kind, M, H, F, split, fi
 
 
 @pytest.mark.parametrize("layout", ["nk", "kn"])
+@pytest.mark.parametrize("kind,M,H,F,split,policy", [
+    ("gelu", 1, 2048, 1024, 3, "tile"),     # up to 8 rows: the 17 KB-stage kernel, K-splits
+    ("gelu", 100, 2048, 1152, 1, "tile"),   # ragged rows, unsplit
+    ("gelu", 300, 1024, 640, 2, "row"),     # three row blocks, K-splits, RowSync
+    ("gelu", 300, 1024, 640, 1, "strided"),
+    ("gelu", 130, 1024, 640, 2, "stream"),  # the two-kernel control
+    ("swiglu", 64, 2048, 688, 3, "tile"),   # 128-wide gate|up producer, 64-wide consumer tiles
+])
+def test_64_wide_tiles(kind, M, H, F, split, policy, layout):
+    """64-column tiles on single SMs: the output matches the oracle and the
+    128-wide tiles' (the same K order per element) to fp16 rounding, and
+    delayed producers over a poisoned intermediate change no bit."""
+    inp = cs_inputs.make_custom(kind, M, H, F, dtype=torch.bfloat16 if kind == "swiglu" else torch.float16, seed=59)
+    dev = device_tensors(inp, layout)
+    outs = {}
+    for tn in (64, 128):
+        with plan_for(inp, policy, layout, tile_m=128, tile_n=tn, split_k=split) as plan:
+            q = cs.cs_chain_query(plan)
+            assert q["tile_n"][1] == tn and q["tile_n"][0] == (128 if kind == "swiglu" else tn)
+            outs[tn] = poisoned_forward(plan, dev).cpu()
+            if tn == 64:
+                g = torch.Generator().manual_seed(420)
+                delays = (torch.rand(q["units"][0], generator=g) * 100_000).long().tolist()
+                cs.cs_chain_debug_set_delays(plan, 0, delays)
+                assert torch.equal(poisoned_forward(plan, dev).cpu(), outs[64])
+    Yref, _ = _oracle(inp)
+    assert oracle.rel_err(outs[64], Yref) <= TOL
+    assert oracle.rel_err(outs[64], outs[128]) <= 1e-3
+
+
+@pytest.mark.parametrize("layout", ["nk", "kn"])
 @pytest.mark.parametrize("policy", ["row", "strided", "stream"])
 def test_k_range_order_under_every_policy(policy, layout):
     """The K-range order is a dispatch order only: under RowSync, Strided and the

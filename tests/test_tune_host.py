@@ -156,7 +156,7 @@ def test_malformed_files_are_rejected_and_keep_the_table(cs, table, tmp_path, te
     assert cs.cs_tune_size() == 1
 
 
-@pytest.mark.parametrize("field,value", [("tile_m", 384), ("tile_n", 64), ("split_k", 16), ("M", 0),
+@pytest.mark.parametrize("field,value", [("tile_m", 384), ("tile_n", 32), ("split_k", 16), ("M", 0),
                                          ("H", 12.5), ("kind", "conv"), ("dtype", "f32"), ("policy", "none"),
                                          ("layout", "mk"), ("us", -1), ("group_m", -1), ("sms", "152"),
                                          ("split_k_first", 16), ("raster", 4), ("raster", -1)])
