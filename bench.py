@@ -931,7 +931,8 @@ def stream_k_remainder(q):
 def kernel_label(kind, M, q):
     """The instantiation a plan launches (the library's configuration rules:
     up to 8 rows on single SMs, 11 stages of 17 KB or, with 256-wide B, 5 of
-    33 KB; 256-wide B otherwise 4 stages of 48 KB; else 6 of 32 KB)."""
+    33 KB; up to 32 rows 9 of 20 KB or 5 of 36 KB; 256-wide B otherwise 4
+    stages of 48 KB; else 6 of 32 KB)."""
     wide_b = kind == "swiglu" or 256 in q["tile_n"][: q["stages"]]
     if kind == "attn":
         return f"cs_chain_kernel<6,32768,{q['tile_m'] // 128},1> (attention)"
@@ -941,6 +942,8 @@ def kernel_label(kind, M, q):
         return "cs_chain_kernel<6,32768,2>"
     if M <= 8:
         return "cs_chain_kernel<5,33792,1,0,1,8>" if wide_b else "cs_chain_kernel<11,17408,1,0,1,8>"
+    if M <= 32:
+        return "cs_chain_kernel<5,36864,1,0,1,32>" if wide_b else "cs_chain_kernel<9,20480,1,0,1,32>"
     return "cs_chain_kernel<4,49152,1>" if wide_b else "cs_chain_kernel<6,32768,1>"
 
 

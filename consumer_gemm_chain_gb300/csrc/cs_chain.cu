@@ -56,6 +56,10 @@ constexpr int NS_B = 4, SB_B = cs::TILE_A_BYTES + 2 * 128 * cs::BK * 2;  // 48 K
 // up to 8 rows: 8-row A tiles (1 KB) leave room for deeper rings of weights
 constexpr int NS_S = 11, SB_S = 8 * cs::BK * 2 + 128 * cs::BK * 2;      // 17 KB stages
 constexpr int NS_T = 5, SB_T = 8 * cs::BK * 2 + 2 * 128 * cs::BK * 2;   // 33 KB stages
+// 9 to 32 rows: 32-row A tiles (4 KB), 9 stages of 128 weight rows (144 KB in
+// flight against 96 KB with 128-row A tiles) or 5 of 256
+constexpr int NS_U = 9, SB_U = 32 * cs::BK * 2 + 128 * cs::BK * 2;      // 20 KB stages
+constexpr int NS_V = 5, SB_V = 32 * cs::BK * 2 + 2 * 128 * cs::BK * 2;  // 36 KB stages
 
 template <int NS, int SB>
 constexpr int smem_bytes_for() {
@@ -63,7 +67,8 @@ constexpr int smem_bytes_for() {
 }
 // every configuration fits the 227 KB a CTA may use
 static_assert(smem_bytes_for<NS_A, SB_A>() <= 232448 && smem_bytes_for<NS_B, SB_B>() <= 232448 &&
-                  smem_bytes_for<NS_S, SB_S>() <= 232448 && smem_bytes_for<NS_T, SB_T>() <= 232448,
+                  smem_bytes_for<NS_S, SB_S>() <= 232448 && smem_bytes_for<NS_T, SB_T>() <= 232448 &&
+                  smem_bytes_for<NS_U, SB_U>() <= 232448 && smem_bytes_for<NS_V, SB_V>() <= 232448,
               "shared memory");
 
 struct MapSlot {
@@ -97,7 +102,10 @@ struct cs_chain_s {
   int stride = 1;
   int bn[3] = {128, 128, 128};
   int cfg_b = 0;  // 1: 48 KB-stage kernel (256-wide one-SM tiles or gate|up)
-  int cfg_s = 0;  // up to 8 rows: 1 = 11 x 17 KB stages (128-wide B), 2 = 5 x 33 KB (256 rows of B)
+  int cfg_s = 0;  // up to 8 rows: 1 = 11 x 17 KB stages (128-wide B), 2 = 5 x 33 KB (256 rows of B);
+                  // 9 to 32 rows: 3 = 9 x 20 KB, 4 = 5 x 36 KB (measured: GPT-3 M=32
+                  // 66.3 -> 63.7 us, stress M=32 73.7 -> 70.3; 64-row A tiles with 7 x 24 KB
+                  // stages for 33 to 64 rows changed nothing)
   // cs_mlp_forward_host: double-buffered device X / Y, copy streams and events
   void* host_x[2] = {nullptr, nullptr};
   void* host_y[2] = {nullptr, nullptr};
@@ -521,10 +529,12 @@ void shape_plan(cs_chain_s* p, const Geometry& g, int kind, int M) {
   p->kv = g.kv;
   p->kv_max = g.kv_max;
   const bool wide_b = kind == CS_CHAIN_MLP_SWIGLU || g.bn[0] == 256 || g.bn[1] == 256 || g.bn[2] == 256;
-  p->cfg_s = (g.cg == 1 && kind != CS_CHAIN_ATTN && M <= 8) ? (wide_b ? 2 : 1) : 0;
+  p->cfg_s = (g.cg == 1 && kind != CS_CHAIN_ATTN && M <= 32) ? (M <= 8 ? 1 : 3) + (wide_b ? 1 : 0) : 0;
   p->cfg_b = g.cg == 1 && !p->cfg_s && wide_b;
   p->smem = p->cfg_s == 1 ? smem_bytes_for<NS_S, SB_S>()
             : p->cfg_s == 2 ? smem_bytes_for<NS_T, SB_T>()
+            : p->cfg_s == 3 ? smem_bytes_for<NS_U, SB_U>()
+            : p->cfg_s == 4 ? smem_bytes_for<NS_V, SB_V>()
             : p->cfg_b      ? smem_bytes_for<NS_B, SB_B>()
                             : smem_bytes_for<NS_A, SB_A>();
   p->num_sms = p->num_sms / g.cl * g.cl;
@@ -781,10 +791,16 @@ cs_status kernel_for(const cs_chain_s* p, const void** fn) {
   if (p->cg == 2) CS_KERNEL(NS_A, SB_A, 2, false);
   if (p->cfg_s == 1) CS_KERNEL(NS_S, SB_S, 1, false, 1, 8);
   if (p->cfg_s == 2) CS_KERNEL(NS_T, SB_T, 1, false, 1, 8);
+  if (p->cfg_s == 3) CS_KERNEL(NS_U, SB_U, 1, false, 1, 32);
+  if (p->cfg_s == 4) CS_KERNEL(NS_V, SB_V, 1, false, 1, 32);
   if (p->cfg_b) CS_KERNEL(NS_B, SB_B, 1, false);
   CS_KERNEL(NS_A, SB_A, 1, false);
 #undef CS_KERNEL
 }
+
+// Rows of the A operand per pipeline stage (and of the activation load boxes):
+// 8 up to 8 rows, 32 up to 32, else the full 128-row block.
+int a_rows(const cs_chain_s* p) { return p->cfg_s == 1 || p->cfg_s == 2 ? 8 : p->cfg_s ? 32 : cs::BM; }
 
 // Threads per CTA: the attention instantiations run two epilogue warps per TMEM
 // lane quadrant.
@@ -987,7 +1003,7 @@ cs_status bind_mlp(cs_chain_s* p, const cs_mlp_args* a) {
   if (!swiglu && reinterpret_cast<uintptr_t>(a->b1) % 16 != 0) return fail(CS_ERR_INVALID_ARG, "b1 is not 16-byte aligned");
   const int M = p->d.M, H = p->d.H, F = p->d.F;
   cs_status s;
-  if ((s = encode_act(p, MAP_X, a->X, M, H, false, p->cfg_s ? 8 : 128)) != CS_OK) return s;
+  if ((s = encode_act(p, MAP_X, a->X, M, H, false, a_rows(p))) != CS_OK) return s;
   // [N, K] weights: a box holds the B columns one CTA fetches (with 4-CTA
   // clusters, half of its pair share; the other half comes by multicast).  A
   // gate|up pair gives each CTA all bn rows of one of the two operands.
@@ -1157,7 +1173,7 @@ cs_status cs_chain_plan(const cs_chain_desc* desc, cs_chain_t* out) {
     n_owned = 5;
   } else {
     if ((s = encode_act(p, MAP_HST, p->inter[0], desc->M, desc->F, true)) != CS_OK) return bail(s);
-    if ((s = encode_act(p, MAP_HLD, p->inter[0], desc->M, desc->F, false, p->cfg_s ? 8 : 128)) != CS_OK)
+    if ((s = encode_act(p, MAP_HLD, p->inter[0], desc->M, desc->F, false, a_rows(p))) != CS_OK)
       return bail(s);
     owned[0] = MAP_HST, owned[1] = MAP_HLD;
     n_owned = 2;
@@ -1633,7 +1649,7 @@ cs_status cs_mlp_forward_noalloc(const cs_chain_desc* desc, const cs_mlp_args* a
 
   // Tensor maps of the intermediate (in the array) and of the caller's tensors.
   if ((s = encode_act(&p, MAP_HST, p.inter[0], desc->M, desc->F, true)) != CS_OK) return s;
-  if ((s = encode_act(&p, MAP_HLD, p.inter[0], desc->M, desc->F, false, p.cfg_s ? 8 : 128)) != CS_OK) return s;
+  if ((s = encode_act(&p, MAP_HLD, p.inter[0], desc->M, desc->F, false, a_rows(&p))) != CS_OK) return s;
   for (int i = 0; i < kMaxMaps; ++i)
     if (i != MAP_HST && i != MAP_HLD) std::memcpy(&p.maps[i], &p.maps[MAP_HLD], sizeof(CUtensorMap));
   if ((s = bind_mlp(&p, args)) != CS_OK) return s;

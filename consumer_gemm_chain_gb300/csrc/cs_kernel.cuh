@@ -30,7 +30,8 @@
 // leader's TMEM and rows 128-255 in the peer's; commits are multicast to both.
 // CL = 4: two such pairs on consecutive 256-row blocks form a 4-CTA cluster
 // and share every weight box by TMA multicast.  Attention on pairs runs two
-// query blocks per unit.  AR = 8: up to 8 rows, one 8-row A group per stage.
+// query blocks per unit.  AR = 8: up to 8 rows, one 8-row A group per stage;
+// AR = 32: up to 32 rows, four groups.
 // Semaphores stay per 128-row block, so each CTA of a consumer cluster waits
 // only for the producer rows it reads.
 // Every wait is bounded: semaphore polls by the plan's timeout (error word +
@@ -385,9 +386,10 @@ __device__ __noinline__ int tma_wait_slices(SmemCtl<NS>* sc, uint32_t q, int kb,
 // on consecutive 256-row blocks of the same column tile: each weight box is
 // fetched once and multicast to the CTA holding the same B columns in the
 // other pair).
-// AR: A rows held in shared memory per stage: 128, or 8 for up to 8 valid rows
+// AR: A rows held in shared memory per stage: 128, 8 for up to 8 valid rows
 // (the MMA then reads the one 8-row group for every 8-row group of its 128
-// rows, and the rows past the valid ones are never stored).
+// rows) or 32 for up to 32 (its rows 32-127 read the stage's B operand); the
+// accumulator rows past the valid ones are never stored.
 template <int NS, int STAGE_BYTES, int CG, int CL, int AR>
 __device__ bool tma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, RingPos& rp, uint32_t unit,
                               uint32_t q, uint32_t rank) {
@@ -509,7 +511,9 @@ __device__ bool mma_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* ring, 
     tc_fence_after();
     const uint32_t sa = smem_u32(ring + rp.slot * STAGE_BYTES);
     const uint32_t sb = sa + AR * BK * 2;
-    // AR = 8: stride 0 between 8-row groups, so every group reads the one loaded
+    // AR = 8: stride 0 between 8-row groups, so every group reads the one loaded;
+    // AR = 32: rows 32-127 run on into the stage's B slice (finite values, rows
+    // that are never stored)
     const uint64_t adesc = smem_desc_sw128(sa, 16, AR >= 16 ? 1024 : 0);
     // K-major B: 8-row groups 1024 B apart.  MN-major B: 64-column atoms 8 KB
     // apart (LBO), 8-row K groups 1024 B apart (SBO).
@@ -1570,7 +1574,8 @@ __global__ void __launch_bounds__(Roles<ATTN>::THREADS, 1) cs_chain_kernel(const
 #ifdef CS_NO_CLUSTER_MULTICAST
   static_assert(CL != 4, "the replica build has no 4-CTA multicast tiles");
 #endif
-  static_assert(AR == BM || (AR == 8 && CG == 1 && !ATTN), "8-row A tiles are built for single-SM MLP tiles");
+  static_assert(AR == BM || ((AR == 8 || AR == 32) && CG == 1 && !ATTN),
+                "8- and 32-row A tiles are built for single-SM MLP tiles");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
