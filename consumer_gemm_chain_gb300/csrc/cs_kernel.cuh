@@ -799,13 +799,16 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
   // Partial tiles are stored [mma_n/4][128 rows][4 columns]: the float4 of
   // columns 4c..4c+3 of this thread's row sits at (c * 128 + row), so a warp
   // reads or writes 512 contiguous bytes per access.
+  // the row this thread reduces and stores and the lane quadrant of its store
+  // box: its own, unless the valid rows are shared out below
+  int rrow = row, rq = q;
   auto tile_partial = [&](int ks) {
     if (skj != 0xFFFF)
       return reinterpret_cast<float4*>(
                  S.sk_partial +
-                 (static_cast<size_t>(skj * S.sk_max_nc + ks) * CL + rank) * tile_floats) + row;
+                 (static_cast<size_t>(skj * S.sk_max_nc + ks) * CL + rank) * tile_floats) + rrow;
     return reinterpret_cast<float4*>(S.partial + (static_cast<size_t>(ks * S.m_blocks + mb) * S.n_tiles + n) *
-                                                     tile_floats) + row;
+                                                     tile_floats) + rrow;
   };
   auto release_tmem = [&]() {
     // this warp is done with the accumulator buffer: hand it back to the MMA
@@ -861,15 +864,30 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
                                       lane);
     last_buf = -1;
   }
+  // 49 to 64 valid rows (the last K-split; partial sums come from global memory,
+  // so any warp may take any row): the warps of the two empty lane quadrants
+  // take every other chunk of the valid rows.  The staging buffers then change
+  // hands between warps: every warp's earlier stores must have read them first,
+  // and this unit's stores before the next unit writes them again.
+  const bool rows_pair = NH == 1 && split && !rows_small && rows_valid <= 64;
+  int c_first = half, c_step = NH;
+  if (rows_pair) {
+    rrow = (q & 1) * 32 + lane;
+    rq = q & 1;
+    c_first = q >> 1;
+    c_step = 2;
+    if (lane == 0) tma_store_wait_read<0>();
+    named_bar_sync(1, NE * 32);
+  }
 #pragma unroll 1
-  for (int c = half; c < (rows_small ? 0 : nchunks); c += NH) {
+  for (int c = c_first; c < (rows_small ? 0 : nchunks); c += c_step) {
     float va[64], vu[64];
     if (split) {
 #pragma unroll
       for (int j = 0; j < 64; ++j) va[j] = vu[j] = 0.0f;
       // sum the splits in split order (the same bits whichever split arrived last);
       // loads of one split are issued together, then added
-      for (int ks = 0; ks < nc && row < rows_valid; ++ks) {
+      for (int ks = 0; ks < nc && rrow < rows_valid; ++ks) {
         const float4* src = tile_partial(ks);
         float4 x[16];
 #pragma unroll
@@ -930,18 +948,23 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
         tma_store_wait_read<1>();
     }
     __syncwarp();
-    stage_row(staging, buf, row, w);
+    stage_row(staging, buf, rrow, w);
     fence_proxy_async_shared();
     __syncwarp();
     // boxes that start past the tensor's end are skipped, not clipped
-    const int grow = mb * BM + q * 32;
+    const int grow = mb * BM + rq * 32;
     if (col0 < S.n_extent && grow < S.m_extent) {
       if (lane == 0) {
-        tma_store_2d(&p.maps[S.map_out], staging + buf * (BM * 128) + q * 32 * 128, col0, grow);
+        tma_store_2d(&p.maps[S.map_out], staging + buf * (BM * 128) + rq * 32 * 128, col0, grow);
         tma_store_commit();
       }
       last_buf = buf;
     }
+  }
+  if (rows_pair) {
+    if (lane == 0) tma_store_wait_read<0>();
+    named_bar_sync(1, NE * 32);
+    last_buf = -1;
   }
   if (!split) {
     acc ^= 1u;
