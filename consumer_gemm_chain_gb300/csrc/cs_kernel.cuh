@@ -668,7 +668,7 @@ __device__ __forceinline__ void split_reduce_small(const StageP& S, const float4
   }
 }
 
-// The last K-split of a tile with at most 48 valid rows: cooperative passes
+// The last K-split of a tile with at most 32 valid rows: cooperative passes
 // bring every split of the tile's 64-column parts (as many per pass as the
 // staging buffer holds: all of them up to 32 rows) and, once, the bias on chip;
 // each row thread finishes its rows' chunks and writes them with plain 16-byte
@@ -853,20 +853,21 @@ __device__ bool epi_gemm_unit(const KParams& p, SmemCtl<NS>* sc, uint8_t* stagin
       return true;
     }
   }
-  // at most 48 valid rows (the last split of the tile): cooperative passes
-  // and plain row stores; the loop below is skipped (measured against the
-  // row-per-thread path: LLaMA 33 rows 77 -> 58 us, 48 rows 60 -> 57 us, but
-  // 64 rows 59 -> 62 us)
-  const bool rows_small = split && skj == 0xFFFF && rows_valid <= 48 && S.out_ptr != nullptr;
+  // at most 32 valid rows (the last split of the tile): cooperative passes
+  // and plain row stores; the loop below is skipped (33 to 48 rows also ran
+  // this way until the row-per-thread sums were shared by all four warps,
+  // below: then GPT-3 M=40 71.3 -> 68.5 us, LLaMA M=48 53.0 -> 50.9)
+  const bool rows_small = split && skj == 0xFFFF && rows_valid <= 32 && S.out_ptr != nullptr;
   if (rows_small) {
     const size_t kstride = static_cast<size_t>(S.m_blocks) * S.n_tiles * (tile_floats / 4);
     epi_split_rows_small<NS, NE, ACT>(p, S, sc, staging, tile_partial(0) - row, kstride, rows_valid, mb, n, row,
                                       lane);
     last_buf = -1;
   }
-  // 49 to 64 valid rows (the last K-split; partial sums come from global memory,
+  // 33 to 64 valid rows (the last K-split; partial sums come from global memory,
   // so any warp may take any row): the warps of the two empty lane quadrants
-  // take every other chunk of the valid rows.  The staging buffers then change
+  // take every other chunk of the valid rows (measured: GPT-3 M=64 74.0 ->
+  // 69.2 us, LLaMA M=64 54.3 -> 50.5).  The staging buffers then change
   // hands between warps: every warp's earlier stores must have read them first,
   // and this unit's stores before the next unit writes them again.
   const bool rows_pair = NH == 1 && split && !rows_small && rows_valid <= 64;

@@ -316,22 +316,23 @@ def test_split_k_parity(M, H, F, tile_m, tile_n, split):
     ("gelu", 32, 4096, 512, 7),     # cooperative, 5..8 splits, 32 valid rows
     ("gelu", 1, 2048, 384, 3),      # cooperative, a single row
     ("gelu", 17, 2048, 384, 2),     # cooperative, two splits
-    ("gelu", 40, 8192, 256, 12),    # cooperative over 40 rows, both chunks in one pass
-    ("gelu", 48, 4096, 512, 3),     # cooperative over 48 rows
-    ("gelu", 64, 4096, 512, 3),     # 64 rows: row per thread
+    ("gelu", 40, 8192, 256, 12),    # 40 rows: row per thread, the chunks shared by all four warps
+    ("gelu", 48, 4096, 512, 3),     # 48 rows, shared
+    ("gelu", 64, 4096, 512, 3),     # 64 rows, shared
     ("swiglu", 32, 2048, 256, 3),   # cooperative, gate and up parts
-    ("swiglu", 33, 4096, 344, 6),   # one chunk (gate and up) per pass, ragged F
-    ("swiglu", 48, 2048, 256, 3),   # one chunk per pass, 48 valid rows
-    ("swiglu", 64, 2048, 256, 3),   # 64 rows: row per thread
+    ("swiglu", 33, 4096, 344, 6),   # 33 rows, shared, ragged F
+    ("swiglu", 48, 2048, 256, 3),   # 48 rows, shared
+    ("swiglu", 64, 2048, 256, 3),   # 64 rows, shared
     ("swiglu", 130, 2048, 256, 2),  # a full row block (row per thread), then a block of 2 rows
     ("gelu", 100, 2048, 384, 4),    # 100 rows: row per thread
 ])
 def test_split_k_few_valid_rows(kind, M, H, F, split):
     """Ragged row blocks: partials are written for the valid rows only; the last
-    split of a block of at most 48 valid rows reduces cooperatively (every
+    split of a block of at most 32 valid rows reduces cooperatively (every
     epilogue thread fetches elements of every split) and stores its rows
-    directly, a larger block sums row per thread; the result matches the oracle
-    and is the same bits on every call."""
+    directly, a larger block sums row per thread (up to 64 rows with the chunks
+    shared by all four warps); the result matches the oracle and is the same
+    bits on every call."""
     inp = cs_inputs.make_custom(kind, M, H, F, dtype=torch.bfloat16, seed=54)
     dev = device_tensors(inp, "nk")
     with plan_for(inp, "tile", "nk", split_k=split) as plan:
