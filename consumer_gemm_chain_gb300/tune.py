@@ -34,9 +34,9 @@ from . import chain as cs
 
 PRESETS = {
     # name: (kind, H, F, dtype name, heads, default M list)
-    "gpt3": ("gelu", 12288, 6144, "f16", 0, (1, 16, 64, 256, 512, 1024, 2048)),
-    "llama": ("swiglu", 8192, 2752, "bf16", 0, (1, 16, 64, 256, 512, 1024, 2048)),
-    "attn": ("attn", 12288, 1536, "f16", 12, (1, 16, 64, 256, 512, 1024, 2048)),
+    "gpt3": ("gelu", 12288, 6144, "f16", 0, (1, 16, 64, 128, 256, 512, 1024, 2048)),
+    "llama": ("swiglu", 8192, 2752, "bf16", 0, (1, 16, 64, 128, 256, 512, 1024, 2048)),
+    "attn": ("attn", 12288, 1536, "f16", 12, (1, 16, 64, 128, 256, 512, 1024, 2048)),
     "stress": ("gelu", 8192, 8192, "f16", 0, tuple(128 * b for b in range(1, 13))),
 }
 MLP_TILES = ((128, 64), (128, 128), (128, 256), (256, 256), (512, 256))
