@@ -53,6 +53,35 @@ int main(int argc, char** argv) {
   CHECK(seen_consumer_of_row0);
   free(units);
 
+  /* the GPT-3 shard at one row with six K-splits in K-range order: the first
+     consumer units listed are K-split 0 of consecutive column tiles, and
+     cs_chain_plan_info reports the order and the first stage's own splits */
+  {
+    cs_chain_desc k = d;
+    cs_chain_info info;
+    size_t first = 0;
+    k.M = 1;
+    k.tile_m = 128;
+    k.tile_n = 128;
+    k.split_k = 3;
+    k.split_k_first = 6;
+    k.raster = 3;
+    k.tuned = -1;
+    CHECK(cs_chain_plan_info(&k, 152, &info) == CS_OK);
+    CHECK(info.raster == 3 && info.split_k[0] == 6 && info.split_k[1] == 3);
+    CHECK(cs_schedule_build(&k, 152, NULL, 0, &n) == CS_OK);
+    CHECK(n == (size_t)(48 * 6 + 96 * 3));
+    units = (uint32_t*)malloc(n * sizeof(uint32_t));
+    CHECK(units != NULL);
+    CHECK(cs_schedule_build(&k, 152, units, n, &n) == CS_OK);
+    while (first < n && stage_of(units[first]) == 0) ++first;
+    CHECK(first == 48 * 6);
+    for (i = 0; i < 96; ++i) CHECK(units[first + i] == (uint32_t)((1u << 30) | i));
+    free(units);
+    k.raster = 4;
+    CHECK(cs_schedule_build(&k, 152, NULL, 0, &n) == CS_ERR_INVALID_ARG);
+  }
+
   /* validation: status codes and a message, no abort */
   d.tile_m = 64;
   CHECK(cs_schedule_build(&d, 152, NULL, 0, &n) == CS_ERR_INVALID_ARG);
