@@ -624,7 +624,7 @@ __device__ void release_tile(const KParams& p, const StageP& S, int mb, int n, i
   }
 }
 
-// K-split reduction for a row block with few valid rows (R <= 48): the NE * 32
+// K-split reduction for a row block with few valid rows (R <= 32): the NE * 32
 // epilogue threads share the (row, 4-column group) elements of `npc` 64-column
 // parts (the value chunks c0 .. c0+nc-1, then for SwiGLU the same up chunks)
 // and fetch every split of an element at once; each element is summed in split
