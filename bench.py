@@ -616,7 +616,8 @@ def main():
         "vs_baseline": None, "dtype": "f16" if inp.dtype == torch.float16 else "bf16", "data": "synthetic",
         "config": dict(workload_config(args.workload, M, inp, args.policy, lay), parallelism=f"replicas{ws}",
                        tile_n=plan_info["tile_n"][:2], tile_m=plan_info["tile_m"], group_m=plan_info["group_m"],
-                       lag=plan_info["lag"], pdl=args.pdl >= 0, split_k=plan_info["split_k"][:2],
+                       lag=plan_info["lag"], pdl=args.pdl >= 0,
+                       split_k=plan_info["split_k"][:plan_info["stages"]], raster=plan_info["raster"],
                        grid=plan_info["num_sms"], tuning=dict(tuning, entry=plan_info["tuned_entry"])),
         "roofline": roof, "gpu_launches": args.steps * launches_per_step,
     }

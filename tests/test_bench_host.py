@@ -163,3 +163,23 @@ def test_sampled_calls_never_exceed_the_limit_and_spread_evenly(steps):
     assert idx[0] == 0 and all(i < steps for i in idx)
     gaps = {b - a for a, b in zip(idx, idx[1:])}
     assert len(gaps) <= 1  # one stride
+
+
+def test_kernel_label_follows_the_configuration_rules():
+    """The instantiation named in the bench line follows the library's rules:
+    8- and 32-row activation tiles up to 8 and 32 rows on single SMs, the 48 KB
+    stages for 256-wide single-SM tiles, pairs and 4-CTA clusters."""
+    import bench
+
+    def q(tile_m, tile_n, stages=2):
+        return {"tile_m": tile_m, "tile_n": [tile_n] * stages + [128] * (3 - stages), "stages": stages}
+
+    assert bench.kernel_label("gelu", 1, q(128, 128)) == "cs_chain_kernel<11,17408,1,0,1,8>"
+    assert bench.kernel_label("swiglu", 8, q(128, 256)) == "cs_chain_kernel<5,33792,1,0,1,8>"
+    assert bench.kernel_label("gelu", 9, q(128, 128)) == "cs_chain_kernel<9,20480,1,0,1,32>"
+    assert bench.kernel_label("swiglu", 32, q(128, 128)) == "cs_chain_kernel<5,36864,1,0,1,32>"
+    assert bench.kernel_label("gelu", 33, q(128, 128)) == "cs_chain_kernel<6,32768,1>"
+    assert bench.kernel_label("gelu", 64, q(128, 256)) == "cs_chain_kernel<4,49152,1>"
+    assert bench.kernel_label("gelu", 256, q(256, 256)) == "cs_chain_kernel<6,32768,2>"
+    assert bench.kernel_label("gelu", 2048, q(512, 256)).startswith("cs_chain_kernel<6,32768,2,0,4>")
+    assert bench.kernel_label("attn", 16, q(128, 128, 3)).startswith("cs_chain_kernel<6,32768,1,1>")
